@@ -1,0 +1,572 @@
+// moe_oracle.cpp -- plain, slow, single-threaded CPU oracle for the routed-expert
+// hot path (dispatch -> W13 GEMM -> SwiGLU -> W2 GEMM x score -> combine, and the
+// backward: DGRAD, WGRAD, score gradients).
+//
+// TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, loads or calls
+// this file; only the test suite, the smoke check and the CPU-baseline leg of the
+// benchmark do.  It shares no code, header, table or helper with the CUDA path.
+//
+// Sources (page title, section):
+//   [DM]  "Dist-MoE: Meta's Blackwell SM100 MoE Kernels", section "What it is selling":
+//         four caller-owned inputs (activations, top-k ids, scores, weights); the
+//         pipeline  route on GPU -> W13 -> SwiGLU -> W2 -> combine; FPROP/DGRAD/WGRAD;
+//         BF16 operands with FP32 accumulate; MXFP8 E4M3 quantises activations after
+//         routing and takes prepared weights; plain or clamped SwiGLU; in-place
+//         WGRAD accumulation.
+//   [DM-C] same page, section "Caveats": fixed physical token count, padding rows
+//         carry zero scores.
+//   [NV-G] "nvfp4moe" README, section "Grouped GEMM": contiguous expert-major rows,
+//         m_indptr of length E+1, empty experts valid.
+//   [NV-M] same README, section "MoE layer": dispatch, FC1 + gated activation, FC2,
+//         probability weighting, deterministic combine; distinct int32 ids per row,
+//         float32 weights; padded offsets.
+//   [NV-T] same README, section "Training" and "Supported kernel surface":
+//         deterministic dispatch, combine and router gradients; input and weight
+//         gradients.
+//
+// Readings where the pages are silent (each also listed in the design notes):
+//   * W13[e] rows [0,I) are the gate projection and rows [I,2I) the up projection
+//     (not interleaved; interleaved weights are listed as unsupported in [DM]).
+//   * SwiGLU(gate, up) = silu(gate) * up; the clamped variant clips gate and up to
+//     [-L, L] first; its gradient passes at exactly +-L and is zero outside.
+//   * Rounding to bf16 (round-to-nearest-even) happens at R1..R7 below; every sum
+//     is accumulated in the working type in ascending index order.
+//   * Rows of one expert are ordered by ascending flat index t*k+j (stable).
+//   * The score multiplies the W2 output before its bf16 rounding (R3); the combine
+//     sums the k bf16 contributions of a token in column order j = 0..k-1 (R6).
+//   * dscores is the gradient w.r.t. the given scores (no softmax behind them).
+//   * For WGRAD-W2 the score is folded into h: hs = bf16(s * h) (R7).
+//   * MXFP8 (OCP MX): 32-element blocks along K, E8M0 shared exponent
+//     X = floor(log2(amax)) - 8, E4M3 elements rounded to nearest even and
+//     saturated to +-448; an all-zero block gets scale code 0.
+//
+// Working type: float (the pages' FP32 accumulate) unless built with
+// -DORC_DOUBLE, which evaluates every sum and elementwise step in double (used to
+// bound the effect of FP32 summation order).
+//
+// bf16 values cross the C interface as raw uint16 bit patterns.
+
+#include <cstdint>
+#include <cstring>
+#include <cmath>
+#include <vector>
+
+#ifdef ORC_DOUBLE
+typedef double real;
+#else
+typedef float real;
+#endif
+
+namespace {
+
+// ---- scalar conversions ----------------------------------------------------
+
+float bf16_to_float(uint16_t b) {
+  uint32_t u = static_cast<uint32_t>(b) << 16;
+  float f;
+  std::memcpy(&f, &u, 4);
+  return f;
+}
+
+// float -> bf16, round to nearest, ties to even (the standard bf16 conversion).
+uint16_t float_to_bf16(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  if ((u & 0x7f800000u) == 0x7f800000u) {           // inf or nan
+    if (u & 0x007fffffu) return static_cast<uint16_t>((u >> 16) | 0x0040u);
+    return static_cast<uint16_t>(u >> 16);
+  }
+  uint32_t lsb = (u >> 16) & 1u;
+  u += 0x7fffu + lsb;
+  return static_cast<uint16_t>(u >> 16);
+}
+
+uint16_t real_to_bf16(real v) { return float_to_bf16(static_cast<float>(v)); }
+real bf(uint16_t b) { return static_cast<real>(bf16_to_float(b)); }
+
+real rexp(real v) { return static_cast<real>(std::exp(static_cast<double>(v))); }
+
+// ---- problem description ---------------------------------------------------
+
+struct Problem {
+  int T, d, I, E, k;
+  float clamp;                 // 0 = plain SwiGLU, L > 0 = clamped to [-L, L]
+  const uint16_t* x;           // [T, d]
+  const int32_t* ids;          // [T, k]
+  const float* scores;         // [T, k]
+  const uint16_t* w13;         // [E, 2I, d]
+  const uint16_t* w2;          // [E, d, I]
+};
+
+// Is routed element (t, j) valid?  Ids must lie in [0, E) and be distinct within
+// a token row ([NV-M]).  The first occurrence of a repeated id stays valid.
+bool element_valid(const Problem& p, int t, int j) {
+  int e = p.ids[(size_t)t * p.k + j];
+  if (e < 0 || e >= p.E) return false;
+  for (int jj = 0; jj < j; ++jj)
+    if (p.ids[(size_t)t * p.k + jj] == e) return false;
+  return true;
+}
+
+// Forward quantities of one routed row (token t through expert e with score s).
+//   a  [2I] bf16 : gate/up pre-activations               (R1)
+//   h  [I]  bf16 : SwiGLU output                          (R2)
+//   ys [d]  bf16 : score-weighted W2 output               (R3)
+void row_forward(const Problem& p, int t, int e, float s,
+                 uint16_t* a, uint16_t* h, uint16_t* ys) {
+  const int d = p.d, I = p.I;
+  const uint16_t* xt = p.x + (size_t)t * d;
+  const uint16_t* W13 = p.w13 + (size_t)e * 2 * I * d;
+  const uint16_t* W2 = p.w2 + (size_t)e * d * I;
+  // W13 GEMM: a_i = sum_c x[t,c] * W13[e,i,c]   (FPROP, [DM])
+  for (int i = 0; i < 2 * I; ++i) {
+    real acc = 0;
+    const uint16_t* wr = W13 + (size_t)i * d;
+    for (int c = 0; c < d; ++c) acc += bf(xt[c]) * bf(wr[c]);
+    a[i] = real_to_bf16(acc);                                   // R1
+  }
+  // SwiGLU: h = silu(G) * U with G, U from the rounded gate/up (optionally clipped)
+  const real L = p.clamp;
+  for (int i = 0; i < I; ++i) {
+    real G = bf(a[i]);
+    real U = bf(a[I + i]);
+    if (L > 0) {
+      G = G < -L ? -L : (G > L ? L : G);
+      U = U < -L ? -L : (U > L ? L : U);
+    }
+    real silu = G / (real(1) + rexp(-G));
+    h[i] = real_to_bf16(silu * U);                              // R2
+  }
+  // W2 GEMM and probability weighting: ys_c = s * sum_i h_i * W2[e,c,i]   ([NV-M])
+  for (int c = 0; c < d; ++c) {
+    real acc = 0;
+    const uint16_t* wr = W2 + (size_t)c * I;
+    for (int i = 0; i < I; ++i) acc += bf(h[i]) * bf(wr[i]);
+    ys[c] = real_to_bf16(static_cast<real>(s) * acc);           // R3
+  }
+}
+
+// Backward quantities of one routed row, given its forward a and h.
+//   g       [I]  working type : dY_t . W2[e]
+//   dscore        working type : sum_i h_i * g_i
+//   dA      [2I] bf16 : gradient at the gate/up pre-activations     (R4)
+//   dxe     [d]  bf16 : dA . W13[e]                                  (R5)
+//   hs      [I]  bf16 : s * h, the WGRAD-W2 operand                  (R7)
+void row_backward(const Problem& p, int t, int e, float s, const uint16_t* dy,
+                  const uint16_t* a, const uint16_t* h,
+                  real* dscore, uint16_t* dA, uint16_t* dxe, uint16_t* hs) {
+  const int d = p.d, I = p.I;
+  const uint16_t* dyt = dy + (size_t)t * d;
+  const uint16_t* W13 = p.w13 + (size_t)e * 2 * I * d;
+  const uint16_t* W2 = p.w2 + (size_t)e * d * I;
+  std::vector<real> g(I);
+  // DGRAD through W2: g_i = sum_c dY[t,c] * W2[e,c,i]
+  for (int i = 0; i < I; ++i) {
+    real acc = 0;
+    for (int c = 0; c < d; ++c) acc += bf(dyt[c]) * bf(W2[(size_t)c * I + i]);
+    g[i] = acc;
+  }
+  // score gradient: y depends on s through s * (h . W2), so dL/ds = sum_i h_i g_i
+  real ds = 0;
+  for (int i = 0; i < I; ++i) ds += bf(h[i]) * g[i];
+  *dscore = ds;
+  // SwiGLU backward
+  const real L = p.clamp;
+  for (int i = 0; i < I; ++i) {
+    real ag = bf(a[i]), au = bf(a[I + i]);
+    real G = ag, U = au, mg = 1, mu = 1;
+    if (L > 0) {
+      if (G < -L || G > L) mg = 0;
+      if (U < -L || U > L) mu = 0;
+      G = G < -L ? -L : (G > L ? L : G);
+      U = U < -L ? -L : (U > L ? L : U);
+    }
+    real dh = static_cast<real>(s) * g[i];
+    real sig = real(1) / (real(1) + rexp(-G));
+    real silu = G * sig;
+    real dsilu = sig * (real(1) + G * (real(1) - sig));
+    real dgate = dh * U * dsilu * mg;
+    real dup = dh * silu * mu;
+    dA[i] = real_to_bf16(dgate);                                // R4
+    dA[I + i] = real_to_bf16(dup);                              // R4
+    hs[i] = real_to_bf16(static_cast<real>(s) * bf(h[i]));      // R7
+  }
+  // DGRAD through W13: dxe_c = sum_{i<2I} dA_i * W13[e,i,c]
+  for (int c = 0; c < d; ++c) {
+    real acc = 0;
+    for (int i = 0; i < 2 * I; ++i) acc += bf(dA[i]) * bf(W13[(size_t)i * d + c]);
+    dxe[c] = real_to_bf16(acc);                                 // R5
+  }
+}
+
+Problem make_problem(int T, int d, int I, int E, int k, float clamp,
+                     const uint16_t* x, const int32_t* ids, const float* scores,
+                     const uint16_t* w13, const uint16_t* w2) {
+  Problem p;
+  p.T = T; p.d = d; p.I = I; p.E = E; p.k = k; p.clamp = clamp;
+  p.x = x; p.ids = ids; p.scores = scores; p.w13 = w13; p.w2 = w2;
+  return p;
+}
+
+// ---- MXFP8 (E4M3 elements, E8M0 block scales) ------------------------------
+
+// Value of an E4M3 code (1 sign, 4 exponent bits with bias 7, 3 mantissa bits;
+// exponent field 0 is subnormal; 0x7F/0xFF are NaN and never produced here).
+double e4m3_value(uint8_t c) {
+  int sgn = (c >> 7) & 1, ex = (c >> 3) & 15, man = c & 7;
+  double v = ex == 0 ? std::ldexp(man / 8.0, -6) : std::ldexp(1.0 + man / 8.0, ex - 7);
+  return sgn ? -v : v;
+}
+
+// Nearest E4M3 value to v, ties to the even code, saturating to +-448.  The 127
+// non-negative finite codes 0x00..0x7E are monotone in value, so the nearest one
+// is found by bisection over that table.
+uint8_t e4m3_encode(double v) {
+  static double table[127];
+  static bool ready = false;
+  if (!ready) {
+    for (int c = 0; c < 127; ++c) table[c] = e4m3_value(static_cast<uint8_t>(c));
+    ready = true;
+  }
+  uint8_t sgn = std::signbit(v) ? 0x80 : 0x00;
+  double m = std::fabs(v);
+  if (m >= table[126]) return sgn | 126;
+  int lo = 0, hi = 126;                       // table[lo] <= m < table[hi]
+  while (hi - lo > 1) {
+    int mid = (lo + hi) / 2;
+    if (table[mid] <= m) lo = mid; else hi = mid;
+  }
+  double dl = m - table[lo], dh = table[hi] - m;
+  int c = dl < dh ? lo : (dh < dl ? hi : (lo % 2 == 0 ? lo : hi));
+  return sgn | static_cast<uint8_t>(c);
+}
+
+// Quantise one 32-element block (bf16 in) to E4M3 codes and an E8M0 code.
+void quant_block(const uint16_t* in, int n, uint8_t* codes, uint8_t* scale) {
+  float amax = 0;
+  for (int i = 0; i < n; ++i) {
+    float v = std::fabs(bf16_to_float(in[i]));
+    if (v > amax) amax = v;
+  }
+  if (amax == 0) {
+    *scale = 0;
+    for (int i = 0; i < n; ++i) codes[i] = 0;
+    return;
+  }
+  int ex;
+  std::frexp(static_cast<double>(amax), &ex);       // amax = f * 2^ex, f in [0.5, 1)
+  int X = (ex - 1) - 8;                              // floor(log2 amax) - emax(E4M3)
+  if (X < -127) X = -127;
+  if (X > 127) X = 127;
+  *scale = static_cast<uint8_t>(X + 127);
+  for (int i = 0; i < n; ++i)
+    codes[i] = e4m3_encode(std::ldexp(static_cast<double>(bf16_to_float(in[i])), -X));
+}
+
+double e8m0_value(uint8_t s) { return std::ldexp(1.0, static_cast<int>(s) - 127); }
+
+}  // namespace
+
+extern "C" {
+
+// Which working type this build uses: 4 (float) or 8 (double).
+int orc_real_bytes() { return static_cast<int>(sizeof(real)); }
+
+int orc_float_to_bf16(const float* in, uint16_t* out, long n) {
+  for (long i = 0; i < n; ++i) out[i] = float_to_bf16(in[i]);
+  return 0;
+}
+
+// Dispatch ([NV-G], [NV-M], [NV-T]): a stable counting sort of the routed
+// elements by expert.  For each valid element (t, j) with e = ids[t,j]:
+//   rank_of[t*k+j] = number of valid elements of expert e with smaller flat index
+//   row_of[t*k+j]  = off_pad[e] + rank_of[t*k+j]
+// invalid elements get rank_of = row_of = -1.
+//   counts[e]   = valid elements routed to e
+//   m_indptr    = exclusive prefix sum of counts (length E+1)
+//   off_pad     = exclusive prefix sum of counts rounded up to a multiple of BM
+// Returns the smallest invalid flat index, or -1 if all ids are valid.
+long orc_dispatch(int T, int k, int E, int BM, const int32_t* ids,
+                  int32_t* counts, int32_t* m_indptr, int32_t* off_pad,
+                  int32_t* rank_of, int32_t* row_of) {
+  Problem p = make_problem(T, 0, 0, E, k, 0, nullptr, ids, nullptr, nullptr, nullptr);
+  long first_bad = -1;
+  for (int e = 0; e < E; ++e) counts[e] = 0;
+  for (int t = 0; t < T; ++t)
+    for (int j = 0; j < k; ++j) {
+      long f = (long)t * k + j;
+      if (!element_valid(p, t, j)) {
+        if (first_bad < 0) first_bad = f;
+        rank_of[f] = -1;
+        continue;
+      }
+      rank_of[f] = counts[ids[f]]++;
+    }
+  m_indptr[0] = 0;
+  off_pad[0] = 0;
+  for (int e = 0; e < E; ++e) {
+    m_indptr[e + 1] = m_indptr[e] + counts[e];
+    off_pad[e + 1] = off_pad[e] + (counts[e] + BM - 1) / BM * BM;
+  }
+  for (long f = 0; f < (long)T * k; ++f)
+    row_of[f] = rank_of[f] < 0 ? -1 : off_pad[ids[f]] + rank_of[f];
+  return first_bad;
+}
+
+// Gather ([DM] "route on GPU"): xe[r] = x[token_of[r]] for rows r < nrows, zero
+// rows where token_of[r] < 0 (padding).
+int orc_gather_rows(int nrows, int d, const uint16_t* x, const int32_t* token_of,
+                    uint16_t* xe) {
+  for (int r = 0; r < nrows; ++r) {
+    int t = token_of[r];
+    for (int c = 0; c < d; ++c) xe[(size_t)r * d + c] = t < 0 ? 0 : x[(size_t)t * d + c];
+  }
+  return 0;
+}
+
+// Combine ([NV-M], [NV-T] deterministic combine): y[t,c] = bf16(sum_j ys[row_of[t,j], c])
+// in column order j = 0..k-1; elements with row_of < 0 are skipped.        (R6)
+int orc_combine_rows(int T, int k, int d, const uint16_t* ys, const int32_t* row_of,
+                     uint16_t* y) {
+  for (int t = 0; t < T; ++t)
+    for (int c = 0; c < d; ++c) {
+      real acc = 0;
+      for (int j = 0; j < k; ++j) {
+        int r = row_of[(size_t)t * k + j];
+        if (r >= 0) acc += bf(ys[(size_t)r * d + c]);
+      }
+      y[(size_t)t * d + c] = real_to_bf16(acc);
+    }
+  return 0;
+}
+
+// Forward for the listed tokens (toks == NULL: tokens 0..ntok-1).
+//   y  [ntok, d]        bf16 output                               (R6)
+//   a  [ntok, k, 2I]    optional, gate/up pre-activations          (R1)
+//   h  [ntok, k, I]     optional, SwiGLU outputs                   (R2)
+//   ys [ntok, k, d]     optional, score-weighted expert outputs    (R3)
+// Invalid elements contribute nothing and leave their optional rows zero.
+int orc_forward(int T, int d, int I, int E, int k, float clamp,
+                const uint16_t* x, const int32_t* ids, const float* scores,
+                const uint16_t* w13, const uint16_t* w2,
+                int ntok, const int32_t* toks,
+                uint16_t* y, uint16_t* a_out, uint16_t* h_out, uint16_t* ys_out) {
+  Problem p = make_problem(T, d, I, E, k, clamp, x, ids, scores, w13, w2);
+  std::vector<uint16_t> a(2 * I), h(I), ys((size_t)k * d, 0);
+  std::vector<char> ok(k);
+  for (int n = 0; n < ntok; ++n) {
+    int t = toks ? toks[n] : n;
+    for (int j = 0; j < k; ++j) {
+      ok[j] = element_valid(p, t, j);
+      uint16_t* ysj = ys.data() + (size_t)j * d;
+      if (!ok[j]) {
+        std::memset(ysj, 0, sizeof(uint16_t) * d);
+        if (a_out) std::memset(a_out + ((size_t)n * k + j) * 2 * I, 0, sizeof(uint16_t) * 2 * I);
+        if (h_out) std::memset(h_out + ((size_t)n * k + j) * I, 0, sizeof(uint16_t) * I);
+        continue;
+      }
+      int e = ids[(size_t)t * k + j];
+      float s = scores[(size_t)t * k + j];
+      row_forward(p, t, e, s, a.data(), h.data(), ysj);
+      if (a_out) std::memcpy(a_out + ((size_t)n * k + j) * 2 * I, a.data(), sizeof(uint16_t) * 2 * I);
+      if (h_out) std::memcpy(h_out + ((size_t)n * k + j) * I, h.data(), sizeof(uint16_t) * I);
+    }
+    if (ys_out) std::memcpy(ys_out + (size_t)n * k * d, ys.data(), sizeof(uint16_t) * k * d);
+    for (int c = 0; c < d; ++c) {
+      real acc = 0;
+      for (int j = 0; j < k; ++j)
+        if (ok[j]) acc += bf(ys[(size_t)j * d + c]);
+      y[(size_t)n * d + c] = real_to_bf16(acc);                 // R6
+    }
+  }
+  return 0;
+}
+
+// Backward for the listed tokens, given the upstream gradient dy [T, d].
+//   dx      [ntok, d]      bf16, overwritten                     (R6 of R5)
+//   dscores [ntok, k]      float, overwritten (0 for invalid elements)
+//   dA      [ntok, k, 2I]  optional                              (R4)
+//   hs      [ntok, k, I]   optional                              (R7)
+//   g       [ntok, k, I]   optional, float
+int orc_backward(int T, int d, int I, int E, int k, float clamp,
+                 const uint16_t* x, const int32_t* ids, const float* scores,
+                 const uint16_t* w13, const uint16_t* w2, const uint16_t* dy,
+                 int ntok, const int32_t* toks,
+                 uint16_t* dx, float* dscores,
+                 uint16_t* dA_out, uint16_t* hs_out, float* g_out) {
+  Problem p = make_problem(T, d, I, E, k, clamp, x, ids, scores, w13, w2);
+  std::vector<uint16_t> a(2 * I), h(I), ys(d), dA(2 * I), hs(I), dxe((size_t)k * d, 0);
+  std::vector<char> ok(k);
+  for (int n = 0; n < ntok; ++n) {
+    int t = toks ? toks[n] : n;
+    for (int j = 0; j < k; ++j) {
+      ok[j] = element_valid(p, t, j);
+      size_t nj = (size_t)n * k + j;
+      if (!ok[j]) {
+        dscores[nj] = 0;
+        if (dA_out) std::memset(dA_out + nj * 2 * I, 0, sizeof(uint16_t) * 2 * I);
+        if (hs_out) std::memset(hs_out + nj * I, 0, sizeof(uint16_t) * I);
+        if (g_out) std::memset(g_out + nj * I, 0, sizeof(float) * I);
+        continue;
+      }
+      int e = ids[(size_t)t * k + j];
+      float s = scores[(size_t)t * k + j];
+      row_forward(p, t, e, s, a.data(), h.data(), ys.data());
+      real ds;
+      row_backward(p, t, e, s, dy, a.data(), h.data(), &ds, dA.data(),
+                   dxe.data() + (size_t)j * d, hs.data());
+      dscores[nj] = static_cast<float>(ds);
+      if (dA_out) std::memcpy(dA_out + nj * 2 * I, dA.data(), sizeof(uint16_t) * 2 * I);
+      if (hs_out) std::memcpy(hs_out + nj * I, hs.data(), sizeof(uint16_t) * I);
+      if (g_out) {
+        // recompute g in the working type for inspection
+        const uint16_t* W2 = w2 + (size_t)e * d * I;
+        for (int i = 0; i < I; ++i) {
+          real acc = 0;
+          for (int c = 0; c < d; ++c) acc += bf(dy[(size_t)t * d + c]) * bf(W2[(size_t)c * I + i]);
+          g_out[nj * I + i] = static_cast<float>(acc);
+        }
+      }
+    }
+    for (int c = 0; c < d; ++c) {
+      real acc = 0;
+      for (int j = 0; j < k; ++j)
+        if (ok[j]) acc += bf(dxe[(size_t)j * d + c]);
+      dx[(size_t)n * d + c] = real_to_bf16(acc);                // R6
+    }
+  }
+  return 0;
+}
+
+// WGRAD of one expert e ([DM] "in-place WGRAD accumulation"): the increments that
+// a backward pass adds to the existing FP32 gradients, summed in FP32 over the
+// rows of e in dispatch order (ascending flat index):
+//   dw13_delta [2I, d] : sum_rows dA_i * x[t,c]
+//   dw2_delta  [d, I]  : sum_rows dY[t,c] * hs_i
+// Returns the number of rows of expert e.
+int orc_wgrad_expert(int T, int d, int I, int E, int k, float clamp,
+                     const uint16_t* x, const int32_t* ids, const float* scores,
+                     const uint16_t* w13, const uint16_t* w2, const uint16_t* dy,
+                     int e, float* dw13_delta, float* dw2_delta) {
+  Problem p = make_problem(T, d, I, E, k, clamp, x, ids, scores, w13, w2);
+  std::vector<real> acc13((size_t)2 * I * d, 0), acc2((size_t)d * I, 0);
+  std::vector<uint16_t> a(2 * I), h(I), ys(d), dA(2 * I), hs(I), dxe(d);
+  int rows = 0;
+  for (int t = 0; t < T; ++t)
+    for (int j = 0; j < k; ++j) {
+      if (ids[(size_t)t * k + j] != e || !element_valid(p, t, j)) continue;
+      float s = scores[(size_t)t * k + j];
+      row_forward(p, t, e, s, a.data(), h.data(), ys.data());
+      real ds;
+      row_backward(p, t, e, s, dy, a.data(), h.data(), &ds, dA.data(), dxe.data(), hs.data());
+      const uint16_t* xt = x + (size_t)t * d;
+      const uint16_t* dyt = dy + (size_t)t * d;
+      for (int i = 0; i < 2 * I; ++i) {
+        real ai = bf(dA[i]);
+        real* row = acc13.data() + (size_t)i * d;
+        for (int c = 0; c < d; ++c) row[c] += ai * bf(xt[c]);
+      }
+      for (int c = 0; c < d; ++c) {
+        real yc = bf(dyt[c]);
+        real* row = acc2.data() + (size_t)c * I;
+        for (int i = 0; i < I; ++i) row[i] += yc * bf(hs[i]);
+      }
+      ++rows;
+    }
+  for (size_t n = 0; n < acc13.size(); ++n) dw13_delta[n] = static_cast<float>(acc13[n]);
+  for (size_t n = 0; n < acc2.size(); ++n) dw2_delta[n] = static_cast<float>(acc2[n]);
+  return rows;
+}
+
+// MXFP8 quantiser ([DM]: MXFP8 E4M3 with prepared weights): quantise a bf16
+// matrix [rows, K] along K in 32-element blocks.  codes [rows, K] E4M3 bytes;
+// scales [rows, K/32] E8M0 bytes.  K must be a multiple of 32.
+int orc_quant_mxfp8(long rows, int K, const uint16_t* in, uint8_t* codes, uint8_t* scales) {
+  if (K % 32) return -1;
+  for (long r = 0; r < rows; ++r)
+    for (int b = 0; b < K / 32; ++b)
+      quant_block(in + r * K + b * 32, 32, codes + r * K + b * 32, scales + r * (K / 32) + b);
+  return 0;
+}
+
+int orc_e4m3_encode(const double* in, uint8_t* out, long n) {
+  for (long i = 0; i < n; ++i) out[i] = e4m3_encode(in[i]);
+  return 0;
+}
+
+int orc_e4m3_decode(const uint8_t* in, double* out, long n) {
+  for (long i = 0; i < n; ++i) out[i] = e4m3_value(in[i]);
+  return 0;
+}
+
+// MXFP8 forward for the listed tokens.  The routed activation row is quantised
+// along d (after routing), the weights arrive prepared (codes + E8M0 scales along
+// their K: d for W13, I for W2), gate/up accumulate dequantised products, h is
+// rounded to bf16 (R2) and then quantised along I before the W2 GEMM.
+//   w13q [E, 2I, d] codes, w13s [E, 2I, d/32];  w2q [E, d, I] codes, w2s [E, d, I/32]
+int orc_forward_mxfp8(int T, int d, int I, int E, int k, float clamp,
+                      const uint16_t* x, const int32_t* ids, const float* scores,
+                      const uint8_t* w13q, const uint8_t* w13s,
+                      const uint8_t* w2q, const uint8_t* w2s,
+                      int ntok, const int32_t* toks, uint16_t* y, uint16_t* h_out) {
+  Problem p = make_problem(T, d, I, E, k, clamp, x, ids, scores, nullptr, nullptr);
+  std::vector<uint8_t> xq(d), xs(d / 32), hq(I), hsc(I / 32);
+  std::vector<real> xv(d), hv(I);
+  std::vector<uint16_t> a(2 * I), h(I), ys((size_t)k * d);
+  std::vector<char> ok(k);
+  const real L = clamp;
+  for (int n = 0; n < ntok; ++n) {
+    int t = toks ? toks[n] : n;
+    for (int b = 0; b < d / 32; ++b)
+      quant_block(x + (size_t)t * d + b * 32, 32, xq.data() + b * 32, xs.data() + b);
+    for (int c = 0; c < d; ++c)
+      xv[c] = static_cast<real>(e4m3_value(xq[c]) * e8m0_value(xs[c / 32]));
+    for (int j = 0; j < k; ++j) {
+      ok[j] = element_valid(p, t, j);
+      if (!ok[j]) {
+        if (h_out) std::memset(h_out + ((size_t)n * k + j) * I, 0, sizeof(uint16_t) * I);
+        continue;
+      }
+      int e = ids[(size_t)t * k + j];
+      float s = scores[(size_t)t * k + j];
+      for (int i = 0; i < 2 * I; ++i) {
+        size_t row = (size_t)e * 2 * I + i;
+        real acc = 0;
+        for (int c = 0; c < d; ++c)
+          acc += xv[c] * static_cast<real>(e4m3_value(w13q[row * d + c]) *
+                                           e8m0_value(w13s[row * (d / 32) + c / 32]));
+        a[i] = real_to_bf16(acc);                                // R1
+      }
+      for (int i = 0; i < I; ++i) {
+        real G = bf(a[i]), U = bf(a[I + i]);
+        if (L > 0) {
+          G = G < -L ? -L : (G > L ? L : G);
+          U = U < -L ? -L : (U > L ? L : U);
+        }
+        h[i] = real_to_bf16(G / (real(1) + rexp(-G)) * U);       // R2
+      }
+      if (h_out) std::memcpy(h_out + ((size_t)n * k + j) * I, h.data(), sizeof(uint16_t) * I);
+      for (int b = 0; b < I / 32; ++b)
+        quant_block(h.data() + b * 32, 32, hq.data() + b * 32, hsc.data() + b);
+      for (int i = 0; i < I; ++i)
+        hv[i] = static_cast<real>(e4m3_value(hq[i]) * e8m0_value(hsc[i / 32]));
+      for (int c = 0; c < d; ++c) {
+        size_t row = (size_t)e * d + c;
+        real acc = 0;
+        for (int i = 0; i < I; ++i)
+          acc += hv[i] * static_cast<real>(e4m3_value(w2q[row * I + i]) *
+                                           e8m0_value(w2s[row * (I / 32) + i / 32]));
+        ys[(size_t)j * d + c] = real_to_bf16(static_cast<real>(s) * acc);   // R3
+      }
+    }
+    for (int c = 0; c < d; ++c) {
+      real acc = 0;
+      for (int j = 0; j < k; ++j)
+        if (ok[j]) acc += bf(ys[(size_t)j * d + c]);
+      y[(size_t)n * d + c] = real_to_bf16(acc);                 // R6
+    }
+  }
+  return 0;
+}
+
+}  // extern "C"

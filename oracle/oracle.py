@@ -1,0 +1,201 @@
+"""ctypes wrapper around the plain C++ oracle (test infrastructure only).
+
+bf16 tensors cross this interface as numpy ``uint16`` arrays holding raw bit
+patterns; ids are ``int32``; scores and gradients ``float32``.
+"""
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.cpp")
+_LIBS = {
+    "float": os.path.join(_HERE, "_build", "libmoe_oracle.so"),
+    "double": os.path.join(_HERE, "_build", "libmoe_oracle_f64.so"),
+}
+_lock = threading.Lock()
+_cache = {}
+
+
+def build_oracle(force=False):
+    """Compile both oracle builds (working type float, and double)."""
+    os.makedirs(os.path.join(_HERE, "_build"), exist_ok=True)
+    for kind, out in _LIBS.items():
+        if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(_SRC):
+            continue
+        cmd = ["g++", "-std=c++17", "-O2", "-ffp-contract=off", "-fno-fast-math",
+               "-shared", "-fPIC", "-o", out + ".tmp", _SRC]
+        if kind == "double":
+            cmd.insert(1, "-DORC_DOUBLE")
+        subprocess.check_call(cmd)
+        os.replace(out + ".tmp", out)
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+class Oracle:
+    """Typed entry points of one oracle build."""
+
+    def __init__(self, path):
+        self.lib = ctypes.CDLL(path)
+        L = self.lib
+        vp, i32, f32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_long
+        L.orc_real_bytes.restype = i32
+        L.orc_float_to_bf16.argtypes = [vp, vp, i64]
+        L.orc_dispatch.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
+        L.orc_dispatch.restype = i64
+        L.orc_gather_rows.argtypes = [i32, i32, vp, vp, vp]
+        L.orc_combine_rows.argtypes = [i32, i32, i32, vp, vp, vp]
+        L.orc_forward.argtypes = [i32] * 5 + [f32] + [vp] * 5 + [i32, vp] + [vp] * 4
+        L.orc_backward.argtypes = [i32] * 5 + [f32] + [vp] * 6 + [i32, vp] + [vp] * 5
+        L.orc_wgrad_expert.argtypes = [i32] * 5 + [f32] + [vp] * 6 + [i32, vp, vp]
+        L.orc_quant_mxfp8.argtypes = [i64, i32, vp, vp, vp]
+        L.orc_e4m3_encode.argtypes = [vp, vp, i64]
+        L.orc_e4m3_decode.argtypes = [vp, vp, i64]
+        L.orc_forward_mxfp8.argtypes = [i32] * 5 + [f32] + [vp] * 7 + [i32, vp, vp, vp]
+        self.real_bytes = L.orc_real_bytes()
+
+    # -- scalar helpers -------------------------------------------------------
+    def float_to_bf16(self, f):
+        f = np.ascontiguousarray(f, dtype=np.float32)
+        out = np.empty(f.shape, np.uint16)
+        self.lib.orc_float_to_bf16(_ptr(f), _ptr(out), f.size)
+        return out
+
+    # -- dispatch / gather / combine ------------------------------------------
+    def dispatch(self, ids, E, BM):
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        T, k = ids.shape
+        counts = np.empty(E, np.int32)
+        m_indptr = np.empty(E + 1, np.int32)
+        off_pad = np.empty(E + 1, np.int32)
+        rank_of = np.empty(T * k, np.int32)
+        row_of = np.empty(T * k, np.int32)
+        bad = self.lib.orc_dispatch(T, k, E, BM, _ptr(ids), _ptr(counts), _ptr(m_indptr),
+                                    _ptr(off_pad), _ptr(rank_of), _ptr(row_of))
+        return dict(counts=counts, m_indptr=m_indptr, off_pad=off_pad,
+                    rank_of=rank_of.reshape(T, k), row_of=row_of.reshape(T, k), first_bad=bad)
+
+    def gather_rows(self, x, token_of):
+        x = np.ascontiguousarray(x, np.uint16)
+        token_of = np.ascontiguousarray(token_of, np.int32)
+        d = x.shape[1]
+        out = np.empty((token_of.size, d), np.uint16)
+        self.lib.orc_gather_rows(token_of.size, d, _ptr(x), _ptr(token_of), _ptr(out))
+        return out
+
+    def combine_rows(self, ys, row_of):
+        ys = np.ascontiguousarray(ys, np.uint16)
+        row_of = np.ascontiguousarray(row_of, np.int32)
+        T, k = row_of.shape
+        d = ys.shape[1]
+        y = np.empty((T, d), np.uint16)
+        self.lib.orc_combine_rows(T, k, d, _ptr(ys), _ptr(row_of), _ptr(y))
+        return y
+
+    # -- forward / backward ----------------------------------------------------
+    @staticmethod
+    def _dims(x, ids, w13):
+        T, d = x.shape
+        k = ids.shape[1]
+        E, I2, _ = w13.shape
+        return T, d, I2 // 2, E, k
+
+    def forward(self, x, ids, scores, w13, w2, clamp=0.0, toks=None, intermediates=False):
+        T, d, I, E, k = self._dims(x, ids, w13)
+        toks_a = None if toks is None else np.ascontiguousarray(toks, np.int32)
+        n = T if toks is None else toks_a.size
+        y = np.empty((n, d), np.uint16)
+        a = h = ys = None
+        if intermediates:
+            a = np.empty((n, k, 2 * I), np.uint16)
+            h = np.empty((n, k, I), np.uint16)
+            ys = np.empty((n, k, d), np.uint16)
+        self.lib.orc_forward(T, d, I, E, k, float(clamp), _ptr(x), _ptr(ids), _ptr(scores),
+                             _ptr(w13), _ptr(w2), n, _ptr(toks_a), _ptr(y), _ptr(a), _ptr(h), _ptr(ys))
+        if intermediates:
+            return y, dict(a=a, h=h, ys=ys)
+        return y
+
+    def backward(self, x, ids, scores, w13, w2, dy, clamp=0.0, toks=None, intermediates=False):
+        T, d, I, E, k = self._dims(x, ids, w13)
+        toks_a = None if toks is None else np.ascontiguousarray(toks, np.int32)
+        n = T if toks is None else toks_a.size
+        dx = np.empty((n, d), np.uint16)
+        ds = np.empty((n, k), np.float32)
+        dA = hs = g = None
+        if intermediates:
+            dA = np.empty((n, k, 2 * I), np.uint16)
+            hs = np.empty((n, k, I), np.uint16)
+            g = np.empty((n, k, I), np.float32)
+        self.lib.orc_backward(T, d, I, E, k, float(clamp), _ptr(x), _ptr(ids), _ptr(scores),
+                              _ptr(w13), _ptr(w2), _ptr(dy), n, _ptr(toks_a), _ptr(dx), _ptr(ds),
+                              _ptr(dA), _ptr(hs), _ptr(g))
+        if intermediates:
+            return dx, ds, dict(dA=dA, hs=hs, g=g)
+        return dx, ds
+
+    def wgrad_expert(self, x, ids, scores, w13, w2, dy, e, clamp=0.0):
+        T, d, I, E, k = self._dims(x, ids, w13)
+        d13 = np.empty((2 * I, d), np.float32)
+        d2 = np.empty((d, I), np.float32)
+        rows = self.lib.orc_wgrad_expert(T, d, I, E, k, float(clamp), _ptr(x), _ptr(ids),
+                                         _ptr(scores), _ptr(w13), _ptr(w2), _ptr(dy), int(e),
+                                         _ptr(d13), _ptr(d2))
+        return d13, d2, rows
+
+    # -- MXFP8 -----------------------------------------------------------------
+    def quant_mxfp8(self, m):
+        m = np.ascontiguousarray(m, np.uint16)
+        K = m.shape[-1]
+        rows = m.size // K
+        codes = np.empty(m.shape, np.uint8)
+        scales = np.empty(m.shape[:-1] + (K // 32,), np.uint8)
+        rc = self.lib.orc_quant_mxfp8(rows, K, _ptr(m), _ptr(codes), _ptr(scales))
+        assert rc == 0
+        return codes, scales
+
+    def e4m3_encode(self, v):
+        v = np.ascontiguousarray(v, np.float64)
+        out = np.empty(v.shape, np.uint8)
+        self.lib.orc_e4m3_encode(_ptr(v), _ptr(out), v.size)
+        return out
+
+    def e4m3_decode(self, c):
+        c = np.ascontiguousarray(c, np.uint8)
+        out = np.empty(c.shape, np.float64)
+        self.lib.orc_e4m3_decode(_ptr(c), _ptr(out), c.size)
+        return out
+
+    def forward_mxfp8(self, x, ids, scores, w13q, w13s, w2q, w2s, clamp=0.0, toks=None,
+                      return_h=False):
+        T, d = x.shape
+        k = ids.shape[1]
+        E, I2, _ = w13q.shape
+        I = I2 // 2
+        toks_a = None if toks is None else np.ascontiguousarray(toks, np.int32)
+        n = T if toks is None else toks_a.size
+        y = np.empty((n, d), np.uint16)
+        h = np.empty((n, k, I), np.uint16) if return_h else None
+        self.lib.orc_forward_mxfp8(T, d, I, E, k, float(clamp), _ptr(x), _ptr(ids), _ptr(scores),
+                                   _ptr(w13q), _ptr(w13s), _ptr(w2q), _ptr(w2s), n, _ptr(toks_a),
+                                   _ptr(y), _ptr(h))
+        return (y, h) if return_h else y
+
+
+def load_oracle(kind="float"):
+    """The oracle build whose working type is ``kind`` ("float" or "double")."""
+    with _lock:
+        if kind not in _cache:
+            build_oracle()
+            _cache[kind] = Oracle(_LIBS[kind])
+        return _cache[kind]

@@ -1,0 +1,410 @@
+"""Pins of the CPU oracle against things other than itself (CPU only).
+
+Each test checks the oracle against a library routine (torch FP64 autograd,
+numpy's stable sort, torch's bf16 / float8 conversions), a closed form, an
+invariant of the method, or a hand-worked example, chosen so that a plausible
+slip (a swapped gate/up, a dropped score, a transposed weight, a wrong rounding
+point, an off-by-one in the scan) fails at least one of them.
+"""
+
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def f32(bits):
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def bits(f):
+    return torch.from_numpy(np.ascontiguousarray(f, np.float32)).to(torch.bfloat16) \
+        .view(torch.int16).numpy().view(np.uint16)
+
+
+def small(T=24, d=64, I=32, E=5, k=3, seed=3, routing="uniform", pad=0, **kw):
+    inp = mi.make_inputs(None, seed=seed, T=T, d=d, I=I, E=E, k=k, routing=routing, pad=pad,
+                         need=("x", "ids", "scores", "w13", "w2", "dy"), **kw)
+    return inp
+
+
+# ---------------------------------------------------------------------------
+# worked example
+
+
+def test_worked_example(orc):
+    g = json.load(open(os.path.join(GOLDEN, "worked_example.json")))
+    x = bits(np.array(g["x"]))
+    w13 = bits(np.array(g["w13"]))
+    w2 = bits(np.array(g["w2"]))
+    ids = np.array(g["ids"], np.int32)
+    sc = np.array(g["scores"], np.float32)
+    dy = bits(np.array(g["dy"]))
+    ex = {k: np.array(v) for k, v in g["expect"].items()}
+    y, it = orc.forward(x, ids, sc, w13, w2, intermediates=True)
+    assert np.array_equal(f32(y), ex["y"])
+    assert np.array_equal(f32(it["a"]), ex["a"])
+    assert np.array_equal(f32(it["h"]), ex["h"])
+    assert np.array_equal(f32(it["ys"]), ex["ys"])
+    dx, ds, bi = orc.backward(x, ids, sc, w13, w2, dy, intermediates=True)
+    assert np.array_equal(f32(dx), ex["dx"])
+    assert np.array_equal(ds, ex["dscores"].astype(np.float32))
+    assert np.array_equal(f32(bi["dA"]), ex["dA"])
+    assert np.array_equal(f32(bi["hs"]), ex["hs"])
+    for e in range(2):
+        d13, d2, rows = orc.wgrad_expert(x, ids, sc, w13, w2, dy, e)
+        assert rows == 2
+        assert np.array_equal(d13, ex["dw13_delta"][e].astype(np.float32))
+        assert np.array_equal(d2, ex["dw2_delta"][e].astype(np.float32))
+
+
+# ---------------------------------------------------------------------------
+# conversions
+
+
+def test_bf16_rounding_matches_torch(orc):
+    rng = np.random.default_rng(0)
+    v = np.concatenate([
+        rng.standard_normal(100000).astype(np.float32) * np.float32(10.0) ** rng.integers(-30, 30, 100000).astype(np.float32),
+        np.array([0.0, -0.0, 1.0, -1.0, 3.4e38, -3.4e38, 1e-40, -1e-40, np.inf, -np.inf], np.float32),
+        # exact ties between two bf16 neighbours
+        (f32(np.arange(0x3f80, 0x3fa0, dtype=np.uint16)) +
+         np.float32(2.0 ** -8)).astype(np.float32),
+    ]).astype(np.float32)
+    assert np.array_equal(orc.float_to_bf16(v), bits(v))
+
+
+# ---------------------------------------------------------------------------
+# dispatch
+
+
+@pytest.mark.parametrize("T,k,E,BM", [(64, 2, 4, 128), (300, 8, 128, 128), (257, 3, 17, 64),
+                                      (1000, 8, 256, 128), (5, 1, 1, 128)])
+def test_dispatch_is_stable_counting_sort(orc, T, k, E, BM):
+    ids = mi.draw_ids(T, k, E, seed=T + E)
+    r = orc.dispatch(ids, E, BM)
+    flat = ids.reshape(-1)
+    order = np.argsort(flat, kind="stable")          # library stable sort by expert
+    counts = np.bincount(flat, minlength=E)
+    assert r["first_bad"] == -1
+    assert np.array_equal(r["counts"], counts)
+    assert r["m_indptr"][0] == 0 and r["m_indptr"][-1] == T * k
+    assert np.array_equal(np.diff(r["m_indptr"]), counts)
+    padded = -(-counts // BM) * BM
+    assert np.array_equal(np.diff(r["off_pad"]), padded)
+    # position in the sorted order minus the expert's start = rank within the expert
+    rank = np.empty(T * k, np.int64)
+    rank[order] = np.arange(T * k) - np.repeat(np.concatenate([[0], np.cumsum(counts)[:-1]]), counts)
+    assert np.array_equal(r["rank_of"].reshape(-1), rank)
+    rows = r["row_of"].reshape(-1)
+    assert np.array_equal(rows, r["off_pad"][flat] + rank)
+    assert len(np.unique(rows)) == T * k                       # injective
+    assert rows.max() < r["off_pad"][-1]
+
+
+def test_dispatch_flags_invalid_ids(orc):
+    ids = mi.draw_ids(50, 4, 16, seed=1).copy()
+    ids[7, 2] = ids[7, 0]          # duplicate within a row (flat 30)
+    ids[20, 1] = 16                # out of range (flat 81)
+    ids[3, 3] = -1                 # out of range (flat 15)
+    r = orc.dispatch(ids, 16, 128)
+    assert r["first_bad"] == 15
+    bad = {15, 30, 81}
+    for f in range(200):
+        if f in bad:
+            assert r["row_of"].reshape(-1)[f] == -1
+        else:
+            assert r["row_of"].reshape(-1)[f] >= 0
+    assert r["m_indptr"][-1] == 200 - 3
+
+
+def _token_of(row_of, nrows):
+    tok = np.full(nrows, -1, np.int32)
+    T, k = row_of.shape
+    for t in range(T):
+        for j in range(k):
+            if row_of[t, j] >= 0:
+                tok[row_of[t, j]] = t
+    return tok
+
+
+@pytest.mark.parametrize("k", [1, 2, 4, 8])
+def test_gather_combine_identity_experts(orc, k):
+    """Identity experts: combine(gather(x)) with one-hot scores returns x exactly,
+    with unit scores k*x exactly (k a power of two)."""
+    T, d, E = 40, 64, 8
+    inp = mi.make_inputs(None, seed=k, T=T, d=d, I=32, E=E, k=k, need=("x", "ids"))
+    r = orc.dispatch(inp["ids"], E, 16)
+    nrows = int(r["off_pad"][-1])
+    tok = _token_of(r["row_of"], nrows)
+    xe = orc.gather_rows(inp["x"], tok)
+    assert np.array_equal(xe[tok < 0], np.zeros_like(xe[tok < 0]))
+    assert np.array_equal(xe[tok >= 0], inp["x"][tok[tok >= 0]])
+    # unit scores
+    y = orc.combine_rows(xe, r["row_of"])
+    assert np.array_equal(f32(y), f32(inp["x"]) * k)
+    # one-hot scores: keep only the column j0 = t % k
+    ys = xe.copy()
+    for t in range(T):
+        for j in range(k):
+            if j != t % k:
+                ys[r["row_of"][t, j]] = 0
+    y1 = orc.combine_rows(ys, r["row_of"])
+    assert np.array_equal(y1, inp["x"])
+
+
+# ---------------------------------------------------------------------------
+# forward against an FP64 brute force (every expert for every token, then select)
+
+
+def _dense_fp64(inp, clamp=0.0):
+    x = torch.from_numpy(f32(inp["x"]).astype(np.float64))
+    W13 = torch.from_numpy(f32(inp["w13"]).astype(np.float64))
+    W2 = torch.from_numpy(f32(inp["w2"]).astype(np.float64))
+    I = W2.shape[2]
+    gu = torch.einsum("td,eid->eti", x, W13)             # [E, T, 2I]
+    g, u = gu[..., :I], gu[..., I:]
+    if clamp:
+        g, u = g.clamp(-clamp, clamp), u.clamp(-clamp, clamp)
+    h = torch.nn.functional.silu(g) * u
+    o = torch.einsum("eti,edi->etd", h, W2)              # [E, T, d]
+    ids = torch.from_numpy(inp["ids"]).long()
+    s = torch.from_numpy(inp["scores"]).double()
+    T = x.shape[0]
+    sel = o[ids, torch.arange(T)[:, None]]               # [T, k, d]
+    return (s[..., None] * sel).sum(1).numpy()
+
+
+def _rel_fro(a, b):
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+@pytest.mark.parametrize("clamp", [0.0, 1.0])
+def test_forward_matches_fp64_bruteforce(orc, clamp):
+    inp = small(T=40, d=128, I=64, E=6, k=3, seed=11)
+    y = f32(orc.forward(inp["x"], inp["ids"], inp["scores"], inp["w13"], inp["w2"], clamp=clamp))
+    ref = _dense_fp64(inp, clamp)
+    # bf16 rounding at four points: about 2^-9 relative each
+    assert _rel_fro(y, ref) < 8e-3
+    assert np.max(np.abs(y - ref)) < 3e-2 * np.sqrt(np.mean(ref ** 2)) + 2 ** -8 * np.abs(ref).max()
+
+
+def test_forward_single_expert_is_dense_swiglu_mlp(orc):
+    """E=1, k=1, score 1: the routed layer is a dense SwiGLU MLP (torch CPU ops,
+    rounding to bf16 at the same points)."""
+    inp = small(T=33, d=128, I=64, E=1, k=1, seed=5)
+    inp["scores"][:] = 1.0
+    y = orc.forward(inp["x"], inp["ids"], inp["scores"], inp["w13"], inp["w2"])
+    x = torch.from_numpy(f32(inp["x"]))
+    W13 = torch.from_numpy(f32(inp["w13"][0]))
+    W2 = torch.from_numpy(f32(inp["w2"][0]))
+    a = (x @ W13.T).to(torch.bfloat16).float()
+    h = (torch.nn.functional.silu(a[:, :64]) * a[:, 64:]).to(torch.bfloat16).float()
+    ref = (h @ W2.T).to(torch.bfloat16).float().numpy()
+    yy = f32(y)
+    # the only differences are FP32 summation order -> at most one bf16 step, rarely
+    ulp = np.abs(ref) * 2.0 ** -7 + 1e-30
+    assert np.mean(np.abs(yy - ref) <= ulp) == 1.0
+    assert np.mean(yy == ref) > 0.97
+
+
+def test_zero_score_padding_tokens_give_zero(orc):
+    inp = small(T=20, d=64, I=32, E=4, k=2, seed=9, pad=6)
+    y = f32(orc.forward(inp["x"], inp["ids"], inp["scores"], inp["w13"], inp["w2"]))
+    assert np.all(y[-6:] == 0)
+    assert np.all(np.abs(y[:-6]).sum(1) > 0)
+
+
+def test_forward_gate_up_order_matters(orc):
+    """Swapping the gate and up halves of W13 changes the output by O(1):
+    the pins above would catch a swapped reading."""
+    inp = small(T=16, d=64, I=32, E=3, k=2, seed=2)
+    y = f32(orc.forward(inp["x"], inp["ids"], inp["scores"], inp["w13"], inp["w2"]))
+    w = inp["w13"].copy()
+    w = np.concatenate([w[:, 32:], w[:, :32]], axis=1)
+    y2 = f32(orc.forward(inp["x"], inp["ids"], inp["scores"], np.ascontiguousarray(w), inp["w2"]))
+    assert _rel_fro(y2, y) > 0.3
+
+
+# ---------------------------------------------------------------------------
+# backward against torch autograd in FP64 (rounding-free)
+
+
+def _autograd_fp64(inp, clamp=0.0):
+    x = torch.from_numpy(f32(inp["x"]).astype(np.float64)).requires_grad_()
+    W13 = torch.from_numpy(f32(inp["w13"]).astype(np.float64)).requires_grad_()
+    W2 = torch.from_numpy(f32(inp["w2"]).astype(np.float64)).requires_grad_()
+    s = torch.from_numpy(inp["scores"].astype(np.float64)).requires_grad_()
+    ids = torch.from_numpy(inp["ids"]).long()
+    T, k = ids.shape
+    I = W2.shape[2]
+    Wsel = W13[ids]                                       # [T, k, 2I, d]
+    gu = torch.einsum("td,tkid->tki", x, Wsel)
+    # the clamp decision is taken on the bf16-rounded pre-activation (R1); round
+    # the value, pass the gradient straight through
+    gu = gu + (gu.detach().float().to(torch.bfloat16).double() - gu.detach())
+    g, u = gu[..., :I], gu[..., I:]
+    if clamp:
+        g, u = g.clamp(-clamp, clamp), u.clamp(-clamp, clamp)
+    h = torch.nn.functional.silu(g) * u
+    o = torch.einsum("tki,tkdi->tkd", h, W2[ids])
+    y = (s[..., None] * o).sum(1)
+    dy = torch.from_numpy(f32(inp["dy"]).astype(np.float64))
+    (y * dy).sum().backward()
+    return dict(dx=x.grad.numpy(), ds=s.grad.numpy(), dw13=W13.grad.numpy(), dw2=W2.grad.numpy())
+
+
+@pytest.mark.parametrize("clamp", [0.0, 0.75])
+def test_backward_matches_fp64_autograd(orc, clamp):
+    inp = small(T=40, d=64, I=32, E=5, k=3, seed=21)
+    ref = _autograd_fp64(inp, clamp)
+    dx, ds = orc.backward(inp["x"], inp["ids"], inp["scores"], inp["w13"], inp["w2"], inp["dy"],
+                          clamp=clamp)
+    assert _rel_fro(f32(dx), ref["dx"]) < 2e-2
+    assert _rel_fro(ds, ref["ds"]) < 2e-2
+    for e in range(5):
+        d13, d2, rows = orc.wgrad_expert(inp["x"], inp["ids"], inp["scores"], inp["w13"],
+                                         inp["w2"], inp["dy"], e, clamp=clamp)
+        assert rows == int((inp["ids"] == e).sum())
+        assert _rel_fro(d13, ref["dw13"][e]) < 2e-2
+        assert _rel_fro(d2, ref["dw2"][e]) < 2e-2
+
+
+def test_dscores_linearity_invariant(orc):
+    """y is linear in each score, so dscores[t,j] = <dY_t, o_j> where o_j = ys_j / s_j."""
+    inp = small(T=12, d=64, I=32, E=4, k=2, seed=4)
+    _, it = orc.forward(inp["x"], inp["ids"], inp["scores"], inp["w13"], inp["w2"],
+                        intermediates=True)
+    _, ds = orc.backward(inp["x"], inp["ids"], inp["scores"], inp["w13"], inp["w2"], inp["dy"])
+    dy = f32(inp["dy"])
+    o = f32(it["ys"]) / inp["scores"][..., None]
+    lhs = np.einsum("tkd,td->tk", o, dy)
+    assert _rel_fro(ds, lhs) < 1e-2
+
+
+def test_zero_score_padding_gradients(orc):
+    """Padding tokens: no dX, no dW contribution, but their dscores are defined."""
+    inp = small(T=20, d=64, I=32, E=4, k=2, seed=9, pad=6)
+    dx, ds = orc.backward(inp["x"], inp["ids"], inp["scores"], inp["w13"], inp["w2"], inp["dy"])
+    assert np.all(f32(dx)[-6:] == 0)
+    assert np.all(np.abs(ds[-6:]) > 0)
+    cut = {k: (v[:-6] if k in ("x", "ids", "scores", "dy") else v) for k, v in inp.items()}
+    for e in range(4):
+        a13, a2, _ = orc.wgrad_expert(inp["x"], inp["ids"], inp["scores"], inp["w13"], inp["w2"],
+                                      inp["dy"], e)
+        b13, b2, _ = orc.wgrad_expert(cut["x"], cut["ids"], cut["scores"], inp["w13"], inp["w2"],
+                                      cut["dy"], e)
+        assert np.array_equal(a13, b13) and np.array_equal(a2, b2)
+
+
+# ---------------------------------------------------------------------------
+# FP32 working type against the FP64 build of the same definition
+
+
+def test_fp32_oracle_agrees_with_fp64_oracle(orc, orc64):
+    inp = small(T=32, d=256, I=128, E=4, k=2, seed=8)
+    y = f32(orc.forward(inp["x"], inp["ids"], inp["scores"], inp["w13"], inp["w2"]))
+    y64 = f32(orc64.forward(inp["x"], inp["ids"], inp["scores"], inp["w13"], inp["w2"]))
+    assert _rel_fro(y, y64) < 2e-3
+    ulp = np.abs(y64) * 2.0 ** -7 + 1e-30
+    assert np.all(np.abs(y - y64) <= 2 * ulp)
+
+
+# ---------------------------------------------------------------------------
+# MXFP8
+
+
+def test_e4m3_decode_matches_torch_float8(orc):
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    ours = orc.e4m3_decode(codes)
+    theirs = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    assert np.array_equal(ours, theirs)
+    assert ours.max() == 448.0 and ours[codes == 0x01][0] == 2.0 ** -9
+
+
+def test_e4m3_encode_roundtrip_and_ties(orc):
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    vals = orc.e4m3_decode(codes)
+    assert np.array_equal(orc.e4m3_encode(vals), codes)
+    pos = np.sort(vals[vals > 0])
+    mids = (pos[:-1] + pos[1:]) / 2
+    enc = orc.e4m3_encode(mids)
+    lo_code = orc.e4m3_encode(pos[:-1])
+    expect = np.where(lo_code % 2 == 0, lo_code, lo_code + 1)   # ties to the even code
+    assert np.array_equal(enc, expect)
+    # saturation
+    assert np.array_equal(orc.e4m3_encode(np.array([448.0, 460.0, 1e6, -1e9])),
+                          np.array([0x7E, 0x7E, 0x7E, 0xFE], np.uint8))
+
+
+def test_e4m3_encode_matches_torch_float8(orc):
+    rng = np.random.default_rng(1)
+    v = (rng.standard_normal(200000) * 2.0 ** rng.uniform(-12, 10, 200000)).astype(np.float32)
+    v = np.clip(v, -448, 448).astype(np.float64)
+    ours = orc.e4m3_encode(v)
+    theirs = torch.from_numpy(v.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, theirs)
+
+
+def test_mxfp8_block_scale_closed_form(orc):
+    rng = np.random.default_rng(2)
+    m = bits(rng.standard_normal((64, 256)).astype(np.float32) *
+             (2.0 ** rng.integers(-20, 20, (64, 1))).astype(np.float32))
+    m[3, 32:64] = 0                                   # an all-zero block
+    codes, scales = orc.quant_mxfp8(m)
+    v = f32(m).reshape(64, 8, 32).astype(np.float64)
+    amax = np.abs(v).max(-1)
+    _, ex = np.frexp(amax)
+    X = np.clip(ex - 1 - 8, -127, 127)
+    expect = np.where(amax == 0, 0, X + 127)
+    assert np.array_equal(scales, expect.astype(np.uint8))
+    scaled = v * 2.0 ** (-X[..., None])
+    torch_codes = torch.from_numpy(np.clip(scaled, -448, 448).astype(np.float32).reshape(64, 256)) \
+        .to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    torch_codes[3, 32:64] = 0
+    assert np.array_equal(codes, torch_codes)
+    # every block's largest magnitude lands in [256, 448]
+    dec = orc.e4m3_decode(codes).reshape(64, 8, 32)
+    big = np.abs(dec).max(-1)[amax > 0]
+    assert big.min() >= 256 and big.max() <= 448
+
+
+def test_mxfp8_forward_matches_fp64_dequantised(orc):
+    """MXFP8 forward = FP64 matmuls of the dequantised operands (quantised with
+    torch's float8 conversion and numpy's frexp), with the same bf16 points."""
+    inp = small(T=24, d=128, I=64, E=4, k=2, seed=13)
+    w13q, w13s = orc.quant_mxfp8(inp["w13"])
+    w2q, w2s = orc.quant_mxfp8(inp["w2"])
+    y, h = orc.forward_mxfp8(inp["x"], inp["ids"], inp["scores"], w13q, w13s, w2q, w2s,
+                             return_h=True)
+
+    def deq(b):
+        v = f32(b).astype(np.float64)
+        K = v.shape[-1]
+        blk = v.reshape(v.shape[:-1] + (K // 32, 32))
+        amax = np.abs(blk).max(-1, keepdims=True)
+        _, ex = np.frexp(amax)
+        X = ex - 1 - 8
+        q = torch.from_numpy(np.clip(blk * 2.0 ** -X, -448, 448).astype(np.float32)) \
+            .to(torch.float8_e4m3fn).double().numpy()
+        return (q * 2.0 ** X).reshape(v.shape)
+
+    xd, w13d, w2d = deq(inp["x"]), deq(inp["w13"]), deq(inp["w2"])
+    T, k = inp["ids"].shape
+    yref = np.zeros((T, 128))
+    for t in range(T):
+        for j in range(k):
+            e = inp["ids"][t, j]
+            a = f32(bits(w13d[e] @ xd[t]))
+            G, U = a[:64].astype(np.float64), a[64:].astype(np.float64)
+            hh = bits(G / (1 + np.exp(-G)) * U)
+            assert np.mean(hh == h[t, j]) > 0.95
+            o = w2d[e] @ deq(hh[None])[0]
+            yref[t] += f32(bits(inp["scores"][t, j] * o))
+    assert _rel_fro(f32(y), yref) < 5e-3
