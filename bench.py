@@ -1,0 +1,438 @@
+#!/usr/bin/env python
+"""Benchmark of the routed-expert hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one pass of the whole hot path over one batch: forward with saved
+activations (dispatch, gather, W13 GEMM + SwiGLU, W2 GEMM x score, combine) and
+backward (dY gather, DGRAD-W2 + SwiGLU backward, DGRAD-W13, dX/dscores combine,
+WGRAD-W2, WGRAD-W13) of the training workload T=8192, d=2048, I=768, E=128,
+k=8 with uniform routing, on synthetic seeded inputs (moe_inputs).
+
+Throughput is routed-expert TFLOP/s counted as 18*T*k*d*I per forward+backward
+(6*T*k*d*I forward), the whole job over all ranks.  Under torchrun each rank
+runs an independent replica on its own GPU and its own batch (weak scaling; the
+only collectives are the barrier and the max over ranks of the timed region).
+
+--impl reference times the CPU oracle (single-threaded) on a bounded sample of
+the same workload: it is the reference arm of this benchmark.
+
+Prints ONE JSON line on rank 0.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "routed-expert TFLOP/s (fwd; fwd+bwd) at T=8192 E=128 k=8; % of GB300 tensor peak"
+WORKLOAD = "train_e128"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+FWD_STAGES = ["dispatch", "gather_x", "w13_swiglu", "w2_score", "combine_y"]
+BWD_STAGES = ["gather_dy", "dgrad_w2_swiglu", "dgrad_w13", "combine_dx", "wgrad_w2", "wgrad_w13"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work per stage (routed rows R = T*k; padding rows not counted)
+
+
+def stage_model(c):
+    T, d, I, E, k = c["T"], c["d"], c["I"], c["E"], c["k"]
+    R = T * k
+    return {
+        # bound, algorithmic flops, algorithmic bytes
+        "dispatch": ("hbm", 0, 8 * R + 4 * R * 3),
+        "gather_x": ("hbm", 0, 2 * T * d + 2 * R * d),
+        "w13_swiglu": ("tensor", 4 * R * d * I, 2 * R * d + E * 2 * I * d * 2 + 2 * R * I + 4 * R * I),
+        "w2_score": ("tensor", 2 * R * d * I, 2 * R * I + E * d * I * 2 + 2 * R * d),
+        "combine_y": ("hbm", 0, 2 * R * d + 2 * T * d + 4 * T * k),
+        "gather_dy": ("hbm", 0, 2 * T * d + 2 * R * d),
+        "dgrad_w2_swiglu": ("hbm", 2 * R * d * I, 2 * R * d + E * d * I * 2 + 2 * R * I + 4 * R * I
+                            + 4 * R * I + 2 * R * I),
+        "dgrad_w13": ("tensor", 4 * R * d * I, 4 * R * I + E * 2 * I * d * 2 + 2 * R * d),
+        "combine_dx": ("hbm", 0, 2 * R * d + 2 * T * d + 8 * T * k),
+        "wgrad_w2": ("hbm", 2 * R * d * I, 2 * R * d + 2 * R * I + 8 * E * d * I),
+        "wgrad_w13": ("hbm", 4 * R * d * I, 4 * R * I + 2 * R * d + 8 * E * 2 * I * d),
+    }
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            m = json.load(f)
+        return {k: float(m[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "routed_mixture_experts_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(stage):
+    """DRAM bytes per launch of `stage` from the committed ncu summary, if it was
+    taken on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    cur = kernel_source_hash()
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and not line.startswith("#") and parts[0] == stage:
+                return float(parts[1]) if parts[2] == cur else None
+    return None
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+
+
+class ClockSampler:
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_index):
+        self.rows = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == len(self.FIELDS):
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        if not sm:
+            return None
+        mx = max(float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit())
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[3 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": reasons,
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (timing only; no data-path collective)
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value, device=None):
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (reference arm and cpu_baseline)
+
+
+def oracle_sample(inp, n_tokens, seconds, max_experts=None):
+    """Time the single-threaded oracle on forward+backward (with weight
+    gradients) of the routed rows of experts 0, 1, ... among the first
+    n_tokens tokens, until `seconds` have passed.  Returns (flops, seconds, experts)."""
+    from oracle import load_oracle
+
+    orc = load_oracle("float")
+    c = inp["cfg"]
+    sub = {k: inp[k][:n_tokens].copy() for k in ("x", "ids", "scores", "dy")}
+    flops = 0.0
+    t0 = time.perf_counter()
+    e = 0
+    while True:
+        _, _, rows = orc.wgrad_expert(sub["x"], sub["ids"], sub["scores"], inp["w13"], inp["w2"],
+                                      sub["dy"], e % c["E"], clamp=c["clamp"])
+        flops += 18.0 * c["d"] * c["I"] * rows
+        e += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or (max_experts and e >= max_experts):
+            return flops, el, e
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import moe_inputs as mi
+
+    inp = mi.make_inputs(WORKLOAD, seed=args.seed,
+                         need=("x", "ids", "scores", "w13", "w2", "dy"))
+    c = inp["cfg"]
+    n_tok = 1024
+    # warm-up samples, then K timed samples (one expert's rows per step)
+    oracle_sample(inp, n_tok, 0.0, max_experts=max(args.warmup, 1))
+    flops, el, ne = oracle_sample(inp, n_tok, 1e9, max_experts=args.steps)
+    value = flops / el / 1e12
+    sample = ("per step: forward+backward incl. weight gradients of the routed rows of one expert "
+              "among tokens 0..%d (%d steps, %.1f GFLOP, %.1f s)" % (n_tok - 1, ne, flops / 1e9, el))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / ne * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": "%s (T=%d, d=%d, I=%d, E=%d, k=%d, uniform routing, forward+backward)"
+                   % (WORKLOAD, c["T"], c["d"], c["I"], c["E"], c["k"])},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# our arm
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    from routed_mixture_experts_gb300 import build as _build
+
+    _build.build()
+    import moe_inputs as mi
+    import routed_mixture_experts_gb300 as moe
+
+    need = ("x", "ids", "scores", "w13", "w2", "dy", "dw13", "dw2")
+    inp = mi.make_inputs(WORKLOAD, seed=args.seed + rank, need=need)
+    c = inp["cfg"]
+    T, d, I, E, k = c["T"], c["d"], c["I"], c["E"], c["k"]
+
+    def to_dev(a):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        if a.dtype == np.uint16:
+            t = t.view(torch.bfloat16)
+        return t.to(dev)
+
+    D = {key: to_dev(inp[key]) for key in need}
+    plan = moe.MoePlan(T, d, I, E, k, clamp=c["clamp"],
+                       flags=moe.MOE_WS_TRAINING | moe.MOE_WS_HOST_STAGING, device=dev)
+    y = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+    dx = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+    dsc = torch.empty(T, k, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        plan.forward(D["x"], D["ids"], D["scores"], D["w13"], D["w2"], y=y, save=True)
+        plan.backward(D["dy"], D["w13"], D["w2"], D["dw13"], D["dw2"], dx=dx, dscores=dsc)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    rc, det = plan.check()
+    if rc != 0:
+        raise RuntimeError("device error %d (%d) during warm-up" % (rc, det))
+
+    # per-stage events (recorded by the library on this stream), one set per step
+    K = args.steps
+    evf = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    evb = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(K)]
+    for ev in [e for s in evf + evb for e in s]:
+        ev.record(stream)                       # materialise the handles
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    time.sleep(0.25 if clocks else 0)
+    n0 = plan.launch_count()
+    t_start.record(stream)
+    for i in range(K):
+        plan.set_timing_events(0, evf[i])
+        plan.set_timing_events(1, evb[i])
+        step()
+    t_end.record(stream)
+    n1 = plan.launch_count()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    clk = clocks.stop() if clocks else None
+    plan.set_timing_events(0, None)
+    plan.set_timing_events(1, None)
+    rc, det = plan.check()
+    if rc != 0:
+        raise RuntimeError("device error %d (%d) in the timed region" % (rc, det))
+
+    ms = t_start.elapsed_time(t_end)
+    ms = max_over_ranks(ms, dev)
+    ms_step = ms / K
+    flops_step = 18.0 * T * k * d * I
+    value = flops_step * ws / (ms_step * 1e-3) / 1e12
+
+    # stage times (average over the timed steps)
+    stage_ms = {}
+    for j, name in enumerate(FWD_STAGES):
+        stage_ms[name] = sum(evf[i][j].elapsed_time(evf[i][j + 1]) for i in range(K)) / K
+    for j, name in enumerate(BWD_STAGES):
+        stage_ms[name] = sum(evb[i][j].elapsed_time(evb[i][j + 1]) for i in range(K)) / K
+    fwd_ms = sum(stage_ms[s] for s in FWD_STAGES)
+
+    # roofline of every stage; the dominant one is reported as "roofline"
+    pk, pk_src = peaks()
+    model = stage_model(c)
+    stages = {}
+    for name, t_ms in stage_ms.items():
+        bound, fl, by = model[name]
+        if bound == "tensor":
+            ach, peak, unit = fl / (t_ms * 1e-3) / 1e12, pk["bf16_tflops_sustained"], "TFLOP/s"
+        else:
+            ach, peak, unit = by / (t_ms * 1e-3) / 1e9, pk["hbm_gbs"], "GB/s"
+        stages[name] = {"ms": round(t_ms, 5), "bound": bound, "achieved": round(ach, 1),
+                        "peak": peak, "unit": unit, "frac": round(ach / peak, 4),
+                        "tflops": round(fl / (t_ms * 1e-3) / 1e12, 1) if fl else None}
+    dom = max(stage_ms, key=stage_ms.get)
+    ds = stages[dom]
+    roofline = {"kernel": dom, "bound": ds["bound"], "achieved": ds["achieved"], "peak": ds["peak"],
+                "unit": ds["unit"], "frac": ds["frac"], "traffic": traffic_for(dom),
+                "peak_source": "%s (%s)" % (pk_src, "sustained bf16" if ds["bound"] == "tensor"
+                                            else "copy bandwidth")}
+
+    # end to end through the C ABI with pinned host buffers (copies in the timed region)
+    e2e = None
+    if args.e2e_steps > 0:
+        pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+        xh, dyh = pin(inp["x"]).view(torch.bfloat16), pin(inp["dy"]).view(torch.bfloat16)
+        idh, sch = pin(inp["ids"]), pin(inp["scores"])
+        yh = torch.empty(T, d, dtype=torch.bfloat16).pin_memory()
+        dxh = torch.empty(T, d, dtype=torch.bfloat16).pin_memory()
+        dsh = torch.empty(T, k, dtype=torch.float32).pin_memory()
+
+        def hstep():
+            plan.step_host(xh, idh, sch, D["w13"], D["w2"], yh, dyh, D["dw13"], D["dw2"], dxh, dsh)
+
+        for _ in range(2):
+            hstep()
+        torch.cuda.synchronize()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            hstep()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = max_over_ranks(e0.elapsed_time(e1), dev) / args.e2e_steps
+        h2d = 2 * T * d * 2 + 4 * T * k * 2
+        d2h = 2 * T * d * 2 + 4 * T * k
+        e2e = {"value": flops_step * ws / (ems * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems}
+
+    if rank != 0:
+        return
+    cpu = None
+    if ws == 1 or rank == 0:
+        flops, el, ne = oracle_sample(inp, 1024, args.cpu_seconds)
+        cpu = {"value": flops / el / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+               "sample": "forward+backward incl. weight gradients of the routed rows of experts "
+                         "0..%d among tokens 0..1023 (%.2f GFLOP in %.1f s, single thread)"
+                         % (ne - 1, flops / 1e9, el)}
+    ws_bytes = plan.workspace.numel() + sum(t.numel() * t.element_size() for t in D.values())
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "%s (T=%d, d=%d, I=%d, E=%d, k=%d, uniform routing, "
+                               "forward+backward)" % (WORKLOAD, T, d, I, E, k),
+                   "tokens_per_gpu": T, "l2": "inputs larger than L2 (%.1f GB resident per GPU)"
+                   % (ws_bytes / 1e9), "parallelism": "replicas" if ws > 1 else "single GPU"},
+        "fwd_tflops": 6.0 * T * k * d * I / (fwd_ms * 1e-3) / 1e12,
+        "fwd_ms": fwd_ms,
+        "e2e": e2e, "gpu_launches": int(n1 - n0), "roofline": roofline, "stages": stages,
+        "cpu_baseline": cpu, "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+    ws, _, _ = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+
+        if dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,252 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) routed-expert hot path.
+ *
+ * One call runs, on one GPU, the routed-expert layer whose caller owns the
+ * activations x[T,d] (bf16), the top-k expert ids[T,k] (int32, distinct per
+ * row), the routing scores[T,k] (fp32) and the expert weights W13[E,2I,d] and
+ * W2[E,d,I] (bf16):
+ *
+ *     dispatch (expert-major permutation) -> W13 grouped GEMM -> SwiGLU
+ *       -> W2 grouped GEMM x score -> deterministic combine
+ *
+ * and its backward (input gradients, weight gradients accumulated in place,
+ * score gradients).  Sources: "Dist-MoE: Meta's Blackwell SM100 MoE Kernels"
+ * (section "What it is selling": caller-owned inputs, one library-owned
+ * context, the pipeline, FPROP/DGRAD/WGRAD, BF16 with FP32 accumulate, MXFP8
+ * E4M3 after routing with prepared weights, plain/clamped SwiGLU, in-place
+ * WGRAD; section "Caveats": fixed physical token count with zero-score padding,
+ * sequentially reusable, non-reentrant contexts, fatal scratch overflow) and
+ * the "nvfp4moe" README (section "Grouped GEMM": expert-major rows, m_indptr of
+ * length E+1, empty experts; section "MoE layer": distinct int32 ids, fp32
+ * weights, workspace overwritten by the next call, one plan per stream,
+ * allocation-free warmed plans; sections "Training" and "Supported kernel
+ * surface": deterministic dispatch, combine and router gradients; "Limits").
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller unless the
+ *     argument name ends in _host.  The library never frees them.
+ *   - bf16 tensors are passed as void* holding IEEE bfloat16 values; all
+ *     tensors are dense row-major (C order) with the shapes given.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Work is enqueued on it; no entry point below synchronises unless it says
+ *     so.  A plan is not reentrant: use one plan per concurrent stream.
+ *   - Return value: MOE_OK (0) or one of the MOE_ERR_* codes.  Argument errors
+ *     are detected on the host before anything is enqueued.  Errors found by
+ *     the device (bad ids, a wait that gave up) are recorded in the plan's
+ *     device error word and reported by moe_plan_check().
+ *   - No entry point allocates device memory after moe_plan_set_workspace();
+ *     forward and backward enqueue kernels and async copies only, so they may
+ *     be captured in a CUDA graph.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes -------------------------------------------------------- */
+#define MOE_OK                0
+#define MOE_ERR_INVALID_ARG   1  /* bad size, null pointer, misaligned pointer   */
+#define MOE_ERR_WORKSPACE     2  /* workspace missing or too small               */
+#define MOE_ERR_STATE         3  /* e.g. backward without a saving forward       */
+#define MOE_ERR_BAD_IDS       4  /* device found an id outside [0,E) or repeated */
+#define MOE_ERR_TIMEOUT       5  /* a device-side wait gave up                   */
+#define MOE_ERR_CUDA          6  /* a CUDA runtime/driver call failed            */
+#define MOE_ERR_UNSUPPORTED   7  /* combination not implemented                  */
+
+/* ---- precisions ------------------------------------------------------------ */
+#define MOE_PREC_BF16   0   /* bf16 operands, fp32 accumulate                     */
+#define MOE_PREC_MXFP8  1   /* E4M3 operands with E8M0 scales per 32 along K      */
+
+/* ---- workspace flags ------------------------------------------------------- */
+#define MOE_WS_TRAINING     1  /* keep forward activations and backward buffers */
+#define MOE_WS_HOST_STAGING 2  /* device copies of per-step host inputs/outputs  */
+
+typedef struct moe_plan moe_plan;
+
+/*
+ * moe_plan_create -- describe one routed-expert layer.
+ *   T  physical tokens per call (a fixed shape: callers with fewer tokens pad
+ *      and give the padding rows zero scores -- "Caveats", item 2)
+ *   d  hidden size, I expert intermediate size, E experts, k experts per token
+ *   precision  MOE_PREC_BF16 or MOE_PREC_MXFP8
+ * Limits ("Limits" section of the nvfp4moe README, adapted to whole tiles):
+ *   d % 128 == 0, I % 64 == 0, 1 <= k <= E <= 256, T >= 1, T*k < 2^31.
+ * Returns a host-side plan object (owned by the caller, free with
+ * moe_plan_destroy) or NULL on invalid arguments.  Does not touch the GPU
+ * except to query the current device's properties.
+ */
+moe_plan* moe_plan_create(int T, int d, int I, int E, int k, int precision);
+
+/* Free the plan (host memory only; the caller frees its workspace). */
+void moe_plan_destroy(moe_plan* plan);
+
+/*
+ * Clamped SwiGLU ("What it is selling": plain or clamped SwiGLU).  limit = 0
+ * selects plain silu(gate)*up; limit > 0 clips gate and up to [-limit, limit]
+ * before the activation, and the backward passes gradient only where the
+ * pre-activation lies inside the closed interval.
+ */
+int moe_plan_set_swiglu_clamp(moe_plan* plan, float limit);
+
+/*
+ * Bytes of device workspace the plan needs for `flags` (MOE_WS_*).  The size
+ * covers the worst case of padded expert-major rows,
+ *   Rpad <= T*k + E*(BM-1)   (BM = 128 rows per GEMM tile),
+ * so it never depends on the routing.  Returns 0 for a NULL plan.
+ */
+size_t moe_plan_workspace_bytes(const moe_plan* plan, int flags);
+
+/*
+ * Hand the plan a caller-allocated device buffer (256-byte aligned) of at least
+ * moe_plan_workspace_bytes(plan, flags) bytes.  The plan owns its contents from
+ * now on ("MoE layer": the workspace is overwritten by the next call).  Clears
+ * the device error word (a synchronous cudaMemset on the legacy stream).
+ * Returns MOE_ERR_WORKSPACE if `bytes` is too small.
+ */
+int moe_plan_set_workspace(moe_plan* plan, void* workspace, size_t bytes, int flags);
+
+/*
+ * Forward.  Inputs (device):
+ *   x       [T, d]  bf16         ids  [T, k] int32      scores [T, k] fp32
+ *   w13     [E, 2I, d] bf16: rows [0,I) gate, [I,2I) up (not interleaved)
+ *   w2      [E, d, I]  bf16
+ *   For MOE_PREC_MXFP8, w13/w2 hold E4M3 codes (uint8, same shapes) and
+ *   w13_sf [E, 2I, d/32], w2_sf [E, d, I/32] their E8M0 scales (see
+ *   moe_quantize_mxfp8); for bf16 pass NULL.
+ * Output: y [T, d] bf16, overwritten:
+ *   y[t] = bf16( sum_{j=0..k-1} bf16( scores[t,j] * W2[e] . h ) ),
+ *   h = bf16(silu(G) * U),  (G, U) = bf16(W13[e] . x[t]),  e = ids[t,j]
+ * (sum in fixed j order).  save_for_backward = 1 keeps what moe_backward needs
+ * in the workspace (requires a MOE_WS_TRAINING workspace).
+ * Ids outside [0,E) or repeated within a row set MOE_ERR_BAD_IDS in the device
+ * error word (detail = smallest offending flat index t*k+j); such elements are
+ * dropped, so memory stays safe, but y is then not meaningful.
+ */
+int moe_forward(moe_plan* plan, const void* x, const int32_t* ids, const float* scores,
+                const void* w13, const void* w2, const uint8_t* w13_sf, const uint8_t* w2_sf,
+                void* y, int save_for_backward, void* stream);
+
+/*
+ * Backward of the last saving forward on this plan ("What it is selling":
+ * DGRAD and WGRAD; nvfp4moe "Training": router gradients).  Inputs: dy [T, d]
+ * bf16 and the same w13/w2 as the forward.  Outputs:
+ *   dx      [T, d]      bf16, overwritten
+ *   dscores [T, k]      fp32, overwritten (gradient w.r.t. the given scores)
+ *   dw13    [E, 2I, d]  fp32, ACCUMULATED in place (+=); experts with no rows
+ *   dw2     [E, d, I]   fp32, ACCUMULATED in place      are left untouched
+ * Returns MOE_ERR_STATE if no saving forward preceded it, MOE_ERR_UNSUPPORTED
+ * for an MXFP8 plan.
+ */
+int moe_backward(moe_plan* plan, const void* dy, const void* w13, const void* w2,
+                 void* dx, float* dw13, float* dw2, float* dscores, void* stream);
+
+/*
+ * One training (or, with dy_host == NULL, inference) step from HOST buffers:
+ * copies x_host, ids_host, scores_host (and dy_host) into the plan's staging
+ * area, runs moe_forward (+ moe_backward), and copies y (and dx, dscores) back
+ * into the host buffers, all enqueued on `stream`; the caller synchronises the
+ * stream before reading the host outputs.  Host buffers should be pinned
+ * (page-locked) for the copies to be asynchronous.  Weights and weight
+ * gradients stay on the device.  Needs a MOE_WS_HOST_STAGING workspace (plus
+ * MOE_WS_TRAINING when dy_host != NULL).
+ */
+int moe_step_host(moe_plan* plan, const void* x_host, const int32_t* ids_host,
+                  const float* scores_host, const void* dy_host,
+                  const void* w13, const void* w2, float* dw13, float* dw2,
+                  void* y_host, void* dx_host, float* dscores_host, void* stream);
+
+/*
+ * MXFP8 block quantiser ("What it is selling": MXFP8 E4M3 with prepared
+ * weights).  in [rows, K] bf16 -> codes [rows, K] E4M3, scales [rows, K/32]
+ * E8M0, per 32-element block along K: X = floor(log2(amax)) - 8 clamped to
+ * [-127,127], scale code X+127 (0 for an all-zero block), code =
+ * E4M3(v * 2^-X) rounded to nearest even and saturated to +-448.
+ * K % 32 == 0.  Used to prepare weights and exported for bit-exact tests.
+ */
+int moe_quantize_mxfp8(const void* in, long rows, int K, uint8_t* codes, uint8_t* scales,
+                       void* stream);
+
+/*
+ * Synchronise the device, read and clear the plan's device error word.
+ * Returns MOE_OK or the first recorded device error; *detail (may be NULL)
+ * receives its detail (for MOE_ERR_BAD_IDS the smallest offending flat index).
+ */
+int moe_plan_check(moe_plan* plan, long long* detail);
+
+/* Human-readable name of a status code (static string). */
+const char* moe_status_string(int status);
+
+/*
+ * Inspection of the plan's workspace (for tests and tools).  Returns the device
+ * address and byte size of one internal tensor of the last call:
+ *   MOE_BUF_M_INDPTR  int32 [E+1]    expert-major row offsets (exact counts)
+ *   MOE_BUF_OFF_PAD   int32 [E+1]    row offsets with segments padded to BM
+ *   MOE_BUF_ROW_OF    int32 [T*k]    padded row of element t*k+j (-1: dropped)
+ *   MOE_BUF_TOKEN_OF  int32 [Rpad]   token of each padded row (-1: padding)
+ *   MOE_BUF_SCORE_OF  fp32  [Rpad]   score of each padded row (0: padding)
+ *   MOE_BUF_XE        bf16  [Rpad,d] gathered activations
+ *   MOE_BUF_A         bf16  [Rpad,2I] gate/up pre-activations (training)
+ *   MOE_BUF_H         bf16  [Rpad,I] SwiGLU output
+ *   MOE_BUF_YS        bf16  [Rpad,d] score-weighted expert outputs
+ *   MOE_BUF_DYE       bf16  [Rpad,d] gathered upstream gradient
+ *   MOE_BUF_DA        bf16  [Rpad,2I] gradient at gate/up
+ *   MOE_BUF_HS        bf16  [Rpad,I] score * h (WGRAD-W2 operand)
+ *   MOE_BUF_DXE       bf16  [Rpad,d] per-row input gradients
+ * Rows are valid up to off_pad[E].  Sizes are the worst-case capacities.
+ */
+#define MOE_BUF_M_INDPTR 0
+#define MOE_BUF_OFF_PAD  1
+#define MOE_BUF_ROW_OF   2
+#define MOE_BUF_TOKEN_OF 3
+#define MOE_BUF_SCORE_OF 4
+#define MOE_BUF_XE       5
+#define MOE_BUF_A        6
+#define MOE_BUF_H        7
+#define MOE_BUF_YS       8
+#define MOE_BUF_DYE      9
+#define MOE_BUF_DA       10
+#define MOE_BUF_HS       11
+#define MOE_BUF_DXE      12
+int moe_plan_buffer(const moe_plan* plan, int which, void** dev_ptr, size_t* bytes);
+
+/*
+ * Stage timing (for benchmarks and tools).  `events` holds caller-created
+ * cudaEvent_t handles (as void*); while set, each call records them on its
+ * stream at its stage boundaries:
+ *   which = 0 (moe_forward, n >= 6):  [0] start, [1] after dispatch (3 launches),
+ *     [2] after gather, [3] after W13+SwiGLU, [4] after W2 x score, [5] after combine
+ *   which = 1 (moe_backward, n >= 7): [0] start, [1] after dY gather,
+ *     [2] after DGRAD-W2 + SwiGLU backward, [3] after DGRAD-W13,
+ *     [4] after dX/dscores combine, [5] after WGRAD-W2, [6] after WGRAD-W13
+ * n = 0 (or events = NULL) stops recording.  The plan keeps the pointer: the
+ * array must stay valid while set.
+ */
+int moe_plan_set_timing_events(moe_plan* plan, int which, void* const* events, int n);
+
+/* Number of kernels this plan has launched so far (all entry points). */
+long long moe_plan_launch_count(const moe_plan* plan);
+
+/* Rows per GEMM tile (BM), i.e. the padding granule of each expert segment. */
+int moe_tile_rows(void);
+
+/*
+ * Dense bf16 GEMM through the same tcgen05 kernels (for tests):
+ *   mode 0: C[M,N] bf16  = A[M,K] . B[N,K]^T      (both operands K-major)
+ *   mode 1: C[M,N] bf16  = A[M,K] . B[K,N]        (B MN-major)
+ *   mode 2: C[M,N] fp32 += A[K,M]^T . B[K,N]      (both operands MN-major)
+ * M % 128 == 0, N % 64 == 0, K % 64 == 0 (mode 2: K % 128 == 0).  `scratch`
+ * is a device buffer of moe_gemm_scratch_bytes(M, K) bytes for the tile tables.
+ */
+size_t moe_gemm_scratch_bytes(int M, int K);
+int moe_gemm_bf16(int mode, const void* A, const void* B, void* C, int M, int N, int K,
+                  void* scratch, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -388,12 +388,13 @@ int orc_forward(int T, int d, int I, int E, int k, float clamp,
 //   dA      [ntok, k, 2I]  optional                              (R4)
 //   hs      [ntok, k, I]   optional                              (R7)
 //   g       [ntok, k, I]   optional, float
+//   dxe     [ntok, k, d]   optional, per-expert input gradients  (R5)
 int orc_backward(int T, int d, int I, int E, int k, float clamp,
                  const uint16_t* x, const int32_t* ids, const float* scores,
                  const uint16_t* w13, const uint16_t* w2, const uint16_t* dy,
                  int ntok, const int32_t* toks,
                  uint16_t* dx, float* dscores,
-                 uint16_t* dA_out, uint16_t* hs_out, float* g_out) {
+                 uint16_t* dA_out, uint16_t* hs_out, float* g_out, uint16_t* dxe_out) {
   Problem p = make_problem(T, d, I, E, k, clamp, x, ids, scores, w13, w2);
   std::vector<uint16_t> a(2 * I), h(I), ys(d), dA(2 * I), hs(I), dxe((size_t)k * d, 0);
   std::vector<char> ok(k);
@@ -433,6 +434,11 @@ int orc_backward(int T, int d, int I, int E, int k, float clamp,
       for (int j = 0; j < k; ++j)
         if (ok[j]) acc += bf(dxe[(size_t)j * d + c]);
       dx[(size_t)n * d + c] = real_to_bf16(acc);                // R6
+    }
+    if (dxe_out) {
+      for (int j = 0; j < k; ++j)
+        for (int c = 0; c < d; ++c)
+          dxe_out[((size_t)n * k + j) * d + c] = ok[j] ? dxe[(size_t)j * d + c] : 0;
     }
   }
   return 0;

@@ -56,7 +56,7 @@ class Oracle:
         L.orc_gather_rows.argtypes = [i32, i32, vp, vp, vp]
         L.orc_combine_rows.argtypes = [i32, i32, i32, vp, vp, vp]
         L.orc_forward.argtypes = [i32] * 5 + [f32] + [vp] * 5 + [i32, vp] + [vp] * 4
-        L.orc_backward.argtypes = [i32] * 5 + [f32] + [vp] * 6 + [i32, vp] + [vp] * 5
+        L.orc_backward.argtypes = [i32] * 5 + [f32] + [vp] * 6 + [i32, vp] + [vp] * 6
         L.orc_wgrad_expert.argtypes = [i32] * 5 + [f32] + [vp] * 6 + [i32, vp, vp]
         L.orc_quant_mxfp8.argtypes = [i64, i32, vp, vp, vp]
         L.orc_e4m3_encode.argtypes = [vp, vp, i64]
@@ -132,16 +132,17 @@ class Oracle:
         n = T if toks is None else toks_a.size
         dx = np.empty((n, d), np.uint16)
         ds = np.empty((n, k), np.float32)
-        dA = hs = g = None
+        dA = hs = g = dxe = None
         if intermediates:
             dA = np.empty((n, k, 2 * I), np.uint16)
             hs = np.empty((n, k, I), np.uint16)
             g = np.empty((n, k, I), np.float32)
+            dxe = np.empty((n, k, d), np.uint16)
         self.lib.orc_backward(T, d, I, E, k, float(clamp), _ptr(x), _ptr(ids), _ptr(scores),
                               _ptr(w13), _ptr(w2), _ptr(dy), n, _ptr(toks_a), _ptr(dx), _ptr(ds),
-                              _ptr(dA), _ptr(hs), _ptr(g))
+                              _ptr(dA), _ptr(hs), _ptr(g), _ptr(dxe))
         if intermediates:
-            return dx, ds, dict(dA=dA, hs=hs, g=g)
+            return dx, ds, dict(dA=dA, hs=hs, g=g, dxe=dxe)
         return dx, ds
 
     def wgrad_expert(self, x, ids, scores, w13, w2, dy, e, clamp=0.0):

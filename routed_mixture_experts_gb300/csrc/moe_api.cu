@@ -1,0 +1,598 @@
+// moe_api.cu -- the C ABI declared in include/moe.h: plan, workspace layout,
+// tensor-map encoding and the launch sequence of forward and backward.
+//
+// Forward  ("Dist-MoE" note, "What it is selling": route on GPU -> W13 -> SwiGLU
+//           -> W2 -> combine; nvfp4moe README, "MoE layer"):
+//   route (3 small launches) -> gather x rows -> W13 GEMM + SwiGLU -> W2 GEMM x
+//   score -> combine
+// Backward ("What it is selling": DGRAD / WGRAD, in-place WGRAD accumulation;
+//           nvfp4moe README, "Training": router gradients):
+//   gather dY rows -> DGRAD-W2 + SwiGLU backward + score-grad partials ->
+//   DGRAD-W13 -> combine dX and dscores -> WGRAD-W2 -> WGRAD-W13
+// Everything is enqueued on the caller's stream; nothing allocates, nothing
+// synchronises (moe_plan_check and moe_plan_set_workspace excepted).
+
+#include <climits>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/moe.h"
+#include "moe_device.cuh"
+#include "moe_internal.h"
+
+using namespace moe;
+
+struct moe_plan {
+  int T, d, I, E, k, precision;
+  float clamp;
+  int num_sms;
+  int R;        // T*k
+  int RP;       // worst-case padded rows
+  int nblk;     // dispatch chunks
+  int bn13, bn2, bnd2, bnw2, bnw13;
+  // workspace
+  char* ws;
+  size_t ws_bytes;
+  int ws_flags;
+  // pointers into the workspace
+  DevError* err;
+  int32_t *counts, *m_indptr, *off_pad, *num_mtiles, *num_nonempty, *expert_order, *tile_expert,
+      *blockcounts, *row_of, *token_of;
+  float *score_of, *pdscore;
+  uint16_t *xe, *h, *ys, *a, *dye, *dA, *hs, *dxe;
+  // host staging
+  uint16_t *st_x, *st_dy, *st_y, *st_dx;
+  int32_t* st_ids;
+  float *st_scores, *st_dscores;
+  // tensor maps over workspace tensors
+  CUtensorMap tm_xe, tm_h, tm_dye, tm_dA, tm_hs;
+  // tensor maps over the caller's weights (re-encoded when the pointers change)
+  CUtensorMap tm_w13, tm_w2;
+  const void *w13_cached, *w2_cached;
+  int saved;
+  // optional stage events and the launch counter
+  void* const* ev[2];
+  int nev[2];
+  long long launches;
+};
+
+namespace moe {
+
+int encode_tmap_bf16(CUtensorMap* map, const void* base, long long rows, long long cols) {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !p)
+      return MOE_ERR_CUDA;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {64, 64};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace moe
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+int pick_bn_n(int n) { return n % 256 == 0 ? 256 : (n % 128 == 0 ? 128 : 64); }
+
+// Lays the workspace out (bases relative to `base`; base may be nullptr to size it).
+size_t layout(moe_plan* p, char* base, int flags) {
+  size_t off = 0;
+  auto take = [&](size_t bytes) -> char* {
+    char* r = base ? base + off : nullptr;
+    off = align_up(off + bytes);
+    return r;
+  };
+  const size_t RP = p->RP, d = p->d, I = p->I, E = p->E, T = p->T, k = p->k;
+  p->err = reinterpret_cast<DevError*>(take(sizeof(DevError)));
+  p->counts = reinterpret_cast<int32_t*>(take(4 * E));
+  p->m_indptr = reinterpret_cast<int32_t*>(take(4 * (E + 1)));
+  p->off_pad = reinterpret_cast<int32_t*>(take(4 * (E + 1)));
+  p->num_mtiles = reinterpret_cast<int32_t*>(take(4));
+  p->num_nonempty = reinterpret_cast<int32_t*>(take(4));
+  p->expert_order = reinterpret_cast<int32_t*>(take(4 * E));
+  p->tile_expert = reinterpret_cast<int32_t*>(take(4 * (RP / kBM)));
+  p->blockcounts = reinterpret_cast<int32_t*>(take(4 * (size_t)p->nblk * E));
+  p->row_of = reinterpret_cast<int32_t*>(take(4 * (size_t)p->R));
+  p->token_of = reinterpret_cast<int32_t*>(take(4 * RP));
+  p->score_of = reinterpret_cast<float*>(take(4 * RP));
+  p->xe = reinterpret_cast<uint16_t*>(take(2 * RP * d));
+  p->h = reinterpret_cast<uint16_t*>(take(2 * RP * I));
+  p->ys = reinterpret_cast<uint16_t*>(take(2 * RP * d));
+  p->a = p->dye = p->dA = p->hs = p->dxe = nullptr;
+  p->pdscore = nullptr;
+  if (flags & MOE_WS_TRAINING) {
+    p->a = reinterpret_cast<uint16_t*>(take(2 * RP * 2 * I));
+    p->dye = reinterpret_cast<uint16_t*>(take(2 * RP * d));
+    p->dA = reinterpret_cast<uint16_t*>(take(2 * RP * 2 * I));
+    p->hs = reinterpret_cast<uint16_t*>(take(2 * RP * I));
+    p->dxe = reinterpret_cast<uint16_t*>(take(2 * RP * d));
+    p->pdscore = reinterpret_cast<float*>(take(4 * RP * (I / p->bnd2)));
+  }
+  p->st_x = p->st_dy = p->st_y = p->st_dx = nullptr;
+  p->st_ids = nullptr;
+  p->st_scores = p->st_dscores = nullptr;
+  if (flags & MOE_WS_HOST_STAGING) {
+    p->st_x = reinterpret_cast<uint16_t*>(take(2 * T * d));
+    p->st_ids = reinterpret_cast<int32_t*>(take(4 * T * k));
+    p->st_scores = reinterpret_cast<float*>(take(4 * T * k));
+    p->st_y = reinterpret_cast<uint16_t*>(take(2 * T * d));
+    if (flags & MOE_WS_TRAINING) {
+      p->st_dy = reinterpret_cast<uint16_t*>(take(2 * T * d));
+      p->st_dx = reinterpret_cast<uint16_t*>(take(2 * T * d));
+      p->st_dscores = reinterpret_cast<float*>(take(4 * T * k));
+    }
+  }
+  return off;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return MOE_OK;
+  fprintf(stderr, "moe_gb300: CUDA error %s\n", cudaGetErrorString(e));
+  return MOE_ERR_CUDA;
+}
+
+int reset_error_word(DevError* err) {
+  DevError h;
+  h.code = 0;
+  h.first_bad = INT_MAX;
+  h.where = 0;
+  h.pad = 0;
+  return cuda_status(cudaMemcpy(err, &h, sizeof(h), cudaMemcpyHostToDevice));
+}
+
+int refresh_weight_maps(moe_plan* p, const void* w13, const void* w2) {
+  if (w13 != p->w13_cached) {
+    if (encode_tmap_bf16(&p->tm_w13, w13, (long long)p->E * 2 * p->I, p->d) != MOE_OK)
+      return MOE_ERR_CUDA;
+    p->w13_cached = w13;
+  }
+  if (w2 != p->w2_cached) {
+    if (encode_tmap_bf16(&p->tm_w2, w2, (long long)p->E * p->d, p->I) != MOE_OK)
+      return MOE_ERR_CUDA;
+    p->w2_cached = w2;
+  }
+  return MOE_OK;
+}
+
+GemmArgs rows_args(const moe_plan* p) {
+  GemmArgs g;
+  memset(&g, 0, sizeof(g));
+  g.wgrad = 0;
+  g.num_mtiles = p->num_mtiles;
+  g.tile_expert = p->tile_expert;
+  g.err = p->err;
+  g.clamp = p->clamp;
+  g.I = p->I;
+  return g;
+}
+
+GemmArgs wgrad_args(const moe_plan* p) {
+  GemmArgs g;
+  memset(&g, 0, sizeof(g));
+  g.wgrad = 1;
+  g.off_pad = p->off_pad;
+  g.expert_order = p->expert_order;
+  g.num_nonempty = p->num_nonempty;
+  g.err = p->err;
+  return g;
+}
+
+int gather_grid(const moe_plan* p) { return p->num_sms * 8; }
+
+void mark(const moe_plan* p, int which, int i, cudaStream_t st) {
+  if (p->ev[which] && i < p->nev[which] && p->ev[which][i])
+    cudaEventRecord(static_cast<cudaEvent_t>(p->ev[which][i]), st);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(int s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_STATE: return "MOE_ERR_STATE";
+    case MOE_ERR_BAD_IDS: return "MOE_ERR_BAD_IDS";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    default: return "MOE_ERR_UNKNOWN";
+  }
+}
+
+int moe_tile_rows(void) { return kBM; }
+
+moe_plan* moe_plan_create(int T, int d, int I, int E, int k, int precision) {
+  if (T < 1 || d < 128 || I < 64 || d % 128 || I % 64 || k < 1 || E < k || E > 256) return nullptr;
+  if ((long long)T * k >= (1LL << 31) - (long long)E * kBM) return nullptr;
+  if (precision != MOE_PREC_BF16 && precision != MOE_PREC_MXFP8) return nullptr;
+  moe_plan* p = new (std::nothrow) moe_plan;
+  if (!p) return nullptr;
+  memset(p, 0, sizeof(*p));
+  p->T = T; p->d = d; p->I = I; p->E = E; p->k = k; p->precision = precision;
+  p->R = T * k;
+  p->RP = (int)(((long long)p->R + (long long)E * (kBM - 1)) / kBM * kBM);
+  p->nblk = (p->R + 1023) / 1024;
+  p->bn13 = I % 128 == 0 ? 256 : 128;
+  p->bn2 = pick_bn_n(d) == 64 ? 128 : pick_bn_n(d);
+  p->bnd2 = pick_bn_n(I);
+  p->bnw2 = pick_bn_n(I);
+  p->bnw13 = p->bn2;
+  int dev = 0;
+  p->num_sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+      p->num_sms = n;
+  }
+  return p;
+}
+
+void moe_plan_destroy(moe_plan* p) { delete p; }
+
+int moe_plan_set_swiglu_clamp(moe_plan* p, float limit) {
+  if (!p || !(limit >= 0.f)) return MOE_ERR_INVALID_ARG;
+  p->clamp = limit;
+  return MOE_OK;
+}
+
+size_t moe_plan_workspace_bytes(const moe_plan* p, int flags) {
+  if (!p) return 0;
+  moe_plan tmp = *p;
+  return layout(&tmp, nullptr, flags);
+}
+
+int moe_plan_set_workspace(moe_plan* p, void* ws, size_t bytes, int flags) {
+  if (!p || !ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return MOE_ERR_INVALID_ARG;
+  if (bytes < moe_plan_workspace_bytes(p, flags)) return MOE_ERR_WORKSPACE;
+  p->ws = static_cast<char*>(ws);
+  p->ws_bytes = bytes;
+  p->ws_flags = flags;
+  layout(p, p->ws, flags);
+  p->saved = 0;
+  p->w13_cached = p->w2_cached = nullptr;
+  const long long RP = p->RP;
+  if (encode_tmap_bf16(&p->tm_xe, p->xe, RP, p->d) || encode_tmap_bf16(&p->tm_h, p->h, RP, p->I))
+    return MOE_ERR_CUDA;
+  if (flags & MOE_WS_TRAINING) {
+    if (encode_tmap_bf16(&p->tm_dye, p->dye, RP, p->d) ||
+        encode_tmap_bf16(&p->tm_dA, p->dA, RP, 2LL * p->I) ||
+        encode_tmap_bf16(&p->tm_hs, p->hs, RP, p->I))
+      return MOE_ERR_CUDA;
+  }
+  return reset_error_word(p->err);
+}
+
+int moe_forward(moe_plan* p, const void* x, const int32_t* ids, const float* scores,
+                const void* w13, const void* w2, const uint8_t* w13_sf, const uint8_t* w2_sf,
+                void* y, int save_for_backward, void* stream_v) {
+  if (!p || !x || !ids || !scores || !w13 || !w2 || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w13) || !aligned16(w2) || !aligned16(y))
+    return MOE_ERR_INVALID_ARG;
+  if (!p->ws) return MOE_ERR_WORKSPACE;
+  if (save_for_backward && !(p->ws_flags & MOE_WS_TRAINING)) return MOE_ERR_WORKSPACE;
+  if (p->precision != MOE_PREC_BF16) return MOE_ERR_UNSUPPORTED;
+  (void)w13_sf;
+  (void)w2_sf;
+  cudaStream_t st = static_cast<cudaStream_t>(stream_v);
+  if (refresh_weight_maps(p, w13, w2) != MOE_OK) return MOE_ERR_CUDA;
+
+  mark(p, 0, 0, st);
+  // a1-a3: dispatch
+  RouteArgs ra;
+  ra.ids = ids; ra.scores = scores;
+  ra.T = p->T; ra.k = p->k; ra.E = p->E; ra.BM = kBM; ra.nblk = p->nblk;
+  ra.blockcounts = p->blockcounts; ra.counts = p->counts; ra.m_indptr = p->m_indptr;
+  ra.off_pad = p->off_pad; ra.num_mtiles = p->num_mtiles; ra.tile_expert = p->tile_expert;
+  ra.expert_order = p->expert_order; ra.num_nonempty = p->num_nonempty;
+  ra.row_of = p->row_of; ra.token_of = p->token_of; ra.score_of = p->score_of; ra.err = p->err;
+  cudaError_t e = launch_route(ra, st);
+  if (e != cudaSuccess) return cuda_status(e);
+  p->launches += 3;
+  mark(p, 0, 1, st);
+  // a4: gather x rows into expert-major order
+  e = launch_gather_rows(x, p->token_of, p->off_pad + p->E, p->d, p->xe, gather_grid(p), st);
+  if (e != cudaSuccess) return cuda_status(e);
+  p->launches += 1;
+  mark(p, 0, 2, st);
+  // a5: W13 GEMM + SwiGLU
+  {
+    GemmArgs g = rows_args(p);
+    g.k_blocks = p->d / kBK;
+    g.b_expert_rows = 2 * p->I;
+    g.b_half_rows = p->I;
+    g.n_tiles = p->I / (p->bn13 / 2);
+    g.out0 = p->h; g.ld0 = p->I;
+    g.out1 = p->a; g.ld1 = 2LL * p->I;
+    g.save = save_for_backward ? 1 : 0;
+    e = launch_gemm(EPI_SWIGLU, p->bn13, false, false, p->tm_xe, p->tm_w13, g, p->num_sms, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    p->launches += 1;
+    mark(p, 0, 3, st);
+  }
+  // a6: W2 GEMM x score
+  {
+    GemmArgs g = rows_args(p);
+    g.k_blocks = p->I / kBK;
+    g.b_expert_rows = p->d;
+    g.n_tiles = p->d / p->bn2;
+    g.out0 = p->ys; g.ld0 = p->d;
+    g.row_scale = p->score_of;
+    e = launch_gemm(EPI_SCORE, p->bn2, false, false, p->tm_h, p->tm_w2, g, p->num_sms, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    p->launches += 1;
+    mark(p, 0, 4, st);
+  }
+  // a7: combine
+  e = launch_combine(p->ys, p->row_of, p->T, p->k, p->d, y, nullptr, 0, nullptr, gather_grid(p), st);
+  if (e != cudaSuccess) return cuda_status(e);
+  p->launches += 1;
+  mark(p, 0, 5, st);
+  p->saved = save_for_backward ? 1 : 0;
+  return MOE_OK;
+}
+
+int moe_backward(moe_plan* p, const void* dy, const void* w13, const void* w2, void* dx,
+                 float* dw13, float* dw2, float* dscores, void* stream_v) {
+  if (!p || !dy || !w13 || !w2 || !dx || !dw13 || !dw2 || !dscores) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(dy) || !aligned16(w13) || !aligned16(w2) || !aligned16(dx) || !aligned16(dw13) ||
+      !aligned16(dw2))
+    return MOE_ERR_INVALID_ARG;
+  if (p->precision != MOE_PREC_BF16) return MOE_ERR_UNSUPPORTED;
+  if (!p->ws || !(p->ws_flags & MOE_WS_TRAINING)) return MOE_ERR_WORKSPACE;
+  if (!p->saved) return MOE_ERR_STATE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream_v);
+  if (refresh_weight_maps(p, w13, w2) != MOE_OK) return MOE_ERR_CUDA;
+  const int I = p->I, d = p->d;
+  mark(p, 1, 0, st);
+  // b1: gather dY rows
+  cudaError_t e = launch_gather_rows(dy, p->token_of, p->off_pad + p->E, d, p->dye, gather_grid(p), st);
+  if (e != cudaSuccess) return cuda_status(e);
+  p->launches += 1;
+  mark(p, 1, 1, st);
+  // b2: g = dY_e . W2_e, SwiGLU backward, hs, score-grad partials
+  {
+    GemmArgs g = rows_args(p);
+    g.k_blocks = d / kBK;
+    g.b_expert_rows = d;
+    g.n_tiles = I / p->bnd2;
+    g.in0 = p->h; g.ldi0 = I;
+    g.in1 = p->a; g.ldi1 = 2LL * I;
+    g.out0 = p->dA; g.ld0 = 2LL * I;
+    g.out1 = p->hs; g.ld1 = I;
+    g.row_scale = p->score_of;
+    g.pdscore = p->pdscore;
+    e = launch_gemm(EPI_DGRAD2, p->bnd2, false, true, p->tm_dye, p->tm_w2, g, p->num_sms, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    p->launches += 1;
+    mark(p, 1, 2, st);
+  }
+  // b3: dX_e = dA . W13_e
+  {
+    GemmArgs g = rows_args(p);
+    g.k_blocks = 2 * I / kBK;
+    g.b_expert_rows = 2 * I;
+    g.n_tiles = d / p->bn2;
+    g.out0 = p->dxe; g.ld0 = d;
+    e = launch_gemm(EPI_STORE, p->bn2, false, true, p->tm_dA, p->tm_w13, g, p->num_sms, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    p->launches += 1;
+    mark(p, 1, 3, st);
+  }
+  // b4: combine dX and dscores
+  e = launch_combine(p->dxe, p->row_of, p->T, p->k, d, dx, p->pdscore, I / p->bnd2, dscores,
+                     gather_grid(p), st);
+  if (e != cudaSuccess) return cuda_status(e);
+  p->launches += 1;
+  mark(p, 1, 4, st);
+  // b5: dW2[e] += dY_e^T . hs_e
+  {
+    GemmArgs g = wgrad_args(p);
+    g.m_tiles = d / kBM;
+    g.n_tiles = I / p->bnw2;
+    g.out0 = dw2; g.ld0 = I;
+    g.out_expert_stride = (long long)d * I;
+    e = launch_gemm(EPI_WGRAD, p->bnw2, true, true, p->tm_dye, p->tm_hs, g, p->num_sms, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    p->launches += 1;
+    mark(p, 1, 5, st);
+  }
+  // b6: dW13[e] += dA_e^T . x_e
+  {
+    GemmArgs g = wgrad_args(p);
+    g.m_tiles = 2 * I / kBM;
+    g.n_tiles = d / p->bnw13;
+    g.out0 = dw13; g.ld0 = d;
+    g.out_expert_stride = 2LL * I * d;
+    e = launch_gemm(EPI_WGRAD, p->bnw13, true, true, p->tm_dA, p->tm_xe, g, p->num_sms, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    p->launches += 1;
+    mark(p, 1, 6, st);
+  }
+  return MOE_OK;
+}
+
+int moe_step_host(moe_plan* p, const void* x_host, const int32_t* ids_host,
+                  const float* scores_host, const void* dy_host, const void* w13, const void* w2,
+                  float* dw13, float* dw2, void* y_host, void* dx_host, float* dscores_host,
+                  void* stream_v) {
+  if (!p || !x_host || !ids_host || !scores_host || !y_host) return MOE_ERR_INVALID_ARG;
+  if (!p->ws || !(p->ws_flags & MOE_WS_HOST_STAGING)) return MOE_ERR_WORKSPACE;
+  const bool train = dy_host != nullptr;
+  if (train && (!(p->ws_flags & MOE_WS_TRAINING) || !dx_host || !dscores_host))
+    return train && !(p->ws_flags & MOE_WS_TRAINING) ? MOE_ERR_WORKSPACE : MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream_v);
+  const size_t xb = 2ull * p->T * p->d, sb = 4ull * p->T * p->k;
+  cudaError_t e;
+  if ((e = cudaMemcpyAsync(p->st_x, x_host, xb, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(p->st_ids, ids_host, sb, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(p->st_scores, scores_host, sb, cudaMemcpyHostToDevice, st)) != cudaSuccess)
+    return cuda_status(e);
+  if (train && (e = cudaMemcpyAsync(p->st_dy, dy_host, xb, cudaMemcpyHostToDevice, st)) != cudaSuccess)
+    return cuda_status(e);
+  int rc = moe_forward(p, p->st_x, p->st_ids, p->st_scores, w13, w2, nullptr, nullptr, p->st_y,
+                       train ? 1 : 0, stream_v);
+  if (rc != MOE_OK) return rc;
+  if (train) {
+    rc = moe_backward(p, p->st_dy, w13, w2, p->st_dx, dw13, dw2, p->st_dscores, stream_v);
+    if (rc != MOE_OK) return rc;
+  }
+  if ((e = cudaMemcpyAsync(y_host, p->st_y, xb, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
+    return cuda_status(e);
+  if (train) {
+    if ((e = cudaMemcpyAsync(dx_host, p->st_dx, xb, cudaMemcpyDeviceToHost, st)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(dscores_host, p->st_dscores, sb, cudaMemcpyDeviceToHost, st)) !=
+            cudaSuccess)
+      return cuda_status(e);
+  }
+  return MOE_OK;
+}
+
+int moe_quantize_mxfp8(const void* in, long rows, int K, uint8_t* codes, uint8_t* scales,
+                       void* stream) {
+  if (!in || !codes || !scales || rows < 0 || K <= 0 || K % 32 || !aligned16(in) ||
+      !aligned16(codes))
+    return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  return cuda_status(launch_quant_mxfp8(in, rows, K, codes, scales, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_plan_set_timing_events(moe_plan* p, int which, void* const* events, int n) {
+  if (!p || which < 0 || which > 1 || n < 0) return MOE_ERR_INVALID_ARG;
+  if (n > 0 && events && n < (which == 0 ? 6 : 7)) return MOE_ERR_INVALID_ARG;
+  p->ev[which] = n > 0 ? events : nullptr;
+  p->nev[which] = events ? n : 0;
+  return MOE_OK;
+}
+
+long long moe_plan_launch_count(const moe_plan* p) { return p ? p->launches : 0; }
+
+int moe_plan_check(moe_plan* p, long long* detail) {
+  if (!p || !p->ws) return MOE_ERR_INVALID_ARG;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_status(e);
+  DevError h;
+  e = cudaMemcpy(&h, p->err, sizeof(h), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_status(e);
+  int rc = reset_error_word(p->err);
+  if (rc != MOE_OK) return rc;
+  if (detail) *detail = h.code == MOE_ERR_BAD_IDS ? (long long)h.first_bad : (long long)h.where;
+  return h.code;
+}
+
+int moe_plan_buffer(const moe_plan* p, int which, void** ptr, size_t* bytes) {
+  if (!p || !p->ws || !ptr) return MOE_ERR_INVALID_ARG;
+  const size_t RP = p->RP, d = p->d, I = p->I, E = p->E;
+  void* q = nullptr;
+  size_t b = 0;
+  switch (which) {
+    case MOE_BUF_M_INDPTR: q = p->m_indptr; b = 4 * (E + 1); break;
+    case MOE_BUF_OFF_PAD: q = p->off_pad; b = 4 * (E + 1); break;
+    case MOE_BUF_ROW_OF: q = p->row_of; b = 4 * (size_t)p->R; break;
+    case MOE_BUF_TOKEN_OF: q = p->token_of; b = 4 * RP; break;
+    case MOE_BUF_SCORE_OF: q = p->score_of; b = 4 * RP; break;
+    case MOE_BUF_XE: q = p->xe; b = 2 * RP * d; break;
+    case MOE_BUF_A: q = p->a; b = 2 * RP * 2 * I; break;
+    case MOE_BUF_H: q = p->h; b = 2 * RP * I; break;
+    case MOE_BUF_YS: q = p->ys; b = 2 * RP * d; break;
+    case MOE_BUF_DYE: q = p->dye; b = 2 * RP * d; break;
+    case MOE_BUF_DA: q = p->dA; b = 2 * RP * 2 * I; break;
+    case MOE_BUF_HS: q = p->hs; b = 2 * RP * I; break;
+    case MOE_BUF_DXE: q = p->dxe; b = 2 * RP * d; break;
+    default: return MOE_ERR_INVALID_ARG;
+  }
+  if (!q) return MOE_ERR_WORKSPACE;
+  *ptr = q;
+  if (bytes) *bytes = b;
+  return MOE_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// dense GEMM entry point (tests): runs the grouped kernels with one "expert"
+
+namespace {
+
+__global__ void k_dense_meta(int* s, int mtiles, int K) {
+  // s[0] num_mtiles, s[1] num_nonempty, s[2..3] off_pad, s[4] expert_order
+  s[0] = mtiles;
+  s[1] = 1;
+  s[2] = 0;
+  s[3] = K;
+  s[4] = 0;
+}
+
+}  // namespace
+
+extern "C" size_t moe_gemm_scratch_bytes(int M, int K) {
+  (void)M;
+  (void)K;
+  return 256;
+}
+
+extern "C" int moe_gemm_bf16(int mode, const void* A, const void* B, void* C, int M, int N, int K,
+                             void* scratch, void* stream_v) {
+  if (!A || !B || !C || !scratch || M <= 0 || N <= 0 || K <= 0) return MOE_ERR_INVALID_ARG;
+  if (M % 128 || N % 64 || K % 64 || (mode == 2 && K % 128)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream_v);
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int* s = static_cast<int*>(scratch);
+  k_dense_meta<<<1, 1, 0, st>>>(s, M / 128, K);
+  CUtensorMap ta, tb;
+  GemmArgs g;
+  memset(&g, 0, sizeof(g));
+  const int bn = pick_bn_n(N);
+  g.n_tiles = N / bn;
+  g.out0 = C;
+  g.ld0 = N;
+  cudaError_t e;
+  if (mode == 0 || mode == 1) {
+    if (encode_tmap_bf16(&ta, A, M, K)) return MOE_ERR_CUDA;
+    if (mode == 0 ? encode_tmap_bf16(&tb, B, N, K) : encode_tmap_bf16(&tb, B, K, N))
+      return MOE_ERR_CUDA;
+    g.wgrad = 0;
+    g.num_mtiles = s;
+    g.tile_expert = nullptr;
+    g.k_blocks = K / kBK;
+    g.b_expert_rows = mode == 0 ? N : K;
+    e = launch_gemm(EPI_STORE, bn, false, mode == 1, ta, tb, g, sms, st);
+  } else if (mode == 2) {
+    if (encode_tmap_bf16(&ta, A, K, M) || encode_tmap_bf16(&tb, B, K, N)) return MOE_ERR_CUDA;
+    g.wgrad = 1;
+    g.num_nonempty = s + 1;
+    g.off_pad = s + 2;
+    g.expert_order = s + 4;
+    g.m_tiles = M / kBM;
+    g.out_expert_stride = 0;
+    e = launch_gemm(EPI_WGRAD, bn, true, true, ta, tb, g, sms, st);
+  } else {
+    return MOE_ERR_INVALID_ARG;
+  }
+  return cuda_status(e);
+}

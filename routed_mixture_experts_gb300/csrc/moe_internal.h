@@ -1,0 +1,103 @@
+// moe_internal.h -- host-side declarations shared by the library's translation
+// units (kernel launchers and their argument blocks).  Not part of the C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+struct DevError;
+
+constexpr int kBM = 128;  // rows per GEMM tile = padding granule of an expert segment
+constexpr int kBK = 64;   // K per pipeline stage (one 128-byte swizzle atom of bf16)
+
+// Epilogue kinds of the grouped GEMM.
+enum Epi : int {
+  EPI_SWIGLU = 0,  // W13 FPROP: a = bf16(acc) (saved when training), h = bf16(swiglu(a))
+  EPI_SCORE = 1,   // W2 FPROP: ys = bf16(score * acc)
+  EPI_DGRAD2 = 2,  // g = dY_e . W2_e: dscore partials, SwiGLU backward -> dA, hs = bf16(s*h)
+  EPI_STORE = 3,   // plain bf16 store (DGRAD through W13)
+  EPI_WGRAD = 4,   // fp32 read-modify-write accumulate (weight gradients)
+};
+
+// Arguments of one grouped-GEMM launch.  Two tile spaces:
+//  rows mode  (wgrad == 0): output rows are routed rows; m tile mt covers padded rows
+//             [mt*128, mt*128+128) of expert tile_expert[mt]; K loop over k_blocks.
+//  wgrad mode (wgrad == 1): output is a per-expert weight gradient [M, N]; the K
+//             loop runs over the expert's padded row segment [off_pad[e], off_pad[e+1]).
+struct GemmArgs {
+  int wgrad;
+  // rows mode
+  const int* num_mtiles;     // device scalar
+  const int* tile_expert;    // device [max m tiles]; nullptr: every tile is expert 0
+  int k_blocks;
+  int b_expert_rows;         // rows of B's 2-D tensor map per expert
+  int b_half_rows;           // EPI_SWIGLU: row offset of the up half (I)
+  // wgrad mode
+  const int* off_pad;        // device [E+1]
+  const int* expert_order;   // device [E]: experts with rows first, longest first
+  const int* num_nonempty;   // device scalar
+  int m_tiles;               // M / 128
+  long long out_expert_stride;
+  // both
+  int n_tiles;               // N / BN
+  // epilogue operands
+  void* out0;  long long ld0;
+  void* out1;  long long ld1;
+  const void* in0; long long ldi0;
+  const void* in1; long long ldi1;
+  const float* row_scale;    // score of each padded row
+  float* pdscore;            // EPI_DGRAD2: [rows, n_tiles]
+  float clamp;               // SwiGLU limit (0 = plain)
+  int I;                     // column offset of the up half in a / dA
+  int save;                  // EPI_SWIGLU: store a
+  DevError* err;
+};
+
+// Encode a 2-D bf16 tensor map (row-major [rows, cols]) with a 64 x 64 box and
+// 128-byte swizzle, the only box shape the GEMM kernels load.
+int encode_tmap_bf16(CUtensorMap* map, const void* base, long long rows, long long cols);
+
+// Launch the grouped GEMM.  a_mn / b_mn select MN-major operands.
+cudaError_t launch_gemm(int epi, int bn, bool a_mn, bool b_mn, const CUtensorMap& ta,
+                        const CUtensorMap& tb, const GemmArgs& args, int grid,
+                        cudaStream_t stream);
+
+// Dispatch kernels.
+struct RouteArgs {
+  const int32_t* ids;
+  const float* scores;
+  int T, k, E, BM;
+  int nblk;                  // ceil(T*k / 1024)
+  int32_t* blockcounts;      // [nblk, E]
+  int32_t* counts;           // [E]
+  int32_t* m_indptr;         // [E+1]
+  int32_t* off_pad;          // [E+1]
+  int32_t* num_mtiles;       // scalar
+  int32_t* tile_expert;      // [max m tiles]
+  int32_t* expert_order;     // [E]
+  int32_t* num_nonempty;     // scalar
+  int32_t* row_of;           // [T*k]
+  int32_t* token_of;         // [Rpad max]
+  float* score_of;           // [Rpad max]
+  DevError* err;
+};
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t stream);
+
+// rows r < *nrows of dst[r] = src[token_of[r]] (zero where token_of[r] < 0).
+cudaError_t launch_gather_rows(const void* src, const int32_t* token_of, const int32_t* nrows,
+                               int d, void* dst, int grid, cudaStream_t stream);
+
+// y[t] = bf16(sum_j rows[row_of[t,j]]) in j order; optionally dscores[t,j] =
+// sum_nt pdscore[row_of[t,j], nt] in nt order (0 where row_of < 0).
+cudaError_t launch_combine(const void* rows, const int32_t* row_of, int T, int k, int d,
+                           void* y, const float* pdscore, int n_pd, float* dscores, int grid,
+                           cudaStream_t stream);
+
+cudaError_t launch_quant_mxfp8(const void* in, long long rows, int K, uint8_t* codes,
+                               uint8_t* scales, cudaStream_t stream);
+
+}  // namespace moe

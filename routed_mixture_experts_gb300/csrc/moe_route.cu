@@ -1,0 +1,288 @@
+// moe_route.cu -- expert-major dispatch, row gather and deterministic combine.
+//
+// Dispatch ("Dist-MoE" note, "What it is selling": route on GPU; nvfp4moe README,
+// "Grouped GEMM": contiguous expert-major rows and m_indptr of length E+1 with
+// empty experts valid; "MoE layer"/"Training": deterministic permutation and
+// combine metadata, padded offsets) is a stable counting sort of the T*k routed
+// elements by expert, in three launches:
+//   1. k_route_count    per 1024-element chunk: validate ids, per-expert histogram
+//   2. k_route_scan     one CTA: per-expert scan over chunks, warp-shuffle prefix
+//                       scan over experts into m_indptr / off_pad, m-tile table,
+//                       padding rows, expert order for weight-gradient scheduling
+//   3. k_route_scatter  per chunk: stable rank of each element among equal experts
+//                       (warp match + per-warp counts), write row_of / token_of /
+//                       score_of
+// Padded row layout: expert e owns rows [off_pad[e], off_pad[e+1]), its segment
+// rounded up to the 128-row GEMM tile so no tile straddles two experts.
+//
+// Gather and combine are HBM-bound row copies with 16-byte vector accesses, one
+// warp per row (gather) or per token (combine); the combine sums each token's k
+// rows in fixed j order in fp32 ("MoE layer": deterministic combine).
+
+#include <climits>
+
+#include "moe_device.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kChunk = 1024;   // routed elements per dispatch CTA
+constexpr int kMaxE = 256;
+
+__device__ __forceinline__ bool element_valid(const int32_t* ids, int f, int k, int E, int* e_out) {
+  const int t = f / k;
+  const int j = f - t * k;
+  const int e = ids[f];
+  *e_out = e;
+  if (e < 0 || e >= E) return false;
+  for (int jj = 0; jj < j; ++jj)
+    if (ids[t * k + jj] == e) return false;
+  return true;
+}
+
+__global__ void __launch_bounds__(kChunk) k_route_count(RouteArgs a) {
+  __shared__ int hist[kMaxE];
+  for (int i = threadIdx.x; i < a.E; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  const int R = a.T * a.k;
+  const int f = blockIdx.x * kChunk + threadIdx.x;
+  if (f < R) {
+    int e;
+    if (element_valid(a.ids, f, a.k, a.E, &e)) {
+      atomicAdd(&hist[e], 1);
+    } else {
+      atomicMin(&a.err->first_bad, f);
+      atomicCAS(&a.err->code, 0, 4 /*MOE_ERR_BAD_IDS*/);
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < a.E; i += blockDim.x) a.blockcounts[blockIdx.x * a.E + i] = hist[i];
+}
+
+// Inclusive warp scan with shuffles.
+__device__ __forceinline__ int warp_incl_scan(int v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  return v;
+}
+
+__global__ void __launch_bounds__(kMaxE) k_route_scan(RouteArgs a) {
+  __shared__ int cnt[kMaxE];
+  __shared__ int warp_tot[2][kMaxE / 32];
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int E = a.E;
+  // 1. per expert: exclusive scan of the chunk histograms -> chunk bases
+  int c = 0;
+  if (tid < E) {
+    for (int b = 0; b < a.nblk; ++b) {
+      const int v = a.blockcounts[b * E + tid];
+      a.blockcounts[b * E + tid] = c;
+      c += v;
+    }
+    a.counts[tid] = c;
+  }
+  cnt[tid] = tid < E ? c : 0;
+  // 2. warp-level prefix scans over experts: exact counts and padded counts
+  const int p = tid < E ? (c + a.BM - 1) / a.BM * a.BM : 0;
+  const int ic = warp_incl_scan(tid < E ? c : 0, lane);
+  const int ip = warp_incl_scan(p, lane);
+  if (lane == 31) {
+    warp_tot[0][warp] = ic;
+    warp_tot[1][warp] = ip;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x / 32;
+    int t0 = lane < nw ? warp_tot[0][lane] : 0;
+    int t1 = lane < nw ? warp_tot[1][lane] : 0;
+    const int s0 = warp_incl_scan(t0, lane), s1 = warp_incl_scan(t1, lane);
+    if (lane < nw) {
+      warp_tot[0][lane] = s0 - t0;   // exclusive warp bases
+      warp_tot[1][lane] = s1 - t1;
+    }
+  }
+  __syncthreads();
+  const int ec = warp_tot[0][warp] + ic - (tid < E ? c : 0);
+  const int ep = warp_tot[1][warp] + ip - p;
+  if (tid < E) {
+    a.m_indptr[tid] = ec;
+    a.off_pad[tid] = ep;
+    if (tid == E - 1) {
+      a.m_indptr[E] = ec + c;
+      a.off_pad[E] = ep + p;
+      *a.num_mtiles = (ep + p) / a.BM;
+    }
+  }
+  __syncthreads();
+  if (tid < E) {
+    // m tiles of this expert, and its padding rows
+    for (int r = ep; r < ep + p; r += a.BM) a.tile_expert[r / a.BM] = tid;
+    for (int r = ep + c; r < ep + p; ++r) {
+      a.token_of[r] = -1;
+      a.score_of[r] = 0.f;
+    }
+    // order for weight-gradient tiles: experts with more rows first (ties: lower id)
+    int pos = 0;
+    for (int e2 = 0; e2 < E; ++e2) {
+      const int c2 = cnt[e2];
+      pos += (c2 > c) || (c2 == c && e2 < tid);
+    }
+    a.expert_order[pos] = tid;
+  }
+  if (tid == 0) {
+    int ne = 0;
+    for (int e2 = 0; e2 < E; ++e2) ne += cnt[e2] > 0;
+    *a.num_nonempty = ne;
+  }
+}
+
+__global__ void __launch_bounds__(kChunk) k_route_scatter(RouteArgs a) {
+  __shared__ int wcnt[kChunk / 32][kMaxE];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int E = a.E;
+  for (int i = tid; i < (kChunk / 32) * E; i += kChunk) wcnt[i / E][i % E] = 0;
+  __syncthreads();
+  const int R = a.T * a.k;
+  const int f = blockIdx.x * kChunk + tid;
+  int e = -1;
+  bool valid = false;
+  if (f < R) valid = element_valid(a.ids, f, a.k, E, &e);
+  const int key = valid ? e : -1;
+  const unsigned peers = __match_any_sync(0xffffffffu, key);
+  const int rank_w = __popc(peers & ((1u << lane) - 1u));
+  if (valid && lane == __ffs(peers) - 1) wcnt[warp][e] = __popc(peers);
+  __syncthreads();
+  if (valid) {
+    int base = 0;
+    for (int w = 0; w < warp; ++w) base += wcnt[w][e];
+    const int pos = a.off_pad[e] + a.blockcounts[blockIdx.x * E + e] + base + rank_w;
+    a.row_of[f] = pos;
+    a.token_of[pos] = f / a.k;
+    a.score_of[pos] = a.scores[f];
+  } else if (f < R) {
+    a.row_of[f] = -1;
+  }
+}
+
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(256) k_gather_rows(const uint4* __restrict__ src,
+                                                     const int32_t* __restrict__ token_of,
+                                                     const int32_t* __restrict__ nrows_p, int nvec,
+                                                     uint4* __restrict__ dst) {
+  const int nrows = *nrows_p;
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  for (int r = gw; r < nrows; r += nw) {
+    const int t = token_of[r];
+    const uint4* s = src + (long long)(t < 0 ? 0 : t) * nvec;
+    uint4* o = dst + (long long)r * nvec;
+    for (int v0 = 0; v0 < nvec; v0 += 32 * 8) {
+      uint4 buf[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int v = v0 + lane + 32 * u;
+        buf[u] = (t >= 0 && v < nvec) ? s[v] : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int v = v0 + lane + 32 * u;
+        if (v < nvec) o[v] = buf[u];
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void acc8(float* acc, const uint4 v) {
+  acc[0] += __uint_as_float(v.x << 16); acc[1] += __uint_as_float(v.x & 0xFFFF0000u);
+  acc[2] += __uint_as_float(v.y << 16); acc[3] += __uint_as_float(v.y & 0xFFFF0000u);
+  acc[4] += __uint_as_float(v.z << 16); acc[5] += __uint_as_float(v.z & 0xFFFF0000u);
+  acc[6] += __uint_as_float(v.w << 16); acc[7] += __uint_as_float(v.w & 0xFFFF0000u);
+}
+
+__global__ void __launch_bounds__(256) k_combine(const uint4* __restrict__ rows,
+                                                 const int32_t* __restrict__ row_of, int T, int k,
+                                                 int nvec, uint4* __restrict__ y,
+                                                 const float* __restrict__ pdscore, int n_pd,
+                                                 float* __restrict__ dscores) {
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  constexpr int U = 4;   // 16-byte vectors per lane per pass
+  for (int t = gw; t < T; t += nw) {
+    for (int v0 = 0; v0 < nvec; v0 += 32 * U) {
+      float acc[U][8];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[u][q] = 0.f;
+      for (int j = 0; j < k; ++j) {
+        const int r = row_of[t * k + j];
+        if (r < 0) continue;
+        const uint4* src = rows + (long long)r * nvec;
+        uint4 buf[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int v = v0 + lane + 32 * u;
+          buf[u] = v < nvec ? src[v] : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) acc8(acc[u], buf[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + lane + 32 * u;
+        if (v < nvec) {
+          uint4 o;
+          o.x = pack_bf2(acc[u][0], acc[u][1]);
+          o.y = pack_bf2(acc[u][2], acc[u][3]);
+          o.z = pack_bf2(acc[u][4], acc[u][5]);
+          o.w = pack_bf2(acc[u][6], acc[u][7]);
+          y[(long long)t * nvec + v] = o;
+        }
+      }
+    }
+    if (dscores) {
+      for (int j = lane; j < k; j += 32) {
+        const int r = row_of[t * k + j];
+        float s = 0.f;
+        if (r >= 0)
+          for (int nt = 0; nt < n_pd; ++nt) s += pdscore[(long long)r * n_pd + nt];
+        dscores[t * k + j] = s;
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t stream) {
+  k_route_count<<<a.nblk, kChunk, 0, stream>>>(a);
+  k_route_scan<<<1, kMaxE, 0, stream>>>(a);
+  k_route_scatter<<<a.nblk, kChunk, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const void* src, const int32_t* token_of, const int32_t* nrows,
+                               int d, void* dst, int grid, cudaStream_t stream) {
+  k_gather_rows<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(src), token_of, nrows, d / 8,
+                                          static_cast<uint4*>(dst));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const void* rows, const int32_t* row_of, int T, int k, int d, void* y,
+                           const float* pdscore, int n_pd, float* dscores, int grid,
+                           cudaStream_t stream) {
+  k_combine<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(rows), row_of, T, k, d / 8,
+                                      static_cast<uint4*>(y), pdscore, n_pd, dscores);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,121 @@
+"""Runs one routed-expert case through the C ABI and through the oracle, and
+compares them (shared by the GPU parity tests and the smoke check)."""
+
+import numpy as np
+import torch
+
+import moe_inputs as mi
+from parity import REL_FRO, compare, f32, term_flips
+
+
+def to_dev(inp):
+    dev = {}
+    for key, v in inp.items():
+        if key == "cfg":
+            continue
+        t = torch.from_numpy(np.ascontiguousarray(v))
+        if v.dtype == np.uint16:
+            t = t.view(torch.bfloat16)
+        dev[key] = t.cuda()
+    return dev
+
+
+def run_gpu(moe, inp, train=True, stream=None):
+    c = inp["cfg"]
+    dev = to_dev(inp)
+    plan = moe.MoePlan(c["T"], c["d"], c["I"], c["E"], c["k"], clamp=c.get("clamp", 0.0),
+                       flags=moe.MOE_WS_TRAINING if train else 0)
+    out = {"plan": plan, "dev": dev}
+    out["y"] = plan.forward(dev["x"], dev["ids"], dev["scores"], dev["w13"], dev["w2"], save=train)
+    if train:
+        dw13, dw2 = dev["dw13"].clone(), dev["dw2"].clone()
+        dx, ds = plan.backward(dev["dy"], dev["w13"], dev["w2"], dw13, dw2)
+        out.update(dx=dx, dscores=ds, dw13=dw13, dw2=dw2)
+    torch.cuda.synchronize()
+    rc, detail = plan.check()
+    out["rc"], out["detail"] = rc, detail
+    return out
+
+
+def bits(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def check_dispatch(orc, inp, g, BM=128):
+    """Dispatch tables: bit-exact against the oracle's stable counting sort."""
+    c = inp["cfg"]
+    r = orc.dispatch(inp["ids"], c["E"], BM)
+    plan = g["plan"]
+    mi_ = plan.buffer("m_indptr", torch.int32).cpu().numpy()
+    op = plan.buffer("off_pad", torch.int32).cpu().numpy()
+    ro = plan.buffer("row_of", torch.int32).cpu().numpy()[: c["T"] * c["k"]].reshape(c["T"], c["k"])
+    assert np.array_equal(mi_, r["m_indptr"])
+    assert np.array_equal(op, r["off_pad"])
+    assert np.array_equal(ro, r["row_of"])
+    return r
+
+
+def check_forward(orc, inp, g, toks=None, intermediates=True):
+    c = inp["cfg"]
+    y_ref, it = orc.forward(inp["x"], inp["ids"], inp["scores"], inp["w13"], inp["w2"],
+                            clamp=c.get("clamp", 0.0), toks=toks, intermediates=True)
+    y = bits(g["y"])
+    sel = slice(None) if toks is None else np.asarray(toks)
+    compare(f32(y[sel]), f32(y_ref), what="y", flip=term_flips(it["ys"]))
+    if intermediates:
+        plan = g["plan"]
+        ro = plan.buffer("row_of", torch.int32).cpu().numpy()[: c["T"] * c["k"]].reshape(c["T"], c["k"])
+        rows = ro[sel]
+        ok = rows >= 0
+        I, d = c["I"], c["d"]
+        h = bits(plan.buffer("h", torch.bfloat16).view(-1, I))
+        ys = bits(plan.buffer("ys", torch.bfloat16).view(-1, d))
+        compare(f32(h[rows[ok]]), f32(it["h"][ok]), what="h", max_bad_frac=1e-3)
+        compare(f32(ys[rows[ok]]), f32(it["ys"][ok]), what="ys", max_bad_frac=1e-3)
+        if c.get("train", True) and plan.flags & 1:
+            a = bits(plan.buffer("a", torch.bfloat16).view(-1, 2 * I))
+            compare(f32(a[rows[ok]]), f32(it["a"][ok]), what="a", max_bad_frac=1e-3)
+    return y_ref
+
+
+def check_backward(orc, inp, g, toks=None, experts=None, intermediates=True):
+    c = inp["cfg"]
+    clamp = c.get("clamp", 0.0)
+    dx_ref, ds_ref, bi = orc.backward(inp["x"], inp["ids"], inp["scores"], inp["w13"], inp["w2"],
+                                      inp["dy"], clamp=clamp, toks=toks, intermediates=True)
+    sel = slice(None) if toks is None else np.asarray(toks)
+    compare(f32(bits(g["dx"])[sel]), f32(dx_ref), what="dx", flip=term_flips(bi["dxe"]))
+    compare(g["dscores"].cpu().numpy()[sel], ds_ref, bf16_out=False, what="dscores")
+    if intermediates:
+        plan = g["plan"]
+        ro = plan.buffer("row_of", torch.int32).cpu().numpy()[: c["T"] * c["k"]].reshape(c["T"], c["k"])
+        rows = ro[sel]
+        ok = rows >= 0
+        I = c["I"]
+        dA = bits(plan.buffer("dA", torch.bfloat16).view(-1, 2 * I))
+        hs = bits(plan.buffer("hs", torch.bfloat16).view(-1, I))
+        compare(f32(dA[rows[ok]]), f32(bi["dA"][ok]), what="dA", max_bad_frac=1e-3)
+        compare(f32(hs[rows[ok]]), f32(bi["hs"][ok]), what="hs", max_bad_frac=1e-3)
+    E = c["E"]
+    experts = range(E) if experts is None else experts
+    dw13 = g["dw13"]
+    dw2 = g["dw2"]
+    for e in experts:
+        d13, d2, nrows = orc.wgrad_expert(inp["x"], inp["ids"], inp["scores"], inp["w13"],
+                                          inp["w2"], inp["dy"], e, clamp=clamp)
+        got13 = (dw13[e].double() - g["dev"]["dw13"][e].double()).cpu().numpy()
+        got2 = (dw2[e].double() - g["dev"]["dw2"][e].double()).cpu().numpy()
+        if nrows == 0:
+            assert np.all(got13 == 0) and np.all(got2 == 0), "expert %d without rows changed" % e
+            continue
+        compare(got13, d13, bf16_out=False, what="dW13[%d]" % e)
+        compare(got2, d2, bf16_out=False, what="dW2[%d]" % e)
+
+
+def make(name=None, seed=0, train=True, **over):
+    need = ("x", "ids", "scores", "w13", "w2") + (("dy", "dw13", "dw2") if train else ())
+    return mi.make_inputs(name, seed=seed, need=need, **over)
+
+
+__all__ = ["make", "run_gpu", "check_dispatch", "check_forward", "check_backward", "bits",
+           "REL_FRO"]

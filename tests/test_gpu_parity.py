@@ -1,0 +1,158 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Dispatch tables and gathered rows: bit-exact.  Floating-point results: within
+the stated tolerance (tests/parity.py).  Small cases compare every output and
+every intermediate; they span several GEMM tiles, ragged expert segments, empty
+experts, padding tokens and the clamped SwiGLU.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+from gpu_case import bits, check_backward, check_dispatch, check_forward, make, run_gpu
+from parity import f32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from routed_mixture_experts_gb300 import build
+
+    build.build()
+    import routed_mixture_experts_gb300 as m
+
+    return m
+
+
+def test_tiny_forward(moe, orc):
+    inp = make("tiny_fwd", train=False)
+    g = run_gpu(moe, inp, train=False)
+    assert g["rc"] == 0
+    r = check_dispatch(orc, inp, g)
+    # gathered rows: bit-exact copies (padding rows zero)
+    c = inp["cfg"]
+    tok = g["plan"].buffer("token_of", torch.int32).cpu().numpy()[: r["off_pad"][-1]]
+    xe = bits(g["plan"].buffer("xe", torch.bfloat16).view(-1, c["d"]))[: r["off_pad"][-1]]
+    assert np.array_equal(xe, orc.gather_rows(inp["x"], tok))
+    check_forward(orc, inp, g)
+
+
+SMALL = [
+    # name, sizes, extra
+    ("tiny_train", dict(T=64, d=128, I=64, E=4, k=2), {}),
+    ("ragged", dict(T=300, d=256, I=192, E=7, k=3), {}),
+    ("wide", dict(T=517, d=384, I=128, E=16, k=4), {}),
+    ("clamped_pad", dict(T=200, d=256, I=128, E=9, k=2, clamp=1.0, pad=37), {}),
+    ("skew_empty", dict(T=400, d=128, I=256, E=12, k=3, routing="zipf", zipf_s=1.2,
+                        zipf_support=8), {}),
+    ("single_expert", dict(T=130, d=128, I=64, E=1, k=1), {}),
+    ("k8_e256", dict(T=96, d=128, I=64, E=256, k=8), {}),
+]
+
+
+@pytest.mark.parametrize("name,sizes,extra", SMALL, ids=[s[0] for s in SMALL])
+def test_small_forward_backward(moe, orc, name, sizes, extra):
+    inp = make(None, seed=len(name), train=True, **sizes)
+    g = run_gpu(moe, inp, train=True)
+    assert g["rc"] == 0, g
+    check_dispatch(orc, inp, g)
+    check_forward(orc, inp, g)
+    check_backward(orc, inp, g)
+
+
+def test_zero_score_padding_rows_are_zero(moe):
+    inp = make(None, seed=5, train=True, T=160, d=128, I=64, E=6, k=2, pad=40)
+    g = run_gpu(moe, inp, train=True)
+    y = f32(bits(g["y"]))
+    dx = f32(bits(g["dx"]))
+    assert np.all(y[-40:] == 0) and np.all(dx[-40:] == 0)
+    assert np.all(np.abs(g["dscores"].cpu().numpy()[-40:]) > 0)
+
+
+def test_forward_is_deterministic(moe):
+    inp = make(None, seed=6, train=True, T=300, d=256, I=128, E=8, k=4)
+    g1 = run_gpu(moe, inp, train=True)
+    g2 = run_gpu(moe, inp, train=True)
+    for key in ("y", "dx", "dscores", "dw13", "dw2"):
+        assert torch.equal(g1[key], g2[key]), key
+
+
+def test_weight_gradients_accumulate(moe):
+    """Running the backward twice adds the increment twice (in-place +=)."""
+    inp = make(None, seed=7, train=True, T=256, d=128, I=64, E=4, k=2)
+    g = run_gpu(moe, inp, train=True)
+    plan, dev = g["plan"], g["dev"]
+    d13_1 = g["dw13"].double() - dev["dw13"].double()
+    plan.backward(dev["dy"], dev["w13"], dev["w2"], g["dw13"], g["dw2"])
+    torch.cuda.synchronize()
+    d13_2 = g["dw13"].double() - dev["dw13"].double()
+    assert torch.allclose(d13_2, 2 * d13_1, rtol=1e-5, atol=1e-6)
+
+
+def test_bad_ids_are_reported(moe):
+    inp = make(None, seed=8, train=False, T=100, d=128, I=64, E=8, k=3)
+    ids = inp["ids"].copy()
+    ids[40, 2] = ids[40, 0]       # repeated id, flat index 122
+    ids[70, 1] = 8                # out of range, flat index 211
+    inp["ids"] = ids
+    g = run_gpu(moe, inp, train=False)
+    assert g["rc"] == moe.MOE_ERR_BAD_IDS
+    assert g["detail"] == 122
+    # the error word is cleared by the check
+    assert g["plan"].check() == (0, 0)
+
+
+def test_backward_needs_saving_forward(moe):
+    inp = make(None, seed=9, train=True, T=64, d=128, I=64, E=4, k=2)
+    dev = {k: v for k, v in __import__("gpu_case").to_dev(inp).items()}
+    plan = moe.MoePlan(64, 128, 64, 4, 2, flags=moe.MOE_WS_TRAINING)
+    with pytest.raises(moe.MoeError) as ei:
+        plan.backward(dev["dy"], dev["w13"], dev["w2"], dev["dw13"], dev["dw2"])
+    assert ei.value.code == moe.MOE_ERR_STATE
+    plan.forward(dev["x"], dev["ids"], dev["scores"], dev["w13"], dev["w2"], save=False)
+    with pytest.raises(moe.MoeError):
+        plan.backward(dev["dy"], dev["w13"], dev["w2"], dev["dw13"], dev["dw2"])
+    inf_plan = moe.MoePlan(64, 128, 64, 4, 2, flags=0)
+    with pytest.raises(moe.MoeError) as ei:
+        inf_plan.forward(dev["x"], dev["ids"], dev["scores"], dev["w13"], dev["w2"], save=True)
+    assert ei.value.code == moe.MOE_ERR_WORKSPACE
+
+
+def test_host_step_matches_device_path(moe):
+    inp = make(None, seed=10, train=True, T=200, d=256, I=128, E=8, k=4)
+    g = run_gpu(moe, inp, train=True)
+    c = inp["cfg"]
+    dev = g["dev"]
+    plan = moe.MoePlan(c["T"], c["d"], c["I"], c["E"], c["k"],
+                       flags=moe.MOE_WS_TRAINING | moe.MOE_WS_HOST_STAGING)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    x_h = pin(inp["x"]).view(torch.bfloat16)
+    dy_h = pin(inp["dy"]).view(torch.bfloat16)
+    ids_h, sc_h = pin(inp["ids"]), pin(inp["scores"])
+    y_h = torch.empty(c["T"], c["d"], dtype=torch.bfloat16).pin_memory()
+    dx_h = torch.empty(c["T"], c["d"], dtype=torch.bfloat16).pin_memory()
+    ds_h = torch.empty(c["T"], c["k"], dtype=torch.float32).pin_memory()
+    dw13, dw2 = dev["dw13"].clone(), dev["dw2"].clone()
+    plan.step_host(x_h, ids_h, sc_h, dev["w13"], dev["w2"], y_h, dy_h, dw13, dw2, dx_h, ds_h)
+    torch.cuda.synchronize()
+    assert torch.equal(y_h, g["y"].cpu())
+    assert torch.equal(dx_h, g["dx"].cpu())
+    assert torch.equal(ds_h, g["dscores"].cpu())
+    assert torch.equal(dw13, g["dw13"]) and torch.equal(dw2, g["dw2"])
+
+
+def test_mxfp8_quantiser_bit_exact(moe, orc):
+    rng = np.random.default_rng(3)
+    w = rng.standard_normal((96, 512)).astype(np.float32) * \
+        (2.0 ** rng.integers(-30, 30, (96, 1))).astype(np.float32)
+    w[5, 64:96] = 0.0
+    wb = mi.to_bf16_bits(w)
+    codes, scales = orc.quant_mxfp8(wb)
+    t = torch.from_numpy(wb.view(np.int16)).view(torch.bfloat16).cuda()
+    gc, gs = moe.quantize_mxfp8(t)
+    torch.cuda.synchronize()
+    assert np.array_equal(gc.cpu().numpy(), codes)
+    assert np.array_equal(gs.cpu().numpy(), scales)
