@@ -51,6 +51,9 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    # smaller cases of the same workload (profiling captures); defaults = the full workload
+    ap.add_argument("--T", type=int, default=None)
+    ap.add_argument("--E", type=int, default=None)
     return ap.parse_args()
 
 
@@ -270,7 +273,8 @@ def run_ours(args):
     import routed_mixture_experts_gb300 as moe
 
     need = ("x", "ids", "scores", "w13", "w2", "dy", "dw13", "dw2")
-    inp = mi.make_inputs(WORKLOAD, seed=args.seed + rank, need=need)
+    over = {key: v for key, v in (("T", args.T), ("E", args.E)) if v is not None}
+    inp = mi.make_inputs(WORKLOAD, seed=args.seed + rank, need=need, **over)
     c = inp["cfg"]
     T, d, I, E, k = c["T"], c["d"], c["I"], c["E"], c["k"]
 
