@@ -231,6 +231,37 @@ int moe_plan_set_timing_events(moe_plan* plan, int which, void* const* events, i
 /* Number of kernels this plan has launched so far (all entry points). */
 long long moe_plan_launch_count(const moe_plan* plan);
 
+/*
+ * moe_dispatch_static -- the expert-major dispatch of moe_forward (per-expert
+ * histogram, prefix scan, stable scatter) for callers that cannot allocate
+ * device memory: code that runs inside another framework's allocator or
+ * memory-pool callbacks, hosts whose device memory is already carved into
+ * fixed pools, or processes that may only touch memory they are handed.  It
+ * calls no cudaMalloc, cudaFree or other allocating routine; the kernels'
+ * scratch (chunk histograms, counts, tile table, error word) lives in one
+ * static __device__ array of about 280 KB that every GPU loading this library
+ * keeps until the process exits.  The source pages have no counterpart of this
+ * entry point.
+ *   ids [T,k] int32, scores [T,k] fp32                       (inputs, device)
+ *   m_indptr [E+1], off_pad [E+1], row_of [T*k] int32,
+ *   token_of [rows_capacity] int32, score_of [rows_capacity] fp32,
+ *   status [2] int32: {MOE_OK or MOE_ERR_BAD_IDS, smallest bad flat index or -1}
+ *                                                            (outputs, device)
+ * Same contents as the tables moe_forward builds (see moe_plan_buffer).
+ * Limits: T*k <= MOE_STATIC_MAX_ROUTED (else MOE_ERR_WORKSPACE: the static
+ * scratch is too small), k <= E <= 256, rows_capacity >=
+ * floor((T*k + E*(BM-1)) / BM) * BM (else MOE_ERR_INVALID_ARG).
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current: make that first call before
+ * any stream capture.  All calls on a device share the one array, which keeps
+ * the last call's contents (the error word is cleared at the start of each
+ * call): calls whose work overlaps on the GPU race and must not be issued.
+ */
+#define MOE_STATIC_MAX_ROUTED 262144
+int moe_dispatch_static(const int32_t* ids, const float* scores, int T, int k, int E,
+                        int32_t* m_indptr, int32_t* off_pad, int32_t* row_of, int32_t* token_of,
+                        float* score_of, long long rows_capacity, int32_t* status, void* stream);
+
 /* Rows per GEMM tile (BM), i.e. the padding granule of each expert segment. */
 int moe_tile_rows(void);
 
