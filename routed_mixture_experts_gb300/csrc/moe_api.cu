@@ -52,6 +52,9 @@ struct moe_plan {
   // tensor maps over the caller's weights (re-encoded when the pointers change)
   CUtensorMap tm_w13, tm_w2;
   const void *w13_cached, *w2_cached;
+  // tensor maps over the caller's fp32 weight gradients (WGRAD outputs)
+  CUtensorMap tm_dw13, tm_dw2;
+  const void *dw13_cached, *dw2_cached;
   int saved;
   // optional stage events and the launch counter
   void* const* ev[2];
@@ -61,7 +64,9 @@ struct moe_plan {
 
 namespace moe {
 
-int encode_tmap_bf16(CUtensorMap* map, const void* base, long long rows, long long cols) {
+namespace tmap_detail {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
     cudaDriverEntryPointQueryResult q;
@@ -69,17 +74,36 @@ int encode_tmap_bf16(CUtensorMap* map, const void* base, long long rows, long lo
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) != cudaSuccess ||
         q != cudaDriverEntryPointSuccess || !p)
-      return MOE_ERR_CUDA;
+      return nullptr;
     fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
   }
+  return fn;
+}
+
+int encode_2d(CUtensorMap* map, CUtensorMapDataType dt, int esize, const void* base,
+              long long rows, long long cols, cuuint32_t box_cols, cuuint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return MOE_ERR_CUDA;
   const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  const cuuint32_t box[2] = {64, 64};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * esize};
+  const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace tmap_detail
+
+using tmap_detail::encode_2d;
+
+int encode_tmap_bf16(CUtensorMap* map, const void* base, long long rows, long long cols) {
+  return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, rows, cols, 64, 64);
+}
+
+int encode_tmap_f32_out(CUtensorMap* map, const void* base, long long rows, long long cols) {
+  return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, rows, cols, 32, 128);
 }
 
 }  // namespace moe
@@ -273,6 +297,7 @@ int moe_plan_set_workspace(moe_plan* p, void* ws, size_t bytes, int flags) {
   layout(p, p->ws, flags);
   p->saved = 0;
   p->w13_cached = p->w2_cached = nullptr;
+  p->dw13_cached = p->dw2_cached = nullptr;
   const long long RP = p->RP;
   if (encode_tmap_bf16(&p->tm_xe, p->xe, RP, p->d) || encode_tmap_bf16(&p->tm_h, p->h, RP, p->I))
     return MOE_ERR_CUDA;
@@ -327,7 +352,7 @@ int moe_forward(moe_plan* p, const void* x, const int32_t* ids, const float* sco
     g.out0 = p->h; g.ld0 = p->I;
     g.out1 = p->a; g.ld1 = 2LL * p->I;
     g.save = save_for_backward ? 1 : 0;
-    e = launch_gemm(EPI_SWIGLU, p->bn13, false, false, p->tm_xe, p->tm_w13, g, p->num_sms, st);
+    e = launch_gemm(EPI_SWIGLU, p->bn13, false, false, p->tm_xe, p->tm_w13, p->tm_xe, g, p->num_sms, st);
     if (e != cudaSuccess) return cuda_status(e);
     p->launches += 1;
     mark(p, 0, 3, st);
@@ -340,7 +365,7 @@ int moe_forward(moe_plan* p, const void* x, const int32_t* ids, const float* sco
     g.n_tiles = p->d / p->bn2;
     g.out0 = p->ys; g.ld0 = p->d;
     g.row_scale = p->score_of;
-    e = launch_gemm(EPI_SCORE, p->bn2, false, false, p->tm_h, p->tm_w2, g, p->num_sms, st);
+    e = launch_gemm(EPI_SCORE, p->bn2, false, false, p->tm_h, p->tm_w2, p->tm_h, g, p->num_sms, st);
     if (e != cudaSuccess) return cuda_status(e);
     p->launches += 1;
     mark(p, 0, 4, st);
@@ -365,6 +390,14 @@ int moe_backward(moe_plan* p, const void* dy, const void* w13, const void* w2, v
   if (!p->saved) return MOE_ERR_STATE;
   cudaStream_t st = static_cast<cudaStream_t>(stream_v);
   if (refresh_weight_maps(p, w13, w2) != MOE_OK) return MOE_ERR_CUDA;
+  if (dw13 != p->dw13_cached) {
+    if (encode_tmap_f32_out(&p->tm_dw13, dw13, (long long)p->E * 2 * p->I, p->d)) return MOE_ERR_CUDA;
+    p->dw13_cached = dw13;
+  }
+  if (dw2 != p->dw2_cached) {
+    if (encode_tmap_f32_out(&p->tm_dw2, dw2, (long long)p->E * p->d, p->I)) return MOE_ERR_CUDA;
+    p->dw2_cached = dw2;
+  }
   const int I = p->I, d = p->d;
   mark(p, 1, 0, st);
   // b1: gather dY rows
@@ -384,7 +417,7 @@ int moe_backward(moe_plan* p, const void* dy, const void* w13, const void* w2, v
     g.out1 = p->hs; g.ld1 = I;
     g.row_scale = p->score_of;
     g.pdscore = p->pdscore;
-    e = launch_gemm(EPI_DGRAD2, p->bnd2, false, true, p->tm_dye, p->tm_w2, g, p->num_sms, st);
+    e = launch_gemm(EPI_DGRAD2, p->bnd2, false, true, p->tm_dye, p->tm_w2, p->tm_dye, g, p->num_sms, st);
     if (e != cudaSuccess) return cuda_status(e);
     p->launches += 1;
     mark(p, 1, 2, st);
@@ -396,7 +429,7 @@ int moe_backward(moe_plan* p, const void* dy, const void* w13, const void* w2, v
     g.b_expert_rows = 2 * I;
     g.n_tiles = d / p->bn2;
     g.out0 = p->dxe; g.ld0 = d;
-    e = launch_gemm(EPI_STORE, p->bn2, false, true, p->tm_dA, p->tm_w13, g, p->num_sms, st);
+    e = launch_gemm(EPI_STORE, p->bn2, false, true, p->tm_dA, p->tm_w13, p->tm_dA, g, p->num_sms, st);
     if (e != cudaSuccess) return cuda_status(e);
     p->launches += 1;
     mark(p, 1, 3, st);
@@ -414,7 +447,7 @@ int moe_backward(moe_plan* p, const void* dy, const void* w13, const void* w2, v
     g.n_tiles = I / p->bnw2;
     g.out0 = dw2; g.ld0 = I;
     g.out_expert_stride = (long long)d * I;
-    e = launch_gemm(EPI_WGRAD, p->bnw2, true, true, p->tm_dye, p->tm_hs, g, p->num_sms, st);
+    e = launch_gemm(EPI_WGRAD, p->bnw2, true, true, p->tm_dye, p->tm_hs, p->tm_dw2, g, p->num_sms, st);
     if (e != cudaSuccess) return cuda_status(e);
     p->launches += 1;
     mark(p, 1, 5, st);
@@ -426,7 +459,7 @@ int moe_backward(moe_plan* p, const void* dy, const void* w13, const void* w2, v
     g.n_tiles = d / p->bnw13;
     g.out0 = dw13; g.ld0 = d;
     g.out_expert_stride = 2LL * I * d;
-    e = launch_gemm(EPI_WGRAD, p->bnw13, true, true, p->tm_dA, p->tm_xe, g, p->num_sms, st);
+    e = launch_gemm(EPI_WGRAD, p->bnw13, true, true, p->tm_dA, p->tm_xe, p->tm_dw13, g, p->num_sms, st);
     if (e != cudaSuccess) return cuda_status(e);
     p->launches += 1;
     mark(p, 1, 6, st);
@@ -564,7 +597,7 @@ extern "C" int moe_gemm_bf16(int mode, const void* A, const void* B, void* C, in
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   int* s = static_cast<int*>(scratch);
   k_dense_meta<<<1, 1, 0, st>>>(s, M / 128, K);
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tc;
   GemmArgs g;
   memset(&g, 0, sizeof(g));
   const int bn = pick_bn_n(N);
@@ -581,16 +614,18 @@ extern "C" int moe_gemm_bf16(int mode, const void* A, const void* B, void* C, in
     g.tile_expert = nullptr;
     g.k_blocks = K / kBK;
     g.b_expert_rows = mode == 0 ? N : K;
-    e = launch_gemm(EPI_STORE, bn, false, mode == 1, ta, tb, g, sms, st);
+    e = launch_gemm(EPI_STORE, bn, false, mode == 1, ta, tb, ta, g, sms, st);
   } else if (mode == 2) {
-    if (encode_tmap_bf16(&ta, A, K, M) || encode_tmap_bf16(&tb, B, K, N)) return MOE_ERR_CUDA;
+    if (encode_tmap_bf16(&ta, A, K, M) || encode_tmap_bf16(&tb, B, K, N) ||
+        encode_tmap_f32_out(&tc, C, M, N))
+      return MOE_ERR_CUDA;
     g.wgrad = 1;
     g.num_nonempty = s + 1;
     g.off_pad = s + 2;
     g.expert_order = s + 4;
     g.m_tiles = M / kBM;
     g.out_expert_stride = 0;
-    e = launch_gemm(EPI_WGRAD, bn, true, true, ta, tb, g, sms, st);
+    e = launch_gemm(EPI_WGRAD, bn, true, true, ta, tb, tc, g, sms, st);
   } else {
     return MOE_ERR_INVALID_ARG;
   }

@@ -81,6 +81,20 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
   return true;
 }
 
+// AND of `v` over the 128 epilogue threads (named barrier 1).
+__device__ __forceinline__ int epi_bar_and(int v) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.s32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 128, p;\n\t"
+      "selp.s32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(v)
+      : "memory");
+  return r;
+}
+
 __device__ __forceinline__ float swiglu_fwd(float G, float U, float L) {
   if (L > 0.f) {
     G = fminf(fmaxf(G, -L), L);
@@ -209,45 +223,72 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, const TileInfo& ti, 
       store16_bf16(hsrow + c, hs);
     }
     a.pdscore[grow * a.n_tiles + ti.nt] = part;
-  } else if constexpr (EPI == EPI_WGRAD) {
-    if (ti.kb == 0) return;
-    float* out = static_cast<float*>(a.out0) + (long long)ti.e * a.out_expert_stride +
-                 grow * a.ld0 + ti.n0;
-#pragma unroll 1
-    for (int c = 0; c < BN; c += 16) {
-      tmem_ld16(tbase + c, r0);
-      float4* p = reinterpret_cast<float4*>(out + c);
-      float4 o0 = p[0], o1 = p[1], o2 = p[2], o3 = p[3];
-      tmem_ld_wait();
-      o0.x += __uint_as_float(r0[0]);  o0.y += __uint_as_float(r0[1]);
-      o0.z += __uint_as_float(r0[2]);  o0.w += __uint_as_float(r0[3]);
-      o1.x += __uint_as_float(r0[4]);  o1.y += __uint_as_float(r0[5]);
-      o1.z += __uint_as_float(r0[6]);  o1.w += __uint_as_float(r0[7]);
-      o2.x += __uint_as_float(r0[8]);  o2.y += __uint_as_float(r0[9]);
-      o2.z += __uint_as_float(r0[10]); o2.w += __uint_as_float(r0[11]);
-      o3.x += __uint_as_float(r0[12]); o3.y += __uint_as_float(r0[13]);
-      o3.z += __uint_as_float(r0[14]); o3.w += __uint_as_float(r0[15]);
-      p[0] = o0; p[1] = o1; p[2] = o2; p[3] = o3;
-    }
   }
 }
 
+// WGRAD epilogue: the accumulator tile is written, 32 columns at a time, into one
+// of four 16 KB shared-memory buffers (128 rows x 32 fp32, 128-byte swizzle, the
+// layout of the fp32 tensor map), and the TMA unit adds each buffer into the
+// fp32 gradient in global memory (cp.reduce.async.bulk.tensor .add).  The
+// read-modify-write then happens in L2 with many bytes in flight, instead of
+// through per-thread loads and stores.
 template <int BN>
+__device__ __forceinline__ void epilogue_wgrad(const GemmArgs& a, const CUtensorMap* tmC,
+                                               const TileInfo& ti, int row, uint32_t tbase,
+                                               uint32_t stage_smem, int et, int& sub) {
+  if (ti.kb == 0) return;
+  const int ybase = ti.e * a.m_tiles * kBM + ti.m0;
+  uint32_t r0[16], r1[16];
+#pragma unroll 1
+  for (int c = 0; c < BN; c += 32) {
+    const uint32_t buf = stage_smem + (uint32_t)(sub & 3) * 16384u;
+    if (et == 0) bulk_wait_read<3>();          // this buffer's previous add has read it
+    named_bar_sync(1, 128);
+    tmem_ld16(tbase + c, r0);
+    tmem_ld16(tbase + c + 16, r1);
+    tmem_ld_wait();
+    const uint32_t rbase = buf + (uint32_t)row * 128u;
+    const uint32_t sw = (uint32_t)(row & 7);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      st_shared_v4(rbase + (((uint32_t)q ^ sw) << 4), __uint_as_float(r0[4 * q]),
+                   __uint_as_float(r0[4 * q + 1]), __uint_as_float(r0[4 * q + 2]),
+                   __uint_as_float(r0[4 * q + 3]));
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      st_shared_v4(rbase + (((uint32_t)(q + 4) ^ sw) << 4), __uint_as_float(r1[4 * q]),
+                   __uint_as_float(r1[4 * q + 1]), __uint_as_float(r1[4 * q + 2]),
+                   __uint_as_float(r1[4 * q + 3]));
+    fence_proxy_async_smem();
+    named_bar_sync(1, 128);
+    if (et == 0) {
+      tma_reduce_add_2d(tmC, buf, ti.n0 + c, ybase);
+      bulk_commit();
+    }
+    ++sub;
+  }
+}
+
+template <int BN, int EPI>
 struct GemmShape {
   static constexpr int A_BYTES = kBM * kBK * 2;                // 16 KB
   static constexpr int B_BYTES = BN * kBK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (196 * 1024) / STAGE_BYTES > 8 ? 8 : (196 * 1024) / STAGE_BYTES;
+  // WGRAD keeps 64 KB for its four fp32 staging buffers and needs few stages
+  // (its K loop is one expert's rows and it is bound by the gradient traffic).
+  static constexpr int STAGE_BUDGET = EPI == EPI_WGRAD ? 144 * 1024 : 196 * 1024;
+  static constexpr int STAGES = STAGE_BUDGET / STAGE_BYTES > 8 ? 8 : STAGE_BUDGET / STAGE_BYTES;
+  static constexpr int OUT_BYTES = EPI == EPI_WGRAD ? 4 * 16384 : 0;
   static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + OUT_BYTES + BAR_BYTES + 1024;
   static constexpr uint32_t TMEM_COLS = 2 * BN;
 };
 
 template <int BN, bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmArgs args) {
-  using S = GemmShape<BN>;
+                   const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
+  using S = GemmShape<BN, EPI>;
   constexpr int STAGES = S::STAGES;
   constexpr uint32_t IDESC = idesc_bf16(kBM, BN, A_MN, B_MN);
   static_assert(S::SMEM_BYTES <= 232448, "shared memory budget");
@@ -260,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * S::STAGE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * S::STAGE_BYTES + S::OUT_BYTES);
   // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -297,6 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (EPI == EPI_WGRAD) tma_prefetch_desc(&tmC);
   }
   tc_fence_before();
   __syncthreads();
@@ -443,21 +485,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- epilogue (warps 2..5) ----------------
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
+    const int et = threadIdx.x - 64;          // 0..127 over the epilogue warps
     int acc = 0;
     uint32_t acc_phase = 0;
+    int sub = 0;                              // WGRAD staging-buffer sequence number
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const TileInfo ti = decode_tile<BN>(args, tile);
       int w = 1;
       if (lane == 0) w = mbar_wait(tfull_bar(acc), acc_phase, &abort_s, args.err, 5);
-      if (__shfl_sync(0xffffffffu, w, 0) == 0) break;
+      // all four epilogue warps leave together, so their named barriers stay matched
+      const int ok_warp = __shfl_sync(0xffffffffu, w, 0);
+      if (EPI == EPI_WGRAD) {
+        if (epi_bar_and(ok_warp) == 0) break;
+      } else if (ok_warp == 0) {
+        break;
+      }
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
-      epilogue<BN, EPI>(args, ti, row, tbase);
+      if constexpr (EPI == EPI_WGRAD)
+        epilogue_wgrad<BN>(args, &tmC, ti, row, tbase, stage0 + STAGES * S::STAGE_BYTES, et, sub);
+      else
+        epilogue<BN, EPI>(args, ti, row, tbase);
       tc_fence_before();
       mbar_arrive(tempty_bar(acc));
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
+    if (EPI == EPI_WGRAD && et == 0) bulk_wait_all();   // every gradient add has landed
   }
 
   tc_fence_before();
@@ -469,28 +523,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int BN, bool A_MN, bool B_MN, int EPI>
-cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args,
-                       int grid, cudaStream_t stream) {
+cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                       const GemmArgs& args, int grid, cudaStream_t stream) {
   auto kern = k_grouped_gemm<BN, A_MN, B_MN, EPI>;
-  const int smem = GemmShape<BN>::SMEM_BYTES;
+  const int smem = GemmShape<BN, EPI>::SMEM_BYTES;
   static bool configured = false;   // attribute set once per process (same device image)
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  kern<<<grid, kThreads, smem, stream>>>(ta, tb, args);
+  kern<<<grid, kThreads, smem, stream>>>(ta, tb, tc, args);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_gemm(int epi, int bn, bool a_mn, bool b_mn, const CUtensorMap& ta,
-                        const CUtensorMap& tb, const GemmArgs& args, int grid,
-                        cudaStream_t stream) {
+                        const CUtensorMap& tb, const CUtensorMap& tc, const GemmArgs& args,
+                        int grid, cudaStream_t stream) {
 #define MOE_CASE(EPI_, BN_, AMN_, BMN_)                                     \
   if (epi == EPI_ && bn == BN_ && a_mn == AMN_ && b_mn == BMN_)             \
-    return launch_one<BN_, AMN_, BMN_, EPI_>(ta, tb, args, grid, stream);
+    return launch_one<BN_, AMN_, BMN_, EPI_>(ta, tb, tc, args, grid, stream);
   MOE_CASE(EPI_SWIGLU, 128, false, false)
   MOE_CASE(EPI_SWIGLU, 256, false, false)
   MOE_CASE(EPI_SCORE, 128, false, false)

@@ -58,13 +58,19 @@ struct GemmArgs {
 };
 
 // Encode a 2-D bf16 tensor map (row-major [rows, cols]) with a 64 x 64 box and
-// 128-byte swizzle, the only box shape the GEMM kernels load.
+// 128-byte swizzle, the operand box of the GEMM kernels.
 int encode_tmap_bf16(CUtensorMap* map, const void* base, long long rows, long long cols);
 
-// Launch the grouped GEMM.  a_mn / b_mn select MN-major operands.
+// Encode a 2-D fp32 tensor map (row-major [rows, cols]) with a 32 x 128 box
+// (128 bytes x 128 rows) and 128-byte swizzle: the weight-gradient tiles that the
+// WGRAD epilogue adds into global memory.
+int encode_tmap_f32_out(CUtensorMap* map, const void* base, long long rows, long long cols);
+
+// Launch the grouped GEMM.  a_mn / b_mn select MN-major operands; tc is only
+// read by EPI_WGRAD (the fp32 gradient [E*M, N]).
 cudaError_t launch_gemm(int epi, int bn, bool a_mn, bool b_mn, const CUtensorMap& ta,
-                        const CUtensorMap& tb, const GemmArgs& args, int grid,
-                        cudaStream_t stream);
+                        const CUtensorMap& tb, const CUtensorMap& tc, const GemmArgs& args,
+                        int grid, cudaStream_t stream);
 
 // Dispatch kernels.
 struct RouteArgs {
