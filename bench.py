@@ -37,6 +37,7 @@ if ROOT not in sys.path:
 METRIC = "routed-expert TFLOP/s (fwd; fwd+bwd) at T=8192 E=128 k=8; % of GB300 tensor peak"
 WORKLOAD = "train_e128"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_OVER_BF16 = 2.0    # nominal dense E4M3 / bf16 tensor throughput ratio (4.5 / 2.25 PFLOP/s)
 
 FWD_STAGES = ["dispatch", "gather_x", "w13_swiglu", "w2_score", "combine_y"]
 BWD_STAGES = ["gather_dy", "dgrad_w2_swiglu", "dgrad_w13", "combine_dx", "wgrad_w2", "wgrad_w13"]
@@ -51,6 +52,8 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--mx-steps", type=int, default=50,
+                    help="timed MXFP8 forward steps on the same inputs (0: skip)")
     # smaller cases of the same workload (profiling captures); defaults = the full workload
     ap.add_argument("--T", type=int, default=None)
     ap.add_argument("--E", type=int, default=None)
@@ -398,6 +401,52 @@ def run_ours(args):
         e2e = {"value": flops_step * ws / (ems * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems}
 
+    # MXFP8 E4M3 forward on the same inputs (its workload differs only in precision)
+    mx = None
+    if args.mx_steps > 0:
+        w13q, w13s, w2q, w2s = moe.prepare_weights_mxfp8(D["w13"], D["w2"])
+        mplan = moe.MoePlan(T, d, I, E, k, precision=moe.MOE_PREC_MXFP8, clamp=c["clamp"], flags=0,
+                            device=dev)
+        ym = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+
+        def mstep():
+            mplan.forward(D["x"], D["ids"], D["scores"], w13q, w2q, y=ym, w13_sf=w13s, w2_sf=w2s)
+
+        for _ in range(args.warmup):
+            mstep()
+        mev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.mx_steps)]
+        for ev in [e for st_ in mev for e in st_]:
+            ev.record(stream)
+        torch.cuda.synchronize()
+        m0 = torch.cuda.Event(enable_timing=True)
+        m1 = torch.cuda.Event(enable_timing=True)
+        m0.record(stream)
+        for i in range(args.mx_steps):
+            mplan.set_timing_events(0, mev[i])
+            mstep()
+        m1.record(stream)
+        torch.cuda.synchronize()
+        mplan.set_timing_events(0, None)
+        rc, det = mplan.check()
+        if rc != 0:
+            raise RuntimeError("device error %d (%d) in the MXFP8 forward" % (rc, det))
+        mms = max_over_ranks(m0.elapsed_time(m1), dev) / args.mx_steps
+        fp8_peak = pk["bf16_tflops_sustained"] * FP8_OVER_BF16
+        mst = {}
+        for j, name in enumerate(FWD_STAGES):
+            t_ms = sum(mev[i][j].elapsed_time(mev[i][j + 1]) for i in range(args.mx_steps)) / args.mx_steps
+            bound, fl, by = model[name]
+            ent = {"ms": round(t_ms, 5)}
+            if fl:
+                ach = fl / (t_ms * 1e-3) / 1e12
+                ent.update(achieved=round(ach, 1), unit="TFLOP/s", peak=fp8_peak,
+                           frac=round(ach / fp8_peak, 4))
+            mst[name] = ent
+        mx = {"workload": "mxfp8_e128 (same sizes and inputs, E4M3 block-scaled forward)",
+              "value": 6.0 * T * k * d * I * ws / (mms * 1e-3) / 1e12, "unit": "TFLOP/s",
+              "ms_per_step": mms, "steps": args.mx_steps,
+              "peak_note": "fp8 peak = measured sustained bf16 x 2 (nominal ratio)", "stages": mst}
+
     if rank != 0:
         return
     cpu = None
@@ -419,7 +468,7 @@ def run_ours(args):
         "fwd_tflops": 6.0 * T * k * d * I / (fwd_ms * 1e-3) / 1e12,
         "fwd_ms": fwd_ms,
         "e2e": e2e, "gpu_launches": int(n1 - n0), "roofline": roofline, "stages": stages,
-        "cpu_baseline": cpu, "clocks": clk,
+        "cpu_baseline": cpu, "clocks": clk, "mxfp8_forward": mx,
     }
     print(json.dumps(line), flush=True)
 

@@ -116,8 +116,11 @@ int moe_plan_set_workspace(moe_plan* plan, void* workspace, size_t bytes, int fl
  *   w13     [E, 2I, d] bf16: rows [0,I) gate, [I,2I) up (not interleaved)
  *   w2      [E, d, I]  bf16
  *   For MOE_PREC_MXFP8, w13/w2 hold E4M3 codes (uint8, same shapes) and
- *   w13_sf [E, 2I, d/32], w2_sf [E, d, I/32] their E8M0 scales (see
- *   moe_quantize_mxfp8); for bf16 pass NULL.
+ *   w13_sf / w2_sf their E8M0 scales in the tiled layout, both produced by
+ *   moe_prepare_weights_mxfp8; for bf16 pass NULL.  An MXFP8 plan quantises
+ *   the routed activation rows along d and h along I (32-element blocks) and
+ *   runs block-scaled E4M3 GEMMs; it is forward only (save_for_backward = 0),
+ *   and needs I % 128 == 0, d <= 4096, I <= 4096.
  * Output: y [T, d] bf16, overwritten:
  *   y[t] = bf16( sum_{j=0..k-1} bf16( scores[t,j] * W2[e] . h ) ),
  *   h = bf16(silu(G) * U),  (G, U) = bf16(W13[e] . x[t]),  e = ids[t,j]
@@ -172,6 +175,29 @@ int moe_quantize_mxfp8(const void* in, long rows, int K, uint8_t* codes, uint8_t
                        void* stream);
 
 /*
+ * Prepared MXFP8 weights ("What it is selling": MXFP8 E4M3 accepts prepared
+ * weights; nvfp4moe "Training": re-prepare after each optimizer step).
+ * Quantises w13 [E,2I,d] along d and w2 [E,d,I] along I with the block rule of
+ * moe_quantize_mxfp8 into
+ *   w13_codes [E,2I,d], w2_codes [E,d,I]  (E4M3 bytes, same layout as the input)
+ *   w13_scales, w2_scales                 (E8M0 bytes in the tiled layout the
+ *                                           block-scaled GEMMs read; sizes from
+ *                                           moe_mxfp8_weight_scale_bytes)
+ * Tiled scale layout: rows are grouped in blocks of 128 and K in groups of 128
+ * elements (four 32-element blocks); each (row block, K group) is a 512-byte
+ * chunk, chunk index block*(K/128) + kb/4, in which row r = row%128 and block
+ * j = kb%4 sit at byte 16*(r%32) + 4*(r/32) + j.  For W13 the row
+ * blocks are, per expert, the 64 gate rows and 64 up rows of each 64-column
+ * n-tile (block e*(I/64)+t holds gate rows [64t,64t+64) then up rows
+ * [I+64t, I+64t+64)); for W2 they are consecutive 128-row blocks of [E*d].
+ * d % 128 == 0, I % 128 == 0.
+ */
+size_t moe_mxfp8_weight_scale_bytes(int d, int I, int E, int which /* 0: W13, 1: W2 */);
+int moe_prepare_weights_mxfp8(const void* w13, const void* w2, int d, int I, int E,
+                              uint8_t* w13_codes, uint8_t* w13_scales, uint8_t* w2_codes,
+                              uint8_t* w2_scales, void* stream);
+
+/*
  * Synchronise the device, read and clear the plan's device error word.
  * Returns MOE_OK or the first recorded device error; *detail (may be NULL)
  * receives its detail (for MOE_ERR_BAD_IDS the smallest offending flat index).
@@ -212,6 +238,10 @@ const char* moe_status_string(int status);
 #define MOE_BUF_DA       10
 #define MOE_BUF_HS       11
 #define MOE_BUF_DXE      12
+#define MOE_BUF_XQ       13   /* u8   [Rpad,d] E4M3 activations (MXFP8 plans) */
+#define MOE_BUF_XSF      14   /* u8   tiled E8M0 scales of XQ                   */
+#define MOE_BUF_HQ       15   /* u8   [Rpad,I] E4M3 h (MXFP8 plans)             */
+#define MOE_BUF_HSF      16   /* u8   tiled E8M0 scales of HQ                   */
 int moe_plan_buffer(const moe_plan* plan, int which, void** dev_ptr, size_t* bytes);
 
 /*

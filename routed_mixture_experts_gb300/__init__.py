@@ -27,5 +27,6 @@ from .binding import (  # noqa: F401
     MoePlan,
     gemm_bf16,
     lib,
+    prepare_weights_mxfp8,
     quantize_mxfp8,
 )

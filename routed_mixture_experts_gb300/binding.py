@@ -20,7 +20,7 @@ MOE_PREC_MXFP8 = 1
 MOE_WS_TRAINING = 1
 MOE_WS_HOST_STAGING = 2
 MOE_BUF = dict(m_indptr=0, off_pad=1, row_of=2, token_of=3, score_of=4, xe=5, a=6, h=7, ys=8,
-               dye=9, dA=10, hs=11, dxe=12)
+               dye=9, dA=10, hs=11, dxe=12, xq=13, xsf=14, hq=15, hsf=16)
 
 _lock = threading.Lock()
 _lib = None
@@ -56,11 +56,15 @@ def _declare(L):
     L.moe_gemm_scratch_bytes.restype = sz
     L.moe_gemm_bf16.argtypes = [i32, vp, vp, vp, i32, i32, i32, vp, vp]
     L.moe_plan_set_timing_events.argtypes = [vp, i32, ctypes.POINTER(vp), i32]
+    L.moe_mxfp8_weight_scale_bytes.argtypes = [i32, i32, i32, i32]
+    L.moe_mxfp8_weight_scale_bytes.restype = sz
+    L.moe_prepare_weights_mxfp8.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp, vp]
     L.moe_plan_launch_count.argtypes = [vp]
     L.moe_plan_launch_count.restype = ctypes.c_longlong
     for name in ("moe_plan_set_swiglu_clamp", "moe_plan_set_workspace", "moe_forward",
                  "moe_backward", "moe_step_host", "moe_quantize_mxfp8", "moe_plan_check",
-                 "moe_plan_buffer", "moe_gemm_bf16", "moe_plan_set_timing_events"):
+                 "moe_plan_buffer", "moe_gemm_bf16", "moe_plan_set_timing_events",
+                 "moe_prepare_weights_mxfp8"):
         getattr(L, name).restype = i32
     return L
 
@@ -191,6 +195,25 @@ def quantize_mxfp8(w, stream=None):
     _check(lib().moe_quantize_mxfp8(_p(w), rows, K, _p(codes), _p(scales), _stream(stream)),
            "quantize_mxfp8")
     return codes, scales
+
+
+def prepare_weights_mxfp8(w13, w2, stream=None):
+    """bf16 W13 [E,2I,d], W2 [E,d,I] -> (w13 codes, w13 tiled scales, w2 codes,
+    w2 tiled scales), the prepared MXFP8 weights of moe_forward."""
+    import torch
+
+    E, I2, d = w13.shape
+    I = I2 // 2
+    L = lib()
+    w13q = torch.empty(w13.shape, dtype=torch.uint8, device=w13.device)
+    w2q = torch.empty(w2.shape, dtype=torch.uint8, device=w2.device)
+    w13s = torch.empty(L.moe_mxfp8_weight_scale_bytes(d, I, E, 0), dtype=torch.uint8,
+                       device=w13.device)
+    w2s = torch.empty(L.moe_mxfp8_weight_scale_bytes(d, I, E, 1), dtype=torch.uint8,
+                      device=w2.device)
+    _check(L.moe_prepare_weights_mxfp8(_p(w13), _p(w2), d, I, E, _p(w13q), _p(w13s), _p(w2q),
+                                       _p(w2s), _stream(stream)), "prepare_weights_mxfp8")
+    return w13q, w13s, w2q, w2s
 
 
 def gemm_bf16(mode, A, B, C, M, N, K, stream=None):

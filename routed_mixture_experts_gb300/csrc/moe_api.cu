@@ -52,6 +52,11 @@ struct moe_plan {
   // tensor maps over the caller's weights (re-encoded when the pointers change)
   CUtensorMap tm_w13, tm_w2;
   const void *w13_cached, *w2_cached;
+  // MXFP8: quantised expert-major activations and h, with tiled scales
+  uint8_t *xq, *xsf, *hq, *hsf;
+  int ngr_d, ngr_I;                 // 128-element scale groups along d and along I
+  CUtensorMap tm_xq, tm_hq, tm_w13q, tm_w2q;
+  const void *w13q_cached, *w2q_cached;
   // tensor maps over the caller's fp32 weight gradients (WGRAD outputs)
   CUtensorMap tm_dw13, tm_dw2;
   const void *dw13_cached, *dw2_cached;
@@ -106,6 +111,10 @@ int encode_tmap_f32_out(CUtensorMap* map, const void* base, long long rows, long
   return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, rows, cols, 32, 128);
 }
 
+int encode_tmap_u8(CUtensorMap* map, const void* base, long long rows, long long cols) {
+  return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, rows, cols, 128, 64);
+}
+
 }  // namespace moe
 
 namespace {
@@ -137,12 +146,20 @@ size_t layout(moe_plan* p, char* base, int flags) {
   p->row_of = reinterpret_cast<int32_t*>(take(4 * (size_t)p->R));
   p->token_of = reinterpret_cast<int32_t*>(take(4 * RP));
   p->score_of = reinterpret_cast<float*>(take(4 * RP));
-  p->xe = reinterpret_cast<uint16_t*>(take(2 * RP * d));
+  const bool mx = p->precision == MOE_PREC_MXFP8;
+  p->xe = mx ? nullptr : reinterpret_cast<uint16_t*>(take(2 * RP * d));
+  p->xq = p->xsf = p->hq = p->hsf = nullptr;
+  if (mx) {
+    p->xq = reinterpret_cast<uint8_t*>(take(RP * d));
+    p->xsf = reinterpret_cast<uint8_t*>(take((size_t)mx_sf_bytes(RP, (int)d)));
+    p->hq = reinterpret_cast<uint8_t*>(take(RP * I));
+    p->hsf = reinterpret_cast<uint8_t*>(take((size_t)mx_sf_bytes(RP, (int)I)));
+  }
   p->h = reinterpret_cast<uint16_t*>(take(2 * RP * I));
   p->ys = reinterpret_cast<uint16_t*>(take(2 * RP * d));
   p->a = p->dye = p->dA = p->hs = p->dxe = nullptr;
   p->pdscore = nullptr;
-  if (flags & MOE_WS_TRAINING) {
+  if ((flags & MOE_WS_TRAINING) && !mx) {
     p->a = reinterpret_cast<uint16_t*>(take(2 * RP * 2 * I));
     p->dye = reinterpret_cast<uint16_t*>(take(2 * RP * d));
     p->dA = reinterpret_cast<uint16_t*>(take(2 * RP * 2 * I));
@@ -223,6 +240,56 @@ GemmArgs wgrad_args(const moe_plan* p) {
 
 int gather_grid(const moe_plan* p) { return p->num_sms * 8; }
 
+void mark(const moe_plan* p, int which, int i, cudaStream_t st);
+
+// MXFP8 forward after dispatch ("What it is selling": MXFP8 E4M3 quantises
+// activations after routing and takes prepared weights; staged W13 and W2):
+// gather + quantise x rows -> block-scaled W13 GEMM + SwiGLU + quantise h ->
+// block-scaled W2 GEMM x score -> combine.
+int forward_mxfp8(moe_plan* p, const void* x, const uint8_t* w13_sf, const uint8_t* w2_sf,
+                  void* y, cudaStream_t st) {
+  cudaError_t e = launch_gather_quant_rows(x, p->token_of, p->off_pad + p->E, p->d, p->xq, p->xsf,
+                                           gather_grid(p), st);
+  if (e != cudaSuccess) return cuda_status(e);
+  p->launches += 1;
+  mark(p, 0, 2, st);
+  {
+    GemmArgs g = rows_args(p);
+    g.k_blocks = p->d / 128;
+    g.b_expert_rows = 2 * p->I;
+    g.b_half_rows = p->I;
+    g.n_tiles = p->I / 64;
+    g.out0 = p->h; g.ld0 = p->I;
+    g.sfa = p->xsf; g.sfb = w13_sf; g.sf_ngr = p->ngr_d; g.b_blocks_per_expert = p->I / 64;
+    g.hq = p->hq; g.hsf = p->hsf; g.hsf_ngr = p->ngr_I;
+    e = launch_gemm(EPI_SWIGLU, 128, false, false, p->tm_xq, p->tm_w13q, p->tm_xq, g, p->num_sms,
+                    st, true);
+    if (e != cudaSuccess) return cuda_status(e);
+    p->launches += 1;
+    mark(p, 0, 3, st);
+  }
+  {
+    GemmArgs g = rows_args(p);
+    g.k_blocks = p->I / 128;
+    g.b_expert_rows = p->d;
+    g.n_tiles = p->d / 128;
+    g.out0 = p->ys; g.ld0 = p->d;
+    g.row_scale = p->score_of;
+    g.sfa = p->hsf; g.sfb = w2_sf; g.sf_ngr = p->ngr_I; g.b_blocks_per_expert = p->d / 128;
+    e = launch_gemm(EPI_SCORE, 128, false, false, p->tm_hq, p->tm_w2q, p->tm_hq, g, p->num_sms,
+                    st, true);
+    if (e != cudaSuccess) return cuda_status(e);
+    p->launches += 1;
+    mark(p, 0, 4, st);
+  }
+  e = launch_combine(p->ys, p->row_of, p->T, p->k, p->d, y, nullptr, 0, nullptr, gather_grid(p), st);
+  if (e != cudaSuccess) return cuda_status(e);
+  p->launches += 1;
+  mark(p, 0, 5, st);
+  p->saved = 0;
+  return MOE_OK;
+}
+
 void mark(const moe_plan* p, int which, int i, cudaStream_t st) {
   if (p->ev[which] && i < p->nev[which] && p->ev[which][i])
     cudaEventRecord(static_cast<cudaEvent_t>(p->ev[which][i]), st);
@@ -252,6 +319,8 @@ moe_plan* moe_plan_create(int T, int d, int I, int E, int k, int precision) {
   if (T < 1 || d < 128 || I < 64 || d % 128 || I % 64 || k < 1 || E < k || E > 256) return nullptr;
   if ((long long)T * k >= (1LL << 31) - (long long)E * kBM) return nullptr;
   if (precision != MOE_PREC_BF16 && precision != MOE_PREC_MXFP8) return nullptr;
+  // MXFP8: K loops in 128-element stages (scales travel with each stage)
+  if (precision == MOE_PREC_MXFP8 && I % 128) return nullptr;
   moe_plan* p = new (std::nothrow) moe_plan;
   if (!p) return nullptr;
   memset(p, 0, sizeof(*p));
@@ -264,6 +333,8 @@ moe_plan* moe_plan_create(int T, int d, int I, int E, int k, int precision) {
   p->bnd2 = pick_bn_n(I);
   p->bnw2 = pick_bn_n(I);
   p->bnw13 = p->bn2;
+  p->ngr_d = d / 128;
+  p->ngr_I = I / 128;
   int dev = 0;
   p->num_sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) {
@@ -298,7 +369,13 @@ int moe_plan_set_workspace(moe_plan* p, void* ws, size_t bytes, int flags) {
   p->saved = 0;
   p->w13_cached = p->w2_cached = nullptr;
   p->dw13_cached = p->dw2_cached = nullptr;
+  p->w13q_cached = p->w2q_cached = nullptr;
   const long long RP = p->RP;
+  if (p->precision == MOE_PREC_MXFP8) {
+    if (encode_tmap_u8(&p->tm_xq, p->xq, RP, p->d) || encode_tmap_u8(&p->tm_hq, p->hq, RP, p->I))
+      return MOE_ERR_CUDA;
+    return reset_error_word(p->err);
+  }
   if (encode_tmap_bf16(&p->tm_xe, p->xe, RP, p->d) || encode_tmap_bf16(&p->tm_h, p->h, RP, p->I))
     return MOE_ERR_CUDA;
   if (flags & MOE_WS_TRAINING) {
@@ -317,12 +394,24 @@ int moe_forward(moe_plan* p, const void* x, const int32_t* ids, const float* sco
   if (!aligned16(x) || !aligned16(w13) || !aligned16(w2) || !aligned16(y))
     return MOE_ERR_INVALID_ARG;
   if (!p->ws) return MOE_ERR_WORKSPACE;
+  const bool mx = p->precision == MOE_PREC_MXFP8;
+  if (mx && save_for_backward) return MOE_ERR_UNSUPPORTED;   // MXFP8 is forward only
   if (save_for_backward && !(p->ws_flags & MOE_WS_TRAINING)) return MOE_ERR_WORKSPACE;
-  if (p->precision != MOE_PREC_BF16) return MOE_ERR_UNSUPPORTED;
-  (void)w13_sf;
-  (void)w2_sf;
+  if (mx && (!w13_sf || !w2_sf || !aligned16(w13_sf) || !aligned16(w2_sf)))
+    return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream_v);
-  if (refresh_weight_maps(p, w13, w2) != MOE_OK) return MOE_ERR_CUDA;
+  if (mx) {
+    if (w13 != p->w13q_cached) {
+      if (encode_tmap_u8(&p->tm_w13q, w13, (long long)p->E * 2 * p->I, p->d)) return MOE_ERR_CUDA;
+      p->w13q_cached = w13;
+    }
+    if (w2 != p->w2q_cached) {
+      if (encode_tmap_u8(&p->tm_w2q, w2, (long long)p->E * p->d, p->I)) return MOE_ERR_CUDA;
+      p->w2q_cached = w2;
+    }
+  } else if (refresh_weight_maps(p, w13, w2) != MOE_OK) {
+    return MOE_ERR_CUDA;
+  }
 
   mark(p, 0, 0, st);
   // a1-a3: dispatch
@@ -337,6 +426,7 @@ int moe_forward(moe_plan* p, const void* x, const int32_t* ids, const float* sco
   if (e != cudaSuccess) return cuda_status(e);
   p->launches += 3;
   mark(p, 0, 1, st);
+  if (mx) return forward_mxfp8(p, x, w13_sf, w2_sf, y, st);
   // a4: gather x rows into expert-major order
   e = launch_gather_rows(x, p->token_of, p->off_pad + p->E, p->d, p->xe, gather_grid(p), st);
   if (e != cudaSuccess) return cuda_status(e);
@@ -512,6 +602,26 @@ int moe_quantize_mxfp8(const void* in, long rows, int K, uint8_t* codes, uint8_t
   return cuda_status(launch_quant_mxfp8(in, rows, K, codes, scales, static_cast<cudaStream_t>(stream)));
 }
 
+size_t moe_mxfp8_weight_scale_bytes(int d, int I, int E, int which) {
+  if (d <= 0 || I <= 0 || E <= 0 || d % 128 || I % 128) return 0;
+  if (which == 0) return (size_t)mx_sf_bytes((long long)E * (I / 64) * 128, d);   // W13
+  if (which == 1) return (size_t)mx_sf_bytes((long long)E * d, I);                // W2
+  return 0;
+}
+
+int moe_prepare_weights_mxfp8(const void* w13, const void* w2, int d, int I, int E,
+                              uint8_t* w13_codes, uint8_t* w13_scales, uint8_t* w2_codes,
+                              uint8_t* w2_scales, void* stream) {
+  if (!w13 || !w2 || !w13_codes || !w13_scales || !w2_codes || !w2_scales) return MOE_ERR_INVALID_ARG;
+  if (d <= 0 || I <= 0 || E <= 0 || d % 128 || I % 128) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w13) || !aligned16(w2) || !aligned16(w13_codes) || !aligned16(w2_codes))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_quant_tiled(w13, (long long)E * 2 * I, d, I, w13_codes, w13_scales, st);
+  if (e != cudaSuccess) return cuda_status(e);
+  return cuda_status(launch_quant_tiled(w2, (long long)E * d, I, 0, w2_codes, w2_scales, st));
+}
+
 int moe_plan_set_timing_events(moe_plan* p, int which, void* const* events, int n) {
   if (!p || which < 0 || which > 1 || n < 0) return MOE_ERR_INVALID_ARG;
   if (n > 0 && events && n < (which == 0 ? 6 : 7)) return MOE_ERR_INVALID_ARG;
@@ -554,6 +664,10 @@ int moe_plan_buffer(const moe_plan* p, int which, void** ptr, size_t* bytes) {
     case MOE_BUF_DA: q = p->dA; b = 2 * RP * 2 * I; break;
     case MOE_BUF_HS: q = p->hs; b = 2 * RP * I; break;
     case MOE_BUF_DXE: q = p->dxe; b = 2 * RP * d; break;
+    case MOE_BUF_XQ: q = p->xq; b = RP * d; break;
+    case MOE_BUF_XSF: q = p->xsf; b = (size_t)mx_sf_bytes((long long)RP, (int)d); break;
+    case MOE_BUF_HQ: q = p->hq; b = RP * I; break;
+    case MOE_BUF_HSF: q = p->hsf; b = (size_t)mx_sf_bytes((long long)RP, (int)I); break;
     default: return MOE_ERR_INVALID_ARG;
   }
   if (!q) return MOE_ERR_WORKSPACE;

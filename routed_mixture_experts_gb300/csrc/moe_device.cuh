@@ -224,6 +224,109 @@ __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// D[tmem] (+)= (A . 2^sfa) * (B . 2^sfb)^T, kind::mxf8f6f4 with one E8M0 scale per
+// 32 K-elements of each row (block_scale.scale_vec::1X); scales read from TMEM.
+__device__ __forceinline__ void umma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Copy a 32-row x 16-byte matrix from shared memory (descriptor) into TMEM lanes
+// 0..31 of every lane quarter (replicated x4), four 32-bit columns at taddr: the
+// placement block-scaled MMAs read their scale factors from.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+// Contiguous global -> shared bulk copy (size and addresses multiples of 16 bytes).
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor without swizzle (K-major core matrices of
+// 8 rows x 16 bytes; sbo = stride between 8-row groups, lbo = between K chunks).
+__device__ __forceinline__ uint64_t smem_desc_noswz(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+
+// Instruction descriptor, kind::mxf8f6f4 block-scaled: E4M3 A and B, fp32 D,
+// E8M0 scales; the scale bytes used are selected by sfa_id / sfb_id (0..3)
+// within the 32-bit TMEM scale column.
+//   bits 4-5 B scale id   bits 7-9 A format (0 = E4M3)   bits 10-12 B format
+//   bits 17-22 N >> 3     bit 23 scale format (1 = E8M0)  bits 24-28 M >> 4
+//   bits 29-30 A scale id
+__host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N) {
+  return ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ uint32_t idesc_sf_ids(uint32_t base, uint32_t sfa_id, uint32_t sfb_id) {
+  return base | (sfb_id << 4) | (sfa_id << 29);
+}
+
+// ---------------------------------------------------------------------------
+// MXFP8 block quantisation (OCP MX: 32 elements, E8M0 shared exponent,
+// X = floor(log2 amax) - 8 clamped to [-127,127], E4M3 elements RNE saturating).
+
+// Two floats -> two E4M3 bytes (lo in bits 0-7), round to nearest even, saturating.
+__device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// E8M0 exponent X of a block from its amax (>= 0).
+__device__ __forceinline__ int mx_block_exponent(float amax) {
+  const int ef = (int)((__float_as_uint(amax) >> 23) & 0xFF);   // biased exponent
+  if (ef == 0) return -127;                                    // zero or subnormal
+  const int X = ef - 127 - 8;
+  return X < -127 ? -127 : (X > 127 ? 127 : X);
+}
+
+// Quantise 32 values (exact bf16 values held as float): 32 code bytes into
+// out[0..7] (little-endian words) and the scale byte as the return value.
+__device__ __forceinline__ uint8_t mx_quant32(const float (&f)[32], uint32_t (&out)[8]) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  if (!(amax > 0.f)) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) out[q] = 0u;
+    return 0;
+  }
+  const int X = mx_block_exponent(amax);
+  const float inv = __uint_as_float((uint32_t)(127 - X) << 23);   // 2^-X, exact
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const uint16_t p0 = cvt_e4m3x2(f[4 * q] * inv, f[4 * q + 1] * inv);
+    const uint16_t p1 = cvt_e4m3x2(f[4 * q + 2] * inv, f[4 * q + 3] * inv);
+    out[q] = (uint32_t)p0 | ((uint32_t)p1 << 16);
+  }
+  return (uint8_t)(X + 127);
+}
+
+// Byte offset of the scale of (row, 32-block kb) in the tiled scale layout the
+// MXFP8 GEMMs read: rows in blocks of 128, K in groups of 128 elements (four
+// 32-blocks); each (row block, K group) is a contiguous 512-byte chunk in which
+// row r (0..127) and block j (0..3) sit at byte 16*(r%32) + 4*(r/32) + j, so one
+// 32 x 16-byte copy places row r's four scales in TMEM lane r%32, column r/32.
+__host__ __device__ __forceinline__ long long mx_sf_offset(long long rblock, int rin, int kb,
+                                                            int ngroups) {
+  return (rblock * ngroups + (kb >> 2)) * 512 + (rin & 31) * 16 + (rin >> 5) * 4 + (kb & 3);
+}
+
 // Shared-memory matrix descriptor for tcgen05.mma (128-byte swizzle).
 //   bits  0-13 start address >> 4     bits 16-29 leading byte offset >> 4
 //   bits 32-45 stride byte offset >> 4 bits 46-47 descriptor version (1)

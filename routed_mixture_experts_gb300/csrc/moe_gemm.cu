@@ -129,6 +129,49 @@ __device__ __forceinline__ void load16_bf16(const uint16_t* src, float (&v)[16])
 // epilogues: one thread owns one output row (`row` within the tile) and reads
 // its accumulator columns from TMEM at `tbase` (lane quarter already folded in).
 
+// MXFP8 W13 epilogue: like the bf16 one (R1, SwiGLU, R2), then h is quantised
+// along I in 32-column blocks (codes to a.hq, tiled E8M0 scales to a.hsf) as the
+// A operand of the block-scaled W2 GEMM; the bf16 h is kept for inspection.
+template <int BN>
+__device__ __forceinline__ void epilogue_swiglu_mx(const GemmArgs& a, const TileInfo& ti, int row,
+                                                   uint32_t tbase) {
+  constexpr int BNH = BN / 2;
+  const long long grow = (long long)ti.m0 + row;
+  const int c0 = ti.nt * BNH;
+  uint16_t* h = static_cast<uint16_t*>(a.out0) + grow * a.ld0 + c0;
+  uint8_t* hq = a.hq + grow * a.ld0 + c0;
+  uint32_t g0[16], g1[16], u0[16], u1[16];
+#pragma unroll 1
+  for (int c = 0; c < BNH; c += 32) {
+    tmem_ld16(tbase + c, g0);
+    tmem_ld16(tbase + c + 16, g1);
+    tmem_ld16(tbase + BNH + c, u0);
+    tmem_ld16(tbase + BNH + c + 16, u1);
+    tmem_ld_wait();
+    float hv[32];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const float G0 = bf2f(f2bf(__uint_as_float(g0[q]))), U0 = bf2f(f2bf(__uint_as_float(u0[q])));
+      const float G1 = bf2f(f2bf(__uint_as_float(g1[q]))), U1 = bf2f(f2bf(__uint_as_float(u1[q])));
+      hv[q] = bf2f(f2bf(swiglu_fwd(G0, U0, a.clamp)));            // R2
+      hv[16 + q] = bf2f(f2bf(swiglu_fwd(G1, U1, a.clamp)));
+    }
+    float lo[16], hi[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      lo[q] = hv[q];
+      hi[q] = hv[16 + q];
+    }
+    store16_bf16(h + c, lo);
+    store16_bf16(h + c + 16, hi);
+    uint32_t w[8];
+    const uint8_t sc = mx_quant32(hv, w);
+    reinterpret_cast<uint4*>(hq + c)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    reinterpret_cast<uint4*>(hq + c)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    a.hsf[mx_sf_offset(grow >> 7, (int)(grow & 127), (c0 + c) >> 5, a.hsf_ngr)] = sc;
+  }
+}
+
 template <int BN, int EPI>
 __device__ __forceinline__ void epilogue(const GemmArgs& a, const TileInfo& ti, int row,
                                          uint32_t tbase) {
@@ -269,28 +312,38 @@ __device__ __forceinline__ void epilogue_wgrad(const GemmArgs& a, const CUtensor
   }
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool MX>
 struct GemmShape {
-  static constexpr int A_BYTES = kBM * kBK * 2;                // 16 KB
-  static constexpr int B_BYTES = BN * kBK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  // A stage holds 128 rows (A) and BN rows (B) of 128 bytes of K: 64 bf16 or
+  // 128 E4M3 elements; MXFP8 stages also carry the 512-byte scale chunks of A
+  // and of B for those 128 K-elements (padded to keep stages 1024-aligned).
+  static constexpr int A_BYTES = kBM * 128;                    // 16 KB
+  static constexpr int B_BYTES = BN * 128;
+  static constexpr int SF_STAGE_BYTES = MX ? 1024 : 0;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SF_STAGE_BYTES;
   // WGRAD keeps 64 KB for its four fp32 staging buffers and needs few stages
   // (its K loop is one expert's rows and it is bound by the gradient traffic).
-  static constexpr int STAGE_BUDGET = EPI == EPI_WGRAD ? 144 * 1024 : 196 * 1024;
-  static constexpr int STAGES = STAGE_BUDGET / STAGE_BYTES > 8 ? 8 : STAGE_BUDGET / STAGE_BYTES;
   static constexpr int OUT_BYTES = EPI == EPI_WGRAD ? 4 * 16384 : 0;
+  static constexpr int STAGE_BUDGET = 208 * 1024 - OUT_BYTES;
+  static constexpr int STAGES = STAGE_BUDGET / STAGE_BYTES > 8 ? 8 : STAGE_BUDGET / STAGE_BYTES;
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + OUT_BYTES + BAR_BYTES + 1024;
-  static constexpr uint32_t TMEM_COLS = 2 * BN;
+  // accumulators (2 x BN columns), then for MXFP8 eight scale columns per stage
+  // (4 for A, 4 for B)
+  static constexpr uint32_t SF_COL0 = 2 * BN;
+  static constexpr uint32_t TMEM_COLS = MX ? 512 : 2 * BN;
+  static_assert(!MX || SF_COL0 + 8 * STAGES <= 512, "TMEM budget");
 };
 
-template <int BN, bool A_MN, bool B_MN, int EPI>
+template <int BN, bool A_MN, bool B_MN, int EPI, bool MX>
 __global__ void __launch_bounds__(kThreads, 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
-  using S = GemmShape<BN, EPI>;
+  using S = GemmShape<BN, EPI, MX>;
   constexpr int STAGES = S::STAGES;
-  constexpr uint32_t IDESC = idesc_bf16(kBM, BN, A_MN, B_MN);
+  constexpr uint32_t IDESC = MX ? idesc_mxf8(kBM, BN) : idesc_bf16(kBM, BN, A_MN, B_MN);
+  constexpr int KE = MX ? 128 : kBK;     // K elements per stage (128 bytes per row)
+  static_assert(!MX || (!A_MN && !B_MN && BN == 128), "MXFP8: K-major operands, BN = 128");
   static_assert(S::SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
 
@@ -346,6 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = tmem_holder;
   const uint32_t stage0 = smem_u32(smem);
 
+
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     int stage = 0;
@@ -366,15 +420,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sa = stage0 + stage * S::STAGE_BYTES;
           const uint32_t sb = sa + S::A_BYTES;
           mbar_arrive_expect_tx(fb, S::STAGE_BYTES);
+          if constexpr (MX) {
+            // the 512-byte scale chunks of this K group: A's row block, B's row block
+            const uint32_t ssf = sb + S::B_BYTES;
+            const long long ga = ((long long)(ti.m0 >> 7) * args.sf_ngr + kb) * 512;
+            const long long gb =
+                (((long long)ti.e * args.b_blocks_per_expert + ti.nt) * args.sf_ngr + kb) * 512;
+            bulk_g2s(ssf, args.sfa + ga, 512u, fb);
+            bulk_g2s(ssf + 512u, args.sfb + gb, 512u, fb);
+          }
           // A: 128 rows x 64 K
           if (A_MN) {
             // tensor [rows(K), M]: boxes cover 64 M columns x 64 K rows
             tma_load_2d(sa, &tmA, ti.m0, ti.krow0 + kb * kBK, fb);
             tma_load_2d(sa + kBoxBytes, &tmA, ti.m0 + 64, ti.krow0 + kb * kBK, fb);
           } else {
-            // tensor [rows, K]: boxes cover 64 K columns x 64 rows
-            tma_load_2d(sa, &tmA, kb * kBK, ti.m0, fb);
-            tma_load_2d(sa + kBoxBytes, &tmA, kb * kBK, ti.m0 + 64, fb);
+            // tensor [rows, K]: boxes cover 128 bytes of K x 64 rows
+            tma_load_2d(sa, &tmA, kb * KE, ti.m0, fb);
+            tma_load_2d(sa + kBoxBytes, &tmA, kb * KE, ti.m0 + 64, fb);
           }
           // B: BN rows (N) x 64 K
 #pragma unroll
@@ -392,10 +455,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int bi = b - half * NB2;
               const int row = ti.e * args.b_expert_rows + half * args.b_half_rows +
                               ti.nt * (BN / 2) + 64 * bi;
-              tma_load_2d(sb + b * kBoxBytes, &tmB, kb * kBK, row, fb);
+              tma_load_2d(sb + b * kBoxBytes, &tmB, kb * KE, row, fb);
             } else {
               // tensor [E*N, K]
-              tma_load_2d(sb + b * kBoxBytes, &tmB, kb * kBK,
+              tma_load_2d(sb + b * kBoxBytes, &tmB, kb * KE,
                           ti.e * args.b_expert_rows + ti.n0 + 64 * b, fb);
             }
           }
@@ -450,6 +513,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           const uint32_t sa = stage0 + stage * S::STAGE_BYTES;
           const uint32_t sb = sa + S::A_BYTES;
+          if constexpr (MX) {
+            // this stage's scales -> its own 8 TMEM columns (reused only after the
+            // stage is released, i.e. after these MMAs have completed); then four
+            // 32-element K steps, step j reading scale byte j
+            const uint32_t ssf = sb + S::B_BYTES;
+            const uint32_t sfa_t = tmem_base + S::SF_COL0 + 8u * (uint32_t)stage;
+            const uint32_t sfb_t = sfa_t + 4u;
+            tmem_cp_32x128b_x4(sfa_t, smem_desc_noswz(ssf, 512u, 128u));
+            tmem_cp_32x128b_x4(sfb_t, smem_desc_noswz(ssf + 512u, 512u, 128u));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint64_t adesc = smem_desc_sw128(sa + j * 32, 16, 1024);
+              const uint64_t bdesc = smem_desc_sw128(sb + j * 32, 16, 1024);
+              umma_mxf8(d_tmem, adesc, bdesc, idesc_sf_ids(IDESC, (uint32_t)j, (uint32_t)j),
+                        sfa_t, sfb_t, (kb | j) != 0 ? 1u : 0u);
+            }
+          } else {
 #pragma unroll
           for (int k16 = 0; k16 < kBK / 16; ++k16) {
             // K-major: rows of 128 B, 8-row groups 1024 B apart; K step = 32 B.
@@ -460,6 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bdesc = B_MN ? smem_desc_sw128(sb + k16 * 2048, 8192, 1024)
                                         : smem_desc_sw128(sb + k16 * 32, 16, 1024);
             umma_f16(d_tmem, adesc, bdesc, IDESC, (kb | k16) != 0 ? 1u : 0u);
+          }
           }
           umma_commit(empty_bar(stage));
         }
@@ -504,6 +585,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
       if constexpr (EPI == EPI_WGRAD)
         epilogue_wgrad<BN>(args, &tmC, ti, row, tbase, stage0 + STAGES * S::STAGE_BYTES, et, sub);
+      else if constexpr (MX && EPI == EPI_SWIGLU)
+        epilogue_swiglu_mx<BN>(args, ti, row, tbase);
       else
         epilogue<BN, EPI>(args, ti, row, tbase);
       tc_fence_before();
@@ -522,11 +605,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN, bool A_MN, bool B_MN, int EPI>
+template <int BN, bool A_MN, bool B_MN, int EPI, bool MX>
 cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                        const GemmArgs& args, int grid, cudaStream_t stream) {
-  auto kern = k_grouped_gemm<BN, A_MN, B_MN, EPI>;
-  const int smem = GemmShape<BN, EPI>::SMEM_BYTES;
+  auto kern = k_grouped_gemm<BN, A_MN, B_MN, EPI, MX>;
+  const int smem = GemmShape<BN, EPI, MX>::SMEM_BYTES;
   static bool configured = false;   // attribute set once per process (same device image)
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -541,10 +624,17 @@ cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUten
 
 cudaError_t launch_gemm(int epi, int bn, bool a_mn, bool b_mn, const CUtensorMap& ta,
                         const CUtensorMap& tb, const CUtensorMap& tc, const GemmArgs& args,
-                        int grid, cudaStream_t stream) {
+                        int grid, cudaStream_t stream, bool mx) {
+  if (mx) {
+    if (epi == EPI_SWIGLU && bn == 128 && !a_mn && !b_mn)
+      return launch_one<128, false, false, EPI_SWIGLU, true>(ta, tb, tc, args, grid, stream);
+    if (epi == EPI_SCORE && bn == 128 && !a_mn && !b_mn)
+      return launch_one<128, false, false, EPI_SCORE, true>(ta, tb, tc, args, grid, stream);
+    return cudaErrorInvalidValue;
+  }
 #define MOE_CASE(EPI_, BN_, AMN_, BMN_)                                     \
   if (epi == EPI_ && bn == BN_ && a_mn == AMN_ && b_mn == BMN_)             \
-    return launch_one<BN_, AMN_, BMN_, EPI_>(ta, tb, tc, args, grid, stream);
+    return launch_one<BN_, AMN_, BMN_, EPI_, false>(ta, tb, tc, args, grid, stream);
   MOE_CASE(EPI_SWIGLU, 128, false, false)
   MOE_CASE(EPI_SWIGLU, 256, false, false)
   MOE_CASE(EPI_SCORE, 128, false, false)

@@ -54,6 +54,14 @@ struct GemmArgs {
   float clamp;               // SwiGLU limit (0 = plain)
   int I;                     // column offset of the up half in a / dA
   int save;                  // EPI_SWIGLU: store a
+  // MXFP8 (block-scaled) operands: tiled E8M0 scales (see mx_sf_offset)
+  const uint8_t* sfa;        // scales of A, row blocks of 128 padded rows
+  const uint8_t* sfb;        // scales of B, row block = e * b_blocks_per_expert + n tile
+  int sf_ngr;                // 128-element K groups (512-byte scale chunks) per row block
+  int b_blocks_per_expert;
+  uint8_t* hq;               // EPI_SWIGLU (MXFP8): h quantised along I, codes [rows, I]
+  uint8_t* hsf;              // ... and its tiled scales
+  int hsf_ngr;
   DevError* err;
 };
 
@@ -70,7 +78,11 @@ int encode_tmap_f32_out(CUtensorMap* map, const void* base, long long rows, long
 // read by EPI_WGRAD (the fp32 gradient [E*M, N]).
 cudaError_t launch_gemm(int epi, int bn, bool a_mn, bool b_mn, const CUtensorMap& ta,
                         const CUtensorMap& tb, const CUtensorMap& tc, const GemmArgs& args,
-                        int grid, cudaStream_t stream);
+                        int grid, cudaStream_t stream, bool mx = false);
+
+// 2-D uint8 tensor map (row-major [rows, cols]) with a 128-byte x 64-row box and
+// 128-byte swizzle: the E4M3 operand box of the MXFP8 GEMMs.
+int encode_tmap_u8(CUtensorMap* map, const void* base, long long rows, long long cols);
 
 // Dispatch kernels.
 struct RouteArgs {
@@ -105,5 +117,19 @@ cudaError_t launch_combine(const void* rows, const int32_t* row_of, int T, int k
 
 cudaError_t launch_quant_mxfp8(const void* in, long long rows, int K, uint8_t* codes,
                                uint8_t* scales, cudaStream_t stream);
+
+// Bytes of the tiled MXFP8 scale layout for `rows_padded128` rows (a multiple of
+// 128) and K columns (a multiple of 128): rows/128 x K/128 chunks of 512 bytes.
+long long mx_sf_bytes(long long rows_padded128, int K);
+
+// Quantise [rows, K] bf16 to E4M3 codes plus tiled E8M0 scales; gu_I > 0 blocks
+// the rows of W13 [E*2I, K] by (expert, 64-column gate/up n-tile).
+cudaError_t launch_quant_tiled(const void* in, long long rows, int K, int gu_I, uint8_t* codes,
+                               uint8_t* sf, cudaStream_t stream);
+
+// Padded rows r < *nrows: quantise x[token_of[r]] (zero for padding) along d.
+cudaError_t launch_gather_quant_rows(const void* x, const int32_t* token_of, const int32_t* nrows,
+                                     int d, uint8_t* codes, uint8_t* sf, int grid,
+                                     cudaStream_t stream);
 
 }  // namespace moe

@@ -15,21 +15,6 @@ namespace moe {
 
 namespace {
 
-// Two floats -> two E4M3 bytes (lo in bits 0-7), RNE, saturating.
-__device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-// E8M0 exponent X of a block from its (non-negative) bf16-exact amax.
-__device__ __forceinline__ int block_exponent(float amax) {
-  const int ef = (int)((__float_as_uint(amax) >> 23) & 0xFF);   // biased exponent
-  if (ef == 0) return -127;                                    // zero or subnormal
-  const int X = ef - 127 - 8;
-  return X < -127 ? -127 : (X > 127 ? 127 : X);
-}
-
 // One thread per 32-element block.
 __global__ void __launch_bounds__(256) k_quant_mxfp8(const uint4* __restrict__ in, long long nblocks,
                                                      uint4* __restrict__ codes,
@@ -49,31 +34,129 @@ __global__ void __launch_bounds__(256) k_quant_mxfp8(const uint4* __restrict__ i
         f[i * 8 + 2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
       }
     }
-    float amax = 0.f;
+    uint32_t w[8];
+    const uint8_t sc = mx_quant32(f, w);
+    codes[b * 2] = make_uint4(w[0], w[1], w[2], w[3]);
+    codes[b * 2 + 1] = make_uint4(w[4], w[5], w[6], w[7]);
+    scales[b] = sc;
+  }
+}
+
+__device__ __forceinline__ void unpack_bf16x32(const uint4 (&v)[4], float (&f)[32]) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
-    uint4 out0 = make_uint4(0, 0, 0, 0), out1 = make_uint4(0, 0, 0, 0);
-    int X = -127;
-    if (amax > 0.f) {
-      X = block_exponent(amax);
-      const float inv = __uint_as_float((uint32_t)(127 - X) << 23);   // 2^-X, exact
-      uint32_t w[8];
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const uint16_t p0 = cvt_e4m3x2(f[4 * q] * inv, f[4 * q + 1] * inv);
-        const uint16_t p1 = cvt_e4m3x2(f[4 * q + 2] * inv, f[4 * q + 3] * inv);
-        w[q] = (uint32_t)p0 | ((uint32_t)p1 << 16);
-      }
-      out0 = make_uint4(w[0], w[1], w[2], w[3]);
-      out1 = make_uint4(w[4], w[5], w[6], w[7]);
+    for (int q = 0; q < 4; ++q) {
+      f[i * 8 + 2 * q] = __uint_as_float(w[q] << 16);
+      f[i * 8 + 2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
     }
-    codes[b * 2] = out0;
-    codes[b * 2 + 1] = out1;
-    scales[b] = (uint8_t)(X + 127);
+  }
+}
+
+// Quantise [rows, K] bf16 into codes [rows, K] and scales in the tiled layout
+// (moe::mx_sf_offset).  gu_I > 0 selects the W13 row blocking: within each
+// expert's 2I rows, gate rows [64t, 64t+64) and up rows [I+64t, I+64t+64) form
+// row block e*(I/64)+t (the B tile of one 64-column W13 n-tile); gu_I == 0 uses
+// plain 128-row blocks.
+__global__ void __launch_bounds__(256) k_quant_tiled(const uint4* __restrict__ in, long long rows,
+                                                     int K, int gu_I, uint4* __restrict__ codes,
+                                                     uint8_t* __restrict__ sf) {
+  const int kbs = K / 32;
+  const int ngr = K / 128;
+  const long long nblocks = rows * kbs;
+  for (long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x; b < nblocks;
+       b += (long long)gridDim.x * blockDim.x) {
+    const long long row = b / kbs;
+    const int kb = (int)(b - row * kbs);
+    uint4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = in[b * 4 + i];
+    float f[32];
+    unpack_bf16x32(v, f);
+    uint32_t w[8];
+    const uint8_t sc = mx_quant32(f, w);
+    codes[b * 2] = make_uint4(w[0], w[1], w[2], w[3]);
+    codes[b * 2 + 1] = make_uint4(w[4], w[5], w[6], w[7]);
+    long long rblock;
+    int rin;
+    if (gu_I > 0) {
+      const long long e = row / (2 * gu_I);
+      const int i = (int)(row - e * 2 * gu_I);
+      const int up = i >= gu_I;
+      const int ii = up ? i - gu_I : i;
+      rblock = e * (gu_I / 64) + ii / 64;
+      rin = up * 64 + (ii & 63);
+    } else {
+      rblock = row >> 7;
+      rin = (int)(row & 127);
+    }
+    sf[mx_sf_offset(rblock, rin, kb, ngr)] = sc;
+  }
+}
+
+// Gather + quantise: padded row r of the expert-major activations is token
+// token_of[r] of x (zero where token_of[r] < 0), quantised along d.  One warp
+// per row, one 32-element block per lane per pass.
+__global__ void __launch_bounds__(256) k_gather_quant_rows(const uint4* __restrict__ x,
+                                                           const int32_t* __restrict__ token_of,
+                                                           const int32_t* __restrict__ nrows_p,
+                                                           int d, uint4* __restrict__ codes,
+                                                           uint8_t* __restrict__ sf) {
+  const int nrows = *nrows_p;
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  const int kbs = d / 32;
+  const int ngr = d / 128;
+  for (int r = gw; r < nrows; r += nw) {
+    const int t = token_of[r];
+    for (int kb = lane; kb < kbs; kb += 32) {
+      float f[32];
+      if (t >= 0) {
+        uint4 v[4];
+        const uint4* src = x + ((long long)t * d + kb * 32) / 8;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = src[i];
+        unpack_bf16x32(v, f);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) f[i] = 0.f;
+      }
+      uint32_t w[8];
+      const uint8_t sc = mx_quant32(f, w);
+      uint4* dst = codes + ((long long)r * d + kb * 32) / 16;
+      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      sf[mx_sf_offset(r >> 7, r & 127, kb, ngr)] = sc;
+    }
   }
 }
 
 }  // namespace
+
+long long mx_sf_bytes(long long rows_padded128, int K) {
+  return rows_padded128 / 128 * (long long)(K / 128) * 512;
+}
+
+cudaError_t launch_quant_tiled(const void* in, long long rows, int K, int gu_I, uint8_t* codes,
+                               uint8_t* sf, cudaStream_t stream) {
+  const long long nblocks = rows * (K / 32);
+  long long grid = (nblocks + 255) / 256;
+  if (grid > 65535LL * 8) grid = 65535LL * 8;
+  if (grid < 1) grid = 1;
+  k_quant_tiled<<<(unsigned)grid, 256, 0, stream>>>(static_cast<const uint4*>(in), rows, K, gu_I,
+                                                   reinterpret_cast<uint4*>(codes), sf);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_quant_rows(const void* x, const int32_t* token_of, const int32_t* nrows,
+                                     int d, uint8_t* codes, uint8_t* sf, int grid,
+                                     cudaStream_t stream) {
+  k_gather_quant_rows<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x), token_of, nrows, d,
+                                               reinterpret_cast<uint4*>(codes), sf);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_quant_mxfp8(const void* in, long long rows, int K, uint8_t* codes,
                                uint8_t* scales, cudaStream_t stream) {

@@ -1,0 +1,131 @@
+"""MXFP8 E4M3 forward through the C ABI against the oracle.
+
+Prepared weight codes and scales, and the quantised routed activations, must
+match the oracle's quantiser bit for bit (the scales after undoing the tiled
+layout); the output must be within relative Frobenius error 1e-2 of the
+oracle's MXFP8 forward, which quantises the same way (tests/parity.py).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_case import bits, to_dev
+from parity import REL_FRO_MXFP8, compare, f32
+import moe_inputs as mi
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from routed_mixture_experts_gb300 import build
+
+    build.build()
+    import routed_mixture_experts_gb300 as m
+
+    return m
+
+
+def untile(sf, rows, K, gu_I=0):
+    """Tiled scale bytes -> [rows, K/32] (inverse of the documented layout)."""
+    kbs = K // 32
+    ngr = K // 128
+    r = np.arange(rows)
+    if gu_I:
+        e, i = r // (2 * gu_I), r % (2 * gu_I)
+        up = i >= gu_I
+        ii = np.where(up, i - gu_I, i)
+        blk, rin = e * (gu_I // 64) + ii // 64, up * 64 + ii % 64
+    else:
+        blk, rin = r // 128, r % 128
+    kb = np.arange(kbs)
+    off = ((blk[:, None] * ngr + kb[None, :] // 4) * 512 + (rin[:, None] % 32) * 16
+           + (rin[:, None] // 32) * 4 + kb[None, :] % 4)
+    return sf[off]
+
+
+def prepared(moe, dev):
+    w13q, w13s, w2q, w2s = moe.prepare_weights_mxfp8(dev["w13"], dev["w2"])
+    torch.cuda.synchronize()
+    return w13q, w13s, w2q, w2s
+
+
+def run_mx(moe, inp, dev, prep):
+    c = inp["cfg"]
+    plan = moe.MoePlan(c["T"], c["d"], c["I"], c["E"], c["k"], precision=moe.MOE_PREC_MXFP8,
+                       clamp=c.get("clamp", 0.0), flags=0)
+    w13q, w13s, w2q, w2s = prep
+    y = plan.forward(dev["x"], dev["ids"], dev["scores"], w13q, w2q, w13_sf=w13s, w2_sf=w2s)
+    torch.cuda.synchronize()
+    rc, det = plan.check()
+    assert rc == 0, (rc, det)
+    return plan, y
+
+
+@pytest.mark.parametrize("sizes", [
+    dict(T=64, d=128, I=128, E=4, k=2),
+    dict(T=300, d=256, I=256, E=7, k=3),
+    dict(T=200, d=384, I=128, E=9, k=2, clamp=1.0, pad=30),
+])
+def test_mxfp8_small(moe, orc, sizes):
+    inp = mi.make_inputs(None, seed=21, need=("x", "ids", "scores", "w13", "w2"), **sizes)
+    c = inp["cfg"]
+    T, d, I, E, k = c["T"], c["d"], c["I"], c["E"], c["k"]
+    dev = to_dev(inp)
+    prep = prepared(moe, dev)
+    # prepared weights: bit-exact against the oracle's quantiser
+    oq13, os13 = orc.quant_mxfp8(inp["w13"])
+    oq2, os2 = orc.quant_mxfp8(inp["w2"])
+    assert np.array_equal(prep[0].cpu().numpy(), oq13)
+    assert np.array_equal(prep[2].cpu().numpy(), oq2)
+    assert np.array_equal(untile(prep[1].cpu().numpy(), E * 2 * I, d, gu_I=I),
+                          os13.reshape(E * 2 * I, d // 32))
+    assert np.array_equal(untile(prep[3].cpu().numpy(), E * d, I), os2.reshape(E * d, I // 32))
+    plan, y = run_mx(moe, inp, dev, prep)
+    # quantised routed activations: bit-exact (padding rows zero)
+    op = plan.buffer("off_pad", torch.int32).cpu().numpy()
+    n = int(op[-1])
+    tok = plan.buffer("token_of", torch.int32).cpu().numpy()[:n]
+    xrows = orc.gather_rows(inp["x"], tok)
+    qx, sx = orc.quant_mxfp8(xrows)
+    gq = plan.buffer("xq", torch.uint8).cpu().numpy()[: n * d].reshape(n, d)
+    assert np.array_equal(gq, qx)
+    gs = untile(plan.buffer("xsf", torch.uint8).cpu().numpy(), n, d)
+    assert np.array_equal(gs, sx)
+    # output
+    yref, href = orc.forward_mxfp8(inp["x"], inp["ids"], inp["scores"], oq13, os13, oq2, os2,
+                                   clamp=c.get("clamp", 0.0), return_h=True)
+    compare(f32(bits(y)), f32(yref), bf16_out=True, rel_fro=REL_FRO_MXFP8, what="y mxfp8",
+            max_bad_frac=1.0)
+    ro = plan.buffer("row_of", torch.int32).cpu().numpy()[: T * k].reshape(T, k)
+    h = bits(plan.buffer("h", torch.bfloat16).view(-1, I))
+    ok = ro >= 0
+    compare(f32(h[ro[ok]]), f32(href[ok]), what="h mxfp8", max_bad_frac=1e-3)
+
+
+def test_mxfp8_full_size_sampled(moe, orc):
+    inp = mi.make_inputs("mxfp8_e128", need=("x", "ids", "scores", "w13", "w2"))
+    c = inp["cfg"]
+    dev = to_dev(inp)
+    prep = prepared(moe, dev)
+    plan, y = run_mx(moe, inp, dev, prep)
+    yb = f32(bits(y))
+    assert np.all(np.isfinite(yb))
+    toks = np.array([0, 4097, c["T"] - 1], np.int32)
+    experts = sorted(set(int(e) for e in inp["ids"][toks].reshape(-1)))
+    # the oracle quantises the weights of the experts these tokens use
+    I, d = c["I"], c["d"]
+    oq13 = np.zeros((c["E"], 2 * I, d), np.uint8)
+    os13 = np.zeros((c["E"], 2 * I, d // 32), np.uint8)
+    oq2 = np.zeros((c["E"], d, I), np.uint8)
+    os2 = np.zeros((c["E"], d, I // 32), np.uint8)
+    g13q = prep[0].cpu().numpy()
+    g13s = untile(prep[1].cpu().numpy(), c["E"] * 2 * I, d, gu_I=I).reshape(c["E"], 2 * I, d // 32)
+    for e in experts:
+        oq13[e], os13[e] = orc.quant_mxfp8(inp["w13"][e])
+        oq2[e], os2[e] = orc.quant_mxfp8(inp["w2"][e])
+        assert np.array_equal(g13q[e], oq13[e]) and np.array_equal(g13s[e], os13[e])
+    yref = orc.forward_mxfp8(inp["x"], inp["ids"], inp["scores"], oq13, os13, oq2, os2, toks=toks)
+    compare(yb[toks], f32(yref), bf16_out=True, rel_fro=REL_FRO_MXFP8, what="y mxfp8 full",
+            max_bad_frac=1.0)
