@@ -165,7 +165,7 @@ size_t layout(moe_plan* p, char* base, int flags) {
     p->dA = reinterpret_cast<uint16_t*>(take(2 * RP * 2 * I));
     p->hs = reinterpret_cast<uint16_t*>(take(2 * RP * I));
     p->dxe = reinterpret_cast<uint16_t*>(take(2 * RP * d));
-    p->pdscore = reinterpret_cast<float*>(take(4 * RP * (I / p->bnd2)));
+    p->pdscore = reinterpret_cast<float*>(take(4 * RP * 2 * (I / p->bnd2)));
   }
   p->st_x = p->st_dy = p->st_y = p->st_dx = nullptr;
   p->st_ids = nullptr;
@@ -525,7 +525,7 @@ int moe_backward(moe_plan* p, const void* dy, const void* w13, const void* w2, v
     mark(p, 1, 3, st);
   }
   // b4: combine dX and dscores
-  e = launch_combine(p->dxe, p->row_of, p->T, p->k, d, dx, p->pdscore, I / p->bnd2, dscores,
+  e = launch_combine(p->dxe, p->row_of, p->T, p->k, d, dx, p->pdscore, 2 * (I / p->bnd2), dscores,
                      gather_grid(p), st);
   if (e != cudaSuccess) return cuda_status(e);
   p->launches += 1;

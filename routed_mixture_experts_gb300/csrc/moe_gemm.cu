@@ -10,11 +10,12 @@
 //   WGRAD      (fp32 in-place accumulation, "What it is selling")
 //
 // Tile: 128 rows (M) x BN columns (N), K in stages of 64 bf16 (one 128-byte
-// swizzle atom).  One CTA per SM, 6 warps:
+// swizzle atom).  One CTA per SM, 10 warps:
 //   warp 0      TMA producer (one lane issues)
 //   warp 1      TMEM allocator and MMA issuer (one lane issues)
-//   warps 2..5  epilogue: warp w reads TMEM lanes 32*(w%4)..+31, i.e. one output
-//               row per thread, through tcgen05.ld
+//   warps 2..9  epilogue: warp w reads TMEM lanes 32*(w%4)..+31, i.e. one output
+//               row per thread, through tcgen05.ld; warps 2..5 take the first
+//               half of the tile's columns, warps 6..9 the second
 // The accumulator is double buffered in TMEM (2 x BN fp32 columns) so the
 // epilogue of tile i overlaps the main loop of tile i+1.
 //
@@ -29,7 +30,10 @@ namespace moe {
 
 namespace {
 
-constexpr int kThreads = 192;
+// warp 0 TMA producer, warp 1 MMA issuer, warps 2..9 epilogue (two warps per
+// TMEM lane quarter, each taking half of the tile's columns)
+constexpr int kThreads = 320;
+constexpr int kEpiThreads = 256;
 constexpr int kBoxBytes = 64 * 64 * 2;  // every TMA box is 64 x 64 bf16 = 8 KB
 
 struct TileInfo {
@@ -81,13 +85,13 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
   return true;
 }
 
-// AND of `v` over the 128 epilogue threads (named barrier 1).
+// AND of `v` over the 256 epilogue threads (named barrier 1).
 __device__ __forceinline__ int epi_bar_and(int v) {
   int r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.s32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, 1, 128, p;\n\t"
+      "bar.red.and.pred q, 1, 256, p;\n\t"
       "selp.s32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
       : "r"(v)
@@ -134,15 +138,16 @@ __device__ __forceinline__ void load16_bf16(const uint16_t* src, float (&v)[16])
 // A operand of the block-scaled W2 GEMM; the bf16 h is kept for inspection.
 template <int BN>
 __device__ __forceinline__ void epilogue_swiglu_mx(const GemmArgs& a, const TileInfo& ti, int row,
-                                                   uint32_t tbase) {
+                                                   uint32_t tbase, int half) {
   constexpr int BNH = BN / 2;
+  constexpr int W = BNH / 2;             // columns of this thread's half
   const long long grow = (long long)ti.m0 + row;
   const int c0 = ti.nt * BNH;
   uint16_t* h = static_cast<uint16_t*>(a.out0) + grow * a.ld0 + c0;
   uint8_t* hq = a.hq + grow * a.ld0 + c0;
   uint32_t g0[16], g1[16], u0[16], u1[16];
 #pragma unroll 1
-  for (int c = 0; c < BNH; c += 32) {
+  for (int c = half * W; c < (half + 1) * W; c += 32) {
     tmem_ld16(tbase + c, g0);
     tmem_ld16(tbase + c + 16, g1);
     tmem_ld16(tbase + BNH + c, u0);
@@ -174,16 +179,18 @@ __device__ __forceinline__ void epilogue_swiglu_mx(const GemmArgs& a, const Tile
 
 template <int BN, int EPI>
 __device__ __forceinline__ void epilogue(const GemmArgs& a, const TileInfo& ti, int row,
-                                         uint32_t tbase) {
+                                         uint32_t tbase, int half) {
   const long long grow = (long long)ti.m0 + row;
   uint32_t r0[16], r1[16];
+  constexpr int W = BN / 2;              // columns of this thread's half (BN-wide epilogues)
   if constexpr (EPI == EPI_SWIGLU) {
     constexpr int BNH = BN / 2;          // gate columns [0,BNH), up columns [BNH,BN)
+    constexpr int WH = BNH / 2;
     const int c0 = ti.nt * BNH;          // first intermediate column of this tile
     uint16_t* h = static_cast<uint16_t*>(a.out0) + grow * a.ld0 + c0;
     uint16_t* av = static_cast<uint16_t*>(a.out1) + grow * a.ld1 + c0;
 #pragma unroll 1
-    for (int c = 0; c < BNH; c += 16) {
+    for (int c = half * WH; c < (half + 1) * WH; c += 16) {
       tmem_ld16(tbase + c, r0);
       tmem_ld16(tbase + BNH + c, r1);
       tmem_ld_wait();
@@ -204,7 +211,7 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, const TileInfo& ti, 
     const float s = a.row_scale[grow];
     uint16_t* out = static_cast<uint16_t*>(a.out0) + grow * a.ld0 + ti.n0;
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 16) {
+    for (int c = half * W; c < (half + 1) * W; c += 16) {
       tmem_ld16(tbase + c, r0);
       tmem_ld_wait();
       float v[16];
@@ -215,7 +222,7 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, const TileInfo& ti, 
   } else if constexpr (EPI == EPI_STORE) {
     uint16_t* out = static_cast<uint16_t*>(a.out0) + grow * a.ld0 + ti.n0;
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 16) {
+    for (int c = half * W; c < (half + 1) * W; c += 16) {
       tmem_ld16(tbase + c, r0);
       tmem_ld_wait();
       float v[16];
@@ -234,7 +241,7 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, const TileInfo& ti, 
     uint16_t* hsrow = static_cast<uint16_t*>(a.out1) + grow * a.ld1 + ti.n0;
     float part = 0.f;
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 16) {
+    for (int c = half * W; c < (half + 1) * W; c += 16) {
       tmem_ld16(tbase + c, r0);
       float hv[16], ag[16], au[16];
       load16_bf16(hrow + c, hv);
@@ -265,7 +272,8 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, const TileInfo& ti, 
       store16_bf16(darow + a.I + c, du);
       store16_bf16(hsrow + c, hs);
     }
-    a.pdscore[grow * a.n_tiles + ti.nt] = part;
+    // one partial per (n tile, column half), in column order
+    a.pdscore[grow * (2 * a.n_tiles) + 2 * ti.nt + half] = part;
   }
 }
 
@@ -278,32 +286,27 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, const TileInfo& ti, 
 template <int BN>
 __device__ __forceinline__ void epilogue_wgrad(const GemmArgs& a, const CUtensorMap* tmC,
                                                const TileInfo& ti, int row, uint32_t tbase,
-                                               uint32_t stage_smem, int et, int& sub) {
+                                               uint32_t stage_smem, int et, int half, int& sub) {
   if (ti.kb == 0) return;
   const int ybase = ti.e * a.m_tiles * kBM + ti.m0;
-  uint32_t r0[16], r1[16];
+  uint32_t r0[16];
 #pragma unroll 1
   for (int c = 0; c < BN; c += 32) {
     const uint32_t buf = stage_smem + (uint32_t)(sub & 3) * 16384u;
     if (et == 0) bulk_wait_read<3>();          // this buffer's previous add has read it
-    named_bar_sync(1, 128);
-    tmem_ld16(tbase + c, r0);
-    tmem_ld16(tbase + c + 16, r1);
+    named_bar_sync(1, kEpiThreads);
+    // this thread's half: 16 of the sub-tile's 32 columns (16-byte chunks 4h..4h+3)
+    tmem_ld16(tbase + c + 16 * half, r0);
     tmem_ld_wait();
     const uint32_t rbase = buf + (uint32_t)row * 128u;
     const uint32_t sw = (uint32_t)(row & 7);
 #pragma unroll
     for (int q = 0; q < 4; ++q)
-      st_shared_v4(rbase + (((uint32_t)q ^ sw) << 4), __uint_as_float(r0[4 * q]),
+      st_shared_v4(rbase + (((uint32_t)(q + 4 * half) ^ sw) << 4), __uint_as_float(r0[4 * q]),
                    __uint_as_float(r0[4 * q + 1]), __uint_as_float(r0[4 * q + 2]),
                    __uint_as_float(r0[4 * q + 3]));
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      st_shared_v4(rbase + (((uint32_t)(q + 4) ^ sw) << 4), __uint_as_float(r1[4 * q]),
-                   __uint_as_float(r1[4 * q + 1]), __uint_as_float(r1[4 * q + 2]),
-                   __uint_as_float(r1[4 * q + 3]));
     fence_proxy_async_smem();
-    named_bar_sync(1, 128);
+    named_bar_sync(1, kEpiThreads);
     if (et == 0) {
       tma_reduce_add_2d(tmC, buf, ti.n0 + c, ybase);
       bulk_commit();
@@ -375,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), 128);
+      mbar_init(tempty_bar(b), kEpiThreads);
     }
     mbar_init(drain_bar, 1);
     fence_mbar_init();
@@ -566,7 +569,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- epilogue (warps 2..5) ----------------
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
-    const int et = threadIdx.x - 64;          // 0..127 over the epilogue warps
+    const int et = threadIdx.x - 64;          // 0..255 over the epilogue warps
+    const int half = (warp - 2) >> 2;         // warps 2..5: columns' first half, 6..9: second
     int acc = 0;
     uint32_t acc_phase = 0;
     int sub = 0;                              // WGRAD staging-buffer sequence number
@@ -574,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const TileInfo ti = decode_tile<BN>(args, tile);
       int w = 1;
       if (lane == 0) w = mbar_wait(tfull_bar(acc), acc_phase, &abort_s, args.err, 5);
-      // all four epilogue warps leave together, so their named barriers stay matched
+      // all eight epilogue warps leave together, so their named barriers stay matched
       const int ok_warp = __shfl_sync(0xffffffffu, w, 0);
       if (EPI == EPI_WGRAD) {
         if (epi_bar_and(ok_warp) == 0) break;
@@ -584,11 +588,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
       if constexpr (EPI == EPI_WGRAD)
-        epilogue_wgrad<BN>(args, &tmC, ti, row, tbase, stage0 + STAGES * S::STAGE_BYTES, et, sub);
+        epilogue_wgrad<BN>(args, &tmC, ti, row, tbase, stage0 + STAGES * S::STAGE_BYTES, et, half,
+                           sub);
       else if constexpr (MX && EPI == EPI_SWIGLU)
-        epilogue_swiglu_mx<BN>(args, ti, row, tbase);
+        epilogue_swiglu_mx<BN>(args, ti, row, tbase, half);
       else
-        epilogue<BN, EPI>(args, ti, row, tbase);
+        epilogue<BN, EPI>(args, ti, row, tbase, half);
       tc_fence_before();
       mbar_arrive(tempty_bar(acc));
       acc ^= 1;

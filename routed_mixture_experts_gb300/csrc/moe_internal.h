@@ -50,7 +50,7 @@ struct GemmArgs {
   const void* in0; long long ldi0;
   const void* in1; long long ldi1;
   const float* row_scale;    // score of each padded row
-  float* pdscore;            // EPI_DGRAD2: [rows, n_tiles]
+  float* pdscore;            // EPI_DGRAD2: [rows, 2*n_tiles] (n tile, column half)
   float clamp;               // SwiGLU limit (0 = plain)
   int I;                     // column offset of the up half in a / dA
   int save;                  // EPI_SWIGLU: store a
