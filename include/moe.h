@@ -258,6 +258,19 @@ int moe_plan_buffer(const moe_plan* plan, int which, void** dev_ptr, size_t* byt
  */
 int moe_plan_set_timing_events(moe_plan* plan, int which, void* const* events, int n);
 
+/*
+ * Failure-path testing (the pages' kernels trap on fatal conditions, see
+ * "Caveats"; this library records errors instead).  wait_limit_ns > 0 makes
+ * every bounded device wait of this plan's GEMM kernels give up after that many
+ * nanoseconds (0 restores the default of 2 s); stall_w13 = 1 makes the MMA role
+ * of the W13 GEMM wait on a barrier that nothing arrives at, so that wait runs
+ * out: the kernel then records MOE_ERR_TIMEOUT (detail = the wait's site), stops
+ * every role, drains its outstanding copies and MMAs with bounded waits, frees
+ * its tensor memory and exits, leaving the CUDA context usable.  The outputs of
+ * such a call are not meaningful.  stall_w13 = 0 restores normal operation.
+ */
+int moe_plan_set_debug(moe_plan* plan, long long wait_limit_ns, int stall_w13);
+
 /* Number of kernels this plan has launched so far (all entry points). */
 long long moe_plan_launch_count(const moe_plan* plan);
 

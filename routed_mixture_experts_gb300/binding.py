@@ -56,6 +56,7 @@ def _declare(L):
     L.moe_gemm_scratch_bytes.restype = sz
     L.moe_gemm_bf16.argtypes = [i32, vp, vp, vp, i32, i32, i32, vp, vp]
     L.moe_plan_set_timing_events.argtypes = [vp, i32, ctypes.POINTER(vp), i32]
+    L.moe_plan_set_debug.argtypes = [vp, ctypes.c_longlong, i32]
     L.moe_mxfp8_weight_scale_bytes.argtypes = [i32, i32, i32, i32]
     L.moe_mxfp8_weight_scale_bytes.restype = sz
     L.moe_prepare_weights_mxfp8.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp, vp]
@@ -64,7 +65,7 @@ def _declare(L):
     for name in ("moe_plan_set_swiglu_clamp", "moe_plan_set_workspace", "moe_forward",
                  "moe_backward", "moe_step_host", "moe_quantize_mxfp8", "moe_plan_check",
                  "moe_plan_buffer", "moe_gemm_bf16", "moe_plan_set_timing_events",
-                 "moe_prepare_weights_mxfp8"):
+                 "moe_prepare_weights_mxfp8", "moe_plan_set_debug"):
         getattr(L, name).restype = i32
     return L
 
@@ -161,6 +162,11 @@ class MoePlan:
         self._ev = getattr(self, "_ev", {})
         self._ev[which] = (arr, events)          # keep the handles alive while set
         _check(lib().moe_plan_set_timing_events(self.ptr, which, arr, len(events)), "timing")
+
+    def set_debug(self, wait_limit_ns=0, stall_w13=False):
+        """Failure-path testing knobs (see moe_plan_set_debug in moe.h)."""
+        _check(lib().moe_plan_set_debug(self.ptr, int(wait_limit_ns), 1 if stall_w13 else 0),
+               "set_debug")
 
     def launch_count(self):
         return lib().moe_plan_launch_count(self.ptr)

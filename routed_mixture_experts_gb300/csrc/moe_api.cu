@@ -61,6 +61,9 @@ struct moe_plan {
   CUtensorMap tm_dw13, tm_dw2;
   const void *dw13_cached, *dw2_cached;
   int saved;
+  // failure-path testing knobs (moe_plan_set_debug)
+  long long dbg_wait_limit_ns;
+  int dbg_stall_w13;
   // optional stage events and the launch counter
   void* const* ev[2];
   int nev[2];
@@ -218,6 +221,7 @@ int refresh_weight_maps(moe_plan* p, const void* w13, const void* w2) {
 GemmArgs rows_args(const moe_plan* p) {
   GemmArgs g;
   memset(&g, 0, sizeof(g));
+  g.wait_limit_ns = (unsigned long long)p->dbg_wait_limit_ns;
   g.wgrad = 0;
   g.num_mtiles = p->num_mtiles;
   g.tile_expert = p->tile_expert;
@@ -230,6 +234,7 @@ GemmArgs rows_args(const moe_plan* p) {
 GemmArgs wgrad_args(const moe_plan* p) {
   GemmArgs g;
   memset(&g, 0, sizeof(g));
+  g.wait_limit_ns = (unsigned long long)p->dbg_wait_limit_ns;
   g.wgrad = 1;
   g.off_pad = p->off_pad;
   g.expert_order = p->expert_order;
@@ -262,6 +267,7 @@ int forward_mxfp8(moe_plan* p, const void* x, const uint8_t* w13_sf, const uint8
     g.out0 = p->h; g.ld0 = p->I;
     g.sfa = p->xsf; g.sfb = w13_sf; g.sf_ngr = p->ngr_d; g.b_blocks_per_expert = p->I / 64;
     g.hq = p->hq; g.hsf = p->hsf; g.hsf_ngr = p->ngr_I;
+    g.stall_mma = p->dbg_stall_w13;
     e = launch_gemm(EPI_SWIGLU, 128, false, false, p->tm_xq, p->tm_w13q, p->tm_xq, g, p->num_sms,
                     st, true);
     if (e != cudaSuccess) return cuda_status(e);
@@ -442,6 +448,7 @@ int moe_forward(moe_plan* p, const void* x, const int32_t* ids, const float* sco
     g.out0 = p->h; g.ld0 = p->I;
     g.out1 = p->a; g.ld1 = 2LL * p->I;
     g.save = save_for_backward ? 1 : 0;
+    g.stall_mma = p->dbg_stall_w13;
     e = launch_gemm(EPI_SWIGLU, p->bn13, false, false, p->tm_xe, p->tm_w13, p->tm_xe, g, p->num_sms, st);
     if (e != cudaSuccess) return cuda_status(e);
     p->launches += 1;
@@ -600,6 +607,13 @@ int moe_quantize_mxfp8(const void* in, long rows, int K, uint8_t* codes, uint8_t
     return MOE_ERR_INVALID_ARG;
   if (rows == 0) return MOE_OK;
   return cuda_status(launch_quant_mxfp8(in, rows, K, codes, scales, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_plan_set_debug(moe_plan* p, long long wait_limit_ns, int stall_w13) {
+  if (!p || wait_limit_ns < 0) return MOE_ERR_INVALID_ARG;
+  p->dbg_wait_limit_ns = wait_limit_ns;
+  p->dbg_stall_w13 = stall_w13 ? 1 : 0;
+  return MOE_OK;
 }
 
 size_t moe_mxfp8_weight_scale_bytes(int d, int I, int E, int which) {

@@ -86,14 +86,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Default limit of a bounded wait: 2 s, far beyond any legitimate wait.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
 // Wait for the phase of parity `parity` to complete.  Gives up after
 // `limit_ns` (or when another role has already given up and set *abort),
 // recording MOE_ERR_TIMEOUT; returns false in that case.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          DevError* err, int where) {
+                                          DevError* err, int where,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  const uint64_t limit_ns = 2000000000ull;  // 2 s: far beyond any legitimate wait
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0) {

@@ -368,6 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint64_t wlim = args.wait_limit_ns ? args.wait_limit_ns : kWaitLimitNs;
 
   if (threadIdx.x == 0) {
     num_tiles_s = count_tiles(args);
@@ -415,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const TileInfo ti = decode_tile<BN>(args, tile);
       for (int kb = 0; kb < ti.kb; ++kb) {
         int w = 1;
-        if (lane == 0) w = mbar_wait(empty_bar(stage), phase ^ 1u, &abort_s, args.err, 1);
+        if (lane == 0) w = mbar_wait(empty_bar(stage), phase ^ 1u, &abort_s, args.err, 1, wlim);
         ok = __shfl_sync(0xffffffffu, w, 0) != 0;
         if (!ok) break;
         if (lane == 0) {
@@ -478,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!abort_s) {
         // producer tail: every issued stage has been released by the MMA commits
         for (int s = 0; s < STAGES; ++s) {
-          if (!mbar_wait(empty_bar(stage), phase ^ 1u, &abort_s, args.err, 2)) break;
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, &abort_s, args.err, 2, wlim)) break;
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -502,14 +503,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
       const TileInfo ti = decode_tile<BN>(args, tile);
       int w = 1;
-      if (lane == 0) w = mbar_wait(tempty_bar(acc), acc_phase ^ 1u, &abort_s, args.err, 3);
+      if (lane == 0) w = mbar_wait(tempty_bar(acc), acc_phase ^ 1u, &abort_s, args.err, 3, wlim);
+      // failure-path test: wait on the drain barrier, which nothing has arrived at
+      if (args.stall_mma && lane == 0 && w) w = mbar_wait(drain_bar, 0, &abort_s, args.err, 9, wlim);
       ok = __shfl_sync(0xffffffffu, w, 0) != 0;
       if (!ok) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
       for (int kb = 0; kb < ti.kb; ++kb) {
         w = 1;
-        if (lane == 0) w = mbar_wait(full_bar(stage), phase, &abort_s, args.err, 4);
+        if (lane == 0) w = mbar_wait(full_bar(stage), phase, &abort_s, args.err, 4, wlim);
         ok = __shfl_sync(0xffffffffu, w, 0) != 0;
         if (!ok) break;
         tc_fence_after();
@@ -577,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const TileInfo ti = decode_tile<BN>(args, tile);
       int w = 1;
-      if (lane == 0) w = mbar_wait(tfull_bar(acc), acc_phase, &abort_s, args.err, 5);
+      if (lane == 0) w = mbar_wait(tfull_bar(acc), acc_phase, &abort_s, args.err, 5, wlim);
       // all eight epilogue warps leave together, so their named barriers stay matched
       const int ok_warp = __shfl_sync(0xffffffffu, w, 0);
       if (EPI == EPI_WGRAD) {

@@ -62,6 +62,11 @@ struct GemmArgs {
   uint8_t* hq;               // EPI_SWIGLU (MXFP8): h quantised along I, codes [rows, I]
   uint8_t* hsf;              // ... and its tiled scales
   int hsf_ngr;
+  // failure-path testing: every bounded wait gives up after wait_limit_ns (0 =
+  // default); stall_mma = 1 makes the MMA role first wait on a barrier that
+  // nothing arrives at, so the timeout path runs
+  unsigned long long wait_limit_ns;
+  int stall_mma;
   DevError* err;
 };
 
