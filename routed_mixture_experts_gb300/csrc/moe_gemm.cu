@@ -278,11 +278,13 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, const TileInfo& ti, 
 }
 
 // WGRAD epilogue: the accumulator tile is written, 32 columns at a time, into one
-// of four 16 KB shared-memory buffers (128 rows x 32 fp32, 128-byte swizzle, the
+// of kWgradBufs 16 KB shared-memory buffers (128 rows x 32 fp32, 128-byte swizzle, the
 // layout of the fp32 tensor map), and the TMA unit adds each buffer into the
 // fp32 gradient in global memory (cp.reduce.async.bulk.tensor .add).  The
 // read-modify-write then happens in L2 with many bytes in flight, instead of
 // through per-thread loads and stores.
+constexpr int kWgradBufs = 5;   // fp32 staging buffers of 16 KB (adds in flight per SM)
+
 template <int BN>
 __device__ __forceinline__ void epilogue_wgrad(const GemmArgs& a, const CUtensorMap* tmC,
                                                const TileInfo& ti, int row, uint32_t tbase,
@@ -292,8 +294,8 @@ __device__ __forceinline__ void epilogue_wgrad(const GemmArgs& a, const CUtensor
   uint32_t r0[16];
 #pragma unroll 1
   for (int c = 0; c < BN; c += 32) {
-    const uint32_t buf = stage_smem + (uint32_t)(sub & 3) * 16384u;
-    if (et == 0) bulk_wait_read<3>();          // this buffer's previous add has read it
+    const uint32_t buf = stage_smem + (uint32_t)(sub % kWgradBufs) * 16384u;
+    if (et == 0) bulk_wait_read<kWgradBufs - 1>();   // this buffer's previous add has read it
     named_bar_sync(1, kEpiThreads);
     // this thread's half: 16 of the sub-tile's 32 columns (16-byte chunks 4h..4h+3)
     tmem_ld16(tbase + c + 16 * half, r0);
@@ -326,8 +328,8 @@ struct GemmShape {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SF_STAGE_BYTES;
   // WGRAD keeps 64 KB for its four fp32 staging buffers and needs few stages
   // (its K loop is one expert's rows and it is bound by the gradient traffic).
-  static constexpr int OUT_BYTES = EPI == EPI_WGRAD ? 4 * 16384 : 0;
-  static constexpr int STAGE_BUDGET = 208 * 1024 - OUT_BYTES;
+  static constexpr int OUT_BYTES = EPI == EPI_WGRAD ? kWgradBufs * 16384 : 0;
+  static constexpr int STAGE_BUDGET = (EPI == EPI_WGRAD ? 226 : 208) * 1024 - OUT_BYTES;
   static constexpr int STAGES = STAGE_BUDGET / STAGE_BYTES > 8 ? 8 : STAGE_BUDGET / STAGE_BYTES;
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + OUT_BYTES + BAR_BYTES + 1024;

@@ -207,6 +207,10 @@ __device__ __forceinline__ void acc8(float* acc, const uint4 v) {
   acc[6] += __uint_as_float(v.w << 16); acc[7] += __uint_as_float(v.w & 0xFFFF0000u);
 }
 
+// One warp per token.  For small k (<= 8, the common case) every contribution's
+// 16-byte vectors are loaded before any is added, so k*U loads per lane are in
+// flight; the fp32 sums still run in j order.
+template <int KMAX>
 __global__ void __launch_bounds__(256) k_combine(const uint4* __restrict__ rows,
                                                  const int32_t* __restrict__ row_of, int T, int k,
                                                  int nvec, uint4* __restrict__ y,
@@ -215,7 +219,67 @@ __global__ void __launch_bounds__(256) k_combine(const uint4* __restrict__ rows,
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
-  constexpr int U = 4;   // 16-byte vectors per lane per pass
+  constexpr int U = KMAX <= 4 ? 4 : 2;   // 16-byte vectors per lane per pass
+  for (int t = gw; t < T; t += nw) {
+    int rj[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) rj[j] = j < k ? row_of[t * k + j] : -1;
+    for (int v0 = 0; v0 < nvec; v0 += 32 * U) {
+      uint4 buf[KMAX][U];
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        const uint4* src = rows + (long long)(rj[j] < 0 ? 0 : rj[j]) * nvec;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int v = v0 + lane + 32 * u;
+          buf[j][u] = (rj[j] >= 0 && v < nvec) ? src[v] : make_uint4(0, 0, 0, 0);
+        }
+      }
+      float acc[U][8];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[u][q] = 0.f;
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j)
+        if (rj[j] >= 0)
+#pragma unroll
+          for (int u = 0; u < U; ++u) acc8(acc[u], buf[j][u]);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + lane + 32 * u;
+        if (v < nvec) {
+          uint4 o;
+          o.x = pack_bf2(acc[u][0], acc[u][1]);
+          o.y = pack_bf2(acc[u][2], acc[u][3]);
+          o.z = pack_bf2(acc[u][4], acc[u][5]);
+          o.w = pack_bf2(acc[u][6], acc[u][7]);
+          y[(long long)t * nvec + v] = o;
+        }
+      }
+    }
+    if (dscores) {
+      for (int j = lane; j < k; j += 32) {
+        const int r = row_of[t * k + j];
+        float s = 0.f;
+        if (r >= 0)
+          for (int nt = 0; nt < n_pd; ++nt) s += pdscore[(long long)r * n_pd + nt];
+        dscores[t * k + j] = s;
+      }
+    }
+  }
+}
+
+// Any k: contributions are loaded and added one j at a time (fixed j order).
+__global__ void __launch_bounds__(256) k_combine_any(const uint4* __restrict__ rows,
+                                                     const int32_t* __restrict__ row_of, int T,
+                                                     int k, int nvec, uint4* __restrict__ y,
+                                                     const float* __restrict__ pdscore, int n_pd,
+                                                     float* __restrict__ dscores) {
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  constexpr int U = 4;
   for (int t = gw; t < T; t += nw) {
     for (int v0 = 0; v0 < nvec; v0 += 32 * U) {
       float acc[U][8];
@@ -280,8 +344,14 @@ cudaError_t launch_gather_rows(const void* src, const int32_t* token_of, const i
 cudaError_t launch_combine(const void* rows, const int32_t* row_of, int T, int k, int d, void* y,
                            const float* pdscore, int n_pd, float* dscores, int grid,
                            cudaStream_t stream) {
-  k_combine<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(rows), row_of, T, k, d / 8,
-                                      static_cast<uint4*>(y), pdscore, n_pd, dscores);
+  const uint4* r4 = static_cast<const uint4*>(rows);
+  uint4* y4 = static_cast<uint4*>(y);
+  if (k <= 4)
+    k_combine<4><<<grid, 256, 0, stream>>>(r4, row_of, T, k, d / 8, y4, pdscore, n_pd, dscores);
+  else if (k <= 8)
+    k_combine<8><<<grid, 256, 0, stream>>>(r4, row_of, T, k, d / 8, y4, pdscore, n_pd, dscores);
+  else
+    k_combine_any<<<grid, 256, 0, stream>>>(r4, row_of, T, k, d / 8, y4, pdscore, n_pd, dscores);
   return cudaGetLastError();
 }
 
