@@ -96,7 +96,7 @@ int moe_plan_set_swiglu_clamp(moe_plan* plan, float limit);
 /*
  * Bytes of device workspace the plan needs for `flags` (MOE_WS_*).  The size
  * covers the worst case of padded expert-major rows,
- *   Rpad <= T*k + E*(BM-1)   (BM = 128 rows per GEMM tile),
+ *   Rpad <= T*k + E*(G-1)    (G = the plan's row granule, 128 or 256),
  * so it never depends on the routing.  Returns 0 for a NULL plan.
  */
 size_t moe_plan_workspace_bytes(const moe_plan* plan, int flags);
@@ -224,6 +224,7 @@ const char* moe_status_string(int status);
  *   MOE_BUF_HS        bf16  [Rpad,I] score * h (WGRAD-W2 operand)
  *   MOE_BUF_DXE       bf16  [Rpad,d] per-row input gradients
  * Rows are valid up to off_pad[E].  Sizes are the worst-case capacities.
+ * off_pad rounds each expert's segment up to moe_plan_row_granule(plan) rows.
  */
 #define MOE_BUF_M_INDPTR 0
 #define MOE_BUF_OFF_PAD  1
@@ -290,7 +291,8 @@ long long moe_plan_launch_count(const moe_plan* plan);
  *   token_of [rows_capacity] int32, score_of [rows_capacity] fp32,
  *   status [2] int32: {MOE_OK or MOE_ERR_BAD_IDS, smallest bad flat index or -1}
  *                                                            (outputs, device)
- * Same contents as the tables moe_forward builds (see moe_plan_buffer).
+ * Same contents as the tables moe_forward builds (see moe_plan_buffer) for a
+ * plan whose row granule is 128.
  * Limits: T*k <= MOE_STATIC_MAX_ROUTED (else MOE_ERR_WORKSPACE: the static
  * scratch is too small), k <= E <= 256, rows_capacity >=
  * floor((T*k + E*(BM-1)) / BM) * BM (else MOE_ERR_INVALID_ARG).
@@ -305,14 +307,22 @@ int moe_dispatch_static(const int32_t* ids, const float* scores, int T, int k, i
                         int32_t* m_indptr, int32_t* off_pad, int32_t* row_of, int32_t* token_of,
                         float* score_of, long long rows_capacity, int32_t* status, void* stream);
 
-/* Rows per GEMM tile (BM), i.e. the padding granule of each expert segment. */
+/* Rows per GEMM m tile (128). */
 int moe_tile_rows(void);
+
+/*
+ * Padding granule of this plan's expert segments (off_pad): 256 when the bf16
+ * row GEMMs run on CTA pairs (d % 256 == 0 and I % 256 == 0), else 128.
+ */
+int moe_plan_row_granule(const moe_plan* plan);
 
 /*
  * Dense bf16 GEMM through the same tcgen05 kernels (for tests):
  *   mode 0: C[M,N] bf16  = A[M,K] . B[N,K]^T      (both operands K-major)
  *   mode 1: C[M,N] bf16  = A[M,K] . B[K,N]        (B MN-major)
  *   mode 2: C[M,N] fp32 += A[K,M]^T . B[K,N]      (both operands MN-major)
+ *   mode 3: as mode 0 on CTA pairs (256 x 256 tiles, M % 256 == N % 256 == 0)
+ *   mode 4: as mode 1 on CTA pairs
  * M % 128 == 0, N % 64 == 0, K % 64 == 0 (mode 2: K % 128 == 0).  `scratch`
  * is a device buffer of moe_gemm_scratch_bytes(M, K) bytes for the tile tables.
  */

@@ -52,6 +52,8 @@ def _declare(L):
     L.moe_status_string.restype = ctypes.c_char_p
     L.moe_plan_buffer.argtypes = [vp, i32, ctypes.POINTER(vp), ctypes.POINTER(sz)]
     L.moe_tile_rows.restype = i32
+    L.moe_plan_row_granule.argtypes = [vp]
+    L.moe_plan_row_granule.restype = i32
     L.moe_gemm_scratch_bytes.argtypes = [i32, i32]
     L.moe_gemm_scratch_bytes.restype = sz
     L.moe_gemm_bf16.argtypes = [i32, vp, vp, vp, i32, i32, i32, vp, vp]
@@ -167,6 +169,10 @@ class MoePlan:
         """Failure-path testing knobs (see moe_plan_set_debug in moe.h)."""
         _check(lib().moe_plan_set_debug(self.ptr, int(wait_limit_ns), 1 if stall_w13 else 0),
                "set_debug")
+
+    def row_granule(self):
+        """Padding granule of the expert segments (128, or 256 with CTA-pair GEMMs)."""
+        return lib().moe_plan_row_granule(self.ptr)
 
     def launch_count(self):
         return lib().moe_plan_launch_count(self.ptr)

@@ -33,6 +33,8 @@ struct moe_plan {
   int RP;       // worst-case padded rows
   int nblk;     // dispatch chunks
   int bn13, bn2, bnd2, bnw2, bnw13;
+  int pair;     // row GEMMs on CTA pairs (256-row tiles)
+  int gran;     // padding granule of expert segments (128, or 256 with pairs)
   // workspace
   char* ws;
   size_t ws_bytes;
@@ -48,9 +50,14 @@ struct moe_plan {
   int32_t* st_ids;
   float *st_scores, *st_dscores;
   // tensor maps over workspace tensors
-  CUtensorMap tm_xe, tm_h, tm_dye, tm_dA, tm_hs;
+  // K-major maps load 128-row boxes (the A tiles); MN-major maps (suffix _mn) are
+  // 3-D views loading a tile's 64-wide atoms in one box
+  CUtensorMap tm_xe, tm_h, tm_dye, tm_dA;
+  CUtensorMap tm_dye_mn, tm_dA_mn, tm_hs_mn, tm_xe_mn;
+  // bf16 outputs stored by the TMA-store epilogues (128-row boxes)
+  CUtensorMap tm_ys, tm_a, tm_hs, tm_dxe;
   // tensor maps over the caller's weights (re-encoded when the pointers change)
-  CUtensorMap tm_w13, tm_w2;
+  CUtensorMap tm_w13, tm_w2, tm_w13_mn, tm_w2_mn;
   const void *w13_cached, *w2_cached;
   // MXFP8: quantised expert-major activations and h, with tiled scales
   uint8_t *xq, *xsf, *hq, *hsf;
@@ -106,16 +113,35 @@ int encode_2d(CUtensorMap* map, CUtensorMapDataType dt, int esize, const void* b
 
 using tmap_detail::encode_2d;
 
-int encode_tmap_bf16(CUtensorMap* map, const void* base, long long rows, long long cols) {
-  return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, rows, cols, 64, 64);
+int encode_tmap_bf16(CUtensorMap* map, const void* base, long long rows, long long cols,
+                     int box_rows) {
+  return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, rows, cols, 64,
+                   (cuuint32_t)box_rows);
+}
+
+int encode_tmap_bf16_mn(CUtensorMap* map, const void* base, long long krows, long long ncols,
+                        int atoms) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = tmap_detail::encode_fn();
+  if (!fn) return MOE_ERR_CUDA;
+  // [K rows, N] viewed as dims (64 within an atom, K rows, N/64 atoms)
+  const cuuint64_t dims[3] = {64, (cuuint64_t)krows, (cuuint64_t)(ncols / 64)};
+  const cuuint64_t strides[2] = {(cuuint64_t)ncols * 2, 128};
+  const cuuint32_t box[3] = {64, 64, (cuuint32_t)atoms};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
 
 int encode_tmap_f32_out(CUtensorMap* map, const void* base, long long rows, long long cols) {
   return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, rows, cols, 32, 128);
 }
 
-int encode_tmap_u8(CUtensorMap* map, const void* base, long long rows, long long cols) {
-  return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, rows, cols, 128, 64);
+int encode_tmap_u8(CUtensorMap* map, const void* base, long long rows, long long cols,
+                   int box_rows) {
+  return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, rows, cols, 128,
+                   (cuuint32_t)box_rows);
 }
 
 }  // namespace moe
@@ -205,13 +231,20 @@ int reset_error_word(DevError* err) {
 }
 
 int refresh_weight_maps(moe_plan* p, const void* w13, const void* w2) {
+  // B boxes: W13 gate/up halves and W2 rows of one N tile (a CTA's half with pairs)
+  const int b13 = p->pair ? 128 : p->bn13 / 2;
+  const int b2 = p->pair ? 128 : p->bn2;
   if (w13 != p->w13_cached) {
-    if (encode_tmap_bf16(&p->tm_w13, w13, (long long)p->E * 2 * p->I, p->d) != MOE_OK)
+    if (encode_tmap_bf16(&p->tm_w13, w13, (long long)p->E * 2 * p->I, p->d, b13) != MOE_OK ||
+        encode_tmap_bf16_mn(&p->tm_w13_mn, w13, (long long)p->E * 2 * p->I, p->d,
+                            p->pair ? 2 : p->bn2 / 64) != MOE_OK)
       return MOE_ERR_CUDA;
     p->w13_cached = w13;
   }
   if (w2 != p->w2_cached) {
-    if (encode_tmap_bf16(&p->tm_w2, w2, (long long)p->E * p->d, p->I) != MOE_OK)
+    if (encode_tmap_bf16(&p->tm_w2, w2, (long long)p->E * p->d, p->I, b2) != MOE_OK ||
+        encode_tmap_bf16_mn(&p->tm_w2_mn, w2, (long long)p->E * p->d, p->I,
+                            p->pair ? 2 : p->bnd2 / 64) != MOE_OK)
       return MOE_ERR_CUDA;
     p->w2_cached = w2;
   }
@@ -268,7 +301,8 @@ int forward_mxfp8(moe_plan* p, const void* x, const uint8_t* w13_sf, const uint8
     g.sfa = p->xsf; g.sfb = w13_sf; g.sf_ngr = p->ngr_d; g.b_blocks_per_expert = p->I / 64;
     g.hq = p->hq; g.hsf = p->hsf; g.hsf_ngr = p->ngr_I;
     g.stall_mma = p->dbg_stall_w13;
-    e = launch_gemm(EPI_SWIGLU, 128, false, false, p->tm_xq, p->tm_w13q, p->tm_xq, g, p->num_sms,
+    e = launch_gemm(EPI_SWIGLU, 128, false, false, p->tm_xq, p->tm_w13q, p->tm_xq, p->tm_ys,
+                    p->tm_ys, g, p->num_sms,
                     st, true);
     if (e != cudaSuccess) return cuda_status(e);
     p->launches += 1;
@@ -282,7 +316,8 @@ int forward_mxfp8(moe_plan* p, const void* x, const uint8_t* w13_sf, const uint8
     g.out0 = p->ys; g.ld0 = p->d;
     g.row_scale = p->score_of;
     g.sfa = p->hsf; g.sfb = w2_sf; g.sf_ngr = p->ngr_I; g.b_blocks_per_expert = p->d / 128;
-    e = launch_gemm(EPI_SCORE, 128, false, false, p->tm_hq, p->tm_w2q, p->tm_hq, g, p->num_sms,
+    e = launch_gemm(EPI_SCORE, 128, false, false, p->tm_hq, p->tm_w2q, p->tm_hq, p->tm_ys,
+                    p->tm_ys, g, p->num_sms,
                     st, true);
     if (e != cudaSuccess) return cuda_status(e);
     p->launches += 1;
@@ -321,6 +356,8 @@ const char* moe_status_string(int s) {
 
 int moe_tile_rows(void) { return kBM; }
 
+int moe_plan_row_granule(const moe_plan* p) { return p ? p->gran : 0; }
+
 moe_plan* moe_plan_create(int T, int d, int I, int E, int k, int precision) {
   if (T < 1 || d < 128 || I < 64 || d % 128 || I % 64 || k < 1 || E < k || E > 256) return nullptr;
   if ((long long)T * k >= (1LL << 31) - (long long)E * kBM) return nullptr;
@@ -332,7 +369,10 @@ moe_plan* moe_plan_create(int T, int d, int I, int E, int k, int precision) {
   memset(p, 0, sizeof(*p));
   p->T = T; p->d = d; p->I = I; p->E = E; p->k = k; p->precision = precision;
   p->R = T * k;
-  p->RP = (int)(((long long)p->R + (long long)E * (kBM - 1)) / kBM * kBM);
+  // CTA-pair row GEMMs need 256-row expert segments and N tiles of 256
+  p->pair = precision == MOE_PREC_BF16 && I % 256 == 0 && d % 256 == 0;
+  p->gran = p->pair ? 256 : kBM;
+  p->RP = (int)(((long long)p->R + (long long)E * (p->gran - 1)) / p->gran * p->gran);
   p->nblk = (p->R + 1023) / 1024;
   p->bn13 = I % 128 == 0 ? 256 : 128;
   p->bn2 = pick_bn_n(d) == 64 ? 128 : pick_bn_n(d);
@@ -378,16 +418,26 @@ int moe_plan_set_workspace(moe_plan* p, void* ws, size_t bytes, int flags) {
   p->w13q_cached = p->w2q_cached = nullptr;
   const long long RP = p->RP;
   if (p->precision == MOE_PREC_MXFP8) {
-    if (encode_tmap_u8(&p->tm_xq, p->xq, RP, p->d) || encode_tmap_u8(&p->tm_hq, p->hq, RP, p->I))
+    if (encode_tmap_u8(&p->tm_xq, p->xq, RP, p->d, 128) ||
+        encode_tmap_u8(&p->tm_hq, p->hq, RP, p->I, 128) ||
+        encode_tmap_bf16(&p->tm_ys, p->ys, RP, p->d, 128))
       return MOE_ERR_CUDA;
     return reset_error_word(p->err);
   }
-  if (encode_tmap_bf16(&p->tm_xe, p->xe, RP, p->d) || encode_tmap_bf16(&p->tm_h, p->h, RP, p->I))
+  if (encode_tmap_bf16(&p->tm_xe, p->xe, RP, p->d, 128) ||
+      encode_tmap_bf16(&p->tm_h, p->h, RP, p->I, 128) ||
+      encode_tmap_bf16(&p->tm_ys, p->ys, RP, p->d, 128))
     return MOE_ERR_CUDA;
   if (flags & MOE_WS_TRAINING) {
-    if (encode_tmap_bf16(&p->tm_dye, p->dye, RP, p->d) ||
-        encode_tmap_bf16(&p->tm_dA, p->dA, RP, 2LL * p->I) ||
-        encode_tmap_bf16(&p->tm_hs, p->hs, RP, p->I))
+    if (encode_tmap_bf16(&p->tm_dye, p->dye, RP, p->d, 128) ||
+        encode_tmap_bf16(&p->tm_dA, p->dA, RP, 2LL * p->I, 128) ||
+        encode_tmap_bf16_mn(&p->tm_dye_mn, p->dye, RP, p->d, 2) ||
+        encode_tmap_bf16_mn(&p->tm_dA_mn, p->dA, RP, 2LL * p->I, 2) ||
+        encode_tmap_bf16_mn(&p->tm_hs_mn, p->hs, RP, p->I, p->bnw2 / 64) ||
+        encode_tmap_bf16_mn(&p->tm_xe_mn, p->xe, RP, p->d, p->bnw13 / 64) ||
+        encode_tmap_bf16(&p->tm_a, p->a, RP, 2LL * p->I, 128) ||
+        encode_tmap_bf16(&p->tm_hs, p->hs, RP, p->I, 128) ||
+        encode_tmap_bf16(&p->tm_dxe, p->dxe, RP, p->d, 128))
       return MOE_ERR_CUDA;
   }
   return reset_error_word(p->err);
@@ -408,11 +458,11 @@ int moe_forward(moe_plan* p, const void* x, const int32_t* ids, const float* sco
   cudaStream_t st = static_cast<cudaStream_t>(stream_v);
   if (mx) {
     if (w13 != p->w13q_cached) {
-      if (encode_tmap_u8(&p->tm_w13q, w13, (long long)p->E * 2 * p->I, p->d)) return MOE_ERR_CUDA;
+      if (encode_tmap_u8(&p->tm_w13q, w13, (long long)p->E * 2 * p->I, p->d, 64)) return MOE_ERR_CUDA;
       p->w13q_cached = w13;
     }
     if (w2 != p->w2q_cached) {
-      if (encode_tmap_u8(&p->tm_w2q, w2, (long long)p->E * p->d, p->I)) return MOE_ERR_CUDA;
+      if (encode_tmap_u8(&p->tm_w2q, w2, (long long)p->E * p->d, p->I, 128)) return MOE_ERR_CUDA;
       p->w2q_cached = w2;
     }
   } else if (refresh_weight_maps(p, w13, w2) != MOE_OK) {
@@ -423,7 +473,7 @@ int moe_forward(moe_plan* p, const void* x, const int32_t* ids, const float* sco
   // a1-a3: dispatch
   RouteArgs ra;
   ra.ids = ids; ra.scores = scores;
-  ra.T = p->T; ra.k = p->k; ra.E = p->E; ra.BM = kBM; ra.nblk = p->nblk;
+  ra.T = p->T; ra.k = p->k; ra.E = p->E; ra.BM = p->gran; ra.nblk = p->nblk;
   ra.blockcounts = p->blockcounts; ra.counts = p->counts; ra.m_indptr = p->m_indptr;
   ra.off_pad = p->off_pad; ra.num_mtiles = p->num_mtiles; ra.tile_expert = p->tile_expert;
   ra.expert_order = p->expert_order; ra.num_nonempty = p->num_nonempty;
@@ -449,7 +499,15 @@ int moe_forward(moe_plan* p, const void* x, const int32_t* ids, const float* sco
     g.out1 = p->a; g.ld1 = 2LL * p->I;
     g.save = save_for_backward ? 1 : 0;
     g.stall_mma = p->dbg_stall_w13;
-    e = launch_gemm(EPI_SWIGLU, p->bn13, false, false, p->tm_xe, p->tm_w13, p->tm_xe, g, p->num_sms, st);
+    if (p->pair) {
+      g.n_tiles = p->I / 128;
+      e = launch_gemm_pair(EPI_SWIGLU, false, p->tm_xe, p->tm_w13, p->tm_h, p->tm_a, g,
+                           p->num_sms, st);
+    } else {
+      e = launch_gemm(EPI_SWIGLU, p->bn13, false, false, p->tm_xe, p->tm_w13, p->tm_xe, p->tm_h,
+                      p->tm_a, g,
+                      p->num_sms, st);
+    }
     if (e != cudaSuccess) return cuda_status(e);
     p->launches += 1;
     mark(p, 0, 3, st);
@@ -462,7 +520,14 @@ int moe_forward(moe_plan* p, const void* x, const int32_t* ids, const float* sco
     g.n_tiles = p->d / p->bn2;
     g.out0 = p->ys; g.ld0 = p->d;
     g.row_scale = p->score_of;
-    e = launch_gemm(EPI_SCORE, p->bn2, false, false, p->tm_h, p->tm_w2, p->tm_h, g, p->num_sms, st);
+    if (p->pair) {
+      g.n_tiles = p->d / 256;
+      e = launch_gemm_pair(EPI_SCORE, false, p->tm_h, p->tm_w2, p->tm_ys, p->tm_ys, g,
+                           p->num_sms, st);
+    } else {
+      e = launch_gemm(EPI_SCORE, p->bn2, false, false, p->tm_h, p->tm_w2, p->tm_h, p->tm_ys,
+                      p->tm_ys, g, p->num_sms, st);
+    }
     if (e != cudaSuccess) return cuda_status(e);
     p->launches += 1;
     mark(p, 0, 4, st);
@@ -514,7 +579,13 @@ int moe_backward(moe_plan* p, const void* dy, const void* w13, const void* w2, v
     g.out1 = p->hs; g.ld1 = I;
     g.row_scale = p->score_of;
     g.pdscore = p->pdscore;
-    e = launch_gemm(EPI_DGRAD2, p->bnd2, false, true, p->tm_dye, p->tm_w2, p->tm_dye, g, p->num_sms, st);
+    if (p->pair)
+      e = launch_gemm_pair(EPI_DGRAD2, true, p->tm_dye, p->tm_w2_mn, p->tm_dA, p->tm_hs, g,
+                           p->num_sms, st);
+    else
+      e = launch_gemm(EPI_DGRAD2, p->bnd2, false, true, p->tm_dye, p->tm_w2_mn, p->tm_dye,
+                      p->tm_dA, p->tm_hs, g,
+                      p->num_sms, st);
     if (e != cudaSuccess) return cuda_status(e);
     p->launches += 1;
     mark(p, 1, 2, st);
@@ -526,7 +597,15 @@ int moe_backward(moe_plan* p, const void* dy, const void* w13, const void* w2, v
     g.b_expert_rows = 2 * I;
     g.n_tiles = d / p->bn2;
     g.out0 = p->dxe; g.ld0 = d;
-    e = launch_gemm(EPI_STORE, p->bn2, false, true, p->tm_dA, p->tm_w13, p->tm_dA, g, p->num_sms, st);
+    if (p->pair) {
+      g.n_tiles = d / 256;
+      e = launch_gemm_pair(EPI_STORE, true, p->tm_dA, p->tm_w13_mn, p->tm_dxe, p->tm_dxe, g,
+                           p->num_sms, st);
+    } else {
+      e = launch_gemm(EPI_STORE, p->bn2, false, true, p->tm_dA, p->tm_w13_mn, p->tm_dA, p->tm_dxe,
+                      p->tm_dxe, g,
+                      p->num_sms, st);
+    }
     if (e != cudaSuccess) return cuda_status(e);
     p->launches += 1;
     mark(p, 1, 3, st);
@@ -544,7 +623,9 @@ int moe_backward(moe_plan* p, const void* dy, const void* w13, const void* w2, v
     g.n_tiles = I / p->bnw2;
     g.out0 = dw2; g.ld0 = I;
     g.out_expert_stride = (long long)d * I;
-    e = launch_gemm(EPI_WGRAD, p->bnw2, true, true, p->tm_dye, p->tm_hs, p->tm_dw2, g, p->num_sms, st);
+    e = launch_gemm(EPI_WGRAD, p->bnw2, true, true, p->tm_dye_mn, p->tm_hs_mn, p->tm_dw2,
+                    p->tm_dw2, p->tm_dw2, g,
+                    p->num_sms, st);
     if (e != cudaSuccess) return cuda_status(e);
     p->launches += 1;
     mark(p, 1, 5, st);
@@ -556,7 +637,9 @@ int moe_backward(moe_plan* p, const void* dy, const void* w13, const void* w2, v
     g.n_tiles = d / p->bnw13;
     g.out0 = dw13; g.ld0 = d;
     g.out_expert_stride = 2LL * I * d;
-    e = launch_gemm(EPI_WGRAD, p->bnw13, true, true, p->tm_dA, p->tm_xe, p->tm_dw13, g, p->num_sms, st);
+    e = launch_gemm(EPI_WGRAD, p->bnw13, true, true, p->tm_dA_mn, p->tm_xe_mn, p->tm_dw13,
+                    p->tm_dw13, p->tm_dw13, g,
+                    p->num_sms, st);
     if (e != cudaSuccess) return cuda_status(e);
     p->launches += 1;
     mark(p, 1, 6, st);
@@ -718,6 +801,7 @@ extern "C" int moe_gemm_bf16(int mode, const void* A, const void* B, void* C, in
                              void* scratch, void* stream_v) {
   if (!A || !B || !C || !scratch || M <= 0 || N <= 0 || K <= 0) return MOE_ERR_INVALID_ARG;
   if (M % 128 || N % 64 || K % 64 || (mode == 2 && K % 128)) return MOE_ERR_INVALID_ARG;
+  if ((mode == 3 || mode == 4) && (M % 256 || N % 256)) return MOE_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream_v);
   int dev = 0, sms = 148;
@@ -734,17 +818,31 @@ extern "C" int moe_gemm_bf16(int mode, const void* A, const void* B, void* C, in
   g.ld0 = N;
   cudaError_t e;
   if (mode == 0 || mode == 1) {
-    if (encode_tmap_bf16(&ta, A, M, K)) return MOE_ERR_CUDA;
-    if (mode == 0 ? encode_tmap_bf16(&tb, B, N, K) : encode_tmap_bf16(&tb, B, K, N))
+    if (encode_tmap_bf16(&ta, A, M, K, 128)) return MOE_ERR_CUDA;
+    if (mode == 0 ? encode_tmap_bf16(&tb, B, N, K, bn) : encode_tmap_bf16_mn(&tb, B, K, N, bn / 64))
       return MOE_ERR_CUDA;
     g.wgrad = 0;
     g.num_mtiles = s;
     g.tile_expert = nullptr;
     g.k_blocks = K / kBK;
     g.b_expert_rows = mode == 0 ? N : K;
-    e = launch_gemm(EPI_STORE, bn, false, mode == 1, ta, tb, ta, g, sms, st);
+    if (encode_tmap_bf16(&tc, C, M, N, 128)) return MOE_ERR_CUDA;
+    e = launch_gemm(EPI_STORE, bn, false, mode == 1, ta, tb, ta, tc, tc, g, sms, st);
+  } else if (mode == 3 || mode == 4) {
+    // the same products on CTA pairs (256 x 256 tiles)
+    if (encode_tmap_bf16(&ta, A, M, K, 128)) return MOE_ERR_CUDA;
+    if (mode == 3 ? encode_tmap_bf16(&tb, B, N, K, 128) : encode_tmap_bf16_mn(&tb, B, K, N, 2))
+      return MOE_ERR_CUDA;
+    g.wgrad = 0;
+    g.num_mtiles = s;
+    g.tile_expert = nullptr;          // a single "expert"
+    g.k_blocks = K / kBK;
+    g.b_expert_rows = mode == 3 ? N : K;
+    g.n_tiles = N / 256;
+    if (encode_tmap_bf16(&tc, C, M, N, 128)) return MOE_ERR_CUDA;
+    e = launch_gemm_pair(EPI_STORE, mode == 4, ta, tb, tc, tc, g, sms, st);
   } else if (mode == 2) {
-    if (encode_tmap_bf16(&ta, A, K, M) || encode_tmap_bf16(&tb, B, K, N) ||
+    if (encode_tmap_bf16_mn(&ta, A, K, M, 2) || encode_tmap_bf16_mn(&tb, B, K, N, bn / 64) ||
         encode_tmap_f32_out(&tc, C, M, N))
       return MOE_ERR_CUDA;
     g.wgrad = 1;
@@ -753,7 +851,7 @@ extern "C" int moe_gemm_bf16(int mode, const void* A, const void* B, void* C, in
     g.expert_order = s + 4;
     g.m_tiles = M / kBM;
     g.out_expert_stride = 0;
-    e = launch_gemm(EPI_WGRAD, bn, true, true, ta, tb, tc, g, sms, st);
+    e = launch_gemm(EPI_WGRAD, bn, true, true, ta, tb, tc, tc, tc, g, sms, st);
   } else {
     return MOE_ERR_INVALID_ARG;
   }

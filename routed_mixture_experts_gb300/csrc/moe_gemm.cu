@@ -23,299 +23,13 @@
 // MOE_ERR_TIMEOUT, all roles leave their loops, outstanding copies and MMAs are
 // drained with bounded waits, and TMEM is freed before the CTA exits.
 
-#include "moe_device.cuh"
-#include "moe_internal.h"
+#include "moe_gemm_common.cuh"
 
 namespace moe {
 
+using namespace gemm;
+
 namespace {
-
-// warp 0 TMA producer, warp 1 MMA issuer, warps 2..9 epilogue (two warps per
-// TMEM lane quarter, each taking half of the tile's columns)
-constexpr int kThreads = 320;
-constexpr int kEpiThreads = 256;
-constexpr int kBoxBytes = 64 * 64 * 2;  // every TMA box is 64 x 64 bf16 = 8 KB
-
-struct TileInfo {
-  int e;        // expert
-  int m0;       // first output row of the tile (padded row, or weight row in wgrad mode)
-  int n0;       // first output column
-  int nt;       // n tile index
-  int kb;       // number of 64-wide K blocks
-  int krow0;    // wgrad mode: first routed row of the K range
-};
-
-__device__ __forceinline__ int count_tiles(const GemmArgs& a) {
-  if (a.wgrad) return (*a.num_nonempty) * a.m_tiles * a.n_tiles;
-  return (*a.num_mtiles) * a.n_tiles;
-}
-
-template <int BN>
-__device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int tile) {
-  TileInfo ti;
-  if (a.wgrad) {
-    const int per_e = a.m_tiles * a.n_tiles;
-    const int q = tile / per_e;
-    const int rem = tile - q * per_e;
-    ti.e = a.expert_order[q];
-    const int mt = rem / a.n_tiles;
-    ti.nt = rem - mt * a.n_tiles;
-    ti.m0 = mt * kBM;
-    ti.n0 = ti.nt * BN;
-    ti.krow0 = a.off_pad[ti.e];
-    ti.kb = (a.off_pad[ti.e + 1] - ti.krow0) / kBK;
-  } else {
-    const int mt = tile / a.n_tiles;
-    ti.nt = tile - mt * a.n_tiles;
-    ti.e = a.tile_expert ? a.tile_expert[mt] : 0;
-    ti.m0 = mt * kBM;
-    ti.n0 = ti.nt * BN;
-    ti.kb = a.k_blocks;
-    ti.krow0 = 0;
-  }
-  return ti;
-}
-
-// Bounded wait that ignores the abort flag (used only while draining).
-__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > 200000000ull) return false;  // 200 ms
-  }
-  return true;
-}
-
-// AND of `v` over the 256 epilogue threads (named barrier 1).
-__device__ __forceinline__ int epi_bar_and(int v) {
-  int r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.s32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, 1, 256, p;\n\t"
-      "selp.s32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(v)
-      : "memory");
-  return r;
-}
-
-__device__ __forceinline__ float swiglu_fwd(float G, float U, float L) {
-  if (L > 0.f) {
-    G = fminf(fmaxf(G, -L), L);
-    U = fminf(fmaxf(U, -L), L);
-  }
-  const float silu = G / (1.0f + expf(-G));
-  return silu * U;
-}
-
-__device__ __forceinline__ void store16_bf16(uint16_t* dst, const float (&v)[16]) {
-  uint4 lo, hi;
-  lo.x = pack_bf2(v[0], v[1]);   lo.y = pack_bf2(v[2], v[3]);
-  lo.z = pack_bf2(v[4], v[5]);   lo.w = pack_bf2(v[6], v[7]);
-  hi.x = pack_bf2(v[8], v[9]);   hi.y = pack_bf2(v[10], v[11]);
-  hi.z = pack_bf2(v[12], v[13]); hi.w = pack_bf2(v[14], v[15]);
-  reinterpret_cast<uint4*>(dst)[0] = lo;
-  reinterpret_cast<uint4*>(dst)[1] = hi;
-}
-
-__device__ __forceinline__ void load16_bf16(const uint16_t* src, float (&v)[16]) {
-  const uint4 lo = reinterpret_cast<const uint4*>(src)[0];
-  const uint4 hi = reinterpret_cast<const uint4*>(src)[1];
-  const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    v[2 * i] = __uint_as_float(w[i] << 16);
-    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
-}
-
-// ---------------------------------------------------------------------------
-// epilogues: one thread owns one output row (`row` within the tile) and reads
-// its accumulator columns from TMEM at `tbase` (lane quarter already folded in).
-
-// MXFP8 W13 epilogue: like the bf16 one (R1, SwiGLU, R2), then h is quantised
-// along I in 32-column blocks (codes to a.hq, tiled E8M0 scales to a.hsf) as the
-// A operand of the block-scaled W2 GEMM; the bf16 h is kept for inspection.
-template <int BN>
-__device__ __forceinline__ void epilogue_swiglu_mx(const GemmArgs& a, const TileInfo& ti, int row,
-                                                   uint32_t tbase, int half) {
-  constexpr int BNH = BN / 2;
-  constexpr int W = BNH / 2;             // columns of this thread's half
-  const long long grow = (long long)ti.m0 + row;
-  const int c0 = ti.nt * BNH;
-  uint16_t* h = static_cast<uint16_t*>(a.out0) + grow * a.ld0 + c0;
-  uint8_t* hq = a.hq + grow * a.ld0 + c0;
-  uint32_t g0[16], g1[16], u0[16], u1[16];
-#pragma unroll 1
-  for (int c = half * W; c < (half + 1) * W; c += 32) {
-    tmem_ld16(tbase + c, g0);
-    tmem_ld16(tbase + c + 16, g1);
-    tmem_ld16(tbase + BNH + c, u0);
-    tmem_ld16(tbase + BNH + c + 16, u1);
-    tmem_ld_wait();
-    float hv[32];
-#pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      const float G0 = bf2f(f2bf(__uint_as_float(g0[q]))), U0 = bf2f(f2bf(__uint_as_float(u0[q])));
-      const float G1 = bf2f(f2bf(__uint_as_float(g1[q]))), U1 = bf2f(f2bf(__uint_as_float(u1[q])));
-      hv[q] = bf2f(f2bf(swiglu_fwd(G0, U0, a.clamp)));            // R2
-      hv[16 + q] = bf2f(f2bf(swiglu_fwd(G1, U1, a.clamp)));
-    }
-    float lo[16], hi[16];
-#pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      lo[q] = hv[q];
-      hi[q] = hv[16 + q];
-    }
-    store16_bf16(h + c, lo);
-    store16_bf16(h + c + 16, hi);
-    uint32_t w[8];
-    const uint8_t sc = mx_quant32(hv, w);
-    reinterpret_cast<uint4*>(hq + c)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    reinterpret_cast<uint4*>(hq + c)[1] = make_uint4(w[4], w[5], w[6], w[7]);
-    a.hsf[mx_sf_offset(grow >> 7, (int)(grow & 127), (c0 + c) >> 5, a.hsf_ngr)] = sc;
-  }
-}
-
-template <int BN, int EPI>
-__device__ __forceinline__ void epilogue(const GemmArgs& a, const TileInfo& ti, int row,
-                                         uint32_t tbase, int half) {
-  const long long grow = (long long)ti.m0 + row;
-  uint32_t r0[16], r1[16];
-  constexpr int W = BN / 2;              // columns of this thread's half (BN-wide epilogues)
-  if constexpr (EPI == EPI_SWIGLU) {
-    constexpr int BNH = BN / 2;          // gate columns [0,BNH), up columns [BNH,BN)
-    constexpr int WH = BNH / 2;
-    const int c0 = ti.nt * BNH;          // first intermediate column of this tile
-    uint16_t* h = static_cast<uint16_t*>(a.out0) + grow * a.ld0 + c0;
-    uint16_t* av = static_cast<uint16_t*>(a.out1) + grow * a.ld1 + c0;
-#pragma unroll 1
-    for (int c = half * WH; c < (half + 1) * WH; c += 16) {
-      tmem_ld16(tbase + c, r0);
-      tmem_ld16(tbase + BNH + c, r1);
-      tmem_ld_wait();
-      float G[16], U[16], hv[16];
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        G[q] = bf2f(f2bf(__uint_as_float(r0[q])));   // R1
-        U[q] = bf2f(f2bf(__uint_as_float(r1[q])));
-        hv[q] = swiglu_fwd(G[q], U[q], a.clamp);      // R2 on store
-      }
-      store16_bf16(h + c, hv);
-      if (a.save) {
-        store16_bf16(av + c, G);
-        store16_bf16(av + a.I + c, U);
-      }
-    }
-  } else if constexpr (EPI == EPI_SCORE) {
-    const float s = a.row_scale[grow];
-    uint16_t* out = static_cast<uint16_t*>(a.out0) + grow * a.ld0 + ti.n0;
-#pragma unroll 1
-    for (int c = half * W; c < (half + 1) * W; c += 16) {
-      tmem_ld16(tbase + c, r0);
-      tmem_ld_wait();
-      float v[16];
-#pragma unroll
-      for (int q = 0; q < 16; ++q) v[q] = s * __uint_as_float(r0[q]);   // R3 on store
-      store16_bf16(out + c, v);
-    }
-  } else if constexpr (EPI == EPI_STORE) {
-    uint16_t* out = static_cast<uint16_t*>(a.out0) + grow * a.ld0 + ti.n0;
-#pragma unroll 1
-    for (int c = half * W; c < (half + 1) * W; c += 16) {
-      tmem_ld16(tbase + c, r0);
-      tmem_ld_wait();
-      float v[16];
-#pragma unroll
-      for (int q = 0; q < 16; ++q) v[q] = __uint_as_float(r0[q]);
-      store16_bf16(out + c, v);
-    }
-  } else if constexpr (EPI == EPI_DGRAD2) {
-    // acc = g (columns = intermediate index i).  in0 = h [rows, I], in1 = a [rows, 2I],
-    // out0 = dA [rows, 2I], out1 = hs [rows, I].
-    const float s = a.row_scale[grow];
-    const float L = a.clamp;
-    const uint16_t* hrow = static_cast<const uint16_t*>(a.in0) + grow * a.ldi0 + ti.n0;
-    const uint16_t* arow = static_cast<const uint16_t*>(a.in1) + grow * a.ldi1 + ti.n0;
-    uint16_t* darow = static_cast<uint16_t*>(a.out0) + grow * a.ld0 + ti.n0;
-    uint16_t* hsrow = static_cast<uint16_t*>(a.out1) + grow * a.ld1 + ti.n0;
-    float part = 0.f;
-#pragma unroll 1
-    for (int c = half * W; c < (half + 1) * W; c += 16) {
-      tmem_ld16(tbase + c, r0);
-      float hv[16], ag[16], au[16];
-      load16_bf16(hrow + c, hv);
-      load16_bf16(arow + c, ag);
-      load16_bf16(arow + a.I + c, au);
-      tmem_ld_wait();
-      float dg[16], du[16], hs[16];
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const float g = __uint_as_float(r0[q]);
-        part += hv[q] * g;
-        float G = ag[q], U = au[q], mg = 1.f, mu = 1.f;
-        if (L > 0.f) {
-          if (G < -L || G > L) mg = 0.f;
-          if (U < -L || U > L) mu = 0.f;
-          G = fminf(fmaxf(G, -L), L);
-          U = fminf(fmaxf(U, -L), L);
-        }
-        const float dh = s * g;
-        const float sig = 1.0f / (1.0f + expf(-G));
-        const float silu = G * sig;
-        const float dsilu = sig * (1.0f + G * (1.0f - sig));
-        dg[q] = dh * U * dsilu * mg;       // R4 on store
-        du[q] = dh * silu * mu;
-        hs[q] = s * hv[q];                 // R7 on store
-      }
-      store16_bf16(darow + c, dg);
-      store16_bf16(darow + a.I + c, du);
-      store16_bf16(hsrow + c, hs);
-    }
-    // one partial per (n tile, column half), in column order
-    a.pdscore[grow * (2 * a.n_tiles) + 2 * ti.nt + half] = part;
-  }
-}
-
-// WGRAD epilogue: the accumulator tile is written, 32 columns at a time, into one
-// of kWgradBufs 16 KB shared-memory buffers (128 rows x 32 fp32, 128-byte swizzle, the
-// layout of the fp32 tensor map), and the TMA unit adds each buffer into the
-// fp32 gradient in global memory (cp.reduce.async.bulk.tensor .add).  The
-// read-modify-write then happens in L2 with many bytes in flight, instead of
-// through per-thread loads and stores.
-constexpr int kWgradBufs = 5;   // fp32 staging buffers of 16 KB (adds in flight per SM)
-
-template <int BN>
-__device__ __forceinline__ void epilogue_wgrad(const GemmArgs& a, const CUtensorMap* tmC,
-                                               const TileInfo& ti, int row, uint32_t tbase,
-                                               uint32_t stage_smem, int et, int half, int& sub) {
-  if (ti.kb == 0) return;
-  const int ybase = ti.e * a.m_tiles * kBM + ti.m0;
-  uint32_t r0[16];
-#pragma unroll 1
-  for (int c = 0; c < BN; c += 32) {
-    const uint32_t buf = stage_smem + (uint32_t)(sub % kWgradBufs) * 16384u;
-    if (et == 0) bulk_wait_read<kWgradBufs - 1>();   // this buffer's previous add has read it
-    named_bar_sync(1, kEpiThreads);
-    // this thread's half: 16 of the sub-tile's 32 columns (16-byte chunks 4h..4h+3)
-    tmem_ld16(tbase + c + 16 * half, r0);
-    tmem_ld_wait();
-    const uint32_t rbase = buf + (uint32_t)row * 128u;
-    const uint32_t sw = (uint32_t)(row & 7);
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      st_shared_v4(rbase + (((uint32_t)(q + 4 * half) ^ sw) << 4), __uint_as_float(r0[4 * q]),
-                   __uint_as_float(r0[4 * q + 1]), __uint_as_float(r0[4 * q + 2]),
-                   __uint_as_float(r0[4 * q + 3]));
-    fence_proxy_async_smem();
-    named_bar_sync(1, kEpiThreads);
-    if (et == 0) {
-      tma_reduce_add_2d(tmC, buf, ti.n0 + c, ybase);
-      bulk_commit();
-    }
-    ++sub;
-  }
-}
 
 template <int BN, int EPI, bool MX>
 struct GemmShape {
@@ -326,10 +40,13 @@ struct GemmShape {
   static constexpr int B_BYTES = BN * 128;
   static constexpr int SF_STAGE_BYTES = MX ? 1024 : 0;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SF_STAGE_BYTES;
-  // WGRAD keeps 64 KB for its four fp32 staging buffers and needs few stages
-  // (its K loop is one expert's rows and it is bound by the gradient traffic).
-  static constexpr int OUT_BYTES = EPI == EPI_WGRAD ? kWgradBufs * 16384 : 0;
-  static constexpr int STAGE_BUDGET = (EPI == EPI_WGRAD ? 226 : 208) * 1024 - OUT_BYTES;
+  // Output staging: WGRAD's fp32 buffers (it needs few stages: its K loop is one
+  // expert's rows and it is bound by the gradient traffic), else two bf16
+  // sub-tile buffers for the TMA-store epilogues.
+  static constexpr int OUT_BYTES =
+      (EPI == EPI_WGRAD ? kWgradBufs
+                        : (EPI == EPI_SCORE || EPI == EPI_STORE ? kEpiStageBufs : 0)) * 16384;
+  static constexpr int STAGE_BUDGET = 226 * 1024 - OUT_BYTES;
   static constexpr int STAGES = STAGE_BUDGET / STAGE_BYTES > 8 ? 8 : STAGE_BUDGET / STAGE_BYTES;
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + OUT_BYTES + BAR_BYTES + 1024;
@@ -343,7 +60,8 @@ struct GemmShape {
 template <int BN, bool A_MN, bool B_MN, int EPI, bool MX>
 __global__ void __launch_bounds__(kThreads, 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
+                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmO0,
+                   const __grid_constant__ CUtensorMap tmO1, const GemmArgs args) {
   using S = GemmShape<BN, EPI, MX>;
   constexpr int STAGES = S::STAGES;
   constexpr uint32_t IDESC = MX ? idesc_mxf8(kBM, BN) : idesc_bf16(kBM, BN, A_MN, B_MN);
@@ -398,6 +116,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     if (EPI == EPI_WGRAD) tma_prefetch_desc(&tmC);
+    if (EPI != EPI_WGRAD) {
+      tma_prefetch_desc(&tmO0);
+      tma_prefetch_desc(&tmO1);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -435,38 +157,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             bulk_g2s(ssf, args.sfa + ga, 512u, fb);
             bulk_g2s(ssf + 512u, args.sfb + gb, 512u, fb);
           }
-          // A: 128 rows x 64 K
-          if (A_MN) {
-            // tensor [rows(K), M]: boxes cover 64 M columns x 64 K rows
-            tma_load_2d(sa, &tmA, ti.m0, ti.krow0 + kb * kBK, fb);
-            tma_load_2d(sa + kBoxBytes, &tmA, ti.m0 + 64, ti.krow0 + kb * kBK, fb);
-          } else {
-            // tensor [rows, K]: boxes cover 128 bytes of K x 64 rows
+          // One TMA per operand tile (large boxes: the TMA cost is per box).
+          // A: 128 rows x 128 bytes of K.  K-major: a 128-row box of [rows, K];
+          // MN-major: two 64-wide atoms of the [K rows, M] tensor (3-D map).
+          if (A_MN)
+            tma_load_3d(sa, &tmA, 0, ti.krow0 + kb * kBK, ti.m0 >> 6, fb);
+          else
             tma_load_2d(sa, &tmA, kb * KE, ti.m0, fb);
-            tma_load_2d(sa + kBoxBytes, &tmA, kb * KE, ti.m0 + 64, fb);
-          }
-          // B: BN rows (N) x 64 K
-#pragma unroll
-          for (int b = 0; b < BN / 64; ++b) {
-            if (args.wgrad) {
-              tma_load_2d(sb + b * kBoxBytes, &tmB, ti.n0 + 64 * b, ti.krow0 + kb * kBK, fb);
-            } else if (B_MN) {
-              // tensor [E*K, N]: 64 N columns x 64 K rows of expert e
-              tma_load_2d(sb + b * kBoxBytes, &tmB, ti.n0 + 64 * b,
-                          ti.e * args.b_expert_rows + kb * kBK, fb);
-            } else if (EPI == EPI_SWIGLU) {
-              // tensor [E*2I, d]: gate rows then up rows of this tile's columns
-              constexpr int NB2 = BN / 128;   // boxes per half
-              const int half = b / (NB2 > 0 ? NB2 : 1);
-              const int bi = b - half * NB2;
-              const int row = ti.e * args.b_expert_rows + half * args.b_half_rows +
-                              ti.nt * (BN / 2) + 64 * bi;
-              tma_load_2d(sb + b * kBoxBytes, &tmB, kb * KE, row, fb);
-            } else {
-              // tensor [E*N, K]
-              tma_load_2d(sb + b * kBoxBytes, &tmB, kb * KE,
-                          ti.e * args.b_expert_rows + ti.n0 + 64 * b, fb);
-            }
+          // B: BN rows (N) x 128 bytes of K
+          if (args.wgrad) {
+            tma_load_3d(sb, &tmB, 0, ti.krow0 + kb * kBK, ti.n0 >> 6, fb);
+          } else if (B_MN) {
+            // [E*K, N]: BN/64 atoms of expert e's K rows
+            tma_load_3d(sb, &tmB, 0, ti.e * args.b_expert_rows + kb * kBK, ti.n0 >> 6, fb);
+          } else if (EPI == EPI_SWIGLU) {
+            // [E*2I, K]: the gate rows, then the up rows, of this tile's columns
+            constexpr int BNH = BN / 2;
+            const int row = ti.e * args.b_expert_rows + ti.nt * BNH;
+            tma_load_2d(sb, &tmB, kb * KE, row, fb);
+            tma_load_2d(sb + BNH * 128, &tmB, kb * KE, row + args.b_half_rows, fb);
+          } else {
+            // [E*N, K]: a BN-row box
+            tma_load_2d(sb, &tmB, kb * KE, ti.e * args.b_expert_rows + ti.n0, fb);
           }
           issued_parity[stage] = (int)phase;
         }
@@ -578,14 +290,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = (warp - 2) >> 2;         // warps 2..5: columns' first half, 6..9: second
     int acc = 0;
     uint32_t acc_phase = 0;
-    int sub = 0;                              // WGRAD staging-buffer sequence number
+    int sub = 0;                              // output staging-buffer sequence number
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const TileInfo ti = decode_tile<BN>(args, tile);
       int w = 1;
       if (lane == 0) w = mbar_wait(tfull_bar(acc), acc_phase, &abort_s, args.err, 5, wlim);
       // all eight epilogue warps leave together, so their named barriers stay matched
       const int ok_warp = __shfl_sync(0xffffffffu, w, 0);
-      if (EPI == EPI_WGRAD) {
+      // epilogues that share named barriers leave together; the others per warp
+      if (EPI == EPI_WGRAD || EPI == EPI_SCORE || EPI == EPI_STORE) {
         if (epi_bar_and(ok_warp) == 0) break;
       } else if (ok_warp == 0) {
         break;
@@ -598,13 +311,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       else if constexpr (MX && EPI == EPI_SWIGLU)
         epilogue_swiglu_mx<BN>(args, ti, row, tbase, half);
       else
-        epilogue<BN, EPI>(args, ti, row, tbase, half);
+        epilogue<BN, EPI>(args, ti, row, tbase, half, &tmO0, &tmO1,
+                          stage0 + STAGES * S::STAGE_BYTES, et, sub);
       tc_fence_before();
       mbar_arrive(tempty_bar(acc));
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
-    if (EPI == EPI_WGRAD && et == 0) bulk_wait_all();   // every gradient add has landed
+    if (et == 0) bulk_wait_all();   // every output store / gradient add has completed
   }
 
   tc_fence_before();
@@ -617,7 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int BN, bool A_MN, bool B_MN, int EPI, bool MX>
 cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
-                       const GemmArgs& args, int grid, cudaStream_t stream) {
+                       const CUtensorMap& to0, const CUtensorMap& to1, const GemmArgs& args,
+                       int grid, cudaStream_t stream) {
   auto kern = k_grouped_gemm<BN, A_MN, B_MN, EPI, MX>;
   const int smem = GemmShape<BN, EPI, MX>::SMEM_BYTES;
   static bool configured = false;   // attribute set once per process (same device image)
@@ -626,25 +341,26 @@ cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUten
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  kern<<<grid, kThreads, smem, stream>>>(ta, tb, tc, args);
+  kern<<<grid, kThreads, smem, stream>>>(ta, tb, tc, to0, to1, args);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_gemm(int epi, int bn, bool a_mn, bool b_mn, const CUtensorMap& ta,
-                        const CUtensorMap& tb, const CUtensorMap& tc, const GemmArgs& args,
-                        int grid, cudaStream_t stream, bool mx) {
+                        const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& to0,
+                        const CUtensorMap& to1, const GemmArgs& args, int grid,
+                        cudaStream_t stream, bool mx) {
   if (mx) {
     if (epi == EPI_SWIGLU && bn == 128 && !a_mn && !b_mn)
-      return launch_one<128, false, false, EPI_SWIGLU, true>(ta, tb, tc, args, grid, stream);
+      return launch_one<128, false, false, EPI_SWIGLU, true>(ta, tb, tc, to0, to1, args, grid, stream);
     if (epi == EPI_SCORE && bn == 128 && !a_mn && !b_mn)
-      return launch_one<128, false, false, EPI_SCORE, true>(ta, tb, tc, args, grid, stream);
+      return launch_one<128, false, false, EPI_SCORE, true>(ta, tb, tc, to0, to1, args, grid, stream);
     return cudaErrorInvalidValue;
   }
 #define MOE_CASE(EPI_, BN_, AMN_, BMN_)                                     \
   if (epi == EPI_ && bn == BN_ && a_mn == AMN_ && b_mn == BMN_)             \
-    return launch_one<BN_, AMN_, BMN_, EPI_, false>(ta, tb, tc, args, grid, stream);
+    return launch_one<BN_, AMN_, BMN_, EPI_, false>(ta, tb, tc, to0, to1, args, grid, stream);
   MOE_CASE(EPI_SWIGLU, 128, false, false)
   MOE_CASE(EPI_SWIGLU, 256, false, false)
   MOE_CASE(EPI_SCORE, 128, false, false)

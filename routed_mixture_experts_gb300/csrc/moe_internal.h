@@ -70,9 +70,17 @@ struct GemmArgs {
   DevError* err;
 };
 
-// Encode a 2-D bf16 tensor map (row-major [rows, cols]) with a 64 x 64 box and
-// 128-byte swizzle, the operand box of the GEMM kernels.
-int encode_tmap_bf16(CUtensorMap* map, const void* base, long long rows, long long cols);
+// Encode a 2-D bf16 tensor map (row-major [rows, cols]) with a 64-column x
+// box_rows box and 128-byte swizzle: K-major GEMM operand tiles (the TMA cost is
+// per box, so a tile is loaded with one box).
+int encode_tmap_bf16(CUtensorMap* map, const void* base, long long rows, long long cols,
+                     int box_rows);
+
+// Encode an MN-major operand view of a bf16 [krows, ncols] tensor: 3-D (64, krows,
+// ncols/64) with box (64, 64, atoms), so one load lands `atoms` 64-wide atoms of
+// 64 K rows each, 8 KB apart, in the 128-byte-swizzled MN-major tile layout.
+int encode_tmap_bf16_mn(CUtensorMap* map, const void* base, long long krows, long long ncols,
+                        int atoms);
 
 // Encode a 2-D fp32 tensor map (row-major [rows, cols]) with a 32 x 128 box
 // (128 bytes x 128 rows) and 128-byte swizzle: the weight-gradient tiles that the
@@ -80,20 +88,30 @@ int encode_tmap_bf16(CUtensorMap* map, const void* base, long long rows, long lo
 int encode_tmap_f32_out(CUtensorMap* map, const void* base, long long rows, long long cols);
 
 // Launch the grouped GEMM.  a_mn / b_mn select MN-major operands; tc is only
-// read by EPI_WGRAD (the fp32 gradient [E*M, N]).
+// read by EPI_WGRAD (the fp32 gradient [E*M, N]); to0 / to1 are the bf16 output
+// tensors of the TMA-store epilogues (128-row boxes):
+//   EPI_SWIGLU: h, a    EPI_SCORE: ys    EPI_STORE: out    EPI_DGRAD2: dA, hs
 cudaError_t launch_gemm(int epi, int bn, bool a_mn, bool b_mn, const CUtensorMap& ta,
-                        const CUtensorMap& tb, const CUtensorMap& tc, const GemmArgs& args,
-                        int grid, cudaStream_t stream, bool mx = false);
+                        const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& to0,
+                        const CUtensorMap& to1, const GemmArgs& args, int grid,
+                        cudaStream_t stream, bool mx = false);
 
-// 2-D uint8 tensor map (row-major [rows, cols]) with a 128-byte x 64-row box and
-// 128-byte swizzle: the E4M3 operand box of the MXFP8 GEMMs.
-int encode_tmap_u8(CUtensorMap* map, const void* base, long long rows, long long cols);
+// Launch the CTA-pair grouped GEMM over routed rows (256 x 256 tiles, A K-major;
+// requires expert segments padded to 256 rows and N % 256 == 0).
+cudaError_t launch_gemm_pair(int epi, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
+                             const CUtensorMap& to0, const CUtensorMap& to1, const GemmArgs& args,
+                             int grid, cudaStream_t stream);
+
+// 2-D uint8 tensor map (row-major [rows, cols]) with a 128-byte x box_rows box and
+// 128-byte swizzle: the E4M3 operand tiles of the MXFP8 GEMMs.
+int encode_tmap_u8(CUtensorMap* map, const void* base, long long rows, long long cols,
+                   int box_rows);
 
 // Dispatch kernels.
 struct RouteArgs {
   const int32_t* ids;
   const float* scores;
-  int T, k, E, BM;
+  int T, k, E, BM;             // BM: padding granule of expert segments (multiple of 128)
   int nblk;                  // ceil(T*k / 1024)
   int32_t* blockcounts;      // [nblk, E]
   int32_t* counts;           // [E]

@@ -116,13 +116,13 @@ __global__ void __launch_bounds__(kMaxE) k_route_scan(RouteArgs a) {
     if (tid == E - 1) {
       a.m_indptr[E] = ec + c;
       a.off_pad[E] = ep + p;
-      *a.num_mtiles = (ep + p) / a.BM;
+      *a.num_mtiles = (ep + p) / kBM;          // 128-row GEMM m tiles
     }
   }
   __syncthreads();
   if (tid < E) {
     // m tiles of this expert, and its padding rows
-    for (int r = ep; r < ep + p; r += a.BM) a.tile_expert[r / a.BM] = tid;
+    for (int r = ep; r < ep + p; r += kBM) a.tile_expert[r / kBM] = tid;
     for (int r = ep + c; r < ep + p; ++r) {
       a.token_of[r] = -1;
       a.score_of[r] = 0.f;

@@ -41,11 +41,12 @@ def bits(t):
     return t.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def check_dispatch(orc, inp, g, BM=128):
-    """Dispatch tables: bit-exact against the oracle's stable counting sort."""
+def check_dispatch(orc, inp, g):
+    """Dispatch tables: bit-exact against the oracle's stable counting sort with
+    the plan's padding granule."""
     c = inp["cfg"]
-    r = orc.dispatch(inp["ids"], c["E"], BM)
     plan = g["plan"]
+    r = orc.dispatch(inp["ids"], c["E"], plan.row_granule())
     mi_ = plan.buffer("m_indptr", torch.int32).cpu().numpy()
     op = plan.buffer("off_pad", torch.int32).cpu().numpy()
     ro = plan.buffer("row_of", torch.int32).cpu().numpy()[: c["T"] * c["k"]].reshape(c["T"], c["k"])

@@ -23,9 +23,11 @@ def moe():
     return m
 
 
-@pytest.mark.parametrize("precision", ["bf16", "mxfp8"])
-def test_wait_timeout_is_reported_and_context_survives(moe, orc, precision):
-    inp = make(None, seed=31, train=False, T=256, d=128, I=128, E=4, k=2)
+@pytest.mark.parametrize("precision,d,I", [("bf16", 128, 128), ("bf16", 256, 256),
+                                           ("mxfp8", 128, 128)])
+def test_wait_timeout_is_reported_and_context_survives(moe, orc, precision, d, I):
+    """(bf16, 256, 256) runs the CTA-pair W13 kernel; the others the one-CTA kernel."""
+    inp = make(None, seed=31, train=False, T=256, d=d, I=I, E=4, k=2)
     c = inp["cfg"]
     dev = to_dev(inp)
     prec = moe.MOE_PREC_BF16 if precision == "bf16" else moe.MOE_PREC_MXFP8
