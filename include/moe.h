@@ -311,9 +311,19 @@ int moe_dispatch_static(const int32_t* ids, const float* scores, int T, int k, i
 int moe_tile_rows(void);
 
 /*
- * Padding granule of this plan's expert segments (off_pad): 256 when the bf16
- * row GEMMs run on CTA pairs (d % 256 == 0 and I % 256 == 0), else 128.
+ * Row GEMMs on CTA pairs.  on = 1 runs the four row GEMMs of a bf16 plan (W13,
+ * W2, and the two DGRADs) on pairs of CTAs of a thread-block cluster with
+ * 256 x 256 tiles (tcgen05 cta_group::2): each CTA reads a third less operand
+ * data per product, but expert segments are then padded to 256 rows instead of
+ * 128, which pays off when experts receive many rows (few experts, large T).
+ * Must be called before moe_plan_workspace_bytes / moe_plan_set_workspace
+ * (MOE_ERR_STATE afterwards); needs d % 256 == 0 and I % 256 == 0 (else
+ * MOE_ERR_UNSUPPORTED).  Off by default.
  */
+int moe_plan_set_cta_pairs(moe_plan* plan, int on);
+
+/* Padding granule of this plan's expert segments (off_pad): 256 with CTA pairs,
+ * else 128. */
 int moe_plan_row_granule(const moe_plan* plan);
 
 /*

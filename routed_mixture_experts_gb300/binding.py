@@ -52,6 +52,7 @@ def _declare(L):
     L.moe_status_string.restype = ctypes.c_char_p
     L.moe_plan_buffer.argtypes = [vp, i32, ctypes.POINTER(vp), ctypes.POINTER(sz)]
     L.moe_tile_rows.restype = i32
+    L.moe_plan_set_cta_pairs.argtypes = [vp, i32]
     L.moe_plan_row_granule.argtypes = [vp]
     L.moe_plan_row_granule.restype = i32
     L.moe_gemm_scratch_bytes.argtypes = [i32, i32]
@@ -67,7 +68,7 @@ def _declare(L):
     for name in ("moe_plan_set_swiglu_clamp", "moe_plan_set_workspace", "moe_forward",
                  "moe_backward", "moe_step_host", "moe_quantize_mxfp8", "moe_plan_check",
                  "moe_plan_buffer", "moe_gemm_bf16", "moe_plan_set_timing_events",
-                 "moe_prepare_weights_mxfp8", "moe_plan_set_debug"):
+                 "moe_prepare_weights_mxfp8", "moe_plan_set_debug", "moe_plan_set_cta_pairs"):
         getattr(L, name).restype = i32
     return L
 
@@ -105,7 +106,7 @@ class MoePlan:
     """A routed-expert layer plan with its workspace (a torch uint8 device tensor)."""
 
     def __init__(self, T, d, I, E, k, precision=MOE_PREC_BF16, clamp=0.0,
-                 flags=MOE_WS_TRAINING, device="cuda"):
+                 flags=MOE_WS_TRAINING, device="cuda", cta_pairs=False):
         import torch
 
         L = lib()
@@ -116,6 +117,8 @@ class MoePlan:
         if not self.ptr:
             raise MoeError(MOE_ERR_INVALID_ARG, "moe_plan_create(%d,%d,%d,%d,%d)" % (T, d, I, E, k))
         _check(L.moe_plan_set_swiglu_clamp(self.ptr, float(clamp)), "clamp")
+        if cta_pairs:
+            _check(L.moe_plan_set_cta_pairs(self.ptr, 1), "cta_pairs")
         nbytes = L.moe_plan_workspace_bytes(self.ptr, flags)
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
         _check(L.moe_plan_set_workspace(self.ptr, _p(self.workspace), nbytes, flags), "workspace")

@@ -369,9 +369,10 @@ moe_plan* moe_plan_create(int T, int d, int I, int E, int k, int precision) {
   memset(p, 0, sizeof(*p));
   p->T = T; p->d = d; p->I = I; p->E = E; p->k = k; p->precision = precision;
   p->R = T * k;
-  // CTA-pair row GEMMs need 256-row expert segments and N tiles of 256
-  p->pair = precision == MOE_PREC_BF16 && I % 256 == 0 && d % 256 == 0;
-  p->gran = p->pair ? 256 : kBM;
+  // one-CTA row GEMMs with 128-row expert segments unless CTA pairs are chosen
+  // (moe_plan_set_cta_pairs) before the workspace is sized
+  p->pair = 0;
+  p->gran = kBM;
   p->RP = (int)(((long long)p->R + (long long)E * (p->gran - 1)) / p->gran * p->gran);
   p->nblk = (p->R + 1023) / 1024;
   p->bn13 = I % 128 == 0 ? 256 : 128;
@@ -392,6 +393,16 @@ moe_plan* moe_plan_create(int T, int d, int I, int E, int k, int precision) {
 }
 
 void moe_plan_destroy(moe_plan* p) { delete p; }
+
+int moe_plan_set_cta_pairs(moe_plan* p, int on) {
+  if (!p) return MOE_ERR_INVALID_ARG;
+  if (p->ws) return MOE_ERR_STATE;               // the granule sizes the workspace
+  if (on && (p->precision != MOE_PREC_BF16 || p->I % 256 || p->d % 256)) return MOE_ERR_UNSUPPORTED;
+  p->pair = on ? 1 : 0;
+  p->gran = p->pair ? 256 : kBM;
+  p->RP = (int)(((long long)p->R + (long long)p->E * (p->gran - 1)) / p->gran * p->gran);
+  return MOE_OK;
+}
 
 int moe_plan_set_swiglu_clamp(moe_plan* p, float limit) {
   if (!p || !(limit >= 0.f)) return MOE_ERR_INVALID_ARG;

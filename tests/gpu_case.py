@@ -24,7 +24,8 @@ def run_gpu(moe, inp, train=True, stream=None):
     c = inp["cfg"]
     dev = to_dev(inp)
     plan = moe.MoePlan(c["T"], c["d"], c["I"], c["E"], c["k"], clamp=c.get("clamp", 0.0),
-                       flags=moe.MOE_WS_TRAINING if train else 0)
+                       flags=moe.MOE_WS_TRAINING if train else 0,
+                       cta_pairs=c.get("cta_pairs", False))
     out = {"plan": plan, "dev": dev}
     out["y"] = plan.forward(dev["x"], dev["ids"], dev["scores"], dev["w13"], dev["w2"], save=train)
     if train:

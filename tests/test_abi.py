@@ -92,3 +92,22 @@ def test_entry_points_reject_bad_arguments_on_host(L):
 def test_status_strings(L):
     for code, name in [(0, b"MOE_OK"), (4, b"MOE_ERR_BAD_IDS"), (5, b"MOE_ERR_TIMEOUT")]:
         assert L.moe_status_string(code) == name
+
+
+def test_cta_pairs_option_sizes_the_workspace(L):
+    p = L.moe_plan_create(8192, 2048, 768, 128, 8, 0)
+    q = L.moe_plan_create(64, 128, 64, 4, 2, 0)
+    m = L.moe_plan_create(8192, 2048, 768, 128, 8, 1)
+    try:
+        assert L.moe_plan_row_granule(p) == 128
+        one = L.moe_plan_workspace_bytes(p, 1)
+        assert L.moe_plan_set_cta_pairs(p, 1) == 0
+        assert L.moe_plan_row_granule(p) == 256
+        assert L.moe_plan_workspace_bytes(p, 1) > one          # 256-row padding
+        assert L.moe_plan_set_cta_pairs(p, 0) == 0
+        assert L.moe_plan_workspace_bytes(p, 1) == one
+        assert L.moe_plan_set_cta_pairs(q, 1) == 7             # d, I not multiples of 256
+        assert L.moe_plan_set_cta_pairs(m, 1) == 7             # MXFP8 plans: one-CTA only
+    finally:
+        for x in (p, q, m):
+            L.moe_plan_destroy(x)

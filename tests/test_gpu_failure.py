@@ -23,15 +23,16 @@ def moe():
     return m
 
 
-@pytest.mark.parametrize("precision,d,I", [("bf16", 128, 128), ("bf16", 256, 256),
-                                           ("mxfp8", 128, 128)])
-def test_wait_timeout_is_reported_and_context_survives(moe, orc, precision, d, I):
-    """(bf16, 256, 256) runs the CTA-pair W13 kernel; the others the one-CTA kernel."""
+@pytest.mark.parametrize("precision,pairs", [("bf16", False), ("bf16", True), ("mxfp8", False)])
+def test_wait_timeout_is_reported_and_context_survives(moe, orc, precision, pairs):
+    """pairs=True runs the CTA-pair W13 kernel; the others the one-CTA kernel."""
+    d = I = 256 if pairs else 128
     inp = make(None, seed=31, train=False, T=256, d=d, I=I, E=4, k=2)
     c = inp["cfg"]
     dev = to_dev(inp)
     prec = moe.MOE_PREC_BF16 if precision == "bf16" else moe.MOE_PREC_MXFP8
-    plan = moe.MoePlan(c["T"], c["d"], c["I"], c["E"], c["k"], precision=prec, flags=0)
+    plan = moe.MoePlan(c["T"], c["d"], c["I"], c["E"], c["k"], precision=prec, flags=0,
+                       cta_pairs=pairs)
     w = dict(w13=dev["w13"], w2=dev["w2"], sf13=None, sf2=None)
     if precision == "mxfp8":
         w["w13"], w["sf13"], w["w2"], w["sf2"] = moe.prepare_weights_mxfp8(dev["w13"], dev["w2"])

@@ -53,8 +53,9 @@ def test_infer_e16_forward(moe, orc):
     check_forward(orc, inp, g, toks=toks)
 
 
-def test_train_e128_forward_backward(moe, orc):
-    inp = make("train_e128", train=True)
+@pytest.mark.parametrize("pairs", [False, True], ids=["one_cta", "cta_pairs"])
+def test_train_e128_forward_backward(moe, orc, pairs):
+    inp = make("train_e128", train=True, cta_pairs=pairs)
     g = run_gpu(moe, inp, train=True)
     assert g["rc"] == 0
     check_dispatch(orc, inp, g)
