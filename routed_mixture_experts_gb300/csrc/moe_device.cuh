@@ -37,8 +37,11 @@ __device__ __forceinline__ uint16_t f2bf(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
+// two floats to a bf16 pair (lo in the low half), one round-to-nearest-even
+// conversion instruction
 __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
-  return (uint32_t)f2bf(lo) | ((uint32_t)f2bf(hi) << 16);
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
 }
 
 // ---------------------------------------------------------------------------

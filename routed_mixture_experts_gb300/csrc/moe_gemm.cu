@@ -45,7 +45,8 @@ struct GemmShape {
   // sub-tile buffers for the TMA-store epilogues.
   static constexpr int OUT_BYTES =
       (EPI == EPI_WGRAD ? kWgradBufs
-                        : (EPI == EPI_SCORE || EPI == EPI_STORE ? kEpiStageBufs : 0)) * 16384;
+                        : (EPI == EPI_SCORE || EPI == EPI_STORE ? kEpiStageBufs
+                                                                : (MX ? 0 : tri_bufs<EPI>()))) * 16384;
   static constexpr int STAGE_BUDGET = 226 * 1024 - OUT_BYTES;
   static constexpr int STAGES = STAGE_BUDGET / STAGE_BYTES > 8 ? 8 : STAGE_BUDGET / STAGE_BYTES;
   static constexpr int BAR_BYTES = 256;
@@ -298,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // all eight epilogue warps leave together, so their named barriers stay matched
       const int ok_warp = __shfl_sync(0xffffffffu, w, 0);
       // epilogues that share named barriers leave together; the others per warp
-      if (EPI == EPI_WGRAD || EPI == EPI_SCORE || EPI == EPI_STORE) {
+      if (!(MX && EPI == EPI_SWIGLU)) {
         if (epi_bar_and(ok_warp) == 0) break;
       } else if (ok_warp == 0) {
         break;

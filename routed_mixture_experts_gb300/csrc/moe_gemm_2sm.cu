@@ -35,7 +35,7 @@ constexpr uint32_t kPairTmemCols = 512;      // two 256-column accumulators
 // bf16 output staging (one-output epilogues) and the pipeline depth it leaves
 template <int EPI>
 struct PairShape {
-  static constexpr int OUT_BYTES = (EPI == EPI_SCORE || EPI == EPI_STORE) ? kEpiStageBufs * 16384 : 0;
+  static constexpr int OUT_BYTES = ((EPI == EPI_SCORE || EPI == EPI_STORE) ? kEpiStageBufs : tri_bufs<EPI>()) * 16384;
   // at most 6 stages (192 KB): the rest of the on-chip memory stays L1 for the
   // epilogues' row loads (SwiGLU backward reads h and a per row)
   static constexpr int STAGES_FIT = (226 * 1024 - OUT_BYTES) / kPairStageBytes;
@@ -270,11 +270,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane == 0) w = mbar_wait_cluster(tfull_bar(acc), acc_phase, &abort_s, args.err, 5, wlim);
       // epilogues that share named barriers leave together; the others per warp
       const int ok_warp = __shfl_sync(0xffffffffu, w, 0);
-      if (EPI == EPI_SCORE || EPI == EPI_STORE) {
-        if (epi_bar_and(ok_warp) == 0) break;
-      } else if (ok_warp == 0) {
-        break;
-      }
+      if (epi_bar_and(ok_warp) == 0) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
       epilogue<BN, EPI>(args, ti, row, tbase, half, &tmO0, &tmO1, out0, et, seq);

@@ -78,12 +78,21 @@ __device__ __forceinline__ int epi_bar_and(int v) {
   return r;
 }
 
+// logistic sigmoid with the hardware exponential and reciprocal (CUDA's __expf
+// and __fdividef intrinsics, a few ulp of fp32): far below the bf16 rounding
+// the SwiGLU outputs go through.  Large negative G gives exp = inf and sig = 0.
+// The forward (swiglu_fwd) and the backward's recomputation of h use this one
+// function, so both see the same h.
+__device__ __forceinline__ float sigmoid_fast(float G) {
+  return __fdividef(1.0f, 1.0f + __expf(-G));
+}
+
 __device__ __forceinline__ float swiglu_fwd(float G, float U, float L) {
   if (L > 0.f) {
     G = fminf(fmaxf(G, -L), L);
     U = fminf(fmaxf(U, -L), L);
   }
-  const float silu = G / (1.0f + expf(-G));
+  const float silu = G * sigmoid_fast(G);
   return silu * U;
 }
 
@@ -162,6 +171,16 @@ __device__ __forceinline__ void epilogue_swiglu_mx(const GemmArgs& a, const Tile
 // the 64 columns of its row), then one thread stores it with TMA.  Two buffers
 // alternate; a buffer is rewritten only once its previous store has read it.
 constexpr int kEpiStageBufs = 2;
+// 16 KB staging buffers of the three-output epilogues.  SwiGLU forward keeps four
+// 48 KB operand stages with two buffers (its main loop is the longer part);
+// SwiGLU backward, whose epilogue also reads the forward's activations, goes
+// faster with three buffers and three stages (measured on the E = 128 training
+// shapes).
+template <int EPI>
+__host__ __device__ constexpr int tri_bufs() { return EPI == EPI_DGRAD2 ? 3 : 2; }
+
+// SwiGLU backward: recompute h from the saved pre-activations instead of reading it.
+constexpr bool kRecomputeH = true;
 
 __device__ __forceinline__ void epi_stage_store(const CUtensorMap* tm, uint32_t out0, int& seq,
                                                 int et, int row, int half, const float (&v)[32],
@@ -185,6 +204,66 @@ __device__ __forceinline__ void epi_stage_store(const CUtensorMap* tm, uint32_t 
   ++seq;
 }
 
+// Batched staging for epilogues with several outputs: NOUT sub-tiles of one
+// 64-column chunk (this thread's 32 columns of each, already packed to bf16
+// pairs) go to NOUT consecutive 16 KB buffers from `buf` and leave as NOUT TMA
+// stores under one pair of barriers.  Buffers are reused only after the previous
+// batch's stores have read them; the caller computes the next chunk before
+// calling, so that wait overlaps the previous stores.
+template <int NOUT>
+__device__ __forceinline__ void epi_stage_batch(const CUtensorMap* const (&tms)[NOUT],
+                                                uint32_t buf, int et, int row, int half,
+                                                const uint32_t (&pk)[NOUT][16],
+                                                const int (&xs)[NOUT], int y) {
+  if (et == 0) bulk_wait_read<0>();
+  named_bar_sync(1, kEpiThreads);
+  const uint32_t sw = (uint32_t)(row & 7);
+#pragma unroll
+  for (int o = 0; o < NOUT; ++o) {
+    const uint32_t rbase = buf + (uint32_t)o * 16384u + (uint32_t)row * 128u;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      st_shared_v4_u32(rbase + (((uint32_t)(4 * half + q) ^ sw) << 4), pk[o][4 * q],
+                       pk[o][4 * q + 1], pk[o][4 * q + 2], pk[o][4 * q + 3]);
+  }
+  fence_proxy_async_smem();
+  named_bar_sync(1, kEpiThreads);
+  if (et == 0) {
+#pragma unroll
+    for (int o = 0; o < NOUT; ++o) tma_store_2d(tms[o], buf + (uint32_t)o * 16384u, xs[o], y);
+    bulk_commit();
+  }
+}
+
+// The three sub-tiles of a chunk (SwiGLU forward: h, a gate, a up; backward:
+// dA gate, dA up, hs) leave as one batch through three buffers, else as a batch
+// of the first two and then the third, through two.
+template <int NBUF>
+__device__ __forceinline__ void epi_stage_three(const CUtensorMap* t0, const CUtensorMap* t1,
+                                                const CUtensorMap* t2, uint32_t buf, int et,
+                                                int row, int half, const uint32_t (&pk)[3][16],
+                                                int x0, int x1, int x2, int y) {
+  if constexpr (NBUF >= 3) {
+    const CUtensorMap* const tms[3] = {t0, t1, t2};
+    const int xs[3] = {x0, x1, x2};
+    epi_stage_batch<3>(tms, buf, et, row, half, pk, xs, y);
+  } else {
+    const CUtensorMap* const tms2[2] = {t0, t1};
+    const int xs2[2] = {x0, x1};
+    const uint32_t(&pk2)[2][16] = *reinterpret_cast<const uint32_t(*)[2][16]>(&pk[0]);
+    epi_stage_batch<2>(tms2, buf, et, row, half, pk2, xs2, y);
+    const CUtensorMap* const tms1[1] = {t2};
+    const int xs1[1] = {x2};
+    const uint32_t(&pk1)[1][16] = *reinterpret_cast<const uint32_t(*)[1][16]>(&pk[2]);
+    epi_stage_batch<1>(tms1, buf, et, row, half, pk1, xs1, y);
+  }
+}
+
+__device__ __forceinline__ void pack32(const float (&v)[32], uint32_t (&pk)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) pk[i] = pack_bf2(v[2 * i], v[2 * i + 1]);
+}
+
 __device__ __forceinline__ void load32_bf16(const uint16_t* src, float (&v)[32]) {
   float a[16], b[16];
   load16_bf16(src, a);
@@ -196,13 +275,12 @@ __device__ __forceinline__ void load32_bf16(const uint16_t* src, float (&v)[32])
   }
 }
 
-// bf16-output epilogues.  One-output epilogues (W2 x score, plain store) walk
-// the tile in 64-column sub-tiles, the thread owning row `row` handling columns
-// [32*half, 32*half+32) of each, and leave through epi_stage_store (tmO0: the
-// output tensor's map).  The three-output epilogues (SwiGLU: h and a; SwiGLU
-// backward: dA and hs) store their rows directly, each thread taking one half
-// of the tile's columns: staging three outputs through two buffers serialises
-// them on the buffer reuse.
+// bf16-output epilogues.  The tile is walked in 64-column sub-tiles, the thread
+// owning row `row` handling columns [32*half, 32*half+32) of each; outputs leave
+// through shared-memory staging and TMA stores (tmO0 / tmO1: the output tensors'
+// maps): one-output epilogues (W2 x score, plain store) through two alternating
+// buffers, the three-output ones (SwiGLU: h and a; SwiGLU backward: dA and hs)
+// as batches of three buffers per chunk.
 template <int BN, int EPI>
 __device__ __forceinline__ void epilogue(const GemmArgs& a, const TileInfo& ti, int row,
                                          uint32_t tbase, int half, const CUtensorMap* tmO0,
@@ -212,28 +290,39 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, const TileInfo& ti, 
   uint32_t r0[16], r1[16];
   const int ch = 32 * half;
   if constexpr (EPI == EPI_SWIGLU) {
-    // direct row stores (three outputs per column block: h and both halves of a)
+    // per 64-column chunk: h, and (training) the gate and up halves of a
     constexpr int BNH = BN / 2;          // gate columns [0,BNH), up columns [BNH,BN)
-    constexpr int WH = BNH / 2;          // this thread's half of them
     const int c0 = ti.nt * BNH;          // first intermediate column of this tile
-    uint16_t* h = static_cast<uint16_t*>(a.out0) + grow * a.ld0 + c0;
-    uint16_t* av = static_cast<uint16_t*>(a.out1) + grow * a.ld1 + c0;
 #pragma unroll 1
-    for (int c = half * WH; c < (half + 1) * WH; c += 16) {
-      tmem_ld16(tbase + c, r0);
-      tmem_ld16(tbase + BNH + c, r1);
+    for (int c = 0; c < BNH; c += 64) {
+      float G[32], U[32], hv[32];
+      tmem_ld16(tbase + c + ch, r0);
+      tmem_ld16(tbase + c + ch + 16, r1);
       tmem_ld_wait();
-      float G[16], U[16], hv[16];
 #pragma unroll
       for (int q = 0; q < 16; ++q) {
         G[q] = bf2f(f2bf(__uint_as_float(r0[q])));   // R1
-        U[q] = bf2f(f2bf(__uint_as_float(r1[q])));
-        hv[q] = swiglu_fwd(G[q], U[q], a.clamp);      // R2 on store
+        G[16 + q] = bf2f(f2bf(__uint_as_float(r1[q])));
       }
-      store16_bf16(h + c, hv);
+      tmem_ld16(tbase + BNH + c + ch, r0);
+      tmem_ld16(tbase + BNH + c + ch + 16, r1);
+      tmem_ld_wait();
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        U[q] = bf2f(f2bf(__uint_as_float(r0[q])));
+        U[16 + q] = bf2f(f2bf(__uint_as_float(r1[q])));
+      }
+#pragma unroll
+      for (int q = 0; q < 32; ++q) hv[q] = swiglu_fwd(G[q], U[q], a.clamp);   // R2 on store
       if (a.save) {
-        store16_bf16(av + c, G);
-        store16_bf16(av + a.I + c, U);
+        uint32_t pk[3][16];
+        pack32(hv, pk[0]);
+        pack32(G, pk[1]);
+        pack32(U, pk[2]);
+        epi_stage_three<tri_bufs<EPI_SWIGLU>()>(tmO0, tmO1, tmO1, out0, et, row, half, pk, c0 + c, c0 + c,
+                                  a.I + c0 + c, ti.m0);
+      } else {
+        epi_stage_store(tmO0, out0, seq, et, row, half, hv, c0 + c, ti.m0);
       }
     }
   } else if constexpr (EPI == EPI_SCORE || EPI == EPI_STORE) {
@@ -252,49 +341,61 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, const TileInfo& ti, 
       epi_stage_store(tmO0, out0, seq, et, row, half, v, ti.n0 + c, ti.m0);
     }
   } else if constexpr (EPI == EPI_DGRAD2) {
-    // acc = g (columns = intermediate index i).  in0 = h [rows, I], in1 = a [rows, 2I],
-    // out0 = dA [rows, 2I], out1 = hs [rows, I]; direct row stores.
-    constexpr int W = BN / 2;
+    // acc = g (columns = intermediate index i).  in0 = h [rows, I], in1 = a [rows, 2I];
+    // per 64-column chunk: dA gate, dA up (tmO0 = dA [rows, 2I]) and hs (tmO1 = hs).
+    // With kRecomputeH, h is not read back: it is recomputed from a with the
+    // forward's own arithmetic (swiglu_fwd), which gives the stored bf16 value (R2).
     const float s = a.row_scale[grow];
     const float L = a.clamp;
     const uint16_t* hrow = static_cast<const uint16_t*>(a.in0) + grow * a.ldi0 + ti.n0;
     const uint16_t* arow = static_cast<const uint16_t*>(a.in1) + grow * a.ldi1 + ti.n0;
-    uint16_t* darow = static_cast<uint16_t*>(a.out0) + grow * a.ld0 + ti.n0;
-    uint16_t* hsrow = static_cast<uint16_t*>(a.out1) + grow * a.ld1 + ti.n0;
     float part = 0.f;
 #pragma unroll 1
-    for (int c = half * W; c < (half + 1) * W; c += 16) {
-      tmem_ld16(tbase + c, r0);
-      float hv[16], ag[16], au[16];
-      load16_bf16(hrow + c, hv);
-      load16_bf16(arow + c, ag);
-      load16_bf16(arow + a.I + c, au);
-      tmem_ld_wait();
-      float dg[16], du[16], hs[16];
+    for (int c = 0; c < BN; c += 64) {
+      uint32_t pk[3][16];
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const float g = __uint_as_float(r0[q]);
-        part += hv[q] * g;
-        float G = ag[q], U = au[q], mg = 1.f, mu = 1.f;
-        if (L > 0.f) {
-          if (G < -L || G > L) mg = 0.f;
-          if (U < -L || U > L) mu = 0.f;
-          G = fminf(fmaxf(G, -L), L);
-          U = fminf(fmaxf(U, -L), L);
+      for (int hh = 0; hh < 2; ++hh) {            // two 16-column halves of this thread's 32
+        const int cc = c + ch + 16 * hh;
+        tmem_ld16(tbase + cc, r0);
+        float hl[16], ag[16], au[16];
+        if constexpr (!kRecomputeH) load16_bf16(hrow + cc, hl);
+        load16_bf16(arow + cc, ag);
+        load16_bf16(arow + a.I + cc, au);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 16; q += 2) {
+          float dg2[2], du2[2], hs2[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const float g = __uint_as_float(r0[q + u]);
+            float G = ag[q + u], U = au[q + u], mg = 1.f, mu = 1.f;
+            if (L > 0.f) {
+              if (G < -L || G > L) mg = 0.f;
+              if (U < -L || U > L) mu = 0.f;
+              G = fminf(fmaxf(G, -L), L);
+              U = fminf(fmaxf(U, -L), L);
+            }
+            const float sig = sigmoid_fast(G);
+            const float silu = G * sig;                   // as in swiglu_fwd
+            float hv;
+            if constexpr (kRecomputeH) hv = bf2f(f2bf(silu * U));   // h (R2)
+            else hv = hl[q + u];
+            part += hv * g;
+            const float dh = s * g;
+            const float dsilu = sig * (1.0f + G * (1.0f - sig));
+            dg2[u] = dh * U * dsilu * mg;  // R4 on store
+            du2[u] = dh * silu * mu;
+            hs2[u] = s * hv;               // R7 on store
+          }
+          pk[0][8 * hh + q / 2] = pack_bf2(dg2[0], dg2[1]);
+          pk[1][8 * hh + q / 2] = pack_bf2(du2[0], du2[1]);
+          pk[2][8 * hh + q / 2] = pack_bf2(hs2[0], hs2[1]);
         }
-        const float dh = s * g;
-        const float sig = 1.0f / (1.0f + expf(-G));
-        const float silu = G * sig;
-        const float dsilu = sig * (1.0f + G * (1.0f - sig));
-        dg[q] = dh * U * dsilu * mg;       // R4 on store
-        du[q] = dh * silu * mu;
-        hs[q] = s * hv[q];                 // R7 on store
       }
-      store16_bf16(darow + c, dg);
-      store16_bf16(darow + a.I + c, du);
-      store16_bf16(hsrow + c, hs);
+      epi_stage_three<tri_bufs<EPI_DGRAD2>()>(tmO0, tmO0, tmO1, out0, et, row, half, pk, ti.n0 + c,
+                                a.I + ti.n0 + c, ti.n0 + c, ti.m0);
     }
-    // one partial per (n tile, column half), in column order
+    // one partial per (n tile, column half)
     a.pdscore[grow * (2 * a.n_tiles) + 2 * ti.nt + half] = part;
   }
 }
