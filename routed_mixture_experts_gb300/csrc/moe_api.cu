@@ -584,7 +584,6 @@ int moe_backward(moe_plan* p, const void* dy, const void* w13, const void* w2, v
     g.k_blocks = d / kBK;
     g.b_expert_rows = d;
     g.n_tiles = I / p->bnd2;
-    g.in0 = p->h; g.ldi0 = I;
     g.in1 = p->a; g.ldi1 = 2LL * I;
     g.out0 = p->dA; g.ld0 = 2LL * I;
     g.out1 = p->hs; g.ld1 = I;

@@ -179,9 +179,6 @@ constexpr int kEpiStageBufs = 2;
 template <int EPI>
 __host__ __device__ constexpr int tri_bufs() { return EPI == EPI_DGRAD2 ? 3 : 2; }
 
-// SwiGLU backward: recompute h from the saved pre-activations instead of reading it.
-constexpr bool kRecomputeH = true;
-
 __device__ __forceinline__ void epi_stage_store(const CUtensorMap* tm, uint32_t out0, int& seq,
                                                 int et, int row, int half, const float (&v)[32],
                                                 int x, int y) {
@@ -341,13 +338,12 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, const TileInfo& ti, 
       epi_stage_store(tmO0, out0, seq, et, row, half, v, ti.n0 + c, ti.m0);
     }
   } else if constexpr (EPI == EPI_DGRAD2) {
-    // acc = g (columns = intermediate index i).  in0 = h [rows, I], in1 = a [rows, 2I];
-    // per 64-column chunk: dA gate, dA up (tmO0 = dA [rows, 2I]) and hs (tmO1 = hs).
-    // With kRecomputeH, h is not read back: it is recomputed from a with the
-    // forward's own arithmetic (swiglu_fwd), which gives the stored bf16 value (R2).
+    // acc = g (columns = intermediate index i).  in1 = a [rows, 2I]; per 64-column
+    // chunk: dA gate, dA up (tmO0 = dA [rows, 2I]) and hs (tmO1 = hs).  h is not
+    // read back: it is recomputed from a with the forward's own arithmetic
+    // (swiglu_fwd), which gives the bf16 value the forward stored (R2).
     const float s = a.row_scale[grow];
     const float L = a.clamp;
-    const uint16_t* hrow = static_cast<const uint16_t*>(a.in0) + grow * a.ldi0 + ti.n0;
     const uint16_t* arow = static_cast<const uint16_t*>(a.in1) + grow * a.ldi1 + ti.n0;
     float part = 0.f;
 #pragma unroll 1
@@ -357,8 +353,7 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, const TileInfo& ti, 
       for (int hh = 0; hh < 2; ++hh) {            // two 16-column halves of this thread's 32
         const int cc = c + ch + 16 * hh;
         tmem_ld16(tbase + cc, r0);
-        float hl[16], ag[16], au[16];
-        if constexpr (!kRecomputeH) load16_bf16(hrow + cc, hl);
+        float ag[16], au[16];
         load16_bf16(arow + cc, ag);
         load16_bf16(arow + a.I + cc, au);
         tmem_ld_wait();
@@ -377,9 +372,7 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, const TileInfo& ti, 
             }
             const float sig = sigmoid_fast(G);
             const float silu = G * sig;                   // as in swiglu_fwd
-            float hv;
-            if constexpr (kRecomputeH) hv = bf2f(f2bf(silu * U));   // h (R2)
-            else hv = hl[q + u];
+            const float hv = bf2f(f2bf(silu * U));       // h (R2)
             part += hv * g;
             const float dh = s * g;
             const float dsilu = sig * (1.0f + G * (1.0f - sig));

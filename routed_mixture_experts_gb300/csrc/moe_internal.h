@@ -47,7 +47,6 @@ struct GemmArgs {
   // epilogue operands
   void* out0;  long long ld0;
   void* out1;  long long ld1;
-  const void* in0; long long ldi0;   // EPI_DGRAD2: h
   const void* in1; long long ldi1;   // EPI_DGRAD2: a
   const float* row_scale;    // score of each padded row
   float* pdscore;            // EPI_DGRAD2: [rows, 2*n_tiles] (n tile, column half)
