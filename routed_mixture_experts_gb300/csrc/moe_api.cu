@@ -144,6 +144,24 @@ int encode_tmap_u8(CUtensorMap* map, const void* base, long long rows, long long
                    (cuuint32_t)box_rows);
 }
 
+int encode_tmap_gate_up(CUtensorMap* map, bool fp8, const void* base, long long E, long long I,
+                        long long cols, int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = tmap_detail::encode_fn();
+  if (!fn) return MOE_ERR_CUDA;
+  const int esize = fp8 ? 1 : 2;
+  // [E, 2, I, cols] viewed as dims (cols, I, 2E): one box takes box_rows gate rows
+  // and the same rows of the up half
+  const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)I, (cuuint64_t)(2 * E)};
+  const cuuint64_t strides[2] = {(cuuint64_t)(cols * esize), (cuuint64_t)(I * cols * esize)};
+  const cuuint32_t box[3] = {(cuuint32_t)(128 / esize), (cuuint32_t)box_rows, 2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
 }  // namespace moe
 
 namespace {
@@ -235,7 +253,10 @@ int refresh_weight_maps(moe_plan* p, const void* w13, const void* w2) {
   const int b13 = p->pair ? 128 : p->bn13 / 2;
   const int b2 = p->pair ? 128 : p->bn2;
   if (w13 != p->w13_cached) {
-    if (encode_tmap_bf16(&p->tm_w13, w13, (long long)p->E * 2 * p->I, p->d, b13) != MOE_OK ||
+    // one-CTA W13: gate and up rows of a tile in one 3-D box; CTA pairs: 2-D boxes
+    const int r13 = p->pair ? encode_tmap_bf16(&p->tm_w13, w13, (long long)p->E * 2 * p->I, p->d, b13)
+                            : encode_tmap_gate_up(&p->tm_w13, false, w13, p->E, p->I, p->d, b13);
+    if (r13 != MOE_OK ||
         encode_tmap_bf16_mn(&p->tm_w13_mn, w13, (long long)p->E * 2 * p->I, p->d,
                             p->pair ? 2 : p->bn2 / 64) != MOE_OK)
       return MOE_ERR_CUDA;
@@ -469,7 +490,7 @@ int moe_forward(moe_plan* p, const void* x, const int32_t* ids, const float* sco
   cudaStream_t st = static_cast<cudaStream_t>(stream_v);
   if (mx) {
     if (w13 != p->w13q_cached) {
-      if (encode_tmap_u8(&p->tm_w13q, w13, (long long)p->E * 2 * p->I, p->d, 64)) return MOE_ERR_CUDA;
+      if (encode_tmap_gate_up(&p->tm_w13q, true, w13, p->E, p->I, p->d, 64)) return MOE_ERR_CUDA;
       p->w13q_cached = w13;
     }
     if (w2 != p->w2q_cached) {

@@ -79,13 +79,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * S::STAGE_BYTES + S::OUT_BYTES);
-  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain, WGRAD chunk loads
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
   auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
   auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  const uint32_t wg_bar0 = bar0 + 8u * (2 * STAGES + 5);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -103,6 +104,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(tempty_bar(b), kEpiThreads);
     }
     mbar_init(drain_bar, 1);
+    if (EPI == EPI_WGRAD)
+      for (int b = 0; b < kWgradBufs; ++b) mbar_init(wg_bar0 + 8u * b, 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -172,11 +175,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // [E*K, N]: BN/64 atoms of expert e's K rows
             tma_load_3d(sb, &tmB, 0, ti.e * args.b_expert_rows + kb * kBK, ti.n0 >> 6, fb);
           } else if (EPI == EPI_SWIGLU) {
-            // [E*2I, K]: the gate rows, then the up rows, of this tile's columns
-            constexpr int BNH = BN / 2;
-            const int row = ti.e * args.b_expert_rows + ti.nt * BNH;
-            tma_load_2d(sb, &tmB, kb * KE, row, fb);
-            tma_load_2d(sb + BNH * 128, &tmB, kb * KE, row + args.b_half_rows, fb);
+            // (K, I, 2E) view of W13: this tile's BN/2 gate rows, then the same up
+            // rows, in one box
+            tma_load_3d(sb, &tmB, kb * KE, ti.nt * (BN / 2), 2 * ti.e, fb);
           } else {
             // [E*N, K]: a BN-row box
             tma_load_2d(sb, &tmB, kb * KE, ti.e * args.b_expert_rows + ti.n0, fb);
@@ -292,6 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     int sub = 0;                              // output staging-buffer sequence number
+    WgradPipe wp{stage0 + STAGES * S::STAGE_BYTES, wg_bar0, num_tiles, 0, 0};
+    if (EPI == EPI_WGRAD && et == 0) wgrad_issue<BN>(args, &tmC, wp, kWgradBufs - 1);
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const TileInfo ti = decode_tile<BN>(args, tile);
       int w = 1;
@@ -306,10 +309,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
-      if constexpr (EPI == EPI_WGRAD)
-        epilogue_wgrad<BN>(args, &tmC, ti, row, tbase, stage0 + STAGES * S::STAGE_BYTES, et, half,
-                           sub);
-      else if constexpr (MX && EPI == EPI_SWIGLU)
+      if constexpr (EPI == EPI_WGRAD) {
+        if (!epilogue_wgrad<BN>(args, &tmC, ti, row, tbase, et, half, wp, &abort_s, wlim)) break;
+      } else if constexpr (MX && EPI == EPI_SWIGLU)
         epilogue_swiglu_mx<BN>(args, ti, row, tbase, half);
       else
         epilogue<BN, EPI>(args, ti, row, tbase, half, &tmO0, &tmO1,
@@ -319,7 +321,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
-    if (et == 0) bulk_wait_all();   // every output store / gradient add has completed
+    if (EPI == EPI_WGRAD && et == 0) {
+      // after an abort: let every gradient chunk load still in flight land
+      for (int n = wp.next; n < wp.issued; ++n)
+        mbar_wait_drain(wg_bar0 + 8u * (uint32_t)(n % kWgradBufs), (uint32_t)((n / kWgradBufs) & 1));
+    }
+    if (et == 0) bulk_wait_all();   // every output store has completed
   }
 
   tc_fence_before();

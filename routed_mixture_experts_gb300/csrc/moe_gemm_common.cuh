@@ -346,16 +346,37 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, const TileInfo& ti, 
     const float L = a.clamp;
     const uint16_t* arow = static_cast<const uint16_t*>(a.in1) + grow * a.ldi1 + ti.n0;
     float part = 0.f;
+    // the saved gate/up values of the next 16 columns are fetched one round ahead
+    uint4 nx[4];
+    auto fetch = [&](int cc) {
+      const uint4* gp = reinterpret_cast<const uint4*>(arow + cc);
+      const uint4* up = reinterpret_cast<const uint4*>(arow + a.I + cc);
+      nx[0] = gp[0]; nx[1] = gp[1]; nx[2] = up[0]; nx[3] = up[1];
+    };
+    fetch(ch);
 #pragma unroll 1
     for (int c = 0; c < BN; c += 64) {
       uint32_t pk[3][16];
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {            // two 16-column halves of this thread's 32
         const int cc = c + ch + 16 * hh;
+        const uint4 cur[4] = {nx[0], nx[1], nx[2], nx[3]};
+        if (hh == 0) fetch(cc + 16);
+        else if (c + 64 < BN) fetch(c + 64 + ch);
         tmem_ld16(tbase + cc, r0);
         float ag[16], au[16];
-        load16_bf16(arow + cc, ag);
-        load16_bf16(arow + a.I + cc, au);
+        {
+          const uint32_t w[16] = {cur[0].x, cur[0].y, cur[0].z, cur[0].w, cur[1].x, cur[1].y,
+                                  cur[1].z, cur[1].w, cur[2].x, cur[2].y, cur[2].z, cur[2].w,
+                                  cur[3].x, cur[3].y, cur[3].z, cur[3].w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            ag[2 * i] = __uint_as_float(w[i] << 16);
+            ag[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+            au[2 * i] = __uint_as_float(w[8 + i] << 16);
+            au[2 * i + 1] = __uint_as_float(w[8 + i] & 0xFFFF0000u);
+          }
+        }
         tmem_ld_wait();
 #pragma unroll
         for (int q = 0; q < 16; q += 2) {
@@ -393,44 +414,88 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, const TileInfo& ti, 
   }
 }
 
-// WGRAD epilogue: the accumulator tile is written, 32 columns at a time, into one
-// of kWgradBufs 16 KB shared-memory buffers (128 rows x 32 fp32, 128-byte swizzle, the
-// layout of the fp32 tensor map), and the TMA unit adds each buffer into the
-// fp32 gradient in global memory (cp.reduce.async.bulk.tensor .add).  The
-// read-modify-write then happens in L2 with many bytes in flight, instead of
-// through per-thread loads and stores.
-constexpr int kWgradBufs = 5;   // fp32 staging buffers of 16 KB (adds in flight per SM)
+// WGRAD epilogue: read-modify-write of the fp32 gradient, 32 columns (16 KB:
+// 128 rows x 32 fp32, 128-byte swizzle, the layout of the fp32 tensor map) at a
+// time.  Each such chunk is loaded by TMA into one of kWgradBufs shared-memory
+// buffers ahead of use (kWgradBufs - 1 chunks ahead, across tile boundaries),
+// every thread adds its row's accumulator values to it in place, and TMA stores
+// it back.  (A TMA reduce-add in L2 does the same sum but moves fp32 data
+// measurably slower than a load and a store.)  The chunk sequence is this CTA's
+// tiles blockIdx.x, blockIdx.x + gridDim.x, ... times BN/32 chunks each; each
+// output tile is visited once per launch, so no load can see a pending store.
+constexpr int kWgradBufs = 5;   // fp32 chunk buffers of 16 KB
+
+struct WgradPipe {
+  uint32_t buf0;     // first chunk buffer
+  uint32_t bar0;     // first of kWgradBufs load barriers
+  int num_tiles;
+  int next;          // chunks consumed (all epilogue threads)
+  int issued;        // chunks whose load has been issued (thread et == 0)
+};
 
 template <int BN>
-__device__ __forceinline__ void epilogue_wgrad(const GemmArgs& a, const CUtensorMap* tmC,
-                                               const TileInfo& ti, int row, uint32_t tbase,
-                                               uint32_t stage_smem, int et, int half, int& sub) {
-  if (ti.kb == 0) return;
+__device__ __forceinline__ void wgrad_issue(const GemmArgs& a, const CUtensorMap* tmC,
+                                            WgradPipe& p, int upto) {
+  constexpr int CH = BN / 32;
+  while (p.issued < upto) {
+    const int n = p.issued;
+    const int tile = (int)blockIdx.x + (n / CH) * (int)gridDim.x;
+    if (tile >= p.num_tiles) return;
+    const TileInfo t = decode_tile<BN>(a, tile);
+    const int b = n % kWgradBufs;
+    const uint32_t bar = p.bar0 + 8u * (uint32_t)b;
+    mbar_arrive_expect_tx(bar, 16384u);
+    tma_load_2d(p.buf0 + (uint32_t)b * 16384u, tmC, t.n0 + (n % CH) * 32,
+                t.e * a.m_tiles * kBM + t.m0, bar);
+    ++p.issued;
+  }
+}
+
+// Returns false when a wait gave up (every epilogue thread returns the same).
+template <int BN>
+__device__ __forceinline__ bool epilogue_wgrad(const GemmArgs& a, const CUtensorMap* tmC,
+                                               const TileInfo& ti, int row, uint32_t tbase, int et,
+                                               int half, WgradPipe& p, volatile int* abort_flag,
+                                               uint64_t wlim) {
   const int ybase = ti.e * a.m_tiles * kBM + ti.m0;
+  const uint32_t sw = (uint32_t)(row & 7);
   uint32_t r0[16];
 #pragma unroll 1
   for (int c = 0; c < BN; c += 32) {
-    const uint32_t buf = stage_smem + (uint32_t)(sub % kWgradBufs) * 16384u;
-    if (et == 0) bulk_wait_read<kWgradBufs - 1>();   // this buffer's previous add has read it
-    named_bar_sync(1, kEpiThreads);
-    // this thread's half: 16 of the sub-tile's 32 columns (16-byte chunks 4h..4h+3)
+    const int n = p.next;
+    const int b = n % kWgradBufs;
+    const uint32_t buf = p.buf0 + (uint32_t)b * 16384u;
+    // this thread's half: 16 of the chunk's 32 columns (16-byte chunks 4h..4h+3)
     tmem_ld16(tbase + c + 16 * half, r0);
+    const int w = mbar_wait(p.bar0 + 8u * (uint32_t)b, (uint32_t)((n / kWgradBufs) & 1),
+                            abort_flag, a.err, 6, wlim)
+                      ? 1 : 0;
     tmem_ld_wait();
-    const uint32_t rbase = buf + (uint32_t)row * 128u;
-    const uint32_t sw = (uint32_t)(row & 7);
+    if (w) {
+      const uint32_t rbase = buf + (uint32_t)row * 128u;
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      st_shared_v4(rbase + (((uint32_t)(q + 4 * half) ^ sw) << 4), __uint_as_float(r0[4 * q]),
-                   __uint_as_float(r0[4 * q + 1]), __uint_as_float(r0[4 * q + 2]),
-                   __uint_as_float(r0[4 * q + 3]));
-    fence_proxy_async_smem();
-    named_bar_sync(1, kEpiThreads);
-    if (et == 0) {
-      tma_reduce_add_2d(tmC, buf, ti.n0 + c, ybase);
-      bulk_commit();
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t addr = rbase + (((uint32_t)(q + 4 * half) ^ sw) << 4);
+        float v0, v1, v2, v3;
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(v0), "=f"(v1), "=f"(v2), "=f"(v3) : "r"(addr));
+        st_shared_v4(addr, v0 + __uint_as_float(r0[4 * q]), v1 + __uint_as_float(r0[4 * q + 1]),
+                     v2 + __uint_as_float(r0[4 * q + 2]), v3 + __uint_as_float(r0[4 * q + 3]));
+      }
     }
-    ++sub;
+    fence_proxy_async_smem();
+    if (epi_bar_and(w) == 0) return false;
+    p.next = n + 1;
+    if (et == 0) {
+      tma_store_2d(tmC, buf, ti.n0 + c, ybase);
+      bulk_commit();
+      // chunk n-1's buffer is free once its store has read it: load chunk
+      // n + kWgradBufs - 1 there
+      bulk_wait_read<1>();
+      wgrad_issue<BN>(a, tmC, p, n + kWgradBufs);
+    }
   }
+  return true;
 }
 
 }  // namespace gemm

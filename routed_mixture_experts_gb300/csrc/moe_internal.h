@@ -105,6 +105,11 @@ cudaError_t launch_gemm_pair(int epi, bool b_mn, const CUtensorMap& ta, const CU
 // 128-byte swizzle: the E4M3 operand tiles of the MXFP8 GEMMs.
 int encode_tmap_u8(CUtensorMap* map, const void* base, long long rows, long long cols,
                    int box_rows);
+// W13 [E, 2I, cols] (bf16, or E4M3 bytes) as (cols, I, 2E): a box of box_rows gate
+// rows of expert e followed by the same rows of its up half (coordinates
+// (k, row within the half, 2e)), one 128-byte swizzled K chunk wide
+int encode_tmap_gate_up(CUtensorMap* map, bool fp8, const void* base, long long E, long long I,
+                        long long cols, int box_rows);
 
 // Dispatch kernels.
 struct RouteArgs {
