@@ -199,13 +199,17 @@ def barrier():
 # CPU oracle timing (reference arm and cpu_baseline)
 
 
-def oracle_sample(inp, n_tokens, seconds, max_experts=None):
-    """Time the single-threaded oracle on forward+backward (with weight
-    gradients) of the routed rows of experts 0, 1, ... among the first
-    n_tokens tokens, until `seconds` have passed.  Returns (flops, seconds, experts)."""
+def oracle_sample(inp, n_tokens, seconds, max_experts=None, threads=0):
+    """Time the oracle on forward+backward (with weight gradients) of the routed
+    rows of experts 0, 1, ... among the first n_tokens tokens, until `seconds`
+    have passed, on `threads` host threads (0: all cores).  Returns (flops,
+    seconds, experts, threads used)."""
     from oracle import load_oracle
 
     orc = load_oracle("float")
+    n_all = orc.threads() if not hasattr(oracle_sample, "n_all") else oracle_sample.n_all
+    oracle_sample.n_all = n_all
+    used = orc.set_threads(threads if threads > 0 else n_all)
     c = inp["cfg"]
     sub = {k: inp[k][:n_tokens].copy() for k in ("x", "ids", "scores", "dy")}
     flops = 0.0
@@ -218,7 +222,8 @@ def oracle_sample(inp, n_tokens, seconds, max_experts=None):
         e += 1
         el = time.perf_counter() - t0
         if el >= seconds or (max_experts and e >= max_experts):
-            return flops, el, e
+            orc.set_threads(n_all)
+            return flops, el, e, used
 
 
 def run_reference(args):
@@ -233,10 +238,11 @@ def run_reference(args):
     n_tok = 1024
     # warm-up samples, then K timed samples (one expert's rows per step)
     oracle_sample(inp, n_tok, 0.0, max_experts=max(args.warmup, 1))
-    flops, el, ne = oracle_sample(inp, n_tok, 1e9, max_experts=args.steps)
+    flops, el, ne, cores = oracle_sample(inp, n_tok, 1e9, max_experts=args.steps)
     value = flops / el / 1e12
     sample = ("per step: forward+backward incl. weight gradients of the routed rows of one expert "
-              "among tokens 0..%d (%d steps, %.1f GFLOP, %.1f s)" % (n_tok - 1, ne, flops / 1e9, el))
+              "among tokens 0..%d (%d steps, %.1f GFLOP, %.1f s, %d host threads)"
+              % (n_tok - 1, ne, flops / 1e9, el, cores))
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / ne * 1e3,
@@ -244,7 +250,7 @@ def run_reference(args):
         "data": "synthetic",
         "config": {"workload": "%s (T=%d, d=%d, I=%d, E=%d, k=%d, uniform routing, forward+backward)"
                    % (WORKLOAD, c["T"], c["d"], c["I"], c["E"], c["k"])},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -451,11 +457,16 @@ def run_ours(args):
         return
     cpu = None
     if ws == 1 or rank == 0:
-        flops, el, ne = oracle_sample(inp, 1024, args.cpu_seconds)
-        cpu = {"value": flops / el / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+        # all host cores (the parallel oracle; same sums, same order), then one core
+        flops, el, ne, cores = oracle_sample(inp, 1024, 0.7 * args.cpu_seconds)
+        cpu = {"value": flops / el / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                "sample": "forward+backward incl. weight gradients of the routed rows of experts "
-                         "0..%d among tokens 0..1023 (%.2f GFLOP in %.1f s, single thread)"
-                         % (ne - 1, flops / 1e9, el)}
+                         "0..%d among tokens 0..1023 (%.2f GFLOP in %.1f s, %d host threads)"
+                         % (ne - 1, flops / 1e9, el, cores)}
+        f1, e1, n1c, _ = oracle_sample(inp, 1024, 0.3 * args.cpu_seconds, threads=1)
+        cpu["single_core"] = {"value": f1 / e1 / 1e12, "unit": "TFLOP/s", "cores": 1,
+                              "sample": "experts 0..%d, same tokens (%.2f GFLOP in %.1f s)"
+                                        % (n1c - 1, f1 / 1e9, e1)}
     ws_bytes = plan.workspace.numel() + sum(t.numel() * t.element_size() for t in D.values())
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": K,

@@ -44,12 +44,20 @@
 // -DORC_DOUBLE, which evaluates every sum and elementwise step in double (used to
 // bound the effect of FP32 summation order).
 //
+// Built with -fopenmp, the token loops of the forward and backward and the
+// output rows of WGRAD run on all host cores.  Every sum keeps its order (one
+// thread owns each output element and adds in the same index order), so the
+// results are bit-identical to the single-threaded build.
+//
 // bf16 values cross the C interface as raw uint16 bit patterns.
 
 #include <cstdint>
 #include <cstring>
 #include <cmath>
 #include <vector>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #ifdef ORC_DOUBLE
 typedef double real;
@@ -272,6 +280,25 @@ extern "C" {
 // Which working type this build uses: 4 (float) or 8 (double).
 int orc_real_bytes() { return static_cast<int>(sizeof(real)); }
 
+// Host threads the parallel loops use (1 without OpenMP).
+int orc_threads() {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+// Set the number of host threads (ignored without OpenMP); returns orc_threads().
+int orc_set_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+  return orc_threads();
+}
+
 int orc_float_to_bf16(const float* in, uint16_t* out, long n) {
   for (long i = 0; i < n; ++i) out[i] = float_to_bf16(in[i]);
   return 0;
@@ -352,9 +379,10 @@ int orc_forward(int T, int d, int I, int E, int k, float clamp,
                 int ntok, const int32_t* toks,
                 uint16_t* y, uint16_t* a_out, uint16_t* h_out, uint16_t* ys_out) {
   Problem p = make_problem(T, d, I, E, k, clamp, x, ids, scores, w13, w2);
-  std::vector<uint16_t> a(2 * I), h(I), ys((size_t)k * d, 0);
-  std::vector<char> ok(k);
+#pragma omp parallel for schedule(dynamic)
   for (int n = 0; n < ntok; ++n) {
+    std::vector<uint16_t> a(2 * I), h(I), ys((size_t)k * d, 0);
+    std::vector<char> ok(k);
     int t = toks ? toks[n] : n;
     for (int j = 0; j < k; ++j) {
       ok[j] = element_valid(p, t, j);
@@ -396,9 +424,10 @@ int orc_backward(int T, int d, int I, int E, int k, float clamp,
                  uint16_t* dx, float* dscores,
                  uint16_t* dA_out, uint16_t* hs_out, float* g_out, uint16_t* dxe_out) {
   Problem p = make_problem(T, d, I, E, k, clamp, x, ids, scores, w13, w2);
-  std::vector<uint16_t> a(2 * I), h(I), ys(d), dA(2 * I), hs(I), dxe((size_t)k * d, 0);
-  std::vector<char> ok(k);
+#pragma omp parallel for schedule(dynamic)
   for (int n = 0; n < ntok; ++n) {
+    std::vector<uint16_t> a(2 * I), h(I), ys(d), dA(2 * I), hs(I), dxe((size_t)k * d, 0);
+    std::vector<char> ok(k);
     int t = toks ? toks[n] : n;
     for (int j = 0; j < k; ++j) {
       ok[j] = element_valid(p, t, j);
@@ -455,32 +484,49 @@ int orc_wgrad_expert(int T, int d, int I, int E, int k, float clamp,
                      const uint16_t* w13, const uint16_t* w2, const uint16_t* dy,
                      int e, float* dw13_delta, float* dw2_delta) {
   Problem p = make_problem(T, d, I, E, k, clamp, x, ids, scores, w13, w2);
-  std::vector<real> acc13((size_t)2 * I * d, 0), acc2((size_t)d * I, 0);
-  std::vector<uint16_t> a(2 * I), h(I), ys(d), dA(2 * I), hs(I), dxe(d);
-  int rows = 0;
+  // the rows of expert e in dispatch order
+  std::vector<int> row_t, row_j;
   for (int t = 0; t < T; ++t)
-    for (int j = 0; j < k; ++j) {
-      if (ids[(size_t)t * k + j] != e || !element_valid(p, t, j)) continue;
-      float s = scores[(size_t)t * k + j];
-      row_forward(p, t, e, s, a.data(), h.data(), ys.data());
-      real ds;
-      row_backward(p, t, e, s, dy, a.data(), h.data(), &ds, dA.data(), dxe.data(), hs.data());
-      const uint16_t* xt = x + (size_t)t * d;
-      const uint16_t* dyt = dy + (size_t)t * d;
-      for (int i = 0; i < 2 * I; ++i) {
-        real ai = bf(dA[i]);
-        real* row = acc13.data() + (size_t)i * d;
-        for (int c = 0; c < d; ++c) row[c] += ai * bf(xt[c]);
+    for (int j = 0; j < k; ++j)
+      if (ids[(size_t)t * k + j] == e && element_valid(p, t, j)) {
+        row_t.push_back(t);
+        row_j.push_back(j);
       }
-      for (int c = 0; c < d; ++c) {
-        real yc = bf(dyt[c]);
-        real* row = acc2.data() + (size_t)c * I;
-        for (int i = 0; i < I; ++i) row[i] += yc * bf(hs[i]);
-      }
-      ++rows;
+  const int rows = static_cast<int>(row_t.size());
+  // each row's backward operands dA (R4) and hs (R7)
+  std::vector<uint16_t> dA_rows((size_t)rows * 2 * I), hs_rows((size_t)rows * I);
+#pragma omp parallel for schedule(dynamic)
+  for (int r = 0; r < rows; ++r) {
+    std::vector<uint16_t> a(2 * I), h(I), ys(d), dxe(d);
+    const int t = row_t[r];
+    const float s = scores[(size_t)t * k + row_j[r]];
+    row_forward(p, t, e, s, a.data(), h.data(), ys.data());
+    real ds;
+    row_backward(p, t, e, s, dy, a.data(), h.data(), &ds, dA_rows.data() + (size_t)r * 2 * I,
+                 dxe.data(), hs_rows.data() + (size_t)r * I);
+  }
+  // dW13 increment: each output row i sums over the rows in dispatch order
+#pragma omp parallel for schedule(static)
+  for (int i = 0; i < 2 * I; ++i) {
+    std::vector<real> acc(d, 0);
+    for (int r = 0; r < rows; ++r) {
+      const real ai = bf(dA_rows[(size_t)r * 2 * I + i]);
+      const uint16_t* xt = x + (size_t)row_t[r] * d;
+      for (int c = 0; c < d; ++c) acc[c] += ai * bf(xt[c]);
     }
-  for (size_t n = 0; n < acc13.size(); ++n) dw13_delta[n] = static_cast<float>(acc13[n]);
-  for (size_t n = 0; n < acc2.size(); ++n) dw2_delta[n] = static_cast<float>(acc2[n]);
+    for (int c = 0; c < d; ++c) dw13_delta[(size_t)i * d + c] = static_cast<float>(acc[c]);
+  }
+  // dW2 increment: each output row c sums over the rows in dispatch order
+#pragma omp parallel for schedule(static)
+  for (int c = 0; c < d; ++c) {
+    std::vector<real> acc(I, 0);
+    for (int r = 0; r < rows; ++r) {
+      const real yc = bf(dy[(size_t)row_t[r] * d + c]);
+      const uint16_t* hs = hs_rows.data() + (size_t)r * I;
+      for (int i = 0; i < I; ++i) acc[i] += yc * bf(hs[i]);
+    }
+    for (int i = 0; i < I; ++i) dw2_delta[(size_t)c * I + i] = static_cast<float>(acc[i]);
+  }
   return rows;
 }
 

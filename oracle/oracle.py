@@ -22,7 +22,9 @@ _cache = {}
 
 
 def build_oracle(force=False):
-    """Compile both oracle builds (working type float, and double)."""
+    """Compile both oracle builds (working type float, and double), with OpenMP
+    where the compiler has it (the parallel loops keep every summation order, so
+    the results do not depend on the thread count)."""
     os.makedirs(os.path.join(_HERE, "_build"), exist_ok=True)
     for kind, out in _LIBS.items():
         if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(_SRC):
@@ -31,7 +33,9 @@ def build_oracle(force=False):
                "-shared", "-fPIC", "-o", out + ".tmp", _SRC]
         if kind == "double":
             cmd.insert(1, "-DORC_DOUBLE")
-        subprocess.check_call(cmd)
+        r = subprocess.run(cmd[:1] + ["-fopenmp"] + cmd[1:], capture_output=True, text=True)
+        if r.returncode != 0:
+            subprocess.check_call(cmd)
         os.replace(out + ".tmp", out)
 
 
@@ -62,7 +66,18 @@ class Oracle:
         L.orc_e4m3_encode.argtypes = [vp, vp, i64]
         L.orc_e4m3_decode.argtypes = [vp, vp, i64]
         L.orc_forward_mxfp8.argtypes = [i32] * 5 + [f32] + [vp] * 7 + [i32, vp, vp, vp]
+        L.orc_threads.restype = i32
+        L.orc_set_threads.argtypes = [i32]
+        L.orc_set_threads.restype = i32
         self.real_bytes = L.orc_real_bytes()
+
+    def threads(self):
+        """Host threads of the parallel loops (1 without OpenMP)."""
+        return self.lib.orc_threads()
+
+    def set_threads(self, n):
+        """Use n host threads (results do not depend on n)."""
+        return self.lib.orc_set_threads(int(n))
 
     # -- scalar helpers -------------------------------------------------------
     def float_to_bf16(self, f):

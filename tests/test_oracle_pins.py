@@ -304,6 +304,34 @@ def test_zero_score_padding_gradients(orc):
 
 
 # ---------------------------------------------------------------------------
+# the parallel build: every sum keeps its order, so the thread count changes nothing
+
+
+def test_oracle_results_do_not_depend_on_thread_count(orc):
+    inp = small(T=40, d=128, I=64, E=5, k=3, seed=21, clamp=1.0)
+    args = (inp["x"], inp["ids"], inp["scores"], inp["w13"], inp["w2"])
+    n_all = orc.threads()
+    res = []
+    try:
+        for n in (1, max(n_all, 3)):
+            orc.set_threads(n)
+            y, fi = orc.forward(*args, clamp=1.0, intermediates=True)
+            dx, ds, bi = orc.backward(*args, inp["dy"], clamp=1.0, intermediates=True)
+            w = [orc.wgrad_expert(*args, inp["dy"], e, clamp=1.0) for e in range(5)]
+            res.append((y, fi, dx, ds, bi, w))
+    finally:
+        orc.set_threads(n_all)
+    (y1, f1, dx1, ds1, b1, w1), (yn, fn, dxn, dsn, bn, wn) = res
+    assert np.array_equal(y1, yn) and np.array_equal(dx1, dxn) and np.array_equal(ds1, dsn)
+    for key in f1:
+        assert np.array_equal(f1[key], fn[key]), key
+    for key in b1:
+        assert np.array_equal(b1[key], bn[key]), key
+    for (a13, a2, ra), (b13, b2, rb) in zip(w1, wn):
+        assert ra == rb and np.array_equal(a13, b13) and np.array_equal(a2, b2)
+
+
+# ---------------------------------------------------------------------------
 # FP32 working type against the FP64 build of the same definition
 
 
