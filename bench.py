@@ -456,7 +456,7 @@ def run_ours(args):
     if rank != 0:
         return
     cpu = None
-    if ws == 1 or rank == 0:
+    if args.cpu_seconds > 0 and (ws == 1 or rank == 0):
         # all host cores (the parallel oracle; same sums, same order), then one core
         flops, el, ne, cores = oracle_sample(inp, 1024, 0.7 * args.cpu_seconds)
         cpu = {"value": flops / el / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
