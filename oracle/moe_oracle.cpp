@@ -154,6 +154,33 @@ void row_forward(const Problem& p, int t, int e, float s,
   }
 }
 
+// SwiGLU backward of one routed row, given g = dY_t . W2[e] and the forward's a, h:
+//   dA [2I] bf16 (R4), hs [I] bf16 (R7)
+void swiglu_backward(const Problem& p, float s, const real* g, const uint16_t* a,
+                     const uint16_t* h, uint16_t* dA, uint16_t* hs) {
+  const int I = p.I;
+  const real L = p.clamp;
+  for (int i = 0; i < I; ++i) {
+    real ag = bf(a[i]), au = bf(a[I + i]);
+    real G = ag, U = au, mg = 1, mu = 1;
+    if (L > 0) {
+      if (G < -L || G > L) mg = 0;
+      if (U < -L || U > L) mu = 0;
+      G = G < -L ? -L : (G > L ? L : G);
+      U = U < -L ? -L : (U > L ? L : U);
+    }
+    real dh = static_cast<real>(s) * g[i];
+    real sig = real(1) / (real(1) + rexp(-G));
+    real silu = G * sig;
+    real dsilu = sig * (real(1) + G * (real(1) - sig));
+    real dgate = dh * U * dsilu * mg;
+    real dup = dh * silu * mu;
+    dA[i] = real_to_bf16(dgate);                                // R4
+    dA[I + i] = real_to_bf16(dup);                              // R4
+    hs[i] = real_to_bf16(static_cast<real>(s) * bf(h[i]));      // R7
+  }
+}
+
 // Backward quantities of one routed row, given its forward a and h.
 //   g       [I]  working type : dY_t . W2[e]
 //   dscore        working type : sum_i h_i * g_i
@@ -178,27 +205,7 @@ void row_backward(const Problem& p, int t, int e, float s, const uint16_t* dy,
   real ds = 0;
   for (int i = 0; i < I; ++i) ds += bf(h[i]) * g[i];
   *dscore = ds;
-  // SwiGLU backward
-  const real L = p.clamp;
-  for (int i = 0; i < I; ++i) {
-    real ag = bf(a[i]), au = bf(a[I + i]);
-    real G = ag, U = au, mg = 1, mu = 1;
-    if (L > 0) {
-      if (G < -L || G > L) mg = 0;
-      if (U < -L || U > L) mu = 0;
-      G = G < -L ? -L : (G > L ? L : G);
-      U = U < -L ? -L : (U > L ? L : U);
-    }
-    real dh = static_cast<real>(s) * g[i];
-    real sig = real(1) / (real(1) + rexp(-G));
-    real silu = G * sig;
-    real dsilu = sig * (real(1) + G * (real(1) - sig));
-    real dgate = dh * U * dsilu * mg;
-    real dup = dh * silu * mu;
-    dA[i] = real_to_bf16(dgate);                                // R4
-    dA[I + i] = real_to_bf16(dup);                              // R4
-    hs[i] = real_to_bf16(static_cast<real>(s) * bf(h[i]));      // R7
-  }
+  swiglu_backward(p, s, g.data(), a, h, dA, hs);
   // DGRAD through W13: dxe_c = sum_{i<2I} dA_i * W13[e,i,c]
   for (int c = 0; c < d; ++c) {
     real acc = 0;
@@ -229,13 +236,16 @@ double e4m3_value(uint8_t c) {
 // Nearest E4M3 value to v, ties to the even code, saturating to +-448.  The 127
 // non-negative finite codes 0x00..0x7E are monotone in value, so the nearest one
 // is found by bisection over that table.
-uint8_t e4m3_encode(double v) {
-  static double table[127];
-  static bool ready = false;
-  if (!ready) {
-    for (int c = 0; c < 127; ++c) table[c] = e4m3_value(static_cast<uint8_t>(c));
-    ready = true;
+struct E4m3Table {
+  double v[127];
+  E4m3Table() {
+    for (int c = 0; c < 127; ++c) v[c] = e4m3_value(static_cast<uint8_t>(c));
   }
+};
+
+uint8_t e4m3_encode(double v) {
+  static const E4m3Table tab;                 // built once (thread-safe static init)
+  const double* table = tab.v;
   uint8_t sgn = std::signbit(v) ? 0x80 : 0x00;
   double m = std::fabs(v);
   if (m >= table[126]) return sgn | 126;
@@ -272,6 +282,89 @@ void quant_block(const uint16_t* in, int n, uint8_t* codes, uint8_t* scale) {
 }
 
 double e8m0_value(uint8_t s) { return std::ldexp(1.0, static_cast<int>(s) - 127); }
+
+// Dequantised value of prepared element n of a [rows, K] code matrix with
+// scales [rows, K/32].
+real mx_value(const uint8_t* q, const uint8_t* sc, int K, size_t row, int col) {
+  return static_cast<real>(e4m3_value(q[row * K + col]) *
+                           e8m0_value(sc[row * (K / 32) + col / 32]));
+}
+
+// Quantise n bf16 values in 32-element blocks (the last block may be shorter)
+// and return their dequantised values.
+void mx_roundtrip(const uint16_t* in, int n, real* out) {
+  uint8_t q[32], sc;
+  for (int b = 0; b < n; b += 32) {
+    const int m = n - b < 32 ? n - b : 32;
+    quant_block(in + b, m, q, &sc);
+    for (int i = 0; i < m; ++i)
+      out[b + i] = static_cast<real>(e4m3_value(q[i]) * e8m0_value(sc));
+  }
+}
+
+// MXFP8 forward quantities of one routed row ([DM]: activations quantised after
+// routing, prepared weights): x row quantised along d, W13 prepared along d,
+// a (R1), h (R2), h quantised along I, W2 prepared along I, ys (R3).
+void row_forward_mx(const Problem& p, int t, int e, float s, const uint8_t* w13q,
+                    const uint8_t* w13s, const uint8_t* w2q, const uint8_t* w2s, uint16_t* a,
+                    uint16_t* h, uint16_t* ys) {
+  const int d = p.d, I = p.I;
+  std::vector<real> xv(d), hv(I);
+  mx_roundtrip(p.x + (size_t)t * d, d, xv.data());
+  for (int i = 0; i < 2 * I; ++i) {
+    const size_t row = (size_t)e * 2 * I + i;
+    real acc = 0;
+    for (int c = 0; c < d; ++c) acc += xv[c] * mx_value(w13q, w13s, d, row, c);
+    a[i] = real_to_bf16(acc);                                  // R1
+  }
+  const real L = p.clamp;
+  for (int i = 0; i < I; ++i) {
+    real G = bf(a[i]), U = bf(a[I + i]);
+    if (L > 0) {
+      G = G < -L ? -L : (G > L ? L : G);
+      U = U < -L ? -L : (U > L ? L : U);
+    }
+    h[i] = real_to_bf16(G / (real(1) + rexp(-G)) * U);         // R2
+  }
+  mx_roundtrip(h, I, hv.data());
+  for (int c = 0; c < d; ++c) {
+    const size_t row = (size_t)e * d + c;
+    real acc = 0;
+    for (int i = 0; i < I; ++i) acc += hv[i] * mx_value(w2q, w2s, I, row, i);
+    ys[c] = real_to_bf16(static_cast<real>(s) * acc);          // R3
+  }
+}
+
+// MXFP8 backward quantities of one routed row: each GEMM takes its operands
+// block-quantised along its own K.
+//   g   = Q_d(dY_t) . W2[e]       W2 prepared along d:  w2tq [E, I, d], w2ts [E, I, d/32]
+//   dscore, dA (R4), hs (R7)      as in the bf16 backward, from the forward's a, h
+//   dxe = Q_2I(dA) . W13[e]       W13 prepared along 2I: w13tq [E, d, 2I], w13ts [E, d, 2I/32]
+void row_backward_mx(const Problem& p, int t, int e, float s, const uint16_t* dy,
+                     const uint16_t* a, const uint16_t* h, const uint8_t* w13tq,
+                     const uint8_t* w13ts, const uint8_t* w2tq, const uint8_t* w2ts,
+                     real* dscore, uint16_t* dA, uint16_t* dxe, uint16_t* hs) {
+  const int d = p.d, I = p.I;
+  std::vector<real> dyv(d), g(I), dav(2 * I);
+  mx_roundtrip(dy + (size_t)t * d, d, dyv.data());
+  for (int i = 0; i < I; ++i) {
+    const size_t row = (size_t)e * I + i;
+    real acc = 0;
+    for (int c = 0; c < d; ++c) acc += dyv[c] * mx_value(w2tq, w2ts, d, row, c);
+    g[i] = acc;
+  }
+  real ds = 0;
+  for (int i = 0; i < I; ++i) ds += bf(h[i]) * g[i];
+  *dscore = ds;
+  swiglu_backward(p, s, g.data(), a, h, dA, hs);
+  mx_roundtrip(dA, 2 * I, dav.data());
+  for (int c = 0; c < d; ++c) {
+    const size_t row = (size_t)e * d + c;
+    real acc = 0;
+    for (int i = 0; i < 2 * I; ++i) acc += dav[i] * mx_value(w13tq, w13ts, 2 * I, row, i);
+    dxe[c] = real_to_bf16(acc);                                // R5
+  }
+}
 
 }  // namespace
 
@@ -562,17 +655,11 @@ int orc_forward_mxfp8(int T, int d, int I, int E, int k, float clamp,
                       const uint8_t* w2q, const uint8_t* w2s,
                       int ntok, const int32_t* toks, uint16_t* y, uint16_t* h_out) {
   Problem p = make_problem(T, d, I, E, k, clamp, x, ids, scores, nullptr, nullptr);
-  std::vector<uint8_t> xq(d), xs(d / 32), hq(I), hsc(I / 32);
-  std::vector<real> xv(d), hv(I);
-  std::vector<uint16_t> a(2 * I), h(I), ys((size_t)k * d);
-  std::vector<char> ok(k);
-  const real L = clamp;
+#pragma omp parallel for schedule(dynamic)
   for (int n = 0; n < ntok; ++n) {
+    std::vector<uint16_t> a(2 * I), h(I), ys((size_t)k * d);
+    std::vector<char> ok(k);
     int t = toks ? toks[n] : n;
-    for (int b = 0; b < d / 32; ++b)
-      quant_block(x + (size_t)t * d + b * 32, 32, xq.data() + b * 32, xs.data() + b);
-    for (int c = 0; c < d; ++c)
-      xv[c] = static_cast<real>(e4m3_value(xq[c]) * e8m0_value(xs[c / 32]));
     for (int j = 0; j < k; ++j) {
       ok[j] = element_valid(p, t, j);
       if (!ok[j]) {
@@ -581,35 +668,9 @@ int orc_forward_mxfp8(int T, int d, int I, int E, int k, float clamp,
       }
       int e = ids[(size_t)t * k + j];
       float s = scores[(size_t)t * k + j];
-      for (int i = 0; i < 2 * I; ++i) {
-        size_t row = (size_t)e * 2 * I + i;
-        real acc = 0;
-        for (int c = 0; c < d; ++c)
-          acc += xv[c] * static_cast<real>(e4m3_value(w13q[row * d + c]) *
-                                           e8m0_value(w13s[row * (d / 32) + c / 32]));
-        a[i] = real_to_bf16(acc);                                // R1
-      }
-      for (int i = 0; i < I; ++i) {
-        real G = bf(a[i]), U = bf(a[I + i]);
-        if (L > 0) {
-          G = G < -L ? -L : (G > L ? L : G);
-          U = U < -L ? -L : (U > L ? L : U);
-        }
-        h[i] = real_to_bf16(G / (real(1) + rexp(-G)) * U);       // R2
-      }
+      row_forward_mx(p, t, e, s, w13q, w13s, w2q, w2s, a.data(), h.data(),
+                     ys.data() + (size_t)j * d);
       if (h_out) std::memcpy(h_out + ((size_t)n * k + j) * I, h.data(), sizeof(uint16_t) * I);
-      for (int b = 0; b < I / 32; ++b)
-        quant_block(h.data() + b * 32, 32, hq.data() + b * 32, hsc.data() + b);
-      for (int i = 0; i < I; ++i)
-        hv[i] = static_cast<real>(e4m3_value(hq[i]) * e8m0_value(hsc[i / 32]));
-      for (int c = 0; c < d; ++c) {
-        size_t row = (size_t)e * d + c;
-        real acc = 0;
-        for (int i = 0; i < I; ++i)
-          acc += hv[i] * static_cast<real>(e4m3_value(w2q[row * I + i]) *
-                                           e8m0_value(w2s[row * (I / 32) + i / 32]));
-        ys[(size_t)j * d + c] = real_to_bf16(static_cast<real>(s) * acc);   // R3
-      }
     }
     for (int c = 0; c < d; ++c) {
       real acc = 0;
@@ -619,6 +680,133 @@ int orc_forward_mxfp8(int T, int d, int I, int E, int k, float clamp,
     }
   }
   return 0;
+}
+
+// MXFP8 backward for the listed tokens (training step of an MXFP8 plan; [DM]
+// "What it is selling": MXFP8 E4M3 for FPROP/DGRAD/WGRAD with prepared weights).
+// The forward quantities are those of orc_forward_mxfp8 (same prepared forward
+// weights); the DGRAD GEMMs take dY quantised along d and dA along 2I, with
+// weights prepared along the same K:
+//   w2tq  [E, I, d]  codes of W2[e]^T,  w2ts  [E, I, d/32]
+//   w13tq [E, d, 2I] codes of W13[e]^T, w13ts [E, d, 2I/32]
+// Outputs as orc_backward: dx [ntok, d] (R6 of R5), dscores [ntok, k], optional
+// dA [ntok, k, 2I] (R4), hs [ntok, k, I] (R7), dxe [ntok, k, d] (R5).
+int orc_backward_mxfp8(int T, int d, int I, int E, int k, float clamp,
+                       const uint16_t* x, const int32_t* ids, const float* scores,
+                       const uint8_t* w13q, const uint8_t* w13s, const uint8_t* w2q,
+                       const uint8_t* w2s, const uint8_t* w13tq, const uint8_t* w13ts,
+                       const uint8_t* w2tq, const uint8_t* w2ts, const uint16_t* dy,
+                       int ntok, const int32_t* toks, uint16_t* dx, float* dscores,
+                       uint16_t* dA_out, uint16_t* hs_out, uint16_t* dxe_out) {
+  Problem p = make_problem(T, d, I, E, k, clamp, x, ids, scores, nullptr, nullptr);
+#pragma omp parallel for schedule(dynamic)
+  for (int n = 0; n < ntok; ++n) {
+    std::vector<uint16_t> a(2 * I), h(I), ys(d), dA(2 * I), hs(I), dxe((size_t)k * d, 0);
+    std::vector<char> ok(k);
+    int t = toks ? toks[n] : n;
+    for (int j = 0; j < k; ++j) {
+      ok[j] = element_valid(p, t, j);
+      const size_t nj = (size_t)n * k + j;
+      if (!ok[j]) {
+        dscores[nj] = 0;
+        if (dA_out) std::memset(dA_out + nj * 2 * I, 0, sizeof(uint16_t) * 2 * I);
+        if (hs_out) std::memset(hs_out + nj * I, 0, sizeof(uint16_t) * I);
+        continue;
+      }
+      int e = ids[(size_t)t * k + j];
+      float s = scores[(size_t)t * k + j];
+      row_forward_mx(p, t, e, s, w13q, w13s, w2q, w2s, a.data(), h.data(), ys.data());
+      real ds;
+      row_backward_mx(p, t, e, s, dy, a.data(), h.data(), w13tq, w13ts, w2tq, w2ts, &ds,
+                      dA.data(), dxe.data() + (size_t)j * d, hs.data());
+      dscores[nj] = static_cast<float>(ds);
+      if (dA_out) std::memcpy(dA_out + nj * 2 * I, dA.data(), sizeof(uint16_t) * 2 * I);
+      if (hs_out) std::memcpy(hs_out + nj * I, hs.data(), sizeof(uint16_t) * I);
+    }
+    for (int c = 0; c < d; ++c) {
+      real acc = 0;
+      for (int j = 0; j < k; ++j)
+        if (ok[j]) acc += bf(dxe[(size_t)j * d + c]);
+      dx[(size_t)n * d + c] = real_to_bf16(acc);                // R6
+    }
+    if (dxe_out)
+      for (int j = 0; j < k; ++j)
+        for (int c = 0; c < d; ++c)
+          dxe_out[((size_t)n * k + j) * d + c] = ok[j] ? dxe[(size_t)j * d + c] : 0;
+  }
+  return 0;
+}
+
+// MXFP8 WGRAD of one expert e: the WGRAD GEMMs run over the rows of e (dispatch
+// order), so their operands are block-quantised along that row dimension: blocks
+// of 32 consecutive rows of e, starting at its first row (a shorter last block;
+// the zero rows that pad the expert's segment do not change a block's scale).
+//   dw2_delta  [d, I]  = sum_rows Q_rows(dY)[r, c] * Q_rows(hs)[r, i]
+//   dw13_delta [2I, d] = sum_rows Q_rows(dA)[r, i] * Q_rows(x)[r, c]
+// dA and hs come from the MXFP8 backward of each row.  Returns the row count.
+int orc_wgrad_expert_mxfp8(int T, int d, int I, int E, int k, float clamp,
+                           const uint16_t* x, const int32_t* ids, const float* scores,
+                           const uint8_t* w13q, const uint8_t* w13s, const uint8_t* w2q,
+                           const uint8_t* w2s, const uint8_t* w13tq, const uint8_t* w13ts,
+                           const uint8_t* w2tq, const uint8_t* w2ts, const uint16_t* dy, int e,
+                           float* dw13_delta, float* dw2_delta) {
+  Problem p = make_problem(T, d, I, E, k, clamp, x, ids, scores, nullptr, nullptr);
+  std::vector<int> row_t, row_j;
+  for (int t = 0; t < T; ++t)
+    for (int j = 0; j < k; ++j)
+      if (ids[(size_t)t * k + j] == e && element_valid(p, t, j)) {
+        row_t.push_back(t);
+        row_j.push_back(j);
+      }
+  const int rows = static_cast<int>(row_t.size());
+  std::vector<uint16_t> dA_rows((size_t)rows * 2 * I), hs_rows((size_t)rows * I);
+#pragma omp parallel for schedule(dynamic)
+  for (int r = 0; r < rows; ++r) {
+    std::vector<uint16_t> a(2 * I), h(I), ys(d), dxe(d);
+    const int t = row_t[r];
+    const float s = scores[(size_t)t * k + row_j[r]];
+    row_forward_mx(p, t, e, s, w13q, w13s, w2q, w2s, a.data(), h.data(), ys.data());
+    real ds;
+    row_backward_mx(p, t, e, s, dy, a.data(), h.data(), w13tq, w13ts, w2tq, w2ts, &ds,
+                    dA_rows.data() + (size_t)r * 2 * I, dxe.data(),
+                    hs_rows.data() + (size_t)r * I);
+  }
+  // dequantised operands, each column quantised along the rows
+  auto along_rows = [&](int cols, auto value_of, std::vector<real>& out) {
+    out.assign((size_t)rows * cols, 0);
+#pragma omp parallel for schedule(static)
+    for (int c = 0; c < cols; ++c) {
+      std::vector<uint16_t> col(rows);
+      std::vector<real> deq(rows);
+      for (int r = 0; r < rows; ++r) col[r] = value_of(r, c);
+      mx_roundtrip(col.data(), rows, deq.data());
+      for (int r = 0; r < rows; ++r) out[(size_t)r * cols + c] = deq[r];
+    }
+  };
+  std::vector<real> qdy, qhs, qdA, qx;
+  along_rows(d, [&](int r, int c) { return dy[(size_t)row_t[r] * d + c]; }, qdy);
+  along_rows(I, [&](int r, int c) { return hs_rows[(size_t)r * I + c]; }, qhs);
+  along_rows(2 * I, [&](int r, int c) { return dA_rows[(size_t)r * 2 * I + c]; }, qdA);
+  along_rows(d, [&](int r, int c) { return x[(size_t)row_t[r] * d + c]; }, qx);
+#pragma omp parallel for schedule(static)
+  for (int i = 0; i < 2 * I; ++i) {
+    std::vector<real> acc(d, 0);
+    for (int r = 0; r < rows; ++r) {
+      const real ai = qdA[(size_t)r * 2 * I + i];
+      for (int c = 0; c < d; ++c) acc[c] += ai * qx[(size_t)r * d + c];
+    }
+    for (int c = 0; c < d; ++c) dw13_delta[(size_t)i * d + c] = static_cast<float>(acc[c]);
+  }
+#pragma omp parallel for schedule(static)
+  for (int c = 0; c < d; ++c) {
+    std::vector<real> acc(I, 0);
+    for (int r = 0; r < rows; ++r) {
+      const real yc = qdy[(size_t)r * d + c];
+      for (int i = 0; i < I; ++i) acc[i] += yc * qhs[(size_t)r * I + i];
+    }
+    for (int i = 0; i < I; ++i) dw2_delta[(size_t)c * I + i] = static_cast<float>(acc[i]);
+  }
+  return rows;
 }
 
 }  // extern "C"

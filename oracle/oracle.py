@@ -66,6 +66,8 @@ class Oracle:
         L.orc_e4m3_encode.argtypes = [vp, vp, i64]
         L.orc_e4m3_decode.argtypes = [vp, vp, i64]
         L.orc_forward_mxfp8.argtypes = [i32] * 5 + [f32] + [vp] * 7 + [i32, vp, vp, vp]
+        L.orc_backward_mxfp8.argtypes = [i32] * 5 + [f32] + [vp] * 12 + [i32] + [vp] * 6
+        L.orc_wgrad_expert_mxfp8.argtypes = [i32] * 5 + [f32] + [vp] * 12 + [i32, vp, vp]
         L.orc_threads.restype = i32
         L.orc_set_threads.argtypes = [i32]
         L.orc_set_threads.restype = i32
@@ -206,6 +208,55 @@ class Oracle:
                                    _ptr(w13q), _ptr(w13s), _ptr(w2q), _ptr(w2s), n, _ptr(toks_a),
                                    _ptr(y), _ptr(h))
         return (y, h) if return_h else y
+
+    def prepare_mxfp8_backward_weights(self, w13, w2):
+        """Weights prepared for the MXFP8 backward GEMMs (quantised along their K):
+        W2[e]^T [E, I, d] along d and W13[e]^T [E, d, 2I] along 2I."""
+        w2t = np.ascontiguousarray(np.swapaxes(w2, 1, 2))
+        w13t = np.ascontiguousarray(np.swapaxes(w13, 1, 2))
+        w2tq, w2ts = self.quant_mxfp8(w2t)
+        w13tq, w13ts = self.quant_mxfp8(w13t)
+        return w13tq, w13ts, w2tq, w2ts
+
+    def backward_mxfp8(self, x, ids, scores, fw, bw, dy, clamp=0.0, toks=None,
+                       intermediates=False):
+        """fw = (w13q, w13s, w2q, w2s) prepared along K of the forward GEMMs;
+        bw = (w13tq, w13ts, w2tq, w2ts) from prepare_mxfp8_backward_weights."""
+        T, d = x.shape
+        k = ids.shape[1]
+        E, I2, _ = fw[0].shape
+        I = I2 // 2
+        toks_a = None if toks is None else np.ascontiguousarray(toks, np.int32)
+        n = T if toks is None else toks_a.size
+        dx = np.empty((n, d), np.uint16)
+        ds = np.empty((n, k), np.float32)
+        dA = hs = dxe = None
+        if intermediates:
+            dA = np.empty((n, k, 2 * I), np.uint16)
+            hs = np.empty((n, k, I), np.uint16)
+            dxe = np.empty((n, k, d), np.uint16)
+        self.lib.orc_backward_mxfp8(T, d, I, E, k, float(clamp), _ptr(x), _ptr(ids), _ptr(scores),
+                                    *[_ptr(np.ascontiguousarray(w)) for w in fw],
+                                    *[_ptr(np.ascontiguousarray(w)) for w in bw], _ptr(dy),
+                                    n, _ptr(toks_a), _ptr(dx), _ptr(ds), _ptr(dA), _ptr(hs),
+                                    _ptr(dxe))
+        if intermediates:
+            return dx, ds, dict(dA=dA, hs=hs, dxe=dxe)
+        return dx, ds
+
+    def wgrad_expert_mxfp8(self, x, ids, scores, fw, bw, dy, e, clamp=0.0):
+        T, d = x.shape
+        k = ids.shape[1]
+        E, I2, _ = fw[0].shape
+        I = I2 // 2
+        d13 = np.empty((2 * I, d), np.float32)
+        d2 = np.empty((d, I), np.float32)
+        rows = self.lib.orc_wgrad_expert_mxfp8(T, d, I, E, k, float(clamp), _ptr(x), _ptr(ids),
+                                               _ptr(scores),
+                                               *[_ptr(np.ascontiguousarray(w)) for w in fw],
+                                               *[_ptr(np.ascontiguousarray(w)) for w in bw],
+                                               _ptr(dy), int(e), _ptr(d13), _ptr(d2))
+        return d13, d2, rows
 
 
 def load_oracle(kind="float"):

@@ -318,6 +318,12 @@ def test_oracle_results_do_not_depend_on_thread_count(orc):
             y, fi = orc.forward(*args, clamp=1.0, intermediates=True)
             dx, ds, bi = orc.backward(*args, inp["dy"], clamp=1.0, intermediates=True)
             w = [orc.wgrad_expert(*args, inp["dy"], e, clamp=1.0) for e in range(5)]
+            fw = orc.quant_mxfp8(inp["w13"]) + orc.quant_mxfp8(inp["w2"])
+            bw = orc.prepare_mxfp8_backward_weights(inp["w13"], inp["w2"])
+            mx = args[:3]
+            _, _, mi = orc.backward_mxfp8(*mx, fw, bw, inp["dy"], clamp=1.0, intermediates=True)
+            bi.update({"mx_" + key: v for key, v in mi.items()})
+            w += [orc.wgrad_expert_mxfp8(*mx, fw, bw, inp["dy"], e, clamp=1.0) for e in range(5)]
             res.append((y, fi, dx, ds, bi, w))
     finally:
         orc.set_threads(n_all)
@@ -401,6 +407,91 @@ def test_mxfp8_block_scale_closed_form(orc):
     dec = orc.e4m3_decode(codes).reshape(64, 8, 32)
     big = np.abs(dec).max(-1)[amax > 0]
     assert big.min() >= 256 and big.max() <= 448
+
+
+def _deq_mx(b):
+    """FP64 values of bf16 bits after MX quantisation along the last axis (32-element
+    blocks; torch's float8_e4m3fn conversion and numpy's frexp for the scale)."""
+    v = f32(b).astype(np.float64)
+    K = v.shape[-1]
+    blk = v.reshape(v.shape[:-1] + (K // 32, 32))
+    amax = np.abs(blk).max(-1, keepdims=True)
+    _, ex = np.frexp(amax)
+    X = ex - 1 - 8
+    q = torch.from_numpy(np.clip(blk * 2.0 ** -X, -448, 448).astype(np.float32)) \
+        .to(torch.float8_e4m3fn).double().numpy()
+    return (q * 2.0 ** X).reshape(v.shape)
+
+
+def _deq_mx_rows(b):
+    """Same, along axis 0 in blocks of 32 rows (zero rows pad the last block)."""
+    n = b.shape[0]
+    pad = (-n) % 32
+    bb = np.concatenate([b, np.zeros((pad,) + b.shape[1:], b.dtype)]) if pad else b
+    return _deq_mx(np.ascontiguousarray(bb.T)).T[:n]
+
+
+def test_mxfp8_backward_matches_fp64_dequantised(orc):
+    """MXFP8 DGRAD = FP64 matmuls of operands quantised along each GEMM's K
+    (dY and W2^T along d; dA and W13^T along 2I), with the bf16 points."""
+    inp = small(T=24, d=128, I=64, E=4, k=2, seed=17)
+    fw = orc.quant_mxfp8(inp["w13"]) + orc.quant_mxfp8(inp["w2"])
+    bw = orc.prepare_mxfp8_backward_weights(inp["w13"], inp["w2"])
+    dx, ds, bi = orc.backward_mxfp8(inp["x"], inp["ids"], inp["scores"], fw, bw, inp["dy"],
+                                    intermediates=True)
+    xd, w13d = _deq_mx(inp["x"]), _deq_mx(inp["w13"])
+    w2d = _deq_mx(inp["w2"])
+    w2td = _deq_mx(np.ascontiguousarray(np.swapaxes(inp["w2"], 1, 2)))     # [E, I, d]
+    w13td = _deq_mx(np.ascontiguousarray(np.swapaxes(inp["w13"], 1, 2)))   # [E, d, 2I]
+    dyd = _deq_mx(inp["dy"])
+    T, k = inp["ids"].shape
+    I = 64
+    ds_ref = np.zeros((T, k))
+    dx_ref = np.zeros((T, 128))
+    dA_all = []
+    for t in range(T):
+        for j in range(k):
+            e, s = inp["ids"][t, j], float(inp["scores"][t, j])
+            a = f32(bits(w13d[e] @ xd[t])).astype(np.float64)
+            G, U = a[:I], a[I:]
+            sig = 1 / (1 + np.exp(-G))
+            h = f32(bits(G * sig * U)).astype(np.float64)
+            g = w2td[e] @ dyd[t]
+            ds_ref[t, j] = h @ g
+            dsilu = sig * (1 + G * (1 - sig))
+            dA = bits(np.concatenate([s * g * U * dsilu, s * g * G * sig]))
+            dA_all.append(np.mean(dA == bi["dA"][t, j]))
+            dxe = bits(w13td[e] @ _deq_mx(dA[None])[0])
+            dx_ref[t] += f32(dxe)
+    assert np.mean(dA_all) > 0.99
+    assert _rel_fro(ds, ds_ref) < 2e-3
+    assert _rel_fro(f32(dx), dx_ref) < 5e-3
+    # the forward the backward sees is the MXFP8 forward (h via W2 quantised along I)
+    assert w2d.shape == inp["w2"].shape
+
+
+def test_mxfp8_wgrad_matches_fp64_dequantised(orc):
+    """MXFP8 WGRAD of each expert = FP64 sums over its rows (dispatch order) of
+    operands quantised along the rows in blocks of 32."""
+    inp = small(T=90, d=128, I=64, E=3, k=2, seed=19)
+    fw = orc.quant_mxfp8(inp["w13"]) + orc.quant_mxfp8(inp["w2"])
+    bw = orc.prepare_mxfp8_backward_weights(inp["w13"], inp["w2"])
+    _, _, bi = orc.backward_mxfp8(inp["x"], inp["ids"], inp["scores"], fw, bw, inp["dy"],
+                                  intermediates=True)
+    for e in range(3):
+        d13, d2, rows = orc.wgrad_expert_mxfp8(inp["x"], inp["ids"], inp["scores"], fw, bw,
+                                               inp["dy"], e)
+        sel = [(t, j) for t in range(90) for j in range(2) if inp["ids"][t, j] == e]
+        assert rows == len(sel) and rows > 32          # more than one row block
+        dA = np.stack([bi["dA"][t, j] for t, j in sel])
+        hs = np.stack([bi["hs"][t, j] for t, j in sel])
+        dy = np.stack([inp["dy"][t] for t, _ in sel])
+        x = np.stack([inp["x"][t] for t, _ in sel])
+        r13 = _deq_mx_rows(dA).T @ _deq_mx_rows(x)
+        r2 = _deq_mx_rows(dy).T @ _deq_mx_rows(hs)
+        assert _rel_fro(d13, r13) < 1e-5 and _rel_fro(d2, r2) < 1e-5
+        # quantising along the other axis gives measurably different sums
+        assert _rel_fro(d13, (_deq_mx(dA).T @ _deq_mx(x))) > 1e-4
 
 
 def test_mxfp8_forward_matches_fp64_dequantised(orc):
