@@ -119,8 +119,9 @@ int moe_plan_set_workspace(moe_plan* plan, void* workspace, size_t bytes, int fl
  *   w13_sf / w2_sf their E8M0 scales in the tiled layout, both produced by
  *   moe_prepare_weights_mxfp8; for bf16 pass NULL.  An MXFP8 plan quantises
  *   the routed activation rows along d and h along I (32-element blocks) and
- *   runs block-scaled E4M3 GEMMs; it is forward only (save_for_backward = 0),
- *   and needs I % 128 == 0, d <= 4096, I <= 4096.
+ *   runs block-scaled E4M3 GEMMs; it needs I % 128 == 0, d <= 4096, I <= 4096.
+ *   With save_for_backward = 1 it also keeps a, h and the routed x rows
+ *   quantised along the rows for moe_backward_mxfp8.
  * Output: y [T, d] bf16, overwritten:
  *   y[t] = bf16( sum_{j=0..k-1} bf16( scores[t,j] * W2[e] . h ) ),
  *   h = bf16(silu(G) * U),  (G, U) = bf16(W13[e] . x[t]),  e = ids[t,j]
@@ -143,10 +144,30 @@ int moe_forward(moe_plan* plan, const void* x, const int32_t* ids, const float* 
  *   dw13    [E, 2I, d]  fp32, ACCUMULATED in place (+=); experts with no rows
  *   dw2     [E, d, I]   fp32, ACCUMULATED in place      are left untouched
  * Returns MOE_ERR_STATE if no saving forward preceded it, MOE_ERR_UNSUPPORTED
- * for an MXFP8 plan.
+ * for an MXFP8 plan (use moe_backward_mxfp8).
  */
 int moe_backward(moe_plan* plan, const void* dy, const void* w13, const void* w2,
                  void* dx, float* dw13, float* dw2, float* dscores, void* stream);
+
+/*
+ * Backward of an MXFP8 plan ("What it is selling": MXFP8 E4M3 for FPROP, DGRAD
+ * and WGRAD; nvfp4moe "Training").  Every block-scaled GEMM takes its operands
+ * quantised in 32-element blocks along its own K (block rule of
+ * moe_quantize_mxfp8):
+ *   DGRAD-W2:  dY rows along d, W2[e]^T prepared along d         -> g
+ *   DGRAD-W13: dA rows along 2I, W13[e]^T prepared along 2I       -> dX_e
+ *   WGRAD-W2:  dY and hs along the rows of each expert            -> dW2[e]
+ *   WGRAD-W13: dA and x along the rows of each expert             -> dW13[e]
+ * (row blocks start at each expert's first padded row; the zero padding rows do
+ * not change a block's scale).  Rounding points and outputs are those of
+ * moe_backward: dx, dscores overwritten, dw13/dw2 accumulated in place.
+ * w13t/w13t_sf and w2t/w2t_sf come from moe_prepare_weights_mxfp8_backward.
+ * Needs a MOE_WS_TRAINING workspace and a saving forward (MOE_ERR_STATE
+ * otherwise); MOE_ERR_UNSUPPORTED for a bf16 plan.
+ */
+int moe_backward_mxfp8(moe_plan* plan, const void* dy, const uint8_t* w13t,
+                       const uint8_t* w13t_sf, const uint8_t* w2t, const uint8_t* w2t_sf,
+                       void* dx, float* dw13, float* dw2, float* dscores, void* stream);
 
 /*
  * One training (or, with dy_host == NULL, inference) step from HOST buffers:
@@ -192,10 +213,25 @@ int moe_quantize_mxfp8(const void* in, long rows, int K, uint8_t* codes, uint8_t
  * [I+64t, I+64t+64)); for W2 they are consecutive 128-row blocks of [E*d].
  * d % 128 == 0, I % 128 == 0.
  */
-size_t moe_mxfp8_weight_scale_bytes(int d, int I, int E, int which /* 0: W13, 1: W2 */);
+size_t moe_mxfp8_weight_scale_bytes(int d, int I, int E,
+                                    int which /* 0: W13, 1: W2, 2: W13^T, 3: W2^T */);
 int moe_prepare_weights_mxfp8(const void* w13, const void* w2, int d, int I, int E,
                               uint8_t* w13_codes, uint8_t* w13_scales, uint8_t* w2_codes,
                               uint8_t* w2_scales, void* stream);
+
+/*
+ * Weights prepared for the MXFP8 backward (moe_backward_mxfp8): each expert's
+ * matrix transposed so that the DGRAD GEMMs read it K-major, and quantised
+ * along that K:
+ *   w13t_codes [E, d, 2I]  W13[e]^T quantised along 2I
+ *   w2t_codes  [E, I, d]   W2[e]^T  quantised along d
+ * Scales in the tiled layout above with plain 128-row blocks of the transposed
+ * matrices ([E*d] and [E*I] rows); sizes from moe_mxfp8_weight_scale_bytes
+ * (which = 2, 3).  d % 128 == 0, I % 128 == 0.
+ */
+int moe_prepare_weights_mxfp8_backward(const void* w13, const void* w2, int d, int I, int E,
+                                       uint8_t* w13t_codes, uint8_t* w13t_scales,
+                                       uint8_t* w2t_codes, uint8_t* w2t_scales, void* stream);
 
 /*
  * Synchronise the device, read and clear the plan's device error word.
@@ -243,6 +279,8 @@ const char* moe_status_string(int status);
 #define MOE_BUF_XSF      14   /* u8   tiled E8M0 scales of XQ                   */
 #define MOE_BUF_HQ       15   /* u8   [Rpad,I] E4M3 h (MXFP8 plans)             */
 #define MOE_BUF_HSF      16   /* u8   tiled E8M0 scales of HQ                   */
+#define MOE_BUF_XQT      17   /* MXFP8 training: E4M3 [d, Rpad], routed x quantised along the rows */
+#define MOE_BUF_XQTSF    18   /* its tiled scales (row blocks over d, K groups over Rpad)      */
 int moe_plan_buffer(const moe_plan* plan, int which, void** dev_ptr, size_t* bytes);
 
 /*

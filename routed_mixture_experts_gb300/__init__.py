@@ -28,5 +28,6 @@ from .binding import (  # noqa: F401
     gemm_bf16,
     lib,
     prepare_weights_mxfp8,
+    prepare_weights_mxfp8_backward,
     quantize_mxfp8,
 )

@@ -20,7 +20,7 @@ MOE_PREC_MXFP8 = 1
 MOE_WS_TRAINING = 1
 MOE_WS_HOST_STAGING = 2
 MOE_BUF = dict(m_indptr=0, off_pad=1, row_of=2, token_of=3, score_of=4, xe=5, a=6, h=7, ys=8,
-               dye=9, dA=10, hs=11, dxe=12, xq=13, xsf=14, hq=15, hsf=16)
+               dye=9, dA=10, hs=11, dxe=12, xq=13, xsf=14, hq=15, hsf=16, xqT=17, xqTsf=18)
 
 _lock = threading.Lock()
 _lib = None
@@ -63,12 +63,15 @@ def _declare(L):
     L.moe_mxfp8_weight_scale_bytes.argtypes = [i32, i32, i32, i32]
     L.moe_mxfp8_weight_scale_bytes.restype = sz
     L.moe_prepare_weights_mxfp8.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp, vp]
+    L.moe_prepare_weights_mxfp8_backward.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp, vp]
+    L.moe_backward_mxfp8.argtypes = [vp] * 11
     L.moe_plan_launch_count.argtypes = [vp]
     L.moe_plan_launch_count.restype = ctypes.c_longlong
     for name in ("moe_plan_set_swiglu_clamp", "moe_plan_set_workspace", "moe_forward",
                  "moe_backward", "moe_step_host", "moe_quantize_mxfp8", "moe_plan_check",
                  "moe_plan_buffer", "moe_gemm_bf16", "moe_plan_set_timing_events",
-                 "moe_prepare_weights_mxfp8", "moe_plan_set_debug", "moe_plan_set_cta_pairs"):
+                 "moe_prepare_weights_mxfp8", "moe_plan_set_debug", "moe_plan_set_cta_pairs",
+                 "moe_prepare_weights_mxfp8_backward", "moe_backward_mxfp8"):
         getattr(L, name).restype = i32
     return L
 
@@ -147,6 +150,20 @@ class MoePlan:
             dscores = torch.empty(self.T, self.k, dtype=torch.float32, device=dy.device)
         _check(lib().moe_backward(self.ptr, _p(dy), _p(w13), _p(w2), _p(dx), _p(dw13), _p(dw2),
                                   _p(dscores), _stream(stream)), "backward")
+        return dx, dscores
+
+    def backward_mxfp8(self, dy, w13t, w13t_sf, w2t, w2t_sf, dw13, dw2, dx=None, dscores=None,
+                       stream=None):
+        """Backward of an MXFP8 plan; w13t.. from prepare_weights_mxfp8_backward."""
+        import torch
+
+        if dx is None:
+            dx = torch.empty(self.T, self.d, dtype=torch.bfloat16, device=dy.device)
+        if dscores is None:
+            dscores = torch.empty(self.T, self.k, dtype=torch.float32, device=dy.device)
+        _check(lib().moe_backward_mxfp8(self.ptr, _p(dy), _p(w13t), _p(w13t_sf), _p(w2t),
+                                        _p(w2t_sf), _p(dx), _p(dw13), _p(dw2), _p(dscores),
+                                        _stream(stream)), "backward_mxfp8")
         return dx, dscores
 
     def step_host(self, x_h, ids_h, scores_h, w13, w2, y_h, dy_h=None, dw13=None, dw2=None,
@@ -229,6 +246,27 @@ def prepare_weights_mxfp8(w13, w2, stream=None):
     _check(L.moe_prepare_weights_mxfp8(_p(w13), _p(w2), d, I, E, _p(w13q), _p(w13s), _p(w2q),
                                        _p(w2s), _stream(stream)), "prepare_weights_mxfp8")
     return w13q, w13s, w2q, w2s
+
+
+def prepare_weights_mxfp8_backward(w13, w2, stream=None):
+    """bf16 W13 [E,2I,d], W2 [E,d,I] -> (W13^T codes [E,d,2I], their tiled scales,
+    W2^T codes [E,I,d], their tiled scales), the prepared weights of
+    moe_backward_mxfp8 (quantised along 2I and along d)."""
+    import torch
+
+    E, I2, d = w13.shape
+    I = I2 // 2
+    L = lib()
+    w13t = torch.empty(E, d, I2, dtype=torch.uint8, device=w13.device)
+    w2t = torch.empty(E, I, d, dtype=torch.uint8, device=w2.device)
+    w13ts = torch.empty(L.moe_mxfp8_weight_scale_bytes(d, I, E, 2), dtype=torch.uint8,
+                        device=w13.device)
+    w2ts = torch.empty(L.moe_mxfp8_weight_scale_bytes(d, I, E, 3), dtype=torch.uint8,
+                       device=w2.device)
+    _check(L.moe_prepare_weights_mxfp8_backward(_p(w13), _p(w2), d, I, E, _p(w13t), _p(w13ts),
+                                                _p(w2t), _p(w2ts), _stream(stream)),
+           "prepare_weights_mxfp8_backward")
+    return w13t, w13ts, w2t, w2ts
 
 
 def gemm_bf16(mode, A, B, C, M, N, K, stream=None):

@@ -64,6 +64,13 @@ struct moe_plan {
   int ngr_d, ngr_I;                 // 128-element scale groups along d and along I
   CUtensorMap tm_xq, tm_hq, tm_w13q, tm_w2q;
   const void *w13q_cached, *w2q_cached;
+  // MXFP8 training: DGRAD operands quantised along their K (dY along d, dA along
+  // 2I) and the WGRAD operands quantised along the rows, stored transposed
+  // ([columns, Rpad], K-major over the rows), each with tiled scales
+  uint8_t *dyq, *dysf, *dAq, *dAsf, *dyqT, *dyqTsf, *dAqT, *dAqTsf, *hsqT, *hsqTsf, *xqT, *xqTsf;
+  CUtensorMap tm_dyq, tm_dAq, tm_dyqT, tm_dAqT, tm_hsqT, tm_xqT;
+  CUtensorMap tm_w13t, tm_w2t;      // weights prepared for the backward (moe_prepare_weights_mxfp8_backward)
+  const void *w13t_cached, *w2t_cached;
   // tensor maps over the caller's fp32 weight gradients (WGRAD outputs)
   CUtensorMap tm_dw13, tm_dw2;
   const void *dw13_cached, *dw2_cached;
@@ -206,6 +213,25 @@ size_t layout(moe_plan* p, char* base, int flags) {
   p->ys = reinterpret_cast<uint16_t*>(take(2 * RP * d));
   p->a = p->dye = p->dA = p->hs = p->dxe = nullptr;
   p->pdscore = nullptr;
+  p->dyq = p->dysf = p->dAq = p->dAsf = p->dyqT = p->dyqTsf = nullptr;
+  p->dAqT = p->dAqTsf = p->hsqT = p->hsqTsf = p->xqT = p->xqTsf = nullptr;
+  if ((flags & MOE_WS_TRAINING) && mx) {
+    p->a = reinterpret_cast<uint16_t*>(take(2 * RP * 2 * I));
+    p->dA = reinterpret_cast<uint16_t*>(take(2 * RP * 2 * I));
+    p->hs = reinterpret_cast<uint16_t*>(take(2 * RP * I));
+    p->dxe = reinterpret_cast<uint16_t*>(take(2 * RP * d));
+    p->pdscore = reinterpret_cast<float*>(take(4 * RP * 2 * (I / p->bnd2)));
+    auto q = [&](size_t rows, size_t cols, uint8_t** codes, uint8_t** sf) {
+      *codes = reinterpret_cast<uint8_t*>(take(rows * cols));
+      *sf = reinterpret_cast<uint8_t*>(take((size_t)mx_sf_bytes((long long)rows, (int)cols)));
+    };
+    q(RP, d, &p->dyq, &p->dysf);
+    q(RP, 2 * I, &p->dAq, &p->dAsf);
+    q(d, RP, &p->dyqT, &p->dyqTsf);
+    q(2 * I, RP, &p->dAqT, &p->dAqTsf);
+    q(I, RP, &p->hsqT, &p->hsqTsf);
+    q(d, RP, &p->xqT, &p->xqTsf);
+  }
   if ((flags & MOE_WS_TRAINING) && !mx) {
     p->a = reinterpret_cast<uint16_t*>(take(2 * RP * 2 * I));
     p->dye = reinterpret_cast<uint16_t*>(take(2 * RP * d));
@@ -306,11 +332,17 @@ void mark(const moe_plan* p, int which, int i, cudaStream_t st);
 // gather + quantise x rows -> block-scaled W13 GEMM + SwiGLU + quantise h ->
 // block-scaled W2 GEMM x score -> combine.
 int forward_mxfp8(moe_plan* p, const void* x, const uint8_t* w13_sf, const uint8_t* w2_sf,
-                  void* y, cudaStream_t st) {
+                  void* y, int save, cudaStream_t st) {
   cudaError_t e = launch_gather_quant_rows(x, p->token_of, p->off_pad + p->E, p->d, p->xq, p->xsf,
                                            gather_grid(p), st);
   if (e != cudaSuccess) return cuda_status(e);
   p->launches += 1;
+  if (save) {
+    // the WGRAD-W13 operand: routed x rows quantised along the rows, transposed
+    e = launch_quant_rows_t(x, p->token_of, p->off_pad + p->E, 1, p->RP, p->d, p->xqT, p->xqTsf, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    p->launches += 1;
+  }
   mark(p, 0, 2, st);
   {
     GemmArgs g = rows_args(p);
@@ -321,6 +353,8 @@ int forward_mxfp8(moe_plan* p, const void* x, const uint8_t* w13_sf, const uint8
     g.out0 = p->h; g.ld0 = p->I;
     g.sfa = p->xsf; g.sfb = w13_sf; g.sf_ngr = p->ngr_d; g.b_blocks_per_expert = p->I / 64;
     g.hq = p->hq; g.hsf = p->hsf; g.hsf_ngr = p->ngr_I;
+    g.out1 = p->a; g.ld1 = 2LL * p->I;
+    g.save = save ? 1 : 0;
     g.stall_mma = p->dbg_stall_w13;
     e = launch_gemm(EPI_SWIGLU, 128, false, false, p->tm_xq, p->tm_w13q, p->tm_xq, p->tm_ys,
                     p->tm_ys, g, p->num_sms,
@@ -398,7 +432,7 @@ moe_plan* moe_plan_create(int T, int d, int I, int E, int k, int precision) {
   p->nblk = (p->R + 1023) / 1024;
   p->bn13 = I % 128 == 0 ? 256 : 128;
   p->bn2 = pick_bn_n(d) == 64 ? 128 : pick_bn_n(d);
-  p->bnd2 = pick_bn_n(I);
+  p->bnd2 = precision == MOE_PREC_MXFP8 ? 128 : pick_bn_n(I);   // block-scaled tiles are 128 wide
   p->bnw2 = pick_bn_n(I);
   p->bnw13 = p->bn2;
   p->ngr_d = d / 128;
@@ -449,10 +483,22 @@ int moe_plan_set_workspace(moe_plan* p, void* ws, size_t bytes, int flags) {
   p->dw13_cached = p->dw2_cached = nullptr;
   p->w13q_cached = p->w2q_cached = nullptr;
   const long long RP = p->RP;
+  p->w13t_cached = p->w2t_cached = nullptr;
   if (p->precision == MOE_PREC_MXFP8) {
     if (encode_tmap_u8(&p->tm_xq, p->xq, RP, p->d, 128) ||
         encode_tmap_u8(&p->tm_hq, p->hq, RP, p->I, 128) ||
         encode_tmap_bf16(&p->tm_ys, p->ys, RP, p->d, 128))
+      return MOE_ERR_CUDA;
+    if ((flags & MOE_WS_TRAINING) &&
+        (encode_tmap_u8(&p->tm_dyq, p->dyq, RP, p->d, 128) ||
+         encode_tmap_u8(&p->tm_dAq, p->dAq, RP, 2LL * p->I, 128) ||
+         encode_tmap_u8(&p->tm_dyqT, p->dyqT, p->d, RP, 128) ||
+         encode_tmap_u8(&p->tm_dAqT, p->dAqT, 2LL * p->I, RP, 128) ||
+         encode_tmap_u8(&p->tm_hsqT, p->hsqT, p->I, RP, 128) ||
+         encode_tmap_u8(&p->tm_xqT, p->xqT, p->d, RP, 128) ||
+         encode_tmap_bf16(&p->tm_dA, p->dA, RP, 2LL * p->I, 128) ||
+         encode_tmap_bf16(&p->tm_hs, p->hs, RP, p->I, 128) ||
+         encode_tmap_bf16(&p->tm_dxe, p->dxe, RP, p->d, 128)))
       return MOE_ERR_CUDA;
     return reset_error_word(p->err);
   }
@@ -483,7 +529,6 @@ int moe_forward(moe_plan* p, const void* x, const int32_t* ids, const float* sco
     return MOE_ERR_INVALID_ARG;
   if (!p->ws) return MOE_ERR_WORKSPACE;
   const bool mx = p->precision == MOE_PREC_MXFP8;
-  if (mx && save_for_backward) return MOE_ERR_UNSUPPORTED;   // MXFP8 is forward only
   if (save_for_backward && !(p->ws_flags & MOE_WS_TRAINING)) return MOE_ERR_WORKSPACE;
   if (mx && (!w13_sf || !w2_sf || !aligned16(w13_sf) || !aligned16(w2_sf)))
     return MOE_ERR_INVALID_ARG;
@@ -514,7 +559,11 @@ int moe_forward(moe_plan* p, const void* x, const int32_t* ids, const float* sco
   if (e != cudaSuccess) return cuda_status(e);
   p->launches += 3;
   mark(p, 0, 1, st);
-  if (mx) return forward_mxfp8(p, x, w13_sf, w2_sf, y, st);
+  if (mx) {
+    const int rc = forward_mxfp8(p, x, w13_sf, w2_sf, y, save_for_backward, st);
+    p->saved = (rc == MOE_OK && save_for_backward) ? 1 : 0;
+    return rc;
+  }
   // a4: gather x rows into expert-major order
   e = launch_gather_rows(x, p->token_of, p->off_pad + p->E, p->d, p->xe, gather_grid(p), st);
   if (e != cudaSuccess) return cuda_status(e);
@@ -678,6 +727,134 @@ int moe_backward(moe_plan* p, const void* dy, const void* w13, const void* w2, v
   return MOE_OK;
 }
 
+// MXFP8 backward ("What it is selling": MXFP8 E4M3 for DGRAD and WGRAD; the
+// block-scaled GEMM takes both operands quantised along its K):
+//   b1  gather + quantise dY rows along d; dY rows quantised along the rows (transposed)
+//   b2  DGRAD-W2 (block-scaled, W2^T prepared along d) + SwiGLU bwd -> dA, hs, dscore partials
+//   b2' dA quantised along 2I; dA and hs quantised along the rows (transposed)
+//   b3  DGRAD-W13 (block-scaled, W13^T prepared along 2I) -> dX_e
+//   b4  combine dX and dscores
+//   b5  WGRAD-W2  += (dY^T)_q . (hs^T)_q over each expert's rows
+//   b6  WGRAD-W13 += (dA^T)_q . (x^T)_q  (x^T quantised by the saving forward)
+int moe_backward_mxfp8(moe_plan* p, const void* dy, const uint8_t* w13t, const uint8_t* w13t_sf,
+                       const uint8_t* w2t, const uint8_t* w2t_sf, void* dx, float* dw13,
+                       float* dw2, float* dscores, void* stream_v) {
+  if (!p || !dy || !w13t || !w13t_sf || !w2t || !w2t_sf || !dx || !dw13 || !dw2 || !dscores)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(dy) || !aligned16(w13t) || !aligned16(w2t) || !aligned16(w13t_sf) ||
+      !aligned16(w2t_sf) || !aligned16(dx) || !aligned16(dw13) || !aligned16(dw2))
+    return MOE_ERR_INVALID_ARG;
+  if (p->precision != MOE_PREC_MXFP8) return MOE_ERR_UNSUPPORTED;
+  if (!p->ws || !(p->ws_flags & MOE_WS_TRAINING)) return MOE_ERR_WORKSPACE;
+  if (!p->saved) return MOE_ERR_STATE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream_v);
+  const int I = p->I, d = p->d, E = p->E;
+  const long long RP = p->RP;
+  if (w13t != p->w13t_cached) {
+    if (encode_tmap_u8(&p->tm_w13t, w13t, (long long)E * d, 2 * I, 128)) return MOE_ERR_CUDA;
+    p->w13t_cached = w13t;
+  }
+  if (w2t != p->w2t_cached) {
+    if (encode_tmap_u8(&p->tm_w2t, w2t, (long long)E * I, d, 128)) return MOE_ERR_CUDA;
+    p->w2t_cached = w2t;
+  }
+  if (dw13 != p->dw13_cached) {
+    if (encode_tmap_f32_out(&p->tm_dw13, dw13, (long long)E * 2 * I, d)) return MOE_ERR_CUDA;
+    p->dw13_cached = dw13;
+  }
+  if (dw2 != p->dw2_cached) {
+    if (encode_tmap_f32_out(&p->tm_dw2, dw2, (long long)E * d, I)) return MOE_ERR_CUDA;
+    p->dw2_cached = dw2;
+  }
+  const int32_t* nrows = p->off_pad + E;
+  mark(p, 1, 0, st);
+  // b1
+  cudaError_t e = launch_gather_quant_rows(dy, p->token_of, nrows, d, p->dyq, p->dysf,
+                                           gather_grid(p), st);
+  if (e != cudaSuccess) return cuda_status(e);
+  e = launch_quant_rows_t(dy, p->token_of, nrows, 1, (int)RP, d, p->dyqT, p->dyqTsf, st);
+  if (e != cudaSuccess) return cuda_status(e);
+  p->launches += 2;
+  mark(p, 1, 1, st);
+  // b2
+  {
+    GemmArgs g = rows_args(p);
+    g.k_blocks = d / 128;
+    g.b_expert_rows = I;
+    g.n_tiles = I / 128;
+    g.in1 = p->a; g.ldi1 = 2LL * I;
+    g.out0 = p->dA; g.ld0 = 2LL * I;
+    g.out1 = p->hs; g.ld1 = I;
+    g.row_scale = p->score_of;
+    g.pdscore = p->pdscore;
+    g.sfa = p->dysf; g.sfb = w2t_sf; g.sf_ngr = d / 128; g.b_blocks_per_expert = I / 128;
+    e = launch_gemm(EPI_DGRAD2, 128, false, false, p->tm_dyq, p->tm_w2t, p->tm_dyq, p->tm_dA,
+                    p->tm_hs, g, p->num_sms, st, true);
+    if (e != cudaSuccess) return cuda_status(e);
+    p->launches += 1;
+  }
+  // b2'
+  if ((e = launch_quant_tiled(p->dA, RP, 2 * I, 0, p->dAq, p->dAsf, st)) != cudaSuccess ||
+      (e = launch_quant_rows_t(p->dA, nullptr, nrows, 1, (int)RP, 2 * I, p->dAqT, p->dAqTsf, st)) !=
+          cudaSuccess ||
+      (e = launch_quant_rows_t(p->hs, nullptr, nrows, 1, (int)RP, I, p->hsqT, p->hsqTsf, st)) !=
+          cudaSuccess)
+    return cuda_status(e);
+  p->launches += 3;
+  mark(p, 1, 2, st);
+  // b3
+  {
+    GemmArgs g = rows_args(p);
+    g.k_blocks = 2 * I / 128;
+    g.b_expert_rows = d;
+    g.n_tiles = d / 128;
+    g.out0 = p->dxe; g.ld0 = d;
+    g.sfa = p->dAsf; g.sfb = w13t_sf; g.sf_ngr = 2 * I / 128; g.b_blocks_per_expert = d / 128;
+    e = launch_gemm(EPI_STORE, 128, false, false, p->tm_dAq, p->tm_w13t, p->tm_dAq, p->tm_dxe,
+                    p->tm_dxe, g, p->num_sms, st, true);
+    if (e != cudaSuccess) return cuda_status(e);
+    p->launches += 1;
+    mark(p, 1, 3, st);
+  }
+  // b4
+  e = launch_combine(p->dxe, p->row_of, p->T, p->k, d, dx, p->pdscore, 2 * (I / p->bnd2), dscores,
+                     gather_grid(p), st);
+  if (e != cudaSuccess) return cuda_status(e);
+  p->launches += 1;
+  mark(p, 1, 4, st);
+  // b5
+  {
+    GemmArgs g = wgrad_args(p);
+    g.wgrad_kstep = 128;
+    g.m_tiles = d / kBM;
+    g.n_tiles = I / 128;
+    g.out0 = dw2; g.ld0 = I;
+    g.out_expert_stride = (long long)d * I;
+    g.sfa = p->dyqTsf; g.sfb = p->hsqTsf; g.sf_ngr = (int)(RP / 128);
+    e = launch_gemm(EPI_WGRAD, 128, false, false, p->tm_dyqT, p->tm_hsqT, p->tm_dw2, p->tm_dw2,
+                    p->tm_dw2, g, p->num_sms, st, true);
+    if (e != cudaSuccess) return cuda_status(e);
+    p->launches += 1;
+    mark(p, 1, 5, st);
+  }
+  // b6
+  {
+    GemmArgs g = wgrad_args(p);
+    g.wgrad_kstep = 128;
+    g.m_tiles = 2 * I / kBM;
+    g.n_tiles = d / 128;
+    g.out0 = dw13; g.ld0 = d;
+    g.out_expert_stride = 2LL * I * d;
+    g.sfa = p->dAqTsf; g.sfb = p->xqTsf; g.sf_ngr = (int)(RP / 128);
+    e = launch_gemm(EPI_WGRAD, 128, false, false, p->tm_dAqT, p->tm_xqT, p->tm_dw13, p->tm_dw13,
+                    p->tm_dw13, g, p->num_sms, st, true);
+    if (e != cudaSuccess) return cuda_status(e);
+    p->launches += 1;
+    mark(p, 1, 6, st);
+  }
+  return MOE_OK;
+}
+
 int moe_step_host(moe_plan* p, const void* x_host, const int32_t* ids_host,
                   const float* scores_host, const void* dy_host, const void* w13, const void* w2,
                   float* dw13, float* dw2, void* y_host, void* dx_host, float* dscores_host,
@@ -734,7 +911,25 @@ size_t moe_mxfp8_weight_scale_bytes(int d, int I, int E, int which) {
   if (d <= 0 || I <= 0 || E <= 0 || d % 128 || I % 128) return 0;
   if (which == 0) return (size_t)mx_sf_bytes((long long)E * (I / 64) * 128, d);   // W13
   if (which == 1) return (size_t)mx_sf_bytes((long long)E * d, I);                // W2
+  if (which == 2) return (size_t)mx_sf_bytes((long long)E * d, 2 * I);            // W13^T
+  if (which == 3) return (size_t)mx_sf_bytes((long long)E * I, d);                // W2^T
   return 0;
+}
+
+int moe_prepare_weights_mxfp8_backward(const void* w13, const void* w2, int d, int I, int E,
+                                       uint8_t* w13t_codes, uint8_t* w13t_scales,
+                                       uint8_t* w2t_codes, uint8_t* w2t_scales, void* stream) {
+  if (!w13 || !w2 || !w13t_codes || !w13t_scales || !w2t_codes || !w2t_scales)
+    return MOE_ERR_INVALID_ARG;
+  if (d <= 0 || I <= 0 || E <= 0 || d % 128 || I % 128) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w13) || !aligned16(w2) || !aligned16(w13t_codes) || !aligned16(w2t_codes))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // W13[e] [2I, d] -> [d, 2I] along 2I;  W2[e] [d, I] -> [I, d] along d
+  cudaError_t e = launch_quant_rows_t(w13, nullptr, nullptr, E, 2 * I, d, w13t_codes, w13t_scales,
+                                      st);
+  if (e != cudaSuccess) return cuda_status(e);
+  return cuda_status(launch_quant_rows_t(w2, nullptr, nullptr, E, d, I, w2t_codes, w2t_scales, st));
 }
 
 int moe_prepare_weights_mxfp8(const void* w13, const void* w2, int d, int I, int E,
@@ -796,6 +991,8 @@ int moe_plan_buffer(const moe_plan* p, int which, void** ptr, size_t* bytes) {
     case MOE_BUF_XSF: q = p->xsf; b = (size_t)mx_sf_bytes((long long)RP, (int)d); break;
     case MOE_BUF_HQ: q = p->hq; b = RP * I; break;
     case MOE_BUF_HSF: q = p->hsf; b = (size_t)mx_sf_bytes((long long)RP, (int)I); break;
+    case MOE_BUF_XQT: q = p->xqT; b = (size_t)d * RP; break;
+    case MOE_BUF_XQTSF: q = p->xqTsf; b = (size_t)mx_sf_bytes((long long)d, (int)RP); break;
     default: return MOE_ERR_INVALID_ARG;
   }
   if (!q) return MOE_ERR_WORKSPACE;

@@ -45,8 +45,9 @@ struct GemmShape {
   // sub-tile buffers for the TMA-store epilogues.
   static constexpr int OUT_BYTES =
       (EPI == EPI_WGRAD ? kWgradBufs
-                        : (EPI == EPI_SCORE || EPI == EPI_STORE ? kEpiStageBufs
-                                                                : (MX ? 0 : tri_bufs<EPI>()))) * 16384;
+                        : (EPI == EPI_SCORE || EPI == EPI_STORE
+                               ? kEpiStageBufs
+                               : (MX && EPI == EPI_SWIGLU ? 0 : tri_bufs<EPI>()))) * 16384;
   static constexpr int STAGE_BUDGET = 226 * 1024 - OUT_BYTES;
   static constexpr int STAGES = STAGE_BUDGET / STAGE_BYTES > 8 ? 8 : STAGE_BUDGET / STAGE_BYTES;
   static constexpr int BAR_BYTES = 256;
@@ -155,9 +156,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (MX) {
             // the 512-byte scale chunks of this K group: A's row block, B's row block
             const uint32_t ssf = sb + S::B_BYTES;
-            const long long ga = ((long long)(ti.m0 >> 7) * args.sf_ngr + kb) * 512;
-            const long long gb =
-                (((long long)ti.e * args.b_blocks_per_expert + ti.nt) * args.sf_ngr + kb) * 512;
+            // row GEMMs: K groups from 0, B row block of (expert, n tile); wgrad
+            // mode: K groups from the expert's first row, B row block n0/128
+            const long long kg = (long long)(ti.krow0 >> 7) + kb;
+            const long long ga = ((long long)(ti.m0 >> 7) * args.sf_ngr + kg) * 512;
+            const long long gbr = args.wgrad ? (long long)(ti.n0 >> 7)
+                                             : (long long)ti.e * args.b_blocks_per_expert + ti.nt;
+            const long long gb = (gbr * args.sf_ngr + kg) * 512;
             bulk_g2s(ssf, args.sfa + ga, 512u, fb);
             bulk_g2s(ssf + 512u, args.sfb + gb, 512u, fb);
           }
@@ -167,10 +172,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (A_MN)
             tma_load_3d(sa, &tmA, 0, ti.krow0 + kb * kBK, ti.m0 >> 6, fb);
           else
-            tma_load_2d(sa, &tmA, kb * KE, ti.m0, fb);
+            tma_load_2d(sa, &tmA, ti.krow0 + kb * KE, ti.m0, fb);
           // B: BN rows (N) x 128 bytes of K
-          if (args.wgrad) {
+          if (args.wgrad && B_MN) {
             tma_load_3d(sb, &tmB, 0, ti.krow0 + kb * kBK, ti.n0 >> 6, fb);
+          } else if (args.wgrad) {
+            // K-major transposed operand [N, rows]: this expert's K range
+            tma_load_2d(sb, &tmB, ti.krow0 + kb * KE, ti.n0, fb);
           } else if (B_MN) {
             // [E*K, N]: BN/64 atoms of expert e's K rows
             tma_load_3d(sb, &tmB, 0, ti.e * args.b_expert_rows + kb * kBK, ti.n0 >> 6, fb);
@@ -364,6 +372,12 @@ cudaError_t launch_gemm(int epi, int bn, bool a_mn, bool b_mn, const CUtensorMap
       return launch_one<128, false, false, EPI_SWIGLU, true>(ta, tb, tc, to0, to1, args, grid, stream);
     if (epi == EPI_SCORE && bn == 128 && !a_mn && !b_mn)
       return launch_one<128, false, false, EPI_SCORE, true>(ta, tb, tc, to0, to1, args, grid, stream);
+    if (epi == EPI_DGRAD2 && bn == 128 && !a_mn && !b_mn)
+      return launch_one<128, false, false, EPI_DGRAD2, true>(ta, tb, tc, to0, to1, args, grid, stream);
+    if (epi == EPI_STORE && bn == 128 && !a_mn && !b_mn)
+      return launch_one<128, false, false, EPI_STORE, true>(ta, tb, tc, to0, to1, args, grid, stream);
+    if (epi == EPI_WGRAD && bn == 128 && !a_mn && !b_mn)
+      return launch_one<128, false, false, EPI_WGRAD, true>(ta, tb, tc, to0, to1, args, grid, stream);
     return cudaErrorInvalidValue;
   }
 #define MOE_CASE(EPI_, BN_, AMN_, BMN_)                                     \

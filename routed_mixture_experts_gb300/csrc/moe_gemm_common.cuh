@@ -42,7 +42,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int tile) {
     ti.m0 = mt * kBM;
     ti.n0 = ti.nt * BN;
     ti.krow0 = a.off_pad[ti.e];
-    ti.kb = (a.off_pad[ti.e + 1] - ti.krow0) / kBK;
+    ti.kb = (a.off_pad[ti.e + 1] - ti.krow0) / (a.wgrad_kstep ? a.wgrad_kstep : kBK);
   } else {
     const int mt = tile / a.n_tiles;
     ti.nt = tile - mt * a.n_tiles;
@@ -121,9 +121,15 @@ __device__ __forceinline__ void load16_bf16(const uint16_t* src, float (&v)[16])
 // epilogues: one thread owns one output row (`row` within the tile) and reads
 // its accumulator columns from TMEM at `tbase` (lane quarter already folded in).
 
+__device__ __forceinline__ void pack32(const float (&v)[32], uint32_t (&pk)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) pk[i] = pack_bf2(v[2 * i], v[2 * i + 1]);
+}
+
 // MXFP8 W13 epilogue: like the bf16 one (R1, SwiGLU, R2), then h is quantised
 // along I in 32-column blocks (codes to a.hq, tiled E8M0 scales to a.hsf) as the
-// A operand of the block-scaled W2 GEMM; the bf16 h is kept for inspection.
+// A operand of the block-scaled W2 GEMM; the bf16 h is kept (the backward's
+// operand), and with a.save so is a (a.out1, [rows, 2I]).
 template <int BN>
 __device__ __forceinline__ void epilogue_swiglu_mx(const GemmArgs& a, const TileInfo& ti, int row,
                                                    uint32_t tbase, int half) {
@@ -141,13 +147,31 @@ __device__ __forceinline__ void epilogue_swiglu_mx(const GemmArgs& a, const Tile
     tmem_ld16(tbase + BNH + c, u0);
     tmem_ld16(tbase + BNH + c + 16, u1);
     tmem_ld_wait();
-    float hv[32];
+    float hv[32], gv[32], uv[32];
 #pragma unroll
     for (int q = 0; q < 16; ++q) {
-      const float G0 = bf2f(f2bf(__uint_as_float(g0[q]))), U0 = bf2f(f2bf(__uint_as_float(u0[q])));
-      const float G1 = bf2f(f2bf(__uint_as_float(g1[q]))), U1 = bf2f(f2bf(__uint_as_float(u1[q])));
-      hv[q] = bf2f(f2bf(swiglu_fwd(G0, U0, a.clamp)));            // R2
-      hv[16 + q] = bf2f(f2bf(swiglu_fwd(G1, U1, a.clamp)));
+      gv[q] = bf2f(f2bf(__uint_as_float(g0[q])));                  // R1
+      uv[q] = bf2f(f2bf(__uint_as_float(u0[q])));
+      gv[16 + q] = bf2f(f2bf(__uint_as_float(g1[q])));
+      uv[16 + q] = bf2f(f2bf(__uint_as_float(u1[q])));
+      hv[q] = bf2f(f2bf(swiglu_fwd(gv[q], uv[q], a.clamp)));       // R2
+      hv[16 + q] = bf2f(f2bf(swiglu_fwd(gv[16 + q], uv[16 + q], a.clamp)));
+    }
+    if (a.save) {
+      // training: keep the gate/up pre-activations a for the backward
+      uint16_t* arow = static_cast<uint16_t*>(a.out1) + grow * a.ld1 + c0 + c;
+      uint32_t pk[16];
+      pack32(gv, pk);
+      reinterpret_cast<uint4*>(arow)[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      reinterpret_cast<uint4*>(arow)[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      reinterpret_cast<uint4*>(arow)[2] = make_uint4(pk[8], pk[9], pk[10], pk[11]);
+      reinterpret_cast<uint4*>(arow)[3] = make_uint4(pk[12], pk[13], pk[14], pk[15]);
+      pack32(uv, pk);
+      arow += a.I;
+      reinterpret_cast<uint4*>(arow)[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      reinterpret_cast<uint4*>(arow)[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      reinterpret_cast<uint4*>(arow)[2] = make_uint4(pk[8], pk[9], pk[10], pk[11]);
+      reinterpret_cast<uint4*>(arow)[3] = make_uint4(pk[12], pk[13], pk[14], pk[15]);
     }
     float lo[16], hi[16];
 #pragma unroll
@@ -254,11 +278,6 @@ __device__ __forceinline__ void epi_stage_three(const CUtensorMap* t0, const CUt
     const uint32_t(&pk1)[1][16] = *reinterpret_cast<const uint32_t(*)[1][16]>(&pk[2]);
     epi_stage_batch<1>(tms1, buf, et, row, half, pk1, xs1, y);
   }
-}
-
-__device__ __forceinline__ void pack32(const float (&v)[32], uint32_t (&pk)[16]) {
-#pragma unroll
-  for (int i = 0; i < 16; ++i) pk[i] = pack_bf2(v[2 * i], v[2 * i + 1]);
 }
 
 __device__ __forceinline__ void load32_bf16(const uint16_t* src, float (&v)[32]) {

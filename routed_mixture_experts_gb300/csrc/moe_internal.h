@@ -53,6 +53,7 @@ struct GemmArgs {
   float clamp;               // SwiGLU limit (0 = plain)
   int I;                     // column offset of the up half in a / dA
   int save;                  // EPI_SWIGLU: store a
+  int wgrad_kstep;           // wgrad mode: rows per K stage (0: 64; MXFP8: 128)
   // MXFP8 (block-scaled) operands: tiled E8M0 scales (see mx_sf_offset)
   const uint8_t* sfa;        // scales of A, row blocks of 128 padded rows
   const uint8_t* sfb;        // scales of B, row block = e * b_blocks_per_expert + n tile
@@ -158,5 +159,13 @@ cudaError_t launch_quant_tiled(const void* in, long long rows, int K, int gu_I, 
 cudaError_t launch_gather_quant_rows(const void* x, const int32_t* token_of, const int32_t* nrows,
                                      int d, uint8_t* codes, uint8_t* sf, int grid,
                                      cudaStream_t stream);
+// Quantise along rows, transposed: `batch` bf16 matrices [R, C] (batch stride
+// R*C; with src_row the single matrix's row r is row src_row[r] of `in`, zero
+// where negative) -> E4M3 codes [batch][C][R] and tiled E8M0 scales with row
+// blocks of 128 over C (block batch*(C/128) + c/128) and K groups of 128 over R.
+// Rows r >= *nrows (when nrows != NULL) are skipped.  R % 128 == 0, C % 128 == 0.
+cudaError_t launch_quant_rows_t(const void* in, const int32_t* src_row, const int32_t* nrows,
+                                int batch, int R, int C, uint8_t* codes, uint8_t* sf,
+                                cudaStream_t stream);
 
 }  // namespace moe

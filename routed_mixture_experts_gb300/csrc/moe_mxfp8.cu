@@ -133,7 +133,63 @@ __global__ void __launch_bounds__(256) k_gather_quant_rows(const uint4* __restri
   }
 }
 
+// Quantise along rows, transposed: for each of `batch` matrices in [R, C] bf16
+// (batch stride R*C; with src_row, row r of the single matrix is row
+// src_row[r] of `in`, zero where src_row[r] < 0), write codes [C, R] (each
+// column becomes a K-major row, K = R) and scales in the tiled layout with row
+// blocks of 128 over the batch's C rows (block batch*(C/128) + c/128) and K
+// groups of 128 over R.  The blocks of 32 run along r.  Rows r >= *nrows_p (when
+// given) are not written.  A CTA takes 32 rows x 256 columns: it stages them in
+// shared memory and each thread quantises one column's 32 values.
+constexpr int kQtRows = 32, kQtCols = 256;
+
+__global__ void __launch_bounds__(kQtCols) k_quant_rows_t(const uint16_t* __restrict__ in,
+                                                          const int32_t* __restrict__ src_row,
+                                                          const int32_t* __restrict__ nrows_p,
+                                                          int R, int C,
+                                                          uint8_t* __restrict__ codes,
+                                                          uint8_t* __restrict__ sf) {
+  __shared__ __align__(16) uint16_t tile[kQtRows][kQtCols];
+  const int r0 = blockIdx.x * kQtRows;
+  const int c0 = blockIdx.y * kQtCols;
+  const long long b = blockIdx.z;
+  const int nrows = nrows_p ? *nrows_p : R;
+  if (r0 >= nrows) return;
+  const uint16_t* mat = in + b * (long long)R * C;
+  // coalesced loads: 32 rows x 256 columns, 8 bf16 (16 bytes) per access
+  for (int q = threadIdx.x; q < kQtRows * kQtCols / 8; q += kQtCols) {
+    const int rr = q / (kQtCols / 8), cc = (q % (kQtCols / 8)) * 8;
+    const int r = r0 + rr;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    const long long srow = r >= nrows ? -1 : (src_row ? (long long)src_row[r] : (long long)r);
+    if (srow >= 0 && c0 + cc < C) v = *reinterpret_cast<const uint4*>(mat + srow * C + c0 + cc);
+    *reinterpret_cast<uint4*>(&tile[rr][cc]) = v;
+  }
+  __syncthreads();
+  const int c = c0 + threadIdx.x;
+  if (c >= C) return;
+  float f[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(((uint32_t)tile[i][threadIdx.x]) << 16);
+  uint32_t w[8];
+  const uint8_t scv = mx_quant32(f, w);
+  uint4* dst = reinterpret_cast<uint4*>(codes + (b * (long long)C + c) * R + r0);
+  dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  sf[mx_sf_offset(b * (C / 128) + (c >> 7), c & 127, r0 / 32, R / 128)] = scv;
+}
+
 }  // namespace
+
+cudaError_t launch_quant_rows_t(const void* in, const int32_t* src_row, const int32_t* nrows,
+                                int batch, int R, int C, uint8_t* codes, uint8_t* sf,
+                                cudaStream_t stream) {
+  if (R % 128 || C % 128 || batch < 1) return cudaErrorInvalidValue;
+  const dim3 grid(R / kQtRows, (C + kQtCols - 1) / kQtCols, batch);
+  k_quant_rows_t<<<grid, kQtCols, 0, stream>>>(static_cast<const uint16_t*>(in), src_row, nrows,
+                                               R, C, codes, sf);
+  return cudaGetLastError();
+}
 
 long long mx_sf_bytes(long long rows_padded128, int K) {
   return rows_padded128 / 128 * (long long)(K / 128) * 512;
