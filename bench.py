@@ -409,6 +409,7 @@ def run_ours(args):
 
     # MXFP8 E4M3 forward on the same inputs (its workload differs only in precision)
     mx = None
+    mx_train = None
     if args.mx_steps > 0:
         w13q, w13s, w2q, w2s = moe.prepare_weights_mxfp8(D["w13"], D["w2"])
         mplan = moe.MoePlan(T, d, I, E, k, precision=moe.MOE_PREC_MXFP8, clamp=c["clamp"], flags=0,
@@ -452,6 +453,52 @@ def run_ours(args):
               "value": 6.0 * T * k * d * I * ws / (mms * 1e-3) / 1e12, "unit": "TFLOP/s",
               "ms_per_step": mms, "steps": args.mx_steps,
               "peak_note": "fp8 peak = measured sustained bf16 x 2 (nominal ratio)", "stages": mst}
+        del mplan
+
+        # MXFP8 training step: saving forward + block-scaled backward
+        w13t, w13ts, w2t, w2ts = moe.prepare_weights_mxfp8_backward(D["w13"], D["w2"])
+        tplan = moe.MoePlan(T, d, I, E, k, precision=moe.MOE_PREC_MXFP8, clamp=c["clamp"],
+                            flags=moe.MOE_WS_TRAINING, device=dev)
+        dxm = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+        dsm = torch.empty(T, k, dtype=torch.float32, device=dev)
+
+        def tstep():
+            tplan.forward(D["x"], D["ids"], D["scores"], w13q, w2q, y=ym, w13_sf=w13s,
+                          w2_sf=w2s, save=True)
+            tplan.backward_mxfp8(D["dy"], w13t, w13ts, w2t, w2ts, D["dw13"], D["dw2"], dx=dxm,
+                                 dscores=dsm)
+
+        for _ in range(args.warmup):
+            tstep()
+        tf = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.mx_steps)]
+        tb = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.mx_steps)]
+        for ev in [e for st_ in tf + tb for e in st_]:
+            ev.record(stream)
+        torch.cuda.synchronize()
+        m0.record(stream)
+        for i in range(args.mx_steps):
+            tplan.set_timing_events(0, tf[i])
+            tplan.set_timing_events(1, tb[i])
+            tstep()
+        m1.record(stream)
+        torch.cuda.synchronize()
+        tplan.set_timing_events(0, None)
+        tplan.set_timing_events(1, None)
+        rc, det = tplan.check()
+        if rc != 0:
+            raise RuntimeError("device error %d (%d) in the MXFP8 training step" % (rc, det))
+        tms = max_over_ranks(m0.elapsed_time(m1), dev) / args.mx_steps
+        tst = {}
+        for evs, names in ((tf, FWD_STAGES), (tb, BWD_STAGES)):
+            for j, name in enumerate(names):
+                t_ms = sum(evs[i][j].elapsed_time(evs[i][j + 1])
+                           for i in range(args.mx_steps)) / args.mx_steps
+                tst[name] = {"ms": round(t_ms, 5)}
+        mx_train = {"workload": "mxfp8_e128 training (same sizes and inputs; forward with saved "
+                                "activations + block-scaled DGRAD and WGRAD)",
+                    "value": 18.0 * T * k * d * I * ws / (tms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                    "ms_per_step": tms, "steps": args.mx_steps, "stages": tst}
+        del tplan
 
     if rank != 0:
         return
@@ -479,7 +526,7 @@ def run_ours(args):
         "fwd_tflops": 6.0 * T * k * d * I / (fwd_ms * 1e-3) / 1e12,
         "fwd_ms": fwd_ms,
         "e2e": e2e, "gpu_launches": int(n1 - n0), "roofline": roofline, "stages": stages,
-        "cpu_baseline": cpu, "clocks": clk, "mxfp8_forward": mx,
+        "cpu_baseline": cpu, "clocks": clk, "mxfp8_forward": mx, "mxfp8_training": mx_train,
     }
     print(json.dumps(line), flush=True)
 
