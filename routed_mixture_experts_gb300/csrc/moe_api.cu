@@ -333,16 +333,15 @@ void mark(const moe_plan* p, int which, int i, cudaStream_t st);
 // block-scaled W2 GEMM x score -> combine.
 int forward_mxfp8(moe_plan* p, const void* x, const uint8_t* w13_sf, const uint8_t* w2_sf,
                   void* y, int save, cudaStream_t st) {
-  cudaError_t e = launch_gather_quant_rows(x, p->token_of, p->off_pad + p->E, p->d, p->xq, p->xsf,
-                                           gather_grid(p), st);
+  // gather + quantise x rows along d; a saving forward also quantises them along
+  // the rows, transposed (the WGRAD-W13 operand), in the same pass
+  cudaError_t e =
+      save ? launch_quant_two_way(x, p->token_of, p->off_pad + p->E, p->RP, p->d, p->xq, p->xsf,
+                                  p->xqT, p->xqTsf, st)
+           : launch_gather_quant_rows(x, p->token_of, p->off_pad + p->E, p->d, p->xq, p->xsf,
+                                      gather_grid(p), st);
   if (e != cudaSuccess) return cuda_status(e);
   p->launches += 1;
-  if (save) {
-    // the WGRAD-W13 operand: routed x rows quantised along the rows, transposed
-    e = launch_quant_rows_t(x, p->token_of, p->off_pad + p->E, 1, p->RP, p->d, p->xqT, p->xqTsf, st);
-    if (e != cudaSuccess) return cuda_status(e);
-    p->launches += 1;
-  }
   mark(p, 0, 2, st);
   {
     GemmArgs g = rows_args(p);
@@ -729,9 +728,9 @@ int moe_backward(moe_plan* p, const void* dy, const void* w13, const void* w2, v
 
 // MXFP8 backward ("What it is selling": MXFP8 E4M3 for DGRAD and WGRAD; the
 // block-scaled GEMM takes both operands quantised along its K):
-//   b1  gather + quantise dY rows along d; dY rows quantised along the rows (transposed)
+//   b1  gather dY rows and quantise them along d and along the rows (transposed), one pass
 //   b2  DGRAD-W2 (block-scaled, W2^T prepared along d) + SwiGLU bwd -> dA, hs, dscore partials
-//   b2' dA quantised along 2I; dA and hs quantised along the rows (transposed)
+//   b2' dA quantised along 2I and along the rows (one pass); hs along the rows
 //   b3  DGRAD-W13 (block-scaled, W13^T prepared along 2I) -> dX_e
 //   b4  combine dX and dscores
 //   b5  WGRAD-W2  += (dY^T)_q . (hs^T)_q over each expert's rows
@@ -769,12 +768,10 @@ int moe_backward_mxfp8(moe_plan* p, const void* dy, const uint8_t* w13t, const u
   const int32_t* nrows = p->off_pad + E;
   mark(p, 1, 0, st);
   // b1
-  cudaError_t e = launch_gather_quant_rows(dy, p->token_of, nrows, d, p->dyq, p->dysf,
-                                           gather_grid(p), st);
+  cudaError_t e = launch_quant_two_way(dy, p->token_of, nrows, (int)RP, d, p->dyq, p->dysf,
+                                       p->dyqT, p->dyqTsf, st);
   if (e != cudaSuccess) return cuda_status(e);
-  e = launch_quant_rows_t(dy, p->token_of, nrows, 1, (int)RP, d, p->dyqT, p->dyqTsf, st);
-  if (e != cudaSuccess) return cuda_status(e);
-  p->launches += 2;
+  p->launches += 1;
   mark(p, 1, 1, st);
   // b2
   {
@@ -794,13 +791,12 @@ int moe_backward_mxfp8(moe_plan* p, const void* dy, const uint8_t* w13t, const u
     p->launches += 1;
   }
   // b2'
-  if ((e = launch_quant_tiled(p->dA, RP, 2 * I, 0, p->dAq, p->dAsf, st)) != cudaSuccess ||
-      (e = launch_quant_rows_t(p->dA, nullptr, nrows, 1, (int)RP, 2 * I, p->dAqT, p->dAqTsf, st)) !=
-          cudaSuccess ||
+  if ((e = launch_quant_two_way(p->dA, nullptr, nrows, (int)RP, 2 * I, p->dAq, p->dAsf, p->dAqT,
+                                p->dAqTsf, st)) != cudaSuccess ||
       (e = launch_quant_rows_t(p->hs, nullptr, nrows, 1, (int)RP, I, p->hsqT, p->hsqTsf, st)) !=
           cudaSuccess)
     return cuda_status(e);
-  p->launches += 3;
+  p->launches += 2;
   mark(p, 1, 2, st);
   // b3
   {

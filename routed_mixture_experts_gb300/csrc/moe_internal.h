@@ -167,5 +167,11 @@ cudaError_t launch_gather_quant_rows(const void* x, const int32_t* token_of, con
 cudaError_t launch_quant_rows_t(const void* in, const int32_t* src_row, const int32_t* nrows,
                                 int batch, int R, int C, uint8_t* codes, uint8_t* sf,
                                 cudaStream_t stream);
+// Both quantisations of one [R, C] bf16 operand (rows via src_row as above) in
+// one pass: along C into codes_row [R, C] + tiled scales (128-row blocks, K
+// groups over C), and along the rows into codes_t [C, R] + tiled scales.
+cudaError_t launch_quant_two_way(const void* in, const int32_t* src_row, const int32_t* nrows,
+                                 int R, int C, uint8_t* codes_row, uint8_t* sf_row,
+                                 uint8_t* codes_t, uint8_t* sf_t, cudaStream_t stream);
 
 }  // namespace moe

@@ -3,7 +3,7 @@ against the oracle's MXFP8 backward.
 
 Bit-exact: the weights prepared for the backward (W13^T along 2I, W2^T along
 d, codes and scales) and the routed x rows quantised along the rows (the
-WGRAD-W13 operand).  Within the MXFP8 tolerance (relative Frobenius 1e-2,
+WGRAD-W13 operand) and along d (the forward's operand, same pass).  Within the MXFP8 tolerance (relative Frobenius 1e-2,
 tests/parity.py): dx, dscores, the intermediates dA and hs, and the weight
 gradient increments of every expert (small cases) or of sampled experts (full
 size).
@@ -103,6 +103,10 @@ def test_mxfp8_backward_small(moe, orc, sizes):
     assert np.array_equal(gq, qT)
     gs = untile(plan.buffer("xqTsf", torch.uint8).cpu().numpy(), d, RP)[:, : n // 32]
     assert np.array_equal(gs, sT)
+    # ... and along d (the forward's A operand), from the same pass
+    qx, sx = orc.quant_mxfp8(xrows)
+    assert np.array_equal(plan.buffer("xq", torch.uint8).cpu().numpy()[: n * d].reshape(n, d), qx)
+    assert np.array_equal(untile(plan.buffer("xsf", torch.uint8).cpu().numpy(), n, d), sx)
     # outputs and intermediates
     dxr, dsr, bi = orc.backward_mxfp8(inp["x"], inp["ids"], inp["scores"], fw, bw, inp["dy"],
                                       clamp=L, intermediates=True)
