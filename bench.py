@@ -57,6 +57,8 @@ def parse():
     # smaller cases of the same workload (profiling captures); defaults = the full workload
     ap.add_argument("--T", type=int, default=None)
     ap.add_argument("--E", type=int, default=None)
+    ap.add_argument("--cta-pairs", action="store_true",
+                    help="W13, W2 and DGRAD-W13 on CTA pairs (moe_plan_set_cta_pairs)")
     return ap.parse_args()
 
 
@@ -295,7 +297,8 @@ def run_ours(args):
 
     D = {key: to_dev(inp[key]) for key in need}
     plan = moe.MoePlan(T, d, I, E, k, clamp=c["clamp"],
-                       flags=moe.MOE_WS_TRAINING | moe.MOE_WS_HOST_STAGING, device=dev)
+                       flags=moe.MOE_WS_TRAINING | moe.MOE_WS_HOST_STAGING, device=dev,
+                       cta_pairs=args.cta_pairs)
     y = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
     dx = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
     dsc = torch.empty(T, k, dtype=torch.float32, device=dev)

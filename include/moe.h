@@ -349,19 +349,19 @@ int moe_dispatch_static(const int32_t* ids, const float* scores, int T, int k, i
 int moe_tile_rows(void);
 
 /*
- * Row GEMMs on CTA pairs.  on = 1 runs the four row GEMMs of a bf16 plan (W13,
- * W2, and the two DGRADs) on pairs of CTAs of a thread-block cluster with
- * 256 x 256 tiles (tcgen05 cta_group::2): each CTA reads a third less operand
- * data per product, but expert segments are then padded to 256 rows instead of
- * 128, which pays off when experts receive many rows (few experts, large T).
+ * Row GEMMs on CTA pairs.  on = 1 runs W13, W2 and DGRAD-W13 of a bf16 plan on
+ * pairs of CTAs of a thread-block cluster with 256 x 256 tiles (tcgen05
+ * cta_group::2), each CTA reading a third less operand data per product: the
+ * 128-row m tiles of each expert go to the pair kernel two at a time, and an
+ * expert's odd last m tile to the one-CTA kernel (dispatch builds both lists),
+ * so expert segments stay padded to 128 rows.  DGRAD-W2 stays on one CTA.
  * Must be called before moe_plan_workspace_bytes / moe_plan_set_workspace
  * (MOE_ERR_STATE afterwards); needs d % 256 == 0 and I % 256 == 0 (else
- * MOE_ERR_UNSUPPORTED).  Off by default.
+ * MOE_ERR_UNSUPPORTED).
  */
 int moe_plan_set_cta_pairs(moe_plan* plan, int on);
 
-/* Padding granule of this plan's expert segments (off_pad): 256 with CTA pairs,
- * else 128. */
+/* Padding granule of this plan's expert segments (off_pad): 128. */
 int moe_plan_row_granule(const moe_plan* plan);
 
 /*

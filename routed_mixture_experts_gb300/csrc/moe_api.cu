@@ -33,8 +33,9 @@ struct moe_plan {
   int RP;       // worst-case padded rows
   int nblk;     // dispatch chunks
   int bn13, bn2, bnd2, bnw2, bnw13;
-  int pair;     // row GEMMs on CTA pairs (256-row tiles)
-  int gran;     // padding granule of expert segments (128, or 256 with pairs)
+  int pair;     // W13, W2 and DGRAD-W13 on CTA pairs (256-row tiles over pairs of an
+                // expert's 128-row m tiles; an odd last m tile runs on one CTA)
+  int gran;     // padding granule of expert segments (128)
   // workspace
   char* ws;
   size_t ws_bytes;
@@ -58,7 +59,10 @@ struct moe_plan {
   CUtensorMap tm_ys, tm_a, tm_hs, tm_dxe;
   // tensor maps over the caller's weights (re-encoded when the pointers change)
   CUtensorMap tm_w13, tm_w2, tm_w13_mn, tm_w2_mn;
+  CUtensorMap tm_w13_p, tm_w2_p, tm_w13_mn_p;   // the CTA-pair kernel's (128-row halves)
   const void *w13_cached, *w2_cached;
+  // CTA-pair tile lists (dispatch output): pairs of m tiles, odd last m tiles
+  int32_t *pair_list, *left_list, *num_pairs, *num_left;
   // MXFP8: quantised expert-major activations and h, with tiled scales
   uint8_t *xq, *xsf, *hq, *hsf;
   int ngr_d, ngr_I;                 // 128-element scale groups along d and along I
@@ -196,6 +200,13 @@ size_t layout(moe_plan* p, char* base, int flags) {
   p->num_nonempty = reinterpret_cast<int32_t*>(take(4));
   p->expert_order = reinterpret_cast<int32_t*>(take(4 * E));
   p->tile_expert = reinterpret_cast<int32_t*>(take(4 * (RP / kBM)));
+  p->pair_list = p->left_list = p->num_pairs = p->num_left = nullptr;
+  if (p->pair) {
+    p->pair_list = reinterpret_cast<int32_t*>(take(4 * (RP / kBM / 2 + 1)));
+    p->left_list = reinterpret_cast<int32_t*>(take(4 * E));
+    p->num_pairs = reinterpret_cast<int32_t*>(take(4));
+    p->num_left = reinterpret_cast<int32_t*>(take(4));
+  }
   p->blockcounts = reinterpret_cast<int32_t*>(take(4 * (size_t)p->nblk * E));
   p->row_of = reinterpret_cast<int32_t*>(take(4 * (size_t)p->R));
   p->token_of = reinterpret_cast<int32_t*>(take(4 * RP));
@@ -275,24 +286,25 @@ int reset_error_word(DevError* err) {
 }
 
 int refresh_weight_maps(moe_plan* p, const void* w13, const void* w2) {
-  // B boxes: W13 gate/up halves and W2 rows of one N tile (a CTA's half with pairs)
-  const int b13 = p->pair ? 128 : p->bn13 / 2;
-  const int b2 = p->pair ? 128 : p->bn2;
+  // B boxes of the one-CTA kernel: W13 gate and up rows of a tile in one 3-D box,
+  // W2 rows of one N tile; the CTA-pair kernel loads 128-row halves (2-D boxes,
+  // two 64-wide atoms MN-major)
   if (w13 != p->w13_cached) {
-    // one-CTA W13: gate and up rows of a tile in one 3-D box; CTA pairs: 2-D boxes
-    const int r13 = p->pair ? encode_tmap_bf16(&p->tm_w13, w13, (long long)p->E * 2 * p->I, p->d, b13)
-                            : encode_tmap_gate_up(&p->tm_w13, false, w13, p->E, p->I, p->d, b13);
-    if (r13 != MOE_OK ||
-        encode_tmap_bf16_mn(&p->tm_w13_mn, w13, (long long)p->E * 2 * p->I, p->d,
-                            p->pair ? 2 : p->bn2 / 64) != MOE_OK)
+    const long long r13 = (long long)p->E * 2 * p->I;
+    if (encode_tmap_gate_up(&p->tm_w13, false, w13, p->E, p->I, p->d, p->bn13 / 2) != MOE_OK ||
+        encode_tmap_bf16_mn(&p->tm_w13_mn, w13, r13, p->d, p->bn2 / 64) != MOE_OK)
+      return MOE_ERR_CUDA;
+    if (p->pair && (encode_tmap_bf16(&p->tm_w13_p, w13, r13, p->d, 128) != MOE_OK ||
+                    encode_tmap_bf16_mn(&p->tm_w13_mn_p, w13, r13, p->d, 2) != MOE_OK))
       return MOE_ERR_CUDA;
     p->w13_cached = w13;
   }
   if (w2 != p->w2_cached) {
-    if (encode_tmap_bf16(&p->tm_w2, w2, (long long)p->E * p->d, p->I, b2) != MOE_OK ||
-        encode_tmap_bf16_mn(&p->tm_w2_mn, w2, (long long)p->E * p->d, p->I,
-                            p->pair ? 2 : p->bnd2 / 64) != MOE_OK)
+    const long long r2 = (long long)p->E * p->d;
+    if (encode_tmap_bf16(&p->tm_w2, w2, r2, p->I, p->bn2) != MOE_OK ||
+        encode_tmap_bf16_mn(&p->tm_w2_mn, w2, r2, p->I, p->bnd2 / 64) != MOE_OK)
       return MOE_ERR_CUDA;
+    if (p->pair && encode_tmap_bf16(&p->tm_w2_p, w2, r2, p->I, 128) != MOE_OK) return MOE_ERR_CUDA;
     p->w2_cached = w2;
   }
   return MOE_OK;
@@ -453,8 +465,6 @@ int moe_plan_set_cta_pairs(moe_plan* p, int on) {
   if (p->ws) return MOE_ERR_STATE;               // the granule sizes the workspace
   if (on && (p->precision != MOE_PREC_BF16 || p->I % 256 || p->d % 256)) return MOE_ERR_UNSUPPORTED;
   p->pair = on ? 1 : 0;
-  p->gran = p->pair ? 256 : kBM;
-  p->RP = (int)(((long long)p->R + (long long)p->E * (p->gran - 1)) / p->gran * p->gran);
   return MOE_OK;
 }
 
@@ -547,13 +557,15 @@ int moe_forward(moe_plan* p, const void* x, const int32_t* ids, const float* sco
 
   mark(p, 0, 0, st);
   // a1-a3: dispatch
-  RouteArgs ra;
+  RouteArgs ra{};                 // every pointer not set below stays NULL
   ra.ids = ids; ra.scores = scores;
   ra.T = p->T; ra.k = p->k; ra.E = p->E; ra.BM = p->gran; ra.nblk = p->nblk;
   ra.blockcounts = p->blockcounts; ra.counts = p->counts; ra.m_indptr = p->m_indptr;
   ra.off_pad = p->off_pad; ra.num_mtiles = p->num_mtiles; ra.tile_expert = p->tile_expert;
   ra.expert_order = p->expert_order; ra.num_nonempty = p->num_nonempty;
   ra.row_of = p->row_of; ra.token_of = p->token_of; ra.score_of = p->score_of; ra.err = p->err;
+  ra.pair_list = p->pair_list; ra.left_list = p->left_list;
+  ra.num_pairs = p->num_pairs; ra.num_left = p->num_left;
   cudaError_t e = launch_route(ra, st);
   if (e != cudaSuccess) return cuda_status(e);
   p->launches += 3;
@@ -580,14 +592,17 @@ int moe_forward(moe_plan* p, const void* x, const int32_t* ids, const float* sco
     g.save = save_for_backward ? 1 : 0;
     g.stall_mma = p->dbg_stall_w13;
     if (p->pair) {
-      g.n_tiles = p->I / 128;
-      e = launch_gemm_pair(EPI_SWIGLU, false, p->tm_xe, p->tm_w13, p->tm_h, p->tm_a, g,
+      GemmArgs gp = g;
+      gp.n_tiles = p->I / 128;
+      gp.mtile_list = p->pair_list; gp.list_count = p->num_pairs;
+      e = launch_gemm_pair(EPI_SWIGLU, false, p->tm_xe, p->tm_w13_p, p->tm_h, p->tm_a, gp,
                            p->num_sms, st);
-    } else {
-      e = launch_gemm(EPI_SWIGLU, p->bn13, false, false, p->tm_xe, p->tm_w13, p->tm_xe, p->tm_h,
-                      p->tm_a, g,
-                      p->num_sms, st);
+      if (e != cudaSuccess) return cuda_status(e);
+      p->launches += 1;
+      g.mtile_list = p->left_list; g.list_count = p->num_left;   // odd last m tiles
     }
+    e = launch_gemm(EPI_SWIGLU, p->bn13, false, false, p->tm_xe, p->tm_w13, p->tm_xe, p->tm_h,
+                    p->tm_a, g, p->num_sms, st);
     if (e != cudaSuccess) return cuda_status(e);
     p->launches += 1;
     mark(p, 0, 3, st);
@@ -601,13 +616,17 @@ int moe_forward(moe_plan* p, const void* x, const int32_t* ids, const float* sco
     g.out0 = p->ys; g.ld0 = p->d;
     g.row_scale = p->score_of;
     if (p->pair) {
-      g.n_tiles = p->d / 256;
-      e = launch_gemm_pair(EPI_SCORE, false, p->tm_h, p->tm_w2, p->tm_ys, p->tm_ys, g,
+      GemmArgs gp = g;
+      gp.n_tiles = p->d / 256;
+      gp.mtile_list = p->pair_list; gp.list_count = p->num_pairs;
+      e = launch_gemm_pair(EPI_SCORE, false, p->tm_h, p->tm_w2_p, p->tm_ys, p->tm_ys, gp,
                            p->num_sms, st);
-    } else {
-      e = launch_gemm(EPI_SCORE, p->bn2, false, false, p->tm_h, p->tm_w2, p->tm_h, p->tm_ys,
-                      p->tm_ys, g, p->num_sms, st);
+      if (e != cudaSuccess) return cuda_status(e);
+      p->launches += 1;
+      g.mtile_list = p->left_list; g.list_count = p->num_left;
     }
+    e = launch_gemm(EPI_SCORE, p->bn2, false, false, p->tm_h, p->tm_w2, p->tm_h, p->tm_ys,
+                    p->tm_ys, g, p->num_sms, st);
     if (e != cudaSuccess) return cuda_status(e);
     p->launches += 1;
     mark(p, 0, 4, st);
@@ -658,13 +677,9 @@ int moe_backward(moe_plan* p, const void* dy, const void* w13, const void* w2, v
     g.out1 = p->hs; g.ld1 = I;
     g.row_scale = p->score_of;
     g.pdscore = p->pdscore;
-    if (p->pair)
-      e = launch_gemm_pair(EPI_DGRAD2, true, p->tm_dye, p->tm_w2_mn, p->tm_dA, p->tm_hs, g,
-                           p->num_sms, st);
-    else
-      e = launch_gemm(EPI_DGRAD2, p->bnd2, false, true, p->tm_dye, p->tm_w2_mn, p->tm_dye,
-                      p->tm_dA, p->tm_hs, g,
-                      p->num_sms, st);
+    // one CTA per tile (also with CTA pairs: this epilogue-bound GEMM measured no faster on pairs)
+    e = launch_gemm(EPI_DGRAD2, p->bnd2, false, true, p->tm_dye, p->tm_w2_mn, p->tm_dye, p->tm_dA,
+                    p->tm_hs, g, p->num_sms, st);
     if (e != cudaSuccess) return cuda_status(e);
     p->launches += 1;
     mark(p, 1, 2, st);
@@ -677,14 +692,17 @@ int moe_backward(moe_plan* p, const void* dy, const void* w13, const void* w2, v
     g.n_tiles = d / p->bn2;
     g.out0 = p->dxe; g.ld0 = d;
     if (p->pair) {
-      g.n_tiles = d / 256;
-      e = launch_gemm_pair(EPI_STORE, true, p->tm_dA, p->tm_w13_mn, p->tm_dxe, p->tm_dxe, g,
+      GemmArgs gp = g;
+      gp.n_tiles = d / 256;
+      gp.mtile_list = p->pair_list; gp.list_count = p->num_pairs;
+      e = launch_gemm_pair(EPI_STORE, true, p->tm_dA, p->tm_w13_mn_p, p->tm_dxe, p->tm_dxe, gp,
                            p->num_sms, st);
-    } else {
-      e = launch_gemm(EPI_STORE, p->bn2, false, true, p->tm_dA, p->tm_w13_mn, p->tm_dA, p->tm_dxe,
-                      p->tm_dxe, g,
-                      p->num_sms, st);
+      if (e != cudaSuccess) return cuda_status(e);
+      p->launches += 1;
+      g.mtile_list = p->left_list; g.list_count = p->num_left;
     }
+    e = launch_gemm(EPI_STORE, p->bn2, false, true, p->tm_dA, p->tm_w13_mn, p->tm_dA, p->tm_dxe,
+                    p->tm_dxe, g, p->num_sms, st);
     if (e != cudaSuccess) return cuda_status(e);
     p->launches += 1;
     mark(p, 1, 3, st);

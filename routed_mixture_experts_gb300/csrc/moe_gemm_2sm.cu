@@ -78,7 +78,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint64_t wlim = args.wait_limit_ns ? args.wait_limit_ns : kWaitLimitNs;
 
   if (threadIdx.x == 0) {
-    num_tiles_s = (*args.num_mtiles >> 1) * args.n_tiles;
+    num_tiles_s = (args.mtile_list ? *args.list_count : (*args.num_mtiles >> 1)) * args.n_tiles;
     abort_s = 0;
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);        // leader: one arrive (with both CTAs' bytes)
@@ -117,8 +117,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   auto decode = [&](int tile, TileInfo& ti) {
     const int mp = tile / args.n_tiles;
     ti.nt = tile - mp * args.n_tiles;
-    ti.e = args.tile_expert ? args.tile_expert[2 * mp] : 0;
-    ti.m0 = mp * 256 + 128 * (int)rank;        // this CTA's rows
+    const int mt = args.mtile_list ? args.mtile_list[mp] : 2 * mp;   // the pair's first m tile
+    ti.e = args.tile_expert ? args.tile_expert[mt] : 0;
+    ti.m0 = mt * 128 + 128 * (int)rank;        // this CTA's rows
     ti.n0 = ti.nt * BN;
     ti.kb = args.k_blocks;
     ti.krow0 = 0;

@@ -26,7 +26,7 @@ struct TileInfo {
 
 __device__ __forceinline__ int count_tiles(const GemmArgs& a) {
   if (a.wgrad) return (*a.num_nonempty) * a.m_tiles * a.n_tiles;
-  return (*a.num_mtiles) * a.n_tiles;
+  return (a.mtile_list ? *a.list_count : *a.num_mtiles) * a.n_tiles;
 }
 
 template <int BN>
@@ -44,8 +44,9 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int tile) {
     ti.krow0 = a.off_pad[ti.e];
     ti.kb = (a.off_pad[ti.e + 1] - ti.krow0) / (a.wgrad_kstep ? a.wgrad_kstep : kBK);
   } else {
-    const int mt = tile / a.n_tiles;
-    ti.nt = tile - mt * a.n_tiles;
+    const int q = tile / a.n_tiles;
+    ti.nt = tile - q * a.n_tiles;
+    const int mt = a.mtile_list ? a.mtile_list[q] : q;
     ti.e = a.tile_expert ? a.tile_expert[mt] : 0;
     ti.m0 = mt * kBM;
     ti.n0 = ti.nt * BN;

@@ -37,6 +37,9 @@ struct GemmArgs {
   int b_expert_rows;         // rows of B's 2-D tensor map per expert
   int b_half_rows;           // EPI_SWIGLU: row offset of the up half (I)
   // wgrad mode
+  const int* mtile_list;     // row mode: the m tiles to run (NULL: all, 0..num_mtiles-1);
+                             // pair kernel: first m tile of each pair (NULL: 2q)
+  const int* list_count;     // device count of mtile_list entries
   const int* off_pad;        // device [E+1]
   const int* expert_order;   // device [E]: experts with rows first, longest first
   const int* num_nonempty;   // device scalar
@@ -130,6 +133,12 @@ struct RouteArgs {
   int32_t* token_of;         // [Rpad max]
   float* score_of;           // [Rpad max]
   DevError* err;
+  // CTA-pair row GEMMs (NULL otherwise): each expert's m tiles two at a time
+  // (first m tile of each pair) and its odd last m tile, with their counts
+  int32_t* pair_list;        // [max m tiles / 2]
+  int32_t* left_list;        // [E]
+  int32_t* num_pairs;        // scalar
+  int32_t* num_left;         // scalar
 };
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t stream);
 

@@ -140,6 +140,41 @@ __global__ void __launch_bounds__(kMaxE) k_route_scan(RouteArgs a) {
     for (int e2 = 0; e2 < E; ++e2) ne += cnt[e2] > 0;
     *a.num_nonempty = ne;
   }
+  if (a.pair_list) {
+    // CTA-pair tile lists: expert e's m tiles [f, f+mt) go two at a time to the
+    // pair kernel (pair_list), an odd last one to the one-CTA kernel (left_list)
+    const int mt = p / kBM;
+    const int np = mt >> 1, nl = mt & 1;
+    const int ipp = warp_incl_scan(np, lane), ipl = warp_incl_scan(nl, lane);
+    __syncthreads();                       // warp_tot reused
+    if (lane == 31) {
+      warp_tot[0][warp] = ipp;
+      warp_tot[1][warp] = ipl;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const int nw = blockDim.x / 32;
+      int t0 = lane < nw ? warp_tot[0][lane] : 0;
+      int t1 = lane < nw ? warp_tot[1][lane] : 0;
+      const int s0 = warp_incl_scan(t0, lane), s1 = warp_incl_scan(t1, lane);
+      if (lane < nw) {
+        warp_tot[0][lane] = s0 - t0;
+        warp_tot[1][lane] = s1 - t1;
+      }
+    }
+    __syncthreads();
+    const int bp = warp_tot[0][warp] + ipp - np;   // exclusive bases
+    const int bl = warp_tot[1][warp] + ipl - nl;
+    if (tid < E) {
+      const int f = ep / kBM;
+      for (int j = 0; j < np; ++j) a.pair_list[bp + j] = f + 2 * j;
+      if (nl) a.left_list[bl] = f + mt - 1;
+      if (tid == E - 1) {
+        *a.num_pairs = bp + np;
+        *a.num_left = bl + nl;
+      }
+    }
+  }
 }
 
 __global__ void __launch_bounds__(kChunk) k_route_scatter(RouteArgs a) {

@@ -94,7 +94,7 @@ extern "C" int moe_dispatch_static(const int32_t* ids, const float* scores, int 
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   moe::DevError* err = reinterpret_cast<moe::DevError*>(base + kOffErr);
-  moe::RouteArgs ra;
+  moe::RouteArgs ra{};            // every pointer not set below stays NULL
   ra.ids = ids;
   ra.scores = scores;
   ra.T = T;

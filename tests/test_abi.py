@@ -102,8 +102,8 @@ def test_cta_pairs_option_sizes_the_workspace(L):
         assert L.moe_plan_row_granule(p) == 128
         one = L.moe_plan_workspace_bytes(p, 1)
         assert L.moe_plan_set_cta_pairs(p, 1) == 0
-        assert L.moe_plan_row_granule(p) == 256
-        assert L.moe_plan_workspace_bytes(p, 1) > one          # 256-row padding
+        assert L.moe_plan_row_granule(p) == 128                # segments stay 128-row
+        assert one < L.moe_plan_workspace_bytes(p, 1) < one + 65536   # + the pair tile lists
         assert L.moe_plan_set_cta_pairs(p, 0) == 0
         assert L.moe_plan_workspace_bytes(p, 1) == one
         assert L.moe_plan_set_cta_pairs(q, 1) == 7             # d, I not multiples of 256

@@ -50,8 +50,10 @@ SMALL = [
                         zipf_support=8), {}),
     ("single_expert", dict(T=130, d=128, I=64, E=1, k=1), {}),
     ("k8_e256", dict(T=96, d=128, I=64, E=256, k=8), {}),
-    # row GEMMs on CTA pairs (moe_plan_set_cta_pairs), 256-row expert segments
+    # W13, W2 and DGRAD-W13 on CTA pairs (moe_plan_set_cta_pairs): pairs of an
+    # expert's m tiles on the pair kernel, an odd last m tile on one CTA
     ("pairs", dict(T=300, d=256, I=256, E=6, k=3, cta_pairs=True), {}),
+    ("pairs_odd_tiles", dict(T=700, d=256, I=256, E=6, k=3, cta_pairs=True), {}),
     ("pairs_clamp_pad", dict(T=200, d=512, I=256, E=9, k=2, clamp=1.0, pad=20, cta_pairs=True),
      {}),
     ("pairs_skew", dict(T=400, d=256, I=512, E=12, k=3, routing="zipf", zipf_s=1.2,
