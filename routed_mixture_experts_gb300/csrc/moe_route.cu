@@ -207,31 +207,49 @@ __global__ void __launch_bounds__(kChunk) k_route_scatter(RouteArgs a) {
 
 // ---------------------------------------------------------------------------
 
+// One warp per pair of rows: both rows' 16-byte vectors are loaded before any is
+// stored (2 x 8 loads in flight per lane), and the next pair's token ids are
+// fetched before this pair's data.
 __global__ void __launch_bounds__(256) k_gather_rows(const uint4* __restrict__ src,
                                                      const int32_t* __restrict__ token_of,
                                                      const int32_t* __restrict__ nrows_p, int nvec,
                                                      uint4* __restrict__ dst) {
+  constexpr int U = 8;                     // vectors per lane per row and pass
   const int nrows = *nrows_p;
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
-  for (int r = gw; r < nrows; r += nw) {
-    const int t = token_of[r];
-    const uint4* s = src + (long long)(t < 0 ? 0 : t) * nvec;
-    uint4* o = dst + (long long)r * nvec;
-    for (int v0 = 0; v0 < nvec; v0 += 32 * 8) {
-      uint4 buf[8];
+  int r = 2 * gw;
+  int t0 = r < nrows ? token_of[r] : -1;
+  int t1 = r + 1 < nrows ? token_of[r + 1] : -1;
+  for (; r < nrows; r += 2 * nw) {
+    const int rn = r + 2 * nw;
+    const int n0 = rn < nrows ? token_of[rn] : -1;
+    const int n1 = rn + 1 < nrows ? token_of[rn + 1] : -1;
+    const bool has1 = r + 1 < nrows;
+    const uint4* s0 = src + (long long)(t0 < 0 ? 0 : t0) * nvec;
+    const uint4* s1 = src + (long long)(t1 < 0 ? 0 : t1) * nvec;
+    uint4* o0 = dst + (long long)r * nvec;
+    uint4* o1 = o0 + nvec;
+    for (int v0 = 0; v0 < nvec; v0 += 32 * U) {
+      uint4 b0[U], b1[U];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < U; ++u) {
         const int v = v0 + lane + 32 * u;
-        buf[u] = (t >= 0 && v < nvec) ? s[v] : make_uint4(0, 0, 0, 0);
+        b0[u] = (t0 >= 0 && v < nvec) ? s0[v] : make_uint4(0, 0, 0, 0);
+        b1[u] = (t1 >= 0 && v < nvec) ? s1[v] : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < U; ++u) {
         const int v = v0 + lane + 32 * u;
-        if (v < nvec) o[v] = buf[u];
+        if (v < nvec) {
+          o0[v] = b0[u];
+          if (has1) o1[v] = b1[u];
+        }
       }
     }
+    t0 = n0;
+    t1 = n1;
   }
 }
 
