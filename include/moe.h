@@ -174,7 +174,10 @@ int moe_backward_mxfp8(moe_plan* plan, const void* dy, const uint8_t* w13t,
  * copies x_host, ids_host, scores_host (and dy_host) into the plan's staging
  * area, runs moe_forward (+ moe_backward), and copies y (and dx, dscores) back
  * into the host buffers, all enqueued on `stream`; the caller synchronises the
- * stream before reading the host outputs.  Host buffers should be pinned
+ * stream before reading the host outputs.  In a training step the dY upload
+ * and the y download run on a plan-owned side stream (created with the
+ * host-staging workspace), overlapped with the forward and the backward; it
+ * forks from and joins `stream`, so ordering is that of one stream.  Host buffers should be pinned
  * (page-locked) for the copies to be asynchronous.  Weights and weight
  * gradients stay on the device.  Needs a MOE_WS_HOST_STAGING workspace (plus
  * MOE_WS_TRAINING when dy_host != NULL).

@@ -86,6 +86,14 @@ struct moe_plan {
   void* const* ev[2];
   int nev[2];
   long long launches;
+  // moe_step_host: a side stream and events that overlap the dY upload with the
+  // forward and the y download with the backward (created with a host-staging
+  // workspace)
+  cudaStream_t side;
+  cudaEvent_t ev_fork, ev_dy, ev_y, ev_ydone, ev_x, ev_comb, ev_dxdone;
+  // set by moe_step_host only: the forward waits on wait_before_gather before
+  // its gather, the backward records record_after_combine after its combine
+  cudaEvent_t wait_before_gather, record_after_combine;
 };
 
 namespace moe {
@@ -458,7 +466,20 @@ moe_plan* moe_plan_create(int T, int d, int I, int E, int k, int precision) {
   return p;
 }
 
-void moe_plan_destroy(moe_plan* p) { delete p; }
+void moe_plan_destroy(moe_plan* p) {
+  if (!p) return;
+  if (p->side) {
+    cudaStreamDestroy(p->side);
+    cudaEventDestroy(p->ev_fork);
+    cudaEventDestroy(p->ev_dy);
+    cudaEventDestroy(p->ev_y);
+    cudaEventDestroy(p->ev_ydone);
+    cudaEventDestroy(p->ev_x);
+    cudaEventDestroy(p->ev_comb);
+    cudaEventDestroy(p->ev_dxdone);
+  }
+  delete p;
+}
 
 int moe_plan_set_cta_pairs(moe_plan* p, int on) {
   if (!p) return MOE_ERR_INVALID_ARG;
@@ -483,6 +504,18 @@ size_t moe_plan_workspace_bytes(const moe_plan* p, int flags) {
 int moe_plan_set_workspace(moe_plan* p, void* ws, size_t bytes, int flags) {
   if (!p || !ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return MOE_ERR_INVALID_ARG;
   if (bytes < moe_plan_workspace_bytes(p, flags)) return MOE_ERR_WORKSPACE;
+  if ((flags & MOE_WS_HOST_STAGING) && !p->side) {
+    const unsigned ef = cudaEventDisableTiming;
+    if (cudaStreamCreateWithFlags(&p->side, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p->ev_fork, ef) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p->ev_dy, ef) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p->ev_y, ef) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p->ev_ydone, ef) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p->ev_x, ef) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p->ev_comb, ef) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p->ev_dxdone, ef) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
   p->ws = static_cast<char*>(ws);
   p->ws_bytes = bytes;
   p->ws_flags = flags;
@@ -571,11 +604,16 @@ int moe_forward(moe_plan* p, const void* x, const int32_t* ids, const float* sco
   p->launches += 3;
   mark(p, 0, 1, st);
   if (mx) {
+    if (p->wait_before_gather &&
+        (e = cudaStreamWaitEvent(st, p->wait_before_gather, 0)) != cudaSuccess)
+      return cuda_status(e);
     const int rc = forward_mxfp8(p, x, w13_sf, w2_sf, y, save_for_backward, st);
     p->saved = (rc == MOE_OK && save_for_backward) ? 1 : 0;
     return rc;
   }
   // a4: gather x rows into expert-major order
+  if (p->wait_before_gather && (e = cudaStreamWaitEvent(st, p->wait_before_gather, 0)) != cudaSuccess)
+    return cuda_status(e);
   e = launch_gather_rows(x, p->token_of, p->off_pad + p->E, p->d, p->xe, gather_grid(p), st);
   if (e != cudaSuccess) return cuda_status(e);
   p->launches += 1;
@@ -713,6 +751,9 @@ int moe_backward(moe_plan* p, const void* dy, const void* w13, const void* w2, v
   if (e != cudaSuccess) return cuda_status(e);
   p->launches += 1;
   mark(p, 1, 4, st);
+  if (p->record_after_combine &&
+      (e = cudaEventRecord(p->record_after_combine, st)) != cudaSuccess)
+    return cuda_status(e);
   // b5: dW2[e] += dY_e^T . hs_e
   {
     GemmArgs g = wgrad_args(p);
@@ -879,29 +920,50 @@ int moe_step_host(moe_plan* p, const void* x_host, const int32_t* ids_host,
   if (train && (!(p->ws_flags & MOE_WS_TRAINING) || !dx_host || !dscores_host))
     return train && !(p->ws_flags & MOE_WS_TRAINING) ? MOE_ERR_WORKSPACE : MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream_v);
+  cudaStream_t sd = p->side;
   const size_t xb = 2ull * p->T * p->d, sb = 4ull * p->T * p->k;
   cudaError_t e;
-  if ((e = cudaMemcpyAsync(p->st_x, x_host, xb, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
-      (e = cudaMemcpyAsync(p->st_ids, ids_host, sb, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
+  // Copies overlap compute on a plan-owned side stream that forks from and
+  // joins `stream`: x uploads during dispatch, dY during the forward; y
+  // downloads during the backward, dx and dscores during the weight gradients.
+  if ((e = cudaEventRecord(p->ev_fork, st)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(sd, p->ev_fork, 0)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(p->st_x, x_host, xb, cudaMemcpyHostToDevice, sd)) != cudaSuccess ||
+      (e = cudaEventRecord(p->ev_x, sd)) != cudaSuccess)
+    return cuda_status(e);
+  if (train && ((e = cudaMemcpyAsync(p->st_dy, dy_host, xb, cudaMemcpyHostToDevice, sd)) !=
+                    cudaSuccess ||
+                (e = cudaEventRecord(p->ev_dy, sd)) != cudaSuccess))
+    return cuda_status(e);
+  if ((e = cudaMemcpyAsync(p->st_ids, ids_host, sb, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
       (e = cudaMemcpyAsync(p->st_scores, scores_host, sb, cudaMemcpyHostToDevice, st)) != cudaSuccess)
     return cuda_status(e);
-  if (train && (e = cudaMemcpyAsync(p->st_dy, dy_host, xb, cudaMemcpyHostToDevice, st)) != cudaSuccess)
-    return cuda_status(e);
+  p->wait_before_gather = p->ev_x;
   int rc = moe_forward(p, p->st_x, p->st_ids, p->st_scores, w13, w2, nullptr, nullptr, p->st_y,
                        train ? 1 : 0, stream_v);
+  p->wait_before_gather = nullptr;
   if (rc != MOE_OK) return rc;
-  if (train) {
-    rc = moe_backward(p, p->st_dy, w13, w2, p->st_dx, dw13, dw2, p->st_dscores, stream_v);
-    if (rc != MOE_OK) return rc;
-  }
-  if ((e = cudaMemcpyAsync(y_host, p->st_y, xb, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
-    return cuda_status(e);
-  if (train) {
-    if ((e = cudaMemcpyAsync(dx_host, p->st_dx, xb, cudaMemcpyDeviceToHost, st)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(dscores_host, p->st_dscores, sb, cudaMemcpyDeviceToHost, st)) !=
-            cudaSuccess)
+  if (!train) {
+    if ((e = cudaMemcpyAsync(y_host, p->st_y, xb, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
       return cuda_status(e);
+    return MOE_OK;
   }
+  if ((e = cudaEventRecord(p->ev_y, st)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(sd, p->ev_y, 0)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(y_host, p->st_y, xb, cudaMemcpyDeviceToHost, sd)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(st, p->ev_dy, 0)) != cudaSuccess)
+    return cuda_status(e);
+  p->record_after_combine = p->ev_comb;
+  rc = moe_backward(p, p->st_dy, w13, w2, p->st_dx, dw13, dw2, p->st_dscores, stream_v);
+  p->record_after_combine = nullptr;
+  if (rc != MOE_OK) return rc;
+  if ((e = cudaStreamWaitEvent(sd, p->ev_comb, 0)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(dx_host, p->st_dx, xb, cudaMemcpyDeviceToHost, sd)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(dscores_host, p->st_dscores, sb, cudaMemcpyDeviceToHost, sd)) !=
+          cudaSuccess ||
+      (e = cudaEventRecord(p->ev_dxdone, sd)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(st, p->ev_dxdone, 0)) != cudaSuccess)
+    return cuda_status(e);
   return MOE_OK;
 }
 
