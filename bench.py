@@ -57,6 +57,8 @@ def parse():
     # smaller cases of the same workload (profiling captures); defaults = the full workload
     ap.add_argument("--T", type=int, default=None)
     ap.add_argument("--E", type=int, default=None)
+    ap.add_argument("--graph", action="store_true",
+                    help="time the steps as one CUDA graph replay (stage events as graph nodes)")
     ap.add_argument("--cta-pairs", action="store_true",
                     help="W13, W2 and DGRAD-W13 on CTA pairs (moe_plan_set_cta_pairs)")
     return ap.parse_args()
@@ -329,12 +331,28 @@ def run_ours(args):
     clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     time.sleep(0.25 if clocks else 0)
     n0 = plan.launch_count()
-    t_start.record(stream)
-    for i in range(K):
-        plan.set_timing_events(0, evf[i])
-        plan.set_timing_events(1, evb[i])
-        step()
-    t_end.record(stream)
+    if args.graph:
+        # the K timed steps (with their stage events) as one CUDA graph: the
+        # plan allocates nothing and never synchronises, so the step captures
+        cs = torch.cuda.Stream()
+        cs.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cs):
+            for i in range(K):
+                plan.set_timing_events(0, evf[i])
+                plan.set_timing_events(1, evb[i])
+                step()
+        torch.cuda.synchronize()
+        t_start.record(stream)
+        graph.replay()
+        t_end.record(stream)
+    else:
+        t_start.record(stream)
+        for i in range(K):
+            plan.set_timing_events(0, evf[i])
+            plan.set_timing_events(1, evb[i])
+            step()
+        t_end.record(stream)
     n1 = plan.launch_count()
     torch.cuda.synchronize()
     barrier()
@@ -525,7 +543,9 @@ def run_ours(args):
         "config": {"workload": "%s (T=%d, d=%d, I=%d, E=%d, k=%d, uniform routing, "
                                "forward+backward)" % (WORKLOAD, T, d, I, E, k),
                    "tokens_per_gpu": T, "l2": "inputs larger than L2 (%.1f GB resident per GPU)"
-                   % (ws_bytes / 1e9), "parallelism": "replicas" if ws > 1 else "single GPU"},
+                   % (ws_bytes / 1e9), "parallelism": "replicas" if ws > 1 else "single GPU",
+                   "launch": "CUDA graph replay of the timed steps" if args.graph
+                             else "eager launches"},
         "fwd_tflops": 6.0 * T * k * d * I / (fwd_ms * 1e-3) / 1e12,
         "fwd_ms": fwd_ms,
         "e2e": e2e, "gpu_launches": int(n1 - n0), "roofline": roofline, "stages": stages,

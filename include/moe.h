@@ -296,7 +296,9 @@ int moe_plan_buffer(const moe_plan* plan, int which, void** dev_ptr, size_t* byt
  *     [2] after DGRAD-W2 + SwiGLU backward, [3] after DGRAD-W13,
  *     [4] after dX/dscores combine, [5] after WGRAD-W2, [6] after WGRAD-W13
  * n = 0 (or events = NULL) stops recording.  The plan keeps the pointer: the
- * array must stay valid while set.
+ * array must stay valid while set.  The records are "external" ones
+ * (cudaEventRecordExternal), so events captured in a CUDA graph still time
+ * each replay.
  */
 int moe_plan_set_timing_events(moe_plan* plan, int which, void* const* events, int n);
 

@@ -278,11 +278,12 @@ size_t layout(moe_plan* p, char* base, int flags) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int cuda_status(cudaError_t e) {
+int cuda_status_at(cudaError_t e, int line) {
   if (e == cudaSuccess) return MOE_OK;
-  fprintf(stderr, "moe_gb300: CUDA error %s\n", cudaGetErrorString(e));
+  fprintf(stderr, "moe_gb300: CUDA error %s (moe_api.cu:%d)\n", cudaGetErrorString(e), line);
   return MOE_ERR_CUDA;
 }
+#define cuda_status(e) cuda_status_at((e), __LINE__)
 
 int reset_error_word(DevError* err) {
   DevError h;
@@ -406,8 +407,16 @@ int forward_mxfp8(moe_plan* p, const void* x, const uint8_t* w13_sf, const uint8
 }
 
 void mark(const moe_plan* p, int which, int i, cudaStream_t st) {
-  if (p->ev[which] && i < p->nev[which] && p->ev[which][i])
-    cudaEventRecord(static_cast<cudaEvent_t>(p->ev[which][i]), st);
+  if (!(p->ev[which] && i < p->nev[which] && p->ev[which][i])) return;
+  cudaEvent_t ev = static_cast<cudaEvent_t>(p->ev[which][i]);
+  // while a stream is being captured into a CUDA graph the record must be an
+  // "external" one to stay a real (timed) event record in the graph
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  const bool capturing =
+      cudaStreamIsCapturing(st, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive;
+  const cudaError_t e = capturing ? cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal)
+                                  : cudaEventRecord(ev, st);
+  if (e != cudaSuccess) (void)cudaGetLastError();   // optional timing: never fail the step
 }
 
 }  // namespace
