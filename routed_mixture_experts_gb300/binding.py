@@ -173,14 +173,15 @@ class MoePlan:
                                    _stream(stream)), "step_host")
 
     def set_timing_events(self, which, events):
-        """Record `events` (torch.cuda.Event list, or None) at the stage boundaries
-        of every following forward (which=0) or backward (which=1) call."""
+        """Record `events` (torch.cuda.Event list, None entries skipped; or None) at the
+        stage boundaries of every following forward (which=0) or backward (which=1) call."""
         if not events:
             self._ev = getattr(self, "_ev", {})
             self._ev.pop(which, None)
             _check(lib().moe_plan_set_timing_events(self.ptr, which, None, 0), "timing")
             return
-        arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+        handles = [None if e is None else e.cuda_event for e in events]
+        arr = (ctypes.c_void_p * len(events))(*handles)
         self._ev = getattr(self, "_ev", {})
         self._ev[which] = (arr, events)          # keep the handles alive while set
         _check(lib().moe_plan_set_timing_events(self.ptr, which, arr, len(events)), "timing")

@@ -45,6 +45,19 @@ __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Kernels of the hot path are launched so that
+// the next kernel in the stream may be scheduled before this one has finished
+// (launch_pdl); every kernel therefore starts with pdl_wait(), which returns
+// once the previous kernel has completed and its writes are visible, and calls
+// pdl_trigger() when its own work is done (a CTA that exits counts as
+// triggered), so a dependent grid only takes resources the current one no
+// longer needs.  Launched without the attribute, both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // shared-memory addresses
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

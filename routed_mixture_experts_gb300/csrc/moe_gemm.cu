@@ -71,6 +71,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   static_assert(!MX || (!A_MN && !B_MN && BN == 128), "MXFP8: K-major operands, BN = 128");
   static_assert(S::SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
+  pdl_wait();   // the previous kernel of the stream has completed
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t tmem_holder;
@@ -337,6 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (et == 0) bulk_wait_all();   // every output store has completed
   }
 
+  pdl_trigger();   // this CTA's tiles are done: the next kernel may be scheduled
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -357,8 +359,7 @@ cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUten
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  kern<<<grid, kThreads, smem, stream>>>(ta, tb, tc, to0, to1, args);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, stream, ta, tb, tc, to0, to1, args);
 }
 
 }  // namespace

@@ -55,6 +55,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   static_assert(PS::SMEM <= 232448, "shared memory budget");
   constexpr uint32_t IDESC = idesc_bf16(256, BN, false, B_MN);
   static_assert(EPI != EPI_WGRAD, "rows mode only");
+  pdl_wait();   // the previous kernel of the stream has completed
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t tmem_holder;
@@ -284,6 +285,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (et == 0) bulk_wait_all();   // every output store has completed
   }
 
+  pdl_trigger();   // this CTA's tiles are done: the next kernel may be scheduled
   tc_fence_before();
   __syncthreads();
   cluster_sync();                  // no CTA leaves while its peer may still signal it
@@ -301,8 +303,7 @@ cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
   constexpr int smem = PairShape<EPI>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid & ~1, kThreads, smem, stream>>>(ta, tb, to0, to1, args);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid & ~1), dim3(kThreads), smem, stream, ta, tb, to0, to1, args);
 }
 
 }  // namespace

@@ -62,6 +62,7 @@ __device__ __forceinline__ void unpack_bf16x32(const uint4 (&v)[4], float (&f)[3
 __global__ void __launch_bounds__(256) k_quant_tiled(const uint4* __restrict__ in, long long rows,
                                                      int K, int gu_I, uint4* __restrict__ codes,
                                                      uint8_t* __restrict__ sf) {
+  pdl_wait();   // the previous kernel of the stream has completed
   const int kbs = K / 32;
   const int ngr = K / 128;
   const long long nblocks = rows * kbs;
@@ -93,6 +94,7 @@ __global__ void __launch_bounds__(256) k_quant_tiled(const uint4* __restrict__ i
     }
     sf[mx_sf_offset(rblock, rin, kb, ngr)] = sc;
   }
+  pdl_trigger();
 }
 
 // Gather + quantise: padded row r of the expert-major activations is token
@@ -103,6 +105,7 @@ __global__ void __launch_bounds__(256) k_gather_quant_rows(const uint4* __restri
                                                            const int32_t* __restrict__ nrows_p,
                                                            int d, uint4* __restrict__ codes,
                                                            uint8_t* __restrict__ sf) {
+  pdl_wait();   // the previous kernel of the stream has completed
   const int nrows = *nrows_p;
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -131,6 +134,7 @@ __global__ void __launch_bounds__(256) k_gather_quant_rows(const uint4* __restri
       sf[mx_sf_offset(r >> 7, r & 127, kb, ngr)] = sc;
     }
   }
+  pdl_trigger();
 }
 
 // Quantise along rows, transposed: for each of `batch` matrices in [R, C] bf16
@@ -149,6 +153,7 @@ __global__ void __launch_bounds__(kQtCols) k_quant_rows_t(const uint16_t* __rest
                                                           int R, int C,
                                                           uint8_t* __restrict__ codes,
                                                           uint8_t* __restrict__ sf) {
+  pdl_wait();   // the previous kernel of the stream has completed
   __shared__ __align__(16) uint16_t tile[kQtRows][kQtCols];
   const int r0 = blockIdx.x * kQtRows;
   const int c0 = blockIdx.y * kQtCols;
@@ -177,6 +182,7 @@ __global__ void __launch_bounds__(kQtCols) k_quant_rows_t(const uint16_t* __rest
   dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
   dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
   sf[mx_sf_offset(b * (C / 128) + (c >> 7), c & 127, r0 / 32, R / 128)] = scv;
+  pdl_trigger();
 }
 
 // Both quantisations of one [R, C] bf16 operand in one pass (R = padded rows;
@@ -200,6 +206,7 @@ __global__ void __launch_bounds__(kQtCols) k_quant_two_way(const uint16_t* __res
                                                            uint8_t* __restrict__ sf_row,
                                                            uint8_t* __restrict__ codes_t,
                                                            uint8_t* __restrict__ sf_t) {
+  pdl_wait();   // the previous kernel of the stream has completed
   extern __shared__ __align__(16) uint16_t tw_tile[];    // [kTwRows][kTwLd]
   const int r0 = blockIdx.x * kTwRows;
   const int c0 = blockIdx.y * kQtCols;
@@ -263,6 +270,7 @@ __global__ void __launch_bounds__(kQtCols) k_quant_two_way(const uint16_t* __res
     *reinterpret_cast<uint32_t*>(sfp) = sc4;
   else
     *reinterpret_cast<uint16_t*>(sfp) = (uint16_t)sc4;
+  pdl_trigger();
 }
 
 }  // namespace
@@ -279,10 +287,9 @@ cudaError_t launch_quant_two_way(const void* in, const int32_t* src_row, const i
     configured = true;
   }
   const dim3 grid(R / kTwRows, (C + kQtCols - 1) / kQtCols, 1);
-  k_quant_two_way<<<grid, kQtCols, kTwSmem, stream>>>(static_cast<const uint16_t*>(in), src_row,
-                                                      nrows, R, C, codes_row, sf_row, codes_t,
-                                                      sf_t);
-  return cudaGetLastError();
+  return launch_pdl(k_quant_two_way, grid, dim3(kQtCols), kTwSmem, stream,
+                    static_cast<const uint16_t*>(in), src_row, nrows, R, C, codes_row, sf_row,
+                    codes_t, sf_t);
 }
 
 cudaError_t launch_quant_rows_t(const void* in, const int32_t* src_row, const int32_t* nrows,
@@ -290,9 +297,8 @@ cudaError_t launch_quant_rows_t(const void* in, const int32_t* src_row, const in
                                 cudaStream_t stream) {
   if (R % 128 || C % 128 || batch < 1) return cudaErrorInvalidValue;
   const dim3 grid(R / kQtRows, (C + kQtCols - 1) / kQtCols, batch);
-  k_quant_rows_t<<<grid, kQtCols, 0, stream>>>(static_cast<const uint16_t*>(in), src_row, nrows,
-                                               R, C, codes, sf);
-  return cudaGetLastError();
+  return launch_pdl(k_quant_rows_t, grid, dim3(kQtCols), 0, stream,
+                    static_cast<const uint16_t*>(in), src_row, nrows, R, C, codes, sf);
 }
 
 long long mx_sf_bytes(long long rows_padded128, int K) {
@@ -305,17 +311,17 @@ cudaError_t launch_quant_tiled(const void* in, long long rows, int K, int gu_I, 
   long long grid = (nblocks + 255) / 256;
   if (grid > 65535LL * 8) grid = 65535LL * 8;
   if (grid < 1) grid = 1;
-  k_quant_tiled<<<(unsigned)grid, 256, 0, stream>>>(static_cast<const uint4*>(in), rows, K, gu_I,
-                                                   reinterpret_cast<uint4*>(codes), sf);
-  return cudaGetLastError();
+  return launch_pdl(k_quant_tiled, dim3((unsigned)grid), dim3(256), 0, stream,
+                    static_cast<const uint4*>(in), rows, K, gu_I,
+                    reinterpret_cast<uint4*>(codes), sf);
 }
 
 cudaError_t launch_gather_quant_rows(const void* x, const int32_t* token_of, const int32_t* nrows,
                                      int d, uint8_t* codes, uint8_t* sf, int grid,
                                      cudaStream_t stream) {
-  k_gather_quant_rows<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x), token_of, nrows, d,
-                                               reinterpret_cast<uint4*>(codes), sf);
-  return cudaGetLastError();
+  return launch_pdl(k_gather_quant_rows, dim3(grid), dim3(256), 0, stream,
+                    static_cast<const uint4*>(x), token_of, nrows, d,
+                    reinterpret_cast<uint4*>(codes), sf);
 }
 
 cudaError_t launch_quant_mxfp8(const void* in, long long rows, int K, uint8_t* codes,

@@ -43,6 +43,7 @@ __device__ __forceinline__ bool element_valid(const int32_t* ids, int f, int k, 
 }
 
 __global__ void __launch_bounds__(kChunk) k_route_count(RouteArgs a) {
+  pdl_wait();   // the previous kernel of the stream has completed
   __shared__ int hist[kMaxE];
   for (int i = threadIdx.x; i < a.E; i += blockDim.x) hist[i] = 0;
   __syncthreads();
@@ -59,6 +60,7 @@ __global__ void __launch_bounds__(kChunk) k_route_count(RouteArgs a) {
   }
   __syncthreads();
   for (int i = threadIdx.x; i < a.E; i += blockDim.x) a.blockcounts[blockIdx.x * a.E + i] = hist[i];
+  pdl_trigger();
 }
 
 // Inclusive warp scan with shuffles.
@@ -72,6 +74,7 @@ __device__ __forceinline__ int warp_incl_scan(int v, int lane) {
 }
 
 __global__ void __launch_bounds__(kMaxE) k_route_scan(RouteArgs a) {
+  pdl_wait();   // the previous kernel of the stream has completed
   __shared__ int cnt[kMaxE];
   __shared__ int warp_tot[2][kMaxE / 32];
   const int tid = threadIdx.x;
@@ -175,9 +178,11 @@ __global__ void __launch_bounds__(kMaxE) k_route_scan(RouteArgs a) {
       }
     }
   }
+  pdl_trigger();
 }
 
 __global__ void __launch_bounds__(kChunk) k_route_scatter(RouteArgs a) {
+  pdl_wait();   // the previous kernel of the stream has completed
   __shared__ int wcnt[kChunk / 32][kMaxE];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int E = a.E;
@@ -203,6 +208,7 @@ __global__ void __launch_bounds__(kChunk) k_route_scatter(RouteArgs a) {
   } else if (f < R) {
     a.row_of[f] = -1;
   }
+  pdl_trigger();
 }
 
 // ---------------------------------------------------------------------------
@@ -214,6 +220,7 @@ __global__ void __launch_bounds__(256) k_gather_rows(const uint4* __restrict__ s
                                                      const int32_t* __restrict__ token_of,
                                                      const int32_t* __restrict__ nrows_p, int nvec,
                                                      uint4* __restrict__ dst) {
+  pdl_wait();   // the previous kernel of the stream has completed
   constexpr int U = 8;                     // vectors per lane per row and pass
   const int nrows = *nrows_p;
   const int lane = threadIdx.x & 31;
@@ -251,6 +258,7 @@ __global__ void __launch_bounds__(256) k_gather_rows(const uint4* __restrict__ s
     t0 = n0;
     t1 = n1;
   }
+  pdl_trigger();
 }
 
 __device__ __forceinline__ void acc8(float* acc, const uint4 v) {
@@ -269,6 +277,7 @@ __global__ void __launch_bounds__(256) k_combine(const uint4* __restrict__ rows,
                                                  int nvec, uint4* __restrict__ y,
                                                  const float* __restrict__ pdscore, int n_pd,
                                                  float* __restrict__ dscores) {
+  pdl_wait();   // the previous kernel of the stream has completed
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
@@ -321,6 +330,7 @@ __global__ void __launch_bounds__(256) k_combine(const uint4* __restrict__ rows,
       }
     }
   }
+  pdl_trigger();
 }
 
 // Any k: contributions are loaded and added one j at a time (fixed j order).
@@ -329,6 +339,7 @@ __global__ void __launch_bounds__(256) k_combine_any(const uint4* __restrict__ r
                                                      int k, int nvec, uint4* __restrict__ y,
                                                      const float* __restrict__ pdscore, int n_pd,
                                                      float* __restrict__ dscores) {
+  pdl_wait();   // the previous kernel of the stream has completed
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
@@ -376,22 +387,23 @@ __global__ void __launch_bounds__(256) k_combine_any(const uint4* __restrict__ r
       }
     }
   }
+  pdl_trigger();
 }
 
 }  // namespace
 
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t stream) {
-  k_route_count<<<a.nblk, kChunk, 0, stream>>>(a);
-  k_route_scan<<<1, kMaxE, 0, stream>>>(a);
-  k_route_scatter<<<a.nblk, kChunk, 0, stream>>>(a);
-  return cudaGetLastError();
+  cudaError_t e = launch_pdl(k_route_count, dim3(a.nblk), dim3(kChunk), 0, stream, a);
+  if (e == cudaSuccess) e = launch_pdl(k_route_scan, dim3(1), dim3(kMaxE), 0, stream, a);
+  if (e == cudaSuccess) e = launch_pdl(k_route_scatter, dim3(a.nblk), dim3(kChunk), 0, stream, a);
+  return e;
 }
 
 cudaError_t launch_gather_rows(const void* src, const int32_t* token_of, const int32_t* nrows,
                                int d, void* dst, int grid, cudaStream_t stream) {
-  k_gather_rows<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(src), token_of, nrows, d / 8,
-                                          static_cast<uint4*>(dst));
-  return cudaGetLastError();
+  return launch_pdl(k_gather_rows, dim3(grid), dim3(256), 0, stream,
+                    static_cast<const uint4*>(src), token_of, nrows, d / 8,
+                    static_cast<uint4*>(dst));
 }
 
 cudaError_t launch_combine(const void* rows, const int32_t* row_of, int T, int k, int d, void* y,
@@ -400,12 +412,14 @@ cudaError_t launch_combine(const void* rows, const int32_t* row_of, int T, int k
   const uint4* r4 = static_cast<const uint4*>(rows);
   uint4* y4 = static_cast<uint4*>(y);
   if (k <= 4)
-    k_combine<4><<<grid, 256, 0, stream>>>(r4, row_of, T, k, d / 8, y4, pdscore, n_pd, dscores);
+    return launch_pdl(k_combine<4>, dim3(grid), dim3(256), 0, stream, r4, row_of, T, k, d / 8,
+                      y4, pdscore, n_pd, dscores);
   else if (k <= 8)
-    k_combine<8><<<grid, 256, 0, stream>>>(r4, row_of, T, k, d / 8, y4, pdscore, n_pd, dscores);
+    return launch_pdl(k_combine<8>, dim3(grid), dim3(256), 0, stream, r4, row_of, T, k, d / 8,
+                      y4, pdscore, n_pd, dscores);
   else
-    k_combine_any<<<grid, 256, 0, stream>>>(r4, row_of, T, k, d / 8, y4, pdscore, n_pd, dscores);
-  return cudaGetLastError();
+    return launch_pdl(k_combine_any, dim3(grid), dim3(256), 0, stream, r4, row_of, T, k, d / 8,
+                      y4, pdscore, n_pd, dscores);
 }
 
 }  // namespace moe
