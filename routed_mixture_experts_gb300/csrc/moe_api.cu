@@ -376,9 +376,8 @@ int forward_mxfp8(moe_plan* p, const void* x, const uint8_t* w13_sf, const uint8
     g.out1 = p->a; g.ld1 = 2LL * p->I;
     g.save = save ? 1 : 0;
     g.stall_mma = p->dbg_stall_w13;
-    e = launch_gemm(EPI_SWIGLU, 128, false, false, p->tm_xq, p->tm_w13q, p->tm_xq, p->tm_ys,
-                    p->tm_ys, g, p->num_sms,
-                    st, true);
+    e = launch_gemm(EPI_SWIGLU, 128, false, false, p->tm_xq, p->tm_w13q, p->tm_xq, p->tm_h,
+                    save ? p->tm_a : p->tm_h, g, p->num_sms, st, true);
     if (e != cudaSuccess) return cuda_status(e);
     p->launches += 1;
     mark(p, 0, 3, st);
@@ -538,7 +537,11 @@ int moe_plan_set_workspace(moe_plan* p, void* ws, size_t bytes, int flags) {
   if (p->precision == MOE_PREC_MXFP8) {
     if (encode_tmap_u8(&p->tm_xq, p->xq, RP, p->d, 128) ||
         encode_tmap_u8(&p->tm_hq, p->hq, RP, p->I, 128) ||
-        encode_tmap_bf16(&p->tm_ys, p->ys, RP, p->d, 128))
+        encode_tmap_bf16(&p->tm_ys, p->ys, RP, p->d, 128) ||
+        encode_tmap_bf16(&p->tm_h, p->h, RP, p->I, 128))
+      return MOE_ERR_CUDA;
+    if ((flags & MOE_WS_TRAINING) &&
+        encode_tmap_bf16(&p->tm_a, p->a, RP, 2LL * p->I, 128))
       return MOE_ERR_CUDA;
     if ((flags & MOE_WS_TRAINING) &&
         (encode_tmap_u8(&p->tm_dyq, p->dyq, RP, p->d, 128) ||

@@ -47,7 +47,7 @@ struct GemmShape {
       (EPI == EPI_WGRAD ? kWgradBufs
                         : (EPI == EPI_SCORE || EPI == EPI_STORE
                                ? kEpiStageBufs
-                               : (MX && EPI == EPI_SWIGLU ? 0 : tri_bufs<EPI>()))) * 16384;
+                               : tri_bufs<EPI>())) * 16384;
   static constexpr int STAGE_BUDGET = 226 * 1024 - OUT_BYTES;
   static constexpr int STAGES = STAGE_BUDGET / STAGE_BYTES > 8 ? 8 : STAGE_BUDGET / STAGE_BYTES;
   static constexpr int BAR_BYTES = 256;
@@ -310,18 +310,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) w = mbar_wait(tfull_bar(acc), acc_phase, &abort_s, args.err, 5, wlim);
       // all eight epilogue warps leave together, so their named barriers stay matched
       const int ok_warp = __shfl_sync(0xffffffffu, w, 0);
-      // epilogues that share named barriers leave together; the others per warp
-      if (!(MX && EPI == EPI_SWIGLU)) {
-        if (epi_bar_and(ok_warp) == 0) break;
-      } else if (ok_warp == 0) {
-        break;
-      }
+      if (epi_bar_and(ok_warp) == 0) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
       if constexpr (EPI == EPI_WGRAD) {
         if (!epilogue_wgrad<BN>(args, &tmC, ti, row, tbase, et, half, wp, &abort_s, wlim)) break;
       } else if constexpr (MX && EPI == EPI_SWIGLU)
-        epilogue_swiglu_mx<BN>(args, ti, row, tbase, half);
+        epilogue_swiglu_mx<BN>(args, ti, row, tbase, half, &tmO0, &tmO1,
+                               stage0 + STAGES * S::STAGE_BYTES, et, sub);
       else
         epilogue<BN, EPI>(args, ti, row, tbase, half, &tmO0, &tmO1,
                           stage0 + STAGES * S::STAGE_BYTES, et, sub);

@@ -127,68 +127,6 @@ __device__ __forceinline__ void pack32(const float (&v)[32], uint32_t (&pk)[16])
   for (int i = 0; i < 16; ++i) pk[i] = pack_bf2(v[2 * i], v[2 * i + 1]);
 }
 
-// MXFP8 W13 epilogue: like the bf16 one (R1, SwiGLU, R2), then h is quantised
-// along I in 32-column blocks (codes to a.hq, tiled E8M0 scales to a.hsf) as the
-// A operand of the block-scaled W2 GEMM; the bf16 h is kept (the backward's
-// operand), and with a.save so is a (a.out1, [rows, 2I]).
-template <int BN>
-__device__ __forceinline__ void epilogue_swiglu_mx(const GemmArgs& a, const TileInfo& ti, int row,
-                                                   uint32_t tbase, int half) {
-  constexpr int BNH = BN / 2;
-  constexpr int W = BNH / 2;             // columns of this thread's half
-  const long long grow = (long long)ti.m0 + row;
-  const int c0 = ti.nt * BNH;
-  uint16_t* h = static_cast<uint16_t*>(a.out0) + grow * a.ld0 + c0;
-  uint8_t* hq = a.hq + grow * a.ld0 + c0;
-  uint32_t g0[16], g1[16], u0[16], u1[16];
-#pragma unroll 1
-  for (int c = half * W; c < (half + 1) * W; c += 32) {
-    tmem_ld16(tbase + c, g0);
-    tmem_ld16(tbase + c + 16, g1);
-    tmem_ld16(tbase + BNH + c, u0);
-    tmem_ld16(tbase + BNH + c + 16, u1);
-    tmem_ld_wait();
-    float hv[32], gv[32], uv[32];
-#pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      gv[q] = bf2f(f2bf(__uint_as_float(g0[q])));                  // R1
-      uv[q] = bf2f(f2bf(__uint_as_float(u0[q])));
-      gv[16 + q] = bf2f(f2bf(__uint_as_float(g1[q])));
-      uv[16 + q] = bf2f(f2bf(__uint_as_float(u1[q])));
-      hv[q] = bf2f(f2bf(swiglu_fwd(gv[q], uv[q], a.clamp)));       // R2
-      hv[16 + q] = bf2f(f2bf(swiglu_fwd(gv[16 + q], uv[16 + q], a.clamp)));
-    }
-    if (a.save) {
-      // training: keep the gate/up pre-activations a for the backward
-      uint16_t* arow = static_cast<uint16_t*>(a.out1) + grow * a.ld1 + c0 + c;
-      uint32_t pk[16];
-      pack32(gv, pk);
-      reinterpret_cast<uint4*>(arow)[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      reinterpret_cast<uint4*>(arow)[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-      reinterpret_cast<uint4*>(arow)[2] = make_uint4(pk[8], pk[9], pk[10], pk[11]);
-      reinterpret_cast<uint4*>(arow)[3] = make_uint4(pk[12], pk[13], pk[14], pk[15]);
-      pack32(uv, pk);
-      arow += a.I;
-      reinterpret_cast<uint4*>(arow)[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      reinterpret_cast<uint4*>(arow)[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-      reinterpret_cast<uint4*>(arow)[2] = make_uint4(pk[8], pk[9], pk[10], pk[11]);
-      reinterpret_cast<uint4*>(arow)[3] = make_uint4(pk[12], pk[13], pk[14], pk[15]);
-    }
-    float lo[16], hi[16];
-#pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      lo[q] = hv[q];
-      hi[q] = hv[16 + q];
-    }
-    store16_bf16(h + c, lo);
-    store16_bf16(h + c + 16, hi);
-    uint32_t w[8];
-    const uint8_t sc = mx_quant32(hv, w);
-    reinterpret_cast<uint4*>(hq + c)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    reinterpret_cast<uint4*>(hq + c)[1] = make_uint4(w[4], w[5], w[6], w[7]);
-    a.hsf[mx_sf_offset(grow >> 7, (int)(grow & 127), (c0 + c) >> 5, a.hsf_ngr)] = sc;
-  }
-}
 
 // Staging of bf16 outputs: the epilogue threads write one 128-row x 64-column
 // sub-tile (16 KB) into a shared-memory buffer in the 128-byte-swizzled layout of
@@ -289,6 +227,57 @@ __device__ __forceinline__ void load32_bf16(const uint16_t* src, float (&v)[32])
   for (int q = 0; q < 16; ++q) {
     v[q] = a[q];
     v[16 + q] = b[q];
+  }
+}
+
+// MXFP8 W13 epilogue: like the bf16 one (R1, SwiGLU, R2), then h is quantised
+// along I in 32-column blocks (codes to a.hq, tiled E8M0 scales to a.hsf) as the
+// A operand of the block-scaled W2 GEMM.  The bf16 h (the backward's operand)
+// and, with a.save, a (gate and up) leave through shared-memory staging and TMA
+// stores like the bf16 epilogue's (tmO0: h, tmO1: a); the codes are stored
+// directly (32 contiguous bytes per thread).
+template <int BN>
+__device__ __forceinline__ void epilogue_swiglu_mx(const GemmArgs& a, const TileInfo& ti, int row,
+                                                   uint32_t tbase, int half,
+                                                   const CUtensorMap* tmO0,
+                                                   const CUtensorMap* tmO1, uint32_t out0, int et,
+                                                   int& seq) {
+  constexpr int BNH = BN / 2;
+  static_assert(BNH == 64, "one 64-column chunk of h per tile");
+  const long long grow = (long long)ti.m0 + row;
+  const int c0 = ti.nt * BNH;
+  const int ch = 32 * half;             // this thread's 32 columns of the chunk
+  uint32_t g0[16], g1[16], u0[16], u1[16];
+  tmem_ld16(tbase + ch, g0);
+  tmem_ld16(tbase + ch + 16, g1);
+  tmem_ld16(tbase + BNH + ch, u0);
+  tmem_ld16(tbase + BNH + ch + 16, u1);
+  tmem_ld_wait();
+  float hv[32], gv[32], uv[32];
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    gv[q] = bf2f(f2bf(__uint_as_float(g0[q])));                  // R1
+    uv[q] = bf2f(f2bf(__uint_as_float(u0[q])));
+    gv[16 + q] = bf2f(f2bf(__uint_as_float(g1[q])));
+    uv[16 + q] = bf2f(f2bf(__uint_as_float(u1[q])));
+  }
+#pragma unroll
+  for (int q = 0; q < 32; ++q) hv[q] = bf2f(f2bf(swiglu_fwd(gv[q], uv[q], a.clamp)));   // R2
+  uint32_t w[8];
+  const uint8_t sc = mx_quant32(hv, w);
+  uint8_t* hq = a.hq + grow * a.ld0 + c0 + ch;
+  reinterpret_cast<uint4*>(hq)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  reinterpret_cast<uint4*>(hq)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  a.hsf[mx_sf_offset(grow >> 7, (int)(grow & 127), (c0 + ch) >> 5, a.hsf_ngr)] = sc;
+  if (a.save) {
+    uint32_t pk[3][16];
+    pack32(hv, pk[0]);
+    pack32(gv, pk[1]);
+    pack32(uv, pk[2]);
+    epi_stage_three<tri_bufs<EPI_SWIGLU>()>(tmO0, tmO1, tmO1, out0, et, row, half, pk, c0, c0,
+                                            a.I + c0, ti.m0);
+  } else {
+    epi_stage_store(tmO0, out0, seq, et, row, half, hv, c0, ti.m0);
   }
 }
 
