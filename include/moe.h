@@ -120,8 +120,9 @@ int moe_plan_set_workspace(moe_plan* plan, void* workspace, size_t bytes, int fl
  *   moe_prepare_weights_mxfp8; for bf16 pass NULL.  An MXFP8 plan quantises
  *   the routed activation rows along d and h along I (32-element blocks) and
  *   runs block-scaled E4M3 GEMMs; it needs I % 128 == 0, d <= 4096, I <= 4096.
- *   With save_for_backward = 1 it also keeps a, h and the routed x rows
- *   quantised along the rows for moe_backward_mxfp8.
+ *   With save_for_backward = 1 it also keeps a and the routed x rows
+ *   quantised along the rows for moe_backward_mxfp8 (h is kept as its E4M3
+ *   codes only; the backward recomputes the bf16 h from a).
  * Output: y [T, d] bf16, overwritten:
  *   y[t] = bf16( sum_{j=0..k-1} bf16( scores[t,j] * W2[e] . h ) ),
  *   h = bf16(silu(G) * U),  (G, U) = bf16(W13[e] . x[t]),  e = ids[t,j]
@@ -256,13 +257,15 @@ const char* moe_status_string(int status);
  *   MOE_BUF_SCORE_OF  fp32  [Rpad]   score of each padded row (0: padding)
  *   MOE_BUF_XE        bf16  [Rpad,d] gathered activations
  *   MOE_BUF_A         bf16  [Rpad,2I] gate/up pre-activations (training)
- *   MOE_BUF_H         bf16  [Rpad,I] SwiGLU output
+ *   MOE_BUF_H         bf16  [Rpad,I] SwiGLU output (bf16 plans; MXFP8 plans keep
+ *                                    only its E4M3 codes, MOE_BUF_HQ)
  *   MOE_BUF_YS        bf16  [Rpad,d] score-weighted expert outputs
  *   MOE_BUF_DYE       bf16  [Rpad,d] gathered upstream gradient
  *   MOE_BUF_DA        bf16  [Rpad,2I] gradient at gate/up
  *   MOE_BUF_HS        bf16  [Rpad,I] score * h (WGRAD-W2 operand)
  *   MOE_BUF_DXE       bf16  [Rpad,d] per-row input gradients
- * Rows are valid up to off_pad[E].  Sizes are the worst-case capacities.
+ * Rows are valid up to off_pad[E].  Sizes are the worst-case capacities.  A
+ * tensor the plan does not hold returns MOE_ERR_WORKSPACE.
  * off_pad rounds each expert's segment up to moe_plan_row_granule(plan) rows.
  */
 #define MOE_BUF_M_INDPTR 0

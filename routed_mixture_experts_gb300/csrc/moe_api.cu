@@ -33,6 +33,7 @@ struct moe_plan {
   int RP;       // worst-case padded rows
   int nblk;     // dispatch chunks
   int bn13, bn2, bnd2, bnw2, bnw13;
+  int bnmx_d;   // MXFP8 GEMMs whose N is d (W2, DGRAD-W13): 256-wide tiles when d allows
   int pair;     // W13, W2 and DGRAD-W13 on CTA pairs (256-row tiles over pairs of an
                 // expert's 128-row m tiles; an odd last m tile runs on one CTA)
   int gran;     // padding granule of expert segments (128)
@@ -181,6 +182,25 @@ int encode_tmap_gate_up(CUtensorMap* map, bool fp8, const void* base, long long 
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// MXFP8 W13 [E, 2I, cols] (E4M3) viewed as (cols, 64, 2, I/64, E): one box takes
+// two consecutive 64-row blocks of intermediate columns, each block its 64 gate
+// rows followed by the same 64 up rows, which is the row order of the tiled
+// scales of W13 (blocks of 64 gate + 64 up rows).
+int encode_tmap_gate_up_blocks(CUtensorMap* map, const void* base, long long E, long long I,
+                               long long cols) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = tmap_detail::encode_fn();
+  if (!fn) return MOE_ERR_CUDA;
+  const cuuint64_t dims[5] = {(cuuint64_t)cols, 64, 2, (cuuint64_t)(I / 64), (cuuint64_t)E};
+  const cuuint64_t strides[4] = {(cuuint64_t)cols, (cuuint64_t)(I * cols),
+                                 (cuuint64_t)(64 * cols), (cuuint64_t)(2 * I * cols)};
+  const cuuint32_t box[5] = {128, 64, 2, 2, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
 }  // namespace moe
 
 namespace {
@@ -228,7 +248,8 @@ size_t layout(moe_plan* p, char* base, int flags) {
     p->hq = reinterpret_cast<uint8_t*>(take(RP * I));
     p->hsf = reinterpret_cast<uint8_t*>(take((size_t)mx_sf_bytes(RP, (int)I)));
   }
-  p->h = reinterpret_cast<uint16_t*>(take(2 * RP * I));
+  // bf16 h: the W2 operand of bf16 plans (MXFP8 plans keep only its E4M3 codes)
+  p->h = mx ? nullptr : reinterpret_cast<uint16_t*>(take(2 * RP * I));
   p->ys = reinterpret_cast<uint16_t*>(take(2 * RP * d));
   p->a = p->dye = p->dA = p->hs = p->dxe = nullptr;
   p->pdscore = nullptr;
@@ -365,19 +386,21 @@ int forward_mxfp8(moe_plan* p, const void* x, const uint8_t* w13_sf, const uint8
   p->launches += 1;
   mark(p, 0, 2, st);
   {
+    // 256-wide tiles: 128 intermediate columns (two 64-row blocks of gate and up
+    // rows) per tile; outputs hq/hsf, and a when saving
     GemmArgs g = rows_args(p);
     g.k_blocks = p->d / 128;
     g.b_expert_rows = 2 * p->I;
     g.b_half_rows = p->I;
-    g.n_tiles = p->I / 64;
-    g.out0 = p->h; g.ld0 = p->I;
+    g.n_tiles = p->I / 128;
+    g.ld0 = p->I;                        // row stride of hq
     g.sfa = p->xsf; g.sfb = w13_sf; g.sf_ngr = p->ngr_d; g.b_blocks_per_expert = p->I / 64;
     g.hq = p->hq; g.hsf = p->hsf; g.hsf_ngr = p->ngr_I;
-    g.out1 = p->a; g.ld1 = 2LL * p->I;
     g.save = save ? 1 : 0;
     g.stall_mma = p->dbg_stall_w13;
-    e = launch_gemm(EPI_SWIGLU, 128, false, false, p->tm_xq, p->tm_w13q, p->tm_xq, p->tm_h,
-                    save ? p->tm_a : p->tm_h, g, p->num_sms, st, true);
+    const CUtensorMap& to = save ? p->tm_a : p->tm_ys;   // tm_ys: not written here
+    e = launch_gemm(EPI_SWIGLU, 256, false, false, p->tm_xq, p->tm_w13q, p->tm_xq, to, to, g,
+                    p->num_sms, st, true);
     if (e != cudaSuccess) return cuda_status(e);
     p->launches += 1;
     mark(p, 0, 3, st);
@@ -386,13 +409,12 @@ int forward_mxfp8(moe_plan* p, const void* x, const uint8_t* w13_sf, const uint8
     GemmArgs g = rows_args(p);
     g.k_blocks = p->I / 128;
     g.b_expert_rows = p->d;
-    g.n_tiles = p->d / 128;
+    g.n_tiles = p->d / p->bnmx_d;
     g.out0 = p->ys; g.ld0 = p->d;
     g.row_scale = p->score_of;
     g.sfa = p->hsf; g.sfb = w2_sf; g.sf_ngr = p->ngr_I; g.b_blocks_per_expert = p->d / 128;
-    e = launch_gemm(EPI_SCORE, 128, false, false, p->tm_hq, p->tm_w2q, p->tm_hq, p->tm_ys,
-                    p->tm_ys, g, p->num_sms,
-                    st, true);
+    e = launch_gemm(EPI_SCORE, p->bnmx_d, false, false, p->tm_hq, p->tm_w2q, p->tm_hq, p->tm_ys,
+                    p->tm_ys, g, p->num_sms, st, true);
     if (e != cudaSuccess) return cuda_status(e);
     p->launches += 1;
     mark(p, 0, 4, st);
@@ -459,7 +481,8 @@ moe_plan* moe_plan_create(int T, int d, int I, int E, int k, int precision) {
   p->nblk = (p->R + 1023) / 1024;
   p->bn13 = I % 128 == 0 ? 256 : 128;
   p->bn2 = pick_bn_n(d) == 64 ? 128 : pick_bn_n(d);
-  p->bnd2 = precision == MOE_PREC_MXFP8 ? 128 : pick_bn_n(I);   // block-scaled tiles are 128 wide
+  p->bnd2 = precision == MOE_PREC_MXFP8 ? 128 : pick_bn_n(I);   // block-scaled DGRAD-W2: 128 wide
+  p->bnmx_d = d % 256 == 0 ? 256 : 128;
   p->bnw2 = pick_bn_n(I);
   p->bnw13 = p->bn2;
   p->ngr_d = d / 128;
@@ -537,8 +560,7 @@ int moe_plan_set_workspace(moe_plan* p, void* ws, size_t bytes, int flags) {
   if (p->precision == MOE_PREC_MXFP8) {
     if (encode_tmap_u8(&p->tm_xq, p->xq, RP, p->d, 128) ||
         encode_tmap_u8(&p->tm_hq, p->hq, RP, p->I, 128) ||
-        encode_tmap_bf16(&p->tm_ys, p->ys, RP, p->d, 128) ||
-        encode_tmap_bf16(&p->tm_h, p->h, RP, p->I, 128))
+        encode_tmap_bf16(&p->tm_ys, p->ys, RP, p->d, 128))
       return MOE_ERR_CUDA;
     if ((flags & MOE_WS_TRAINING) &&
         encode_tmap_bf16(&p->tm_a, p->a, RP, 2LL * p->I, 128))
@@ -589,11 +611,12 @@ int moe_forward(moe_plan* p, const void* x, const int32_t* ids, const float* sco
   cudaStream_t st = static_cast<cudaStream_t>(stream_v);
   if (mx) {
     if (w13 != p->w13q_cached) {
-      if (encode_tmap_gate_up(&p->tm_w13q, true, w13, p->E, p->I, p->d, 64)) return MOE_ERR_CUDA;
+      if (encode_tmap_gate_up_blocks(&p->tm_w13q, w13, p->E, p->I, p->d)) return MOE_ERR_CUDA;
       p->w13q_cached = w13;
     }
     if (w2 != p->w2q_cached) {
-      if (encode_tmap_u8(&p->tm_w2q, w2, (long long)p->E * p->d, p->I, 128)) return MOE_ERR_CUDA;
+      if (encode_tmap_u8(&p->tm_w2q, w2, (long long)p->E * p->d, p->I, p->bnmx_d))
+        return MOE_ERR_CUDA;
       p->w2q_cached = w2;
     }
   } else if (refresh_weight_maps(p, w13, w2) != MOE_OK) {
@@ -821,7 +844,7 @@ int moe_backward_mxfp8(moe_plan* p, const void* dy, const uint8_t* w13t, const u
   const int I = p->I, d = p->d, E = p->E;
   const long long RP = p->RP;
   if (w13t != p->w13t_cached) {
-    if (encode_tmap_u8(&p->tm_w13t, w13t, (long long)E * d, 2 * I, 128)) return MOE_ERR_CUDA;
+    if (encode_tmap_u8(&p->tm_w13t, w13t, (long long)E * d, 2 * I, p->bnmx_d)) return MOE_ERR_CUDA;
     p->w13t_cached = w13t;
   }
   if (w2t != p->w2t_cached) {
@@ -874,11 +897,11 @@ int moe_backward_mxfp8(moe_plan* p, const void* dy, const uint8_t* w13t, const u
     GemmArgs g = rows_args(p);
     g.k_blocks = 2 * I / 128;
     g.b_expert_rows = d;
-    g.n_tiles = d / 128;
+    g.n_tiles = d / p->bnmx_d;
     g.out0 = p->dxe; g.ld0 = d;
     g.sfa = p->dAsf; g.sfb = w13t_sf; g.sf_ngr = 2 * I / 128; g.b_blocks_per_expert = d / 128;
-    e = launch_gemm(EPI_STORE, 128, false, false, p->tm_dAq, p->tm_w13t, p->tm_dAq, p->tm_dxe,
-                    p->tm_dxe, g, p->num_sms, st, true);
+    e = launch_gemm(EPI_STORE, p->bnmx_d, false, false, p->tm_dAq, p->tm_w13t, p->tm_dAq,
+                    p->tm_dxe, p->tm_dxe, g, p->num_sms, st, true);
     if (e != cudaSuccess) return cuda_status(e);
     p->launches += 1;
     mark(p, 1, 3, st);

@@ -153,6 +153,18 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int 
       : "memory");
 }
 
+// 5-D tiled load (the block-ordered view of MXFP8 W13: K, rows of a 64-row block,
+// gate/up, block, expert).
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const void* tmap, int x0, int x1, int x2,
+                                            int x3, int x4, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x0), "r"(x1), "r"(x2), "r"(x3), "r"(x4),
+      "r"(bar)
+      : "memory");
+}
+
 // Element-wise add of a shared-memory tile into global memory, performed by the
 // TMA unit (read-modify-write in L2), tracked by the issuing thread's bulk group.
 __device__ __forceinline__ void tma_reduce_add_2d(const void* tmap, uint32_t src, int x, int y) {

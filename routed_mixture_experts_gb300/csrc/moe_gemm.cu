@@ -35,28 +35,37 @@ template <int BN, int EPI, bool MX>
 struct GemmShape {
   // A stage holds 128 rows (A) and BN rows (B) of 128 bytes of K: 64 bf16 or
   // 128 E4M3 elements; MXFP8 stages also carry the 512-byte scale chunks of A
-  // and of B for those 128 K-elements (padded to keep stages 1024-aligned).
+  // (one) and of B (one per 128 rows) for those 128 K-elements, padded to keep
+  // stages 1024-aligned.
   static constexpr int A_BYTES = kBM * 128;                    // 16 KB
   static constexpr int B_BYTES = BN * 128;
-  static constexpr int SF_STAGE_BYTES = MX ? 1024 : 0;
+  static constexpr int SF_LOAD_BYTES = MX ? 512 * (1 + BN / 128) : 0;
+  static constexpr int SF_STAGE_BYTES = (SF_LOAD_BYTES + 1023) / 1024 * 1024;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SF_STAGE_BYTES;
+  static constexpr int TX_BYTES = A_BYTES + B_BYTES + SF_LOAD_BYTES;   // bytes a stage receives
   // Output staging: WGRAD's fp32 buffers (it needs few stages: its K loop is one
   // expert's rows and it is bound by the gradient traffic), else two bf16
   // sub-tile buffers for the TMA-store epilogues.
   static constexpr int OUT_BYTES =
       (EPI == EPI_WGRAD ? kWgradBufs
-                        : (EPI == EPI_SCORE || EPI == EPI_STORE
-                               ? kEpiStageBufs
-                               : tri_bufs<EPI>())) * 16384;
+                        : (MX && BN == 256 ? kMxWideBufs
+                                           : (EPI == EPI_SCORE || EPI == EPI_STORE
+                                                  ? kEpiStageBufs
+                                                  : tri_bufs<EPI>()))) * 16384;
   static constexpr int STAGE_BUDGET = 226 * 1024 - OUT_BYTES;
   static constexpr int STAGES = STAGE_BUDGET / STAGE_BYTES > 8 ? 8 : STAGE_BUDGET / STAGE_BYTES;
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + OUT_BYTES + BAR_BYTES + 1024;
-  // accumulators (2 x BN columns), then for MXFP8 eight scale columns per stage
-  // (4 for A, 4 for B)
-  static constexpr uint32_t SF_COL0 = 2 * BN;
+  // TMEM: the accumulators, then (MXFP8) SF_COLS scale columns per stage, A's
+  // at +0 and B's at +SF_COLS/2 (four per 128 rows).  Two BN-column accumulators
+  // alternate, except for 256-wide MXFP8 tiles, whose scale columns leave room
+  // for one: their epilogue releases it as soon as it has read it.
+  static constexpr int NACC = (MX && BN == 256) ? 1 : 2;
+  static constexpr uint32_t SF_COL0 = NACC * BN;
+  static constexpr uint32_t SF_COLS = MX ? (BN == 256 ? 16 : 8) : 0;
   static constexpr uint32_t TMEM_COLS = MX ? 512 : 2 * BN;
-  static_assert(!MX || SF_COL0 + 8 * STAGES <= 512, "TMEM budget");
+  static_assert(!MX || SF_COL0 + SF_COLS * STAGES <= 512, "TMEM budget");
+  static_assert(STAGES >= 3, "operand ring");
 };
 
 template <int BN, bool A_MN, bool B_MN, int EPI, bool MX>
@@ -68,7 +77,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int STAGES = S::STAGES;
   constexpr uint32_t IDESC = MX ? idesc_mxf8(kBM, BN) : idesc_bf16(kBM, BN, A_MN, B_MN);
   constexpr int KE = MX ? 128 : kBK;     // K elements per stage (128 bytes per row)
-  static_assert(!MX || (!A_MN && !B_MN && BN == 128), "MXFP8: K-major operands, BN = 128");
+  static_assert(!MX || (!A_MN && !B_MN && (BN == 128 || BN == 256)),
+                "MXFP8: K-major operands, BN = 128 or 256");
   static_assert(S::SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
   pdl_wait();   // the previous kernel of the stream has completed
@@ -153,19 +163,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t fb = full_bar(stage);
           const uint32_t sa = stage0 + stage * S::STAGE_BYTES;
           const uint32_t sb = sa + S::A_BYTES;
-          mbar_arrive_expect_tx(fb, S::STAGE_BYTES);
+          mbar_arrive_expect_tx(fb, S::TX_BYTES);
           if constexpr (MX) {
-            // the 512-byte scale chunks of this K group: A's row block, B's row block
+            // the 512-byte scale chunks of this K group: A's row block, then B's
+            // BN/128 row blocks
             const uint32_t ssf = sb + S::B_BYTES;
-            // row GEMMs: K groups from 0, B row block of (expert, n tile); wgrad
-            // mode: K groups from the expert's first row, B row block n0/128
+            // row GEMMs: K groups from 0, B row blocks of (expert, n tile); wgrad
+            // mode: K groups from the expert's first row, B row blocks from n0/128
             const long long kg = (long long)(ti.krow0 >> 7) + kb;
             const long long ga = ((long long)(ti.m0 >> 7) * args.sf_ngr + kg) * 512;
-            const long long gbr = args.wgrad ? (long long)(ti.n0 >> 7)
-                                             : (long long)ti.e * args.b_blocks_per_expert + ti.nt;
-            const long long gb = (gbr * args.sf_ngr + kg) * 512;
+            const long long gbr =
+                args.wgrad ? (long long)(ti.n0 >> 7)
+                           : (long long)ti.e * args.b_blocks_per_expert + (long long)ti.nt * (BN / 128);
             bulk_g2s(ssf, args.sfa + ga, 512u, fb);
-            bulk_g2s(ssf + 512u, args.sfb + gb, 512u, fb);
+#pragma unroll
+            for (int rb = 0; rb < BN / 128; ++rb)
+              bulk_g2s(ssf + 512u * (uint32_t)(1 + rb),
+                       args.sfb + ((gbr + rb) * args.sf_ngr + kg) * 512, 512u, fb);
           }
           // One TMA per operand tile (large boxes: the TMA cost is per box).
           // A: 128 rows x 128 bytes of K.  K-major: a 128-row box of [rows, K];
@@ -183,6 +197,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else if (B_MN) {
             // [E*K, N]: BN/64 atoms of expert e's K rows
             tma_load_3d(sb, &tmB, 0, ti.e * args.b_expert_rows + kb * kBK, ti.n0 >> 6, fb);
+          } else if (EPI == EPI_SWIGLU && MX && BN == 256) {
+            // (K, 64, 2, I/64, E) view of W13: two 64-row blocks, each its gate
+            // rows then the same up rows (the row order of the scale chunks)
+            tma_load_5d(sb, &tmB, kb * KE, 0, 0, 2 * ti.nt, ti.e, fb);
           } else if (EPI == EPI_SWIGLU) {
             // (K, I, 2E) view of W13: this tile's BN/2 gate rows, then the same up
             // rows, in one box
@@ -245,14 +263,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sa = stage0 + stage * S::STAGE_BYTES;
           const uint32_t sb = sa + S::A_BYTES;
           if constexpr (MX) {
-            // this stage's scales -> its own 8 TMEM columns (reused only after the
+            // this stage's scales -> its own TMEM columns (reused only after the
             // stage is released, i.e. after these MMAs have completed); then four
             // 32-element K steps, step j reading scale byte j
             const uint32_t ssf = sb + S::B_BYTES;
-            const uint32_t sfa_t = tmem_base + S::SF_COL0 + 8u * (uint32_t)stage;
-            const uint32_t sfb_t = sfa_t + 4u;
+            const uint32_t sfa_t = tmem_base + S::SF_COL0 + S::SF_COLS * (uint32_t)stage;
+            const uint32_t sfb_t = sfa_t + S::SF_COLS / 2;
             tmem_cp_32x128b_x4(sfa_t, smem_desc_noswz(ssf, 512u, 128u));
-            tmem_cp_32x128b_x4(sfb_t, smem_desc_noswz(ssf + 512u, 512u, 128u));
+#pragma unroll
+            for (int rb = 0; rb < BN / 128; ++rb)
+              tmem_cp_32x128b_x4(sfb_t + 4u * (uint32_t)rb,
+                                 smem_desc_noswz(ssf + 512u * (uint32_t)(1 + rb), 512u, 128u));
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const uint64_t adesc = smem_desc_sw128(sa + j * 32, 16, 1024);
@@ -284,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       if (lane == 0) umma_commit(tfull_bar(acc));
       __syncwarp();
-      acc ^= 1;
+      if (S::NACC == 2) acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
     if (abort_s && lane == 0) {
@@ -313,14 +334,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (epi_bar_and(ok_warp) == 0) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
-      if constexpr (EPI == EPI_WGRAD) {
+      if constexpr (S::NACC == 1) {
+        // one accumulator: read it, release it, then compute the outputs
+        epilogue_mx_wide<EPI>(args, ti, row, tbase, half, &tmO0, &tmO1,
+                              stage0 + STAGES * S::STAGE_BYTES, et, tempty_bar(0));
+        acc_phase ^= 1u;
+        continue;
+      } else if constexpr (EPI == EPI_WGRAD) {
         if (!epilogue_wgrad<BN>(args, &tmC, ti, row, tbase, et, half, wp, &abort_s, wlim)) break;
-      } else if constexpr (MX && EPI == EPI_SWIGLU)
-        epilogue_swiglu_mx<BN>(args, ti, row, tbase, half, &tmO0, &tmO1,
-                               stage0 + STAGES * S::STAGE_BYTES, et, sub);
-      else
+      } else {
         epilogue<BN, EPI>(args, ti, row, tbase, half, &tmO0, &tmO1,
                           stage0 + STAGES * S::STAGE_BYTES, et, sub);
+      }
       tc_fence_before();
       mbar_arrive(tempty_bar(acc));
       acc ^= 1;
@@ -365,10 +390,14 @@ cudaError_t launch_gemm(int epi, int bn, bool a_mn, bool b_mn, const CUtensorMap
                         const CUtensorMap& to1, const GemmArgs& args, int grid,
                         cudaStream_t stream, bool mx) {
   if (mx) {
-    if (epi == EPI_SWIGLU && bn == 128 && !a_mn && !b_mn)
-      return launch_one<128, false, false, EPI_SWIGLU, true>(ta, tb, tc, to0, to1, args, grid, stream);
+    if (epi == EPI_SWIGLU && bn == 256 && !a_mn && !b_mn)
+      return launch_one<256, false, false, EPI_SWIGLU, true>(ta, tb, tc, to0, to1, args, grid, stream);
+    if (epi == EPI_SCORE && bn == 256 && !a_mn && !b_mn)
+      return launch_one<256, false, false, EPI_SCORE, true>(ta, tb, tc, to0, to1, args, grid, stream);
     if (epi == EPI_SCORE && bn == 128 && !a_mn && !b_mn)
       return launch_one<128, false, false, EPI_SCORE, true>(ta, tb, tc, to0, to1, args, grid, stream);
+    if (epi == EPI_STORE && bn == 256 && !a_mn && !b_mn)
+      return launch_one<256, false, false, EPI_STORE, true>(ta, tb, tc, to0, to1, args, grid, stream);
     if (epi == EPI_DGRAD2 && bn == 128 && !a_mn && !b_mn)
       return launch_one<128, false, false, EPI_DGRAD2, true>(ta, tb, tc, to0, to1, args, grid, stream);
     if (epi == EPI_STORE && bn == 128 && !a_mn && !b_mn)

@@ -230,54 +230,121 @@ __device__ __forceinline__ void load32_bf16(const uint16_t* src, float (&v)[32])
   }
 }
 
-// MXFP8 W13 epilogue: like the bf16 one (R1, SwiGLU, R2), then h is quantised
-// along I in 32-column blocks (codes to a.hq, tiled E8M0 scales to a.hsf) as the
-// A operand of the block-scaled W2 GEMM.  The bf16 h (the backward's operand)
-// and, with a.save, a (gate and up) leave through shared-memory staging and TMA
-// stores like the bf16 epilogue's (tmO0: h, tmO1: a); the codes are stored
-// directly (32 contiguous bytes per thread).
-template <int BN>
-__device__ __forceinline__ void epilogue_swiglu_mx(const GemmArgs& a, const TileInfo& ti, int row,
-                                                   uint32_t tbase, int half,
-                                                   const CUtensorMap* tmO0,
-                                                   const CUtensorMap* tmO1, uint32_t out0, int et,
-                                                   int& seq) {
-  constexpr int BNH = BN / 2;
-  static_assert(BNH == 64, "one 64-column chunk of h per tile");
-  const long long grow = (long long)ti.m0 + row;
-  const int c0 = ti.nt * BNH;
-  const int ch = 32 * half;             // this thread's 32 columns of the chunk
-  uint32_t g0[16], g1[16], u0[16], u1[16];
-  tmem_ld16(tbase + ch, g0);
-  tmem_ld16(tbase + ch + 16, g1);
-  tmem_ld16(tbase + BNH + ch, u0);
-  tmem_ld16(tbase + BNH + ch + 16, u1);
-  tmem_ld_wait();
-  float hv[32], gv[32], uv[32];
+// Staging for the 256-wide MXFP8 epilogues: thread (row, half) owns 64
+// consecutive output columns of its row (32 packed bf16 pairs), written in the
+// 128-byte-swizzled layout of a 64 x 128 box and stored with TMA, half 0's at
+// column x0 and half 1's at x1.  With two 16 KB buffers both halves write at
+// once (buffer `half`); with one, half 0's sub-tile goes first.  A buffer is
+// rewritten only once the previous store has read it.  One buffer: the 16 KB it
+// frees give the operand ring a fourth stage, which is worth more (W13 0.272 ->
+// 0.233 ms, W2 0.161 -> 0.137 ms on the E = 128 training shapes).
+constexpr int kMxWideBufs = 1;
+
+__device__ __forceinline__ void epi_stage_wide(const CUtensorMap* tm, uint32_t out0, int et,
+                                               int row, int half, const uint32_t (&pk)[32],
+                                               int x0, int x1, int y) {
+  const uint32_t sw = (uint32_t)(row & 7);
 #pragma unroll
-  for (int q = 0; q < 16; ++q) {
-    gv[q] = bf2f(f2bf(__uint_as_float(g0[q])));                  // R1
-    uv[q] = bf2f(f2bf(__uint_as_float(u0[q])));
-    gv[16 + q] = bf2f(f2bf(__uint_as_float(g1[q])));
-    uv[16 + q] = bf2f(f2bf(__uint_as_float(u1[q])));
+  for (int r = 0; r < 3 - kMxWideBufs; ++r) {
+    if (et == 0) bulk_wait_read<0>();
+    named_bar_sync(1, kEpiThreads);
+    if (kMxWideBufs == 2 || half == r) {
+      const uint32_t rbase = out0 + (uint32_t)(kMxWideBufs == 2 ? half : 0) * 16384u +
+                             (uint32_t)row * 128u;
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        st_shared_v4_u32(rbase + (((uint32_t)q ^ sw) << 4), pk[4 * q], pk[4 * q + 1],
+                         pk[4 * q + 2], pk[4 * q + 3]);
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(1, kEpiThreads);
+    if (et == 0) {
+      if (kMxWideBufs == 2) {
+        tma_store_2d(tm, out0, x0, y);
+        tma_store_2d(tm, out0 + 16384u, x1, y);
+      } else {
+        tma_store_2d(tm, out0, r == 0 ? x0 : x1, y);
+      }
+      bulk_commit();
+    }
   }
+}
+
+// Epilogues of the 256-wide MXFP8 tiles, which have one accumulator: each thread
+// reads its 128 accumulator columns [128*half, 128*half + 128) into registers and
+// releases the accumulator (arrive on `release`, so the next tile's MMAs can
+// start) before it computes and writes its outputs.
+//   W13 + SwiGLU: the B tile's rows are two 64-row blocks, each the gate rows of
+//     64 intermediate columns followed by the same up rows, so the thread holds
+//     the gate (first 64) and up (last 64) values of the intermediate columns
+//     c0 = 128*nt + 64*half ...: R1, SwiGLU, R2, then h is quantised along I in
+//     32-column blocks (codes to a.hq, tiled E8M0 scales to a.hsf) as the A
+//     operand of the block-scaled W2 GEMM; with a.save, a (gate and up, bf16)
+//     leaves through shared-memory staging and TMA stores (tmO1).
+//   W2 x score (R3) and the plain store (R5): output columns n0 + 128*half ...,
+//     in two 64-column sub-tiles through staging (tmO0).
+template <int EPI>
+__device__ __forceinline__ void epilogue_mx_wide(const GemmArgs& a, const TileInfo& ti, int row,
+                                                 uint32_t tbase, int half,
+                                                 const CUtensorMap* tmO0,
+                                                 const CUtensorMap* tmO1, uint32_t out0, int et,
+                                                 uint32_t release) {
+  uint32_t v[8][16];
 #pragma unroll
-  for (int q = 0; q < 32; ++q) hv[q] = bf2f(f2bf(swiglu_fwd(gv[q], uv[q], a.clamp)));   // R2
-  uint32_t w[8];
-  const uint8_t sc = mx_quant32(hv, w);
-  uint8_t* hq = a.hq + grow * a.ld0 + c0 + ch;
-  reinterpret_cast<uint4*>(hq)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-  reinterpret_cast<uint4*>(hq)[1] = make_uint4(w[4], w[5], w[6], w[7]);
-  a.hsf[mx_sf_offset(grow >> 7, (int)(grow & 127), (c0 + ch) >> 5, a.hsf_ngr)] = sc;
-  if (a.save) {
-    uint32_t pk[3][16];
-    pack32(hv, pk[0]);
-    pack32(gv, pk[1]);
-    pack32(uv, pk[2]);
-    epi_stage_three<tri_bufs<EPI_SWIGLU>()>(tmO0, tmO1, tmO1, out0, et, row, half, pk, c0, c0,
-                                            a.I + c0, ti.m0);
+  for (int i = 0; i < 8; ++i) tmem_ld16(tbase + 128 * half + 16 * i, v[i]);
+  tmem_ld_wait();
+  tc_fence_before();
+  mbar_arrive(release);
+  const long long grow = (long long)ti.m0 + row;
+  if constexpr (EPI == EPI_SWIGLU) {
+    const int c0 = ti.nt * 128 + 64 * half;
+    // R1 first: gate and up to bf16 pairs (a's values), which frees the fp32 copies
+    uint32_t pg[32], pu[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int c = 2 * i;
+      pg[i] = pack_bf2(__uint_as_float(v[c >> 4][c & 15]), __uint_as_float(v[c >> 4][(c & 15) + 1]));
+      pu[i] = pack_bf2(__uint_as_float(v[4 + (c >> 4)][c & 15]),
+                       __uint_as_float(v[4 + (c >> 4)][(c & 15) + 1]));
+    }
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      float hv[32];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t g2 = pg[16 * s + i], u2 = pu[16 * s + i];
+        hv[2 * i] = bf2f(f2bf(swiglu_fwd(__uint_as_float(g2 << 16), __uint_as_float(u2 << 16),
+                                         a.clamp)));                                // R2
+        hv[2 * i + 1] = bf2f(f2bf(swiglu_fwd(__uint_as_float(g2 & 0xFFFF0000u),
+                                             __uint_as_float(u2 & 0xFFFF0000u), a.clamp)));
+      }
+      uint32_t w[8];
+      const uint8_t sc = mx_quant32(hv, w);
+      uint8_t* hq = a.hq + grow * a.ld0 + c0 + 32 * s;
+      reinterpret_cast<uint4*>(hq)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      reinterpret_cast<uint4*>(hq)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      a.hsf[mx_sf_offset(grow >> 7, (int)(grow & 127), (c0 + 32 * s) >> 5, a.hsf_ngr)] = sc;
+    }
+    if (a.save) {
+      const int xg = ti.nt * 128;        // buffer 0: half 0's columns, buffer 1: half 1's
+      epi_stage_wide(tmO1, out0, et, row, half, pg, xg, xg + 64, ti.m0);
+      epi_stage_wide(tmO1, out0, et, row, half, pu, a.I + xg, a.I + xg + 64, ti.m0);
+    }
   } else {
-    epi_stage_store(tmO0, out0, seq, et, row, half, hv, c0, ti.m0);
+    static_assert(EPI == EPI_SCORE || EPI == EPI_STORE, "256-wide MXFP8 epilogues");
+    const float s = EPI == EPI_SCORE ? a.row_scale[grow] : 1.0f;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      uint32_t pk[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int c = 64 * j + 2 * i;
+        pk[i] = pack_bf2(s * __uint_as_float(v[c >> 4][c & 15]),            // R3 / R5 on store
+                         s * __uint_as_float(v[(c + 1) >> 4][(c + 1) & 15]));
+      }
+      const int x = ti.n0 + 64 * j;      // buffer 0: half 0's sub-tile, buffer 1: half 1's
+      epi_stage_wide(tmO0, out0, et, row, half, pk, x, x + 128, ti.m0);
+    }
   }
 }
 

@@ -134,6 +134,10 @@ int encode_tmap_u8(CUtensorMap* map, const void* base, long long rows, long long
 // (k, row within the half, 2e)), one 128-byte swizzled K chunk wide
 int encode_tmap_gate_up(CUtensorMap* map, bool fp8, const void* base, long long E, long long I,
                         long long cols, int box_rows);
+// MXFP8 W13 [E, 2I, cols] as (cols, 64, 2, I/64, E): a box of two 64-row blocks,
+// each its gate rows then the same up rows (coordinates (k, 0, 0, block, e))
+int encode_tmap_gate_up_blocks(CUtensorMap* map, const void* base, long long E, long long I,
+                               long long cols);
 
 // Dispatch kernels.
 struct RouteArgs {

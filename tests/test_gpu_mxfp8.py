@@ -45,6 +45,11 @@ def untile(sf, rows, K, gu_I=0):
     return sf[off]
 
 
+def dequant(orc, codes, scales):
+    """E4M3 codes [rows, K] with E8M0 scales [rows, K/32] -> float64 values."""
+    return orc.e4m3_decode(codes) * np.repeat(2.0 ** (scales.astype(np.float64) - 127), 32, axis=1)
+
+
 def prepared(moe, dev):
     w13q, w13s, w2q, w2s = moe.prepare_weights_mxfp8(dev["w13"], dev["w2"])
     torch.cuda.synchronize()
@@ -98,10 +103,20 @@ def test_mxfp8_small(moe, orc, sizes):
                                    clamp=c.get("clamp", 0.0), return_h=True)
     compare(f32(bits(y)), f32(yref), bf16_out=True, rel_fro=REL_FRO_MXFP8, what="y mxfp8",
             max_bad_frac=1.0)
+    # h quantised along I (the W2 GEMM's A operand): the dequantised codes against
+    # the oracle's h quantised by the oracle; a code may differ by one step where
+    # the two h values differ in their last bf16 bit
     ro = plan.buffer("row_of", torch.int32).cpu().numpy()[: T * k].reshape(T, k)
-    h = bits(plan.buffer("h", torch.bfloat16).view(-1, I))
     ok = ro >= 0
-    compare(f32(h[ro[ok]]), f32(href[ok]), what="h mxfp8", max_bad_frac=1e-3)
+    rows = ro[ok]
+    hq_all = plan.buffer("hq", torch.uint8).cpu().numpy()
+    RP = hq_all.size // I
+    hq = hq_all.reshape(RP, I)[rows]
+    hs = untile(plan.buffer("hsf", torch.uint8).cpu().numpy(), RP, I)[rows]
+    qh, sh = orc.quant_mxfp8(href[ok])
+    compare(dequant(orc, hq, hs), dequant(orc, qh, sh), bf16_out=False, rel_fro=REL_FRO_MXFP8,
+            what="hq mxfp8", max_bad_frac=1e-2)
+    assert np.mean(hq == qh) > 0.99
 
 
 def test_mxfp8_full_size_sampled(moe, orc):
