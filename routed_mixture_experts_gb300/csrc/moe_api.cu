@@ -379,7 +379,7 @@ int forward_mxfp8(moe_plan* p, const void* x, const uint8_t* w13_sf, const uint8
   // the rows, transposed (the WGRAD-W13 operand), in the same pass
   cudaError_t e =
       save ? launch_quant_two_way(x, p->token_of, p->off_pad + p->E, p->RP, p->d, p->xq, p->xsf,
-                                  p->xqT, p->xqTsf, st)
+                                  p->xqT, p->xqTsf, p->num_sms, st)
            : launch_gather_quant_rows(x, p->token_of, p->off_pad + p->E, p->d, p->xq, p->xsf,
                                       gather_grid(p), st);
   if (e != cudaSuccess) return cuda_status(e);
@@ -863,7 +863,7 @@ int moe_backward_mxfp8(moe_plan* p, const void* dy, const uint8_t* w13t, const u
   mark(p, 1, 0, st);
   // b1
   cudaError_t e = launch_quant_two_way(dy, p->token_of, nrows, (int)RP, d, p->dyq, p->dysf,
-                                       p->dyqT, p->dyqTsf, st);
+                                       p->dyqT, p->dyqTsf, p->num_sms, st);
   if (e != cudaSuccess) return cuda_status(e);
   p->launches += 1;
   mark(p, 1, 1, st);
@@ -886,7 +886,7 @@ int moe_backward_mxfp8(moe_plan* p, const void* dy, const uint8_t* w13t, const u
   }
   // b2'
   if ((e = launch_quant_two_way(p->dA, nullptr, nrows, (int)RP, 2 * I, p->dAq, p->dAsf, p->dAqT,
-                                p->dAqTsf, st)) != cudaSuccess ||
+                                p->dAqTsf, p->num_sms, st)) != cudaSuccess ||
       (e = launch_quant_rows_t(p->hs, nullptr, nrows, 1, (int)RP, I, p->hsqT, p->hsqTsf, st)) !=
           cudaSuccess)
     return cuda_status(e);

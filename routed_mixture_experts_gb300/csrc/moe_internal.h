@@ -202,9 +202,11 @@ cudaError_t launch_quant_rows_t(const void* in, const int32_t* src_row, const in
                                 cudaStream_t stream);
 // Both quantisations of one [R, C] bf16 operand (rows via src_row as above) in
 // one pass: along C into codes_row [R, C] + tiled scales (128-row blocks, K
-// groups over C), and along the rows into codes_t [C, R] + tiled scales.
+// groups over C), and along the rows into codes_t [C, R] + tiled scales
+// (persistent: a few CTAs on each of num_sms SMs).
 cudaError_t launch_quant_two_way(const void* in, const int32_t* src_row, const int32_t* nrows,
                                  int R, int C, uint8_t* codes_row, uint8_t* sf_row,
-                                 uint8_t* codes_t, uint8_t* sf_t, cudaStream_t stream);
+                                 uint8_t* codes_t, uint8_t* sf_t, int num_sms,
+                                 cudaStream_t stream);
 
 }  // namespace moe

@@ -189,87 +189,134 @@ __global__ void __launch_bounds__(kQtCols) k_quant_rows_t(const uint16_t* __rest
 // with src_row, row r is row src_row[r] of `in`, zero where negative; rows
 // r >= *nrows_p are skipped): along C into codes_row [R, C] with tiled scales
 // (128-row blocks, K groups over C), and along the rows, transposed, into
-// codes_t [C, R] with tiled scales as k_quant_rows_t.  A CTA stages kTwRows
-// (64 or 128) rows x 256 columns in shared memory (rows padded by 16 bytes so
-// both access patterns are free of bank conflicts): each thread quantises
-// kTwRows/32 32-column blocks of rows, then the kTwRows/32 32-row blocks of one
-// column, whose codes (contiguous) and scales (consecutive bytes) it writes whole.
+// codes_t [C, R] with tiled scales as k_quant_rows_t.  The work is cut into
+// tiles of kTwRows rows x 256 columns, staged in shared memory (rows padded by
+// 16 bytes so the column pass is free of bank conflicts): each thread
+// quantises kTwRows/32 32-column blocks of rows, then the kTwRows/32 32-row
+// blocks of one column, whose codes (contiguous) and scales (consecutive bytes)
+// it writes whole.  The kernel is persistent and double-buffered: while a CTA
+// quantises one tile, the 16-byte asynchronous copies of its next tile are in
+// flight.
 constexpr int kTwRows = 64;
 constexpr int kTwLd = kQtCols + 8;                 // staged row stride in elements (528 bytes)
-constexpr int kTwSmem = kTwRows * kTwLd * 2;
+constexpr int kTwBuf = kTwRows * kTwLd;            // elements per staging buffer
+constexpr int kTwSmem = 2 * kTwBuf * 2;            // two buffers, bytes
+constexpr int kTwCtasPerSm = 3;
 
-__global__ void __launch_bounds__(kQtCols) k_quant_two_way(const uint16_t* __restrict__ in,
-                                                           const int32_t* __restrict__ src_row,
-                                                           const int32_t* __restrict__ nrows_p,
-                                                           int R, int C,
-                                                           uint8_t* __restrict__ codes_row,
-                                                           uint8_t* __restrict__ sf_row,
-                                                           uint8_t* __restrict__ codes_t,
-                                                           uint8_t* __restrict__ sf_t) {
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  // bytes past src_bytes (0 or 16) are zero-filled
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_1() {
+  asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(kQtCols, kTwCtasPerSm)
+    k_quant_two_way(const uint16_t* __restrict__ in, const int32_t* __restrict__ src_row,
+                    const int32_t* __restrict__ nrows_p, int R, int C,
+                    uint8_t* __restrict__ codes_row, uint8_t* __restrict__ sf_row,
+                    uint8_t* __restrict__ codes_t, uint8_t* __restrict__ sf_t) {
   pdl_wait();   // the previous kernel of the stream has completed
-  extern __shared__ __align__(16) uint16_t tw_tile[];    // [kTwRows][kTwLd]
-  const int r0 = blockIdx.x * kTwRows;
-  const int c0 = blockIdx.y * kQtCols;
+  extern __shared__ __align__(16) uint16_t tw_tile[];    // [2][kTwRows][kTwLd]
   const int nrows = nrows_p ? *nrows_p : R;
-  if (r0 >= nrows) return;
-  for (int q = threadIdx.x; q < kTwRows * kQtCols / 8; q += kQtCols) {
-    const int rr = q / (kQtCols / 8), cc = (q % (kQtCols / 8)) * 8;
-    const int r = r0 + rr;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    const long long srow = r >= nrows ? -1 : (src_row ? (long long)src_row[r] : (long long)r);
-    if (srow >= 0 && c0 + cc < C) v = *reinterpret_cast<const uint4*>(in + srow * C + c0 + cc);
-    *reinterpret_cast<uint4*>(&tw_tile[rr * kTwLd + cc]) = v;
-  }
-  __syncthreads();
-  // along C: rows rr = threadIdx/8 + 32*i, 32-column block jb
-#pragma unroll 1
-  for (int i = 0; i < kTwRows / 32; ++i) {
-    const int rr = (threadIdx.x >> 3) + 32 * i, jb = threadIdx.x & 7;
-    const int c = c0 + jb * 32;
-    if (c < C) {
-      float f[32];
+  const int ncb = (C + kQtCols - 1) / kQtCols;
+  const int ntiles = (nrows + kTwRows - 1) / kTwRows * ncb;
+  // A warp copies 512 contiguous bytes of one row.  The source rows of a tile's
+  // copies are looked up one tile ahead (lookup), so no copy waits for them.
+  constexpr int kPer = kTwRows * kQtCols / 8 / kQtCols;   // copies per thread and tile
+  int srow[kPer];
+  auto lookup = [&](int tile) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint4 v = *reinterpret_cast<const uint4*>(&tw_tile[rr * kTwLd + jb * 32 + q * 8]);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          f[q * 8 + 2 * u] = __uint_as_float(w[u] << 16);
-          f[q * 8 + 2 * u + 1] = __uint_as_float(w[u] & 0xFFFF0000u);
-        }
-      }
-      uint32_t w[8];
-      const uint8_t scv = mx_quant32(f, w);
-      const long long r = r0 + rr;
-      uint4* dst = reinterpret_cast<uint4*>(codes_row + r * C + c);
-      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-      sf_row[mx_sf_offset(r >> 7, (int)(r & 127), c >> 5, C / 128)] = scv;
+    for (int j = 0; j < kPer; ++j) {
+      const int r = tile / ncb * kTwRows + (threadIdx.x + j * kQtCols) / (kQtCols / 8);
+      srow[j] = tile >= ntiles || r >= nrows ? -1 : (src_row ? src_row[r] : r);
     }
-  }
-  // along the rows: column c, its four 32-row blocks
-  const int c = c0 + threadIdx.x;
-  if (c >= C) return;
-  uint4* dst = reinterpret_cast<uint4*>(codes_t + (long long)c * R + r0);
-  static_assert(kTwRows == 64 || kTwRows == 128, "rows per CTA");
-  uint32_t sc4 = 0;
-#pragma unroll 1
-  for (int b = 0; b < kTwRows / 32; ++b) {
-    float f[32];
+  };
+  auto issue = [&](int tile, int buf) {
+    const int c0 = tile % ncb * kQtCols;
+    const uint32_t base = smem_u32(tw_tile + buf * kTwBuf);
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-      f[i] = __uint_as_float(((uint32_t)tw_tile[(32 * b + i) * kTwLd + threadIdx.x]) << 16);
-    uint32_t w[8];
-    sc4 |= (uint32_t)mx_quant32(f, w) << (8 * b);
-    dst[2 * b] = make_uint4(w[0], w[1], w[2], w[3]);
-    dst[2 * b + 1] = make_uint4(w[4], w[5], w[6], w[7]);
+    for (int j = 0; j < kPer; ++j) {
+      const int q = threadIdx.x + j * kQtCols;
+      const int rr = q / (kQtCols / 8), cc = (q % (kQtCols / 8)) * 8;
+      const bool ok = srow[j] >= 0 && c0 + cc < C;
+      cp_async16(base + (uint32_t)(rr * kTwLd + cc) * 2u,
+                 ok ? in + (long long)srow[j] * C + c0 + cc : in, ok ? 16u : 0u);
+    }
+  };
+  int tile = blockIdx.x;
+  lookup(tile);
+  if (tile < ntiles) issue(tile, 0);
+  cp_async_commit();
+  lookup(tile + gridDim.x);
+#pragma unroll 1
+  for (int it = 0; tile < ntiles; ++it, tile += gridDim.x) {
+    const int buf = it & 1;
+    if (tile + (int)gridDim.x < ntiles) issue(tile + gridDim.x, buf ^ 1);
+    cp_async_commit();               // (possibly empty) group of the next tile
+    lookup(tile + 2 * gridDim.x);    // in flight while this tile is quantised
+    cp_async_wait_1();               // this tile's copies have landed
+    __syncthreads();
+    const uint16_t* t = tw_tile + buf * kTwBuf;
+    const int r0 = tile / ncb * kTwRows, c0 = tile % ncb * kQtCols;
+    // along C: rows rr = threadIdx/8 + 32*i, 32-column block jb (eight threads
+    // write a row's 256 codes contiguously)
+#pragma unroll 1
+    for (int i = 0; i < kTwRows / 32; ++i) {
+      const int rr = (threadIdx.x >> 3) + 32 * i, jb = threadIdx.x & 7;
+      const int c = c0 + jb * 32;
+      if (c < C) {
+        float f[32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 v = *reinterpret_cast<const uint4*>(&t[rr * kTwLd + jb * 32 + q * 8]);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            f[q * 8 + 2 * u] = __uint_as_float(w[u] << 16);
+            f[q * 8 + 2 * u + 1] = __uint_as_float(w[u] & 0xFFFF0000u);
+          }
+        }
+        uint32_t w[8];
+        const uint8_t scv = mx_quant32(f, w);
+        const long long r = r0 + rr;
+        uint4* dst = reinterpret_cast<uint4*>(codes_row + r * C + c);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        sf_row[mx_sf_offset(r >> 7, (int)(r & 127), c >> 5, C / 128)] = scv;
+      }
+    }
+    // along the rows: column c, its kTwRows/32 32-row blocks
+    const int c = c0 + threadIdx.x;
+    if (c < C) {
+      uint4* dst = reinterpret_cast<uint4*>(codes_t + (long long)c * R + r0);
+      static_assert(kTwRows == 64 || kTwRows == 128, "rows per tile");
+      uint32_t sc4 = 0;
+#pragma unroll 1
+      for (int b = 0; b < kTwRows / 32; ++b) {
+        float f[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          f[i] = __uint_as_float(((uint32_t)t[(32 * b + i) * kTwLd + threadIdx.x]) << 16);
+        uint32_t w[8];
+        sc4 |= (uint32_t)mx_quant32(f, w) << (8 * b);
+        dst[2 * b] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[2 * b + 1] = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+      // the blocks of one K group sit in consecutive bytes of the tiled layout
+      uint8_t* sfp = sf_t + mx_sf_offset(c >> 7, c & 127, r0 / 32, R / 128);
+      if (kTwRows == 128)
+        *reinterpret_cast<uint32_t*>(sfp) = sc4;
+      else
+        *reinterpret_cast<uint16_t*>(sfp) = (uint16_t)sc4;
+    }
+    __syncthreads();                 // buffer `buf` is refilled next iteration
   }
-  // the blocks of one K group sit in consecutive bytes of the tiled layout
-  uint8_t* sfp = sf_t + mx_sf_offset(c >> 7, c & 127, r0 / 32, R / 128);
-  if (kTwRows == 128)
-    *reinterpret_cast<uint32_t*>(sfp) = sc4;
-  else
-    *reinterpret_cast<uint16_t*>(sfp) = (uint16_t)sc4;
   pdl_trigger();
 }
 
@@ -277,8 +324,9 @@ __global__ void __launch_bounds__(kQtCols) k_quant_two_way(const uint16_t* __res
 
 cudaError_t launch_quant_two_way(const void* in, const int32_t* src_row, const int32_t* nrows,
                                  int R, int C, uint8_t* codes_row, uint8_t* sf_row,
-                                 uint8_t* codes_t, uint8_t* sf_t, cudaStream_t stream) {
-  if (R % 128 || C % 128) return cudaErrorInvalidValue;
+                                 uint8_t* codes_t, uint8_t* sf_t, int num_sms,
+                                 cudaStream_t stream) {
+  if (R % 128 || C % 128 || num_sms < 1) return cudaErrorInvalidValue;
   static bool configured = false;   // attribute set once per process
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(k_quant_two_way,
@@ -286,8 +334,11 @@ cudaError_t launch_quant_two_way(const void* in, const int32_t* src_row, const i
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const dim3 grid(R / kTwRows, (C + kQtCols - 1) / kQtCols, 1);
-  return launch_pdl(k_quant_two_way, grid, dim3(kQtCols), kTwSmem, stream,
+  // persistent: a few CTAs per SM, at most one per tile
+  const long long tiles = (long long)(R / kTwRows) * ((C + kQtCols - 1) / kQtCols);
+  const int grid = (int)(tiles < (long long)num_sms * kTwCtasPerSm ? tiles
+                                                                   : (long long)num_sms * kTwCtasPerSm);
+  return launch_pdl(k_quant_two_way, dim3(grid), dim3(kQtCols), kTwSmem, stream,
                     static_cast<const uint16_t*>(in), src_row, nrows, R, C, codes_row, sf_row,
                     codes_t, sf_t);
 }

@@ -80,13 +80,22 @@ __global__ void __launch_bounds__(kMaxE) k_route_scan(RouteArgs a) {
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
   const int E = a.E;
-  // 1. per expert: exclusive scan of the chunk histograms -> chunk bases
+  // 1. per expert: exclusive scan of the chunk histograms -> chunk bases.  The
+  // counts are read 16 at a time before any base is written, so the loads of a
+  // batch are in flight together instead of one memory round trip per chunk.
   int c = 0;
   if (tid < E) {
-    for (int b = 0; b < a.nblk; ++b) {
-      const int v = a.blockcounts[b * E + tid];
-      a.blockcounts[b * E + tid] = c;
-      c += v;
+    constexpr int kB = 16;
+    for (int b0 = 0; b0 < a.nblk; b0 += kB) {
+      int v[kB];
+#pragma unroll
+      for (int u = 0; u < kB; ++u)
+        v[u] = b0 + u < a.nblk ? a.blockcounts[(b0 + u) * E + tid] : 0;
+#pragma unroll
+      for (int u = 0; u < kB; ++u) {
+        if (b0 + u < a.nblk) a.blockcounts[(b0 + u) * E + tid] = c;
+        c += v[u];
+      }
     }
     a.counts[tid] = c;
   }
@@ -249,9 +258,9 @@ __global__ void __launch_bounds__(256) k_gather_rows(const uint4* __restrict__ s
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int v = v0 + lane + 32 * u;
-        if (v < nvec) {
-          o0[v] = b0[u];
-          if (has1) o1[v] = b1[u];
+        if (v < nvec) {          // streaming stores: the rows are written once here
+          __stcs(o0 + v, b0[u]);
+          if (has1) __stcs(o1 + v, b1[u]);
         }
       }
     }
@@ -294,7 +303,8 @@ __global__ void __launch_bounds__(256) k_combine(const uint4* __restrict__ rows,
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int v = v0 + lane + 32 * u;
-          buf[j][u] = (rj[j] >= 0 && v < nvec) ? src[v] : make_uint4(0, 0, 0, 0);
+          // streaming loads: each expert row is read once, here
+          buf[j][u] = (rj[j] >= 0 && v < nvec) ? __ldcs(src + v) : make_uint4(0, 0, 0, 0);
         }
       }
       float acc[U][8];
@@ -359,7 +369,7 @@ __global__ void __launch_bounds__(256) k_combine_any(const uint4* __restrict__ r
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int v = v0 + lane + 32 * u;
-          buf[u] = v < nvec ? src[v] : make_uint4(0, 0, 0, 0);
+          buf[u] = v < nvec ? __ldcs(src + v) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) acc8(acc[u], buf[u]);
