@@ -175,11 +175,17 @@ int moe_backward_mxfp8(moe_plan* plan, const void* dy, const uint8_t* w13t,
  * copies x_host, ids_host, scores_host (and dy_host) into the plan's staging
  * area, runs moe_forward (+ moe_backward), and copies y (and dx, dscores) back
  * into the host buffers, all enqueued on `stream`; the caller synchronises the
- * stream before reading the host outputs.  In a training step the dY upload
- * and the y download run on a plan-owned side stream (created with the
- * host-staging workspace), overlapped with the forward and the backward; it
- * forks from and joins `stream`, so ordering is that of one stream.  Host buffers should be pinned
- * (page-locked) for the copies to be asynchronous.  Weights and weight
+ * stream before reading the host outputs.  The copies run on a plan-owned side
+ * stream (created with the host-staging workspace) that joins `stream` at the
+ * end of the step, overlapped with compute: x and dY upload during dispatch and
+ * the forward, y downloads during the backward, dx and dscores during the
+ * weight-gradient GEMMs.  After a training step on the plan, the next step's
+ * uploads need not wait for that step to end (its last reads of the staged
+ * inputs came before its dX combine), so in a loop of training steps they
+ * overlap the previous step's weight-gradient GEMMs.  The host buffers are read
+ * and written asynchronously: the caller keeps the inputs unchanged and leaves
+ * the outputs alone until the stream has passed the step.  Host buffers should
+ * be pinned (page-locked) for the copies to be asynchronous.  Weights and weight
  * gradients stay on the device.  Needs a MOE_WS_HOST_STAGING workspace (plus
  * MOE_WS_TRAINING when dy_host != NULL).
  */

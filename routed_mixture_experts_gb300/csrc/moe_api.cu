@@ -95,6 +95,7 @@ struct moe_plan {
   // set by moe_step_host only: the forward waits on wait_before_gather before
   // its gather, the backward records record_after_combine after its combine
   cudaEvent_t wait_before_gather, record_after_combine;
+  int prev_step_train;   // the last moe_step_host call on this plan was a complete training step
 };
 
 namespace moe {
@@ -552,6 +553,7 @@ int moe_plan_set_workspace(moe_plan* p, void* ws, size_t bytes, int flags) {
   p->ws_flags = flags;
   layout(p, p->ws, flags);
   p->saved = 0;
+  p->prev_step_train = 0;
   p->w13_cached = p->w2_cached = nullptr;
   p->dw13_cached = p->dw2_cached = nullptr;
   p->w13q_cached = p->w2q_cached = nullptr;
@@ -958,12 +960,19 @@ int moe_step_host(moe_plan* p, const void* x_host, const int32_t* ids_host,
   cudaStream_t sd = p->side;
   const size_t xb = 2ull * p->T * p->d, sb = 4ull * p->T * p->k;
   cudaError_t e;
-  // Copies overlap compute on a plan-owned side stream that forks from and
-  // joins `stream`: x uploads during dispatch, dY during the forward; y
+  // Copies overlap compute on a plan-owned side stream that joins `stream` at
+  // the end of the step: x uploads during dispatch, dY during the forward; y
   // downloads during the backward, dx and dscores during the weight gradients.
-  if ((e = cudaEventRecord(p->ev_fork, st)) != cudaSuccess ||
-      (e = cudaStreamWaitEvent(sd, p->ev_fork, 0)) != cudaSuccess ||
-      (e = cudaMemcpyAsync(p->st_x, x_host, xb, cudaMemcpyHostToDevice, sd)) != cudaSuccess ||
+  // The side stream forks from `stream` unless the previous step on this plan
+  // was a training step: that step's last side-stream copies (dx, dscores)
+  // waited for its dX combine, which came after every read of the staged x and
+  // dY, so this step's uploads may start while its weight gradients still run.
+  p->prev_step_train = p->prev_step_train && train;
+  if (!p->prev_step_train && ((e = cudaEventRecord(p->ev_fork, st)) != cudaSuccess ||
+                              (e = cudaStreamWaitEvent(sd, p->ev_fork, 0)) != cudaSuccess))
+    return cuda_status(e);
+  p->prev_step_train = 0;            // set again only when this step is fully enqueued
+  if ((e = cudaMemcpyAsync(p->st_x, x_host, xb, cudaMemcpyHostToDevice, sd)) != cudaSuccess ||
       (e = cudaEventRecord(p->ev_x, sd)) != cudaSuccess)
     return cuda_status(e);
   if (train && ((e = cudaMemcpyAsync(p->st_dy, dy_host, xb, cudaMemcpyHostToDevice, sd)) !=
@@ -999,6 +1008,7 @@ int moe_step_host(moe_plan* p, const void* x_host, const int32_t* ids_host,
       (e = cudaEventRecord(p->ev_dxdone, sd)) != cudaSuccess ||
       (e = cudaStreamWaitEvent(st, p->ev_dxdone, 0)) != cudaSuccess)
     return cuda_status(e);
+  p->prev_step_train = 1;
   return MOE_OK;
 }
 

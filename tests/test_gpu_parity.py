@@ -153,6 +153,49 @@ def test_host_step_matches_device_path(moe):
     assert torch.equal(dw13, g["dw13"]) and torch.equal(dw2, g["dw2"])
 
 
+def test_host_steps_back_to_back(moe):
+    """Training steps from host buffers enqueued without synchronising in between:
+    a step's uploads may overlap the previous step's weight gradients, and each
+    step must still give the outputs of its own inputs."""
+    c0 = dict(T=200, d=256, I=128, E=8, k=4)
+    a = make(None, seed=12, train=True, **c0)
+    b = make(None, seed=13, train=True, **c0)
+    b2 = dict(a)                         # same weights, other tokens, routing and dY
+    for key in ("x", "ids", "scores", "dy"):
+        b2[key] = b[key]
+    inps = [a, b2]
+    refs = [run_gpu(moe, inp, train=True) for inp in inps]
+    c = inps[0]["cfg"]
+    plan = moe.MoePlan(c["T"], c["d"], c["I"], c["E"], c["k"],
+                       flags=moe.MOE_WS_TRAINING | moe.MOE_WS_HOST_STAGING)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    dev = refs[0]["dev"]
+    dw13, dw2 = dev["dw13"].clone(), dev["dw2"].clone()
+    order = [0, 1, 0, 1]
+    outs = []
+    for i in order:
+        inp = inps[i]
+        h = dict(x=pin(inp["x"]).view(torch.bfloat16), dy=pin(inp["dy"]).view(torch.bfloat16),
+                 ids=pin(inp["ids"]), sc=pin(inp["scores"]),
+                 y=torch.empty(c["T"], c["d"], dtype=torch.bfloat16).pin_memory(),
+                 dx=torch.empty(c["T"], c["d"], dtype=torch.bfloat16).pin_memory(),
+                 ds=torch.empty(c["T"], c["k"], dtype=torch.float32).pin_memory())
+        plan.step_host(h["x"], h["ids"], h["sc"], dev["w13"], dev["w2"], h["y"], h["dy"], dw13,
+                       dw2, h["dx"], h["ds"])
+        outs.append(h)
+    torch.cuda.synchronize()
+    for i, h in zip(order, outs):
+        assert torch.equal(h["y"], refs[i]["y"].cpu())
+        assert torch.equal(h["dx"], refs[i]["dx"].cpu())
+        assert torch.equal(h["ds"], refs[i]["dscores"].cpu())
+    # the weight gradients received every step's increment
+    want13 = dev["dw13"] + 2 * (refs[0]["dw13"] - dev["dw13"]) + 2 * (refs[1]["dw13"] - dev["dw13"])
+    want2 = dev["dw2"] + 2 * (refs[0]["dw2"] - dev["dw2"]) + 2 * (refs[1]["dw2"] - dev["dw2"])
+    assert torch.allclose(dw13, want13, rtol=1e-4, atol=1e-4)
+    assert torch.allclose(dw2, want2, rtol=1e-4, atol=1e-4)
+    assert plan.check() == (0, 0)
+
+
 def test_mxfp8_quantiser_bit_exact(moe, orc):
     rng = np.random.default_rng(3)
     w = rng.standard_normal((96, 512)).astype(np.float32) * \
