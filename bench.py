@@ -79,7 +79,8 @@ def stage_model(c):
         "w2_score": ("tensor", 2 * R * d * I, 2 * R * I + E * d * I * 2 + 2 * R * d),
         "combine_y": ("hbm", 0, 2 * R * d + 2 * T * d + 4 * T * k),
         "gather_dy": ("hbm", 0, 2 * T * d + 2 * R * d),
-        "dgrad_w2_swiglu": ("hbm", 2 * R * d * I, 2 * R * d + E * d * I * 2 + 2 * R * I + 4 * R * I
+        # dY, W2, a (h is recomputed from a, not read), dA and hs written
+        "dgrad_w2_swiglu": ("hbm", 2 * R * d * I, 2 * R * d + E * d * I * 2 + 4 * R * I
                             + 4 * R * I + 2 * R * I),
         "dgrad_w13": ("tensor", 4 * R * d * I, 4 * R * I + E * 2 * I * d * 2 + 2 * R * d),
         "combine_dx": ("hbm", 0, 2 * R * d + 2 * T * d + 8 * T * k),
