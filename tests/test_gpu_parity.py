@@ -171,26 +171,32 @@ def test_host_steps_back_to_back(moe):
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
     dev = refs[0]["dev"]
     dw13, dw2 = dev["dw13"].clone(), dev["dw2"].clone()
-    order = [0, 1, 0, 1]
+    # training steps with alternating inputs, an inference step in between
+    order = [(0, True), (1, True), (0, False), (1, True), (0, True)]
     outs = []
-    for i in order:
+    for i, train in order:
         inp = inps[i]
         h = dict(x=pin(inp["x"]).view(torch.bfloat16), dy=pin(inp["dy"]).view(torch.bfloat16),
                  ids=pin(inp["ids"]), sc=pin(inp["scores"]),
                  y=torch.empty(c["T"], c["d"], dtype=torch.bfloat16).pin_memory(),
                  dx=torch.empty(c["T"], c["d"], dtype=torch.bfloat16).pin_memory(),
                  ds=torch.empty(c["T"], c["k"], dtype=torch.float32).pin_memory())
-        plan.step_host(h["x"], h["ids"], h["sc"], dev["w13"], dev["w2"], h["y"], h["dy"], dw13,
-                       dw2, h["dx"], h["ds"])
+        if train:
+            plan.step_host(h["x"], h["ids"], h["sc"], dev["w13"], dev["w2"], h["y"], h["dy"], dw13,
+                           dw2, h["dx"], h["ds"])
+        else:
+            plan.step_host(h["x"], h["ids"], h["sc"], dev["w13"], dev["w2"], h["y"])
         outs.append(h)
     torch.cuda.synchronize()
-    for i, h in zip(order, outs):
+    for (i, train), h in zip(order, outs):
         assert torch.equal(h["y"], refs[i]["y"].cpu())
-        assert torch.equal(h["dx"], refs[i]["dx"].cpu())
-        assert torch.equal(h["ds"], refs[i]["dscores"].cpu())
+        if train:
+            assert torch.equal(h["dx"], refs[i]["dx"].cpu())
+            assert torch.equal(h["ds"], refs[i]["dscores"].cpu())
     # the weight gradients received every step's increment
     want13 = dev["dw13"] + 2 * (refs[0]["dw13"] - dev["dw13"]) + 2 * (refs[1]["dw13"] - dev["dw13"])
     want2 = dev["dw2"] + 2 * (refs[0]["dw2"] - dev["dw2"]) + 2 * (refs[1]["dw2"] - dev["dw2"])
+    # (two training steps of each input)
     assert torch.allclose(dw13, want13, rtol=1e-4, atol=1e-4)
     assert torch.allclose(dw2, want2, rtol=1e-4, atol=1e-4)
     assert plan.check() == (0, 0)
