@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--mx-steps", type=int, default=50,
                     help="timed MXFP8 forward steps on the same inputs (0: skip)")
+    ap.add_argument("--fwd-steps", type=int, default=50,
+                    help="timed bf16 forward steps that save nothing (inference; 0: skip)")
     # smaller cases of the same workload (profiling captures); defaults = the full workload
     ap.add_argument("--T", type=int, default=None)
     ap.add_argument("--E", type=int, default=None)
@@ -457,6 +459,45 @@ def run_ours(args):
         e2e = {"value": flops_step * ws / (ems * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems}
 
+    # bf16 forward that saves nothing (inference) on the same inputs
+    fwd_inf = None
+    if args.fwd_steps > 0:
+        iplan = moe.MoePlan(T, d, I, E, k, clamp=c["clamp"], flags=0, device=dev)
+        yi = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+
+        def istep():
+            iplan.forward(D["x"], D["ids"], D["scores"], D["w13"], D["w2"], y=yi)
+
+        for _ in range(args.warmup):
+            istep()
+        iev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)]
+               for _ in range(args.fwd_steps)]
+        for ev in [e for st_ in iev for e in st_]:
+            ev.record(stream)
+        torch.cuda.synchronize()
+        i0 = torch.cuda.Event(enable_timing=True)
+        i1 = torch.cuda.Event(enable_timing=True)
+        i0.record(stream)
+        for i in range(args.fwd_steps):
+            iplan.set_timing_events(0, iev[i])
+            istep()
+        i1.record(stream)
+        torch.cuda.synchronize()
+        iplan.set_timing_events(0, None)
+        rc, det = iplan.check()
+        if rc != 0:
+            raise RuntimeError("device error %d (%d) in the bf16 forward" % (rc, det))
+        ims = max_over_ranks(i0.elapsed_time(i1), dev) / args.fwd_steps
+        ist = {}
+        for j, name in enumerate(FWD_STAGES):
+            ist[name] = {"ms": round(sum(iev[i][j].elapsed_time(iev[i][j + 1])
+                                         for i in range(args.fwd_steps)) / args.fwd_steps, 5)}
+        fwd_inf = {"workload": "train_e128 sizes and inputs, bf16 forward that saves nothing "
+                               "(inference)",
+                   "value": 6.0 * T * k * d * I * ws / (ims * 1e-3) / 1e12, "unit": "TFLOP/s",
+                   "ms_per_step": ims, "steps": args.fwd_steps, "stages": ist}
+        del iplan
+
     # MXFP8 E4M3 forward on the same inputs (its workload differs only in precision)
     mx = None
     mx_train = None
@@ -577,6 +618,7 @@ def run_ours(args):
                    "launch": "CUDA graph replay of the timed steps" if args.graph
                              else "eager launches"},
         "fwd_tflops": 6.0 * T * k * d * I / (fwd_ms * 1e-3) / 1e12,
+        "bf16_forward": fwd_inf,
         "fwd_ms": fwd_ms,
         "e2e": e2e, "gpu_launches": int(n1 - n0), "roofline": roofline, "stages": stages,
         "stages_note": "%d untimed steps with an event at every stage boundary; the timed steps "

@@ -31,13 +31,20 @@ def test_tiny_forward(moe, orc):
     inp = make("tiny_fwd", train=False)
     g = run_gpu(moe, inp, train=False)
     assert g["rc"] == 0
+    check_dispatch(orc, inp, g)
+    check_forward(orc, inp, g)
+
+
+def test_gathered_rows_bit_exact(moe, orc):
+    # the gather of a saving forward: bit-exact copies, padding rows zero
+    inp = make("tiny_fwd", train=True)
+    g = run_gpu(moe, inp, train=True)
+    assert g["rc"] == 0
     r = check_dispatch(orc, inp, g)
-    # gathered rows: bit-exact copies (padding rows zero)
     c = inp["cfg"]
     tok = g["plan"].buffer("token_of", torch.int32).cpu().numpy()[: r["off_pad"][-1]]
     xe = bits(g["plan"].buffer("xe", torch.bfloat16).view(-1, c["d"]))[: r["off_pad"][-1]]
     assert np.array_equal(xe, orc.gather_rows(inp["x"], tok))
-    check_forward(orc, inp, g)
 
 
 SMALL = [
