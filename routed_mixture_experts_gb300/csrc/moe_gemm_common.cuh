@@ -499,7 +499,7 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, const TileInfo& ti, 
 // measurably slower than a load and a store.)  The chunk sequence is this CTA's
 // tiles blockIdx.x, blockIdx.x + gridDim.x, ... times BN/32 chunks each; each
 // output tile is visited once per launch, so no load can see a pending store.
-constexpr int kWgradBufs = 5;   // fp32 chunk buffers of 16 KB
+constexpr int kWgradBufs = 4;   // fp32 chunk buffers of 16 KB (three loads ahead)
 
 struct WgradPipe {
   uint32_t buf0;     // first chunk buffer
