@@ -47,7 +47,7 @@ struct GemmShape {
   // expert's rows and it is bound by the gradient traffic), else two bf16
   // sub-tile buffers for the TMA-store epilogues.
   static constexpr int OUT_BYTES =
-      (EPI == EPI_WGRAD ? kWgradBufs
+      (EPI == EPI_WGRAD ? wgrad_bufs<MX>()
                         : (MX && BN == 256 ? kMxWideBufs
                                            : (EPI == EPI_SCORE || EPI == EPI_STORE
                                                   ? kEpiStageBufs
@@ -77,6 +77,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int STAGES = S::STAGES;
   constexpr uint32_t IDESC = MX ? idesc_mxf8(kBM, BN) : idesc_bf16(kBM, BN, A_MN, B_MN);
   constexpr int KE = MX ? 128 : kBK;     // K elements per stage (128 bytes per row)
+  constexpr int WB = wgrad_bufs<MX>();   // WGRAD: fp32 gradient chunk buffers
   static_assert(!MX || (!A_MN && !B_MN && (BN == 128 || BN == 256)),
                 "MXFP8: K-major operands, BN = 128 or 256");
   static_assert(S::SMEM_BYTES <= 232448, "shared memory budget");
@@ -117,7 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(drain_bar, 1);
     if (EPI == EPI_WGRAD)
-      for (int b = 0; b < kWgradBufs; ++b) mbar_init(wg_bar0 + 8u * b, 1);
+      for (int b = 0; b < WB; ++b) mbar_init(wg_bar0 + 8u * b, 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -324,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     int sub = 0;                              // output staging-buffer sequence number
     WgradPipe wp{stage0 + STAGES * S::STAGE_BYTES, wg_bar0, num_tiles, 0, 0};
-    if (EPI == EPI_WGRAD && et == 0) wgrad_issue<BN>(args, &tmC, wp, kWgradBufs - 1);
+    if (EPI == EPI_WGRAD && et == 0) wgrad_issue<BN, WB>(args, &tmC, wp, WB - 1);
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const TileInfo ti = decode_tile<BN>(args, tile);
       int w = 1;
@@ -341,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc_phase ^= 1u;
         continue;
       } else if constexpr (EPI == EPI_WGRAD) {
-        if (!epilogue_wgrad<BN>(args, &tmC, ti, row, tbase, et, half, wp, &abort_s, wlim)) break;
+        if (!epilogue_wgrad<BN, WB>(args, &tmC, ti, row, tbase, et, half, wp, &abort_s, wlim)) break;
       } else {
         epilogue<BN, EPI>(args, ti, row, tbase, half, &tmO0, &tmO1,
                           stage0 + STAGES * S::STAGE_BYTES, et, sub);
@@ -354,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (EPI == EPI_WGRAD && et == 0) {
       // after an abort: let every gradient chunk load still in flight land
       for (int n = wp.next; n < wp.issued; ++n)
-        mbar_wait_drain(wg_bar0 + 8u * (uint32_t)(n % kWgradBufs), (uint32_t)((n / kWgradBufs) & 1));
+        mbar_wait_drain(wg_bar0 + 8u * (uint32_t)(n % WB), (uint32_t)((n / WB) & 1));
     }
     if (et == 0) bulk_wait_all();   // every output store has completed
   }

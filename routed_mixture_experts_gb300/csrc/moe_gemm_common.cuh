@@ -492,24 +492,27 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, const TileInfo& ti, 
 
 // WGRAD epilogue: read-modify-write of the fp32 gradient, 32 columns (16 KB:
 // 128 rows x 32 fp32, 128-byte swizzle, the layout of the fp32 tensor map) at a
-// time.  Each such chunk is loaded by TMA into one of kWgradBufs shared-memory
-// buffers ahead of use (kWgradBufs - 1 chunks ahead, across tile boundaries),
+// time.  Each such chunk is loaded by TMA into one of NB shared-memory
+// buffers ahead of use (NB - 1 chunks ahead, across tile boundaries),
 // every thread adds its row's accumulator values to it in place, and TMA stores
 // it back.  (A TMA reduce-add in L2 does the same sum but moves fp32 data
 // measurably slower than a load and a store.)  The chunk sequence is this CTA's
 // tiles blockIdx.x, blockIdx.x + gridDim.x, ... times BN/32 chunks each; each
 // output tile is visited once per launch, so no load can see a pending store.
-constexpr int kWgradBufs = 4;   // fp32 chunk buffers of 16 KB (three loads ahead)
+// fp32 chunk buffers of 16 KB: 4 (three loads ahead) for the 256-wide bf16
+// tiles, 5 for the 128-wide block-scaled ones (measured best for each)
+template <bool MX>
+__host__ __device__ constexpr int wgrad_bufs() { return MX ? 5 : 4; }
 
 struct WgradPipe {
   uint32_t buf0;     // first chunk buffer
-  uint32_t bar0;     // first of kWgradBufs load barriers
+  uint32_t bar0;     // first of the NB chunk-load barriers
   int num_tiles;
   int next;          // chunks consumed (all epilogue threads)
   int issued;        // chunks whose load has been issued (thread et == 0)
 };
 
-template <int BN>
+template <int BN, int NB>
 __device__ __forceinline__ void wgrad_issue(const GemmArgs& a, const CUtensorMap* tmC,
                                             WgradPipe& p, int upto) {
   constexpr int CH = BN / 32;
@@ -518,7 +521,7 @@ __device__ __forceinline__ void wgrad_issue(const GemmArgs& a, const CUtensorMap
     const int tile = (int)blockIdx.x + (n / CH) * (int)gridDim.x;
     if (tile >= p.num_tiles) return;
     const TileInfo t = decode_tile<BN>(a, tile);
-    const int b = n % kWgradBufs;
+    const int b = n % NB;
     const uint32_t bar = p.bar0 + 8u * (uint32_t)b;
     mbar_arrive_expect_tx(bar, 16384u);
     tma_load_2d(p.buf0 + (uint32_t)b * 16384u, tmC, t.n0 + (n % CH) * 32,
@@ -528,7 +531,7 @@ __device__ __forceinline__ void wgrad_issue(const GemmArgs& a, const CUtensorMap
 }
 
 // Returns false when a wait gave up (every epilogue thread returns the same).
-template <int BN>
+template <int BN, int NB>
 __device__ __forceinline__ bool epilogue_wgrad(const GemmArgs& a, const CUtensorMap* tmC,
                                                const TileInfo& ti, int row, uint32_t tbase, int et,
                                                int half, WgradPipe& p, volatile int* abort_flag,
@@ -539,11 +542,11 @@ __device__ __forceinline__ bool epilogue_wgrad(const GemmArgs& a, const CUtensor
 #pragma unroll 1
   for (int c = 0; c < BN; c += 32) {
     const int n = p.next;
-    const int b = n % kWgradBufs;
+    const int b = n % NB;
     const uint32_t buf = p.buf0 + (uint32_t)b * 16384u;
     // this thread's half: 16 of the chunk's 32 columns (16-byte chunks 4h..4h+3)
     tmem_ld16(tbase + c + 16 * half, r0);
-    const int w = mbar_wait(p.bar0 + 8u * (uint32_t)b, (uint32_t)((n / kWgradBufs) & 1),
+    const int w = mbar_wait(p.bar0 + 8u * (uint32_t)b, (uint32_t)((n / NB) & 1),
                             abort_flag, a.err, 6, wlim)
                       ? 1 : 0;
     tmem_ld_wait();
@@ -566,9 +569,9 @@ __device__ __forceinline__ bool epilogue_wgrad(const GemmArgs& a, const CUtensor
       tma_store_2d(tmC, buf, ti.n0 + c, ybase);
       bulk_commit();
       // chunk n-1's buffer is free once its store has read it: load chunk
-      // n + kWgradBufs - 1 there
+      // n + NB - 1 there
       bulk_wait_read<1>();
-      wgrad_issue<BN>(a, tmC, p, n + kWgradBufs);
+      wgrad_issue<BN, NB>(a, tmC, p, n + NB);
     }
   }
   return true;
