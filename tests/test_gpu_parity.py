@@ -56,6 +56,7 @@ SMALL = [
     ("skew_empty", dict(T=400, d=128, I=256, E=12, k=3, routing="zipf", zipf_s=1.2,
                         zipf_support=8), {}),
     ("single_expert", dict(T=130, d=128, I=64, E=1, k=1), {}),
+    ("one_token", dict(T=1, d=128, I=64, E=4, k=2), {}),
     ("k8_e256", dict(T=96, d=128, I=64, E=256, k=8), {}),
     # W13, W2 and DGRAD-W13 on CTA pairs (moe_plan_set_cta_pairs): pairs of an
     # expert's m tiles on the pair kernel, an odd last m tile on one CTA
@@ -119,6 +120,18 @@ def test_bad_ids_are_reported(moe):
     assert g["detail"] == 122
     # the error word is cleared by the check
     assert g["plan"].check() == (0, 0)
+
+
+def test_all_ids_invalid(moe):
+    # every routed element dropped: no rows reach any expert, so the GEMMs have no
+    # tiles; y and dx are zero, dscores zero, the weight gradients untouched
+    inp = make(None, seed=10, train=True, T=50, d=128, I=64, E=4, k=2)
+    inp["ids"] = np.full_like(inp["ids"], 4)       # out of range for E = 4
+    g = run_gpu(moe, inp, train=True)
+    assert g["rc"] == moe.MOE_ERR_BAD_IDS and g["detail"] == 0
+    assert not g["y"].any() and not g["dx"].any() and not g["dscores"].any()
+    assert torch.equal(g["dw13"], g["dev"]["dw13"]) and torch.equal(g["dw2"], g["dev"]["dw2"])
+    assert int(g["plan"].buffer("off_pad", torch.int32)[-1]) == 0
 
 
 def test_backward_needs_saving_forward(moe):
