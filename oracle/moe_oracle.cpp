@@ -1,6 +1,9 @@
-// moe_oracle.cpp -- plain, slow, single-threaded CPU oracle for the routed-expert
-// hot path (dispatch -> W13 GEMM -> SwiGLU -> W2 GEMM x score -> combine, and the
-// backward: DGRAD, WGRAD, score gradients).
+// moe_oracle.cpp -- plain, slow CPU oracle for the routed-expert hot path
+// (dispatch -> W13 GEMM -> SwiGLU -> W2 GEMM x score -> combine, and the backward:
+// DGRAD, WGRAD, score gradients).  Loops token by token; where OpenMP is
+// available the independent outer loops (tokens, gradient rows) are spread over
+// host threads, each output element still summed by one thread in index order,
+// so results do not depend on the thread count.
 //
 // TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, loads or calls
 // this file; only the test suite, the smoke check and the CPU-baseline leg of the
