@@ -134,13 +134,13 @@ __device__ __forceinline__ void pack32(const float (&v)[32], uint32_t (&pk)[16])
 // the 64 columns of its row), then one thread stores it with TMA.  Two buffers
 // alternate; a buffer is rewritten only once its previous store has read it.
 constexpr int kEpiStageBufs = 2;
-// 16 KB staging buffers of the three-output epilogues.  SwiGLU forward keeps four
-// 48 KB operand stages with two buffers (its main loop is the longer part);
-// SwiGLU backward, whose epilogue also reads the forward's activations, goes
-// faster with three buffers and three stages (measured on the E = 128 training
-// shapes).
+// 16 KB staging buffers of the three-output epilogues (SwiGLU forward: h, a gate,
+// a up; backward: dA gate, dA up, hs): two, which leaves room for four 48 KB
+// operand stages.  Both main loops are bound by load latency, so the fourth
+// stage is worth more than a buffer per output (SwiGLU backward 0.293 -> 0.284 ms
+// on the E = 128 training shapes).
 template <int EPI>
-__host__ __device__ constexpr int tri_bufs() { return EPI == EPI_DGRAD2 ? 3 : 2; }
+__host__ __device__ constexpr int tri_bufs() { return 2; }
 
 __device__ __forceinline__ void epi_stage_store(const CUtensorMap* tm, uint32_t out0, int& seq,
                                                 int et, int row, int half, const float (&v)[32],
