@@ -53,7 +53,12 @@ struct GemmShape {
                                                   ? kEpiStageBufs
                                                   : tri_bufs<EPI>()))) * 16384;
   static constexpr int STAGE_BUDGET = 226 * 1024 - OUT_BYTES;
-  static constexpr int STAGES = STAGE_BUDGET / STAGE_BYTES > 8 ? 8 : STAGE_BUDGET / STAGE_BYTES;
+  // at most 8 stages; block-scaled kernels at most 4: a fifth made the SwiGLU
+  // backward slower (its epilogue's row loads gain from the L1 a smaller ring
+  // leaves), and the 256-wide ones fit no more than four
+  static constexpr int MAX_STAGES = MX ? 4 : 8;
+  static constexpr int STAGES =
+      STAGE_BUDGET / STAGE_BYTES > MAX_STAGES ? MAX_STAGES : STAGE_BUDGET / STAGE_BYTES;
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + OUT_BYTES + BAR_BYTES + 1024;
   // TMEM: the accumulators, then (MXFP8) SF_COLS scale columns per stage, A's
