@@ -290,7 +290,9 @@ __global__ void __launch_bounds__(256) k_combine(const uint4* __restrict__ rows,
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
-  constexpr int U = KMAX <= 4 ? 4 : 2;   // 16-byte vectors per lane per pass
+  // 16-byte vectors per lane per pass: with k = 8 one (8 loads in flight per lane
+  // keep the registers, and so the resident warps, low; measured faster than 2)
+  constexpr int U = KMAX <= 4 ? 4 : 1;
   for (int t = gw; t < T; t += nw) {
     int rj[KMAX];
 #pragma unroll
