@@ -160,7 +160,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
       const TileInfo ti = decode_tile<BN>(args, tile);
+      // k_rotate (row GEMMs): the tiles that share an A tile (same m tile) or a
+      // B tile (same expert and n tile) run at the same time; each starts its K
+      // loop at its own offset (wrapping around), so each K chunk is read from
+      // DRAM by one of them and from L2 by the others, instead of all of them
+      // waiting on DRAM for the same chunk.
+      const int kb0 = args.k_rotate ? (int)(((unsigned)(ti.m0 >> 7) * 7u + (unsigned)ti.nt * 5u) %
+                                            (unsigned)ti.kb)
+                                    : 0;
       for (int kb = 0; kb < ti.kb; ++kb) {
+        const int kc = kb + kb0 < ti.kb ? kb + kb0 : kb + kb0 - ti.kb;   // K chunk loaded
         int w = 1;
         if (lane == 0) w = mbar_wait(empty_bar(stage), phase ^ 1u, &abort_s, args.err, 1, wlim);
         ok = __shfl_sync(0xffffffffu, w, 0) != 0;
@@ -176,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t ssf = sb + S::B_BYTES;
             // row GEMMs: K groups from 0, B row blocks of (expert, n tile); wgrad
             // mode: K groups from the expert's first row, B row blocks from n0/128
-            const long long kg = (long long)(ti.krow0 >> 7) + kb;
+            const long long kg = (long long)(ti.krow0 >> 7) + kc;
             const long long ga = ((long long)(ti.m0 >> 7) * args.sf_ngr + kg) * 512;
             const long long gbr =
                 args.wgrad ? (long long)(ti.n0 >> 7)
@@ -191,29 +200,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           // A: 128 rows x 128 bytes of K.  K-major: a 128-row box of [rows, K];
           // MN-major: two 64-wide atoms of the [K rows, M] tensor (3-D map).
           if (A_MN)
-            tma_load_3d(sa, &tmA, 0, ti.krow0 + kb * kBK, ti.m0 >> 6, fb);
+            tma_load_3d(sa, &tmA, 0, ti.krow0 + kc * kBK, ti.m0 >> 6, fb);
           else
-            tma_load_2d(sa, &tmA, ti.krow0 + kb * KE, ti.m0, fb);
+            tma_load_2d(sa, &tmA, ti.krow0 + kc * KE, ti.m0, fb);
           // B: BN rows (N) x 128 bytes of K
           if (args.wgrad && B_MN) {
-            tma_load_3d(sb, &tmB, 0, ti.krow0 + kb * kBK, ti.n0 >> 6, fb);
+            tma_load_3d(sb, &tmB, 0, ti.krow0 + kc * kBK, ti.n0 >> 6, fb);
           } else if (args.wgrad) {
             // K-major transposed operand [N, rows]: this expert's K range
-            tma_load_2d(sb, &tmB, ti.krow0 + kb * KE, ti.n0, fb);
+            tma_load_2d(sb, &tmB, ti.krow0 + kc * KE, ti.n0, fb);
           } else if (B_MN) {
             // [E*K, N]: BN/64 atoms of expert e's K rows
-            tma_load_3d(sb, &tmB, 0, ti.e * args.b_expert_rows + kb * kBK, ti.n0 >> 6, fb);
+            tma_load_3d(sb, &tmB, 0, ti.e * args.b_expert_rows + kc * kBK, ti.n0 >> 6, fb);
           } else if (EPI == EPI_SWIGLU && MX && BN == 256) {
             // (K, 64, 2, I/64, E) view of W13: two 64-row blocks, each its gate
             // rows then the same up rows (the row order of the scale chunks)
-            tma_load_5d(sb, &tmB, kb * KE, 0, 0, 2 * ti.nt, ti.e, fb);
+            tma_load_5d(sb, &tmB, kc * KE, 0, 0, 2 * ti.nt, ti.e, fb);
           } else if (EPI == EPI_SWIGLU) {
             // (K, I, 2E) view of W13: this tile's BN/2 gate rows, then the same up
             // rows, in one box
-            tma_load_3d(sb, &tmB, kb * KE, ti.nt * (BN / 2), 2 * ti.e, fb);
+            tma_load_3d(sb, &tmB, kc * KE, ti.nt * (BN / 2), 2 * ti.e, fb);
           } else {
             // [E*N, K]: a BN-row box
-            tma_load_2d(sb, &tmB, kb * KE, ti.e * args.b_expert_rows + ti.n0, fb);
+            tma_load_2d(sb, &tmB, kc * KE, ti.e * args.b_expert_rows + ti.n0, fb);
           }
           issued_parity[stage] = (int)phase;
         }

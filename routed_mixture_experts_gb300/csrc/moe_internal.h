@@ -76,6 +76,9 @@ struct GemmArgs {
   float clamp;               // SwiGLU limit (0 = plain)
   int I;                     // column offset of the up half in a / dA
   int save;                  // EPI_SWIGLU: store a
+  int k_rotate;              // rows mode: start each tile's K loop at an offset of its own
+                             // (m and n tile), so tiles sharing an operand tile read
+                             // different K chunks at a time (changes the summation order)
   int wgrad_kstep;           // wgrad mode: rows per K stage (0: 64; MXFP8: 128)
   // MXFP8 (block-scaled) operands: tiled E8M0 scales (see mx_sf_offset)
   const uint8_t* sfa;        // scales of A, row blocks of 128 padded rows
