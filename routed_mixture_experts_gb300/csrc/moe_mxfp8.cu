@@ -193,13 +193,18 @@ __global__ void __launch_bounds__(kQtCols) k_quant_rows_t(const uint16_t* __rest
 // tiles of kTwRows rows x 256 columns, staged in shared memory (rows padded by
 // 16 bytes so the column pass is free of bank conflicts): each thread
 // quantises kTwRows/32 32-column blocks of rows, then the kTwRows/32 32-row
-// blocks of one column, whose codes (contiguous) and scales (consecutive bytes)
-// it writes whole.  The kernel is persistent and double-buffered: while a CTA
+// blocks of one column, whose scales (consecutive bytes) it writes whole and
+// whose codes go back through shared memory so that the stores are coalesced.
+// The kernel is persistent and double-buffered: while a CTA
 // quantises one tile, the 16-byte asynchronous copies of its next tile are in
 // flight.
 constexpr int kTwRows = 64;
 constexpr int kTwLd = kQtCols + 8;                 // staged row stride in elements (528 bytes)
 constexpr int kTwBuf = kTwRows * kTwLd;            // elements per staging buffer
+// transposed codes staged per column (bytes): kTwRows plus 16, so the 16-byte
+// stores of a quarter warp fall in distinct banks
+constexpr int kTwTLd = kTwRows + 16;
+static_assert(kQtCols * kTwTLd <= kTwBuf * 2, "transposed codes fit the tile's buffer");
 constexpr int kTwSmem = 2 * kTwBuf * 2;            // two buffers, bytes
 constexpr int kTwCtasPerSm = 3;
 
@@ -293,11 +298,11 @@ __global__ void __launch_bounds__(kQtCols, kTwCtasPerSm)
     }
     // along the rows: column c, its kTwRows/32 32-row blocks
     const int c = c0 + threadIdx.x;
+    static_assert(kTwRows == 64, "rows per tile");
+    uint4 tq[kTwRows / 16];          // column c's codes, 16 rows per vector
     if (c < C) {
-      uint4* dst = reinterpret_cast<uint4*>(codes_t + (long long)c * R + r0);
-      static_assert(kTwRows == 64 || kTwRows == 128, "rows per tile");
       uint32_t sc4 = 0;
-#pragma unroll 1
+#pragma unroll
       for (int b = 0; b < kTwRows / 32; ++b) {
         float f[32];
 #pragma unroll
@@ -305,15 +310,32 @@ __global__ void __launch_bounds__(kQtCols, kTwCtasPerSm)
           f[i] = __uint_as_float(((uint32_t)t[(32 * b + i) * kTwLd + threadIdx.x]) << 16);
         uint32_t w[8];
         sc4 |= (uint32_t)mx_quant32(f, w) << (8 * b);
-        dst[2 * b] = make_uint4(w[0], w[1], w[2], w[3]);
-        dst[2 * b + 1] = make_uint4(w[4], w[5], w[6], w[7]);
+        tq[2 * b] = make_uint4(w[0], w[1], w[2], w[3]);
+        tq[2 * b + 1] = make_uint4(w[4], w[5], w[6], w[7]);
       }
       // the blocks of one K group sit in consecutive bytes of the tiled layout
-      uint8_t* sfp = sf_t + mx_sf_offset(c >> 7, c & 127, r0 / 32, R / 128);
-      if (kTwRows == 128)
-        *reinterpret_cast<uint32_t*>(sfp) = sc4;
-      else
-        *reinterpret_cast<uint16_t*>(sfp) = (uint16_t)sc4;
+      *reinterpret_cast<uint16_t*>(sf_t + mx_sf_offset(c >> 7, c & 127, r0 / 32, R / 128)) =
+          (uint16_t)sc4;
+    }
+    // Each column's codes are one kTwRows-byte piece of a different output row.
+    // Stored from registers, a warp's 16-byte stores would land in 32 rows; the
+    // tile's buffer (read completely by now) stages them instead, and
+    // consecutive threads then write consecutive 16-byte pieces of a row.
+    __syncthreads();
+    uint8_t* stg = reinterpret_cast<uint8_t*>(tw_tile + buf * kTwBuf);
+    if (c < C) {
+#pragma unroll
+      for (int j = 0; j < kTwRows / 16; ++j)
+        *reinterpret_cast<uint4*>(stg + threadIdx.x * kTwTLd + j * 16) = tq[j];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kTwRows / 16; ++j) {
+      const int idx = threadIdx.x + j * kQtCols;
+      const int cc = idx / (kTwRows / 16), pc = idx % (kTwRows / 16);
+      if (c0 + cc < C)
+        *reinterpret_cast<uint4*>(codes_t + (long long)(c0 + cc) * R + r0 + pc * 16) =
+            *reinterpret_cast<const uint4*>(stg + cc * kTwTLd + pc * 16);
     }
     __syncthreads();                 // buffer `buf` is refilled next iteration
   }
