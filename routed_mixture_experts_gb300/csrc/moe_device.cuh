@@ -165,16 +165,6 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const void* tmap, int 
       : "memory");
 }
 
-// Element-wise add of a shared-memory tile into global memory, performed by the
-// TMA unit (read-modify-write in L2), tracked by the issuing thread's bulk group.
-__device__ __forceinline__ void tma_reduce_add_2d(const void* tmap, uint32_t src, int x, int y) {
-  asm volatile(
-      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-          reinterpret_cast<uint64_t>(tmap)),
-      "r"(src), "r"(x), "r"(y)
-      : "memory");
-}
-
 // Shared-memory tile -> global memory through the TMA unit (bulk group).
 __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int x, int y) {
   asm volatile(

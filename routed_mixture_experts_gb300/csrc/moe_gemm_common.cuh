@@ -97,27 +97,6 @@ __device__ __forceinline__ float swiglu_fwd(float G, float U, float L) {
   return silu * U;
 }
 
-__device__ __forceinline__ void store16_bf16(uint16_t* dst, const float (&v)[16]) {
-  uint4 lo, hi;
-  lo.x = pack_bf2(v[0], v[1]);   lo.y = pack_bf2(v[2], v[3]);
-  lo.z = pack_bf2(v[4], v[5]);   lo.w = pack_bf2(v[6], v[7]);
-  hi.x = pack_bf2(v[8], v[9]);   hi.y = pack_bf2(v[10], v[11]);
-  hi.z = pack_bf2(v[12], v[13]); hi.w = pack_bf2(v[14], v[15]);
-  reinterpret_cast<uint4*>(dst)[0] = lo;
-  reinterpret_cast<uint4*>(dst)[1] = hi;
-}
-
-__device__ __forceinline__ void load16_bf16(const uint16_t* src, float (&v)[16]) {
-  const uint4 lo = reinterpret_cast<const uint4*>(src)[0];
-  const uint4 hi = reinterpret_cast<const uint4*>(src)[1];
-  const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    v[2 * i] = __uint_as_float(w[i] << 16);
-    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
-}
-
 // ---------------------------------------------------------------------------
 // epilogues: one thread owns one output row (`row` within the tile) and reads
 // its accumulator columns from TMEM at `tbase` (lane quarter already folded in).
@@ -216,17 +195,6 @@ __device__ __forceinline__ void epi_stage_three(const CUtensorMap* t0, const CUt
     const int xs1[1] = {x2};
     const uint32_t(&pk1)[1][16] = *reinterpret_cast<const uint32_t(*)[1][16]>(&pk[2]);
     epi_stage_batch<1>(tms1, buf, et, row, half, pk1, xs1, y);
-  }
-}
-
-__device__ __forceinline__ void load32_bf16(const uint16_t* src, float (&v)[32]) {
-  float a[16], b[16];
-  load16_bf16(src, a);
-  load16_bf16(src + 16, b);
-#pragma unroll
-  for (int q = 0; q < 16; ++q) {
-    v[q] = a[q];
-    v[16 + q] = b[q];
   }
 }
 
