@@ -267,8 +267,10 @@ const char* moe_status_string(int status);
  *                                    only its E4M3 codes, MOE_BUF_HQ)
  *   MOE_BUF_YS        bf16  [Rpad,d] score-weighted expert outputs
  *   MOE_BUF_DYE       bf16  [Rpad,d] gathered upstream gradient
- *   MOE_BUF_DA        bf16  [Rpad,2I] gradient at gate/up
- *   MOE_BUF_HS        bf16  [Rpad,I] score * h (WGRAD-W2 operand)
+ *   MOE_BUF_DA        bf16  [Rpad,2I] gradient at gate/up (bf16 plans; MXFP8 plans
+ *                                    keep only its E4M3 codes, MOE_BUF_DAQ / DAQT)
+ *   MOE_BUF_HS        bf16  [Rpad,I] score * h, the WGRAD-W2 operand (bf16 plans;
+ *                                    MXFP8 plans keep only MOE_BUF_HSQT)
  *   MOE_BUF_DXE       bf16  [Rpad,d] per-row input gradients
  * Rows are valid up to off_pad[E].  Sizes are the worst-case capacities.  A
  * tensor the plan does not hold returns MOE_ERR_WORKSPACE.
@@ -293,6 +295,12 @@ const char* moe_status_string(int status);
 #define MOE_BUF_HSF      16   /* u8   tiled E8M0 scales of HQ                   */
 #define MOE_BUF_XQT      17   /* MXFP8 training: E4M3 [d, Rpad], routed x quantised along the rows */
 #define MOE_BUF_XQTSF    18   /* its tiled scales (row blocks over d, K groups over Rpad)      */
+#define MOE_BUF_DAQ      19   /* MXFP8 training: E4M3 [Rpad, 2I], dA quantised along 2I        */
+#define MOE_BUF_DASF     20   /* its tiled scales (row blocks over Rpad, K groups over 2I)     */
+#define MOE_BUF_DAQT     21   /* MXFP8 training: E4M3 [2I, Rpad], dA quantised along the rows  */
+#define MOE_BUF_DAQTSF   22   /* its tiled scales (row blocks over 2I, K groups over Rpad)     */
+#define MOE_BUF_HSQT     23   /* MXFP8 training: E4M3 [I, Rpad], hs quantised along the rows   */
+#define MOE_BUF_HSQTSF   24   /* its tiled scales (row blocks over I, K groups over Rpad)      */
 int moe_plan_buffer(const moe_plan* plan, int which, void** dev_ptr, size_t* bytes);
 
 /*

@@ -20,7 +20,8 @@ MOE_PREC_MXFP8 = 1
 MOE_WS_TRAINING = 1
 MOE_WS_HOST_STAGING = 2
 MOE_BUF = dict(m_indptr=0, off_pad=1, row_of=2, token_of=3, score_of=4, xe=5, a=6, h=7, ys=8,
-               dye=9, dA=10, hs=11, dxe=12, xq=13, xsf=14, hq=15, hsf=16, xqT=17, xqTsf=18)
+               dye=9, dA=10, hs=11, dxe=12, xq=13, xsf=14, hq=15, hsf=16, xqT=17, xqTsf=18,
+               dAq=19, dAsf=20, dAqT=21, dAqTsf=22, hsqT=23, hsqTsf=24)
 
 _lock = threading.Lock()
 _lib = None

@@ -257,9 +257,8 @@ size_t layout(moe_plan* p, char* base, int flags) {
   p->dyq = p->dysf = p->dAq = p->dAsf = p->dyqT = p->dyqTsf = nullptr;
   p->dAqT = p->dAqTsf = p->hsqT = p->hsqTsf = p->xqT = p->xqTsf = nullptr;
   if ((flags & MOE_WS_TRAINING) && mx) {
+    // dA and hs only as E4M3 codes (written by the DGRAD-W2 epilogue)
     p->a = reinterpret_cast<uint16_t*>(take(2 * RP * 2 * I));
-    p->dA = reinterpret_cast<uint16_t*>(take(2 * RP * 2 * I));
-    p->hs = reinterpret_cast<uint16_t*>(take(2 * RP * I));
     p->dxe = reinterpret_cast<uint16_t*>(take(2 * RP * d));
     p->pdscore = reinterpret_cast<float*>(take(4 * RP * 2 * (I / p->bnd2)));
     auto q = [&](size_t rows, size_t cols, uint8_t** codes, uint8_t** sf) {
@@ -578,8 +577,6 @@ int moe_plan_set_workspace(moe_plan* p, void* ws, size_t bytes, int flags) {
          encode_tmap_u8(&p->tm_dAqT, p->dAqT, 2LL * p->I, RP, 128) ||
          encode_tmap_u8(&p->tm_hsqT, p->hsqT, p->I, RP, 128) ||
          encode_tmap_u8(&p->tm_xqT, p->xqT, p->d, RP, 128) ||
-         encode_tmap_bf16(&p->tm_dA, p->dA, RP, 2LL * p->I, 128) ||
-         encode_tmap_bf16(&p->tm_hs, p->hs, RP, p->I, 128) ||
          encode_tmap_bf16(&p->tm_dxe, p->dxe, RP, p->d, 128)))
       return MOE_ERR_CUDA;
     return reset_error_word(p->err);
@@ -881,23 +878,21 @@ int moe_backward_mxfp8(moe_plan* p, const void* dy, const uint8_t* w13t, const u
     g.b_expert_rows = I;
     g.n_tiles = I / 128;
     g.in1 = p->a; g.ldi1 = 2LL * I;
-    g.out0 = p->dA; g.ld0 = 2LL * I;
-    g.out1 = p->hs; g.ld1 = I;
     g.row_scale = p->score_of;
     g.pdscore = p->pdscore;
     g.sfa = p->dysf; g.sfb = w2t_sf; g.sf_ngr = d / 128; g.b_blocks_per_expert = I / 128;
-    e = launch_gemm(EPI_DGRAD2, 128, false, false, p->tm_dyq, p->tm_w2t, p->tm_dyq, p->tm_dA,
-                    p->tm_hs, g, p->num_sms, st, true);
+    // dA and hs leave quantised: dA along 2I (the DGRAD-W13 operand), dA and hs
+    // along the rows (the WGRAD operands)
+    g.q_row = p->dAq; g.sf_row = p->dAsf; g.sf_row_ngr = 2 * I / 128;
+    g.qt_a = p->dAqT; g.sft_a = p->dAqTsf;
+    g.qt_h = p->hsqT; g.sft_h = p->hsqTsf;
+    g.qt_ld = RP;
+    // (the output maps are unused: this epilogue stores without TMA)
+    e = launch_gemm(EPI_DGRAD2, 128, false, false, p->tm_dyq, p->tm_w2t, p->tm_dyq, p->tm_dyq,
+                    p->tm_dyq, g, p->num_sms, st, true);
     if (e != cudaSuccess) return cuda_status(e);
     p->launches += 1;
   }
-  // b2'
-  if ((e = launch_quant_two_way(p->dA, nullptr, nrows, (int)RP, 2 * I, p->dAq, p->dAsf, p->dAqT,
-                                p->dAqTsf, p->num_sms, st)) != cudaSuccess ||
-      (e = launch_quant_rows_t(p->hs, nullptr, nrows, 1, (int)RP, I, p->hsqT, p->hsqTsf, st)) !=
-          cudaSuccess)
-    return cuda_status(e);
-  p->launches += 2;
   mark(p, 1, 2, st);
   // b3
   {
@@ -1120,6 +1115,12 @@ int moe_plan_buffer(const moe_plan* p, int which, void** ptr, size_t* bytes) {
     case MOE_BUF_HSF: q = p->hsf; b = (size_t)mx_sf_bytes((long long)RP, (int)I); break;
     case MOE_BUF_XQT: q = p->xqT; b = (size_t)d * RP; break;
     case MOE_BUF_XQTSF: q = p->xqTsf; b = (size_t)mx_sf_bytes((long long)d, (int)RP); break;
+    case MOE_BUF_DAQ: q = p->dAq; b = RP * 2 * I; break;
+    case MOE_BUF_DASF: q = p->dAsf; b = (size_t)mx_sf_bytes((long long)RP, (int)(2 * I)); break;
+    case MOE_BUF_DAQT: q = p->dAqT; b = 2 * I * RP; break;
+    case MOE_BUF_DAQTSF: q = p->dAqTsf; b = (size_t)mx_sf_bytes((long long)(2 * I), (int)RP); break;
+    case MOE_BUF_HSQT: q = p->hsqT; b = I * RP; break;
+    case MOE_BUF_HSQTSF: q = p->hsqTsf; b = (size_t)mx_sf_bytes((long long)I, (int)RP); break;
     default: return MOE_ERR_INVALID_ARG;
   }
   if (!q) return MOE_ERR_WORKSPACE;

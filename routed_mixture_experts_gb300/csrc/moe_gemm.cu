@@ -357,6 +357,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       } else if constexpr (EPI == EPI_WGRAD) {
         if (!epilogue_wgrad<BN, WB>(args, &tmC, ti, row, tbase, et, half, wp, &abort_s, wlim)) break;
+      } else if constexpr (MX && EPI == EPI_DGRAD2) {
+        static_assert(S::OUT_BYTES >= 8 * kD2WarpBytes, "per-warp staging");
+        epilogue_dgrad2_mx<BN>(args, ti, row, tbase, half, smem + STAGES * S::STAGE_BYTES, et);
       } else {
         epilogue<BN, EPI>(args, ti, row, tbase, half, &tmO0, &tmO1,
                           stage0 + STAGES * S::STAGE_BYTES, et, sub);

@@ -97,6 +97,31 @@ __device__ __forceinline__ float swiglu_fwd(float G, float U, float L) {
   return silu * U;
 }
 
+// SwiGLU backward of one element.  g: the DGRAD-W2 accumulator (dh before the
+// routing score s); G, U: the saved gate and up values (bf16, R1); L: clamp
+// limit (0 = plain).  Returns h * g (the score-gradient term, h as the forward
+// stored it, R2) and sets dgate, dup and hs = s * h, all before their bf16
+// rounding (R4, R7).
+__device__ __forceinline__ float swiglu_bwd(float g, float G, float U, float s, float L,
+                                            float& dgate, float& dup, float& hs) {
+  float mg = 1.f, mu = 1.f;
+  if (L > 0.f) {
+    if (G < -L || G > L) mg = 0.f;
+    if (U < -L || U > L) mu = 0.f;
+    G = fminf(fmaxf(G, -L), L);
+    U = fminf(fmaxf(U, -L), L);
+  }
+  const float sig = sigmoid_fast(G);
+  const float silu = G * sig;                   // as in swiglu_fwd
+  const float hv = bf2f(f2bf(silu * U));        // h (R2)
+  const float dh = s * g;
+  const float dsilu = sig * (1.0f + G * (1.0f - sig));
+  dgate = dh * U * dsilu * mg;
+  dup = dh * silu * mu;
+  hs = s * hv;
+  return hv * g;
+}
+
 // ---------------------------------------------------------------------------
 // epilogues: one thread owns one output row (`row` within the tile) and reads
 // its accumulator columns from TMEM at `tbase` (lane quarter already folded in).
@@ -426,28 +451,12 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, const TileInfo& ti, 
         for (int q = 0; q < 16; q += 2) {
           float dg2[2], du2[2], hs2[2];
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const float g = __uint_as_float(r0[q + u]);
-            float G = ag[q + u], U = au[q + u], mg = 1.f, mu = 1.f;
-            if (L > 0.f) {
-              if (G < -L || G > L) mg = 0.f;
-              if (U < -L || U > L) mu = 0.f;
-              G = fminf(fmaxf(G, -L), L);
-              U = fminf(fmaxf(U, -L), L);
-            }
-            const float sig = sigmoid_fast(G);
-            const float silu = G * sig;                   // as in swiglu_fwd
-            const float hv = bf2f(f2bf(silu * U));       // h (R2)
-            part += hv * g;
-            const float dh = s * g;
-            const float dsilu = sig * (1.0f + G * (1.0f - sig));
-            dg2[u] = dh * U * dsilu * mg;  // R4 on store
-            du2[u] = dh * silu * mu;
-            hs2[u] = s * hv;               // R7 on store
-          }
-          pk[0][8 * hh + q / 2] = pack_bf2(dg2[0], dg2[1]);
+          for (int u = 0; u < 2; ++u)
+            part += swiglu_bwd(__uint_as_float(r0[q + u]), ag[q + u], au[q + u], s, L, dg2[u],
+                               du2[u], hs2[u]);
+          pk[0][8 * hh + q / 2] = pack_bf2(dg2[0], dg2[1]);   // R4
           pk[1][8 * hh + q / 2] = pack_bf2(du2[0], du2[1]);
-          pk[2][8 * hh + q / 2] = pack_bf2(hs2[0], hs2[1]);
+          pk[2][8 * hh + q / 2] = pack_bf2(hs2[0], hs2[1]);   // R7
         }
       }
       epi_stage_three<tri_bufs<EPI_DGRAD2>()>(tmO0, tmO0, tmO1, out0, et, row, half, pk, ti.n0 + c,
@@ -456,6 +465,115 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, const TileInfo& ti, 
     // one partial per (n tile, column half)
     a.pdscore[grow * (2 * a.n_tiles) + 2 * ti.nt + half] = part;
   }
+}
+
+// DGRAD-W2 epilogue of the MXFP8 backward.  The SwiGLU backward as in
+// `epilogue`, but dA and hs leave only as E4M3 codes with E8M0 scales (their
+// bf16 values, R4 and R7, quantised; nothing reads bf16 copies):
+//  - dA along 2I: each thread quantises the 32-column blocks of its row;
+//  - dA and hs along the rows, transposed: a warp's 32 rows are one block.  The
+//    warp stages each 32 x 32 block of bf16 values in its own 4 KB of shared
+//    memory, each lane quantises one column of it, and the codes (32 bytes per
+//    column) go back through the same staging, so that the stores are
+//    coalesced.
+// Thread (row, half) takes columns [64c + 32*half, +32) of each 64-column chunk.
+constexpr int kD2ValLd = 80;    // staged bf16 row (64 bytes + 16: conflict-free 16-byte stores)
+constexpr int kD2CodeLd = 48;   // staged code row (32 bytes + 16)
+constexpr int kD2WarpBytes = 32 * kD2ValLd + 32 * kD2CodeLd;
+static_assert(kD2WarpBytes == 4096, "4 KB of staging per epilogue warp");
+
+template <int BN>
+__device__ __forceinline__ void epilogue_dgrad2_mx(const GemmArgs& a, const TileInfo& ti, int row,
+                                                   uint32_t tbase, int half, uint8_t* stg, int et) {
+  const int lane = row & 31;
+  const long long grow = (long long)ti.m0 + row;
+  const long long r32 = (long long)ti.m0 + (row & ~31);     // the warp's first row
+  uint8_t* vals = stg + (et >> 5) * kD2WarpBytes;              // [32 rows][kD2ValLd]
+  uint8_t* codes = vals + 32 * kD2ValLd;                       // [32 columns][kD2CodeLd]
+  const float s = a.row_scale[grow];
+  const float L = a.clamp;
+  const uint16_t* arow = static_cast<const uint16_t*>(a.in1) + grow * a.ldi1 + ti.n0;
+  float part = 0.f;
+#pragma unroll 1
+  for (int c = 0; c < BN; c += 64) {
+    const int cc0 = c + 32 * half;                             // this thread's 32 columns
+    uint32_t pw[3][16];                                        // bf16 pairs: dA gate, dA up, hs
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int cc = cc0 + 16 * hh;
+      uint32_t r0[16];
+      tmem_ld16(tbase + cc, r0);
+      const uint4* gp = reinterpret_cast<const uint4*>(arow + cc);
+      const uint4* up = reinterpret_cast<const uint4*>(arow + a.I + cc);
+      const uint4 g0 = gp[0], g1 = gp[1], u0 = up[0], u1 = up[1];
+      const uint32_t wg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+      const uint32_t wu[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        float dg2[2], du2[2], hs2[2];
+        part += swiglu_bwd(__uint_as_float(r0[2 * i]), __uint_as_float(wg[i] << 16),
+                           __uint_as_float(wu[i] << 16), s, L, dg2[0], du2[0], hs2[0]);
+        part += swiglu_bwd(__uint_as_float(r0[2 * i + 1]), __uint_as_float(wg[i] & 0xFFFF0000u),
+                           __uint_as_float(wu[i] & 0xFFFF0000u), s, L, dg2[1], du2[1], hs2[1]);
+        pw[0][8 * hh + i] = pack_bf2(dg2[0], dg2[1]);   // R4
+        pw[1][8 * hh + i] = pack_bf2(du2[0], du2[1]);
+        pw[2][8 * hh + i] = pack_bf2(hs2[0], hs2[1]);   // R7
+      }
+    }
+    // dA along 2I: this row's 32-column block of the gate half and of the up half
+#pragma unroll
+    for (int o = 0; o < 2; ++o) {
+      float f[32];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        f[2 * i] = __uint_as_float(pw[o][i] << 16);
+        f[2 * i + 1] = __uint_as_float(pw[o][i] & 0xFFFF0000u);
+      }
+      uint32_t w[8];
+      const uint8_t sc = mx_quant32(f, w);
+      const int col = (o ? a.I : 0) + ti.n0 + cc0;
+      uint4* dst = reinterpret_cast<uint4*>(a.q_row + grow * (2LL * a.I) + col);
+      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      a.sf_row[mx_sf_offset(grow >> 7, (int)(grow & 127), col >> 5, a.sf_row_ngr)] = sc;
+    }
+    // dA gate, dA up and hs along the rows: the warp's 32 x 32 blocks
+#pragma unroll
+    for (int o = 0; o < 3; ++o) {
+      uint4* vr = reinterpret_cast<uint4*>(vals + lane * kD2ValLd);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        vr[j] = make_uint4(pw[o][4 * j], pw[o][4 * j + 1], pw[o][4 * j + 2], pw[o][4 * j + 3]);
+      __syncwarp();
+      float f[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        f[i] = __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(vals + i * kD2ValLd)[lane]
+                               << 16);
+      uint32_t w[8];
+      const uint8_t sc = mx_quant32(f, w);
+      __syncwarp();                     // every lane has read the block
+      uint4* cr = reinterpret_cast<uint4*>(codes + lane * kD2CodeLd);
+      cr[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      cr[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      __syncwarp();
+      const long long colbase = (o == 1 ? a.I : 0) + ti.n0 + cc0;
+      uint8_t* qt = o < 2 ? a.qt_a : a.qt_h;
+      uint8_t* sft = o < 2 ? a.sft_a : a.sft_h;
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const int p = lane + 32 * t, col = p >> 1, hf = p & 1;
+        *reinterpret_cast<uint4*>(qt + (colbase + col) * a.qt_ld + r32 + 16 * hf) =
+            *reinterpret_cast<const uint4*>(codes + col * kD2CodeLd + 16 * hf);
+      }
+      const long long cl = colbase + lane;
+      sft[mx_sf_offset(cl >> 7, (int)(cl & 127), (int)(r32 >> 5), (int)(a.qt_ld / 128))] = sc;
+      __syncwarp();                     // the staging is rewritten next round
+    }
+  }
+  // one partial per (n tile, column half)
+  a.pdscore[grow * (2 * a.n_tiles) + 2 * ti.nt + half] = part;
 }
 
 // WGRAD epilogue: read-modify-write of the fp32 gradient, 32 columns (16 KB:

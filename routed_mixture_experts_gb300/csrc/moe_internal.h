@@ -88,6 +88,18 @@ struct GemmArgs {
   uint8_t* hq;               // EPI_SWIGLU (MXFP8): h quantised along I, codes [rows, I]
   uint8_t* hsf;              // ... and its tiled scales
   int hsf_ngr;
+  // EPI_DGRAD2 (MXFP8): dA and hs leave only as E4M3 codes with tiled scales: dA
+  // along 2I (q_row [rows, 2I], sf_row with sf_row_ngr K groups), dA and hs along
+  // the rows, transposed (qt_a [2I, qt_ld], qt_h [I, qt_ld]; scales sft_a, sft_h
+  // with qt_ld/128 K groups)
+  uint8_t* q_row;
+  uint8_t* sf_row;
+  int sf_row_ngr;
+  uint8_t* qt_a;
+  uint8_t* sft_a;
+  uint8_t* qt_h;
+  uint8_t* sft_h;
+  long long qt_ld;
   // failure-path testing: every bounded wait gives up after wait_limit_ns (0 =
   // default); stall_mma = 1 makes the MMA role first wait on a barrier that
   // nothing arrives at, so the timeout path runs
