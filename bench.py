@@ -24,6 +24,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -101,13 +102,25 @@ def peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+_TOKEN = re.compile(r'"(?:\\.|[^"\\])*"' r"|'(?:\\.|[^'\\])*'" r"|//[^\n]*|/\*.*?\*/", re.S)
+
+
+def _code_only(src):
+    """C/C++ source without its comments and blank space: what the compiler sees
+    (string and character literals are kept as they are)."""
+    out = _TOKEN.sub(lambda m: " " if m.group(0)[0] == "/" else m.group(0), src)
+    return " ".join(out.split())
+
+
 def kernel_source_hash():
+    """Hash of the CUDA sources' code (comments and layout excluded), so that a
+    committed counter taken on the same kernels stays valid across comment edits."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "routed_mixture_experts_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(f.read())
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                h.update(name.encode() + b"\0" + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -44,8 +44,9 @@ struct GemmShape {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SF_STAGE_BYTES;
   static constexpr int TX_BYTES = A_BYTES + B_BYTES + SF_LOAD_BYTES;   // bytes a stage receives
   // Output staging: WGRAD's fp32 buffers (it needs few stages: its K loop is one
-  // expert's rows and it is bound by the gradient traffic), else two bf16
-  // sub-tile buffers for the TMA-store epilogues.
+  // expert's rows and it is bound by the gradient traffic), else bf16 sub-tile
+  // buffers for the TMA-store epilogues (the MXFP8 DGRAD-W2 epilogue uses the
+  // same 32 KB as 4 KB of staging per epilogue warp).
   static constexpr int OUT_BYTES =
       (EPI == EPI_WGRAD ? wgrad_bufs<MX>()
                         : (MX && BN == 256 ? kMxWideBufs

@@ -75,3 +75,19 @@ def test_stage_model_counts_the_method_flops():
     bwd = sum(m[s][1] for s in ("dgrad_w2_swiglu", "dgrad_w13", "wgrad_w2", "wgrad_w13"))
     assert fwd == 6 * R * 2048 * 768
     assert fwd + bwd == 18 * R * 2048 * 768
+
+
+def test_kernel_hash_ignores_comments_only():
+    """The committed DRAM counters stay tied to the kernels' code: a comment or
+    layout edit keeps the hash, a code edit (also inside a string) changes it."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    a = 'int f(int x) { // twice\n  return 2 * x; /* no\n overflow */ }\nconst char* s = "// kept";\n'
+    b = 'int f(int x) {\n    return 2 * x;\n}\nconst char* s = "// kept";  // the same code\n'
+    c = 'int f(int x) { return 3 * x; }\nconst char* s = "// kept";\n'
+    d = 'int f(int x) { return 2 * x; }\nconst char* s = "// changed";\n'
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(c)
+    assert bench._code_only(a) != bench._code_only(d)
+    assert "kept" in bench._code_only(a)
