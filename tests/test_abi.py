@@ -111,3 +111,23 @@ def test_cta_pairs_option_sizes_the_workspace(L):
     finally:
         for x in (p, q, m):
             L.moe_plan_destroy(x)
+
+
+def test_mxfp8_training_workspace_keeps_dA_and_hs_only_as_codes(L):
+    """An MXFP8 training plan adds the saved a, dX_e, the score-gradient partials
+    and the E4M3 operands of the backward (dY and dA along K, dY, dA, hs and x
+    along the rows, each with 1/32 of scale bytes), but no bf16 dA or hs
+    (6*Rpad*I bytes)."""
+    T, d, I, E, k = 8192, 2048, 768, 128, 8
+    p = L.moe_plan_create(T, d, I, E, k, 1)
+    assert p
+    try:
+        extra = L.moe_plan_workspace_bytes(p, 1) - L.moe_plan_workspace_bytes(p, 0)
+        R, BM = T * k, L.moe_tile_rows()
+        RP = (R + E * (BM - 1)) // BM * BM
+        codes = RP * (d + 2 * I) + RP * (d + 2 * I + I + d)
+        expected = 2 * RP * 2 * I + 2 * RP * d + 4 * RP * 2 * (I // 128) + codes * 33 // 32
+        assert expected - (1 << 20) <= extra <= expected + (1 << 20)
+        assert extra < expected + 6 * RP * I - (1 << 20)
+    finally:
+        L.moe_plan_destroy(p)
