@@ -78,7 +78,10 @@ typedef struct moe_plan moe_plan;
  *   d % 128 == 0, I % 64 == 0, 1 <= k <= E <= 256, T >= 1, T*k < 2^31.
  * Returns a host-side plan object (owned by the caller, free with
  * moe_plan_destroy) or NULL on invalid arguments.  Does not touch the GPU
- * except to query the current device's properties.
+ * except to query the current device's properties.  A plan belongs to the
+ * device current at creation (its grids are sized for that device's SMs): make
+ * that device current for every later call with the plan.  Plans on different
+ * devices may be used from different host threads at once.
  */
 moe_plan* moe_plan_create(int T, int d, int I, int E, int k, int precision);
 

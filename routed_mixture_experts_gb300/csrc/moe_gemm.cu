@@ -393,12 +393,9 @@ cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUten
                        int grid, cudaStream_t stream) {
   auto kern = k_grouped_gemm<BN, A_MN, B_MN, EPI, MX>;
   const int smem = GemmShape<BN, EPI, MX>::SMEM_BYTES;
-  static bool configured = false;   // attribute set once per process (same device image)
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<unsigned long long> configured{0};   // devices this kernel is set up on
+  const cudaError_t e = smem_optin_once(kern, smem, configured);
+  if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, stream, ta, tb, tc, to0, to1, args);
 }
 

@@ -301,7 +301,8 @@ cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
                         cudaStream_t stream) {
   auto kern = k_grouped_gemm_2sm<B_MN, EPI>;
   constexpr int smem = PairShape<EPI>::SMEM;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static std::atomic<unsigned long long> configured{0};   // devices this kernel is set up on
+  const cudaError_t e = smem_optin_once(kern, smem, configured);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(grid & ~1), dim3(kThreads), smem, stream, ta, tb, to0, to1, args);
 }

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <atomic>
 #include <utility>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -13,6 +14,22 @@ namespace moe {
 // Launch with programmatic stream serialization (see pdl_wait / pdl_trigger in
 // moe_device.cuh): the kernel may be scheduled while the previous kernel of the
 // stream finishes, and waits for it in pdl_wait().
+// Opt `kernel` in to `bytes` of dynamic shared memory on the current device.
+// The attribute belongs to the kernel on one device, so it is set once per
+// device: `done` holds one bit per device (devices 64 and up set it every time).
+template <typename... KArgs>
+inline cudaError_t smem_optin_once(void (*kernel)(KArgs...), int bytes,
+                                   std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev >= 0 && dev < 64 ? 1ull << dev : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
+
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                               cudaStream_t stream, Args&&... args) {

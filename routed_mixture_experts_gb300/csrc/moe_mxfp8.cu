@@ -349,13 +349,9 @@ cudaError_t launch_quant_two_way(const void* in, const int32_t* src_row, const i
                                  uint8_t* codes_t, uint8_t* sf_t, int num_sms,
                                  cudaStream_t stream) {
   if (R % 128 || C % 128 || num_sms < 1) return cudaErrorInvalidValue;
-  static bool configured = false;   // attribute set once per process
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(k_quant_two_way,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kTwSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<unsigned long long> configured{0};   // devices the kernel is set up on
+  const cudaError_t e = smem_optin_once(k_quant_two_way, kTwSmem, configured);
+  if (e != cudaSuccess) return e;
   // persistent: a few CTAs per SM, at most one per tile
   const long long tiles = (long long)(R / kTwRows) * ((C + kQtCols - 1) / kQtCols);
   const int grid = (int)(tiles < (long long)num_sms * kTwCtasPerSm ? tiles
