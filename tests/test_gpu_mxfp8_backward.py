@@ -78,7 +78,11 @@ def oracle_weights(orc, inp, experts=None):
     dict(T=300, d=256, I=256, E=7, k=3),
     dict(T=200, d=384, I=128, E=9, k=2, clamp=1.0, pad=30),
     dict(T=400, d=128, I=128, E=12, k=3, routing="zipf", zipf_s=1.2, zipf_support=8),
-], ids=["tiny", "ragged", "clamped_pad", "skew_empty"])
+    # degenerate routing: one token; k = 8 of 256 experts (most experts hold a few
+    # rows, so most 32-row blocks along the rows are mostly padding)
+    dict(T=1, d=128, I=128, E=4, k=2),
+    dict(T=96, d=128, I=128, E=256, k=8),
+], ids=["tiny", "ragged", "clamped_pad", "skew_empty", "one_token", "k8_e256"])
 def test_mxfp8_backward_small(moe, orc, sizes):
     inp = mi.make_inputs(None, seed=23, need=NEED, **sizes)
     c = inp["cfg"]
