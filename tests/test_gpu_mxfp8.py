@@ -72,7 +72,10 @@ def run_mx(moe, inp, dev, prep):
     dict(T=64, d=128, I=128, E=4, k=2),
     dict(T=300, d=256, I=256, E=7, k=3),
     dict(T=200, d=384, I=128, E=9, k=2, clamp=1.0, pad=30),
-])
+    dict(T=400, d=128, I=128, E=12, k=3, routing="zipf", zipf_s=1.2, zipf_support=8),
+    dict(T=1, d=128, I=128, E=4, k=2),
+    dict(T=96, d=128, I=128, E=256, k=8),
+], ids=["tiny", "ragged", "clamped_pad", "skew_empty", "one_token", "k8_e256"])
 def test_mxfp8_small(moe, orc, sizes):
     inp = mi.make_inputs(None, seed=21, need=("x", "ids", "scores", "w13", "w2"), **sizes)
     c = inp["cfg"]
