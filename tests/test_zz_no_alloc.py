@@ -60,7 +60,9 @@ def _static_dispatch(moe, dev, T, k, E):
 @pytest.mark.parametrize("sizes", [
     dict(T=300, d=128, I=64, E=7, k=3),
     dict(T=2048, d=128, I=64, E=128, k=8, routing="zipf", zipf_s=1.2, zipf_support=102),
-])
+    # at the static scratch's capacity: T*k = MOE_STATIC_MAX_ROUTED, E = 256
+    dict(T=32768, d=128, I=64, E=256, k=8),
+], ids=["ragged", "skew_e128", "at_capacity"])
 def test_static_dispatch_matches_plan_dispatch(moe, sizes):
     cases = [make(None, seed=s, train=False, **sizes) for s in (11, 12)]
     for inp in cases:                     # two calls in a row, different routings
