@@ -87,3 +87,18 @@ def test_skew_pad_forward_backward(moe, orc):
     empty = torch.from_numpy(np.flatnonzero(counts == 0)).cuda()
     assert torch.equal(g["dw13"][empty], g["dev"]["dw13"][empty])
     assert torch.equal(g["dw2"][empty], g["dev"]["dw2"][empty])
+
+
+def test_train_e256_forward_backward(moe, orc):
+    """The plan's largest expert count (E = 256, k = 8) at the full d and I: about
+    256 routed rows per expert, so most experts end in a part-filled m tile."""
+    inp = make(None, seed=31, train=True, T=8192, d=2048, I=768, E=256, k=8)
+    c = inp["cfg"]
+    g = run_gpu(moe, inp, train=True)
+    assert g["rc"] == 0
+    check_dispatch(orc, inp, g)
+    assert np.all(np.isfinite(f32(bits(g["y"])))) and np.all(np.isfinite(f32(bits(g["dx"]))))
+    toks = _sample_tokens(c["T"], 12, 4, must=(0, c["T"] - 1))
+    check_forward(orc, inp, g, toks=toks)
+    experts = _sample_experts(inp["ids"], c["E"], include_empty=False)
+    check_backward(orc, inp, g, toks=toks, experts=experts)
