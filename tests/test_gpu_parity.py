@@ -234,3 +234,45 @@ def test_mxfp8_quantiser_bit_exact(moe, orc):
     torch.cuda.synchronize()
     assert np.array_equal(gc.cpu().numpy(), codes)
     assert np.array_equal(gs.cpu().numpy(), scales)
+
+
+def _bf16_bits(a):
+    return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16) \
+        .view(torch.int16).numpy().view(np.uint16)
+
+
+def test_clamp_gradient_boundary(moe, orc):
+    """Clamped SwiGLU on the GPU: where the bf16 pre-activation is exactly -L or
+    L the gradient passes, one bf16 step outside it is exactly zero (the oracle
+    takes the same decisions, pinned on the CPU).  x = e_0 with one expert, so
+    every gate and up value is one weight exactly."""
+    T, d, I, E, k, L = 1, 128, 64, 1, 1, 1.0
+    out = 1.0078125                         # the bf16 value just above 1.0
+    gate = np.full(I, 0.5)
+    up = np.full(I, 0.5)
+    gate[[0, 1, 2, 3]] = [L, -L, out, -out]
+    up[[4, 5, 6, 7]] = [L, -L, out, -out]
+    x = np.zeros((T, d), np.float32)
+    x[0, 0] = 1.0
+    w13 = np.zeros((E, 2 * I, d), np.float32)
+    w13[0, :I, 0] = gate
+    w13[0, I:, 0] = up
+    rng = np.random.default_rng(7)
+    inp = dict(x=_bf16_bits(x), ids=np.zeros((T, k), np.int32),
+               scores=np.ones((T, k), np.float32), w13=_bf16_bits(w13),
+               w2=_bf16_bits(rng.normal(0, I ** -0.5, (E, d, I))),
+               dy=_bf16_bits(rng.normal(0, 1, (T, d))),
+               dw13=np.zeros((E, 2 * I, d), np.float32), dw2=np.zeros((E, d, I), np.float32),
+               cfg=dict(T=T, d=d, I=I, E=E, k=k, clamp=L))
+    g = run_gpu(moe, inp, train=True)
+    assert g["rc"] == 0
+    dA = f32(bits(g["plan"].buffer("dA", torch.bfloat16)))[: 2 * I].astype(np.float64)
+    dg, du = dA[:I], dA[I:]
+    assert np.all(dg[[2, 3]] == 0) and np.all(du[[6, 7]] == 0)
+    _, _, bi = orc.backward(inp["x"], inp["ids"], inp["scores"], inp["w13"], inp["w2"],
+                            inp["dy"], clamp=L, intermediates=True)
+    ref = f32(bi["dA"])[0, 0].astype(np.float64)
+    for i in (0, 1, 8):
+        assert dg[i] != 0 and abs(dg[i] - ref[i]) <= 2.0 ** -7 * abs(ref[i]), i
+    for i in (4, 5, 8):
+        assert du[i] != 0 and abs(du[i] - ref[I + i]) <= 2.0 ** -7 * abs(ref[I + i]), i

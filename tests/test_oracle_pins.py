@@ -276,6 +276,52 @@ def test_backward_matches_fp64_autograd(orc, clamp):
         assert _rel_fro(d2, ref["dw2"][e]) < 2e-2
 
 
+def test_clamp_gradient_boundary(orc):
+    """Clamped SwiGLU (limit L): the gradient passes where the bf16 pre-activation
+    equals -L or L exactly and is exactly zero one bf16 step outside; where it
+    passes it is the closed form dh*U*sigma(G)*(1 + G*(1 - sigma(G))) (gate) or
+    dh*silu(G)*[G clamped] (up), rounded to bf16.  One token, one expert, x = e_0,
+    so every gate and up value is one weight exactly."""
+    d, I, L = 64, 32, 1.0
+    out = 1.0078125                         # the bf16 value just above 1.0
+    gate = np.full(I, 0.5)
+    up = np.full(I, 0.5)
+    gate[[0, 1, 2, 3]] = [L, -L, out, -out]
+    up[[4, 5, 6, 7]] = [L, -L, out, -out]
+    x = np.zeros((1, d), np.float32)
+    x[0, 0] = 1.0
+    w13 = np.zeros((1, 2 * I, d), np.float32)
+    w13[0, :I, 0] = gate
+    w13[0, I:, 0] = up
+    rng = np.random.default_rng(5)
+    w2 = rng.normal(0, I ** -0.5, (1, d, I)).astype(np.float32)
+    dy = rng.normal(0, 1, (1, d)).astype(np.float32)
+    ids = np.zeros((1, 1), np.int32)
+    scores = np.ones((1, 1), np.float32)
+    args = (bits(x), ids, scores, bits(w13), bits(w2), bits(dy))
+    _, _, it = orc.backward(*args, clamp=L, intermediates=True)
+    dA = f32(it["dA"])[0, 0].astype(np.float64)
+    dg, du = dA[:I], dA[I:]
+    dh = it["g"][0, 0].astype(np.float64)           # score 1: dh = g
+    assert np.all(dh[:8] != 0)
+    assert np.all(dg[[2, 3]] == 0) and np.all(du[[6, 7]] == 0)
+    G = np.clip(gate, -L, L)
+    U = np.clip(up, -L, L)
+    sig = 1.0 / (1.0 + np.exp(-G))
+    ref_g = dh * U * sig * (1.0 + G * (1.0 - sig))
+    ref_u = dh * G * sig
+    for i in (0, 1, 8):                             # gate at +L, -L, inside
+        assert dg[i] != 0 and abs(dg[i] - ref_g[i]) <= 2.0 ** -7 * abs(ref_g[i]), i
+    for i in (4, 5, 8):                             # up at +L, -L, inside
+        assert du[i] != 0 and abs(du[i] - ref_u[i]) <= 2.0 ** -7 * abs(ref_u[i]), i
+    # outside the interval the forward uses the clamped value
+    _, fi = orc.forward(*args[:5], clamp=L, intermediates=True)
+    h = f32(fi["h"])[0, 0].astype(np.float64)
+    silu_L = L / (1.0 + np.exp(-L))
+    assert abs(h[2] - silu_L * 0.5) <= 2.0 ** -8 * silu_L * 0.5
+    assert h[2] == h[0]                             # G = out clamps to the same L
+
+
 def test_dscores_linearity_invariant(orc):
     """y is linear in each score, so dscores[t,j] = <dY_t, o_j> where o_j = ys_j / s_j."""
     inp = small(T=12, d=64, I=32, E=4, k=2, seed=4)
