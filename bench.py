@@ -39,6 +39,7 @@ METRIC = "routed-expert TFLOP/s (fwd; fwd+bwd) at T=8192 E=128 k=8; % of GB300 t
 WORKLOAD = "train_e128"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_OVER_BF16 = 2.0    # nominal dense E4M3 / bf16 tensor throughput ratio (4.5 / 2.25 PFLOP/s)
+NOMINAL_HBM_GBS = 8000.0   # nominal HBM3e bandwidth of the part (~8 TB/s), beside the measured copy rate
 
 FWD_STAGES = ["dispatch", "gather_x", "w13_swiglu", "w2_score", "combine_y"]
 BWD_STAGES = ["gather_dy", "dgrad_w2_swiglu", "dgrad_w13", "combine_dx", "wgrad_w2", "wgrad_w13"]
@@ -64,6 +65,9 @@ def parse():
                     help="time the steps as one CUDA graph replay (stage events as graph nodes)")
     ap.add_argument("--cta-pairs", action="store_true",
                     help="W13, W2 and DGRAD-W13 on CTA pairs (moe_plan_set_cta_pairs)")
+    ap.add_argument("--extra-steps", type=int, default=30,
+                    help="timed steps of the inference (E=16) and skewed-routing workloads "
+                         "(0: skip)")
     return ap.parse_args()
 
 
@@ -100,6 +104,35 @@ def peaks():
         return {k: float(m[k]) for k in FALLBACK_PEAKS}, "measured"
     except Exception:
         return dict(FALLBACK_PEAKS), "fallback"
+
+
+def tensor_peak(pk, clk):
+    """bf16 tensor peak for kernels timed here: the burst figure while the clock
+    record shows no power capping, the sustained (power-capped) one otherwise."""
+    capped = clk is None or "sw_power_cap" in (clk.get("reasons") or [])
+    if capped:
+        return pk["bf16_tflops_sustained"], "sustained bf16 (%s)" % (
+            "power cap active" if clk else "no clock record")
+    return pk["bf16_tflops"], "burst bf16 (no power cap in the clock record)"
+
+
+def stage_table(model, stage_ms, tpeak, hbm_peak):
+    """Per stage: time, roofline bound, achieved rate and fraction of its peak
+    (and, for HBM-bound stages, of the nominal HBM bandwidth)."""
+    out = {}
+    for name, t_ms in stage_ms.items():
+        bound, fl, by = model[name]
+        if bound == "tensor":
+            ach, peak, unit = fl / (t_ms * 1e-3) / 1e12, tpeak, "TFLOP/s"
+        else:
+            ach, peak, unit = by / (t_ms * 1e-3) / 1e9, hbm_peak, "GB/s"
+        ent = {"ms": round(t_ms, 5), "bound": bound, "achieved": round(ach, 1), "peak": peak,
+               "unit": unit, "frac": round(ach / peak, 4),
+               "tflops": round(fl / (t_ms * 1e-3) / 1e12, 1) if fl else None}
+        if bound == "hbm":
+            ent["frac_nominal_hbm"] = round(ach / NOMINAL_HBM_GBS, 4)
+        out[name] = ent
+    return out
 
 
 _TOKEN = re.compile(r'"(?:\\.|[^"\\])*"' r"|'(?:\\.|[^'\\])*'" r"|//[^\n]*|/\*.*?\*/", re.S)
@@ -416,31 +449,28 @@ def run_ours(args):
     value = flops_step * ws / (ms_step * 1e-3) / 1e12
     dom_timed_ms = sum(a_.elapsed_time(b_) for a_, b_ in ed) / K
 
-    # roofline of every stage; the dominant one is reported as "roofline"
+    # roofline of every stage; the dominant one is reported as "roofline".  Tensor
+    # peak: burst unless the clock record of the timed region shows power capping
     pk, pk_src = peaks()
+    tpeak, tpeak_src = tensor_peak(pk, clk)
     model = stage_model(c)
-    stages = {}
-    for name, t_ms in stage_ms.items():
-        bound, fl, by = model[name]
-        if bound == "tensor":
-            ach, peak, unit = fl / (t_ms * 1e-3) / 1e12, pk["bf16_tflops_sustained"], "TFLOP/s"
-        else:
-            ach, peak, unit = by / (t_ms * 1e-3) / 1e9, pk["hbm_gbs"], "GB/s"
-        stages[name] = {"ms": round(t_ms, 5), "bound": bound, "achieved": round(ach, 1),
-                        "peak": peak, "unit": unit, "frac": round(ach / peak, 4),
-                        "tflops": round(fl / (t_ms * 1e-3) / 1e12, 1) if fl else None}
+    stages = stage_table(model, stage_ms, tpeak, pk["hbm_gbs"])
     # the dominant kernel's roofline from its events in the timed region
     bound, fl, by = model[dom]
     if bound == "tensor":
-        d_ach, d_peak = fl / (dom_timed_ms * 1e-3) / 1e12, pk["bf16_tflops_sustained"]
+        d_ach, d_peak = fl / (dom_timed_ms * 1e-3) / 1e12, tpeak
         d_unit = "TFLOP/s"
     else:
         d_ach, d_peak, d_unit = by / (dom_timed_ms * 1e-3) / 1e9, pk["hbm_gbs"], "GB/s"
     roofline = {"kernel": dom, "bound": bound, "achieved": round(d_ach, 1), "peak": d_peak,
                 "unit": d_unit, "frac": round(d_ach / d_peak, 4), "ms": round(dom_timed_ms, 5),
                 "traffic": traffic_for(dom),
-                "peak_source": "%s (%s)" % (pk_src, "sustained bf16" if bound == "tensor"
+                "peak_source": "%s (%s)" % (pk_src, tpeak_src if bound == "tensor"
                                             else "copy bandwidth")}
+    if bound == "hbm":
+        roofline["frac_nominal_hbm"] = round(d_ach / NOMINAL_HBM_GBS, 4)
+    peak_note = {"tensor": tpeak_src, "tensor_peak": tpeak, "hbm": "measured copy bandwidth",
+                 "hbm_peak": pk["hbm_gbs"], "nominal_hbm": NOMINAL_HBM_GBS, "source": pk_src}
 
     # end to end through the C ABI with pinned host buffers (copies in the timed region)
     e2e = None
@@ -542,7 +572,7 @@ def run_ours(args):
         if rc != 0:
             raise RuntimeError("device error %d (%d) in the MXFP8 forward" % (rc, det))
         mms = max_over_ranks(m0.elapsed_time(m1), dev) / args.mx_steps
-        fp8_peak = pk["bf16_tflops_sustained"] * FP8_OVER_BF16
+        fp8_peak = tpeak * FP8_OVER_BF16
         mst = {}
         for j, name in enumerate(FWD_STAGES):
             t_ms = sum(mev[i][j].elapsed_time(mev[i][j + 1]) for i in range(args.mx_steps)) / args.mx_steps
@@ -556,7 +586,7 @@ def run_ours(args):
         mx = {"workload": "mxfp8_e128 (same sizes and inputs, E4M3 block-scaled forward)",
               "value": 6.0 * T * k * d * I * ws / (mms * 1e-3) / 1e12, "unit": "TFLOP/s",
               "ms_per_step": mms, "steps": args.mx_steps,
-              "peak_note": "fp8 peak = measured sustained bf16 x 2 (nominal ratio)", "stages": mst}
+              "peak_note": "fp8 peak = %s x 2 (nominal ratio)" % tpeak_src, "stages": mst}
         del mplan
 
         # MXFP8 training step: saving forward + block-scaled backward
@@ -604,6 +634,11 @@ def run_ours(args):
                     "ms_per_step": tms, "steps": args.mx_steps, "stages": tst}
         del tplan
 
+    extra = {}
+    if args.extra_steps > 0:
+        for name, train in (("infer_e16", False), ("skew_pad", True)):
+            extra[name] = run_extra(moe, name, train, args, dev, ws, tpeak, pk)
+
     if rank != 0:
         return
     cpu = None
@@ -636,9 +671,105 @@ def run_ours(args):
         "e2e": e2e, "gpu_launches": int(n1 - n0), "roofline": roofline, "stages": stages,
         "stages_note": "%d untimed steps with an event at every stage boundary; the timed steps "
                        "record only the dominant stage's events" % KB,
-        "cpu_baseline": cpu, "clocks": clk, "mxfp8_forward": mx, "mxfp8_training": mx_train,
+        "cpu_baseline": cpu, "clocks": clk, "peaks": peak_note, "mxfp8_forward": mx,
+        "mxfp8_training": mx_train, "infer_e16": extra.get("infer_e16"),
+        "skew_pad": extra.get("skew_pad"),
     }
     print(json.dumps(line), flush=True)
+
+
+def run_extra(moe, name, train, args, dev, ws, tpeak, pk):
+    """Throughput of another workload of the method: the bf16 inference forward at
+    E = 16 (forward only) or the skewed-routing training step (Zipf routing,
+    zero-score padding tokens, clamped SwiGLU).  A timed loop without stage events
+    gives the value; a separate pass with an event at every stage boundary gives
+    the stage table."""
+    import numpy as np
+    import torch
+
+    import moe_inputs as mi
+
+    _, rank, _ = dist_env()
+    need = ("x", "ids", "scores", "w13", "w2") + (("dy", "dw13", "dw2") if train else ())
+    inp = mi.make_inputs(name, seed=args.seed + rank, need=need)
+    c = inp["cfg"]
+    T, d, I, E, k = c["T"], c["d"], c["I"], c["E"], c["k"]
+
+    def to_dev(a):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        if a.dtype == np.uint16:
+            t = t.view(torch.bfloat16)
+        return t.to(dev)
+
+    D = {key: to_dev(inp[key]) for key in need}
+    del inp
+    plan = moe.MoePlan(T, d, I, E, k, clamp=c["clamp"],
+                       flags=moe.MOE_WS_TRAINING if train else 0, device=dev)
+    y = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+    if train:
+        dx = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+        dsc = torch.empty(T, k, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        plan.forward(D["x"], D["ids"], D["scores"], D["w13"], D["w2"], y=y, save=train)
+        if train:
+            plan.backward(D["dy"], D["w13"], D["w2"], D["dw13"], D["dw2"], dx=dx, dscores=dsc)
+
+    for _ in range(args.warmup):
+        step()
+    K = args.extra_steps
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(K):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(t0.elapsed_time(t1), dev) / K
+    evf = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    evb = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(K)]
+    for ev in [e for s_ in evf + evb for e in s_]:
+        ev.record(stream)
+    torch.cuda.synchronize()
+    for i in range(K):
+        plan.set_timing_events(0, evf[i])
+        if train:
+            plan.set_timing_events(1, evb[i])
+        step()
+    torch.cuda.synchronize()
+    plan.set_timing_events(0, None)
+    plan.set_timing_events(1, None)
+    rc, det = plan.check()
+    if rc != 0:
+        raise RuntimeError("device error %d (%d) in %s" % (rc, det, name))
+    stage_ms = {}
+    for j, st_ in enumerate(FWD_STAGES):
+        stage_ms[st_] = sum(evf[i][j].elapsed_time(evf[i][j + 1]) for i in range(K)) / K
+    if train:
+        for j, st_ in enumerate(BWD_STAGES):
+            stage_ms[st_] = sum(evb[i][j].elapsed_time(evb[i][j + 1]) for i in range(K)) / K
+    model = stage_model(c)
+    if not train:
+        # an inference forward does not store a
+        b, fl, by = model["w13_swiglu"]
+        model["w13_swiglu"] = (b, fl, by - 4 * T * k * I)
+    stages = stage_table(model, stage_ms, tpeak, pk["hbm_gbs"])
+    flops = (18.0 if train else 6.0) * T * k * d * I
+    counts = np.bincount(D["ids"].cpu().numpy().reshape(-1), minlength=E)
+    desc = ("%s (T=%d, d=%d, I=%d, E=%d, k=%d, %s routing%s%s, %s)"
+            % (name, T, d, I, E, k, c["routing"],
+               ", last %d tokens zero-score padding" % c["pad"] if c["pad"] else "",
+               ", SwiGLU clamped to +-%g" % c["clamp"] if c["clamp"] else "",
+               "forward+backward" if train else "forward"))
+    out = {"workload": desc, "value": flops * ws / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+           "ms_per_step": ms, "steps": K, "stages": stages,
+           "rows_per_expert": {"max": int(counts.max()), "median": float(np.median(counts)),
+                               "empty": int((counts == 0).sum())}}
+    del plan, D
+    torch.cuda.empty_cache()
+    return out
 
 
 def main():

@@ -361,9 +361,13 @@ long long moe_plan_launch_count(const moe_plan* plan);
  * floor((T*k + E*(BM-1)) / BM) * BM (else MOE_ERR_INVALID_ARG).
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current: make that first call before
- * any stream capture.  All calls on a device share the one array, which keeps
- * the last call's contents (the error word is cleared at the start of each
- * call): calls whose work overlaps on the GPU race and must not be issued.
+ * any stream capture.  The address is kept per device and CUDA context: the
+ * first call from another context on the device (a non-primary context, or the
+ * primary context re-created after cudaDeviceReset) looks it up again and is a
+ * first call in the same sense.  All calls on a device share the one array,
+ * which keeps the last call's contents (the error word is cleared at the start
+ * of each call): calls whose work overlaps on the GPU (for example on two
+ * streams) race and must not be issued.
  */
 #define MOE_STATIC_MAX_ROUTED 262144
 int moe_dispatch_static(const int32_t* ids, const float* scores, int T, int k, int E,

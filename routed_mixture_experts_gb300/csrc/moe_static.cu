@@ -14,9 +14,12 @@
 // Properties of the static scratch:
 //   - every GPU that loads this library holds the array (about 280 KB) until the
 //     process exits;
-//   - its device address is looked up once per device, by the first call made
-//     with that device current (cudaGetSymbolAddress); make that first call
-//     before any stream capture;
+//   - its device address is looked up once per device and CUDA context, by the
+//     first call made with that device current (cudaGetSymbolAddress); make that
+//     first call before any stream capture.  A call from another context on the
+//     same device (a non-primary context, or the primary one re-created after
+//     cudaDeviceReset) looks the address up again, in that context, so it is
+//     also a first call;
 //   - every call on a device shares the one array and it keeps the last call's
 //     contents: the error word is cleared at the start of each call, everything
 //     else is fully rewritten; calls whose kernels overlap on the GPU (for
@@ -24,6 +27,8 @@
 
 #include <climits>
 #include <mutex>
+
+#include <cudaTypedefs.h>
 
 #include "../../include/moe.h"
 #include "moe_device.cuh"
@@ -51,7 +56,37 @@ constexpr size_t kWords = kOffChunks + (size_t)kStaticMaxChunks * kStaticMaxE;
 __device__ __align__(256) int32_t g_dispatch_scratch[kWords];
 
 std::mutex g_mu;
-int32_t* g_scratch_addr[64] = {nullptr};   // per device ordinal
+// per device ordinal: the array's address and the context it was looked up in
+int32_t* g_scratch_addr[64] = {nullptr};
+CUcontext g_scratch_ctx[64] = {nullptr};
+
+// The calling thread's current CUDA context (driver entry point, looked up once).
+CUcontext current_context() {
+  static const PFN_cuCtxGetCurrent_v4000 fn = []() -> PFN_cuCtxGetCurrent_v4000 {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+  }();
+  CUcontext c = nullptr;
+  if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
+
+// Launch without launch attributes, returning the launch's own status (a
+// <<<>>> launch leaves it to cudaGetLastError, which also reports and clears
+// errors the caller left pending).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_plain(void (*kernel)(KArgs...), cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(1);
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
 
 __global__ void k_static_begin(moe::DevError* err) {
   err->code = 0;
@@ -81,13 +116,20 @@ extern "C" int moe_dispatch_static(const int32_t* ids, const float* scores, int 
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  // NULL until the runtime has made a context current on this thread
+  CUcontext ctx = current_context();
   int32_t* base;
   {
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_addr[dev]) {
+    if (!ctx || !g_scratch_addr[dev] || g_scratch_ctx[dev] != ctx) {
+      // set-up: the array's address in the current context (the lookup also
+      // initialises the device's primary context when none is current yet)
       void* p = nullptr;
       if (cudaGetSymbolAddress(&p, g_dispatch_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+      ctx = current_context();
+      if (!ctx) return MOE_ERR_CUDA;
       g_scratch_addr[dev] = static_cast<int32_t*>(p);
+      g_scratch_ctx[dev] = ctx;
     }
     base = g_scratch_addr[dev];
   }
@@ -114,9 +156,9 @@ extern "C" int moe_dispatch_static(const int32_t* ids, const float* scores, int 
   ra.token_of = token_of;
   ra.score_of = score_of;
   ra.err = err;
-  k_static_begin<<<1, 1, 0, st>>>(err);
-  cudaError_t e = moe::launch_route(ra, st);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
-  k_static_end<<<1, 1, 0, st>>>(err, status);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  if (launch_plain(k_static_begin, st, err) != cudaSuccess) return MOE_ERR_CUDA;
+  if (moe::launch_route(ra, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_plain(k_static_end, st, static_cast<const moe::DevError*>(err), status) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
 }

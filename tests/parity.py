@@ -15,9 +15,22 @@ Intermediates (a, h, ys, dA, hs) are diagnostics, not outputs: one bf16 flip
 at an earlier rounding point (say of gate or up) can move a later intermediate
 by several of its own bf16 steps, so there a small fraction of elements
 (max_bad_frac) may exceed the max-abs limit; the Frobenius bound still holds.
+
+Every compare also counts the elements whose difference exceeds the literal
+max-abs bound 2e-2 * rms(ref), whatever the bf16 allowance, and the largest such
+difference in bf16 steps of the reference value.  For bf16 results that count
+must stay at or below LITERAL_FRAC of the elements.  With MOE_PARITY_STATS set
+to a file path, each compare appends its figures there as one JSON line.
 """
 
+import json
+import os
+
 import numpy as np
+
+# at most this fraction of a bf16 result's elements may exceed the literal
+# max-abs bound (they pass only through the bf16 rounding allowance)
+LITERAL_FRAC = 1e-3
 
 REL_FRO = 5e-3
 MAX_ABS_RMS = 2e-2
@@ -49,10 +62,24 @@ def compare(got, ref, bf16_out=True, rel_fro=REL_FRO, what="", max_bad_frac=0.0,
     if bf16_out:
         allow = bf16_spacing(ref) if flip is None else bf16_spacing(ref) + flip
         bad &= diff > allow * 1.0000001
-    info = "%s: rel_fro=%.3e max_abs=%.3e (limit %.3e) n_bad=%d" % (
-        what, rf, diff.max() if diff.size else 0.0, lim, int(bad.sum()))
+    over = diff > lim                      # beyond the literal max-abs bound
+    n_over = int(over.sum())
+    steps = float((diff[over] / bf16_spacing(ref[over])).max()) if n_over else 0.0
+    info = "%s: rel_fro=%.3e max_abs=%.3e (limit %.3e) n_bad=%d n_over_literal=%d/%d (max %.2f bf16 steps)" % (
+        what, rf, diff.max() if diff.size else 0.0, lim, int(bad.sum()), n_over, diff.size, steps)
+    path = os.environ.get("MOE_PARITY_STATS")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps({"what": what, "n": int(diff.size), "rel_fro": rf,
+                                "max_abs": float(diff.max() if diff.size else 0.0),
+                                "literal_limit": float(lim), "n_over_literal": n_over,
+                                "frac_over_literal": n_over / max(diff.size, 1),
+                                "max_over_bf16_steps": steps, "n_bad": int(bad.sum()),
+                                "bf16_out": bool(bf16_out)}) + "\n")
     assert rf <= rel_fro, info
     assert bad.sum() <= max_bad_frac * bad.size, info
+    if bf16_out and max_bad_frac < 1.0:
+        assert n_over <= LITERAL_FRAC * diff.size, info
     return rf, float(diff.max() if diff.size else 0.0)
 
 

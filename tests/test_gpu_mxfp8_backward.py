@@ -186,11 +186,13 @@ def test_mxfp8_backward_full_size_sampled(moe, orc):
     g = train_step(moe, inp, dev)
     dx = f32(bits(g["dx"]))
     assert np.all(np.isfinite(dx)) and np.all(np.isfinite(g["ds"].cpu().numpy()))
-    toks = np.array([0, 3001, c["T"] - 1], np.int32)
+    rng = np.random.default_rng(6)
+    toks = np.array(sorted(set(rng.choice(c["T"], 256, replace=False).tolist())
+                           | {0, c["T"] - 1}), np.int32)
     counts = np.bincount(inp["ids"].reshape(-1), minlength=c["E"])
-    wg_experts = [int(np.argmin(np.where(counts > 0, counts, 1 << 30)))]
-    experts = sorted(set(int(e) for e in inp["ids"][toks].reshape(-1)) | set(wg_experts))
-    fw, bw = oracle_weights(orc, inp, experts)
+    # the heaviest expert (longest WGRAD K loop) and the lightest
+    wg_experts = [int(np.argmax(counts)), int(np.argmin(np.where(counts > 0, counts, 1 << 30)))]
+    fw, bw = oracle_weights(orc, inp)
     dxr, dsr = orc.backward_mxfp8(inp["x"], inp["ids"], inp["scores"], fw, bw, inp["dy"],
                                   toks=toks)
     compare(dx[toks], f32(dxr), bf16_out=True, rel_fro=REL_FRO_MXFP8, what="dx mxfp8 full",
@@ -202,6 +204,6 @@ def test_mxfp8_backward_full_size_sampled(moe, orc):
                                                inp["dy"], e)
         assert rows == counts[e]
         compare((g["dw13"][e] - dev["dw13"][e]).cpu().numpy(), r13, rel_fro=REL_FRO_MXFP8,
-                what="dW13 mxfp8 full", max_bad_frac=1.0)
+                what="dW13[%d] mxfp8 full" % e, max_bad_frac=1.0)
         compare((g["dw2"][e] - dev["dw2"][e]).cpu().numpy(), r2, rel_fro=REL_FRO_MXFP8,
-                what="dW2 mxfp8 full", max_bad_frac=1.0)
+                what="dW2[%d] mxfp8 full" % e, max_bad_frac=1.0)

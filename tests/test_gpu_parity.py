@@ -58,6 +58,9 @@ SMALL = [
     ("single_expert", dict(T=130, d=128, I=64, E=1, k=1), {}),
     ("one_token", dict(T=1, d=128, I=64, E=4, k=2), {}),
     ("k8_e256", dict(T=96, d=128, I=64, E=256, k=8), {}),
+    # more than eight experts per token: the combine's general-k kernel
+    ("k16", dict(T=150, d=128, I=64, E=40, k=16), {}),
+    ("k11_pad", dict(T=90, d=256, I=128, E=24, k=11, pad=10), {}),
     # W13, W2 and DGRAD-W13 on CTA pairs (moe_plan_set_cta_pairs): pairs of an
     # expert's m tiles on the pair kernel, an odd last m tile on one CTA
     ("pairs", dict(T=300, d=256, I=256, E=6, k=3, cta_pairs=True), {}),

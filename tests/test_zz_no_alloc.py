@@ -57,6 +57,33 @@ def _static_dispatch(moe, dev, T, k, E):
     return {key: v.cpu().numpy() for key, v in out.items()}
 
 
+def test_static_dispatch_allocates_nothing(moe):
+    # after the first call (the set-up), a call leaves the device's free memory
+    # unchanged: it allocates nothing (device allocations are 2 MB granular)
+    inp = make(None, seed=15, train=False, T=4096, d=128, I=64, E=64, k=8)
+    dev = {k: torch.from_numpy(np.ascontiguousarray(v)).cuda() for k, v in inp.items()
+           if k in ("ids", "scores")}
+    _static_dispatch(moe, dev, 4096, 8, 64)              # set-up (and outputs allocated)
+    L = moe.lib()
+    BM = L.moe_tile_rows()
+    cap = (4096 * 8 + 64 * (BM - 1)) // BM * BM
+    outs = [torch.empty(n, dtype=dt, device="cuda") for n, dt in
+            ((65, torch.int32), (65, torch.int32), (4096 * 8, torch.int32), (cap, torch.int32),
+             (cap, torch.float32), (2, torch.int32))]
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    for _ in range(3):
+        rc = L.moe_dispatch_static(p(dev["ids"]), p(dev["scores"]), 4096, 8, 64, *map(p, outs[:5]),
+                                   cap, p(outs[5]),
+                                   ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        assert rc == 0
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
+    assert outs[5].tolist() == [0, -1]
+
+
 @pytest.mark.parametrize("sizes", [
     dict(T=300, d=128, I=64, E=7, k=3),
     dict(T=2048, d=128, I=64, E=128, k=8, routing="zipf", zipf_s=1.2, zipf_support=102),
@@ -95,6 +122,10 @@ def test_static_dispatch_reports_bad_ids_and_clears(moe):
            if k in ("ids", "scores")}
     got = _static_dispatch(moe, dev, 100, 3, 8)
     assert got["status"].tolist() == [moe.MOE_ERR_BAD_IDS, 122]
+    # the repeated id is dropped; the tables stay consistent without it
+    assert got["row_of"][122] == -1
+    assert got["m_indptr"][-1] == 100 * 3 - 1
+    assert np.all(got["row_of"][np.arange(300) != 122] >= 0)
     dev["ids"] = torch.from_numpy(make(None, seed=14, train=False, T=100, d=128, I=64, E=8,
                                        k=3)["ids"]).cuda()
     got = _static_dispatch(moe, dev, 100, 3, 8)
