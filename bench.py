@@ -75,9 +75,12 @@ def parse():
 # algorithmic work per stage (routed rows R = T*k; padding rows not counted)
 
 
-def stage_model(c):
+def stage_model(c, n_nonempty=None):
+    """n_nonempty: experts with routed rows (default E); the weight-gradient
+    read-modify-write touches only theirs."""
     T, d, I, E, k = c["T"], c["d"], c["I"], c["E"], c["k"]
     R = T * k
+    Ew = E if n_nonempty is None else n_nonempty
     return {
         # bound, algorithmic flops, algorithmic bytes
         "dispatch": ("hbm", 0, 8 * R + 4 * R * 3),
@@ -91,8 +94,8 @@ def stage_model(c):
                             + 4 * R * I + 2 * R * I),
         "dgrad_w13": ("tensor", 4 * R * d * I, 4 * R * I + E * 2 * I * d * 2 + 2 * R * d),
         "combine_dx": ("hbm", 0, 2 * R * d + 2 * T * d + 8 * T * k),
-        "wgrad_w2": ("hbm", 2 * R * d * I, 2 * R * d + 2 * R * I + 8 * E * d * I),
-        "wgrad_w13": ("hbm", 4 * R * d * I, 4 * R * I + 2 * R * d + 8 * E * 2 * I * d),
+        "wgrad_w2": ("hbm", 2 * R * d * I, 2 * R * d + 2 * R * I + 8 * Ew * d * I),
+        "wgrad_w13": ("hbm", 4 * R * d * I, 4 * R * I + 2 * R * d + 8 * Ew * 2 * I * d),
     }
 
 
@@ -750,14 +753,14 @@ def run_extra(moe, name, train, args, dev, ws, tpeak, pk):
     if train:
         for j, st_ in enumerate(BWD_STAGES):
             stage_ms[st_] = sum(evb[i][j].elapsed_time(evb[i][j + 1]) for i in range(K)) / K
-    model = stage_model(c)
+    counts = np.bincount(D["ids"].cpu().numpy().reshape(-1), minlength=E)
+    model = stage_model(c, n_nonempty=int((counts > 0).sum()))
     if not train:
         # an inference forward does not store a
         b, fl, by = model["w13_swiglu"]
         model["w13_swiglu"] = (b, fl, by - 4 * T * k * I)
     stages = stage_table(model, stage_ms, tpeak, pk["hbm_gbs"])
     flops = (18.0 if train else 6.0) * T * k * d * I
-    counts = np.bincount(D["ids"].cpu().numpy().reshape(-1), minlength=E)
     desc = ("%s (T=%d, d=%d, I=%d, E=%d, k=%d, %s routing%s%s, %s)"
             % (name, T, d, I, E, k, c["routing"],
                ", last %d tokens zero-score padding" % c["pad"] if c["pad"] else "",

@@ -140,6 +140,45 @@ int moe_forward(moe_plan* plan, const void* x, const int32_t* ids, const float* 
                 void* y, int save_for_backward, void* stream);
 
 /*
+ * Forward over rows the caller has already laid out expert-major (nvfp4moe
+ * README, "MoE layer": frameworks that already have expert-major rows call
+ * run_routed(x, m_indptr, padded_offsets, out=...)).  Dispatch and gather are
+ * skipped; the W13 GEMM + SwiGLU and the W2 GEMM run over the caller's layout,
+ * and the combine runs when row_of and y are given.  Inputs (device):
+ *   x_e      [rows, d] bf16: expert e's routed rows at [off_pad[e], off_pad[e] + m_e)
+ *            with m_e = m_indptr[e+1] - m_indptr[e]; the rows up to off_pad[e+1]
+ *            are padding (computed like routed rows; zero rows give zero outputs)
+ *   m_indptr [E+1] int32: m_indptr[0] = 0, non-decreasing (exact row counts)
+ *   off_pad  [E+1] int32: off_pad[0] = 0, every entry a multiple of
+ *            moe_tile_rows() (128), off_pad[e+1] - off_pad[e] >= m_e,
+ *            off_pad[E] <= rows
+ *   score_of [rows] fp32 routing score of each row, or NULL (no score)
+ *   w13, w2  as moe_forward (bf16 plans)
+ *   row_of   [T, k] int32 row of x_e holding token t's j-th contribution (-1:
+ *            none), or NULL
+ * Outputs (device):
+ *   ys [rows, d] bf16: ys[r] = bf16(score_of[r] * W2[e] . h),
+ *      h = bf16(silu(G) * U), (G, U) = bf16(W13[e] . x_e[r]), for the m tiles
+ *      that hold routed rows (rows in other tiles are not written)
+ *   y  [T, d] bf16 (with row_of, else NULL): y[t] = bf16(sum_j ys[row_of[t,j]])
+ *      in fixed j order
+ * On the same layout, inputs and weights, ys and y equal those of moe_forward
+ * bit for bit.  rows <= the plan's worst-case padded row count
+ * (T*k + E*127 rounded down to a multiple of 128), else MOE_ERR_INVALID_ARG.
+ * The layout is checked on the device: an inconsistent m_indptr / off_pad runs
+ * no tile and records MOE_ERR_INVALID_ARG in the device error word (detail:
+ * the first offending expert index e, 0..E); on a consistent layout a row_of
+ * entry outside [0, off_pad[E]) is treated as -1 and records
+ * MOE_ERR_INVALID_ARG with detail E + 1 + its flat index t*k + j.  bf16 plans
+ * only (MOE_ERR_UNSUPPORTED otherwise).  The call uses the plan's workspace
+ * (h, the tile list, a checked copy of row_of), so it overwrites the tables of
+ * the previous call and cannot be followed by moe_backward.
+ */
+int moe_forward_routed(moe_plan* plan, const void* x_e, long long rows, const int32_t* m_indptr,
+                       const int32_t* off_pad, const float* score_of, const void* w13,
+                       const void* w2, void* ys, const int32_t* row_of, void* y, void* stream);
+
+/*
  * Backward of the last saving forward on this plan ("What it is selling":
  * DGRAD and WGRAD; nvfp4moe "Training": router gradients).  Inputs: dy [T, d]
  * bf16 and the same w13/w2 as the forward.  Outputs:

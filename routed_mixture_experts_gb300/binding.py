@@ -46,6 +46,7 @@ def _declare(L):
     L.moe_plan_set_workspace.argtypes = [vp, vp, sz, i32]
     L.moe_forward.argtypes = [vp] * 9 + [i32, vp]
     L.moe_backward.argtypes = [vp] * 9
+    L.moe_forward_routed.argtypes = [vp, vp, ctypes.c_longlong] + [vp] * 9
     L.moe_step_host.argtypes = [vp] * 13
     L.moe_quantize_mxfp8.argtypes = [vp, i64, i32, vp, vp, vp]
     L.moe_plan_check.argtypes = [vp, ctypes.POINTER(ctypes.c_longlong)]
@@ -69,6 +70,7 @@ def _declare(L):
     L.moe_plan_launch_count.argtypes = [vp]
     L.moe_plan_launch_count.restype = ctypes.c_longlong
     for name in ("moe_plan_set_swiglu_clamp", "moe_plan_set_workspace", "moe_forward",
+                 "moe_forward_routed",
                  "moe_backward", "moe_step_host", "moe_quantize_mxfp8", "moe_plan_check",
                  "moe_plan_buffer", "moe_gemm_bf16", "moe_plan_set_timing_events",
                  "moe_prepare_weights_mxfp8", "moe_plan_set_debug", "moe_plan_set_cta_pairs",
@@ -141,6 +143,22 @@ class MoePlan:
         _check(lib().moe_forward(self.ptr, _p(x), _p(ids), _p(scores), _p(w13), _p(w2), _p(w13_sf),
                                  _p(w2_sf), _p(y), 1 if save else 0, _stream(stream)), "forward")
         return y
+
+    def forward_routed(self, x_e, m_indptr, off_pad, w13, w2, score_of=None, ys=None,
+                       row_of=None, y=None, stream=None):
+        """Forward over caller-laid-out expert-major rows x_e [rows, d] (see
+        moe_forward_routed in moe.h).  Returns (ys, y); y only with row_of."""
+        import torch
+
+        rows = x_e.shape[0]
+        if ys is None:
+            ys = torch.empty(rows, self.d, dtype=torch.bfloat16, device=x_e.device)
+        if row_of is not None and y is None:
+            y = torch.empty(self.T, self.d, dtype=torch.bfloat16, device=x_e.device)
+        _check(lib().moe_forward_routed(self.ptr, _p(x_e), rows, _p(m_indptr), _p(off_pad),
+                                        _p(score_of), _p(w13), _p(w2), _p(ys), _p(row_of), _p(y),
+                                        _stream(stream)), "forward_routed")
+        return ys, y
 
     def backward(self, dy, w13, w2, dw13, dw2, dx=None, dscores=None, stream=None):
         import torch

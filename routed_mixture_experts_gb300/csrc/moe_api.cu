@@ -64,6 +64,12 @@ struct moe_plan {
   const void *w13_cached, *w2_cached;
   // CTA-pair tile lists (dispatch output): pairs of m tiles, odd last m tiles
   int32_t *pair_list, *left_list, *num_pairs, *num_left;
+  // moe_forward_routed: the m tiles of the caller's layout and their count;
+  // tensor maps over the caller's expert-major rows and outputs
+  int32_t *routed_list, *routed_count;
+  CUtensorMap tm_rx, tm_rys;
+  const void *rx_cached, *rys_cached;
+  long long rx_rows, rys_rows;
   // MXFP8: quantised expert-major activations and h, with tiled scales
   uint8_t *xq, *xsf, *hq, *hsf;
   int ngr_d, ngr_I;                 // 128-element scale groups along d and along I
@@ -229,6 +235,8 @@ size_t layout(moe_plan* p, char* base, int flags) {
   p->num_nonempty = reinterpret_cast<int32_t*>(take(4));
   p->expert_order = reinterpret_cast<int32_t*>(take(4 * E));
   p->tile_expert = reinterpret_cast<int32_t*>(take(4 * (RP / kBM)));
+  p->routed_list = reinterpret_cast<int32_t*>(take(4 * (RP / kBM)));
+  p->routed_count = reinterpret_cast<int32_t*>(take(4));
   p->pair_list = p->left_list = p->num_pairs = p->num_left = nullptr;
   if (p->pair) {
     p->pair_list = reinterpret_cast<int32_t*>(take(4 * (RP / kBM / 2 + 1)));
@@ -560,6 +568,7 @@ int moe_plan_set_workspace(moe_plan* p, void* ws, size_t bytes, int flags) {
   p->w13_cached = p->w2_cached = nullptr;
   p->dw13_cached = p->dw2_cached = nullptr;
   p->w13q_cached = p->w2q_cached = nullptr;
+  p->rx_cached = p->rys_cached = nullptr;
   const long long RP = p->RP;
   p->w13t_cached = p->w2t_cached = nullptr;
   if (p->precision == MOE_PREC_MXFP8) {
@@ -948,6 +957,94 @@ int moe_backward_mxfp8(moe_plan* p, const void* dy, const uint8_t* w13t, const u
   return MOE_OK;
 }
 
+// Forward over a caller-provided expert-major layout (nvfp4moe README, "MoE
+// layer": frameworks with expert-major rows call run_routed): check the layout
+// and list its m tiles -> W13 GEMM + SwiGLU -> W2 GEMM (x score_of) into the
+// caller's ys -> optionally combine into y.  Dispatch and gather are skipped.
+int moe_forward_routed(moe_plan* p, const void* x_e, long long rows, const int32_t* m_indptr,
+                       const int32_t* off_pad, const float* score_of, const void* w13,
+                       const void* w2, void* ys, const int32_t* row_of, void* y, void* stream_v) {
+  if (!p || !x_e || !m_indptr || !off_pad || !w13 || !w2 || !ys) return MOE_ERR_INVALID_ARG;
+  if ((row_of == nullptr) != (y == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x_e) || !aligned16(w13) || !aligned16(w2) || !aligned16(ys) ||
+      (y && !aligned16(y)))
+    return MOE_ERR_INVALID_ARG;
+  if (rows < 0 || rows > p->RP) return MOE_ERR_INVALID_ARG;
+  if (p->precision != MOE_PREC_BF16) return MOE_ERR_UNSUPPORTED;
+  if (!p->ws) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream_v);
+  if (rows == 0) {
+    // no routed rows: y is all zeros
+    if (y) return cuda_status(cudaMemsetAsync(y, 0, 2ull * p->T * p->d, st));
+    return MOE_OK;
+  }
+  if (refresh_weight_maps(p, w13, w2) != MOE_OK) return MOE_ERR_CUDA;
+  if (x_e != p->rx_cached || rows != p->rx_rows) {
+    if (encode_tmap_bf16(&p->tm_rx, x_e, rows, p->d, 128)) return MOE_ERR_CUDA;
+    p->rx_cached = x_e;
+    p->rx_rows = rows;
+  }
+  if (ys != p->rys_cached || rows != p->rys_rows) {
+    if (encode_tmap_bf16(&p->tm_rys, ys, rows, p->d, 128)) return MOE_ERR_CUDA;
+    p->rys_cached = ys;
+    p->rys_rows = rows;
+  }
+  RoutedArgs ra{};
+  ra.m_indptr = m_indptr;
+  ra.off_pad = off_pad;
+  ra.E = p->E;
+  ra.rows = rows;
+  ra.row_of_in = row_of;
+  ra.Tk = row_of ? p->R : 0;
+  ra.row_of_out = p->row_of;
+  ra.tile_expert = p->tile_expert;
+  ra.mtile_list = p->routed_list;
+  ra.list_count = p->routed_count;
+  ra.err = p->err;
+  const int pgrid = row_of ? (p->R + 4095) / 4096 : 1;
+  cudaError_t e = launch_routed_prepare(ra, pgrid < 1 ? 1 : pgrid, st);
+  if (e != cudaSuccess) return cuda_status(e);
+  p->launches += 1;
+  {
+    GemmArgs g = rows_args(p);
+    g.mtile_list = p->routed_list;
+    g.list_count = p->routed_count;
+    g.k_blocks = p->d / kBK;
+    g.b_expert_rows = 2 * p->I;
+    g.b_half_rows = p->I;
+    g.n_tiles = p->I / (p->bn13 / 2);
+    g.out0 = p->h; g.ld0 = p->I;
+    g.ld1 = 2LL * p->I;
+    g.save = 0;
+    e = launch_gemm(EPI_SWIGLU, p->bn13, false, false, p->tm_rx, p->tm_w13, p->tm_rx, p->tm_h,
+                    p->tm_h, g, p->num_sms, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    p->launches += 1;
+  }
+  {
+    GemmArgs g = rows_args(p);
+    g.mtile_list = p->routed_list;
+    g.list_count = p->routed_count;
+    g.k_blocks = p->I / kBK;
+    g.b_expert_rows = p->d;
+    g.n_tiles = p->d / p->bn2;
+    g.out0 = ys; g.ld0 = p->d;
+    g.row_scale = score_of;           // NULL: no routing score
+    g.k_rotate = 1;
+    e = launch_gemm(EPI_SCORE, p->bn2, false, false, p->tm_h, p->tm_w2, p->tm_h, p->tm_rys,
+                    p->tm_rys, g, p->num_sms, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    p->launches += 1;
+  }
+  if (y) {
+    e = launch_combine(ys, p->row_of, p->T, p->k, p->d, y, nullptr, 0, nullptr, gather_grid(p), st);
+    if (e != cudaSuccess) return cuda_status(e);
+    p->launches += 1;
+  }
+  p->saved = 0;
+  return MOE_OK;
+}
+
 int moe_step_host(moe_plan* p, const void* x_host, const int32_t* ids_host,
                   const float* scores_host, const void* dy_host, const void* w13, const void* w2,
                   float* dw13, float* dw2, void* y_host, void* dx_host, float* dscores_host,
@@ -1086,7 +1183,9 @@ int moe_plan_check(moe_plan* p, long long* detail) {
   if (e != cudaSuccess) return cuda_status(e);
   int rc = reset_error_word(p->err);
   if (rc != MOE_OK) return rc;
-  if (detail) *detail = h.code == MOE_ERR_BAD_IDS ? (long long)h.first_bad : (long long)h.where;
+  if (detail)
+    *detail = (h.code == MOE_ERR_BAD_IDS || h.code == MOE_ERR_INVALID_ARG) ? (long long)h.first_bad
+                                                                           : (long long)h.where;
   return h.code;
 }
 

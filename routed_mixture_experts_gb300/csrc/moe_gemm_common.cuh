@@ -325,7 +325,7 @@ __device__ __forceinline__ void epilogue_mx_wide(const GemmArgs& a, const TileIn
     }
   } else {
     static_assert(EPI == EPI_SCORE || EPI == EPI_STORE, "256-wide MXFP8 epilogues");
-    const float s = EPI == EPI_SCORE ? a.row_scale[grow] : 1.0f;
+    const float s = EPI == EPI_SCORE && a.row_scale ? a.row_scale[grow] : 1.0f;
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       uint32_t pk[32];
@@ -392,7 +392,7 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, const TileInfo& ti, 
       }
     }
   } else if constexpr (EPI == EPI_SCORE || EPI == EPI_STORE) {
-    const float s = EPI == EPI_SCORE ? a.row_scale[grow] : 1.0f;
+    const float s = EPI == EPI_SCORE && a.row_scale ? a.row_scale[grow] : 1.0f;
 #pragma unroll 1
     for (int c = 0; c < BN; c += 64) {
       tmem_ld16(tbase + c + ch, r0);

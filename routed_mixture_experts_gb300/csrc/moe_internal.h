@@ -198,6 +198,23 @@ struct RouteArgs {
 };
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t stream);
 
+// Caller-provided expert-major layout (moe_forward_routed).
+constexpr int kRoutedGranule = 128;   // off_pad entries are multiples of the GEMM tile rows
+struct RoutedArgs {
+  const int32_t* m_indptr;   // [E+1] caller's
+  const int32_t* off_pad;    // [E+1] caller's
+  int E;
+  long long rows;            // rows of the caller's expert-major buffers
+  const int32_t* row_of_in;  // [Tk] caller's (NULL: Tk = 0)
+  int Tk;
+  int32_t* row_of_out;       // [Tk] checked copy
+  int32_t* tile_expert;      // [max m tiles]
+  int32_t* mtile_list;       // [max m tiles]
+  int32_t* list_count;       // scalar
+  DevError* err;
+};
+cudaError_t launch_routed_prepare(const RoutedArgs& a, int grid, cudaStream_t stream);
+
 // rows r < *nrows of dst[r] = src[token_of[r]] (zero where token_of[r] < 0).
 cudaError_t launch_gather_rows(const void* src, const int32_t* token_of, const int32_t* nrows,
                                int d, void* dst, int grid, cudaStream_t stream);

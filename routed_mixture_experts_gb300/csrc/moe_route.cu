@@ -402,6 +402,78 @@ __global__ void __launch_bounds__(256) k_combine_any(const uint4* __restrict__ r
   pdl_trigger();
 }
 
+// Caller-provided expert-major layout (moe_forward_routed): check m_indptr and
+// off_pad, list the m tiles that hold routed rows, and copy row_of with entries
+// outside the laid-out rows replaced by -1.  Every CTA checks the layout (E+1
+// entries); CTA 0 writes the tile list, all CTAs copy row_of.  An inconsistent
+// layout lists no tiles, drops every row_of entry and records
+// MOE_ERR_INVALID_ARG with the first offending expert as detail; an out-of-range
+// row_of entry (checked only on a consistent layout) records detail
+// E + 1 + its flat index.
+__global__ void __launch_bounds__(kMaxE) k_routed_prepare(RoutedArgs a) {
+  pdl_wait();   // the previous kernel of the stream has completed
+  __shared__ int bad_s;
+  __shared__ int warp_tot[kMaxE / 32];
+  const int tid = threadIdx.x;
+  const int E = a.E;
+  if (tid == 0) bad_s = INT_MAX;
+  __syncthreads();
+  for (int e = tid; e <= E; e += blockDim.x) {
+    const int o = a.off_pad[e];
+    bool ok = o >= 0 && (o & (kRoutedGranule - 1)) == 0 && (long long)o <= a.rows;
+    if (e == 0) ok = ok && o == 0 && a.m_indptr[0] == 0;
+    if (e < E) {
+      const int m = a.m_indptr[e + 1] - a.m_indptr[e];
+      ok = ok && m >= 0 && a.off_pad[e + 1] - o >= m;
+    }
+    if (!ok) atomicMin(&bad_s, e);
+  }
+  __syncthreads();
+  const bool valid = bad_s == INT_MAX;
+  const int nrows = valid ? a.off_pad[E] : 0;
+  if (blockIdx.x == 0) {
+    if (!valid && tid == 0) {
+      atomicMin(&a.err->first_bad, bad_s);
+      atomicCAS(&a.err->code, 0, 1 /*MOE_ERR_INVALID_ARG*/);
+    }
+    // m tiles per expert: those holding its routed rows (ceil(m_e / 128))
+    const int lane = tid & 31, warp = tid >> 5;
+    const int nt = (valid && tid < E) ? (a.m_indptr[tid + 1] - a.m_indptr[tid] + kRoutedGranule - 1) /
+                                            kRoutedGranule
+                                      : 0;
+    const int inc = warp_incl_scan(nt, lane);
+    if (lane == 31) warp_tot[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+      const int nw = blockDim.x / 32;
+      const int t0 = lane < nw ? warp_tot[lane] : 0;
+      const int s0 = warp_incl_scan(t0, lane);
+      if (lane < nw) warp_tot[lane] = s0 - t0;
+    }
+    __syncthreads();
+    const int base = warp_tot[warp] + inc - nt;
+    if (tid < E) {
+      const int mt0 = a.off_pad[tid] / kRoutedGranule;
+      for (int i = 0; i < nt; ++i) {
+        a.mtile_list[base + i] = mt0 + i;
+        a.tile_expert[mt0 + i] = tid;
+      }
+    }
+    if (tid == blockDim.x - 1) *a.list_count = base + nt;   // the last thread's end = the total
+  }
+  const int Tk = a.Tk;
+  for (int f = blockIdx.x * blockDim.x + tid; f < Tk; f += gridDim.x * blockDim.x) {
+    const int r = a.row_of_in[f];
+    const bool in = r >= 0 && r < nrows;
+    a.row_of_out[f] = in ? r : -1;
+    if (valid && r >= nrows) {
+      atomicMin(&a.err->first_bad, E + 1 + f);
+      atomicCAS(&a.err->code, 0, 1 /*MOE_ERR_INVALID_ARG*/);
+    }
+  }
+  pdl_trigger();
+}
+
 }  // namespace
 
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t stream) {
@@ -409,6 +481,11 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t stream) {
   if (e == cudaSuccess) e = launch_pdl(k_route_scan, dim3(1), dim3(kMaxE), 0, stream, a);
   if (e == cudaSuccess) e = launch_pdl(k_route_scatter, dim3(a.nblk), dim3(kChunk), 0, stream, a);
   return e;
+}
+
+cudaError_t launch_routed_prepare(const RoutedArgs& a, int grid, cudaStream_t stream) {
+  if (a.E < 1 || a.E > kMaxE) return cudaErrorInvalidValue;
+  return launch_pdl(k_routed_prepare, dim3(grid), dim3(kMaxE), 0, stream, a);
 }
 
 cudaError_t launch_gather_rows(const void* src, const int32_t* token_of, const int32_t* nrows,
