@@ -31,6 +31,10 @@ import numpy as np
 # at most this fraction of a bf16 result's elements may exceed the literal
 # max-abs bound (they pass only through the bf16 rounding allowance)
 LITERAL_FRAC = 1e-3
+# fp32 weight gradients sum products of bf16 per-row operands (hs, dA): at most
+# this fraction of their elements may exceed the literal max-abs bound, through
+# bf16 flips of those operands (measured at the full workloads: up to 3.3e-5)
+WGRAD_FLIP_FRAC = 1e-4
 
 REL_FRO = 5e-3
 MAX_ABS_RMS = 2e-2
