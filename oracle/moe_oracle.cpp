@@ -23,6 +23,9 @@
 //   [NV-M] same README, section "MoE layer": dispatch, FC1 + gated activation, FC2,
 //         probability weighting, deterministic combine; distinct int32 ids per row,
 //         float32 weights; padded offsets.
+//   [NV-D] same README, sections "Dense GEMM" and "Grouped GEMM": quantize returns
+//         packed E2M1 values, blocked E4M3 scale factors and the per-tensor
+//         dequantisation scale; the GEMM takes their product as alpha.
 //   [NV-T] same README, section "Training" and "Supported kernel surface":
 //         deterministic dispatch, combine and router gradients; input and weight
 //         gradients.
@@ -42,6 +45,18 @@
 //   * MXFP8 (OCP MX): 32-element blocks along K, E8M0 shared exponent
 //     X = floor(log2(amax)) - 8, E4M3 elements rounded to nearest even and
 //     saturated to +-448; an all-zero block gets scale code 0.
+//   * NVFP4 ([DM] "NVFP4 is infer-only ... prepare weights before the call";
+//     [NV-D] packed E2M1 values, blocked E4M3 scale factors and a per-tensor
+//     dequantisation scale; [NV-M] static activation scales): two-level scaling.
+//     A tensor with per-tensor dequantisation scale s has encode scale g = 1/s
+//     (fp32).  A 16-element block along K with amax A gets the E4M3 scale code
+//     E4M3_RNE_satfinite((A / 6) * g), fp32 arithmetic (6 = E2M1's largest
+//     value); with S its value, each element becomes E2M1_RNE_satfinite(v * (g / S))
+//     (S = 0: all codes 0).  Weights are prepared per expert with
+//     s = amax(W[e]) / (6 * 448) (1 for an all-zero expert); activations (x and
+//     h) use static scales the caller sets.  A GEMM sums the dequantised block
+//     products (code value times block scale) in fp32 and multiplies the sum by
+//     alpha = s_activation * s_weight[e] before its rounding point.
 //
 // Working type: float (the pages' FP32 accumulate) unless built with
 // -DORC_DOUBLE, which evaluates every sum and elementwise step in double (used to
@@ -366,6 +381,119 @@ void row_backward_mx(const Problem& p, int t, int e, float s, const uint16_t* dy
     real acc = 0;
     for (int i = 0; i < 2 * I; ++i) acc += dav[i] * mx_value(w13tq, w13ts, 2 * I, row, i);
     dxe[c] = real_to_bf16(acc);                                // R5
+  }
+}
+
+// ---- NVFP4 (E2M1 elements, E4M3 scales per 16 elements, per-tensor scale) ----
+
+// Value of an E2M1 code (1 sign bit, 2 exponent bits with bias 1, 1 mantissa
+// bit; exponent field 0 is subnormal): magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+double e2m1_value(uint8_t c) {
+  int sgn = (c >> 3) & 1, ex = (c >> 1) & 3, man = c & 1;
+  double v = ex == 0 ? man * 0.5 : std::ldexp(1.0 + man / 2.0, ex - 1);
+  return sgn ? -v : v;
+}
+
+// Nearest E2M1 value to v, ties to the even code (mantissa bit 0), saturating
+// to +-6; the sign is kept (negative values that round to zero give code 8).
+uint8_t e2m1_encode(double v) {
+  const uint8_t sgn = std::signbit(v) ? 8 : 0;
+  const double m = std::fabs(v);
+  if (m >= 6.0) return sgn | 7;
+  int lo = 0;                                   // e2m1_value(lo) <= m < e2m1_value(lo + 1)
+  while (lo < 6 && e2m1_value(static_cast<uint8_t>(lo + 1)) <= m) ++lo;
+  const double dl = m - e2m1_value(static_cast<uint8_t>(lo));
+  const double dh = e2m1_value(static_cast<uint8_t>(lo + 1)) - m;
+  const int c = dl < dh ? lo : (dh < dl ? lo + 1 : (lo % 2 == 0 ? lo : lo + 1));
+  return sgn | static_cast<uint8_t>(c);
+}
+
+// Quantise n (<= 16) bf16 values of one block with encode scale g: E2M1 codes
+// (one per byte here) and the E4M3 scale code.
+void nv_quant_block(const uint16_t* in, int n, float g, uint8_t* codes, uint8_t* scale) {
+  float amax = 0;
+  for (int i = 0; i < n; ++i) {
+    const float v = std::fabs(bf16_to_float(in[i]));
+    if (v > amax) amax = v;
+  }
+  float t = amax / 6.0f;
+  t = t * g;
+  const uint8_t sc = e4m3_encode(static_cast<double>(t));
+  *scale = sc;
+  const float S = static_cast<float>(e4m3_value(sc));
+  if (S == 0.0f) {
+    for (int i = 0; i < n; ++i) codes[i] = 0;
+    return;
+  }
+  const float r = g / S;
+  for (int i = 0; i < n; ++i) {
+    const float v = bf16_to_float(in[i]) * r;
+    codes[i] = e2m1_encode(static_cast<double>(v));
+  }
+}
+
+// Dequantised element (row, col) of a packed [rows, K/2] code matrix (element
+// 2i in the low nibble of byte i) with E4M3 scales [rows, K/16].
+real nv_value(const uint8_t* q, const uint8_t* sc, int K, size_t row, int col) {
+  const uint8_t b = q[row * (K / 2) + col / 2];
+  const uint8_t c = (col & 1) ? (b >> 4) : (b & 15);
+  return static_cast<real>(e2m1_value(c) * e4m3_value(sc[row * (K / 16) + col / 16]));
+}
+
+// Quantise n bf16 values (n a multiple of 16) with encode scale g and return
+// their dequantised values (code value times block scale; the per-tensor scale
+// is applied to the GEMM sum).
+void nv_roundtrip(const uint16_t* in, int n, float g, real* out) {
+  uint8_t q[16], sc;
+  for (int b = 0; b < n; b += 16) {
+    nv_quant_block(in + b, 16, g, q, &sc);
+    for (int i = 0; i < 16; ++i)
+      out[b + i] = static_cast<real>(e2m1_value(q[i]) * e4m3_value(sc));
+  }
+}
+
+// NVFP4 forward quantities of one routed row ([DM], [NV-M]: BF16 activation
+// quantisation, FC1 + gated activation + NVFP4 requantisation, FC2, probability
+// weighting): x row quantised along d with the static input scale, W13 and W2
+// prepared, a (R1, after alpha), h (R2), h quantised along I with the static
+// hidden scale, ys (R3, score times alpha times the W2 sum).
+struct NvScales {
+  float x_scale, h_scale;            // static activation dequantisation scales
+  const float* w13_scale;            // [E] per-expert weight dequantisation scales
+  const float* w2_scale;             // [E]
+};
+
+void row_forward_nv(const Problem& p, int t, int e, float s, const uint8_t* w13q,
+                    const uint8_t* w13s, const uint8_t* w2q, const uint8_t* w2s,
+                    const NvScales& sc, uint16_t* a, uint16_t* h, uint16_t* ys) {
+  const int d = p.d, I = p.I;
+  std::vector<real> xv(d), hv(I);
+  const float gx = 1.0f / sc.x_scale, gh = 1.0f / sc.h_scale;
+  nv_roundtrip(p.x + (size_t)t * d, d, gx, xv.data());
+  const float alpha13 = sc.x_scale * sc.w13_scale[e];
+  for (int i = 0; i < 2 * I; ++i) {
+    const size_t row = (size_t)e * 2 * I + i;
+    real acc = 0;
+    for (int c = 0; c < d; ++c) acc += xv[c] * nv_value(w13q, w13s, d, row, c);
+    a[i] = real_to_bf16(acc * static_cast<real>(alpha13));     // R1
+  }
+  const real L = p.clamp;
+  for (int i = 0; i < I; ++i) {
+    real G = bf(a[i]), U = bf(a[I + i]);
+    if (L > 0) {
+      G = G < -L ? -L : (G > L ? L : G);
+      U = U < -L ? -L : (U > L ? L : U);
+    }
+    h[i] = real_to_bf16(G / (real(1) + rexp(-G)) * U);         // R2
+  }
+  nv_roundtrip(h, I, gh, hv.data());
+  const float alpha2 = sc.h_scale * sc.w2_scale[e];
+  for (int c = 0; c < d; ++c) {
+    const size_t row = (size_t)e * d + c;
+    real acc = 0;
+    for (int i = 0; i < I; ++i) acc += hv[i] * nv_value(w2q, w2s, I, row, i);
+    const real v = acc * static_cast<real>(alpha2);
+    ys[c] = real_to_bf16(static_cast<real>(s) * v);            // R3
   }
 }
 
@@ -810,6 +938,99 @@ int orc_wgrad_expert_mxfp8(int T, int d, int I, int E, int k, float clamp,
     for (int i = 0; i < I; ++i) dw2_delta[(size_t)c * I + i] = static_cast<float>(acc[i]);
   }
   return rows;
+}
+
+int orc_e2m1_encode(const double* in, uint8_t* out, long n) {
+  for (long i = 0; i < n; ++i) out[i] = e2m1_encode(in[i]);
+  return 0;
+}
+
+int orc_e2m1_decode(const uint8_t* in, double* out, long n) {
+  for (long i = 0; i < n; ++i) out[i] = e2m1_value(in[i]);
+  return 0;
+}
+
+// NVFP4 quantiser ([NV-D] quantize): a bf16 matrix [rows, K] along K in
+// 16-element blocks with the encode scale g (1 / the per-tensor dequantisation
+// scale).  codes [rows, K/2] packed E2M1 (element 2i in the low nibble of byte
+// i); scales [rows, K/16] E4M3 bytes.  K must be a multiple of 16.
+int orc_quant_nvfp4(long rows, int K, const uint16_t* in, float g, uint8_t* codes,
+                    uint8_t* scales) {
+  if (K % 16) return -1;
+  uint8_t q[16];
+  for (long r = 0; r < rows; ++r)
+    for (int b = 0; b < K / 16; ++b) {
+      nv_quant_block(in + r * K + b * 16, 16, g, q, scales + r * (K / 16) + b);
+      for (int i = 0; i < 8; ++i)
+        codes[r * (K / 2) + b * 8 + i] = static_cast<uint8_t>(q[2 * i] | (q[2 * i + 1] << 4));
+    }
+  return 0;
+}
+
+// Prepared NVFP4 weights ([DM] "prepare weights before the call"): E matrices
+// [rows, K] (bf16, consecutive), each with its own dequantisation scale
+// scale[e] = amax(W[e]) / (6 * 448) (1 for an all-zero matrix), quantised along
+// K with encode scale 1 / scale[e].
+int orc_prepare_nvfp4(int E, long rows, int K, const uint16_t* in, uint8_t* codes,
+                      uint8_t* scales, float* scale) {
+  if (K % 16) return -1;
+  for (int e = 0; e < E; ++e) {
+    const uint16_t* w = in + (size_t)e * rows * K;
+    float amax = 0;
+    for (long i = 0; i < rows * K; ++i) {
+      const float v = std::fabs(bf16_to_float(w[i]));
+      if (v > amax) amax = v;
+    }
+    const float se = amax > 0 ? amax / 2688.0f : 1.0f;
+    scale[e] = se;
+    orc_quant_nvfp4(rows, K, w, 1.0f / se, codes + (size_t)e * rows * (K / 2),
+                    scales + (size_t)e * rows * (K / 16));
+  }
+  return 0;
+}
+
+// NVFP4 inference forward for the listed tokens ([DM]: NVFP4 is inference-only;
+// [NV-M]: static activation scales).  Prepared weights (orc_prepare_nvfp4):
+//   w13q [E, 2I, d/2], w13s [E, 2I, d/16], w13_scale [E]
+//   w2q  [E, d, I/2],  w2s  [E, d, I/16],  w2_scale  [E]
+// x_scale, h_scale: the static dequantisation scales of x and h.
+//   y [ntok, d] (R6), optional a [ntok, k, 2I] (R1), h [ntok, k, I] (R2)
+int orc_forward_nvfp4(int T, int d, int I, int E, int k, float clamp,
+                      const uint16_t* x, const int32_t* ids, const float* scores,
+                      const uint8_t* w13q, const uint8_t* w13s, const float* w13_scale,
+                      const uint8_t* w2q, const uint8_t* w2s, const float* w2_scale,
+                      float x_scale, float h_scale, int ntok, const int32_t* toks, uint16_t* y,
+                      uint16_t* a_out, uint16_t* h_out) {
+  Problem p = make_problem(T, d, I, E, k, clamp, x, ids, scores, nullptr, nullptr);
+  const NvScales sc{x_scale, h_scale, w13_scale, w2_scale};
+#pragma omp parallel for schedule(dynamic)
+  for (int n = 0; n < ntok; ++n) {
+    std::vector<uint16_t> a(2 * I), h(I), ys((size_t)k * d);
+    std::vector<char> ok(k);
+    int t = toks ? toks[n] : n;
+    for (int j = 0; j < k; ++j) {
+      ok[j] = element_valid(p, t, j);
+      const size_t nj = (size_t)n * k + j;
+      if (!ok[j]) {
+        if (a_out) std::memset(a_out + nj * 2 * I, 0, sizeof(uint16_t) * 2 * I);
+        if (h_out) std::memset(h_out + nj * I, 0, sizeof(uint16_t) * I);
+        continue;
+      }
+      int e = ids[(size_t)t * k + j];
+      float s = scores[(size_t)t * k + j];
+      row_forward_nv(p, t, e, s, w13q, w13s, w2q, w2s, sc, a.data(), h.data(),
+                     ys.data() + (size_t)j * d);
+      if (a_out) std::memcpy(a_out + nj * 2 * I, a.data(), sizeof(uint16_t) * 2 * I);
+      if (h_out) std::memcpy(h_out + nj * I, h.data(), sizeof(uint16_t) * I);
+    }
+    for (int c = 0; c < d; ++c) {
+      real acc = 0;
+      for (int j = 0; j < k; ++j)
+        if (ok[j]) acc += bf(ys[(size_t)j * d + c]);
+      y[(size_t)n * d + c] = real_to_bf16(acc);                 // R6
+    }
+  }
+  return 0;
 }
 
 }  // extern "C"

@@ -68,6 +68,12 @@ class Oracle:
         L.orc_forward_mxfp8.argtypes = [i32] * 5 + [f32] + [vp] * 7 + [i32, vp, vp, vp]
         L.orc_backward_mxfp8.argtypes = [i32] * 5 + [f32] + [vp] * 12 + [i32] + [vp] * 6
         L.orc_wgrad_expert_mxfp8.argtypes = [i32] * 5 + [f32] + [vp] * 12 + [i32, vp, vp]
+        L.orc_e2m1_encode.argtypes = [vp, vp, i64]
+        L.orc_e2m1_decode.argtypes = [vp, vp, i64]
+        L.orc_quant_nvfp4.argtypes = [i64, i32, vp, f32, vp, vp]
+        L.orc_prepare_nvfp4.argtypes = [i32, i64, i32, vp, vp, vp, vp]
+        L.orc_forward_nvfp4.argtypes = ([i32] * 5 + [f32] + [vp] * 9 + [f32, f32, i32, vp]
+                                        + [vp] * 3)
         L.orc_threads.restype = i32
         L.orc_set_threads.argtypes = [i32]
         L.orc_set_threads.restype = i32
@@ -257,6 +263,79 @@ class Oracle:
                                                *[_ptr(np.ascontiguousarray(w)) for w in bw],
                                                _ptr(dy), int(e), _ptr(d13), _ptr(d2))
         return d13, d2, rows
+
+
+def _nvfp4_methods(cls):
+    """NVFP4 entry points (E2M1 codes, E4M3 scales per 16 elements, per-tensor
+    scale)."""
+
+    def e2m1_encode(self, v):
+        v = np.ascontiguousarray(v, np.float64)
+        out = np.empty(v.shape, np.uint8)
+        self.lib.orc_e2m1_encode(_ptr(v), _ptr(out), v.size)
+        return out
+
+    def e2m1_decode(self, c):
+        c = np.ascontiguousarray(c, np.uint8)
+        out = np.empty(c.shape, np.float64)
+        self.lib.orc_e2m1_decode(_ptr(c), _ptr(out), c.size)
+        return out
+
+    def quant_nvfp4(self, m, g):
+        """bf16 [..., K] with encode scale g -> (packed codes uint8 [..., K/2],
+        E4M3 scales uint8 [..., K/16])."""
+        m = np.ascontiguousarray(m, np.uint16)
+        K = m.shape[-1]
+        rows = m.size // K
+        codes = np.empty(m.shape[:-1] + (K // 2,), np.uint8)
+        scales = np.empty(m.shape[:-1] + (K // 16,), np.uint8)
+        rc = self.lib.orc_quant_nvfp4(rows, K, _ptr(m), float(g), _ptr(codes), _ptr(scales))
+        assert rc == 0
+        return codes, scales
+
+    def prepare_nvfp4(self, w):
+        """bf16 [E, rows, K] -> (codes [E, rows, K/2], scales [E, rows, K/16],
+        per-expert dequantisation scales float32 [E])."""
+        w = np.ascontiguousarray(w, np.uint16)
+        E, rows, K = w.shape
+        codes = np.empty((E, rows, K // 2), np.uint8)
+        scales = np.empty((E, rows, K // 16), np.uint8)
+        sc = np.empty(E, np.float32)
+        rc = self.lib.orc_prepare_nvfp4(E, rows, K, _ptr(w), _ptr(codes), _ptr(scales), _ptr(sc))
+        assert rc == 0
+        return codes, scales, sc
+
+    def forward_nvfp4(self, x, ids, scores, w13p, w2p, x_scale, h_scale, clamp=0.0, toks=None,
+                      intermediates=False):
+        """w13p = prepare_nvfp4(W13), w2p = prepare_nvfp4(W2)."""
+        T, d = x.shape
+        k = ids.shape[1]
+        E, I2, _ = w13p[0].shape
+        I = I2 // 2
+        toks_a = None if toks is None else np.ascontiguousarray(toks, np.int32)
+        n = T if toks is None else toks_a.size
+        y = np.empty((n, d), np.uint16)
+        a = h = None
+        if intermediates:
+            a = np.empty((n, k, 2 * I), np.uint16)
+            h = np.empty((n, k, I), np.uint16)
+        c = lambda v: np.ascontiguousarray(v)
+        self.lib.orc_forward_nvfp4(T, d, I, E, k, float(clamp), _ptr(c(x)), _ptr(c(ids)),
+                                   _ptr(c(scores)), _ptr(c(w13p[0])), _ptr(c(w13p[1])),
+                                   _ptr(c(np.asarray(w13p[2], np.float32))), _ptr(c(w2p[0])),
+                                   _ptr(c(w2p[1])), _ptr(c(np.asarray(w2p[2], np.float32))),
+                                   float(x_scale), float(h_scale), n, _ptr(toks_a), _ptr(y),
+                                   _ptr(a), _ptr(h))
+        if intermediates:
+            return y, dict(a=a, h=h)
+        return y
+
+    for f in (e2m1_encode, e2m1_decode, quant_nvfp4, prepare_nvfp4, forward_nvfp4):
+        setattr(cls, f.__name__, f)
+    return cls
+
+
+_nvfp4_methods(Oracle)
 
 
 def load_oracle(kind="float"):

@@ -573,3 +573,166 @@ def test_mxfp8_forward_matches_fp64_dequantised(orc):
             o = w2d[e] @ deq(hh[None])[0]
             yref[t] += f32(bits(inp["scores"][t, j] * o))
     assert _rel_fro(f32(y), yref) < 5e-3
+
+
+# ---------------------------------------------------------------------------
+# NVFP4: E2M1 elements, E4M3 scales per 16 elements, per-tensor scale
+
+# The E2M1 magnitudes in code order (1 sign, 2 exponent bits with bias 1, 1
+# mantissa bit; exponent 0 subnormal), written from the format's definition.
+E2M1_MAG = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def _e2m1_brute(v):
+    """Nearest E2M1 code by brute force over the eight magnitudes (ties to the
+    even code, saturation to 6, sign kept)."""
+    v = np.asarray(v, np.float64)
+    m = np.minimum(np.abs(v), 6.0)
+    dist = np.abs(m[..., None] - E2M1_MAG)                      # [..., 8]
+    best = dist.min(-1, keepdims=True)
+    cand = dist == best
+    # among equally near codes prefer an even one (mantissa bit 0)
+    even = cand & (np.arange(8) % 2 == 0)
+    code = np.where(even.any(-1), even.argmax(-1), cand.argmax(-1))
+    return (code | np.where(np.signbit(v), 8, 0)).astype(np.uint8)
+
+
+def test_e2m1_codes_roundtrip_ties_and_brute_force(orc):
+    codes = np.arange(16, dtype=np.uint8)
+    vals = orc.e2m1_decode(codes)
+    assert np.array_equal(np.abs(vals[:8]), E2M1_MAG) and np.array_equal(vals[8:], -E2M1_MAG)
+    assert np.array_equal(orc.e2m1_encode(vals), codes)           # every code round-trips
+    # midpoints between neighbours go to the even code
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+    assert orc.e2m1_encode(mids).tolist() == [0, 2, 2, 4, 4, 6, 6]
+    assert orc.e2m1_encode(-mids).tolist() == [8, 10, 10, 12, 12, 14, 14]
+    # saturation and signed zero
+    assert orc.e2m1_encode(np.array([6.0, 7.0, 1e30, -9.0, -0.0, -0.2])).tolist() == \
+        [7, 7, 7, 15, 8, 8]
+    grid = np.linspace(-8, 8, 64001)
+    assert np.array_equal(orc.e2m1_encode(grid), _e2m1_brute(grid))
+
+
+def _nv_quant_ref(v_bits, g):
+    """NVFP4 block quantisation restated in numpy/torch: fp32 arithmetic, torch's
+    float8_e4m3fn conversion (after explicit saturation) for the block scale,
+    brute-force E2M1 for the elements.  Returns (codes unpacked [..., K], scales)."""
+    v = f32(v_bits)
+    K = v.shape[-1]
+    blk = v.reshape(v.shape[:-1] + (K // 16, 16))
+    amax = np.abs(blk).max(-1)
+    t = (amax / np.float32(6.0)).astype(np.float32) * np.float32(g)
+    t = np.minimum(t.astype(np.float32), np.float32(448.0))
+    sf = torch.from_numpy(np.ascontiguousarray(t)).to(torch.float8_e4m3fn)
+    S = sf.float().numpy()
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = (np.float32(g) / S).astype(np.float32)
+        q = _e2m1_brute((blk * r[..., None]).astype(np.float32))
+    q = np.where((S == 0)[..., None], 0, q).astype(np.uint8)
+    return q.reshape(v.shape), sf.view(torch.uint8).numpy()
+
+
+def _unpack(p):
+    return np.stack([p & 15, p >> 4], -1).reshape(p.shape[:-1] + (2 * p.shape[-1],))
+
+
+@pytest.mark.parametrize("g", [1.0, 64.0, 1.0 / 3.0, 2688.0 / 5.5])
+def test_nvfp4_block_quantiser_matches_restatement(orc, g):
+    rng = np.random.default_rng(int(g * 1000) % 97)
+    v = rng.standard_normal((40, 128)).astype(np.float32) * \
+        np.exp2(rng.integers(-12, 8, (40, 1))).astype(np.float32)
+    v[0] = 0.0                                   # all-zero blocks
+    v[1, :16] = 1e-30                            # a scale that rounds to zero
+    v[2, 16:32] = -v[2, 16:32]
+    vb = bits(v)
+    codes, scales = orc.quant_nvfp4(vb, g)
+    q, sf = _nv_quant_ref(vb, g)
+    assert np.array_equal(scales, sf)
+    assert np.array_equal(_unpack(codes), q)
+    assert np.all(scales[0] == 0) and np.all(codes[0] == 0)
+
+
+def test_nvfp4_prepared_weights_per_expert_scale(orc):
+    inp = small(T=8, d=64, I=32, E=3, k=2, seed=17)
+    w = inp["w13"].copy()
+    w[1] = 0                                     # an all-zero expert: scale 1
+    codes, scales, sc = orc.prepare_nvfp4(w)
+    amax = np.abs(f32(w)).reshape(3, -1).max(1)
+    want = np.where(amax > 0, (amax / np.float32(2688.0)).astype(np.float32), np.float32(1.0))
+    assert np.array_equal(sc, want.astype(np.float32))
+    for e in range(3):
+        q, sf = _nv_quant_ref(w[e], np.float32(1.0) / sc[e])
+        assert np.array_equal(scales[e], sf) and np.array_equal(_unpack(codes[e]), q)
+    # the largest block of each non-empty expert uses the top of the E4M3 range
+    assert scales[0].max() == 0x7E and scales[2].max() == 0x7E
+
+
+def _grid_values(rng, shape):
+    """E2M1 grid values with +-6 in every 16-element block (so the block amax is 6)."""
+    v = rng.choice(np.concatenate([E2M1_MAG, -E2M1_MAG[1:]]), size=shape)
+    v[..., ::16] = np.where(rng.random(v[..., ::16].shape) < 0.5, 6.0, -6.0)
+    return v.astype(np.float32)
+
+
+def test_nvfp4_forward_reduces_to_bf16_on_grid_values(orc):
+    """Inputs exactly representable with block scale 64 and per-tensor scale
+    1/64: the NVFP4 pre-activations a equal the bf16 forward's bit for bit (the
+    sums differ only by the exact factor 64 * 64 * 2^-12)."""
+    rng = np.random.default_rng(3)
+    T, d, I, E, k = 12, 64, 32, 3, 2
+    inp = small(T=T, d=d, I=I, E=E, k=k, seed=19)
+    x = _grid_values(rng, (T, d))
+    w13 = _grid_values(rng, (E, 2 * I, d))
+    w2 = _grid_values(rng, (E, d, I))
+    xb, w13b, w2b = bits(x), bits(w13), bits(w2)
+    pack = lambda q: (q[..., 0::2] | (q[..., 1::2] << 4)).astype(np.uint8)
+    sf64 = 0x68                                  # E4M3 code of 64 = 2^6
+    w13p = (pack(orc.e2m1_encode(w13)), np.full((E, 2 * I, d // 16), sf64, np.uint8),
+            np.full(E, 1 / 64, np.float32))
+    w2p = (pack(orc.e2m1_encode(w2)), np.full((E, d, I // 16), sf64, np.uint8),
+           np.full(E, 1 / 64, np.float32))
+    assert orc.e4m3_decode(np.array([sf64], np.uint8))[0] == 64.0
+    _, it = orc.forward_nvfp4(xb, inp["ids"], inp["scores"], w13p, w2p, 1 / 64, 1 / 64,
+                              intermediates=True)
+    _, ib = orc.forward(xb, inp["ids"], inp["scores"], w13b, w2b, intermediates=True)
+    assert np.array_equal(it["a"], ib["a"])
+    assert np.array_equal(it["h"], ib["h"])
+
+
+def test_nvfp4_forward_matches_fp64_dequantised(orc):
+    """NVFP4 forward = FP64 matmuls of the dequantised operands (quantised by the
+    numpy/torch restatement), with the same alpha and bf16 points."""
+    T, d, I, E, k = 16, 128, 64, 4, 2
+    inp = small(T=T, d=d, I=I, E=E, k=k, seed=23)
+    w13p = orc.prepare_nvfp4(inp["w13"])
+    w2p = orc.prepare_nvfp4(inp["w2"])
+    xs = np.float32(np.abs(f32(inp["x"])).max() / 2688.0)
+    hs = np.float32(0.05)
+    y, it = orc.forward_nvfp4(inp["x"], inp["ids"], inp["scores"], w13p, w2p, xs, hs,
+                              intermediates=True)
+
+    def deq(b, g):
+        q, sf = _nv_quant_ref(b, g)
+        S = torch.from_numpy(sf).view(torch.float8_e4m3fn).double().numpy()
+        val = np.where(q >= 8, -1.0, 1.0) * E2M1_MAG[q & 7]
+        return val * np.repeat(S, 16, axis=-1)
+
+    xd = deq(inp["x"], np.float32(1) / xs)
+    yref = np.zeros((T, d))
+    for t in range(T):
+        for j in range(k):
+            e = inp["ids"][t, j]
+            w13d = deq(inp["w13"][e], np.float32(1) / w13p[2][e])
+            w2d = deq(inp["w2"][e], np.float32(1) / w2p[2][e])
+            a = bits(float(xs * w13p[2][e]) * (w13d @ xd[t]))
+            assert np.mean(a == it["a"][t, j]) > 0.97
+            G, U = f32(a[:I]).astype(np.float64), f32(a[I:]).astype(np.float64)
+            hh = bits(G / (1 + np.exp(-G)) * U)
+            assert np.mean(hh == it["h"][t, j]) > 0.95
+            o = float(hs * w2p[2][e]) * (w2d @ deq(hh[None], np.float32(1) / hs)[0])
+            yref[t] += f32(bits(inp["scores"][t, j] * o))
+    assert _rel_fro(f32(y), yref) < 5e-3
+    # a wrong nibble order would not pass
+    swapped = (w13p[0] >> 4) | ((w13p[0] & 15) << 4)
+    y2 = orc.forward_nvfp4(inp["x"], inp["ids"], inp["scores"], (swapped,) + w13p[1:], w2p, xs, hs)
+    assert _rel_fro(f32(y2), yref) > 0.1
