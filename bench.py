@@ -39,6 +39,7 @@ METRIC = "routed-expert TFLOP/s (fwd; fwd+bwd) at T=8192 E=128 k=8; % of GB300 t
 WORKLOAD = "train_e128"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_OVER_BF16 = 2.0    # nominal dense E4M3 / bf16 tensor throughput ratio (4.5 / 2.25 PFLOP/s)
+FP4_OVER_BF16 = 6.0    # nominal dense E2M1 / bf16 tensor throughput ratio (13.5 / 2.25 PFLOP/s)
 NOMINAL_HBM_GBS = 8000.0   # nominal HBM3e bandwidth of the part (~8 TB/s), beside the measured copy rate
 
 FWD_STAGES = ["dispatch", "gather_x", "w13_swiglu", "w2_score", "combine_y"]
@@ -770,9 +771,75 @@ def run_extra(moe, name, train, args, dev, ws, tpeak, pk):
            "ms_per_step": ms, "steps": K, "stages": stages,
            "rows_per_expert": {"max": int(counts.max()), "median": float(np.median(counts)),
                                "empty": int((counts == 0).sum())}}
+    if not train and d % 256 == 0 and I % 256 == 0:
+        out["nvfp4"] = run_nvfp4(moe, plan, D, c, args, dev, ws, tpeak, model, stage_ms)
     del plan, D
     torch.cuda.empty_cache()
     return out
+
+
+def run_nvfp4(moe, bplan, D, c, args, dev, ws, tpeak, model, bf16_stage_ms):
+    """NVFP4 inference forward on the same inputs: static activation scales from a
+    calibration on them (amax / (6 * 448) of x and of the bf16 forward's h, device
+    amax), prepared weights, then the timed loop and the stage table."""
+    import torch
+
+    T, d, I, E, k = c["T"], c["d"], c["I"], c["E"], c["k"]
+    n = int(bplan.buffer("off_pad", torch.int32)[-1].item())
+    x_amax = float(moe.amax_bf16(D["x"]).item())
+    h_amax = float(moe.amax_bf16(bplan.buffer("h", torch.bfloat16)[: n * I]).item())
+    prep = moe.prepare_weights_nvfp4(D["w13"], D["w2"])
+    plan = moe.MoePlan(T, d, I, E, k, precision=moe.MOE_PREC_NVFP4, clamp=c["clamp"], flags=0,
+                       device=dev)
+    plan.set_activation_scales(x_amax / 2688.0, h_amax / 2688.0)
+    y = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        plan.forward_nvfp4(D["x"], D["ids"], D["scores"], prep, y=y)
+
+    for _ in range(args.warmup):
+        step()
+    K = args.extra_steps
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(K):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(t0.elapsed_time(t1), dev) / K
+    evf = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    for ev in [e for s_ in evf for e in s_]:
+        ev.record(stream)
+    torch.cuda.synchronize()
+    for i in range(K):
+        plan.set_timing_events(0, evf[i])
+        step()
+    torch.cuda.synchronize()
+    plan.set_timing_events(0, None)
+    rc, det = plan.check()
+    if rc != 0:
+        raise RuntimeError("device error %d (%d) in the NVFP4 forward" % (rc, det))
+    fp4_peak = tpeak * FP4_OVER_BF16
+    stages = {}
+    for j, name in enumerate(FWD_STAGES):
+        t_ms = sum(evf[i][j].elapsed_time(evf[i][j + 1]) for i in range(K)) / K
+        bound, fl, by = model[name]
+        ent = {"ms": round(t_ms, 5)}
+        if fl:
+            ach = fl / (t_ms * 1e-3) / 1e12
+            ent.update(achieved=round(ach, 1), unit="TFLOP/s", peak=fp4_peak,
+                       frac=round(ach / fp4_peak, 4))
+        stages[name] = ent
+    return {"workload": "infer_e16 sizes and inputs, NVFP4 (E2M1, E4M3 scales per 16, "
+                        "per-tensor scales) inference forward, static activation scales "
+                        "calibrated on the same inputs",
+            "value": 6.0 * T * k * d * I * ws / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "ms_per_step": ms, "steps": K,
+            "peak_note": "fp4 peak = bf16 tensor peak x %g (nominal ratio)" % FP4_OVER_BF16,
+            "stages": stages}
 
 
 def main():

@@ -61,6 +61,8 @@ extern "C" {
 /* ---- precisions ------------------------------------------------------------ */
 #define MOE_PREC_BF16   0   /* bf16 operands, fp32 accumulate                     */
 #define MOE_PREC_MXFP8  1   /* E4M3 operands with E8M0 scales per 32 along K      */
+#define MOE_PREC_NVFP4  2   /* E2M1 operands with E4M3 scales per 16 along K and
+                               per-tensor scales; inference only                   */
 
 /* ---- workspace flags ------------------------------------------------------- */
 #define MOE_WS_TRAINING     1  /* keep forward activations and backward buffers */
@@ -286,6 +288,73 @@ int moe_prepare_weights_mxfp8_backward(const void* w13, const void* w2, int d, i
                                        uint8_t* w2t_codes, uint8_t* w2t_scales, void* stream);
 
 /*
+ * NVFP4 inference ("Dist-MoE" note, "What it is selling": NVFP4 is
+ * inference-only, refuses a training context and takes prepared weights;
+ * nvfp4moe README, "Dense GEMM" / "Grouped GEMM": packed E2M1 values, blocked
+ * E4M3 scale factors and a per-tensor dequantisation scale whose product is the
+ * GEMM's alpha; "MoE layer": static activation scales set by calibration or
+ * from a checkpoint).  Block rule: a tensor with per-tensor dequantisation
+ * scale s has encode scale g = 1/s; each 16-element block along K with amax A
+ * gets the E4M3 scale code E4M3((A / 6) * g) and its elements
+ * E2M1(v * (g / S)), S the scale's value (fp32 arithmetic, round to nearest
+ * even, saturating; S = 0 gives zero codes).  Codes are packed two per byte,
+ * element 2i in the low nibble.
+ *
+ * An NVFP4 plan (precision MOE_PREC_NVFP4; d % 256 == 0, I % 256 == 0) takes
+ * only an inference workspace (flags 0; MOE_ERR_UNSUPPORTED for
+ * MOE_WS_TRAINING or MOE_WS_HOST_STAGING) and runs moe_forward_nvfp4 only
+ * (moe_forward returns MOE_ERR_UNSUPPORTED).
+ */
+
+/*
+ * Static activation scales of an NVFP4 plan: the per-tensor dequantisation
+ * scales of the routed activation rows (x_scale) and of h (h_scale), e.g.
+ * amax / (6 * 448) of calibration data (moe_amax_bf16).  Values beyond the
+ * calibrated range saturate.  Both > 0 and finite (MOE_ERR_INVALID_ARG).
+ */
+int moe_plan_set_activation_scales(moe_plan* plan, float x_scale, float h_scale);
+
+/*
+ * Prepared NVFP4 weights: W13 [E,2I,d] quantised along d and W2 [E,d,I] along I,
+ * each expert with its own dequantisation scale amax(W[e]) / (6 * 448) (1 for
+ * an all-zero expert):
+ *   w13_codes [E, 2I, d/2], w2_codes [E, d, I/2]   packed E2M1
+ *   w13_sf, w2_sf                                  E4M3 scales, tiled: rows in
+ *       blocks of 128, K in groups of 64 elements (four 16-element blocks); each
+ *       (row block, K group) a 512-byte chunk, chunk index block*(K/64) + k/64,
+ *       row r = row%128 and block j = (k/16)%4 at byte 16*(r%32) + 4*(r/32) + j;
+ *       W13 row blocks per expert and 64-column n-tile (64 gate rows, then the
+ *       same 64 up rows), W2 plain 128-row blocks of [E*d]
+ *   w13_scale, w2_scale [E] fp32 (device)
+ * Buffer sizes from moe_nvfp4_weight_bytes (which: 0 W13 codes, 1 W13 scales,
+ * 2 W2 codes, 3 W2 scales).  d % 256 == 0, I % 256 == 0.
+ */
+size_t moe_nvfp4_weight_bytes(int d, int I, int E, int which);
+int moe_prepare_weights_nvfp4(const void* w13, const void* w2, int d, int I, int E,
+                              uint8_t* w13_codes, uint8_t* w13_sf, float* w13_scale,
+                              uint8_t* w2_codes, uint8_t* w2_sf, float* w2_scale, void* stream);
+
+/*
+ * NVFP4 inference forward: x [T,d] bf16, ids, scores as moe_forward; weights
+ * from moe_prepare_weights_nvfp4.  The routed x rows are quantised along d with
+ * the static x scale; gate/up = bf16(alpha13 * sum) with alpha13 = x_scale *
+ * w13_scale[e] (R1); h = bf16(silu(G) * U) (R2) quantised along I with the
+ * static h scale; ys = bf16(s * (alpha2 * sum)), alpha2 = h_scale * w2_scale[e]
+ * (R3); y = the fixed-order combine (R6).  MOE_ERR_STATE if the activation
+ * scales were not set.
+ */
+int moe_forward_nvfp4(moe_plan* plan, const void* x, const int32_t* ids, const float* scores,
+                      const uint8_t* w13_codes, const uint8_t* w13_sf, const float* w13_scale,
+                      const uint8_t* w2_codes, const uint8_t* w2_sf, const float* w2_scale,
+                      void* y, void* stream);
+
+/*
+ * amax = max |in[i]| over n bf16 values (device pointers; amax is one fp32 on
+ * the device), for calibrating static NVFP4 scales.
+ */
+int moe_amax_bf16(const void* in, long long n, float* amax, void* stream);
+
+/*
  * Synchronise the device, read and clear the plan's device error word.
  * Returns MOE_OK or the first recorded device error; *detail (may be NULL)
  * receives its detail (for MOE_ERR_BAD_IDS the smallest offending flat index).
@@ -303,6 +372,8 @@ const char* moe_status_string(int status);
  *   MOE_BUF_ROW_OF    int32 [T*k]    padded row of element t*k+j (-1: dropped)
  *   MOE_BUF_TOKEN_OF  int32 [Rpad]   token of each padded row (-1: padding)
  *   MOE_BUF_SCORE_OF  fp32  [Rpad]   score of each padded row (0: padding)
+ *   (NVFP4 plans: MOE_BUF_XQ / XSF / HQ / HSF hold packed E2M1 codes [Rpad, d/2],
+ *   [Rpad, I/2] and their tiled E4M3 scales)
  *   MOE_BUF_XE        bf16  [Rpad,d] gathered activations
  *   MOE_BUF_A         bf16  [Rpad,2I] gate/up pre-activations (training)
  *   MOE_BUF_H         bf16  [Rpad,I] SwiGLU output (bf16 plans; MXFP8 plans keep

@@ -21,13 +21,16 @@ from .binding import (  # noqa: F401
     MOE_OK,
     MOE_PREC_BF16,
     MOE_PREC_MXFP8,
+    MOE_PREC_NVFP4,
     MOE_WS_HOST_STAGING,
     MOE_WS_TRAINING,
     MoeError,
     MoePlan,
+    amax_bf16,
     gemm_bf16,
     lib,
     prepare_weights_mxfp8,
     prepare_weights_mxfp8_backward,
+    prepare_weights_nvfp4,
     quantize_mxfp8,
 )

@@ -17,6 +17,7 @@ MOE_ERR_CUDA = 6
 MOE_ERR_UNSUPPORTED = 7
 MOE_PREC_BF16 = 0
 MOE_PREC_MXFP8 = 1
+MOE_PREC_NVFP4 = 2
 MOE_WS_TRAINING = 1
 MOE_WS_HOST_STAGING = 2
 MOE_BUF = dict(m_indptr=0, off_pad=1, row_of=2, token_of=3, score_of=4, xe=5, a=6, h=7, ys=8,
@@ -67,6 +68,12 @@ def _declare(L):
     L.moe_prepare_weights_mxfp8.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp, vp]
     L.moe_prepare_weights_mxfp8_backward.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp, vp]
     L.moe_backward_mxfp8.argtypes = [vp] * 11
+    L.moe_plan_set_activation_scales.argtypes = [vp, f32, f32]
+    L.moe_nvfp4_weight_bytes.argtypes = [i32, i32, i32, i32]
+    L.moe_nvfp4_weight_bytes.restype = sz
+    L.moe_prepare_weights_nvfp4.argtypes = [vp, vp, i32, i32, i32] + [vp] * 7
+    L.moe_forward_nvfp4.argtypes = [vp] * 12
+    L.moe_amax_bf16.argtypes = [vp, ctypes.c_longlong, vp, vp]
     L.moe_plan_launch_count.argtypes = [vp]
     L.moe_plan_launch_count.restype = ctypes.c_longlong
     for name in ("moe_plan_set_swiglu_clamp", "moe_plan_set_workspace", "moe_forward",
@@ -74,7 +81,9 @@ def _declare(L):
                  "moe_backward", "moe_step_host", "moe_quantize_mxfp8", "moe_plan_check",
                  "moe_plan_buffer", "moe_gemm_bf16", "moe_plan_set_timing_events",
                  "moe_prepare_weights_mxfp8", "moe_plan_set_debug", "moe_plan_set_cta_pairs",
-                 "moe_prepare_weights_mxfp8_backward", "moe_backward_mxfp8"):
+                 "moe_prepare_weights_mxfp8_backward", "moe_backward_mxfp8",
+                 "moe_plan_set_activation_scales", "moe_prepare_weights_nvfp4",
+                 "moe_forward_nvfp4", "moe_amax_bf16"):
         getattr(L, name).restype = i32
     return L
 
@@ -159,6 +168,23 @@ class MoePlan:
                                         _p(score_of), _p(w13), _p(w2), _p(ys), _p(row_of), _p(y),
                                         _stream(stream)), "forward_routed")
         return ys, y
+
+    def set_activation_scales(self, x_scale, h_scale):
+        """Static NVFP4 activation dequantisation scales (see moe.h)."""
+        _check(lib().moe_plan_set_activation_scales(self.ptr, float(x_scale), float(h_scale)),
+               "set_activation_scales")
+
+    def forward_nvfp4(self, x, ids, scores, prepared, y=None, stream=None):
+        """NVFP4 inference forward; prepared = prepare_weights_nvfp4(w13, w2)."""
+        import torch
+
+        if y is None:
+            y = torch.empty(self.T, self.d, dtype=torch.bfloat16, device=x.device)
+        w13q, w13s, w13c, w2q, w2s, w2c = prepared
+        _check(lib().moe_forward_nvfp4(self.ptr, _p(x), _p(ids), _p(scores), _p(w13q), _p(w13s),
+                                       _p(w13c), _p(w2q), _p(w2s), _p(w2c), _p(y),
+                                       _stream(stream)), "forward_nvfp4")
+        return y
 
     def backward(self, dy, w13, w2, dw13, dw2, dx=None, dscores=None, stream=None):
         import torch
@@ -266,6 +292,38 @@ def prepare_weights_mxfp8(w13, w2, stream=None):
     _check(L.moe_prepare_weights_mxfp8(_p(w13), _p(w2), d, I, E, _p(w13q), _p(w13s), _p(w2q),
                                        _p(w2s), _stream(stream)), "prepare_weights_mxfp8")
     return w13q, w13s, w2q, w2s
+
+
+def prepare_weights_nvfp4(w13, w2, stream=None):
+    """bf16 W13 [E,2I,d], W2 [E,d,I] -> (w13 codes, w13 tiled scales, w13 per-expert
+    scales, w2 codes, w2 tiled scales, w2 per-expert scales), the prepared NVFP4
+    weights of moe_forward_nvfp4."""
+    import torch
+
+    E, I2, d = w13.shape
+    I = I2 // 2
+    L = lib()
+    dev = w13.device
+    nb = lambda which: L.moe_nvfp4_weight_bytes(d, I, E, which)
+    w13q = torch.empty(E, I2, d // 2, dtype=torch.uint8, device=dev)
+    w13s = torch.empty(nb(1), dtype=torch.uint8, device=dev)
+    w2q = torch.empty(E, d, I // 2, dtype=torch.uint8, device=dev)
+    w2s = torch.empty(nb(3), dtype=torch.uint8, device=dev)
+    w13c = torch.empty(E, dtype=torch.float32, device=dev)
+    w2c = torch.empty(E, dtype=torch.float32, device=dev)
+    _check(L.moe_prepare_weights_nvfp4(_p(w13), _p(w2), d, I, E, _p(w13q), _p(w13s), _p(w13c),
+                                       _p(w2q), _p(w2s), _p(w2c), _stream(stream)),
+           "prepare_weights_nvfp4")
+    return w13q, w13s, w13c, w2q, w2s, w2c
+
+
+def amax_bf16(t, stream=None):
+    """max |t| of a bf16 device tensor, as a one-element fp32 device tensor."""
+    import torch
+
+    out = torch.empty(1, dtype=torch.float32, device=t.device)
+    _check(lib().moe_amax_bf16(_p(t), t.numel(), _p(out), _stream(stream)), "amax_bf16")
+    return out
 
 
 def prepare_weights_mxfp8_backward(w13, w2, stream=None):

@@ -13,6 +13,7 @@
 // synchronises (moe_plan_check and moe_plan_set_workspace excepted).
 
 #include <climits>
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <new>
@@ -70,8 +71,13 @@ struct moe_plan {
   CUtensorMap tm_rx, tm_rys;
   const void *rx_cached, *rys_cached;
   long long rx_rows, rys_rows;
-  // MXFP8: quantised expert-major activations and h, with tiled scales
+  // MXFP8: quantised expert-major activations and h, with tiled scales (NVFP4:
+  // the same buffers hold packed E2M1 codes and E4M3 scales)
   uint8_t *xq, *xsf, *hq, *hsf;
+  // NVFP4: static activation dequantisation scales (0: not set) and the weight maps
+  float nv_x_scale, nv_h_scale;
+  CUtensorMap tm_w13nv, tm_w2nv;
+  const void *w13nv_cached, *w2nv_cached;
   int ngr_d, ngr_I;                 // 128-element scale groups along d and along I
   CUtensorMap tm_xq, tm_hq, tm_w13q, tm_w2q;
   const void *w13q_cached, *w2q_cached;
@@ -249,8 +255,16 @@ size_t layout(moe_plan* p, char* base, int flags) {
   p->token_of = reinterpret_cast<int32_t*>(take(4 * RP));
   p->score_of = reinterpret_cast<float*>(take(4 * RP));
   const bool mx = p->precision == MOE_PREC_MXFP8;
-  p->xe = mx ? nullptr : reinterpret_cast<uint16_t*>(take(2 * RP * d));
+  const bool nv = p->precision == MOE_PREC_NVFP4;
+  p->xe = (mx || nv) ? nullptr : reinterpret_cast<uint16_t*>(take(2 * RP * d));
   p->xq = p->xsf = p->hq = p->hsf = nullptr;
+  if (nv) {
+    // packed E2M1 codes, E4M3 scales per 16 elements (tiled, 64-element K groups)
+    p->xq = reinterpret_cast<uint8_t*>(take(RP * d / 2));
+    p->xsf = reinterpret_cast<uint8_t*>(take((size_t)nv_sf_bytes(RP, (int)d)));
+    p->hq = reinterpret_cast<uint8_t*>(take(RP * I / 2));
+    p->hsf = reinterpret_cast<uint8_t*>(take((size_t)nv_sf_bytes(RP, (int)I)));
+  }
   if (mx) {
     p->xq = reinterpret_cast<uint8_t*>(take(RP * d));
     p->xsf = reinterpret_cast<uint8_t*>(take((size_t)mx_sf_bytes(RP, (int)d)));
@@ -258,7 +272,7 @@ size_t layout(moe_plan* p, char* base, int flags) {
     p->hsf = reinterpret_cast<uint8_t*>(take((size_t)mx_sf_bytes(RP, (int)I)));
   }
   // bf16 h: the W2 operand of bf16 plans (MXFP8 plans keep only its E4M3 codes)
-  p->h = mx ? nullptr : reinterpret_cast<uint16_t*>(take(2 * RP * I));
+  p->h = (mx || nv) ? nullptr : reinterpret_cast<uint16_t*>(take(2 * RP * I));
   p->ys = reinterpret_cast<uint16_t*>(take(2 * RP * d));
   p->a = p->dye = p->dA = p->hs = p->dxe = nullptr;
   p->pdscore = nullptr;
@@ -477,9 +491,12 @@ int moe_plan_row_granule(const moe_plan* p) { return p ? p->gran : 0; }
 moe_plan* moe_plan_create(int T, int d, int I, int E, int k, int precision) {
   if (T < 1 || d < 128 || I < 64 || d % 128 || I % 64 || k < 1 || E < k || E > 256) return nullptr;
   if ((long long)T * k >= (1LL << 31) - (long long)E * kBM) return nullptr;
-  if (precision != MOE_PREC_BF16 && precision != MOE_PREC_MXFP8) return nullptr;
-  // MXFP8: K loops in 128-element stages (scales travel with each stage)
+  if (precision != MOE_PREC_BF16 && precision != MOE_PREC_MXFP8 && precision != MOE_PREC_NVFP4)
+    return nullptr;
+  // MXFP8: K loops in 128-element stages (scales travel with each stage); NVFP4:
+  // 256-element stages along d (W13) and I (W2)
   if (precision == MOE_PREC_MXFP8 && I % 128) return nullptr;
+  if (precision == MOE_PREC_NVFP4 && (I % 256 || d % 256)) return nullptr;
   moe_plan* p = new (std::nothrow) moe_plan;
   if (!p) return nullptr;
   memset(p, 0, sizeof(*p));
@@ -546,6 +563,8 @@ size_t moe_plan_workspace_bytes(const moe_plan* p, int flags) {
 
 int moe_plan_set_workspace(moe_plan* p, void* ws, size_t bytes, int flags) {
   if (!p || !ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return MOE_ERR_INVALID_ARG;
+  // NVFP4 is inference-only: it refuses a training workspace
+  if (p->precision == MOE_PREC_NVFP4 && (flags & MOE_WS_TRAINING)) return MOE_ERR_UNSUPPORTED;
   if (bytes < moe_plan_workspace_bytes(p, flags)) return MOE_ERR_WORKSPACE;
   if ((flags & MOE_WS_HOST_STAGING) && !p->side) {
     const unsigned ef = cudaEventDisableTiming;
@@ -569,7 +588,16 @@ int moe_plan_set_workspace(moe_plan* p, void* ws, size_t bytes, int flags) {
   p->dw13_cached = p->dw2_cached = nullptr;
   p->w13q_cached = p->w2q_cached = nullptr;
   p->rx_cached = p->rys_cached = nullptr;
+  p->w13nv_cached = p->w2nv_cached = nullptr;
   const long long RP = p->RP;
+  if (p->precision == MOE_PREC_NVFP4) {
+    if (encode_tmap_u8(&p->tm_xq, p->xq, RP, p->d / 2, 128) ||
+        encode_tmap_u8(&p->tm_hq, p->hq, RP, p->I / 2, 128) ||
+        encode_tmap_bf16(&p->tm_ys, p->ys, RP, p->d, 128))
+      return MOE_ERR_CUDA;
+    if (flags & MOE_WS_HOST_STAGING) return MOE_ERR_UNSUPPORTED;
+    return reset_error_word(p->err);
+  }
   p->w13t_cached = p->w2t_cached = nullptr;
   if (p->precision == MOE_PREC_MXFP8) {
     if (encode_tmap_u8(&p->tm_xq, p->xq, RP, p->d, 128) ||
@@ -616,6 +644,7 @@ int moe_forward(moe_plan* p, const void* x, const int32_t* ids, const float* sco
   if (!aligned16(x) || !aligned16(w13) || !aligned16(w2) || !aligned16(y))
     return MOE_ERR_INVALID_ARG;
   if (!p->ws) return MOE_ERR_WORKSPACE;
+  if (p->precision == MOE_PREC_NVFP4) return MOE_ERR_UNSUPPORTED;   // moe_forward_nvfp4
   const bool mx = p->precision == MOE_PREC_MXFP8;
   if (save_for_backward && !(p->ws_flags & MOE_WS_TRAINING)) return MOE_ERR_WORKSPACE;
   if (mx && (!w13_sf || !w2_sf || !aligned16(w13_sf) || !aligned16(w2_sf)))
@@ -1045,6 +1074,105 @@ int moe_forward_routed(moe_plan* p, const void* x_e, long long rows, const int32
   return MOE_OK;
 }
 
+int moe_plan_set_activation_scales(moe_plan* p, float x_scale, float h_scale) {
+  if (!p || !(x_scale > 0.f) || !(h_scale > 0.f) || !std::isfinite(x_scale) ||
+      !std::isfinite(h_scale))
+    return MOE_ERR_INVALID_ARG;
+  if (p->precision != MOE_PREC_NVFP4) return MOE_ERR_UNSUPPORTED;
+  p->nv_x_scale = x_scale;
+  p->nv_h_scale = h_scale;
+  return MOE_OK;
+}
+
+// NVFP4 inference forward ("Dist-MoE" note, "What it is selling": NVFP4 is
+// inference-only with prepared weights; nvfp4moe README, "MoE layer": dispatch,
+// BF16 activation quantisation, FC1 + gated activation + NVFP4 requantisation,
+// FC2, probability weighting, deterministic combine):
+//   route -> gather x rows + quantise (static input scale) -> NVFP4 W13 GEMM +
+//   SwiGLU + h quantisation (static hidden scale) -> NVFP4 W2 GEMM x score ->
+//   combine
+int moe_forward_nvfp4(moe_plan* p, const void* x, const int32_t* ids, const float* scores,
+                      const uint8_t* w13q, const uint8_t* w13_sf, const float* w13_scale,
+                      const uint8_t* w2q, const uint8_t* w2_sf, const float* w2_scale, void* y,
+                      void* stream_v) {
+  if (!p || !x || !ids || !scores || !w13q || !w13_sf || !w13_scale || !w2q || !w2_sf ||
+      !w2_scale || !y)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w13q) || !aligned16(w2q) || !aligned16(w13_sf) ||
+      !aligned16(w2_sf) || !aligned16(y))
+    return MOE_ERR_INVALID_ARG;
+  if (p->precision != MOE_PREC_NVFP4) return MOE_ERR_UNSUPPORTED;
+  if (!p->ws) return MOE_ERR_WORKSPACE;
+  if (!(p->nv_x_scale > 0.f) || !(p->nv_h_scale > 0.f)) return MOE_ERR_STATE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream_v);
+  const int d = p->d, I = p->I, E = p->E;
+  if (w13q != p->w13nv_cached) {
+    // (K bytes, 64, gate/up, I/64, E): two 64-row blocks of gate then up rows
+    if (encode_tmap_gate_up_blocks(&p->tm_w13nv, w13q, E, I, d / 2)) return MOE_ERR_CUDA;
+    p->w13nv_cached = w13q;
+  }
+  if (w2q != p->w2nv_cached) {
+    if (encode_tmap_u8(&p->tm_w2nv, w2q, (long long)E * d, I / 2, 256)) return MOE_ERR_CUDA;
+    p->w2nv_cached = w2q;
+  }
+  mark(p, 0, 0, st);
+  RouteArgs ra{};
+  ra.ids = ids; ra.scores = scores;
+  ra.T = p->T; ra.k = p->k; ra.E = E; ra.BM = p->gran; ra.nblk = p->nblk;
+  ra.blockcounts = p->blockcounts; ra.counts = p->counts; ra.m_indptr = p->m_indptr;
+  ra.off_pad = p->off_pad; ra.num_mtiles = p->num_mtiles; ra.tile_expert = p->tile_expert;
+  ra.expert_order = p->expert_order; ra.num_nonempty = p->num_nonempty;
+  ra.row_of = p->row_of; ra.token_of = p->token_of; ra.score_of = p->score_of; ra.err = p->err;
+  cudaError_t e = launch_route(ra, st);
+  if (e != cudaSuccess) return cuda_status(e);
+  p->launches += 3;
+  mark(p, 0, 1, st);
+  // gather + quantise along d with the static input scale (encode scale 1/x_scale)
+  e = launch_gather_quant_nvfp4(x, p->token_of, p->off_pad + E, d, 1.0f / p->nv_x_scale, p->xq,
+                                p->xsf, gather_grid(p), st);
+  if (e != cudaSuccess) return cuda_status(e);
+  p->launches += 1;
+  mark(p, 0, 2, st);
+  {
+    GemmArgs g = rows_args(p);
+    g.k_blocks = d / 256;
+    g.b_expert_rows = 2 * I;
+    g.b_half_rows = I;
+    g.n_tiles = I / 128;
+    g.ld0 = I / 2;                       // row stride of hq (bytes)
+    g.sfa = p->xsf; g.sfb = w13_sf; g.sf_ngr = d / 64; g.b_blocks_per_expert = I / 64;
+    g.hq = p->hq; g.hsf = p->hsf; g.hsf_ngr = I / 64;
+    g.w_scale = w13_scale; g.act_scale = p->nv_x_scale; g.h_enc = 1.0f / p->nv_h_scale;
+    g.k_rotate = 1;
+    g.stall_mma = p->dbg_stall_w13;
+    e = launch_gemm_nvfp4(EPI_SWIGLU, p->tm_xq, p->tm_w13nv, p->tm_ys, g, p->num_sms, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    p->launches += 1;
+    mark(p, 0, 3, st);
+  }
+  {
+    GemmArgs g = rows_args(p);
+    g.k_blocks = I / 256;
+    g.b_expert_rows = d;
+    g.n_tiles = d / 256;
+    g.out0 = p->ys; g.ld0 = d;
+    g.row_scale = p->score_of;
+    g.sfa = p->hsf; g.sfb = w2_sf; g.sf_ngr = I / 64; g.b_blocks_per_expert = d / 128;
+    g.w_scale = w2_scale; g.act_scale = p->nv_h_scale;
+    g.k_rotate = 1;
+    e = launch_gemm_nvfp4(EPI_SCORE, p->tm_hq, p->tm_w2nv, p->tm_ys, g, p->num_sms, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    p->launches += 1;
+    mark(p, 0, 4, st);
+  }
+  e = launch_combine(p->ys, p->row_of, p->T, p->k, d, y, nullptr, 0, nullptr, gather_grid(p), st);
+  if (e != cudaSuccess) return cuda_status(e);
+  p->launches += 1;
+  mark(p, 0, 5, st);
+  p->saved = 0;
+  return MOE_OK;
+}
+
 int moe_step_host(moe_plan* p, const void* x_host, const int32_t* ids_host,
                   const float* scores_host, const void* dy_host, const void* w13, const void* w2,
                   float* dw13, float* dw2, void* y_host, void* dx_host, float* dscores_host,
@@ -1126,6 +1254,36 @@ int moe_plan_set_debug(moe_plan* p, long long wait_limit_ns, int stall_w13) {
   return MOE_OK;
 }
 
+size_t moe_nvfp4_weight_bytes(int d, int I, int E, int which) {
+  if (d <= 0 || I <= 0 || E <= 0 || d % 256 || I % 256) return 0;
+  if (which == 0) return (size_t)E * 2 * I * d / 2;                                  // W13 codes
+  if (which == 1) return (size_t)nv_sf_bytes((long long)E * (I / 64) * 128, d);      // W13 scales
+  if (which == 2) return (size_t)E * d * I / 2;                                      // W2 codes
+  if (which == 3) return (size_t)nv_sf_bytes((long long)E * d, I);                   // W2 scales
+  return 0;
+}
+
+int moe_prepare_weights_nvfp4(const void* w13, const void* w2, int d, int I, int E,
+                              uint8_t* w13_codes, uint8_t* w13_sf, float* w13_scale,
+                              uint8_t* w2_codes, uint8_t* w2_sf, float* w2_scale, void* stream) {
+  if (!w13 || !w2 || !w13_codes || !w13_sf || !w13_scale || !w2_codes || !w2_sf || !w2_scale)
+    return MOE_ERR_INVALID_ARG;
+  if (d <= 0 || I <= 0 || E <= 0 || d % 256 || I % 256) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w13) || !aligned16(w2) || !aligned16(w13_codes) || !aligned16(w2_codes) ||
+      (reinterpret_cast<uintptr_t>(w13_sf) & 3) || (reinterpret_cast<uintptr_t>(w2_sf) & 3))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_prepare_nvfp4(w13, E, 2LL * I, d, I, w13_codes, w13_sf, w13_scale, st);
+  if (e != cudaSuccess) return cuda_status(e);
+  return cuda_status(launch_prepare_nvfp4(w2, E, (long long)d, I, 0, w2_codes, w2_sf, w2_scale, st));
+}
+
+int moe_amax_bf16(const void* in, long long n, float* amax, void* stream) {
+  if (!in || !amax || n < 0 || !aligned16(in)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_amax_bf16(in, 1, n, reinterpret_cast<unsigned int*>(amax),
+                                      static_cast<cudaStream_t>(stream)));
+}
+
 size_t moe_mxfp8_weight_scale_bytes(int d, int I, int E, int which) {
   if (d <= 0 || I <= 0 || E <= 0 || d % 128 || I % 128) return 0;
   if (which == 0) return (size_t)mx_sf_bytes((long long)E * (I / 64) * 128, d);   // W13
@@ -1192,6 +1350,7 @@ int moe_plan_check(moe_plan* p, long long* detail) {
 int moe_plan_buffer(const moe_plan* p, int which, void** ptr, size_t* bytes) {
   if (!p || !p->ws || !ptr) return MOE_ERR_INVALID_ARG;
   const size_t RP = p->RP, d = p->d, I = p->I, E = p->E;
+  const bool nvp = p->precision == MOE_PREC_NVFP4;
   void* q = nullptr;
   size_t b = 0;
   switch (which) {
@@ -1208,10 +1367,16 @@ int moe_plan_buffer(const moe_plan* p, int which, void** ptr, size_t* bytes) {
     case MOE_BUF_DA: q = p->dA; b = 2 * RP * 2 * I; break;
     case MOE_BUF_HS: q = p->hs; b = 2 * RP * I; break;
     case MOE_BUF_DXE: q = p->dxe; b = 2 * RP * d; break;
-    case MOE_BUF_XQ: q = p->xq; b = RP * d; break;
-    case MOE_BUF_XSF: q = p->xsf; b = (size_t)mx_sf_bytes((long long)RP, (int)d); break;
-    case MOE_BUF_HQ: q = p->hq; b = RP * I; break;
-    case MOE_BUF_HSF: q = p->hsf; b = (size_t)mx_sf_bytes((long long)RP, (int)I); break;
+    case MOE_BUF_XQ: q = p->xq; b = nvp ? RP * d / 2 : RP * d; break;
+    case MOE_BUF_XSF:
+      q = p->xsf;
+      b = (size_t)(nvp ? nv_sf_bytes((long long)RP, (int)d) : mx_sf_bytes((long long)RP, (int)d));
+      break;
+    case MOE_BUF_HQ: q = p->hq; b = nvp ? RP * I / 2 : RP * I; break;
+    case MOE_BUF_HSF:
+      q = p->hsf;
+      b = (size_t)(nvp ? nv_sf_bytes((long long)RP, (int)I) : mx_sf_bytes((long long)RP, (int)I));
+      break;
     case MOE_BUF_XQT: q = p->xqT; b = (size_t)d * RP; break;
     case MOE_BUF_XQTSF: q = p->xqTsf; b = (size_t)mx_sf_bytes((long long)d, (int)RP); break;
     case MOE_BUF_DAQ: q = p->dAq; b = RP * 2 * I; break;

@@ -6,6 +6,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -294,6 +295,21 @@ __device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdes
                : "memory");
 }
 
+// D[tmem] (+)= (A . sfa) * (B . sfb)^T, kind::mxf4nvf4 with one E4M3 scale per 16
+// K-elements of each row (block_scale.scale_vec::4X): packed E2M1 operands, K = 64
+// per instruction, each row's four scale bytes in one 32-bit TMEM column.
+__device__ __forceinline__ void umma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
 // Contiguous global -> shared bulk copy (size and addresses multiples of 16 bytes).
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
                                          uint32_t bar) {
@@ -322,6 +338,13 @@ __host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N) {
 }
 __device__ __forceinline__ uint32_t idesc_sf_ids(uint32_t base, uint32_t sfa_id, uint32_t sfb_id) {
   return base | (sfb_id << 4) | (sfa_id << 29);
+}
+
+// Instruction descriptor, kind::mxf4nvf4 block-scaled: E2M1 A and B (format code 1
+// in bits 7-9 and 10-12 for this kind), fp32 D, UE4M3 scales (bit 23 = 0), scale
+// ids 0 (scale_vec::4X reads all four bytes of a scale column).
+__host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // ---------------------------------------------------------------------------
@@ -480,6 +503,58 @@ __device__ __forceinline__ uint8_t mx_quant32(const float (&f)[32], uint32_t (&o
     out[q] = (uint32_t)p0 | ((uint32_t)p1 << 16);
   }
   return (uint8_t)(X + 127);
+}
+
+// ---------------------------------------------------------------------------
+// NVFP4 block quantisation (E2M1 elements, E4M3 scale per 16 elements, per-tensor
+// encode scale g): sf = E4M3(RNE, satfinite)((amax / 6) * g); with S its value,
+// element codes E2M1(RNE, satfinite)(v * (g / S)); S = 0 gives all-zero codes.
+
+// Eight floats -> eight E2M1 codes, element i in bits 4i..4i+3 (round to nearest
+// even, saturating to +-6).
+__device__ __forceinline__ uint32_t cvt_e2m1x8(const float (&v)[8]) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 q0, q1, q2, q3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q3, %8, %7;\n\t"
+      "mov.b32 %0, {q0, q1, q2, q3};\n\t}"
+      : "=r"(r)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+  return r;
+}
+
+// Value of an E4M3 byte (exact, through the f16 conversion).
+__device__ __forceinline__ float e4m3_to_f32(uint8_t c) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)c));
+  return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+}
+
+// Quantise 16 values (exact bf16 values held as float) with encode scale g:
+// 16 codes in out[0..1] (element i in bits 4(i%8).. of word i/8) and the E4M3
+// scale byte as the return value.
+__device__ __forceinline__ uint8_t nv_quant16(const float (&f)[16], float g, uint32_t (&out)[2]) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  const float t = __fmul_rn(__fdiv_rn(amax, 6.0f), g);
+  const uint8_t sf = (uint8_t)(cvt_e4m3x2(t, 0.f) & 0xFFu);
+  const float S = e4m3_to_f32(sf);
+  if (!(S > 0.f)) {
+    out[0] = out[1] = 0u;
+    return sf;
+  }
+  const float r = __fdiv_rn(g, S);
+#pragma unroll
+  for (int w = 0; w < 2; ++w) {
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(f[8 * w + i], r);
+    out[w] = cvt_e2m1x8(v);
+  }
+  return sf;
 }
 
 // Byte offset of the scale of (row, 32-block kb) in the tiled scale layout the

@@ -31,15 +31,17 @@ using namespace gemm;
 
 namespace {
 
-template <int BN, int EPI, bool MX>
+template <int BN, int EPI, bool MX, bool NV = false>
 struct GemmShape {
-  // A stage holds 128 rows (A) and BN rows (B) of 128 bytes of K: 64 bf16 or
-  // 128 E4M3 elements; MXFP8 stages also carry the 512-byte scale chunks of A
-  // (one) and of B (one per 128 rows) for those 128 K-elements, padded to keep
-  // stages 1024-aligned.
+  // A stage holds 128 rows (A) and BN rows (B) of 128 bytes of K: 64 bf16, 128
+  // E4M3 or 256 E2M1 elements; MXFP8 stages also carry the 512-byte scale chunks
+  // of A (one) and of B (one per 128 rows) for those 128 K-elements, NVFP4 stages
+  // four chunks per 128 rows (one per 64-element K group), padded to keep stages
+  // 1024-aligned.
+  static_assert(!NV || MX, "NVFP4 is a block-scaled format");
   static constexpr int A_BYTES = kBM * 128;                    // 16 KB
   static constexpr int B_BYTES = BN * 128;
-  static constexpr int SF_LOAD_BYTES = MX ? 512 * (1 + BN / 128) : 0;
+  static constexpr int SF_LOAD_BYTES = MX ? (NV ? 2048 : 512) * (1 + BN / 128) : 0;
   static constexpr int SF_STAGE_BYTES = (SF_LOAD_BYTES + 1023) / 1024 * 1024;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SF_STAGE_BYTES;
   static constexpr int TX_BYTES = A_BYTES + B_BYTES + SF_LOAD_BYTES;   // bytes a stage receives
@@ -47,8 +49,9 @@ struct GemmShape {
   // expert's rows and it is bound by the gradient traffic), else bf16 sub-tile
   // buffers for the TMA-store epilogues (the MXFP8 DGRAD-W2 epilogue uses the
   // same 32 KB as 4 KB of staging per epilogue warp).
+  // (the NVFP4 W13 epilogue writes h from registers and never saves a: no staging)
   static constexpr int OUT_BYTES =
-      (EPI == EPI_WGRAD ? wgrad_bufs<MX>()
+      (NV && EPI == EPI_SWIGLU ? 0 : EPI == EPI_WGRAD ? wgrad_bufs<MX>()
                         : (MX && BN == 256 ? kMxWideBufs
                                            : (EPI == EPI_SCORE || EPI == EPI_STORE
                                                   ? kEpiStageBufs
@@ -68,20 +71,25 @@ struct GemmShape {
   // for one: their epilogue releases it as soon as it has read it.
   static constexpr int NACC = (MX && BN == 256) ? 1 : 2;
   static constexpr uint32_t SF_COL0 = NACC * BN;
-  static constexpr uint32_t SF_COLS = MX ? (BN == 256 ? 16 : 8) : 0;
+  // per stage: MXFP8 A 4 + B 4 per 128 rows; NVFP4 four times that (one set per
+  // 64-element K group), B's at +16, rounded up to 64 columns
+  static constexpr uint32_t SF_COLS = MX ? (NV ? 64 : (BN == 256 ? 16 : 8)) : 0;
   static constexpr uint32_t TMEM_COLS = MX ? 512 : 2 * BN;
   static_assert(!MX || SF_COL0 + SF_COLS * STAGES <= 512, "TMEM budget");
   static_assert(STAGES >= 3, "operand ring");
 };
 
-template <int BN, bool A_MN, bool B_MN, int EPI, bool MX>
+template <int BN, bool A_MN, bool B_MN, int EPI, bool MX, bool NV = false>
 __global__ void __launch_bounds__(kThreads, 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmO0,
                    const __grid_constant__ CUtensorMap tmO1, const GemmArgs args) {
-  using S = GemmShape<BN, EPI, MX>;
+  using S = GemmShape<BN, EPI, MX, NV>;
   constexpr int STAGES = S::STAGES;
-  constexpr uint32_t IDESC = MX ? idesc_mxf8(kBM, BN) : idesc_bf16(kBM, BN, A_MN, B_MN);
+  constexpr uint32_t IDESC =
+      NV ? idesc_nvf4(kBM, BN) : (MX ? idesc_mxf8(kBM, BN) : idesc_bf16(kBM, BN, A_MN, B_MN));
+  static_assert(!NV || (BN == 256 && (EPI == EPI_SWIGLU || EPI == EPI_SCORE)),
+                "NVFP4: 256-wide row GEMMs (W13 + SwiGLU, W2 x score)");
   constexpr int KE = MX ? 128 : kBK;     // K elements per stage (128 bytes per row)
   constexpr int WB = wgrad_bufs<MX>();   // WGRAD: fp32 gradient chunk buffers
   static_assert(!MX || (!A_MN && !B_MN && (BN == 128 || BN == 256)),
@@ -180,7 +188,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sa = stage0 + stage * S::STAGE_BYTES;
           const uint32_t sb = sa + S::A_BYTES;
           mbar_arrive_expect_tx(fb, S::TX_BYTES);
-          if constexpr (MX) {
+          if constexpr (NV) {
+            // the four 512-byte scale chunks of this stage's 64-element K groups
+            // (contiguous in the tiled layout): A's row block, then B's BN/128 row
+            // blocks, 2 KB each (row GEMMs only)
+            const uint32_t ssf = sb + S::B_BYTES;
+            const long long kg = 4LL * kc;
+            const long long gbr =
+                (long long)ti.e * args.b_blocks_per_expert + (long long)ti.nt * (BN / 128);
+            bulk_g2s(ssf, args.sfa + ((long long)(ti.m0 >> 7) * args.sf_ngr + kg) * 512, 2048u, fb);
+#pragma unroll
+            for (int rb = 0; rb < BN / 128; ++rb)
+              bulk_g2s(ssf + 2048u * (uint32_t)(1 + rb),
+                       args.sfb + ((gbr + rb) * args.sf_ngr + kg) * 512, 2048u, fb);
+          } else if constexpr (MX) {
             // the 512-byte scale chunks of this K group: A's row block, then B's
             // BN/128 row blocks
             const uint32_t ssf = sb + S::B_BYTES;
@@ -278,7 +299,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           const uint32_t sa = stage0 + stage * S::STAGE_BYTES;
           const uint32_t sb = sa + S::A_BYTES;
-          if constexpr (MX) {
+          if constexpr (NV) {
+            // this stage's scales -> its own TMEM columns: for each 64-element K
+            // group j, A's four columns at sfa_t + 4j and B's (four per 128 rows) at
+            // sfb_t + (BN/32)j; then four K = 64 steps, step j reading group j's
+            const uint32_t ssf = sb + S::B_BYTES;
+            const uint32_t sfa_t = tmem_base + S::SF_COL0 + S::SF_COLS * (uint32_t)stage;
+            const uint32_t sfb_t = sfa_t + 16u;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              tmem_cp_32x128b_x4(sfa_t + 4u * (uint32_t)j,
+                                 smem_desc_noswz(ssf + 512u * (uint32_t)j, 512u, 128u));
+#pragma unroll
+              for (int rb = 0; rb < BN / 128; ++rb)
+                tmem_cp_32x128b_x4(sfb_t + (uint32_t)(BN / 32) * (uint32_t)j + 4u * (uint32_t)rb,
+                                   smem_desc_noswz(ssf + 2048u * (uint32_t)(1 + rb) +
+                                                       512u * (uint32_t)j,
+                                                   512u, 128u));
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint64_t adesc = smem_desc_sw128(sa + j * 32, 16, 1024);
+              const uint64_t bdesc = smem_desc_sw128(sb + j * 32, 16, 1024);
+              umma_nvf4(d_tmem, adesc, bdesc, IDESC, sfa_t + 4u * (uint32_t)j,
+                        sfb_t + (uint32_t)(BN / 32) * (uint32_t)j, (kb | j) != 0 ? 1u : 0u);
+            }
+          } else if constexpr (MX) {
             // this stage's scales -> its own TMEM columns (reused only after the
             // stage is released, i.e. after these MMAs have completed); then four
             // 32-element K steps, step j reading scale byte j
@@ -352,8 +398,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
       if constexpr (S::NACC == 1) {
         // one accumulator: read it, release it, then compute the outputs
-        epilogue_mx_wide<EPI>(args, ti, row, tbase, half, &tmO0, &tmO1,
-                              stage0 + STAGES * S::STAGE_BYTES, et, tempty_bar(0));
+        epilogue_mx_wide<EPI, NV>(args, ti, row, tbase, half, &tmO0, &tmO1,
+                                  stage0 + STAGES * S::STAGE_BYTES, et, tempty_bar(0));
         acc_phase ^= 1u;
         continue;
       } else if constexpr (EPI == EPI_WGRAD) {
@@ -387,12 +433,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN, bool A_MN, bool B_MN, int EPI, bool MX>
+template <int BN, bool A_MN, bool B_MN, int EPI, bool MX, bool NV = false>
 cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                        const CUtensorMap& to0, const CUtensorMap& to1, const GemmArgs& args,
                        int grid, cudaStream_t stream) {
-  auto kern = k_grouped_gemm<BN, A_MN, B_MN, EPI, MX>;
-  const int smem = GemmShape<BN, EPI, MX>::SMEM_BYTES;
+  auto kern = k_grouped_gemm<BN, A_MN, B_MN, EPI, MX, NV>;
+  const int smem = GemmShape<BN, EPI, MX, NV>::SMEM_BYTES;
   static std::atomic<unsigned long long> configured{0};   // devices this kernel is set up on
   const cudaError_t e = smem_optin_once(kern, smem, configured);
   if (e != cudaSuccess) return e;
@@ -400,6 +446,18 @@ cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUten
 }
 
 }  // namespace
+
+cudaError_t launch_gemm_nvfp4(int epi, const CUtensorMap& ta, const CUtensorMap& tb,
+                              const CUtensorMap& to0, const GemmArgs& args, int grid,
+                              cudaStream_t stream) {
+  if (epi == EPI_SWIGLU)
+    return launch_one<256, false, false, EPI_SWIGLU, true, true>(ta, tb, ta, to0, to0, args, grid,
+                                                                 stream);
+  if (epi == EPI_SCORE)
+    return launch_one<256, false, false, EPI_SCORE, true, true>(ta, tb, ta, to0, to0, args, grid,
+                                                                stream);
+  return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_gemm(int epi, int bn, bool a_mn, bool b_mn, const CUtensorMap& ta,
                         const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& to0,

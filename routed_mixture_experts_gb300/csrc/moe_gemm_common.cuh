@@ -276,7 +276,10 @@ __device__ __forceinline__ void epi_stage_wide(const CUtensorMap* tm, uint32_t o
 //     leaves through shared-memory staging and TMA stores (tmO1).
 //   W2 x score (R3) and the plain store (R5): output columns n0 + 128*half ...,
 //     in two 64-column sub-tiles through staging (tmO0).
-template <int EPI>
+//   NVFP4 (NV): the accumulator is first multiplied by alpha = act_scale *
+//     w_scale[e]; h is quantised to NVFP4 along I (16-element blocks, encode
+//     scale h_enc: 32 code bytes and one word of four scale bytes per thread).
+template <int EPI, bool NV = false>
 __device__ __forceinline__ void epilogue_mx_wide(const GemmArgs& a, const TileInfo& ti, int row,
                                                  uint32_t tbase, int half,
                                                  const CUtensorMap* tmO0,
@@ -289,7 +292,43 @@ __device__ __forceinline__ void epilogue_mx_wide(const GemmArgs& a, const TileIn
   tc_fence_before();
   mbar_arrive(release);
   const long long grow = (long long)ti.m0 + row;
-  if constexpr (EPI == EPI_SWIGLU) {
+  if constexpr (NV) {
+    const float alpha = a.act_scale * a.w_scale[ti.e];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int q = 0; q < 16; ++q) v[i][q] = __float_as_uint(__uint_as_float(v[i][q]) * alpha);
+  }
+  if constexpr (NV && EPI == EPI_SWIGLU) {
+    const int c0 = ti.nt * 128 + 64 * half;
+    uint32_t sc = 0;
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      float hv[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int c = 32 * s + i;
+        const float G = bf2f(f2bf(__uint_as_float(v[c >> 4][c & 15])));          // R1
+        const float U = bf2f(f2bf(__uint_as_float(v[4 + (c >> 4)][c & 15])));
+        hv[i] = bf2f(f2bf(swiglu_fwd(G, U, a.clamp)));                              // R2
+      }
+      uint32_t w[4];
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        float f[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) f[i] = hv[16 * b + i];
+        uint32_t q[2];
+        sc |= (uint32_t)nv_quant16(f, a.h_enc, q) << (16 * s + 8 * b);
+        w[2 * b] = q[0];
+        w[2 * b + 1] = q[1];
+      }
+      *reinterpret_cast<uint4*>(a.hq + grow * a.ld0 + (c0 + 32 * s) / 2) =
+          make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    *reinterpret_cast<uint32_t*>(a.hsf + mx_sf_offset(grow >> 7, (int)(grow & 127), c0 >> 4,
+                                                      a.hsf_ngr)) = sc;
+  } else if constexpr (EPI == EPI_SWIGLU) {
     const int c0 = ti.nt * 128 + 64 * half;
     // R1 first: gate and up to bf16 pairs (a's values), which frees the fp32 copies
     uint32_t pg[32], pu[32];

@@ -103,8 +103,15 @@ struct GemmArgs {
   int sf_ngr;                // 128-element K groups (512-byte scale chunks) per row block
   int b_blocks_per_expert;
   uint8_t* hq;               // EPI_SWIGLU (MXFP8): h quantised along I, codes [rows, I]
+                             // (NVFP4: packed E2M1 codes [rows, I/2])
   uint8_t* hsf;              // ... and its tiled scales
   int hsf_ngr;
+  // NVFP4: the accumulator is multiplied by alpha = act_scale * w_scale[e] (the
+  // per-tensor dequantisation scales of the activation and of expert e's weights)
+  // before its rounding point; EPI_SWIGLU quantises h with encode scale h_enc
+  const float* w_scale;
+  float act_scale;
+  float h_enc;
   // EPI_DGRAD2 (MXFP8): dA and hs leave only as E4M3 codes with tiled scales: dA
   // along 2I (q_row [rows, 2I], sf_row with sf_row_ngr K groups), dA and hs along
   // the rows, transposed (qt_a [2I, qt_ld], qt_h [I, qt_ld]; scales sft_a, sft_h
@@ -150,6 +157,30 @@ cudaError_t launch_gemm(int epi, int bn, bool a_mn, bool b_mn, const CUtensorMap
                         const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& to0,
                         const CUtensorMap& to1, const GemmArgs& args, int grid,
                         cudaStream_t stream, bool mx = false);
+
+// The NVFP4 grouped GEMM (kind::mxf4nvf4, E4M3 scales per 16 elements): 128 x 256
+// tiles over routed rows, K-major packed E2M1 operands (uint8 tensor maps over
+// [rows, K/2]), scales in the tiled layout with 64-element K groups (sf_ngr =
+// K/64).  EPI_SWIGLU (W13 through the gate/up block view; h quantised to NVFP4)
+// or EPI_SCORE (W2, bf16 ys through tmO0).
+cudaError_t launch_gemm_nvfp4(int epi, const CUtensorMap& ta, const CUtensorMap& tb,
+                              const CUtensorMap& to0, const GemmArgs& args, int grid,
+                              cudaStream_t stream);
+
+// NVFP4 quantisers (moe_nvfp4.cu).  Scale bytes of the tiled layout for
+// rows_padded128 rows and K columns: rows/128 x K/64 chunks of 512 bytes.
+long long nv_sf_bytes(long long rows_padded128, int K);
+// padded rows r < *nrows: quantise x[token_of[r]] (zero for padding) along d
+cudaError_t launch_gather_quant_nvfp4(const void* x, const int32_t* token_of, const int32_t* nrows,
+                                      int d, float g, uint8_t* codes, uint8_t* sf, int grid,
+                                      cudaStream_t stream);
+// amax[m] (float bits) of nmat consecutive bf16 matrices of `per` elements
+cudaError_t launch_amax_bf16(const void* in, int nmat, long long per, unsigned int* amax,
+                             cudaStream_t stream);
+// prepared weights: per-expert scales scale[E], codes [E*rows, K/2], tiled scales
+// (gu_I > 0: the W13 row blocking)
+cudaError_t launch_prepare_nvfp4(const void* w, int E, long long rows_per_expert, int K, int gu_I,
+                                 uint8_t* codes, uint8_t* sf, float* scale, cudaStream_t stream);
 
 // Launch the CTA-pair grouped GEMM over routed rows (256 x 256 tiles, A K-major;
 // requires expert segments padded to 256 rows and N % 256 == 0).
