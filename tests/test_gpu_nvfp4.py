@@ -120,6 +120,7 @@ def test_nvfp4_small(moe, orc, sizes):
     # output and the requantised h
     yref, it = orc.forward_nvfp4(inp["x"], inp["ids"], inp["scores"], o13, o2, xs, hs,
                                  clamp=c.get("clamp", 0.0), intermediates=True)
+    assert np.sqrt(np.mean(f32(yref) ** 2)) > 1e-3          # a non-trivial output
     compare(f32(bits(y)), f32(yref), bf16_out=True, rel_fro=REL_FRO_MXFP8, what="y nvfp4",
             max_bad_frac=1.0)
     ro = plan.buffer("row_of", torch.int32).cpu().numpy()[: T * k].reshape(T, k)
@@ -172,5 +173,6 @@ def test_nvfp4_full_size_sampled(moe, orc):
     toks = np.array(sorted(set(rng.choice(c["T"], 1024, replace=False).tolist())
                            | {0, c["T"] - 1}), np.int32)
     yref = orc.forward_nvfp4(inp["x"], inp["ids"], inp["scores"], o13, o2, xs, hs, toks=toks)
+    assert np.sqrt(np.mean(f32(yref) ** 2)) > 1e-3
     compare(yb[toks], f32(yref), bf16_out=True, rel_fro=REL_FRO_MXFP8, what="y nvfp4 full",
             max_bad_frac=1.0)
