@@ -143,8 +143,8 @@ int moe_forward(moe_plan* plan, const void* x, const int32_t* ids, const float* 
 
 /*
  * Forward over rows the caller has already laid out expert-major (nvfp4moe
- * README, "MoE layer": frameworks that already have expert-major rows call
- * run_routed(x, m_indptr, padded_offsets, out=...)).  Dispatch and gather are
+ * README, "MoE layer": its run_routed entry takes such rows with m_indptr and
+ * the padded offsets, for callers that route on their own).  Dispatch and gather are
  * skipped; the W13 GEMM + SwiGLU and the W2 GEMM run over the caller's layout,
  * and the combine runs when row_of and y are given.  Inputs (device):
  *   x_e      [rows, d] bf16: expert e's routed rows at [off_pad[e], off_pad[e] + m_e)
@@ -288,12 +288,12 @@ int moe_prepare_weights_mxfp8_backward(const void* w13, const void* w2, int d, i
                                        uint8_t* w2t_codes, uint8_t* w2t_scales, void* stream);
 
 /*
- * NVFP4 inference ("Dist-MoE" note, "What it is selling": NVFP4 is
- * inference-only, refuses a training context and takes prepared weights;
- * nvfp4moe README, "Dense GEMM" / "Grouped GEMM": packed E2M1 values, blocked
- * E4M3 scale factors and a per-tensor dequantisation scale whose product is the
- * GEMM's alpha; "MoE layer": static activation scales set by calibration or
- * from a checkpoint).  Block rule: a tensor with per-tensor dequantisation
+ * NVFP4 inference ("Dist-MoE" note, "What it is selling": the FP4 mode serves
+ * inference only, with weights prepared ahead of the call; nvfp4moe README,
+ * "Dense GEMM" / "Grouped GEMM": E2M1 codes two to a byte, one E4M3 scale per
+ * block, one dequantisation scale per tensor, the GEMM scaled by the product of
+ * its operands' tensor scales; "MoE layer": fixed activation scales from a
+ * calibration pass or a checkpoint).  Block rule: a tensor with per-tensor dequantisation
  * scale s has encode scale g = 1/s; each 16-element block along K with amax A
  * gets the E4M3 scale code E4M3((A / 6) * g) and its elements
  * E2M1(v * (g / S)), S the scale's value (fp32 arithmetic, round to nearest

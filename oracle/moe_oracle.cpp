@@ -23,9 +23,10 @@
 //   [NV-M] same README, section "MoE layer": dispatch, FC1 + gated activation, FC2,
 //         probability weighting, deterministic combine; distinct int32 ids per row,
 //         float32 weights; padded offsets.
-//   [NV-D] same README, sections "Dense GEMM" and "Grouped GEMM": quantize returns
-//         packed E2M1 values, blocked E4M3 scale factors and the per-tensor
-//         dequantisation scale; the GEMM takes their product as alpha.
+//   [NV-D] same README, sections "Dense GEMM" and "Grouped GEMM": the quantiser
+//         yields E2M1 codes two to a byte, one E4M3 scale per block and one
+//         dequantisation scale per tensor; a GEMM is scaled by the product of its
+//         operands' tensor scales.
 //   [NV-T] same README, section "Training" and "Supported kernel surface":
 //         deterministic dispatch, combine and router gradients; input and weight
 //         gradients.
@@ -45,9 +46,9 @@
 //   * MXFP8 (OCP MX): 32-element blocks along K, E8M0 shared exponent
 //     X = floor(log2(amax)) - 8, E4M3 elements rounded to nearest even and
 //     saturated to +-448; an all-zero block gets scale code 0.
-//   * NVFP4 ([DM] "NVFP4 is infer-only ... prepare weights before the call";
-//     [NV-D] packed E2M1 values, blocked E4M3 scale factors and a per-tensor
-//     dequantisation scale; [NV-M] static activation scales): two-level scaling.
+//   * NVFP4 ([DM]: inference only, weights prepared ahead of the call; [NV-D]:
+//     E2M1 codes, E4M3 block scales, a per-tensor dequantisation scale; [NV-M]:
+//     fixed activation scales): two-level scaling.
 //     A tensor with per-tensor dequantisation scale s has encode scale g = 1/s
 //     (fp32).  A 16-element block along K with amax A gets the E4M3 scale code
 //     E4M3_RNE_satfinite((A / 6) * g), fp32 arithmetic (6 = E2M1's largest
@@ -967,7 +968,7 @@ int orc_quant_nvfp4(long rows, int K, const uint16_t* in, float g, uint8_t* code
   return 0;
 }
 
-// Prepared NVFP4 weights ([DM] "prepare weights before the call"): E matrices
+// Prepared NVFP4 weights ([DM]: weights are prepared ahead of the call): E matrices
 // [rows, K] (bf16, consecutive), each with its own dequantisation scale
 // scale[e] = amax(W[e]) / (6 * 448) (1 for an all-zero matrix), quantised along
 // K with encode scale 1 / scale[e].

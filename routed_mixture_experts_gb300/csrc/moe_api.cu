@@ -987,7 +987,7 @@ int moe_backward_mxfp8(moe_plan* p, const void* dy, const uint8_t* w13t, const u
 }
 
 // Forward over a caller-provided expert-major layout (nvfp4moe README, "MoE
-// layer": frameworks with expert-major rows call run_routed): check the layout
+// layer": the run_routed entry for callers that route on their own): check the layout
 // and list its m tiles -> W13 GEMM + SwiGLU -> W2 GEMM (x score_of) into the
 // caller's ys -> optionally combine into y.  Dispatch and gather are skipped.
 int moe_forward_routed(moe_plan* p, const void* x_e, long long rows, const int32_t* m_indptr,
