@@ -66,6 +66,10 @@ def parse():
                     help="time the steps as one CUDA graph replay (stage events as graph nodes)")
     ap.add_argument("--cta-pairs", action="store_true",
                     help="W13, W2 and DGRAD-W13 on CTA pairs (moe_plan_set_cta_pairs)")
+    ap.add_argument("--dp-allreduce", action="store_true",
+                    help="with --gpus N > 1: sum the weight gradients over the ranks after "
+                         "every backward (one data-parallel training step instead of N "
+                         "independent replicas)")
     ap.add_argument("--extra-steps", type=int, default=30,
                     help="timed steps of the inference (E=16) and skewed-routing workloads "
                          "(0: skip)")
@@ -252,6 +256,20 @@ def barrier():
         dist.barrier()
 
 
+def allreduce_grads(tensors):
+    """Data-parallel split of the training step: after the backward each rank holds
+    the weight-gradient increments of its own tokens; summing the fp32 gradient
+    buffers over the ranks gives every rank the step's full gradient.  Works on
+    any backend (NCCL for device tensors, gloo for CPU tensors); a no-op on one
+    rank."""
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return
+    for t in tensors:
+        dist.all_reduce(t, op=dist.ReduceOp.SUM)
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle timing (reference arm and cpu_baseline)
 
@@ -359,9 +377,13 @@ def run_ours(args):
     dsc = torch.empty(T, k, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
+    dp = args.dp_allreduce and ws > 1
+
     def step():
         plan.forward(D["x"], D["ids"], D["scores"], D["w13"], D["w2"], y=y, save=True)
         plan.backward(D["dy"], D["w13"], D["w2"], D["dw13"], D["dw2"], dx=dx, dscores=dsc)
+        if dp:
+            allreduce_grads((D["dw13"], D["dw2"]))
 
     for _ in range(args.warmup):
         step()
@@ -666,7 +688,10 @@ def run_ours(args):
         "config": {"workload": "%s (T=%d, d=%d, I=%d, E=%d, k=%d, uniform routing, "
                                "forward+backward)" % (WORKLOAD, T, d, I, E, k),
                    "tokens_per_gpu": T, "l2": "inputs larger than L2 (%.1f GB resident per GPU)"
-                   % (ws_bytes / 1e9), "parallelism": "replicas" if ws > 1 else "single GPU",
+                   % (ws_bytes / 1e9),
+                   "parallelism": ("data parallel, weight gradients summed over ranks (NCCL "
+                                   "all-reduce) every step" if dp else "replicas")
+                   if ws > 1 else "single GPU",
                    "launch": "CUDA graph replay of the timed steps" if args.graph
                              else "eager launches"},
         "fwd_tflops": 6.0 * T * k * d * I / (fwd_ms * 1e-3) / 1e12,

@@ -1,6 +1,8 @@
 """The benchmark's multi-rank plumbing on CPU (gloo, world size 2): each rank
 reports its own timed region, the job takes the maximum, and only rank 0
-prints.  No data-path collective exists: ranks are independent replicas."""
+prints.  By default ranks are independent replicas; with --dp-allreduce the
+weight gradients are summed over the ranks after every backward, through the
+same function tested here on CPU tensors."""
 
 import json
 import os
@@ -53,6 +55,47 @@ def test_max_over_ranks_gloo(tmp_path):
     res = [json.load(open(o)) for o in outs]
     assert all(r["max"] == 15.0 for r in res)
     assert sorted(r["rank"] for r in res) == [0, 1] and all(r["ws"] == 2 for r in res)
+
+
+def _grad_worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import torch
+    import torch.distributed as dist
+
+    import bench
+
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    # each rank's fp32 gradient increments of its own tokens (as the backward
+    # leaves them), two buffers of the shapes dW13 [E, 2I, d] and dW2 [E, d, I]
+    g = torch.Generator().manual_seed(100 + rank)
+    dw13 = torch.randn(3, 8, 16, generator=g)
+    dw2 = torch.randn(3, 16, 4, generator=g)
+    mine = (dw13.clone(), dw2.clone())
+    bench.allreduce_grads((dw13, dw2))
+    dist.destroy_process_group()
+    torch.save({"mine": mine, "sum": (dw13, dw2)}, out)
+
+
+def test_dp_allreduce_sums_weight_gradients_gloo(tmp_path):
+    import torch
+    import torch.multiprocessing as mp
+
+    port = _free_port()
+    outs = [str(tmp_path / ("g%d.pt" % r)) for r in range(2)]
+    ctx = mp.get_context("spawn")
+    procs = [ctx.Process(target=_grad_worker, args=(r, 2, port, outs[r])) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    res = [torch.load(o) for o in outs]
+    for i in range(2):
+        want = res[0]["mine"][i] + res[1]["mine"][i]
+        assert torch.allclose(res[0]["sum"][i], want) and torch.equal(res[0]["sum"][i],
+                                                                      res[1]["sum"][i])
 
 
 def test_reference_arm_prints_only_on_rank0():
