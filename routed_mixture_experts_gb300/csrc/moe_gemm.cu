@@ -16,6 +16,8 @@
 //   warps 2..9  epilogue: warp w reads TMEM lanes 32*(w%4)..+31, i.e. one output
 //               row per thread, through tcgen05.ld; warps 2..5 take the first
 //               half of the tile's columns, warps 6..9 the second
+//   warp 10     NVFP4 only: copies each stage's scale factors into TMEM
+//               (tcgen05.cp), so the MMA issuer only issues MMAs
 // The accumulator is double buffered in TMEM (2 x BN fp32 columns) so the
 // epilogue of tile i overlaps the main loop of tile i+1.
 //
@@ -79,8 +81,15 @@ struct GemmShape {
   static_assert(STAGES >= 3, "operand ring");
 };
 
+// NVFP4 kernels add a warp that copies the scale factors into tensor memory: a
+// stage's twelve copies cost as much tensor-core issue time as its MMAs when the
+// MMA thread issues them itself (a diagnostic build without them ran W13 36 %
+// faster).
+template <bool NV>
+constexpr int gemm_threads() { return NV ? kThreads + 32 : kThreads; }
+
 template <int BN, bool A_MN, bool B_MN, int EPI, bool MX, bool NV = false>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(gemm_threads<NV>(), 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmO0,
                    const __grid_constant__ CUtensorMap tmO1, const GemmArgs args) {
@@ -106,7 +115,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * S::STAGE_BYTES + S::OUT_BYTES);
-  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain, WGRAD chunk loads
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain, then WGRAD chunk
+  // loads, or (NVFP4) sf_full[STAGES] (a stage's scales are in TMEM) and sf_drain
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
@@ -114,6 +124,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
   const uint32_t wg_bar0 = bar0 + 8u * (2 * STAGES + 5);
+  auto sf_full_bar = [&](int s) { return wg_bar0 + 8u * s; };
+  const uint32_t sf_drain_bar = wg_bar0 + 8u * STAGES;
+  static_assert(8 * (3 * STAGES + 6) <= S::BAR_BYTES, "barrier space");
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -133,6 +146,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(drain_bar, 1);
     if (EPI == EPI_WGRAD)
       for (int b = 0; b < WB; ++b) mbar_init(wg_bar0 + 8u * b, 1);
+    if (NV) {
+      for (int s = 0; s < STAGES; ++s) mbar_init(sf_full_bar(s), 1);
+      mbar_init(sf_drain_bar, 1);
+    }
     fence_mbar_init();
   }
   __syncthreads();
@@ -167,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+    for (int r = 0, tile = cta_tile(args, 0); tile < num_tiles && ok; tile = cta_tile(args, ++r)) {
       const TileInfo ti = decode_tile<BN>(args, tile);
       // k_rotate (row GEMMs): the tiles that share an A tile (same m tile) or a
       // B tile (same expert and n tile) run at the same time; each starts its K
@@ -280,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+    for (int r = 0, tile = cta_tile(args, 0); tile < num_tiles && ok; tile = cta_tile(args, ++r)) {
       const TileInfo ti = decode_tile<BN>(args, tile);
       int w = 1;
       if (lane == 0) w = mbar_wait(tempty_bar(acc), acc_phase ^ 1u, &abort_s, args.err, 3, wlim);
@@ -293,6 +310,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kb = 0; kb < ti.kb; ++kb) {
         w = 1;
         if (lane == 0) w = mbar_wait(full_bar(stage), phase, &abort_s, args.err, 4, wlim);
+        // NVFP4: also wait until the scale warp's copies of this stage are in TMEM
+        if (NV && lane == 0 && w)
+          w = mbar_wait(sf_full_bar(stage), phase, &abort_s, args.err, 10, wlim);
         ok = __shfl_sync(0xffffffffu, w, 0) != 0;
         if (!ok) break;
         tc_fence_after();
@@ -300,23 +320,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sa = stage0 + stage * S::STAGE_BYTES;
           const uint32_t sb = sa + S::A_BYTES;
           if constexpr (NV) {
-            // this stage's scales -> its own TMEM columns: for each 64-element K
-            // group j, A's four columns at sfa_t + 4j and B's (four per 128 rows) at
-            // sfb_t + (BN/32)j; then four K = 64 steps, step j reading group j's
-            const uint32_t ssf = sb + S::B_BYTES;
+            // four K = 64 steps, step j reading the scale columns of 64-element K
+            // group j: A's four at sfa_t + 4j, B's (four per 128 rows) at sfb_t + (BN/32)j
             const uint32_t sfa_t = tmem_base + S::SF_COL0 + S::SF_COLS * (uint32_t)stage;
             const uint32_t sfb_t = sfa_t + 16u;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              tmem_cp_32x128b_x4(sfa_t + 4u * (uint32_t)j,
-                                 smem_desc_noswz(ssf + 512u * (uint32_t)j, 512u, 128u));
-#pragma unroll
-              for (int rb = 0; rb < BN / 128; ++rb)
-                tmem_cp_32x128b_x4(sfb_t + (uint32_t)(BN / 32) * (uint32_t)j + 4u * (uint32_t)rb,
-                                   smem_desc_noswz(ssf + 2048u * (uint32_t)(1 + rb) +
-                                                       512u * (uint32_t)j,
-                                                   512u, 128u));
-            }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const uint64_t adesc = smem_desc_sw128(sa + j * 32, 16, 1024);
@@ -376,7 +383,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_drain(drain_bar, 0);
     }
     __syncwarp();
-  } else {
+  } else if (NV && warp == kThreads / 32) {
+    // ---------------- scale-factor copies (NVFP4) ----------------
+    // For each stage the MMA issuer consumes: wait for its bytes, copy the scales
+    // of its four 64-element K groups into the stage's own TMEM columns (reused
+    // only after the stage was released, i.e. after the MMAs that read them have
+    // completed), and signal sf_full when the copies are done.
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int r = 0, tile = cta_tile(args, 0); tile < num_tiles && ok; tile = cta_tile(args, ++r)) {
+      const TileInfo ti = decode_tile<BN>(args, tile);
+      for (int kb = 0; kb < ti.kb; ++kb) {
+        int w = 1;
+        if (lane == 0) w = mbar_wait(full_bar(stage), phase, &abort_s, args.err, 11, wlim);
+        ok = __shfl_sync(0xffffffffu, w, 0) != 0;
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t ssf = stage0 + stage * S::STAGE_BYTES + S::A_BYTES + S::B_BYTES;
+          const uint32_t sfa_t = tmem_base + S::SF_COL0 + S::SF_COLS * (uint32_t)stage;
+          const uint32_t sfb_t = sfa_t + 16u;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            tmem_cp_32x128b_x4(sfa_t + 4u * (uint32_t)j,
+                               smem_desc_noswz(ssf + 512u * (uint32_t)j, 512u, 128u));
+#pragma unroll
+            for (int rb = 0; rb < BN / 128; ++rb)
+              tmem_cp_32x128b_x4(sfb_t + (uint32_t)(BN / 32) * (uint32_t)j + 4u * (uint32_t)rb,
+                                 smem_desc_noswz(ssf + 2048u * (uint32_t)(1 + rb) +
+                                                     512u * (uint32_t)j,
+                                                 512u, 128u));
+          }
+          umma_commit(sf_full_bar(stage));
+        }
+        __syncwarp();
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (abort_s && lane == 0) {
+      // drain: every copy issued so far lands before TMEM is freed
+      umma_commit(sf_drain_bar);
+      mbar_wait_drain(sf_drain_bar, 0);
+    }
+    __syncwarp();
+  } else if (warp < kThreads / 32) {
     // ---------------- epilogue (warps 2..5) ----------------
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
@@ -387,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int sub = 0;                              // output staging-buffer sequence number
     WgradPipe wp{stage0 + STAGES * S::STAGE_BYTES, wg_bar0, num_tiles, 0, 0};
     if (EPI == EPI_WGRAD && et == 0) wgrad_issue<BN, WB>(args, &tmC, wp, WB - 1);
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+    for (int r = 0, tile = cta_tile(args, 0); tile < num_tiles; tile = cta_tile(args, ++r)) {
       const TileInfo ti = decode_tile<BN>(args, tile);
       int w = 1;
       if (lane == 0) w = mbar_wait(tfull_bar(acc), acc_phase, &abort_s, args.err, 5, wlim);
@@ -439,10 +493,11 @@ cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUten
                        int grid, cudaStream_t stream) {
   auto kern = k_grouped_gemm<BN, A_MN, B_MN, EPI, MX, NV>;
   const int smem = GemmShape<BN, EPI, MX, NV>::SMEM_BYTES;
+  constexpr int threads = gemm_threads<NV>();
   static std::atomic<unsigned long long> configured{0};   // devices this kernel is set up on
   const cudaError_t e = smem_optin_once(kern, smem, configured);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, stream, ta, tb, tc, to0, to1, args);
+  return launch_pdl(kern, dim3(grid), dim3(threads), smem, stream, ta, tb, tc, to0, to1, args);
 }
 
 }  // namespace

@@ -29,6 +29,17 @@ __device__ __forceinline__ int count_tiles(const GemmArgs& a) {
   return (a.mtile_list ? *a.list_count : *a.num_mtiles) * a.n_tiles;
 }
 
+// The r-th tile of this CTA (persistent kernels: every role of a CTA walks the
+// same sequence).  Round-robin over the grid; weight-gradient tiles, which come
+// longest expert first and so shrink from one round to the next, alternate the
+// direction of each round (tile r*G + b, then r*G + G-1-b, ...), so the CTAs that
+// drew the longest tiles of one round draw the shortest of the next.  Only the
+// last round can hold tiles past the end, so the sequence ends at the first one.
+__device__ __forceinline__ int cta_tile(const GemmArgs& a, int r) {
+  const int G = (int)gridDim.x, b = (int)blockIdx.x;
+  return r * G + ((a.wgrad && (r & 1)) ? G - 1 - b : b);
+}
+
 template <int BN>
 __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int tile) {
   TileInfo ti;
@@ -622,8 +633,8 @@ __device__ __forceinline__ void epilogue_dgrad2_mx(const GemmArgs& a, const Tile
 // every thread adds its row's accumulator values to it in place, and TMA stores
 // it back.  (A TMA reduce-add in L2 does the same sum but moves fp32 data
 // measurably slower than a load and a store.)  The chunk sequence is this CTA's
-// tiles blockIdx.x, blockIdx.x + gridDim.x, ... times BN/32 chunks each; each
-// output tile is visited once per launch, so no load can see a pending store.
+// tiles (cta_tile) times BN/32 chunks each; each output tile is visited once per
+// launch, so no load can see a pending store.
 // fp32 chunk buffers of 16 KB: 4 (three loads ahead) for the 256-wide bf16
 // tiles, 5 for the 128-wide block-scaled ones (measured best for each)
 template <bool MX>
@@ -643,7 +654,7 @@ __device__ __forceinline__ void wgrad_issue(const GemmArgs& a, const CUtensorMap
   constexpr int CH = BN / 32;
   while (p.issued < upto) {
     const int n = p.issued;
-    const int tile = (int)blockIdx.x + (n / CH) * (int)gridDim.x;
+    const int tile = cta_tile(a, n / CH);
     if (tile >= p.num_tiles) return;
     const TileInfo t = decode_tile<BN>(a, tile);
     const int b = n % NB;
