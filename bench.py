@@ -40,6 +40,7 @@ WORKLOAD = "train_e128"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_OVER_BF16 = 2.0    # nominal dense E4M3 / bf16 tensor throughput ratio (4.5 / 2.25 PFLOP/s)
 FP4_OVER_BF16 = 6.0    # nominal dense E2M1 / bf16 tensor throughput ratio (13.5 / 2.25 PFLOP/s)
+WGRAD_SMS = 0          # default split of the backward (set from measurements)
 NOMINAL_HBM_GBS = 8000.0   # nominal HBM3e bandwidth of the part (~8 TB/s), beside the measured copy rate
 
 FWD_STAGES = ["dispatch", "gather_x", "w13_swiglu", "w2_score", "combine_y"]
@@ -66,6 +67,9 @@ def parse():
                     help="time the steps as one CUDA graph replay (stage events as graph nodes)")
     ap.add_argument("--cta-pairs", action="store_true",
                     help="W13, W2 and DGRAD-W13 on CTA pairs (moe_plan_set_cta_pairs)")
+    ap.add_argument("--wgrad-sms", type=int, default=WGRAD_SMS,
+                    help="SMs of the weight-gradient GEMMs running beside DGRAD-W13 in the "
+                         "backward (moe_plan_set_backward_split; 0: one stream)")
     ap.add_argument("--dp-allreduce", action="store_true",
                     help="with --gpus N > 1: sum the weight gradients over the ranks after "
                          "every backward (one data-parallel training step instead of N "
@@ -372,6 +376,8 @@ def run_ours(args):
     plan = moe.MoePlan(T, d, I, E, k, clamp=c["clamp"],
                        flags=moe.MOE_WS_TRAINING | moe.MOE_WS_HOST_STAGING, device=dev,
                        cta_pairs=args.cta_pairs)
+    if args.wgrad_sms:
+        plan.set_backward_split(args.wgrad_sms)
     y = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
     dx = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
     dsc = torch.empty(T, k, dtype=torch.float32, device=dev)
@@ -401,6 +407,8 @@ def run_ours(args):
     evb = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(KB)]
     for ev in [e for s_ in evf + evb for e in s_]:
         ev.record(stream)                       # materialise the handles
+    # (one kernel at a time here, so that every stage has its own time)
+    plan.set_backward_split(0)
     for i in range(KB):
         plan.set_timing_events(0, evf[i])
         plan.set_timing_events(1, evb[i])
@@ -408,6 +416,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     plan.set_timing_events(0, None)
     plan.set_timing_events(1, None)
+    plan.set_backward_split(args.wgrad_sms)
     stage_ms = {}
     for j, name in enumerate(FWD_STAGES):
         stage_ms[name] = sum(evf[i][j].elapsed_time(evf[i][j + 1]) for i in range(KB)) / KB
@@ -693,13 +702,15 @@ def run_ours(args):
                                    "all-reduce) every step" if dp else "replicas")
                    if ws > 1 else "single GPU",
                    "launch": "CUDA graph replay of the timed steps" if args.graph
-                             else "eager launches"},
+                             else "eager launches",
+                   "backward": ("weight gradients on %d SMs beside DGRAD-W13 (own stream)"
+                                % args.wgrad_sms) if args.wgrad_sms else "one stream"},
         "fwd_tflops": 6.0 * T * k * d * I / (fwd_ms * 1e-3) / 1e12,
         "bf16_forward": fwd_inf,
         "fwd_ms": fwd_ms,
         "e2e": e2e, "gpu_launches": int(n1 - n0), "roofline": roofline, "stages": stages,
-        "stages_note": "%d untimed steps with an event at every stage boundary; the timed steps "
-                       "record only the dominant stage's events" % KB,
+        "stages_note": "%d untimed steps with an event at every stage boundary, one kernel at "
+                       "a time; the timed steps record only the dominant stage's events" % KB,
         "cpu_baseline": cpu, "clocks": clk, "peaks": peak_note, "mxfp8_forward": mx,
         "mxfp8_training": mx_train, "infer_e16": extra.get("infer_e16"),
         "skew_pad": extra.get("skew_pad"),

@@ -445,6 +445,25 @@ int moe_plan_set_timing_events(moe_plan* plan, int which, void* const* events, i
  */
 int moe_plan_set_debug(moe_plan* plan, long long wait_limit_ns, int stall_w13);
 
+/*
+ * Concurrent backward.  wgrad_sms > 0 makes moe_backward run the two
+ * weight-gradient GEMMs (bound by the fp32 gradient traffic) on a plan-owned
+ * stream, with persistent grids of wgrad_sms CTAs, while DGRAD-W13 (bound by
+ * the tensor pipe and its operand loads) and the dX combine run on the
+ * caller's stream on the other SMs; the caller's stream then waits for the
+ * weight gradients, so the call's semantics are unchanged and the results are
+ * bit-identical (every tile is computed the same way).  0 (the default)
+ * launches every GEMM on every SM, one after the other.  With stage timing
+ * events set, the events of the weight-gradient stages are recorded on the
+ * plan's stream.  The first call with wgrad_sms > 0 creates the stream and two
+ * events (no device memory).  0 <= wgrad_sms < the number of SMs, else
+ * MOE_ERR_INVALID_ARG.  bf16 plans (moe_backward); moe_backward_mxfp8 ignores it.
+ */
+int moe_plan_set_backward_split(moe_plan* plan, int wgrad_sms);
+
+/* Number of SMs of the plan's device (the persistent kernels' grid size). */
+int moe_plan_num_sms(const moe_plan* plan);
+
 /* Number of kernels this plan has launched so far (all entry points). */
 long long moe_plan_launch_count(const moe_plan* plan);
 

@@ -74,6 +74,9 @@ def _declare(L):
     L.moe_prepare_weights_nvfp4.argtypes = [vp, vp, i32, i32, i32] + [vp] * 7
     L.moe_forward_nvfp4.argtypes = [vp] * 12
     L.moe_amax_bf16.argtypes = [vp, ctypes.c_longlong, vp, vp]
+    L.moe_plan_set_backward_split.argtypes = [vp, i32]
+    L.moe_plan_num_sms.argtypes = [vp]
+    L.moe_plan_num_sms.restype = i32
     L.moe_plan_launch_count.argtypes = [vp]
     L.moe_plan_launch_count.restype = ctypes.c_longlong
     for name in ("moe_plan_set_swiglu_clamp", "moe_plan_set_workspace", "moe_forward",
@@ -83,7 +86,7 @@ def _declare(L):
                  "moe_prepare_weights_mxfp8", "moe_plan_set_debug", "moe_plan_set_cta_pairs",
                  "moe_prepare_weights_mxfp8_backward", "moe_backward_mxfp8",
                  "moe_plan_set_activation_scales", "moe_prepare_weights_nvfp4",
-                 "moe_forward_nvfp4", "moe_amax_bf16"):
+                 "moe_forward_nvfp4", "moe_amax_bf16", "moe_plan_set_backward_split"):
         getattr(L, name).restype = i32
     return L
 
@@ -230,6 +233,13 @@ class MoePlan:
         self._ev = getattr(self, "_ev", {})
         self._ev[which] = (arr, events)          # keep the handles alive while set
         _check(lib().moe_plan_set_timing_events(self.ptr, which, arr, len(events)), "timing")
+
+    def set_backward_split(self, wgrad_sms):
+        """Weight-gradient GEMMs on wgrad_sms SMs beside DGRAD-W13 (0: off); see moe.h."""
+        _check(lib().moe_plan_set_backward_split(self.ptr, int(wgrad_sms)), "backward_split")
+
+    def num_sms(self):
+        return lib().moe_plan_num_sms(self.ptr)
 
     def set_debug(self, wait_limit_ns=0, stall_w13=False):
         """Failure-path testing knobs (see moe_plan_set_debug in moe.h)."""

@@ -108,6 +108,12 @@ struct moe_plan {
   // its gather, the backward records record_after_combine after its combine
   cudaEvent_t wait_before_gather, record_after_combine;
   int prev_step_train;   // the last moe_step_host call on this plan was a complete training step
+  // concurrent backward (moe_plan_set_backward_split): the weight-gradient GEMMs
+  // run on wgrad_sms SMs on a plan-owned stream, beside DGRAD-W13 and the dX
+  // combine on the rest (0: one stream, every GEMM on every SM)
+  int wgrad_sms;
+  cudaStream_t wstream;
+  cudaEvent_t ev_wfork, ev_wjoin;
 };
 
 namespace moe {
@@ -392,6 +398,7 @@ GemmArgs wgrad_args(const moe_plan* p) {
 int gather_grid(const moe_plan* p) { return p->num_sms * 16; }
 
 void mark(const moe_plan* p, int which, int i, cudaStream_t st);
+cudaError_t launch_wgrad_bf16(moe_plan* p, cudaStream_t st, float* dw13, float* dw2, int grid);
 
 // MXFP8 forward after dispatch ("What it is selling": MXFP8 E4M3 quantises
 // activations after routing and takes prepared weights; staged W13 and W2):
@@ -451,6 +458,37 @@ int forward_mxfp8(moe_plan* p, const void* x, const uint8_t* w13_sf, const uint8
   mark(p, 0, 5, st);
   p->saved = 0;
   return MOE_OK;
+}
+
+// b5, b6 of the bf16 backward: dW2[e] += dY_e^T . hs_e, then dW13[e] += dA_e^T .
+// x_e, on `grid` CTAs of stream st (stage marks 5 and 6 recorded there).
+cudaError_t launch_wgrad_bf16(moe_plan* p, cudaStream_t st, float* dw13, float* dw2, int grid) {
+  const int I = p->I, d = p->d;
+  {
+    GemmArgs g = wgrad_args(p);
+    g.m_tiles = d / kBM;
+    g.n_tiles = I / p->bnw2;
+    g.out0 = dw2; g.ld0 = I;
+    g.out_expert_stride = (long long)d * I;
+    cudaError_t e = launch_gemm(EPI_WGRAD, p->bnw2, true, true, p->tm_dye_mn, p->tm_hs_mn,
+                                p->tm_dw2, p->tm_dw2, p->tm_dw2, g, grid, st);
+    if (e != cudaSuccess) return e;
+    p->launches += 1;
+    mark(p, 1, 5, st);
+  }
+  {
+    GemmArgs g = wgrad_args(p);
+    g.m_tiles = 2 * I / kBM;
+    g.n_tiles = d / p->bnw13;
+    g.out0 = dw13; g.ld0 = d;
+    g.out_expert_stride = 2LL * I * d;
+    cudaError_t e = launch_gemm(EPI_WGRAD, p->bnw13, true, true, p->tm_dA_mn, p->tm_xe_mn,
+                                p->tm_dw13, p->tm_dw13, p->tm_dw13, g, grid, st);
+    if (e != cudaSuccess) return e;
+    p->launches += 1;
+    mark(p, 1, 6, st);
+  }
+  return cudaSuccess;
 }
 
 void mark(const moe_plan* p, int which, int i, cudaStream_t st) {
@@ -528,6 +566,11 @@ moe_plan* moe_plan_create(int T, int d, int I, int E, int k, int precision) {
 
 void moe_plan_destroy(moe_plan* p) {
   if (!p) return;
+  if (p->wstream) {
+    cudaStreamDestroy(p->wstream);
+    cudaEventDestroy(p->ev_wfork);
+    cudaEventDestroy(p->ev_wjoin);
+  }
   if (p->side) {
     cudaStreamDestroy(p->side);
     cudaEventDestroy(p->ev_fork);
@@ -799,6 +842,18 @@ int moe_backward(moe_plan* p, const void* dy, const void* w13, const void* w2, v
     p->launches += 1;
     mark(p, 1, 2, st);
   }
+  // With a split, the weight gradients (b5, b6) run on their own stream and
+  // SMs from here on, beside b3 and b4.
+  const bool split = p->wgrad_sms > 0 && p->wstream;
+  const int rows_grid = split ? p->num_sms - p->wgrad_sms : p->num_sms;
+  cudaStream_t wst = split ? p->wstream : st;
+  if (split && ((e = cudaEventRecord(p->ev_wfork, st)) != cudaSuccess ||
+                (e = cudaStreamWaitEvent(wst, p->ev_wfork, 0)) != cudaSuccess))
+    return cuda_status(e);
+  if (split) {
+    e = launch_wgrad_bf16(p, wst, dw13, dw2, p->wgrad_sms);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
   // b3: dX_e = dA . W13_e
   {
     GemmArgs g = rows_args(p);
@@ -817,7 +872,7 @@ int moe_backward(moe_plan* p, const void* dy, const void* w13, const void* w2, v
       g.mtile_list = p->left_list; g.list_count = p->num_left;
     }
     e = launch_gemm(EPI_STORE, p->bn2, false, true, p->tm_dA, p->tm_w13_mn, p->tm_dA, p->tm_dxe,
-                    p->tm_dxe, g, p->num_sms, st);
+                    p->tm_dxe, g, rows_grid, st);
     if (e != cudaSuccess) return cuda_status(e);
     p->launches += 1;
     mark(p, 1, 3, st);
@@ -831,35 +886,15 @@ int moe_backward(moe_plan* p, const void* dy, const void* w13, const void* w2, v
   if (p->record_after_combine &&
       (e = cudaEventRecord(p->record_after_combine, st)) != cudaSuccess)
     return cuda_status(e);
-  // b5: dW2[e] += dY_e^T . hs_e
-  {
-    GemmArgs g = wgrad_args(p);
-    g.m_tiles = d / kBM;
-    g.n_tiles = I / p->bnw2;
-    g.out0 = dw2; g.ld0 = I;
-    g.out_expert_stride = (long long)d * I;
-    e = launch_gemm(EPI_WGRAD, p->bnw2, true, true, p->tm_dye_mn, p->tm_hs_mn, p->tm_dw2,
-                    p->tm_dw2, p->tm_dw2, g,
-                    p->num_sms, st);
-    if (e != cudaSuccess) return cuda_status(e);
-    p->launches += 1;
-    mark(p, 1, 5, st);
+  if (split) {
+    // join: the caller's stream continues once the weight gradients are done
+    if ((e = cudaEventRecord(p->ev_wjoin, wst)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(st, p->ev_wjoin, 0)) != cudaSuccess)
+      return cuda_status(e);
+    return MOE_OK;
   }
-  // b6: dW13[e] += dA_e^T . x_e
-  {
-    GemmArgs g = wgrad_args(p);
-    g.m_tiles = 2 * I / kBM;
-    g.n_tiles = d / p->bnw13;
-    g.out0 = dw13; g.ld0 = d;
-    g.out_expert_stride = 2LL * I * d;
-    e = launch_gemm(EPI_WGRAD, p->bnw13, true, true, p->tm_dA_mn, p->tm_xe_mn, p->tm_dw13,
-                    p->tm_dw13, p->tm_dw13, g,
-                    p->num_sms, st);
-    if (e != cudaSuccess) return cuda_status(e);
-    p->launches += 1;
-    mark(p, 1, 6, st);
-  }
-  return MOE_OK;
+  e = launch_wgrad_bf16(p, st, dw13, dw2, p->num_sms);
+  return e == cudaSuccess ? MOE_OK : cuda_status(e);
 }
 
 // MXFP8 backward ("What it is selling": MXFP8 E4M3 for DGRAD and WGRAD; the
@@ -1246,6 +1281,20 @@ int moe_quantize_mxfp8(const void* in, long rows, int K, uint8_t* codes, uint8_t
   if (rows == 0) return MOE_OK;
   return cuda_status(launch_quant_mxfp8(in, rows, K, codes, scales, static_cast<cudaStream_t>(stream)));
 }
+
+int moe_plan_set_backward_split(moe_plan* p, int wgrad_sms) {
+  if (!p || wgrad_sms < 0 || wgrad_sms >= p->num_sms) return MOE_ERR_INVALID_ARG;
+  if (wgrad_sms > 0 && !p->wstream) {
+    if (cudaStreamCreateWithFlags(&p->wstream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p->ev_wfork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p->ev_wjoin, cudaEventDisableTiming) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  p->wgrad_sms = wgrad_sms;
+  return MOE_OK;
+}
+
+int moe_plan_num_sms(const moe_plan* p) { return p ? p->num_sms : 0; }
 
 int moe_plan_set_debug(moe_plan* p, long long wait_limit_ns, int stall_w13) {
   if (!p || wait_limit_ns < 0) return MOE_ERR_INVALID_ARG;

@@ -83,6 +83,29 @@ def test_small_forward_backward(moe, orc, name, sizes, extra):
     check_backward(orc, inp, g)
 
 
+@pytest.mark.parametrize("sizes", [dict(T=300, d=256, I=192, E=7, k=3),
+                                   dict(T=2048, d=512, I=256, E=32, k=8, routing="zipf",
+                                        zipf_s=1.2, zipf_support=24)], ids=["ragged", "skew"])
+def test_backward_split_is_bit_identical(moe, sizes):
+    """Weight gradients on their own stream and SMs beside DGRAD-W13: the same bits
+    as one stream, for every output, twice in a row."""
+    inp = make(None, seed=61, train=True, **sizes)
+    ref = run_gpu(moe, inp, train=True)
+    assert ref["rc"] == 0
+    dev = ref["dev"]
+    plan = ref["plan"]
+    plan.set_backward_split(plan.num_sms() // 2)
+    for _ in range(2):
+        dw13, dw2 = dev["dw13"].clone(), dev["dw2"].clone()
+        plan.forward(dev["x"], dev["ids"], dev["scores"], dev["w13"], dev["w2"], save=True)
+        dx, ds = plan.backward(dev["dy"], dev["w13"], dev["w2"], dw13, dw2)
+        torch.cuda.synchronize()
+        assert plan.check()[0] == 0
+        assert torch.equal(dx.view(torch.int16), ref["dx"].view(torch.int16))
+        assert torch.equal(ds, ref["dscores"])
+        assert torch.equal(dw13, ref["dw13"]) and torch.equal(dw2, ref["dw2"])
+
+
 def test_zero_score_padding_rows_are_zero(moe):
     inp = make(None, seed=5, train=True, T=160, d=128, I=64, E=6, k=2, pad=40)
     g = run_gpu(moe, inp, train=True)
