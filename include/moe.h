@@ -457,7 +457,7 @@ int moe_plan_set_debug(moe_plan* plan, long long wait_limit_ns, int stall_w13);
  * events set, the events of the weight-gradient stages are recorded on the
  * plan's stream.  The first call with wgrad_sms > 0 creates the stream and two
  * events (no device memory).  0 <= wgrad_sms < the number of SMs, else
- * MOE_ERR_INVALID_ARG.  bf16 plans (moe_backward); moe_backward_mxfp8 ignores it.
+ * MOE_ERR_INVALID_ARG.  Applies to moe_backward and moe_backward_mxfp8.
  */
 int moe_plan_set_backward_split(moe_plan* plan, int wgrad_sms);
 

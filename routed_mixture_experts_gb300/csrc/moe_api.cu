@@ -399,6 +399,7 @@ int gather_grid(const moe_plan* p) { return p->num_sms * 16; }
 
 void mark(const moe_plan* p, int which, int i, cudaStream_t st);
 cudaError_t launch_wgrad_bf16(moe_plan* p, cudaStream_t st, float* dw13, float* dw2, int grid);
+cudaError_t launch_wgrad_mx(moe_plan* p, cudaStream_t st, float* dw13, float* dw2, int grid);
 
 // MXFP8 forward after dispatch ("What it is selling": MXFP8 E4M3 quantises
 // activations after routing and takes prepared weights; staged W13 and W2):
@@ -484,6 +485,42 @@ cudaError_t launch_wgrad_bf16(moe_plan* p, cudaStream_t st, float* dw13, float* 
     g.out_expert_stride = 2LL * I * d;
     cudaError_t e = launch_gemm(EPI_WGRAD, p->bnw13, true, true, p->tm_dA_mn, p->tm_xe_mn,
                                 p->tm_dw13, p->tm_dw13, p->tm_dw13, g, grid, st);
+    if (e != cudaSuccess) return e;
+    p->launches += 1;
+    mark(p, 1, 6, st);
+  }
+  return cudaSuccess;
+}
+
+// b5, b6 of the MXFP8 backward (block-scaled WGRAD over each expert's rows), on
+// `grid` CTAs of stream st.
+cudaError_t launch_wgrad_mx(moe_plan* p, cudaStream_t st, float* dw13, float* dw2, int grid) {
+  const int I = p->I, d = p->d;
+  const long long RP = p->RP;
+  {
+    GemmArgs g = wgrad_args(p);
+    g.wgrad_kstep = 128;
+    g.m_tiles = d / kBM;
+    g.n_tiles = I / 128;
+    g.out0 = dw2; g.ld0 = I;
+    g.out_expert_stride = (long long)d * I;
+    g.sfa = p->dyqTsf; g.sfb = p->hsqTsf; g.sf_ngr = (int)(RP / 128);
+    cudaError_t e = launch_gemm(EPI_WGRAD, 128, false, false, p->tm_dyqT, p->tm_hsqT, p->tm_dw2,
+                                p->tm_dw2, p->tm_dw2, g, grid, st, true);
+    if (e != cudaSuccess) return e;
+    p->launches += 1;
+    mark(p, 1, 5, st);
+  }
+  {
+    GemmArgs g = wgrad_args(p);
+    g.wgrad_kstep = 128;
+    g.m_tiles = 2 * I / kBM;
+    g.n_tiles = d / 128;
+    g.out0 = dw13; g.ld0 = d;
+    g.out_expert_stride = 2LL * I * d;
+    g.sfa = p->dAqTsf; g.sfb = p->xqTsf; g.sf_ngr = (int)(RP / 128);
+    cudaError_t e = launch_gemm(EPI_WGRAD, 128, false, false, p->tm_dAqT, p->tm_xqT, p->tm_dw13,
+                                p->tm_dw13, p->tm_dw13, g, grid, st, true);
     if (e != cudaSuccess) return e;
     p->launches += 1;
     mark(p, 1, 6, st);
@@ -967,6 +1004,16 @@ int moe_backward_mxfp8(moe_plan* p, const void* dy, const uint8_t* w13t, const u
     p->launches += 1;
   }
   mark(p, 1, 2, st);
+  // With a split, the weight gradients (b5, b6) run on their own stream and
+  // SMs from here on, beside b3 and b4.
+  const bool split = p->wgrad_sms > 0 && p->wstream;
+  const int rows_grid = split ? p->num_sms - p->wgrad_sms : p->num_sms;
+  cudaStream_t wst = split ? p->wstream : st;
+  if (split && ((e = cudaEventRecord(p->ev_wfork, st)) != cudaSuccess ||
+                (e = cudaStreamWaitEvent(wst, p->ev_wfork, 0)) != cudaSuccess))
+    return cuda_status(e);
+  if (split && (e = launch_wgrad_mx(p, wst, dw13, dw2, p->wgrad_sms)) != cudaSuccess)
+    return cuda_status(e);
   // b3
   {
     GemmArgs g = rows_args(p);
@@ -977,7 +1024,7 @@ int moe_backward_mxfp8(moe_plan* p, const void* dy, const uint8_t* w13t, const u
     g.sfa = p->dAsf; g.sfb = w13t_sf; g.sf_ngr = 2 * I / 128; g.b_blocks_per_expert = d / 128;
     g.k_rotate = 1;
     e = launch_gemm(EPI_STORE, p->bnmx_d, false, false, p->tm_dAq, p->tm_w13t, p->tm_dAq,
-                    p->tm_dxe, p->tm_dxe, g, p->num_sms, st, true);
+                    p->tm_dxe, p->tm_dxe, g, rows_grid, st, true);
     if (e != cudaSuccess) return cuda_status(e);
     p->launches += 1;
     mark(p, 1, 3, st);
@@ -988,37 +1035,14 @@ int moe_backward_mxfp8(moe_plan* p, const void* dy, const uint8_t* w13t, const u
   if (e != cudaSuccess) return cuda_status(e);
   p->launches += 1;
   mark(p, 1, 4, st);
-  // b5
-  {
-    GemmArgs g = wgrad_args(p);
-    g.wgrad_kstep = 128;
-    g.m_tiles = d / kBM;
-    g.n_tiles = I / 128;
-    g.out0 = dw2; g.ld0 = I;
-    g.out_expert_stride = (long long)d * I;
-    g.sfa = p->dyqTsf; g.sfb = p->hsqTsf; g.sf_ngr = (int)(RP / 128);
-    e = launch_gemm(EPI_WGRAD, 128, false, false, p->tm_dyqT, p->tm_hsqT, p->tm_dw2, p->tm_dw2,
-                    p->tm_dw2, g, p->num_sms, st, true);
-    if (e != cudaSuccess) return cuda_status(e);
-    p->launches += 1;
-    mark(p, 1, 5, st);
+  if (split) {
+    if ((e = cudaEventRecord(p->ev_wjoin, wst)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(st, p->ev_wjoin, 0)) != cudaSuccess)
+      return cuda_status(e);
+    return MOE_OK;
   }
-  // b6
-  {
-    GemmArgs g = wgrad_args(p);
-    g.wgrad_kstep = 128;
-    g.m_tiles = 2 * I / kBM;
-    g.n_tiles = d / 128;
-    g.out0 = dw13; g.ld0 = d;
-    g.out_expert_stride = 2LL * I * d;
-    g.sfa = p->dAqTsf; g.sfb = p->xqTsf; g.sf_ngr = (int)(RP / 128);
-    e = launch_gemm(EPI_WGRAD, 128, false, false, p->tm_dAqT, p->tm_xqT, p->tm_dw13, p->tm_dw13,
-                    p->tm_dw13, g, p->num_sms, st, true);
-    if (e != cudaSuccess) return cuda_status(e);
-    p->launches += 1;
-    mark(p, 1, 6, st);
-  }
-  return MOE_OK;
+  e = launch_wgrad_mx(p, st, dw13, dw2, p->num_sms);
+  return e == cudaSuccess ? MOE_OK : cuda_status(e);
 }
 
 // Forward over a caller-provided expert-major layout (nvfp4moe README, "MoE
