@@ -74,6 +74,8 @@ def parse():
                     help="with --gpus N > 1: sum the weight gradients over the ranks after "
                          "every backward (one data-parallel training step instead of N "
                          "independent replicas)")
+    ap.add_argument("--extra-workloads", default="infer_e16,skew_pad",
+                    help="comma list of the other workloads to time (infer_e16, skew_pad)")
     ap.add_argument("--extra-steps", type=int, default=30,
                     help="timed steps of the inference (E=16) and skewed-routing workloads "
                          "(0: skip)")
@@ -671,8 +673,10 @@ def run_ours(args):
 
     extra = {}
     if args.extra_steps > 0:
+        wanted = [w for w in args.extra_workloads.split(",") if w]
         for name, train in (("infer_e16", False), ("skew_pad", True)):
-            extra[name] = run_extra(moe, name, train, args, dev, ws, tpeak, pk)
+            if name in wanted:
+                extra[name] = run_extra(moe, name, train, args, dev, ws, tpeak, pk)
 
     if rank != 0:
         return
