@@ -179,6 +179,31 @@ __device__ __forceinline__ void epi_stage_store(const CUtensorMap* tm, uint32_t 
   ++seq;
 }
 
+// One packed bf16 sub-tile (this thread's 32 columns as 16 bf16 pairs) through
+// the two alternating staging buffers of epi_stage_store: a buffer is rewritten
+// once the store issued two sub-tiles earlier has read it, so a thread block
+// never waits for the store it has just issued.
+__device__ __forceinline__ void epi_stage_packed(const CUtensorMap* tm, uint32_t out0, int& seq,
+                                                 int et, int row, int half,
+                                                 const uint32_t (&pk)[16], int x, int y) {
+  const uint32_t buf = out0 + (uint32_t)(seq % kEpiStageBufs) * 16384u;
+  if (et == 0) bulk_wait_read<kEpiStageBufs - 1>();
+  named_bar_sync(1, kEpiThreads);
+  const uint32_t rbase = buf + (uint32_t)row * 128u;
+  const uint32_t sw = (uint32_t)(row & 7);
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    st_shared_v4_u32(rbase + (((uint32_t)(4 * half + q) ^ sw) << 4), pk[4 * q], pk[4 * q + 1],
+                     pk[4 * q + 2], pk[4 * q + 3]);
+  fence_proxy_async_smem();
+  named_bar_sync(1, kEpiThreads);
+  if (et == 0) {
+    tma_store_2d(tm, buf, x, y);
+    bulk_commit();
+  }
+  ++seq;
+}
+
 // Batched staging for epilogues with several outputs: NOUT sub-tiles of one
 // 64-column chunk (this thread's 32 columns of each, already packed to bf16
 // pairs) go to NOUT consecutive 16 KB buffers from `buf` and leave as NOUT TMA
@@ -509,8 +534,10 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, const TileInfo& ti, 
           pk[2][8 * hh + q / 2] = pack_bf2(hs2[0], hs2[1]);   // R7
         }
       }
-      epi_stage_three<tri_bufs<EPI_DGRAD2>()>(tmO0, tmO0, tmO1, out0, et, row, half, pk, ti.n0 + c,
-                                a.I + ti.n0 + c, ti.n0 + c, ti.m0);
+      // dA gate, dA up, hs: one sub-tile at a time through the two buffers
+      epi_stage_packed(tmO0, out0, seq, et, row, half, pk[0], ti.n0 + c, ti.m0);
+      epi_stage_packed(tmO0, out0, seq, et, row, half, pk[1], a.I + ti.n0 + c, ti.m0);
+      epi_stage_packed(tmO1, out0, seq, et, row, half, pk[2], ti.n0 + c, ti.m0);
     }
     // one partial per (n tile, column half)
     a.pdscore[grow * (2 * a.n_tiles) + 2 * ti.nt + half] = part;
