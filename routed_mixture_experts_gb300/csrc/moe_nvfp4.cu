@@ -64,7 +64,11 @@ __device__ __forceinline__ uint32_t nv_quant64(const uint4* src, float g, uint4*
 
 // Gather + quantise: padded row r of the expert-major activations is token
 // token_of[r] of x (zero where token_of[r] < 0), quantised along d with the
-// static encode scale g.  One warp per row, one 64-element group per lane per pass.
+// static encode scale g.  One warp per row; the row is read in coalesced 16-byte
+// pieces (piece p = 8 elements, lane p % 32), so a 16-element block spans two
+// neighbouring lanes: its amax is combined with one shuffle, each lane
+// quantises its 8 elements (4 code bytes, stored coalesced) and the even lane
+// writes the block's scale.
 __global__ void __launch_bounds__(256) k_gather_quant_nvfp4(const uint4* __restrict__ x,
                                                             const int32_t* __restrict__ token_of,
                                                             const int32_t* __restrict__ nrows_p,
@@ -76,14 +80,44 @@ __global__ void __launch_bounds__(256) k_gather_quant_nvfp4(const uint4* __restr
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
+  const int npc = d / 8;                     // 16-byte pieces per row (a multiple of 2)
   const int ngr = d / 64;
   for (int r = gw; r < nrows; r += nw) {
     const int t = token_of[r];
-    for (int kg = lane; kg < ngr; kg += 32) {
-      const uint4* src = t >= 0 ? x + ((long long)t * d + kg * 64) / 8 : nullptr;
-      uint4* dst = reinterpret_cast<uint4*>(codes + (long long)r * (d / 2) + kg * 32);
-      const uint32_t sc = nv_quant64(src, g, dst);
-      *reinterpret_cast<uint32_t*>(sf + mx_sf_offset(r >> 7, r & 127, kg * 4, ngr)) = sc;
+    const uint4* src = x + (long long)(t < 0 ? 0 : t) * npc;
+    uint32_t* dst = reinterpret_cast<uint32_t*>(codes + (long long)r * (d / 2));
+    // every lane runs every pass (the shuffles need the whole warp); a lane past
+    // the row's end holds zeros and stores nothing (blocks never straddle it)
+#pragma unroll 4
+    for (int p0 = 0; p0 < npc; p0 += 32) {
+      const int pc = p0 + lane;
+      const bool in = pc < npc;
+      const uint4 v = (t >= 0 && in) ? src[pc] : make_uint4(0u, 0u, 0u, 0u);
+      float f[8];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        f[2 * q] = __uint_as_float(w[q] << 16);
+        f[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+      }
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));   // the block's other half
+      const float tt = __fmul_rn(__fdiv_rn(amax, 6.0f), g);
+      const uint8_t sc = (uint8_t)(cvt_e4m3x2(tt, 0.f) & 0xFFu);
+      const float S = e4m3_to_f32(sc);
+      uint32_t q8 = 0u;
+      if (S > 0.f) {
+        const float rr = __fdiv_rn(g, S);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) f[i] = __fmul_rn(f[i], rr);
+        q8 = cvt_e2m1x8(f);
+      }
+      if (in) {
+        dst[pc] = q8;
+        if (!(lane & 1)) sf[mx_sf_offset(r >> 7, r & 127, pc >> 1, ngr)] = sc;
+      }
     }
   }
   pdl_trigger();
