@@ -178,101 +178,99 @@ __global__ void __launch_bounds__(gemm_threads<NV>(), 1)
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
-    int stage = 0;
-    uint32_t phase = 0;
-    int issued_parity[STAGES];
+    // (lane 0 alone, like the MMA issuer: no warp-wide step per stage)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued_parity[STAGES];
 #pragma unroll
-    for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
-    bool ok = true;
-    for (int r = 0, tile = cta_tile(args, 0); tile < num_tiles && ok; tile = cta_tile(args, ++r)) {
-      const TileInfo ti = decode_tile<BN>(args, tile);
-      // k_rotate (row GEMMs): the tiles that share an A tile (same m tile) or a
-      // B tile (same expert and n tile) run at the same time; each starts its K
-      // loop at its own offset (wrapping around), so each K chunk is read from
-      // DRAM by one of them and from L2 by the others, instead of all of them
-      // waiting on DRAM for the same chunk.
-      const int kb0 = args.k_rotate ? (int)(((unsigned)(ti.m0 >> 7) * 7u + (unsigned)ti.nt * 5u) %
-                                            (unsigned)ti.kb)
-                                    : 0;
-      for (int kb = 0; kb < ti.kb; ++kb) {
-        const int kc = kb + kb0 < ti.kb ? kb + kb0 : kb + kb0 - ti.kb;   // K chunk loaded
-        int w = 1;
-        if (lane == 0) w = mbar_wait(empty_bar(stage), phase ^ 1u, &abort_s, args.err, 1, wlim);
-        ok = __shfl_sync(0xffffffffu, w, 0) != 0;
-        if (!ok) break;
-        if (lane == 0) {
-          const uint32_t fb = full_bar(stage);
-          const uint32_t sa = stage0 + stage * S::STAGE_BYTES;
-          const uint32_t sb = sa + S::A_BYTES;
-          mbar_arrive_expect_tx(fb, S::TX_BYTES);
-          if constexpr (NV) {
-            // the four 512-byte scale chunks of this stage's 64-element K groups
-            // (contiguous in the tiled layout): A's row block, then B's BN/128 row
-            // blocks, 2 KB each (row GEMMs only)
-            const uint32_t ssf = sb + S::B_BYTES;
-            const long long kg = 4LL * kc;
-            const long long gbr =
-                (long long)ti.e * args.b_blocks_per_expert + (long long)ti.nt * (BN / 128);
-            bulk_g2s(ssf, args.sfa + ((long long)(ti.m0 >> 7) * args.sf_ngr + kg) * 512, 2048u, fb);
+      for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
+      bool ok = true;
+      for (int r = 0, tile = cta_tile(args, 0); tile < num_tiles && ok; tile = cta_tile(args, ++r)) {
+        const TileInfo ti = decode_tile<BN>(args, tile);
+        // k_rotate (row GEMMs): the tiles that share an A tile (same m tile) or a
+        // B tile (same expert and n tile) run at the same time; each starts its K
+        // loop at its own offset (wrapping around), so each K chunk is read from
+        // DRAM by one of them and from L2 by the others, instead of all of them
+        // waiting on DRAM for the same chunk.
+        const int kb0 = args.k_rotate ? (int)(((unsigned)(ti.m0 >> 7) * 7u + (unsigned)ti.nt * 5u) %
+                                              (unsigned)ti.kb)
+                                      : 0;
+        for (int kb = 0; kb < ti.kb; ++kb) {
+          const int kc = kb + kb0 < ti.kb ? kb + kb0 : kb + kb0 - ti.kb;   // K chunk loaded
+          ok = mbar_wait(empty_bar(stage), phase ^ 1u, &abort_s, args.err, 1, wlim);
+          if (!ok) break;
+          {
+            const uint32_t fb = full_bar(stage);
+            const uint32_t sa = stage0 + stage * S::STAGE_BYTES;
+            const uint32_t sb = sa + S::A_BYTES;
+            mbar_arrive_expect_tx(fb, S::TX_BYTES);
+            if constexpr (NV) {
+              // the four 512-byte scale chunks of this stage's 64-element K groups
+              // (contiguous in the tiled layout): A's row block, then B's BN/128 row
+              // blocks, 2 KB each (row GEMMs only)
+              const uint32_t ssf = sb + S::B_BYTES;
+              const long long kg = 4LL * kc;
+              const long long gbr =
+                  (long long)ti.e * args.b_blocks_per_expert + (long long)ti.nt * (BN / 128);
+              bulk_g2s(ssf, args.sfa + ((long long)(ti.m0 >> 7) * args.sf_ngr + kg) * 512, 2048u, fb);
 #pragma unroll
-            for (int rb = 0; rb < BN / 128; ++rb)
-              bulk_g2s(ssf + 2048u * (uint32_t)(1 + rb),
-                       args.sfb + ((gbr + rb) * args.sf_ngr + kg) * 512, 2048u, fb);
-          } else if constexpr (MX) {
-            // the 512-byte scale chunks of this K group: A's row block, then B's
-            // BN/128 row blocks
-            const uint32_t ssf = sb + S::B_BYTES;
-            // row GEMMs: K groups from 0, B row blocks of (expert, n tile); wgrad
-            // mode: K groups from the expert's first row, B row blocks from n0/128
-            const long long kg = (long long)(ti.krow0 >> 7) + kc;
-            const long long ga = ((long long)(ti.m0 >> 7) * args.sf_ngr + kg) * 512;
-            const long long gbr =
-                args.wgrad ? (long long)(ti.n0 >> 7)
-                           : (long long)ti.e * args.b_blocks_per_expert + (long long)ti.nt * (BN / 128);
-            bulk_g2s(ssf, args.sfa + ga, 512u, fb);
+              for (int rb = 0; rb < BN / 128; ++rb)
+                bulk_g2s(ssf + 2048u * (uint32_t)(1 + rb),
+                         args.sfb + ((gbr + rb) * args.sf_ngr + kg) * 512, 2048u, fb);
+            } else if constexpr (MX) {
+              // the 512-byte scale chunks of this K group: A's row block, then B's
+              // BN/128 row blocks
+              const uint32_t ssf = sb + S::B_BYTES;
+              // row GEMMs: K groups from 0, B row blocks of (expert, n tile); wgrad
+              // mode: K groups from the expert's first row, B row blocks from n0/128
+              const long long kg = (long long)(ti.krow0 >> 7) + kc;
+              const long long ga = ((long long)(ti.m0 >> 7) * args.sf_ngr + kg) * 512;
+              const long long gbr =
+                  args.wgrad ? (long long)(ti.n0 >> 7)
+                             : (long long)ti.e * args.b_blocks_per_expert + (long long)ti.nt * (BN / 128);
+              bulk_g2s(ssf, args.sfa + ga, 512u, fb);
 #pragma unroll
-            for (int rb = 0; rb < BN / 128; ++rb)
-              bulk_g2s(ssf + 512u * (uint32_t)(1 + rb),
-                       args.sfb + ((gbr + rb) * args.sf_ngr + kg) * 512, 512u, fb);
+              for (int rb = 0; rb < BN / 128; ++rb)
+                bulk_g2s(ssf + 512u * (uint32_t)(1 + rb),
+                         args.sfb + ((gbr + rb) * args.sf_ngr + kg) * 512, 512u, fb);
+            }
+            // One TMA per operand tile (large boxes: the TMA cost is per box).
+            // A: 128 rows x 128 bytes of K.  K-major: a 128-row box of [rows, K];
+            // MN-major: two 64-wide atoms of the [K rows, M] tensor (3-D map).
+            if (A_MN)
+              tma_load_3d(sa, &tmA, 0, ti.krow0 + kc * kBK, ti.m0 >> 6, fb);
+            else
+              tma_load_2d(sa, &tmA, ti.krow0 + kc * KE, ti.m0, fb);
+            // B: BN rows (N) x 128 bytes of K
+            if (args.wgrad && B_MN) {
+              tma_load_3d(sb, &tmB, 0, ti.krow0 + kc * kBK, ti.n0 >> 6, fb);
+            } else if (args.wgrad) {
+              // K-major transposed operand [N, rows]: this expert's K range
+              tma_load_2d(sb, &tmB, ti.krow0 + kc * KE, ti.n0, fb);
+            } else if (B_MN) {
+              // [E*K, N]: BN/64 atoms of expert e's K rows
+              tma_load_3d(sb, &tmB, 0, ti.e * args.b_expert_rows + kc * kBK, ti.n0 >> 6, fb);
+            } else if (EPI == EPI_SWIGLU && MX && BN == 256) {
+              // (K, 64, 2, I/64, E) view of W13: two 64-row blocks, each its gate
+              // rows then the same up rows (the row order of the scale chunks)
+              tma_load_5d(sb, &tmB, kc * KE, 0, 0, 2 * ti.nt, ti.e, fb);
+            } else if (EPI == EPI_SWIGLU) {
+              // (K, I, 2E) view of W13: this tile's BN/2 gate rows, then the same up
+              // rows, in one box
+              tma_load_3d(sb, &tmB, kc * KE, ti.nt * (BN / 2), 2 * ti.e, fb);
+            } else {
+              // [E*N, K]: a BN-row box
+              tma_load_2d(sb, &tmB, kc * KE, ti.e * args.b_expert_rows + ti.n0, fb);
+            }
+            issued_parity[stage] = (int)phase;
           }
-          // One TMA per operand tile (large boxes: the TMA cost is per box).
-          // A: 128 rows x 128 bytes of K.  K-major: a 128-row box of [rows, K];
-          // MN-major: two 64-wide atoms of the [K rows, M] tensor (3-D map).
-          if (A_MN)
-            tma_load_3d(sa, &tmA, 0, ti.krow0 + kc * kBK, ti.m0 >> 6, fb);
-          else
-            tma_load_2d(sa, &tmA, ti.krow0 + kc * KE, ti.m0, fb);
-          // B: BN rows (N) x 128 bytes of K
-          if (args.wgrad && B_MN) {
-            tma_load_3d(sb, &tmB, 0, ti.krow0 + kc * kBK, ti.n0 >> 6, fb);
-          } else if (args.wgrad) {
-            // K-major transposed operand [N, rows]: this expert's K range
-            tma_load_2d(sb, &tmB, ti.krow0 + kc * KE, ti.n0, fb);
-          } else if (B_MN) {
-            // [E*K, N]: BN/64 atoms of expert e's K rows
-            tma_load_3d(sb, &tmB, 0, ti.e * args.b_expert_rows + kc * kBK, ti.n0 >> 6, fb);
-          } else if (EPI == EPI_SWIGLU && MX && BN == 256) {
-            // (K, 64, 2, I/64, E) view of W13: two 64-row blocks, each its gate
-            // rows then the same up rows (the row order of the scale chunks)
-            tma_load_5d(sb, &tmB, kc * KE, 0, 0, 2 * ti.nt, ti.e, fb);
-          } else if (EPI == EPI_SWIGLU) {
-            // (K, I, 2E) view of W13: this tile's BN/2 gate rows, then the same up
-            // rows, in one box
-            tma_load_3d(sb, &tmB, kc * KE, ti.nt * (BN / 2), 2 * ti.e, fb);
-          } else {
-            // [E*N, K]: a BN-row box
-            tma_load_2d(sb, &tmB, kc * KE, ti.e * args.b_expert_rows + ti.n0, fb);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
           }
-          issued_parity[stage] = (int)phase;
-        }
-        __syncwarp();
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
         }
       }
-    }
-    if (lane == 0) {
       if (!abort_s) {
         // producer tail: every issued stage has been released by the MMA commits
         for (int s = 0; s < STAGES; ++s) {
@@ -292,95 +290,94 @@ __global__ void __launch_bounds__(gemm_threads<NV>(), 1)
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
-    int stage = 0;
-    uint32_t phase = 0;
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    bool ok = true;
-    for (int r = 0, tile = cta_tile(args, 0); tile < num_tiles && ok; tile = cta_tile(args, ++r)) {
-      const TileInfo ti = decode_tile<BN>(args, tile);
-      int w = 1;
-      if (lane == 0) w = mbar_wait(tempty_bar(acc), acc_phase ^ 1u, &abort_s, args.err, 3, wlim);
-      // failure-path test: wait on the drain barrier, which nothing has arrived at
-      if (args.stall_mma && lane == 0 && w) w = mbar_wait(drain_bar, 0, &abort_s, args.err, 9, wlim);
-      ok = __shfl_sync(0xffffffffu, w, 0) != 0;
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-      for (int kb = 0; kb < ti.kb; ++kb) {
-        w = 1;
-        if (lane == 0) w = mbar_wait(full_bar(stage), phase, &abort_s, args.err, 4, wlim);
-        // NVFP4: also wait until the scale warp's copies of this stage are in TMEM
-        if (NV && lane == 0 && w)
-          w = mbar_wait(sf_full_bar(stage), phase, &abort_s, args.err, 10, wlim);
-        ok = __shfl_sync(0xffffffffu, w, 0) != 0;
+    // Lane 0 runs the whole loop alone: a stage costs a barrier test and the
+    // MMAs, whose shared-memory descriptors are a fixed base plus the stage and
+    // K-step offsets (the address field counts 16-byte units, and no operand
+    // address leaves its 14 bits), so the tensor pipe is not left idle between
+    // stages while the next ones are prepared.
+    if (lane == 0) {
+      // K-major: rows of 128 B, 8-row groups 1024 B apart; K step = 32 B.
+      // MN-major: 64-wide MN atoms 8 KB apart (LBO), 8-row K groups 1024 B apart
+      // (SBO); K step of 16 rows = 2048 B.
+      const uint64_t a_desc0 = A_MN ? smem_desc_sw128(stage0, 8192, 1024)
+                                    : smem_desc_sw128(stage0, 16, 1024);
+      const uint64_t b_desc0 = B_MN ? smem_desc_sw128(stage0 + S::A_BYTES, 8192, 1024)
+                                    : smem_desc_sw128(stage0 + S::A_BYTES, 16, 1024);
+      // (block-scaled: K-major, 32 bytes of K per MMA step as well)
+      constexpr uint32_t A_KSTEP = (A_MN ? 2048u : 32u) >> 4;
+      constexpr uint32_t B_KSTEP = (B_MN ? 2048u : 32u) >> 4;
+      // MXFP8 scale chunks of a stage: A's 512 bytes after B, then B's per 128 rows
+      const uint64_t sf_desc0 = smem_desc_noswz(stage0 + S::A_BYTES + S::B_BYTES, 512u, 128u);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int r = 0, tile = cta_tile(args, 0); tile < num_tiles && ok; tile = cta_tile(args, ++r)) {
+        const TileInfo ti = decode_tile<BN>(args, tile);
+        ok = mbar_wait(tempty_bar(acc), acc_phase ^ 1u, &abort_s, args.err, 3, wlim);
+        // failure-path test: wait on the drain barrier, which nothing has arrived at
+        if (args.stall_mma && ok) ok = mbar_wait(drain_bar, 0, &abort_s, args.err, 9, wlim);
         if (!ok) break;
         tc_fence_after();
-        if (lane == 0) {
-          const uint32_t sa = stage0 + stage * S::STAGE_BYTES;
-          const uint32_t sb = sa + S::A_BYTES;
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < ti.kb; ++kb) {
+          ok = mbar_wait(full_bar(stage), phase, &abort_s, args.err, 4, wlim);
+          // NVFP4: also wait until the scale warp's copies of this stage are in TMEM
+          if (NV && ok) ok = mbar_wait(sf_full_bar(stage), phase, &abort_s, args.err, 10, wlim);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t soff = (uint64_t)((uint32_t)(stage * S::STAGE_BYTES) >> 4);
           if constexpr (NV) {
             // four K = 64 steps, step j reading the scale columns of 64-element K
             // group j: A's four at sfa_t + 4j, B's (four per 128 rows) at sfb_t + (BN/32)j
             const uint32_t sfa_t = tmem_base + S::SF_COL0 + S::SF_COLS * (uint32_t)stage;
             const uint32_t sfb_t = sfa_t + 16u;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint64_t adesc = smem_desc_sw128(sa + j * 32, 16, 1024);
-              const uint64_t bdesc = smem_desc_sw128(sb + j * 32, 16, 1024);
-              umma_nvf4(d_tmem, adesc, bdesc, IDESC, sfa_t + 4u * (uint32_t)j,
+            for (int j = 0; j < 4; ++j)
+              umma_nvf4(d_tmem, a_desc0 + soff + (uint64_t)(j * A_KSTEP),
+                        b_desc0 + soff + (uint64_t)(j * B_KSTEP), IDESC, sfa_t + 4u * (uint32_t)j,
                         sfb_t + (uint32_t)(BN / 32) * (uint32_t)j, (kb | j) != 0 ? 1u : 0u);
-            }
           } else if constexpr (MX) {
             // this stage's scales -> its own TMEM columns (reused only after the
             // stage is released, i.e. after these MMAs have completed); then four
             // 32-element K steps, step j reading scale byte j
-            const uint32_t ssf = sb + S::B_BYTES;
             const uint32_t sfa_t = tmem_base + S::SF_COL0 + S::SF_COLS * (uint32_t)stage;
             const uint32_t sfb_t = sfa_t + S::SF_COLS / 2;
-            tmem_cp_32x128b_x4(sfa_t, smem_desc_noswz(ssf, 512u, 128u));
+            tmem_cp_32x128b_x4(sfa_t, sf_desc0 + soff);
 #pragma unroll
             for (int rb = 0; rb < BN / 128; ++rb)
               tmem_cp_32x128b_x4(sfb_t + 4u * (uint32_t)rb,
-                                 smem_desc_noswz(ssf + 512u * (uint32_t)(1 + rb), 512u, 128u));
+                                 sf_desc0 + soff + (uint64_t)(32u * (uint32_t)(1 + rb)));
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint64_t adesc = smem_desc_sw128(sa + j * 32, 16, 1024);
-              const uint64_t bdesc = smem_desc_sw128(sb + j * 32, 16, 1024);
-              umma_mxf8(d_tmem, adesc, bdesc, idesc_sf_ids(IDESC, (uint32_t)j, (uint32_t)j),
-                        sfa_t, sfb_t, (kb | j) != 0 ? 1u : 0u);
-            }
+            for (int j = 0; j < 4; ++j)
+              umma_mxf8(d_tmem, a_desc0 + soff + (uint64_t)(j * A_KSTEP),
+                        b_desc0 + soff + (uint64_t)(j * B_KSTEP),
+                        idesc_sf_ids(IDESC, (uint32_t)j, (uint32_t)j), sfa_t, sfb_t,
+                        (kb | j) != 0 ? 1u : 0u);
           } else {
 #pragma unroll
-          for (int k16 = 0; k16 < kBK / 16; ++k16) {
-            // K-major: rows of 128 B, 8-row groups 1024 B apart; K step = 32 B.
-            // MN-major: 64-wide MN atoms 8 KB apart (LBO), 8-row K groups 1024 B
-            // apart (SBO); K step of 16 rows = 2048 B.
-            const uint64_t adesc = A_MN ? smem_desc_sw128(sa + k16 * 2048, 8192, 1024)
-                                        : smem_desc_sw128(sa + k16 * 32, 16, 1024);
-            const uint64_t bdesc = B_MN ? smem_desc_sw128(sb + k16 * 2048, 8192, 1024)
-                                        : smem_desc_sw128(sb + k16 * 32, 16, 1024);
-            umma_f16(d_tmem, adesc, bdesc, IDESC, (kb | k16) != 0 ? 1u : 0u);
-          }
+            for (int k16 = 0; k16 < kBK / 16; ++k16)
+              umma_f16(d_tmem, a_desc0 + soff + (uint64_t)(k16 * A_KSTEP),
+                       b_desc0 + soff + (uint64_t)(k16 * B_KSTEP), IDESC,
+                       (kb | k16) != 0 ? 1u : 0u);
           }
           umma_commit(empty_bar(stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
-        __syncwarp();
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
+        if (!ok) break;
+        umma_commit(tfull_bar(acc));
+        if (S::NACC == 2) acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
       }
-      if (!ok) break;
-      if (lane == 0) umma_commit(tfull_bar(acc));
-      __syncwarp();
-      if (S::NACC == 2) acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
-    }
-    if (abort_s && lane == 0) {
-      // drain: wait for every MMA issued so far before TMEM is freed
-      umma_commit(drain_bar);
-      mbar_wait_drain(drain_bar, 0);
+      if (abort_s) {
+        // drain: wait for every MMA issued so far before TMEM is freed
+        umma_commit(drain_bar);
+        mbar_wait_drain(drain_bar, 0);
+      }
     }
     __syncwarp();
   } else if (NV && warp == kThreads / 32) {
@@ -388,46 +385,42 @@ __global__ void __launch_bounds__(gemm_threads<NV>(), 1)
     // For each stage the MMA issuer consumes: wait for its bytes, copy the scales
     // of its four 64-element K groups into the stage's own TMEM columns (reused
     // only after the stage was released, i.e. after the MMAs that read them have
-    // completed), and signal sf_full when the copies are done.
-    int stage = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    for (int r = 0, tile = cta_tile(args, 0); tile < num_tiles && ok; tile = cta_tile(args, ++r)) {
-      const TileInfo ti = decode_tile<BN>(args, tile);
-      for (int kb = 0; kb < ti.kb; ++kb) {
-        int w = 1;
-        if (lane == 0) w = mbar_wait(full_bar(stage), phase, &abort_s, args.err, 11, wlim);
-        ok = __shfl_sync(0xffffffffu, w, 0) != 0;
-        if (!ok) break;
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t ssf = stage0 + stage * S::STAGE_BYTES + S::A_BYTES + S::B_BYTES;
+    // completed), and signal sf_full when the copies are done.  Lane 0 alone.
+    if (lane == 0) {
+      const uint64_t sf_desc0 = smem_desc_noswz(stage0 + S::A_BYTES + S::B_BYTES, 512u, 128u);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int r = 0, tile = cta_tile(args, 0); tile < num_tiles && ok; tile = cta_tile(args, ++r)) {
+        const TileInfo ti = decode_tile<BN>(args, tile);
+        for (int kb = 0; kb < ti.kb; ++kb) {
+          ok = mbar_wait(full_bar(stage), phase, &abort_s, args.err, 11, wlim);
+          if (!ok) break;
+          tc_fence_after();
+          // chunk j of A at +512 j bytes; of B's row block rb at +2048 (1 + rb) + 512 j
+          const uint64_t sdesc = sf_desc0 + (uint64_t)((uint32_t)(stage * S::STAGE_BYTES) >> 4);
           const uint32_t sfa_t = tmem_base + S::SF_COL0 + S::SF_COLS * (uint32_t)stage;
           const uint32_t sfb_t = sfa_t + 16u;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            tmem_cp_32x128b_x4(sfa_t + 4u * (uint32_t)j,
-                               smem_desc_noswz(ssf + 512u * (uint32_t)j, 512u, 128u));
+            tmem_cp_32x128b_x4(sfa_t + 4u * (uint32_t)j, sdesc + (uint64_t)(32u * (uint32_t)j));
 #pragma unroll
             for (int rb = 0; rb < BN / 128; ++rb)
               tmem_cp_32x128b_x4(sfb_t + (uint32_t)(BN / 32) * (uint32_t)j + 4u * (uint32_t)rb,
-                                 smem_desc_noswz(ssf + 2048u * (uint32_t)(1 + rb) +
-                                                     512u * (uint32_t)j,
-                                                 512u, 128u));
+                                 sdesc + (uint64_t)(128u * (uint32_t)(1 + rb) + 32u * (uint32_t)j));
           }
           umma_commit(sf_full_bar(stage));
-        }
-        __syncwarp();
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
       }
-    }
-    if (abort_s && lane == 0) {
-      // drain: every copy issued so far lands before TMEM is freed
-      umma_commit(sf_drain_bar);
-      mbar_wait_drain(sf_drain_bar, 0);
+      if (abort_s) {
+        // drain: every copy issued so far lands before TMEM is freed
+        umma_commit(sf_drain_bar);
+        mbar_wait_drain(sf_drain_bar, 0);
+      }
     }
     __syncwarp();
   } else if (warp < kThreads / 32) {

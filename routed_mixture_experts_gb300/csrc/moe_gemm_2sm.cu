@@ -127,22 +127,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   };
 
   if (warp == 0) {
-    // ---------------- TMA producer (both CTAs) ----------------
-    int stage = 0;
-    uint32_t phase = 0;
-    int issued_parity[STAGES];
+    // ---------------- TMA producer (both CTAs; lane 0 alone) ----------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued_parity[STAGES];
 #pragma unroll
-    for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
-    bool ok = true;
-    for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
-      TileInfo ti;
-      decode(tile, ti);
-      for (int kb = 0; kb < ti.kb; ++kb) {
-        int w = 1;
-        if (lane == 0) w = mbar_wait_cluster(empty_bar(stage), phase ^ 1u, &abort_s, args.err, 1, wlim);
-        ok = __shfl_sync(0xffffffffu, w, 0) != 0;
-        if (!ok) break;
-        if (lane == 0) {
+      for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
+      bool ok = true;
+      for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
+        TileInfo ti;
+        decode(tile, ti);
+        for (int kb = 0; kb < ti.kb; ++kb) {
+          ok = mbar_wait_cluster(empty_bar(stage), phase ^ 1u, &abort_s, args.err, 1, wlim);
+          if (!ok) break;
           const uint32_t fb = mapa_shared(full_bar(stage), 0);    // the leader's barrier
           const uint32_t sa = stage0 + stage * kPairStageBytes;
           const uint32_t sb = sa + 16384;
@@ -164,15 +162,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                              ti.e * args.b_expert_rows + ti.n0 + 128 * (int)rank, fb);
           }
           issued_parity[stage] = (int)phase;
-        }
-        __syncwarp();
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
       }
-    }
-    if (lane == 0) {
       if (!abort_s) {
         // every stage this CTA filled has been released by the leader's MMAs
         for (int s = 0; s < STAGES; ++s) {
@@ -198,8 +193,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ---------------- MMA issuer (leader CTA) ----------------
-    if (leader) {
+    // ---------------- MMA issuer (leader CTA, lane 0 alone) ----------------
+    // shared-memory descriptors: a fixed base plus the stage and K-step offsets
+    // in 16-byte units (K-major K step 32 B; MN-major B: 16 K rows = 2048 B)
+    if (leader && lane == 0) {
+      const uint64_t a_desc0 = smem_desc_sw128(stage0, 16, 1024);
+      const uint64_t b_desc0 = B_MN ? smem_desc_sw128(stage0 + 16384, 8192, 1024)
+                                    : smem_desc_sw128(stage0 + 16384, 16, 1024);
+      constexpr uint32_t B_KSTEP = (B_MN ? 2048u : 32u) >> 4;
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -208,51 +209,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
         TileInfo ti;
         decode(tile, ti);
-        int w = 1;
-        if (lane == 0)
-          w = mbar_wait_cluster(tempty_bar(acc), acc_phase ^ 1u, &abort_s, args.err, 3, wlim);
-        if (args.stall_mma && lane == 0 && w)
-          w = mbar_wait(drain_bar, 0, &abort_s, args.err, 9, wlim);   // failure-path test
-        ok = __shfl_sync(0xffffffffu, w, 0) != 0;
+        ok = mbar_wait_cluster(tempty_bar(acc), acc_phase ^ 1u, &abort_s, args.err, 3, wlim);
+        if (args.stall_mma && ok)
+          ok = mbar_wait(drain_bar, 0, &abort_s, args.err, 9, wlim);   // failure-path test
         if (!ok) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         for (int kb = 0; kb < ti.kb; ++kb) {
-          w = 1;
-          if (lane == 0) w = mbar_wait_cluster(full_bar(stage), phase, &abort_s, args.err, 4, wlim);
-          ok = __shfl_sync(0xffffffffu, w, 0) != 0;
+          ok = mbar_wait_cluster(full_bar(stage), phase, &abort_s, args.err, 4, wlim);
           if (!ok) break;
           tc_fence_after();
-          if (lane == 0) {
-            const uint32_t sa = stage0 + stage * kPairStageBytes;
-            const uint32_t sb = sa + 16384;
+          const uint64_t soff = (uint64_t)((uint32_t)(stage * kPairStageBytes) >> 4);
 #pragma unroll
-            for (int k16 = 0; k16 < kBK / 16; ++k16) {
-              const uint64_t adesc = smem_desc_sw128(sa + k16 * 32, 16, 1024);
-              const uint64_t bdesc = B_MN ? smem_desc_sw128(sb + k16 * 2048, 8192, 1024)
-                                          : smem_desc_sw128(sb + k16 * 32, 16, 1024);
-              umma_f16_pair(d_tmem, adesc, bdesc, IDESC, (kb | k16) != 0 ? 1u : 0u);
-            }
-            umma_commit_pair_mc(empty_bar(stage), 0x3);
-          }
-          __syncwarp();
+          for (int k16 = 0; k16 < kBK / 16; ++k16)
+            umma_f16_pair(d_tmem, a_desc0 + soff + (uint64_t)(k16 * 2),
+                          b_desc0 + soff + (uint64_t)(k16 * B_KSTEP), IDESC,
+                          (kb | k16) != 0 ? 1u : 0u);
+          umma_commit_pair_mc(empty_bar(stage), 0x3);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        if (lane == 0) umma_commit_pair_mc(tfull_bar(acc), 0x3);
-        __syncwarp();
+        umma_commit_pair_mc(tfull_bar(acc), 0x3);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
-      if (abort_s && lane == 0) {
+      if (abort_s) {
         umma_commit_pair_mc(drain_bar, 0x1);   // every MMA issued so far has completed
         mbar_wait_drain(drain_bar, 0);
       }
-      __syncwarp();
     }
+    __syncwarp();
   } else {
     // ---------------- epilogue (warps 2..9, both CTAs) ----------------
     const int quarter = warp & 3;
