@@ -461,6 +461,21 @@ int moe_plan_set_debug(moe_plan* plan, long long wait_limit_ns, int stall_w13);
  */
 int moe_plan_set_backward_split(moe_plan* plan, int wgrad_sms);
 
+/*
+ * Weight-gradient tile order.  Each SM walks its weight-gradient tiles
+ * longest expert first; a tile of a heavy expert is bound by its K loop over
+ * the expert's rows and leaves DRAM idle, a tile of a light expert by the
+ * read-modify-write of its fp32 gradient.  With min_rows > 0, the tiles of
+ * experts with more than min_rows routed rows (padded) run in pieces on one
+ * accumulator, each piece followed by a whole tile of a lighter expert on the
+ * other, so that the light tiles' gradient traffic overlaps the heavy tiles'
+ * K loops.  Every tile still sums its K range in the same order, so the
+ * gradients are bit-identical to those of the plain order (min_rows = 0).
+ * Default 2560.  min_rows < 0 or > 2^30: MOE_ERR_INVALID_ARG.  Applies to
+ * moe_backward and moe_backward_mxfp8.
+ */
+int moe_plan_set_wgrad_interleave(moe_plan* plan, long long min_rows);
+
 /* Number of SMs of the plan's device (the persistent kernels' grid size). */
 int moe_plan_num_sms(const moe_plan* plan);
 

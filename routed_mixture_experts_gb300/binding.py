@@ -75,6 +75,7 @@ def _declare(L):
     L.moe_forward_nvfp4.argtypes = [vp] * 12
     L.moe_amax_bf16.argtypes = [vp, ctypes.c_longlong, vp, vp]
     L.moe_plan_set_backward_split.argtypes = [vp, i32]
+    L.moe_plan_set_wgrad_interleave.argtypes = [vp, ctypes.c_longlong]
     L.moe_plan_num_sms.argtypes = [vp]
     L.moe_plan_num_sms.restype = i32
     L.moe_plan_launch_count.argtypes = [vp]
@@ -86,7 +87,8 @@ def _declare(L):
                  "moe_prepare_weights_mxfp8", "moe_plan_set_debug", "moe_plan_set_cta_pairs",
                  "moe_prepare_weights_mxfp8_backward", "moe_backward_mxfp8",
                  "moe_plan_set_activation_scales", "moe_prepare_weights_nvfp4",
-                 "moe_forward_nvfp4", "moe_amax_bf16", "moe_plan_set_backward_split"):
+                 "moe_forward_nvfp4", "moe_amax_bf16", "moe_plan_set_backward_split",
+                 "moe_plan_set_wgrad_interleave"):
         getattr(L, name).restype = i32
     return L
 
@@ -237,6 +239,11 @@ class MoePlan:
     def set_backward_split(self, wgrad_sms):
         """Weight-gradient GEMMs on wgrad_sms SMs beside DGRAD-W13 (0: off); see moe.h."""
         _check(lib().moe_plan_set_backward_split(self.ptr, int(wgrad_sms)), "backward_split")
+
+    def set_wgrad_interleave(self, min_rows):
+        """Weight-gradient tiles of experts with more than min_rows rows run
+        interleaved with the lighter ones (0: plain order); see moe.h."""
+        _check(lib().moe_plan_set_wgrad_interleave(self.ptr, int(min_rows)), "wgrad_interleave")
 
     def num_sms(self):
         return lib().moe_plan_num_sms(self.ptr)

@@ -186,8 +186,11 @@ __global__ void __launch_bounds__(gemm_threads<NV>(), 1)
 #pragma unroll
       for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
       bool ok = true;
-      for (int r = 0, tile = cta_tile(args, 0); tile < num_tiles && ok; tile = cta_tile(args, ++r)) {
-        const TileInfo ti = decode_tile<BN>(args, tile);
+      SegIter<BN, S::NACC> seq;
+      seq.init(args, num_tiles);
+      Seg sg;
+      while (ok && seq.next(args, sg)) {
+        const TileInfo& ti = sg.ti;
         // k_rotate (row GEMMs): the tiles that share an A tile (same m tile) or a
         // B tile (same expert and n tile) run at the same time; each starts its K
         // loop at its own offset (wrapping around), so each K chunk is read from
@@ -196,7 +199,7 @@ __global__ void __launch_bounds__(gemm_threads<NV>(), 1)
         const int kb0 = args.k_rotate ? (int)(((unsigned)(ti.m0 >> 7) * 7u + (unsigned)ti.nt * 5u) %
                                               (unsigned)ti.kb)
                                       : 0;
-        for (int kb = 0; kb < ti.kb; ++kb) {
+        for (int kb = sg.k0; kb < sg.k1; ++kb) {
           const int kc = kb + kb0 < ti.kb ? kb + kb0 : kb + kb0 - ti.kb;   // K chunk loaded
           ok = mbar_wait(empty_bar(stage), phase ^ 1u, &abort_s, args.err, 1, wlim);
           if (!ok) break;
@@ -310,18 +313,24 @@ __global__ void __launch_bounds__(gemm_threads<NV>(), 1)
       const uint64_t sf_desc0 = smem_desc_noswz(stage0 + S::A_BYTES + S::B_BYTES, 512u, 128u);
       int stage = 0;
       uint32_t phase = 0;
-      int acc = 0;
-      uint32_t acc_phase = 0;
+      uint32_t acc_phase = 0u;   // bit a: uses of accumulator a so far, mod 2
       bool ok = true;
-      for (int r = 0, tile = cta_tile(args, 0); tile < num_tiles && ok; tile = cta_tile(args, ++r)) {
-        const TileInfo ti = decode_tile<BN>(args, tile);
-        ok = mbar_wait(tempty_bar(acc), acc_phase ^ 1u, &abort_s, args.err, 3, wlim);
-        // failure-path test: wait on the drain barrier, which nothing has arrived at
-        if (args.stall_mma && ok) ok = mbar_wait(drain_bar, 0, &abort_s, args.err, 9, wlim);
-        if (!ok) break;
-        tc_fence_after();
+      SegIter<BN, S::NACC> seq;
+      seq.init(args, num_tiles);
+      Seg sg;
+      while (ok && seq.next(args, sg)) {
+        const int acc = sg.acc;
+        if (sg.k0 == 0) {
+          // a tile starts: its accumulator's previous tile has been read out
+          ok = mbar_wait(tempty_bar(acc), ((acc_phase >> acc) & 1u) ^ 1u, &abort_s, args.err, 3,
+                         wlim);
+          // failure-path test: wait on the drain barrier, which nothing has arrived at
+          if (args.stall_mma && ok) ok = mbar_wait(drain_bar, 0, &abort_s, args.err, 9, wlim);
+          if (!ok) break;
+          tc_fence_after();
+        }
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-        for (int kb = 0; kb < ti.kb; ++kb) {
+        for (int kb = sg.k0; kb < sg.k1; ++kb) {
           ok = mbar_wait(full_bar(stage), phase, &abort_s, args.err, 4, wlim);
           // NVFP4: also wait until the scale warp's copies of this stage are in TMEM
           if (NV && ok) ok = mbar_wait(sf_full_bar(stage), phase, &abort_s, args.err, 10, wlim);
@@ -369,9 +378,10 @@ __global__ void __launch_bounds__(gemm_threads<NV>(), 1)
           }
         }
         if (!ok) break;
-        umma_commit(tfull_bar(acc));
-        if (S::NACC == 2) acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
+        if (sg.last) {
+          umma_commit(tfull_bar(acc));
+          acc_phase ^= 1u << acc;
+        }
       }
       if (abort_s) {
         // drain: wait for every MMA issued so far before TMEM is freed
@@ -391,9 +401,11 @@ __global__ void __launch_bounds__(gemm_threads<NV>(), 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int r = 0, tile = cta_tile(args, 0); tile < num_tiles && ok; tile = cta_tile(args, ++r)) {
-        const TileInfo ti = decode_tile<BN>(args, tile);
-        for (int kb = 0; kb < ti.kb; ++kb) {
+      SegIter<BN, S::NACC> seq;
+      seq.init(args, num_tiles);
+      Seg sg;
+      while (ok && seq.next(args, sg)) {
+        for (int kb = sg.k0; kb < sg.k1; ++kb) {
           ok = mbar_wait(full_bar(stage), phase, &abort_s, args.err, 11, wlim);
           if (!ok) break;
           tc_fence_after();
@@ -429,15 +441,23 @@ __global__ void __launch_bounds__(gemm_threads<NV>(), 1)
     const int row = quarter * 32 + lane;
     const int et = threadIdx.x - 64;          // 0..255 over the epilogue warps
     const int half = (warp - 2) >> 2;         // warps 2..5: columns' first half, 6..9: second
-    int acc = 0;
-    uint32_t acc_phase = 0;
+    uint32_t acc_phase = 0u;                  // bit a: uses of accumulator a so far, mod 2
     int sub = 0;                              // output staging-buffer sequence number
-    WgradPipe wp{stage0 + STAGES * S::STAGE_BYTES, wg_bar0, num_tiles, 0, 0};
-    if (EPI == EPI_WGRAD && et == 0) wgrad_issue<BN, WB>(args, &tmC, wp, WB - 1);
-    for (int r = 0, tile = cta_tile(args, 0); tile < num_tiles; tile = cta_tile(args, ++r)) {
-      const TileInfo ti = decode_tile<BN>(args, tile);
+    WgradPipe<BN, S::NACC> wp;
+    if (EPI == EPI_WGRAD) {
+      wp.init(args, num_tiles, stage0 + STAGES * S::STAGE_BYTES, wg_bar0, et == 0);
+      if (et == 0) wgrad_issue<BN, S::NACC, WB>(args, &tmC, wp, WB - 1);
+    }
+    // tiles in the order their last segments reach the MMA issuer
+    SegIter<BN, S::NACC> seq;
+    seq.init(args, num_tiles);
+    Seg sg;
+    while (seq.next(args, sg)) {
+      if (!sg.last) continue;
+      const TileInfo& ti = sg.ti;
+      const int acc = sg.acc;
       int w = 1;
-      if (lane == 0) w = mbar_wait(tfull_bar(acc), acc_phase, &abort_s, args.err, 5, wlim);
+      if (lane == 0) w = mbar_wait(tfull_bar(acc), (acc_phase >> acc) & 1u, &abort_s, args.err, 5, wlim);
       // all eight epilogue warps leave together, so their named barriers stay matched
       const int ok_warp = __shfl_sync(0xffffffffu, w, 0);
       if (epi_bar_and(ok_warp) == 0) break;
@@ -450,7 +470,9 @@ __global__ void __launch_bounds__(gemm_threads<NV>(), 1)
         acc_phase ^= 1u;
         continue;
       } else if constexpr (EPI == EPI_WGRAD) {
-        if (!epilogue_wgrad<BN, WB>(args, &tmC, ti, row, tbase, et, half, wp, &abort_s, wlim)) break;
+        if (!epilogue_wgrad<BN, S::NACC, WB>(args, &tmC, ti, row, tbase, et, half, wp, &abort_s,
+                                             wlim))
+          break;
       } else if constexpr (MX && EPI == EPI_DGRAD2) {
         static_assert(S::OUT_BYTES >= 8 * kD2WarpBytes, "per-warp staging");
         epilogue_dgrad2_mx<BN>(args, ti, row, tbase, half, smem + STAGES * S::STAGE_BYTES, et);
@@ -460,8 +482,7 @@ __global__ void __launch_bounds__(gemm_threads<NV>(), 1)
       }
       tc_fence_before();
       mbar_arrive(tempty_bar(acc));
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
+      acc_phase ^= 1u << acc;
     }
     if (EPI == EPI_WGRAD && et == 0) {
       // after an abort: let every gradient chunk load still in flight land

@@ -67,6 +67,141 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int tile) {
   return ti;
 }
 
+// The order in which a CTA's MMA issuer consumes K stages, as segments: a run
+// of K blocks [k0, k1) of one tile on one accumulator; `last` ends the tile, and
+// the tiles' epilogues run in the order their last segments come.  Every role
+// of the CTA (producer, MMA issuer, epilogue, gradient-chunk loads) walks the
+// same sequence.
+//
+// Plain order: the CTA's tiles (cta_tile) whole, accumulators alternating.
+//
+// Two streams (weight gradients with `wgrad_long_kb` set): a tile of a heavy
+// expert runs a long K loop and finishes with one read-modify-write, while the
+// many tiles of light experts are bound by their read-modify-writes.  One after
+// the other on an SM, the first keep the tensor pipe busy with DRAM idle and the
+// second the reverse.  Here the CTA's long tiles (K blocks > wgrad_long_kb: a
+// prefix of its sequence, which is longest first) run on accumulator 0 in
+// pieces of G blocks, with a whole short tile on accumulator 1 after each piece
+// (and right after a long tile ends), G spreading the long blocks evenly over
+// the short tiles: the short tiles' read-modify-writes overlap the long main
+// loops.  When one stream runs out, the other continues with alternating
+// accumulators (an open long tile first finishes on accumulator 0).  A tile
+// starts on an accumulator only after the previous tile on it has ended in
+// this order, and epilogues run in this order, so no wait can cycle.  The
+// split changes only which K blocks run back to back, not any sum.
+struct Seg {
+  TileInfo ti;
+  int tile;
+  int k0, k1;   // K blocks [k0, k1) of the tile
+  int acc;      // accumulator
+  bool last;    // the tile's last segment
+};
+
+template <int BN, int NACC>
+struct SegIter {
+  int n;          // this CTA's tiles
+  int nL;         // long tiles (rounds [0, nL)); 0: plain order
+  int G;          // long-tile K blocks between two short tiles
+  int iL, pL;     // next long tile, K blocks done of the open one
+  int iS;         // next short tile (round)
+  int since;      // long-tile K blocks since the last short tile
+  int last_acc;   // accumulator of the most recent tile
+  TileInfo curL;  // the open long tile
+  int curL_tile;
+
+  __device__ __forceinline__ void init(const GemmArgs& a, int num_tiles) {
+    n = 0;
+    while (cta_tile(a, n) < num_tiles) ++n;
+    nL = 0;
+    long long sumL = 0;
+    if (NACC == 2 && a.wgrad && a.wgrad_long_kb > 0) {
+      while (nL < n) {
+        const int kb = decode_tile<BN>(a, cta_tile(a, nL)).kb;
+        if (kb <= a.wgrad_long_kb) break;
+        sumL += kb;
+        ++nL;
+      }
+      if (nL == n) nL = 0;   // no short tiles: plain order
+    }
+    G = nL ? (int)((sumL + (n - nL) - 1) / (n - nL)) : 0;
+    iL = 0;
+    pL = 0;
+    iS = nL;
+    since = 0;
+    last_acc = 1;
+    if (nL) {
+      curL_tile = cta_tile(a, 0);
+      curL = decode_tile<BN>(a, curL_tile);
+    }
+  }
+
+  __device__ __forceinline__ void open_next_long(const GemmArgs& a) {
+    ++iL;
+    pL = 0;
+    if (iL < nL) {
+      curL_tile = cta_tile(a, iL);
+      curL = decode_tile<BN>(a, curL_tile);
+    }
+  }
+
+  __device__ __forceinline__ void whole(const GemmArgs& a, int r, int acc, Seg& s) {
+    s.tile = cta_tile(a, r);
+    s.ti = decode_tile<BN>(a, s.tile);
+    s.k0 = 0;
+    s.k1 = s.ti.kb;
+    s.acc = acc;
+    s.last = true;
+    last_acc = acc;
+  }
+
+  __device__ __forceinline__ bool next(const GemmArgs& a, Seg& s) {
+    if (iL < nL && iS < n) {
+      if (since >= G) {
+        whole(a, iS++, 1, s);
+        since = 0;
+        return true;
+      }
+      const int m = min(G - since, curL.kb - pL);
+      s.ti = curL;
+      s.tile = curL_tile;
+      s.k0 = pL;
+      s.k1 = pL + m;
+      s.acc = 0;
+      s.last = s.k1 == curL.kb;
+      last_acc = 0;
+      pL += m;
+      since += m;
+      if (s.last) {
+        open_next_long(a);
+        since = G;   // a short tile next, while this one's epilogue runs
+      }
+      return true;
+    }
+    if (iL < nL) {
+      if (pL > 0) {
+        // the open long tile finishes on its accumulator
+        s.ti = curL;
+        s.tile = curL_tile;
+        s.k0 = pL;
+        s.k1 = curL.kb;
+        s.acc = 0;
+        s.last = true;
+        last_acc = 0;
+        open_next_long(a);
+        return true;
+      }
+      whole(a, iL, NACC == 2 ? last_acc ^ 1 : 0, s);
+      open_next_long(a);
+      return true;
+    }
+    if (iS < n) {
+      whole(a, iS++, NACC == 2 ? last_acc ^ 1 : 0, s);
+      return true;
+    }
+    return false;
+  }
+};
+
 // Bounded wait that ignores the abort flag (used only while draining).
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();
@@ -667,23 +802,47 @@ __device__ __forceinline__ void epilogue_dgrad2_mx(const GemmArgs& a, const Tile
 template <bool MX>
 __host__ __device__ constexpr int wgrad_bufs() { return MX ? 5 : 4; }
 
+template <int BN, int NACC>
 struct WgradPipe {
   uint32_t buf0;     // first chunk buffer
   uint32_t bar0;     // first of the NB chunk-load barriers
-  int num_tiles;
   int next;          // chunks consumed (all epilogue threads)
   int issued;        // chunks whose load has been issued (thread et == 0)
+  // thread et == 0: the tiles in epilogue order, for the loads ahead
+  SegIter<BN, NACC> order;
+  int have;          // tiles taken from `order`
+  TileInfo cur;      // the last of them
+  // every epilogue thread; `issuer`: the thread that issues the loads
+  __device__ __forceinline__ void init(const GemmArgs& a, int num_tiles, uint32_t b0,
+                                       uint32_t bar, bool issuer) {
+    buf0 = b0;
+    bar0 = bar;
+    next = 0;
+    issued = 0;
+    have = 0;
+    if (issuer) order.init(a, num_tiles);
+  }
 };
 
-template <int BN, int NB>
+template <int BN, int NACC, int NB>
 __device__ __forceinline__ void wgrad_issue(const GemmArgs& a, const CUtensorMap* tmC,
-                                            WgradPipe& p, int upto) {
+                                            WgradPipe<BN, NACC>& p, int upto) {
   constexpr int CH = BN / 32;
   while (p.issued < upto) {
     const int n = p.issued;
-    const int tile = cta_tile(a, n / CH);
-    if (tile >= p.num_tiles) return;
-    const TileInfo t = decode_tile<BN>(a, tile);
+    while (p.have <= n / CH) {   // the epilogue's next tile
+      Seg sg;
+      bool got = false;
+      while (p.order.next(a, sg))
+        if (sg.last) {
+          got = true;
+          break;
+        }
+      if (!got) return;
+      p.cur = sg.ti;
+      ++p.have;
+    }
+    const TileInfo& t = p.cur;
     const int b = n % NB;
     const uint32_t bar = p.bar0 + 8u * (uint32_t)b;
     mbar_arrive_expect_tx(bar, 16384u);
@@ -694,11 +853,11 @@ __device__ __forceinline__ void wgrad_issue(const GemmArgs& a, const CUtensorMap
 }
 
 // Returns false when a wait gave up (every epilogue thread returns the same).
-template <int BN, int NB>
+template <int BN, int NACC, int NB>
 __device__ __forceinline__ bool epilogue_wgrad(const GemmArgs& a, const CUtensorMap* tmC,
                                                const TileInfo& ti, int row, uint32_t tbase, int et,
-                                               int half, WgradPipe& p, volatile int* abort_flag,
-                                               uint64_t wlim) {
+                                               int half, WgradPipe<BN, NACC>& p,
+                                               volatile int* abort_flag, uint64_t wlim) {
   const int ybase = ti.e * a.m_tiles * kBM + ti.m0;
   const uint32_t sw = (uint32_t)(row & 7);
   uint32_t r0[16];
@@ -734,7 +893,7 @@ __device__ __forceinline__ bool epilogue_wgrad(const GemmArgs& a, const CUtensor
       // chunk n-1's buffer is free once its store has read it: load chunk
       // n + NB - 1 there
       bulk_wait_read<1>();
-      wgrad_issue<BN, NB>(a, tmC, p, n + NB);
+      wgrad_issue<BN, NACC, NB>(a, tmC, p, n + NB);
     }
   }
   return true;

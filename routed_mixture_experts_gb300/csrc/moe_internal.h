@@ -97,6 +97,8 @@ struct GemmArgs {
                              // (m and n tile), so tiles sharing an operand tile read
                              // different K chunks at a time (changes the summation order)
   int wgrad_kstep;           // wgrad mode: rows per K stage (0: 64; MXFP8: 128)
+  int wgrad_long_kb;         // wgrad mode: tiles of more K stages are interleaved with
+                             // the shorter ones (gemm::SegIter); 0: plain order
   // MXFP8 (block-scaled) operands: tiled E8M0 scales (see mx_sf_offset)
   const uint8_t* sfa;        // scales of A, row blocks of 128 padded rows
   const uint8_t* sfb;        // scales of B, row block = e * b_blocks_per_expert + n tile

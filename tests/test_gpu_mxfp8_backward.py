@@ -207,3 +207,27 @@ def test_mxfp8_backward_full_size_sampled(moe, orc):
                 what="dW13[%d] mxfp8 full" % e, max_bad_frac=1.0)
         compare((g["dw2"][e] - dev["dw2"][e]).cpu().numpy(), r2, rel_fro=REL_FRO_MXFP8,
                 what="dW2[%d] mxfp8 full" % e, max_bad_frac=1.0)
+
+
+@pytest.mark.parametrize("min_rows", [0, 128])
+def test_mxfp8_wgrad_interleave_is_bit_identical(moe, min_rows):
+    """Block-scaled weight gradients with the heavy experts' tiles interleaved
+    with lighter ones: the same bits as the default schedule."""
+    inp = mi.make_inputs(None, seed=63, need=NEED, T=4096, d=256, I=256, E=32, k=8,
+                         routing="zipf", zipf_s=1.2, zipf_support=24)
+    counts = np.bincount(inp["ids"].reshape(-1), minlength=32)
+    assert counts.max() > 2560   # the default threshold splits the heaviest experts
+    dev = to_dev(inp)
+    ref = train_step(moe, inp, dev)
+    plan = ref["plan"]
+    plan.set_wgrad_interleave(min_rows)
+    w13q, w13s, w2q, w2s = ref["prep"]
+    plan.forward(dev["x"], dev["ids"], dev["scores"], w13q, w2q, w13_sf=w13s, w2_sf=w2s,
+                 save=True)
+    dw13, dw2 = dev["dw13"].clone(), dev["dw2"].clone()
+    dx, ds = plan.backward_mxfp8(dev["dy"], *ref["prep_t"], dw13, dw2)
+    torch.cuda.synchronize()
+    assert plan.check()[0] == 0
+    assert torch.equal(dx.view(torch.int16), ref["dx"].view(torch.int16))
+    assert torch.equal(ds, ref["ds"])
+    assert torch.equal(dw13, ref["dw13"]) and torch.equal(dw2, ref["dw2"])

@@ -106,6 +106,38 @@ def test_backward_split_is_bit_identical(moe, sizes):
         assert torch.equal(dw13, ref["dw13"]) and torch.equal(dw2, ref["dw2"])
 
 
+@pytest.mark.parametrize("min_rows", [0, 128, 1024])
+def test_wgrad_interleave_is_bit_identical(moe, min_rows):
+    """Weight-gradient tiles of the heavy experts run in pieces interleaved with
+    lighter tiles on the other accumulator (the default threshold, 2560 rows,
+    splits this case's heaviest experts; 128 rows splits nearly every tile):
+    every output has the same bits as with the plain order (0) and as with the
+    default, since each tile still sums its K range in order."""
+    sizes = dict(T=4096, d=512, I=256, E=32, k=8, routing="zipf", zipf_s=1.2, zipf_support=24)
+    inp = make(None, seed=62, train=True, **sizes)
+    counts = np.bincount(inp["ids"].reshape(-1), minlength=sizes["E"])
+    assert counts.max() > 2560
+    ref = run_gpu(moe, inp, train=True)
+    assert ref["rc"] == 0
+    dev = ref["dev"]
+    plan = ref["plan"]
+    plan.set_wgrad_interleave(min_rows)
+    dw13, dw2 = dev["dw13"].clone(), dev["dw2"].clone()
+    plan.forward(dev["x"], dev["ids"], dev["scores"], dev["w13"], dev["w2"], save=True)
+    dx, ds = plan.backward(dev["dy"], dev["w13"], dev["w2"], dw13, dw2)
+    torch.cuda.synchronize()
+    assert plan.check()[0] == 0
+    assert torch.equal(dx.view(torch.int16), ref["dx"].view(torch.int16))
+    assert torch.equal(ds, ref["dscores"])
+    assert torch.equal(dw13, ref["dw13"]) and torch.equal(dw2, ref["dw2"])
+
+
+def test_wgrad_interleave_rejects_bad_threshold(moe):
+    plan = moe.MoePlan(64, 128, 64, 4, 2, flags=moe.MOE_WS_TRAINING)
+    with pytest.raises(moe.MoeError):
+        plan.set_wgrad_interleave(-1)
+
+
 def test_zero_score_padding_rows_are_zero(moe):
     inp = make(None, seed=5, train=True, T=160, d=128, I=64, E=6, k=2, pad=40)
     g = run_gpu(moe, inp, train=True)
