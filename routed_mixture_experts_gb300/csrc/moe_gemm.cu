@@ -54,7 +54,7 @@ struct GemmShape {
   // (the NVFP4 W13 epilogue writes h from registers and never saves a: no staging)
   static constexpr int OUT_BYTES =
       (NV && EPI == EPI_SWIGLU ? 0 : EPI == EPI_WGRAD ? wgrad_bufs<MX>()
-                        : (MX && BN == 256 ? kMxWideBufs
+                        : (MX && BN == 256 ? wide_bufs<NV>()
                                            : (EPI == EPI_SCORE || EPI == EPI_STORE
                                                   ? kEpiStageBufs
                                                   : tri_bufs<EPI>()))) * 16384;

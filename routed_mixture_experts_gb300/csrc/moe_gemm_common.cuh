@@ -399,21 +399,24 @@ __device__ __forceinline__ void epi_stage_three(const CUtensorMap* t0, const CUt
 // 128-byte-swizzled layout of a 64 x 128 box and stored with TMA, half 0's at
 // column x0 and half 1's at x1.  With two 16 KB buffers both halves write at
 // once (buffer `half`); with one, half 0's sub-tile goes first.  A buffer is
-// rewritten only once the previous store has read it.  One buffer: the 16 KB it
-// frees give the operand ring a fourth stage, which is worth more (W13 0.272 ->
-// 0.233 ms, W2 0.161 -> 0.137 ms on the E = 128 training shapes).
-constexpr int kMxWideBufs = 1;
+// rewritten only once the previous store has read it.  MXFP8: one buffer; the
+// 16 KB it frees give the operand ring a fourth stage, which is worth more (W13
+// 0.272 -> 0.233 ms, W2 0.161 -> 0.137 ms on the E = 128 training shapes).
+// NVFP4 (54 KB stages): three stages either way, so two buffers.
+template <bool NV>
+__host__ __device__ constexpr int wide_bufs() { return NV ? 2 : 1; }
 
+template <int NBUF>
 __device__ __forceinline__ void epi_stage_wide(const CUtensorMap* tm, uint32_t out0, int et,
                                                int row, int half, const uint32_t (&pk)[32],
                                                int x0, int x1, int y) {
   const uint32_t sw = (uint32_t)(row & 7);
 #pragma unroll
-  for (int r = 0; r < 3 - kMxWideBufs; ++r) {
+  for (int r = 0; r < 3 - NBUF; ++r) {
     if (et == 0) bulk_wait_read<0>();
     named_bar_sync(1, kEpiThreads);
-    if (kMxWideBufs == 2 || half == r) {
-      const uint32_t rbase = out0 + (uint32_t)(kMxWideBufs == 2 ? half : 0) * 16384u +
+    if (NBUF == 2 || half == r) {
+      const uint32_t rbase = out0 + (uint32_t)(NBUF == 2 ? half : 0) * 16384u +
                              (uint32_t)row * 128u;
 #pragma unroll
       for (int q = 0; q < 8; ++q)
@@ -423,7 +426,7 @@ __device__ __forceinline__ void epi_stage_wide(const CUtensorMap* tm, uint32_t o
     fence_proxy_async_smem();
     named_bar_sync(1, kEpiThreads);
     if (et == 0) {
-      if (kMxWideBufs == 2) {
+      if (NBUF == 2) {
         tma_store_2d(tm, out0, x0, y);
         tma_store_2d(tm, out0 + 16384u, x1, y);
       } else {
@@ -530,8 +533,9 @@ __device__ __forceinline__ void epilogue_mx_wide(const GemmArgs& a, const TileIn
     }
     if (a.save) {
       const int xg = ti.nt * 128;        // buffer 0: half 0's columns, buffer 1: half 1's
-      epi_stage_wide(tmO1, out0, et, row, half, pg, xg, xg + 64, ti.m0);
-      epi_stage_wide(tmO1, out0, et, row, half, pu, a.I + xg, a.I + xg + 64, ti.m0);
+      epi_stage_wide<wide_bufs<NV>()>(tmO1, out0, et, row, half, pg, xg, xg + 64, ti.m0);
+      epi_stage_wide<wide_bufs<NV>()>(tmO1, out0, et, row, half, pu, a.I + xg, a.I + xg + 64,
+                                      ti.m0);
     }
   } else {
     static_assert(EPI == EPI_SCORE || EPI == EPI_STORE, "256-wide MXFP8 epilogues");
@@ -546,7 +550,7 @@ __device__ __forceinline__ void epilogue_mx_wide(const GemmArgs& a, const TileIn
                          s * __uint_as_float(v[(c + 1) >> 4][(c + 1) & 15]));
       }
       const int x = ti.n0 + 64 * j;      // buffer 0: half 0's sub-tile, buffer 1: half 1's
-      epi_stage_wide(tmO0, out0, et, row, half, pk, x, x + 128, ti.m0);
+      epi_stage_wide<wide_bufs<NV>()>(tmO0, out0, et, row, half, pk, x, x + 128, ti.m0);
     }
   }
 }
