@@ -19,7 +19,10 @@
 //   warp 10     NVFP4 only: copies each stage's scale factors into TMEM
 //               (tcgen05.cp), so the MMA issuer only issues MMAs
 // The accumulator is double buffered in TMEM (2 x BN fp32 columns) so the
-// epilogue of tile i overlaps the main loop of tile i+1.
+// epilogue of tile i overlaps the main loop of tile i+1.  Every role walks the
+// same sequence of K-stage segments (gemm::SegIter): whole tiles with the two
+// accumulators alternating, or, for weight gradients of heavy experts, long
+// tiles in pieces interleaved with short ones.
 //
 // Every mbarrier wait is bounded (moe::mbar_wait); a wait that gives up records
 // MOE_ERR_TIMEOUT, all roles leave their loops, outstanding copies and MMAs are
