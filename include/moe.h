@@ -504,8 +504,8 @@ long long moe_plan_launch_count(const moe_plan* plan);
  * scratch is too small), k <= E <= 256, rows_capacity >=
  * floor((T*k + E*(BM-1)) / BM) * BM (else MOE_ERR_INVALID_ARG).
  * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current: make that first call before
- * any stream capture.  The address is kept per device and CUDA context: the
+ * (cudaGetSymbolAddress) with that device current.  The address is kept per
+ * device and CUDA context: the
  * first call from another context on the device (a non-primary context, or the
  * primary context re-created after cudaDeviceReset) looks it up again and is a
  * first call in the same sense.  All calls on a device share the one array,

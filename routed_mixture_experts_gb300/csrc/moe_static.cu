@@ -15,11 +15,10 @@
 //   - every GPU that loads this library holds the array (about 280 KB) until the
 //     process exits;
 //   - its device address is looked up once per device and CUDA context, by the
-//     first call made with that device current (cudaGetSymbolAddress); make that
-//     first call before any stream capture.  A call from another context on the
-//     same device (a non-primary context, or the primary one re-created after
-//     cudaDeviceReset) looks the address up again, in that context, so it is
-//     also a first call;
+//     first call made with that device current (cudaGetSymbolAddress).  A call
+//     from another context on the same device (a non-primary context, or the
+//     primary one re-created after cudaDeviceReset) looks the address up again,
+//     in that context, so it is also a first call;
 //   - every call on a device shares the one array and it keeps the last call's
 //     contents: the error word is cleared at the start of each call, everything
 //     else is fully rewritten; calls whose kernels overlap on the GPU (for
