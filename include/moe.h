@@ -505,10 +505,9 @@ long long moe_plan_launch_count(const moe_plan* plan);
  * floor((T*k + E*(BM-1)) / BM) * BM (else MOE_ERR_INVALID_ARG).
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current.  The address is kept per
- * device and CUDA context: the
- * first call from another context on the device (a non-primary context, or the
- * primary context re-created after cudaDeviceReset) looks it up again and is a
- * first call in the same sense.  All calls on a device share the one array,
+ * device and CUDA context: the first call from another context on the device
+ * (a non-primary context, or the primary context re-created after
+ * cudaDeviceReset) looks it up again and is a first call in the same sense.  All calls on a device share the one array,
  * which keeps the last call's contents (the error word is cleared at the start
  * of each call): calls whose work overlaps on the GPU (for example on two
  * streams) race and must not be issued.
