@@ -106,13 +106,15 @@ def test_backward_split_is_bit_identical(moe, sizes):
         assert torch.equal(dw13, ref["dw13"]) and torch.equal(dw2, ref["dw2"])
 
 
-@pytest.mark.parametrize("min_rows", [0, 128, 1024])
-def test_wgrad_interleave_is_bit_identical(moe, min_rows):
+@pytest.mark.parametrize("min_rows,split", [(0, False), (128, False), (1024, False), (128, True)],
+                         ids=["plain", "interleave128", "interleave1024", "interleave128_split"])
+def test_wgrad_interleave_is_bit_identical(moe, min_rows, split):
     """Weight-gradient tiles of the heavy experts run in pieces interleaved with
     lighter tiles on the other accumulator (the default threshold, 2560 rows,
     splits this case's heaviest experts; 128 rows splits nearly every tile):
     every output has the same bits as with the plain order (0) and as with the
-    default, since each tile still sums its K range in order."""
+    default, since each tile still sums its K range in order; also with the
+    weight gradients on their own stream and half the SMs."""
     sizes = dict(T=4096, d=512, I=256, E=32, k=8, routing="zipf", zipf_s=1.2, zipf_support=24)
     inp = make(None, seed=62, train=True, **sizes)
     counts = np.bincount(inp["ids"].reshape(-1), minlength=sizes["E"])
@@ -122,6 +124,8 @@ def test_wgrad_interleave_is_bit_identical(moe, min_rows):
     dev = ref["dev"]
     plan = ref["plan"]
     plan.set_wgrad_interleave(min_rows)
+    if split:   # weight gradients on their own stream and half the SMs
+        plan.set_backward_split(plan.num_sms() // 2)
     dw13, dw2 = dev["dw13"].clone(), dev["dw2"].clone()
     plan.forward(dev["x"], dev["ids"], dev["scores"], dev["w13"], dev["w2"], save=True)
     dx, ds = plan.backward(dev["dy"], dev["w13"], dev["w2"], dw13, dw2)
